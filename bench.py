@@ -1,0 +1,322 @@
+"""Throughput of the single-GPU MoE layer, forward+backward, on GB300.
+
+One step = one forward+backward pass of the whole layer (routing, dispatch,
+grouped SwiGLU expert GEMMs, combine and every backward step) over one batch
+of seeded synthetic tokens, through libmoe's C ABI.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl ours|reference]
+
+Prints ONE JSON line on rank 0. Under torchrun (N > 1) every rank runs an
+independent replica of the layer (weak scaling; the path has no collective).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from mixture_experts_layer_prefix_gb300 import synth  # noqa: E402
+
+METRIC = "MoE layer tokens/s fwd+bwd at E=128 top-4; grouped-GEMM % of bf16/FP8 peak"
+DEFAULT_CONFIG = "e128_top4"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as fh:
+            p = json.load(fh)
+        return p, "measured"
+    return FALLBACK_PEAKS, "fallback"
+
+
+def workload_desc(s):
+    return (f"{s.name}: MoE layer fwd+bwd, T={s.T} tokens, d={s.d}, E={s.E}, top-k={s.k}, "
+            f"SwiGLU f={s.f}, {s.dtype}")
+
+
+def gemm_flops(s):
+    """Algorithmic FLOPs of the six grouped expert GEMMs of one fwd+bwd step
+    (routed rows only): forward 6*R*d*f, backward 12*R*d*f."""
+    return 18.0 * s.R * s.d * s.f
+
+
+def step_flops(s):
+    """Algorithmic FLOPs of one fwd+bwd step: expert GEMMs + router GEMM (fwd)
+    and its two backward products."""
+    return gemm_flops(s) + 3.0 * 2.0 * s.T * s.d * s.E
+
+
+# ----------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------- CPU oracle
+def oracle_sample(s, tokens, seed=0):
+    """The fp64 oracle on the first `tokens` tokens of the workload (full
+    weights), routed on its own fp64 logits. Returns (seconds, threads)."""
+    import oracle
+    inp = synth.Inputs(s, seed=seed)
+    x, dy = inp.x()[:tokens], inp.dy()[:tokens]
+    wr, wg, wu, wd = inp.w_r(), inp.w_gate(), inp.w_up(), inp.w_down()
+    bias = inp.bias()
+    nthreads = len(os.sched_getaffinity(0)) or 1
+    t0 = time.perf_counter()
+    oracle.layer(x, wr, wg, wu, wd, dy, s.k, bias=bias, nthreads=nthreads)
+    return time.perf_counter() - t0, nthreads
+
+
+def cpu_baseline(s, budget_s=15.0):
+    """Oracle tokens/s on a bounded sample sized for about `budget_s` seconds."""
+    probe = 8
+    t, _ = oracle_sample(s, probe)
+    n = int(max(probe, min(s.T, probe * budget_s / max(t, 1e-3))))
+    t, th = oracle_sample(s, n)
+    return {"value": n / t, "unit": "tokens/s", "cores": th, "kind": "oracle",
+            "sample": f"first {n} of {s.T} tokens of {s.name}, full weights, fp64 C oracle, "
+                      f"{th} threads, {t:.1f} s"}
+
+
+# --------------------------------------------------------------- our arm
+def run_ours(args, s, rank, world):
+    import torch
+
+    from mixture_experts_layer_prefix_gb300 import _native as N
+    from mixture_experts_layer_prefix_gb300 import build as B
+    from mixture_experts_layer_prefix_gb300 import layer as L
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if rank == 0 or not os.path.exists(B.LIB):
+        B.build()
+    if world > 1:
+        torch.distributed.barrier()
+    N.load()
+    dt = {"f32": N.MOE_F32, "bf16": N.MOE_BF16}[s.dtype]
+    inp = synth.Inputs(s, seed=0)
+    p = L.params_from_inputs(inp, dt)
+    b = L.Buffers(s.T, s.d, s.E, s.k, s.f, dt)
+    stream = torch.cuda.current_stream()
+
+    def step_timed(ev):
+        # forward and backward through the C ABI; events bracket the GEMM stages
+        T, d, E, k, f = s.T, s.d, s.E, s.k, s.f
+        N.moe_route(p.x, p.w_router, p.bias, dt, T, d, E, k, b.logits, 0, b.topk_idx, b.gates, b.counts,
+                    b.offsets, b.dest_row, b.src_row, b.workspace)
+        N.moe_permute(p.x, dt, T, d, k, b.dest_row, b.x_perm)
+        ev[0].record(stream)
+        N.moe_grouped_mlp_fwd(b.x_perm, p.w_gate, p.w_up, p.w_down, dt, b.offsets, b.R, E, d, f, b.h_save,
+                              b.a_save, b.y_perm, b.workspace)
+        ev[1].record(stream)
+        N.moe_combine_fwd(b.y_perm, b.gates, b.dest_row, dt, T, d, k, b.y)
+        N.moe_combine_bwd(p.dy, b.y_perm, b.gates, b.dest_row, dt, T, d, k, b.dy_perm, b.dgates)
+        N.moe_route_bwd(b.dgates, b.gates, b.topk_idx, b.offsets, b.src_row, b.x_perm, dt, T, d, E, k,
+                        b.dlogits, b.dw_router)
+        ev[2].record(stream)
+        N.moe_grouped_mlp_bwd(b.dy_perm, b.x_perm, b.h_save, b.a_save, p.w_gate, p.w_up, p.w_down, dt,
+                              b.offsets, b.R, E, d, f, b.dx_perm, b.dw_gate, b.dw_up, b.dw_down,
+                              b.workspace)
+        ev[3].record(stream)
+        N.moe_permute_bwd(b.dx_perm, dt, T, d, E, k, b.dest_row, b.topk_idx, b.dlogits, p.w_router, b.dx)
+
+    mk = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    for _ in range(args.warmup):
+        step_timed([mk() for _ in range(4)])
+    torch.cuda.synchronize()
+    err = N.moe_get_device_error()
+    if err:
+        raise RuntimeError(f"device error word {err} after warm-up")
+
+    # ---- timed region (device-resident inputs)
+    evs = [[mk() for _ in range(4)] for _ in range(args.steps)]
+    t_start, t_end = mk(), mk()
+    clocks = ClockSampler(local)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    n0 = N.moe_launch_count()
+    t_start.record(stream)
+    for i in range(args.steps):
+        step_timed(evs[i])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    launches = N.moe_launch_count() - n0
+    if world > 1:
+        torch.distributed.barrier()
+    clk = clocks.stop()
+    elapsed_ms = t_start.elapsed_time(t_end)
+    gemm_ms = sum(e[0].elapsed_time(e[1]) + e[2].elapsed_time(e[3]) for e in evs) / args.steps
+    if N.moe_get_device_error():
+        raise RuntimeError("device error word set in the timed region")
+
+    # ---- end to end through the C ABI with host buffers (pinned), copies timed
+    x_h = p.x.cpu().pin_memory()
+    dy_h = p.dy.cpu().pin_memory()
+    y_h = torch.empty_like(b.y, device="cpu").pin_memory()
+    dx_h = torch.empty_like(b.dx, device="cpu").pin_memory()
+    e2e_steps = max(1, min(args.steps, 10))
+    torch.cuda.synchronize()
+    e0, e1 = mk(), mk()
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        p.x.copy_(x_h, non_blocking=True)
+        p.dy.copy_(dy_h, non_blocking=True)
+        L.forward(p, b)
+        L.backward(p, b)
+        y_h.copy_(b.y, non_blocking=True)
+        dx_h.copy_(b.dx, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    h2d = x_h.numel() * x_h.element_size() + dy_h.numel() * dy_h.element_size()
+    d2h = y_h.numel() * y_h.element_size() + dx_h.numel() * dx_h.element_size()
+
+    if world > 1:
+        tt = torch.tensor([elapsed_ms, e2e_ms], device="cuda")
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        elapsed_ms, e2e_ms = float(tt[0]), float(tt[1])
+
+    ms_per_step = elapsed_ms / args.steps
+    tokens_per_s = world * s.T * args.steps / (elapsed_ms / 1e3)
+    pk, pk_kind = peaks()
+    peak = float(pk.get("bf16_tflops_sustained", pk.get("bf16_tflops")))
+    achieved = gemm_flops(s) / (gemm_ms / 1e3) / 1e12
+    out = {
+        "metric": METRIC,
+        "value": tokens_per_s,
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_per_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": s.dtype,
+        "data": "synthetic (seeded N(0,1) tokens, N(0,1/fan_in) weights, router N(0,0.02^2))",
+        "config": {"workload": workload_desc(s), "T": s.T, "d": s.d, "E": s.E, "k": s.k, "f": s.f,
+                   "parallelism": f"replicas x{world} (no collective)",
+                   "l2": "no flush: per-step working set (1.6 GB weights + activations) >> 129 MB L2"},
+        "tflops_per_s": step_flops(s) * world * args.steps / (elapsed_ms / 1e3) / 1e12,
+        "roofline": {"kernel": "grouped expert GEMMs (fwd+bwd, 6 GEMMs per step)", "bound": "tensor",
+                     "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                     "peak_kind": f"{pk_kind} bf16 sustained", "traffic": None,
+                     "gemm_ms_per_step": gemm_ms},
+        "e2e": {"value": world * s.T / (e2e_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": launches,
+        "clocks": clk,
+    }
+    return out
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", default=DEFAULT_CONFIG, choices=sorted(synth.CONFIGS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    s = synth.CONFIGS[args.config]
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+
+    if args.impl == "reference":
+        # The reference arm is the fp64 CPU oracle on this machine's host cores.
+        if rank != 0:
+            return
+        per_step = max(2.0, min(15.0, 120.0 / (args.steps + args.warmup)))
+        probe = 8
+        t, th = oracle_sample(s, probe)
+        n = int(max(probe, min(s.T, probe * per_step / max(t, 1e-3))))
+        for _ in range(args.warmup):
+            oracle_sample(s, n)
+        times = [oracle_sample(s, n)[0] for _ in range(args.steps)]
+        v = n * len(times) / sum(times)
+        print(json.dumps({
+            "impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sum(times) / len(times),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": workload_desc(s)},
+            "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": th, "kind": "oracle",
+                             "sample": f"first {n} of {s.T} tokens per step, fp64 C oracle"},
+            "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        }), flush=True)
+        return
+
+    if world > 1:
+        import torch
+        torch.distributed.init_process_group("nccl")
+    out = run_ours(args, s, rank, world)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(s, args.cpu_budget)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        import torch
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,186 @@
+/*
+ * moe.h -- C ABI of libmoe, the single-GPU Mixture-of-Experts layer
+ * (forward and backward) for NVIDIA GB300 (sm_103a).
+ *
+ * The operations follow "Introducing Olmo-core 3: open, scalable training
+ * infrastructure for large MoE models" (page 1), section "Scaling and
+ * optimizing MoE training": routing metadata is computed and kept on the GPU
+ * so the host can enqueue work without waiting for a copy back; routed rows
+ * are written directly into each expert's input buffer; one grouped GEMM runs
+ * all experts' feed-forward computations; MXFP8 is supported for the expert
+ * GEMMs. The layer math (softmax over E router logits, top-k, gates
+ * renormalised to sum 1, SwiGLU experts, E4M3 elements with one E8M0 scale
+ * per 32 along K) is the definition of the 8/128-expert top-4 benchmark
+ * layer of that page's introduction.
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ *  - Notation: T tokens, d hidden size, E experts, k experts per token,
+ *    f expert FFN width, R = T*k routed rows.
+ *  - Every pointer argument is a DEVICE pointer unless stated otherwise. The
+ *    caller owns and allocates every buffer, including the workspace; the
+ *    library never allocates or frees memory and keeps no state besides one
+ *    error word per device.
+ *  - Every call is asynchronous on `stream` (a cudaStream_t passed as void*;
+ *    NULL is the legacy default stream): no host synchronisation, no
+ *    device-to-host copy. Counts and offsets never leave the device.
+ *  - Layouts are row-major: x [T][d]; w_router [E][d] (row e is expert e's
+ *    router vector); w_gate, w_up [E][d][f]; w_down [E][f][d].
+ *  - dtype: MOE_F32 (everything fp32) or MOE_BF16 (activations and weights
+ *    bf16; router logits, gates and all accumulation fp32). MXFP8 expert
+ *    GEMMs are requested with MOE_MXFP8 where a call says so.
+ *  - Argument, shape and alignment errors are returned synchronously and
+ *    nothing is launched. Requirements: T >= 0, 1 <= k <= 8, k <= E <= 1024,
+ *    d and f multiples of 64, pointers 16-byte aligned.
+ *  - Errors found on the device (an index out of range, a bounded wait that
+ *    ran out) set the device error word; kernels then exit cleanly and never
+ *    trap. moe_get_device_error() reads and clears it.
+ *  - Identical inputs give bit-identical outputs (no floating-point atomics).
+ */
+#ifndef MOE_H_
+#define MOE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,   /* null pointer, negative size, k > E, ...        */
+  MOE_ERR_UNSUPPORTED = 2,   /* shape outside the supported set (see above)    */
+  MOE_ERR_ALIGNMENT = 3,     /* a pointer is not 16-byte aligned               */
+  MOE_ERR_WORKSPACE = 4,     /* workspace smaller than moe_workspace_size()    */
+  MOE_ERR_CUDA = 5,          /* a CUDA runtime call failed                     */
+  MOE_ERR_DEVICE_INDEX = 6,  /* device error word: index out of range          */
+  MOE_ERR_TIMEOUT = 7        /* device error word: a bounded wait ran out      */
+} moe_status;
+
+typedef enum { MOE_F32 = 0, MOE_BF16 = 1, MOE_MXFP8 = 2 } moe_dtype;
+
+/* Flags of moe_route. */
+#define MOE_ROUTE_LOGITS_IN 1 /* skip the router GEMM: `logits` is an input */
+
+/* Bytes of workspace that the calls below need for this shape (the maximum
+   over all calls). */
+size_t moe_workspace_size(int T, int d, int E, int k, int f, int dtype);
+
+/* Routing: router GEMM, softmax + top-k gates, per-expert counts, offsets and
+   the row placement ("Scaling and optimizing MoE training": on-GPU routing
+   metadata; rows placed directly into expert input buffers).
+     logits[t][e] = bias[e] + sum_c x[t][c] * w_router[e][c]     (fp32 accum)
+     topk_idx[t][0..k) = the k largest logits, ties to the smaller index,
+                         ordered by (logit desc, index asc)
+     gates[t][j]  = exp(l_j - l_max) / sum_{i in top-k} exp(l_i - l_max)
+     counts[e]    = number of (t, j) with topk_idx[t][j] == e
+     offsets[e]   = sum_{e' < e} counts[e'], offsets[E] = T*k  (unpadded)
+     dest_row[t][j] = offsets[e] + #{t' < t routed to e}   (rows of one expert
+                      in token order); src_row[dest_row[t][j]] = t*k + j
+   x: [T][d] dtype; w_router: [E][d] dtype; bias: [E] fp32 or NULL (a constant
+   per-expert logit bias, no gradient); logits: [T][E] fp32, written, or read
+   when flags & MOE_ROUTE_LOGITS_IN (then x/w_router/bias are unused);
+   topk_idx, dest_row: [T][k] int32; gates [T][k] fp32; counts [E];
+   offsets [E+1]; src_row [T*k] int32. */
+moe_status moe_route(const void* x, const void* w_router, const float* bias, int dtype, int T,
+                     int d, int E, int k, float* logits, int flags, int32_t* topk_idx, float* gates,
+                     int32_t* counts, int32_t* offsets, int32_t* dest_row, int32_t* src_row,
+                     void* workspace, size_t workspace_bytes, void* stream);
+
+/* Dispatch: x_perm[dest_row[t][j]] = x[t]  (an exact copy).
+   x: [T][d]; x_perm: [T*k][d]; both dtype. */
+moe_status moe_permute(const void* x, int dtype, int T, int d, int k, const int32_t* dest_row,
+                       void* x_perm, void* stream);
+
+/* Backward of the dispatch, plus the router's share of dx when dlogits is
+   given:  dx[t] = sum_j dx_perm[dest_row[t][j]]
+                 + sum_j dlogits[t][topk_idx[t][j]] * w_router[topk_idx[t][j]]
+   (fp32 sums in j order, one rounding to dtype). topk_idx, dlogits and
+   w_router are either all NULL (no router term) or all given. */
+moe_status moe_permute_bwd(const void* dx_perm, int dtype, int T, int d, int E, int k,
+                           const int32_t* dest_row, const int32_t* topk_idx, const float* dlogits,
+                           const void* w_router, void* dx, void* stream);
+
+/* Combine: y[t] = sum_j gates[t][j] * y_perm[dest_row[t][j]]
+   (fp32 sum in j order, rounded once to dtype). y_perm [T*k][d]; y [T][d]. */
+moe_status moe_combine_fwd(const void* y_perm, const float* gates, const int32_t* dest_row,
+                           int dtype, int T, int d, int k, void* y, void* stream);
+
+/* Backward of the combine:
+     dy_perm[dest_row[t][j]] = gates[t][j] * dy[t]            (dtype)
+     dgates[t][j] = sum_c dy[t][c] * y_perm[dest_row[t][j]][c] (fp32) */
+moe_status moe_combine_bwd(const void* dy, const void* y_perm, const float* gates,
+                           const int32_t* dest_row, int dtype, int T, int d, int k, void* dy_perm,
+                           float* dgates, void* stream);
+
+/* Router backward (softmax over the selected logits):
+     dlogits[t][i] = g_i * (dg_i - sum_j g_j dg_j) for i in top-k, 0 otherwise
+     dw_router[e][c] = sum over rows r of expert e of dlogits[t(r)][e] * x_perm[r][c]
+   with t(r) = src_row[r] / k. dlogits [T][E] fp32; dw_router [E][d] fp32;
+   x_perm [T*k][d] dtype (rows of x placed by moe_permute). */
+moe_status moe_route_bwd(const float* dgates, const float* gates, const int32_t* topk_idx,
+                         const int32_t* offsets, const int32_t* src_row, const void* x_perm,
+                         int dtype, int T, int d, int E, int k, float* dlogits, float* dw_router,
+                         void* stream);
+
+/* Grouped SwiGLU expert MLP, forward, all experts in one launch per GEMM
+   ("Scaling and optimizing MoE training": grouped GEMM). For every expert e
+   and row r in [offsets[e], offsets[e+1]):
+     h_g = x_perm[r] . w_gate[e],  h_u = x_perm[r] . w_up[e]   (fp32 accum)
+     a   = silu(h_g) * h_u,  y_perm[r] = a . w_down[e]
+   Outputs, saved for the backward: h_save [R][2f] = (h_g | h_u) and
+   a_save [R][f], plus y_perm [R][d]; all dtype. offsets: [E+1] device
+   int32 from moe_route; R = T*k is the row count the caller allocated. */
+moe_status moe_grouped_mlp_fwd(const void* x_perm, const void* w_gate, const void* w_up,
+                               const void* w_down, int dtype, const int32_t* offsets, int R, int E,
+                               int d, int f, void* h_save, void* a_save, void* y_perm,
+                               void* workspace, size_t workspace_bytes, void* stream);
+
+/* Grouped SwiGLU expert MLP, backward. With dh = (dh_g | dh_u):
+     da = dy_perm[r] . w_down[e]^T;  dh_g = da * h_u * silu'(h_g);
+     dh_u = da * silu(h_g);  dx_perm[r] = dh_g . w_gate[e]^T + dh_u . w_up[e]^T
+     dw_down[e] = sum_r a_save[r]^T dy_perm[r];
+     dw_gate[e] = sum_r x_perm[r]^T dh_g[r];  dw_up[e] = sum_r x_perm[r]^T dh_u[r]
+   (sums over the rows of expert e; experts with no rows get zero
+   gradients). dw_* are written (not accumulated), dtype. dh lives in the
+   workspace. */
+moe_status moe_grouped_mlp_bwd(const void* dy_perm, const void* x_perm, const void* h_save,
+                               const void* a_save, const void* w_gate, const void* w_up,
+                               const void* w_down, int dtype, const int32_t* offsets, int R, int E,
+                               int d, int f, void* dx_perm, void* dw_gate, void* dw_up,
+                               void* dw_down, void* workspace, size_t workspace_bytes,
+                               void* stream);
+
+/* MXFP8 block quantisation ("Scaling and optimizing MoE training": MXFP8):
+   E4M3 codes with one E8M0 scale per 32 consecutive elements.
+     axis 0: src [rows][K] bf16, blocks of 32 along K inside a row;
+             dst_e4m3 [rows][K], dst_e8m0 [rows][K/32]. K % 32 == 0.
+     axis 1: blocks of 32 consecutive rows of one column; with seg_offsets
+             ([nseg+1] device int32, NULL for one segment of all rows) blocks
+             start at each segment's first row and a segment's last block is
+             zero-padded; dst_e4m3 [rows][K]; dst_e8m0 [nblk][K] where segment
+             g owns block rows from sum_{h<g} ceil(len_h/32) -- the caller
+             sizes dst_e8m0 for ceil(rows/32) + nseg block rows.
+   Scale exponent s = ceil(log2(amax / 448)) clamped to [-127, 127]
+   (s = -127 for an all-zero block), byte s + 127; elements are
+   round-to-nearest-even of v * 2^-s, saturated to +-448. */
+moe_status mxfp8_quantize(const void* src, int rows, int K, int axis, const int32_t* seg_offsets,
+                          int nseg, uint8_t* dst_e4m3, uint8_t* dst_e8m0, void* stream);
+
+/* Synchronises `stream`, then returns and clears this device's error word
+   (MOE_OK if no kernel reported an error). */
+moe_status moe_get_device_error(void* stream);
+
+/* Number of SMs the kernels size their persistent grids for (0 on error). */
+int moe_sm_count(void);
+
+/* Number of kernels this process has launched through libmoe so far (a host
+   counter, bumped once per successful launch; for instrumentation). */
+uint64_t moe_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_H_ */

@@ -1,0 +1,318 @@
+// api.cu -- the extern "C" entry points of libmoe declared in include/moe.h:
+// argument validation, workspace carving and dispatch to the kernels.
+#include <cuda_bf16.h>
+
+#include <atomic>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+
+__device__ int g_moe_error_word;
+
+int* device_error_word() {
+  static int* ptrs[128] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return nullptr;
+  if (!ptrs[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_moe_error_word) != cudaSuccess) return nullptr;
+    ptrs[dev] = static_cast<int*>(p);
+  }
+  return ptrs[dev];
+}
+
+static std::atomic<unsigned long long> g_launches{0};
+void count_launch(int n) { g_launches.fetch_add((unsigned long long)n, std::memory_order_relaxed); }
+
+namespace {
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline size_t align256(size_t b) { return (b + 255) & ~size_t(255); }
+inline size_t elem_bytes(int dtype) { return dtype == MOE_F32 ? 4 : 2; }
+inline cudaStream_t S(void* s) { return static_cast<cudaStream_t>(s); }
+
+moe_status check_dims(int T, int d, int E, int k) {
+  if (T < 0 || d <= 0 || E <= 0 || k <= 0) return MOE_ERR_INVALID_ARG;
+  if (k > E) return MOE_ERR_INVALID_ARG;
+  if (k > 8 || E > 1024 || d % 64 != 0) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+moe_status check_dtype(int dtype) {
+  return (dtype == MOE_F32 || dtype == MOE_BF16) ? MOE_OK : MOE_ERR_UNSUPPORTED;
+}
+
+#define MOE_TRY(expr)                    \
+  do {                                   \
+    moe_status s_ = (expr);              \
+    if (s_ != MOE_OK) return s_;         \
+  } while (0)
+
+#define MOE_NEED(p)                                   \
+  do {                                                \
+    if ((p) == nullptr) return MOE_ERR_INVALID_ARG;   \
+    if (!aligned16(p)) return MOE_ERR_ALIGNMENT;      \
+  } while (0)
+
+// Workspace of the backward GEMM chain: dA [R][f] and dh [R][2f].
+size_t mlp_bwd_ws(long R, int f, int dtype) {
+  return align256((size_t)R * f * elem_bytes(dtype)) + align256((size_t)R * 2 * f * elem_bytes(dtype));
+}
+
+template <typename T>
+moe_status mlp_fwd_simt(const void* x_perm, const void* wg, const void* wu, const void* wd,
+                        const int32_t* offsets, int R, int E, int d, int f, void* h, void* a,
+                        void* y, cudaStream_t st) {
+  SimtGemm g{};
+  g.A = x_perm; g.sAm = d; g.sAk = 1;
+  g.B0 = wg; g.B1 = wu; g.sBk = f; g.sBn = 1; g.sBe = (long)d * f; g.kSplit = d; g.nSplit = f;
+  g.C0 = h; g.C1 = h; g.sCm = 2L * f; g.sCn = 1; g.cSplit = 2 * f;
+  g.offsets = offsets; g.E = E; g.M = R; g.N = 2 * f; g.K = d;
+  MOE_CUDA_TRY((launch_simt_gemm<T, T, T>(g, st)));
+  MOE_CUDA_TRY(launch_swiglu_fwd<T>(h, R, f, a, st));
+  SimtGemm g2{};
+  g2.A = a; g2.sAm = f; g2.sAk = 1;
+  g2.B0 = wd; g2.B1 = wd; g2.sBk = d; g2.sBn = 1; g2.sBe = (long)f * d; g2.kSplit = f; g2.nSplit = d;
+  g2.C0 = y; g2.C1 = y; g2.sCm = d; g2.sCn = 1; g2.cSplit = d;
+  g2.offsets = offsets; g2.E = E; g2.M = R; g2.N = d; g2.K = f;
+  MOE_CUDA_TRY((launch_simt_gemm<T, T, T>(g2, st)));
+  return MOE_OK;
+}
+
+template <typename T>
+moe_status mlp_bwd_simt(const void* dy_perm, const void* x_perm, const void* h, const void* a,
+                        const void* wg, const void* wu, const void* wd, const int32_t* offsets,
+                        int R, int E, int d, int f, void* dx_perm, void* dwg, void* dwu, void* dwd,
+                        void* ws, cudaStream_t st) {
+  char* w = static_cast<char*>(ws);
+  void* da = w;
+  void* dh = w + align256((size_t)R * f * sizeof(T));
+  // dA = dY . Wd^T
+  SimtGemm g{};
+  g.A = dy_perm; g.sAm = d; g.sAk = 1;
+  g.B0 = wd; g.B1 = wd; g.sBk = 1; g.sBn = d; g.sBe = (long)f * d; g.kSplit = d; g.nSplit = f;
+  g.C0 = da; g.C1 = da; g.sCm = f; g.sCn = 1; g.cSplit = f;
+  g.offsets = offsets; g.E = E; g.M = R; g.N = f; g.K = d;
+  MOE_CUDA_TRY((launch_simt_gemm<T, T, T>(g, st)));
+  MOE_CUDA_TRY(launch_swiglu_bwd<T>(da, h, R, f, dh, st));
+  // dx_perm = dh_g . Wg^T + dh_u . Wu^T
+  SimtGemm g2{};
+  g2.A = dh; g2.sAm = 2L * f; g2.sAk = 1;
+  g2.B0 = wg; g2.B1 = wu; g2.sBk = 1; g2.sBn = f; g2.sBe = (long)d * f; g2.kSplit = f; g2.nSplit = d;
+  g2.C0 = dx_perm; g2.C1 = dx_perm; g2.sCm = d; g2.sCn = 1; g2.cSplit = d;
+  g2.offsets = offsets; g2.E = E; g2.M = R; g2.N = d; g2.K = 2 * f;
+  MOE_CUDA_TRY((launch_simt_gemm<T, T, T>(g2, st)));
+  // dWd[e] = A_e^T dY_e
+  SimtGemm g3{};
+  g3.A = a; g3.sAm = 1; g3.sAk = f;
+  g3.B0 = dy_perm; g3.B1 = dy_perm; g3.sBk = d; g3.sBn = 1; g3.sBe = 0; g3.kSplit = 1 << 30; g3.nSplit = d;
+  g3.C0 = dwd; g3.C1 = dwd; g3.sCe = (long)f * d; g3.sCm = d; g3.sCn = 1; g3.cSplit = d;
+  g3.offsets = offsets; g3.E = E; g3.M = f; g3.N = d; g3.kragged = 1;
+  MOE_CUDA_TRY((launch_simt_gemm<T, T, T>(g3, st)));
+  // [dWg | dWu][e] = x_perm_e^T dh_e
+  SimtGemm g4{};
+  g4.A = x_perm; g4.sAm = 1; g4.sAk = d;
+  g4.B0 = dh; g4.B1 = dh; g4.sBk = 2L * f; g4.sBn = 1; g4.sBe = 0; g4.kSplit = 1 << 30; g4.nSplit = 2 * f;
+  g4.C0 = dwg; g4.C1 = dwu; g4.sCe = (long)d * f; g4.sCm = f; g4.sCn = 1; g4.cSplit = f;
+  g4.offsets = offsets; g4.E = E; g4.M = d; g4.N = 2 * f; g4.kragged = 1;
+  MOE_CUDA_TRY((launch_simt_gemm<T, T, T>(g4, st)));
+  return MOE_OK;
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+size_t moe_workspace_size(int T, int d, int E, int k, int f, int dtype) {
+  if (T < 0 || d <= 0 || E <= 0 || k <= 0 || f <= 0) return 0;
+  const long R = (long)T * k;
+  size_t route = align256(route_workspace_bytes(T, E));
+  size_t bwd = mlp_bwd_ws(R, f, dtype == MOE_F32 ? MOE_F32 : MOE_BF16);
+  return route > bwd ? route : bwd;
+}
+
+moe_status moe_route(const void* x, const void* w_router, const float* bias, int dtype, int T, int d,
+                     int E, int k, float* logits, int flags, int32_t* topk_idx, float* gates,
+                     int32_t* counts, int32_t* offsets, int32_t* dest_row, int32_t* src_row,
+                     void* workspace, size_t workspace_bytes, void* stream) {
+  MOE_TRY(check_dims(T, d, E, k));
+  MOE_TRY(check_dtype(dtype));
+  MOE_NEED(counts); MOE_NEED(offsets);
+  if (T > 0) {
+    MOE_NEED(logits); MOE_NEED(topk_idx); MOE_NEED(gates); MOE_NEED(dest_row); MOE_NEED(src_row);
+  }
+  if (workspace_bytes < route_workspace_bytes(T, E)) return MOE_ERR_WORKSPACE;
+  if (route_workspace_bytes(T, E) > 0) MOE_NEED(workspace);
+  cudaStream_t st = S(stream);
+  if (!(flags & MOE_ROUTE_LOGITS_IN) && T > 0) {
+    MOE_NEED(x); MOE_NEED(w_router);
+    if (bias && !aligned16(bias)) return MOE_ERR_ALIGNMENT;
+    SimtGemm g{};
+    g.A = x; g.sAm = d; g.sAk = 1;
+    g.B0 = w_router; g.B1 = w_router; g.sBk = 1; g.sBn = d; g.sBe = 0; g.kSplit = d; g.nSplit = E;
+    g.C0 = logits; g.C1 = logits; g.sCm = E; g.sCn = 1; g.cSplit = E;
+    g.col_bias = bias; g.offsets = nullptr; g.E = 1; g.M = T; g.N = E; g.K = d;
+    if (dtype == MOE_F32) MOE_CUDA_TRY((launch_simt_gemm<float, float, float>(g, st)));
+    else MOE_CUDA_TRY((launch_simt_gemm<__nv_bfloat16, __nv_bfloat16, float>(g, st)));
+  }
+  MOE_CUDA_TRY(launch_route_meta(logits, T, E, k, topk_idx, gates, counts, offsets, dest_row, src_row,
+                                 static_cast<int32_t*>(workspace), st));
+  return MOE_OK;
+}
+
+moe_status moe_permute(const void* x, int dtype, int T, int d, int k, const int32_t* dest_row,
+                       void* x_perm, void* stream) {
+  MOE_TRY(check_dims(T, d, k, k));
+  MOE_TRY(check_dtype(dtype));
+  if (T == 0) return MOE_OK;
+  MOE_NEED(x); MOE_NEED(dest_row); MOE_NEED(x_perm);
+  if (dtype == MOE_F32) MOE_CUDA_TRY(launch_permute<float>(x, T, d, k, dest_row, x_perm, S(stream)));
+  else MOE_CUDA_TRY(launch_permute<__nv_bfloat16>(x, T, d, k, dest_row, x_perm, S(stream)));
+  return MOE_OK;
+}
+
+moe_status moe_permute_bwd(const void* dx_perm, int dtype, int T, int d, int E, int k,
+                           const int32_t* dest_row, const int32_t* topk_idx, const float* dlogits,
+                           const void* w_router, void* dx, void* stream) {
+  MOE_TRY(check_dims(T, d, E, k));
+  MOE_TRY(check_dtype(dtype));
+  const int given = (topk_idx != nullptr) + (dlogits != nullptr) + (w_router != nullptr);
+  if (given != 0 && given != 3) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  MOE_NEED(dx_perm); MOE_NEED(dest_row); MOE_NEED(dx);
+  if (given == 3) { MOE_NEED(topk_idx); MOE_NEED(dlogits); MOE_NEED(w_router); }
+  if (dtype == MOE_F32)
+    MOE_CUDA_TRY(launch_permute_bwd<float>(dx_perm, T, d, E, k, dest_row, topk_idx, dlogits, w_router,
+                                           dx, S(stream)));
+  else
+    MOE_CUDA_TRY(launch_permute_bwd<__nv_bfloat16>(dx_perm, T, d, E, k, dest_row, topk_idx, dlogits,
+                                                   w_router, dx, S(stream)));
+  return MOE_OK;
+}
+
+moe_status moe_combine_fwd(const void* y_perm, const float* gates, const int32_t* dest_row, int dtype,
+                           int T, int d, int k, void* y, void* stream) {
+  MOE_TRY(check_dims(T, d, k, k));
+  MOE_TRY(check_dtype(dtype));
+  if (T == 0) return MOE_OK;
+  MOE_NEED(y_perm); MOE_NEED(gates); MOE_NEED(dest_row); MOE_NEED(y);
+  if (dtype == MOE_F32)
+    MOE_CUDA_TRY(launch_combine_fwd<float>(y_perm, gates, dest_row, T, d, k, y, S(stream)));
+  else
+    MOE_CUDA_TRY(launch_combine_fwd<__nv_bfloat16>(y_perm, gates, dest_row, T, d, k, y, S(stream)));
+  return MOE_OK;
+}
+
+moe_status moe_combine_bwd(const void* dy, const void* y_perm, const float* gates,
+                           const int32_t* dest_row, int dtype, int T, int d, int k, void* dy_perm,
+                           float* dgates, void* stream) {
+  MOE_TRY(check_dims(T, d, k, k));
+  MOE_TRY(check_dtype(dtype));
+  if (T == 0) return MOE_OK;
+  MOE_NEED(dy); MOE_NEED(y_perm); MOE_NEED(gates); MOE_NEED(dest_row); MOE_NEED(dy_perm);
+  MOE_NEED(dgates);
+  if (dtype == MOE_F32)
+    MOE_CUDA_TRY(launch_combine_bwd<float>(dy, y_perm, gates, dest_row, T, d, k, dy_perm, dgates,
+                                           S(stream)));
+  else
+    MOE_CUDA_TRY(launch_combine_bwd<__nv_bfloat16>(dy, y_perm, gates, dest_row, T, d, k, dy_perm,
+                                                   dgates, S(stream)));
+  return MOE_OK;
+}
+
+moe_status moe_route_bwd(const float* dgates, const float* gates, const int32_t* topk_idx,
+                         const int32_t* offsets, const int32_t* src_row, const void* x_perm,
+                         int dtype, int T, int d, int E, int k, float* dlogits, float* dw_router,
+                         void* stream) {
+  MOE_TRY(check_dims(T, d, E, k));
+  MOE_TRY(check_dtype(dtype));
+  MOE_NEED(offsets); MOE_NEED(dw_router);
+  if (T > 0) {
+    MOE_NEED(dgates); MOE_NEED(gates); MOE_NEED(topk_idx); MOE_NEED(src_row); MOE_NEED(x_perm);
+    MOE_NEED(dlogits);
+  }
+  if (dtype == MOE_F32)
+    MOE_CUDA_TRY(launch_route_bwd<float>(dgates, gates, topk_idx, offsets, src_row, x_perm, T, d, E, k,
+                                         dlogits, dw_router, S(stream)));
+  else
+    MOE_CUDA_TRY(launch_route_bwd<__nv_bfloat16>(dgates, gates, topk_idx, offsets, src_row, x_perm, T,
+                                                 d, E, k, dlogits, dw_router, S(stream)));
+  return MOE_OK;
+}
+
+moe_status moe_grouped_mlp_fwd(const void* x_perm, const void* w_gate, const void* w_up,
+                               const void* w_down, int dtype, const int32_t* offsets, int R, int E,
+                               int d, int f, void* h_save, void* a_save, void* y_perm,
+                               void* workspace, size_t workspace_bytes, void* stream) {
+  MOE_TRY(check_dims(R, d, E, 1));
+  MOE_TRY(check_dtype(dtype));
+  if (f <= 0) return MOE_ERR_INVALID_ARG;
+  if (f % 64 != 0) return MOE_ERR_UNSUPPORTED;
+  MOE_NEED(w_gate); MOE_NEED(w_up); MOE_NEED(w_down); MOE_NEED(offsets);
+  if (R == 0) return MOE_OK;
+  MOE_NEED(x_perm); MOE_NEED(h_save); MOE_NEED(a_save); MOE_NEED(y_perm);
+  (void)workspace; (void)workspace_bytes;
+  if (dtype == MOE_F32)
+    return mlp_fwd_simt<float>(x_perm, w_gate, w_up, w_down, offsets, R, E, d, f, h_save, a_save, y_perm,
+                               S(stream));
+  return mlp_fwd_simt<__nv_bfloat16>(x_perm, w_gate, w_up, w_down, offsets, R, E, d, f, h_save, a_save,
+                                     y_perm, S(stream));
+}
+
+moe_status moe_grouped_mlp_bwd(const void* dy_perm, const void* x_perm, const void* h_save,
+                               const void* a_save, const void* w_gate, const void* w_up,
+                               const void* w_down, int dtype, const int32_t* offsets, int R, int E,
+                               int d, int f, void* dx_perm, void* dw_gate, void* dw_up,
+                               void* dw_down, void* workspace, size_t workspace_bytes,
+                               void* stream) {
+  MOE_TRY(check_dims(R, d, E, 1));
+  MOE_TRY(check_dtype(dtype));
+  if (f <= 0) return MOE_ERR_INVALID_ARG;
+  if (f % 64 != 0) return MOE_ERR_UNSUPPORTED;
+  MOE_NEED(w_gate); MOE_NEED(w_up); MOE_NEED(w_down); MOE_NEED(offsets);
+  MOE_NEED(dw_gate); MOE_NEED(dw_up); MOE_NEED(dw_down);
+  if (workspace_bytes < mlp_bwd_ws(R, f, dtype)) return MOE_ERR_WORKSPACE;
+  if (R > 0) {
+    MOE_NEED(dy_perm); MOE_NEED(x_perm); MOE_NEED(h_save); MOE_NEED(a_save); MOE_NEED(dx_perm);
+    MOE_NEED(workspace);
+  }
+  if (dtype == MOE_F32)
+    return mlp_bwd_simt<float>(dy_perm, x_perm, h_save, a_save, w_gate, w_up, w_down, offsets, R, E, d,
+                               f, dx_perm, dw_gate, dw_up, dw_down, workspace, S(stream));
+  return mlp_bwd_simt<__nv_bfloat16>(dy_perm, x_perm, h_save, a_save, w_gate, w_up, w_down, offsets, R,
+                                     E, d, f, dx_perm, dw_gate, dw_up, dw_down, workspace, S(stream));
+}
+
+moe_status mxfp8_quantize(const void* src, int rows, int K, int axis, const int32_t* seg_offsets,
+                          int nseg, uint8_t* dst_e4m3, uint8_t* dst_e8m0, void* stream) {
+  (void)src; (void)rows; (void)K; (void)axis; (void)seg_offsets; (void)nseg; (void)dst_e4m3;
+  (void)dst_e8m0; (void)stream;
+  return MOE_ERR_UNSUPPORTED;
+}
+
+moe_status moe_get_device_error(void* stream) {
+  MOE_CUDA_TRY(cudaStreamSynchronize(S(stream)));
+  int v = 0;
+  MOE_CUDA_TRY(cudaMemcpyFromSymbol(&v, g_moe_error_word, sizeof(int)));
+  if (v != 0) {
+    const int zero = 0;
+    MOE_CUDA_TRY(cudaMemcpyToSymbol(g_moe_error_word, &zero, sizeof(int)));
+  }
+  return static_cast<moe_status>(v);
+}
+
+uint64_t moe_launch_count(void) { return (uint64_t)g_launches.load(std::memory_order_relaxed); }
+
+int moe_sm_count(void) {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return n;
+}
+
+}  // extern "C"

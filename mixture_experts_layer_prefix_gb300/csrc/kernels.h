@@ -1,0 +1,64 @@
+// kernels.h -- internal host-side launchers of libmoe (not part of the ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace moe {
+
+// ------------------------------------------------------------- routing
+constexpr int kTokensPerChunk = 8;  // tokens per routing chunk (one warp)
+int route_num_chunks(int T);
+size_t route_workspace_bytes(int T, int E);
+cudaError_t launch_route_meta(const float* logits, int T, int E, int k, int32_t* topk_idx,
+                              float* gates, int32_t* counts, int32_t* offsets, int32_t* dest_row,
+                              int32_t* src_row, int32_t* hist, cudaStream_t st);
+
+// ------------------------------------------------ permute / combine / router bwd
+template <typename T>
+cudaError_t launch_permute(const void* x, int Tn, int d, int k, const int32_t* dest_row, void* x_perm,
+                           cudaStream_t st);
+template <typename T>
+cudaError_t launch_combine_fwd(const void* y_perm, const float* gates, const int32_t* dest_row, int Tn,
+                               int d, int k, void* y, cudaStream_t st);
+template <typename T>
+cudaError_t launch_combine_bwd(const void* dy, const void* y_perm, const float* gates,
+                               const int32_t* dest_row, int Tn, int d, int k, void* dy_perm,
+                               float* dgates, cudaStream_t st);
+template <typename T>
+cudaError_t launch_permute_bwd(const void* dx_perm, int Tn, int d, int E, int k,
+                               const int32_t* dest_row, const int32_t* topk_idx, const float* dlogits,
+                               const void* w_r, void* dx, cudaStream_t st);
+template <typename T>
+cudaError_t launch_route_bwd(const float* dgates, const float* gates, const int32_t* topk_idx,
+                             const int32_t* offsets, const int32_t* src_row, const void* x_perm,
+                             int Tn, int d, int E, int k, float* dlogits, float* dw_r,
+                             cudaStream_t st);
+
+// ------------------------------------------------------ CUDA-core grouped GEMM
+struct SimtGemm {
+  const void* A;
+  long sAm, sAk;
+  const void* B0;
+  const void* B1;
+  long sBk, sBn, sBe;
+  int kSplit, nSplit;
+  void* C0;
+  void* C1;
+  long sCm, sCn, sCe;
+  int cSplit;
+  const float* col_bias;
+  const int32_t* offsets;  // nullptr: one group of M rows (row-ragged mode only)
+  int E;
+  int M, N, K;
+  int kragged;
+};
+template <typename TA, typename TB, typename TC>
+cudaError_t launch_simt_gemm(const SimtGemm& g, cudaStream_t st);
+template <typename T>
+cudaError_t launch_swiglu_fwd(const void* h, long rows, int f, void* a, cudaStream_t st);
+template <typename T>
+cudaError_t launch_swiglu_bwd(const void* da, const void* h, long rows, int f, void* dh, cudaStream_t st);
+
+}  // namespace moe

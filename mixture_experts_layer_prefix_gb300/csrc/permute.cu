@@ -1,0 +1,336 @@
+// permute.cu -- dispatch (permute), combine, their backward passes and the
+// router backward. All are HBM-bound row gathers/scatters: one warp per token
+// row, 16-byte vector loads and stores, fp32 arithmetic, one rounding per
+// output element. ("Introducing Olmo-core 3", section "Scaling and optimizing
+// MoE training": routed rows are placed directly into the experts' input
+// buffers; the combine is the gate-weighted return to token order.)
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+
+namespace {
+
+constexpr int kRowWarps = 8;
+
+// x_perm[dest_row[t][j]] = x[t]
+template <typename T>
+__global__ void __launch_bounds__(kRowWarps * 32)
+permute_kernel(const T* __restrict__ x, int Tn, int d, int k, const int32_t* __restrict__ dest_row,
+               T* __restrict__ x_perm) {
+  using V = Vec16<T>;
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x * kRowWarps + (threadIdx.x >> 5);
+  if (t >= Tn) return;
+  int dest = lane < k ? dest_row[(size_t)t * k + lane] : 0;
+  const T* src = x + (size_t)t * d;
+  for (int c = lane * V::N; c < d; c += 32 * V::N) {
+    const uint4 q = *reinterpret_cast<const uint4*>(src + c);
+    for (int j = 0; j < k; ++j) {
+      const int r = __shfl_sync(0xffffffffu, dest, j);
+      *reinterpret_cast<uint4*>(x_perm + (size_t)r * d + c) = q;
+    }
+  }
+}
+
+// y[t] = sum_j g[t][j] * y_perm[dest_row[t][j]]   (fp32, j ascending)
+template <typename T>
+__global__ void __launch_bounds__(kRowWarps * 32)
+combine_fwd_kernel(const T* __restrict__ y_perm, const float* __restrict__ gates,
+                   const int32_t* __restrict__ dest_row, int Tn, int d, int k, T* __restrict__ y) {
+  using V = Vec16<T>;
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x * kRowWarps + (threadIdx.x >> 5);
+  if (t >= Tn) return;
+  const int my_dest = lane < k ? dest_row[(size_t)t * k + lane] : 0;
+  const float my_g = lane < k ? gates[(size_t)t * k + lane] : 0.0f;
+  int dest[8];
+  float g[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    dest[j] = __shfl_sync(0xffffffffu, my_dest, j);
+    g[j] = __shfl_sync(0xffffffffu, my_g, j);
+  }
+  for (int c = lane * V::N; c < d; c += 32 * V::N) {
+    float acc[V::N];
+#pragma unroll
+    for (int i = 0; i < V::N; ++i) acc[i] = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (j < k) {
+        float v[V::N];
+        V::load(y_perm + (size_t)dest[j] * d + c, v);
+#pragma unroll
+        for (int i = 0; i < V::N; ++i) acc[i] = fmaf(g[j], v[i], acc[i]);
+      }
+    }
+    V::store(y + (size_t)t * d + c, acc);
+  }
+}
+
+// dy_perm[dest] = g * dy[t];  dgates[t][j] = <dy[t], y_perm[dest]>
+template <typename T>
+__global__ void __launch_bounds__(kRowWarps * 32)
+combine_bwd_kernel(const T* __restrict__ dy, const T* __restrict__ y_perm,
+                   const float* __restrict__ gates, const int32_t* __restrict__ dest_row, int Tn,
+                   int d, int k, T* __restrict__ dy_perm, float* __restrict__ dgates) {
+  using V = Vec16<T>;
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x * kRowWarps + (threadIdx.x >> 5);
+  if (t >= Tn) return;
+  const int my_dest = lane < k ? dest_row[(size_t)t * k + lane] : 0;
+  const float my_g = lane < k ? gates[(size_t)t * k + lane] : 0.0f;
+  int dest[8];
+  float g[8], dot[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    dest[j] = __shfl_sync(0xffffffffu, my_dest, j);
+    g[j] = __shfl_sync(0xffffffffu, my_g, j);
+    dot[j] = 0.0f;
+  }
+  for (int c = lane * V::N; c < d; c += 32 * V::N) {
+    float u[V::N];
+    V::load(dy + (size_t)t * d + c, u);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (j < k) {
+        float v[V::N], w[V::N];
+        V::load(y_perm + (size_t)dest[j] * d + c, v);
+#pragma unroll
+        for (int i = 0; i < V::N; ++i) {
+          dot[j] = fmaf(u[i], v[i], dot[j]);
+          w[i] = g[j] * u[i];
+        }
+        V::store(dy_perm + (size_t)dest[j] * d + c, w);
+      }
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    if (j < k) {
+      const float s = warp_sum(dot[j]);
+      if (lane == 0) dgates[(size_t)t * k + j] = s;
+    }
+  }
+}
+
+// dx[t] = sum_j dx_perm[dest[t][j]] (+ sum_j dl[t][e_j] * w_r[e_j])
+template <typename T>
+__global__ void __launch_bounds__(kRowWarps * 32)
+permute_bwd_kernel(const T* __restrict__ dx_perm, int Tn, int d, int E, int k,
+                   const int32_t* __restrict__ dest_row, const int32_t* __restrict__ topk_idx,
+                   const float* __restrict__ dlogits, const T* __restrict__ w_r,
+                   T* __restrict__ dx) {
+  using V = Vec16<T>;
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x * kRowWarps + (threadIdx.x >> 5);
+  if (t >= Tn) return;
+  const bool router = dlogits != nullptr;
+  const int my_dest = lane < k ? dest_row[(size_t)t * k + lane] : 0;
+  int my_e = 0;
+  float my_dl = 0.0f;
+  if (router && lane < k) {
+    my_e = topk_idx[(size_t)t * k + lane];
+    my_dl = dlogits[(size_t)t * E + my_e];
+  }
+  int dest[8], ex[8];
+  float dl[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    dest[j] = __shfl_sync(0xffffffffu, my_dest, j);
+    ex[j] = __shfl_sync(0xffffffffu, my_e, j);
+    dl[j] = __shfl_sync(0xffffffffu, my_dl, j);
+  }
+  for (int c = lane * V::N; c < d; c += 32 * V::N) {
+    float acc[V::N];
+#pragma unroll
+    for (int i = 0; i < V::N; ++i) acc[i] = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (j < k) {
+        float v[V::N];
+        V::load(dx_perm + (size_t)dest[j] * d + c, v);
+#pragma unroll
+        for (int i = 0; i < V::N; ++i) acc[i] += v[i];
+      }
+    }
+    if (router) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        if (j < k) {
+          float w[V::N];
+          V::load(w_r + (size_t)ex[j] * d + c, w);
+#pragma unroll
+          for (int i = 0; i < V::N; ++i) acc[i] = fmaf(dl[j], w[i], acc[i]);
+        }
+      }
+    }
+    V::store(dx + (size_t)t * d + c, acc);
+  }
+}
+
+// dlogits[t][i] = g_i (dg_i - sum_j g_j dg_j) on the selected experts, else 0.
+__global__ void __launch_bounds__(kRowWarps * 32)
+router_dlogits_kernel(const float* __restrict__ dgates, const float* __restrict__ gates,
+                      const int32_t* __restrict__ topk_idx, int Tn, int E, int k,
+                      float* __restrict__ dlogits) {
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x * kRowWarps + (threadIdx.x >> 5);
+  if (t >= Tn) return;
+  float g = 0.0f, dg = 0.0f;
+  int e = -1;
+  if (lane < k) {
+    g = gates[(size_t)t * k + lane];
+    dg = dgates[(size_t)t * k + lane];
+    e = topk_idx[(size_t)t * k + lane];
+  }
+  const float s = warp_sum(g * dg);
+  const float dl = g * (dg - s);
+  int ej[8];
+  float dlj[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    ej[j] = __shfl_sync(0xffffffffu, e, j);
+    dlj[j] = __shfl_sync(0xffffffffu, dl, j);
+  }
+  for (int c = lane; c < E; c += 32) {
+    float v = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      if (j < k && ej[j] == c) v = dlj[j];
+    dlogits[(size_t)t * E + c] = v;
+  }
+}
+
+// dw_r[e][c] = sum over rows r of expert e of dlogits[t(r)][e] * x_perm[r][c].
+// Grid (E, ceil(d / 256)); 8 warps split the rows, each lane owns 8 columns;
+// warps are reduced in fixed order through shared memory.
+template <typename T>
+__global__ void __launch_bounds__(256)
+router_dw_kernel(const float* __restrict__ dlogits, const int32_t* __restrict__ offsets,
+                 const int32_t* __restrict__ src_row, const T* __restrict__ x_perm, int d, int E,
+                 int k, float* __restrict__ dw_r) {
+  constexpr int VN = Vec16<T>::N;
+  constexpr int COLS = 32 * VN;  // columns per warp pass
+  __shared__ float part[8][256];
+  const int e = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int r0 = offsets[e], r1 = offsets[e + 1];
+  for (int cbase = blockIdx.y * 256; cbase < min(d, (int)(blockIdx.y + 1) * 256); cbase += COLS) {
+    const int c = cbase + lane * VN;
+    float acc[VN];
+#pragma unroll
+    for (int i = 0; i < VN; ++i) acc[i] = 0.0f;
+    if (c < d) {
+      int r = r0 + warp;
+      for (; r + 24 < r1; r += 32) {
+        float v[4][VN], w[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int rr = r + 8 * u;
+          w[u] = dlogits[(size_t)(src_row[rr] / k) * E + e];
+          Vec16<T>::load(x_perm + (size_t)rr * d + c, v[u]);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+#pragma unroll
+          for (int i = 0; i < VN; ++i) acc[i] = fmaf(w[u], v[u][i], acc[i]);
+      }
+      for (; r < r1; r += 8) {
+        float v[VN];
+        const float w = dlogits[(size_t)(src_row[r] / k) * E + e];
+        Vec16<T>::load(x_perm + (size_t)r * d + c, v);
+#pragma unroll
+        for (int i = 0; i < VN; ++i) acc[i] = fmaf(w, v[i], acc[i]);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < VN; ++i) part[warp][(lane * VN + i) % 256] = acc[i];
+    __syncthreads();
+    const int cc = cbase + threadIdx.x;
+    if (threadIdx.x < COLS && cc < d) {
+      float s = 0.0f;
+#pragma unroll
+      for (int w = 0; w < 8; ++w) s += part[w][threadIdx.x];
+      dw_r[(size_t)e * d + cc] = s;
+    }
+    __syncthreads();
+  }
+}
+
+template <typename T> inline int row_grid(int Tn) { return (Tn + kRowWarps - 1) / kRowWarps; }
+
+}  // namespace
+
+template <typename T>
+cudaError_t launch_permute(const void* x, int Tn, int d, int k, const int32_t* dest_row, void* x_perm,
+                           cudaStream_t st) {
+  if (Tn == 0) return cudaSuccess;
+  MOE_COUNTED permute_kernel<T><<<row_grid<T>(Tn), kRowWarps * 32, 0, st>>>(
+      static_cast<const T*>(x), Tn, d, k, dest_row, static_cast<T*>(x_perm));
+  return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_combine_fwd(const void* y_perm, const float* gates, const int32_t* dest_row, int Tn,
+                               int d, int k, void* y, cudaStream_t st) {
+  if (Tn == 0) return cudaSuccess;
+  MOE_COUNTED combine_fwd_kernel<T><<<row_grid<T>(Tn), kRowWarps * 32, 0, st>>>(
+      static_cast<const T*>(y_perm), gates, dest_row, Tn, d, k, static_cast<T*>(y));
+  return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_combine_bwd(const void* dy, const void* y_perm, const float* gates,
+                               const int32_t* dest_row, int Tn, int d, int k, void* dy_perm,
+                               float* dgates, cudaStream_t st) {
+  if (Tn == 0) return cudaSuccess;
+  MOE_COUNTED combine_bwd_kernel<T><<<row_grid<T>(Tn), kRowWarps * 32, 0, st>>>(
+      static_cast<const T*>(dy), static_cast<const T*>(y_perm), gates, dest_row, Tn, d, k,
+      static_cast<T*>(dy_perm), dgates);
+  return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_permute_bwd(const void* dx_perm, int Tn, int d, int E, int k,
+                               const int32_t* dest_row, const int32_t* topk_idx, const float* dlogits,
+                               const void* w_r, void* dx, cudaStream_t st) {
+  if (Tn == 0) return cudaSuccess;
+  MOE_COUNTED permute_bwd_kernel<T><<<row_grid<T>(Tn), kRowWarps * 32, 0, st>>>(
+      static_cast<const T*>(dx_perm), Tn, d, E, k, dest_row, topk_idx, dlogits,
+      static_cast<const T*>(w_r), static_cast<T*>(dx));
+  return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_route_bwd(const float* dgates, const float* gates, const int32_t* topk_idx,
+                             const int32_t* offsets, const int32_t* src_row, const void* x_perm,
+                             int Tn, int d, int E, int k, float* dlogits, float* dw_r,
+                             cudaStream_t st) {
+  if (Tn > 0)
+    MOE_COUNTED router_dlogits_kernel<<<row_grid<T>(Tn), kRowWarps * 32, 0, st>>>(dgates, gates, topk_idx, Tn,
+                                                                       E, k, dlogits);
+  dim3 grid(E, (d + 255) / 256);
+  MOE_COUNTED router_dw_kernel<T><<<grid, 256, 0, st>>>(dlogits, offsets, src_row, static_cast<const T*>(x_perm),
+                                            d, E, k, dw_r);
+  return cudaGetLastError();
+}
+
+#define MOE_INST(T)                                                                              \
+  template cudaError_t launch_permute<T>(const void*, int, int, int, const int32_t*, void*,      \
+                                         cudaStream_t);                                          \
+  template cudaError_t launch_combine_fwd<T>(const void*, const float*, const int32_t*, int, int, \
+                                             int, void*, cudaStream_t);                          \
+  template cudaError_t launch_combine_bwd<T>(const void*, const void*, const float*,             \
+                                             const int32_t*, int, int, int, void*, float*,       \
+                                             cudaStream_t);                                      \
+  template cudaError_t launch_permute_bwd<T>(const void*, int, int, int, int, const int32_t*,    \
+                                             const int32_t*, const float*, const void*, void*,   \
+                                             cudaStream_t);                                      \
+  template cudaError_t launch_route_bwd<T>(const float*, const float*, const int32_t*,           \
+                                           const int32_t*, const int32_t*, const void*, int, int, \
+                                           int, int, float*, float*, cudaStream_t);
+MOE_INST(float)
+MOE_INST(__nv_bfloat16)
+#undef MOE_INST
+
+}  // namespace moe

@@ -1,0 +1,123 @@
+"""The MoE layer's forward and backward as a sequence of libmoe calls.
+
+This module holds device buffers (torch tensors, allocated once per shape)
+and calls the C ABI in order; every step of the computation runs in the
+library's kernels. Order of calls:
+
+  forward : moe_route -> moe_permute -> moe_grouped_mlp_fwd -> moe_combine_fwd
+  backward: moe_combine_bwd -> moe_route_bwd -> moe_grouped_mlp_bwd
+            -> moe_permute_bwd (adds the router's share of dx)
+"""
+from __future__ import annotations
+
+import dataclasses
+
+import numpy as np
+import torch
+
+from . import _native as N
+
+
+@dataclasses.dataclass
+class Params:
+    x: torch.Tensor
+    w_router: torch.Tensor      # [E, d]
+    bias: torch.Tensor | None   # [E] fp32
+    w_gate: torch.Tensor        # [E, d, f]
+    w_up: torch.Tensor          # [E, d, f]
+    w_down: torch.Tensor        # [E, f, d]
+    dy: torch.Tensor            # [T, d]
+
+
+def torch_dtype(dtype: int):
+    return torch.float32 if dtype == N.MOE_F32 else torch.bfloat16
+
+
+def to_device(a: np.ndarray, dtype: int, device="cuda") -> torch.Tensor:
+    """float32 numpy (bf16-exact when dtype is bf16) -> device tensor of the storage type."""
+    t = torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32))
+    return t.to(device=device).to(torch_dtype(dtype))
+
+
+def params_from_inputs(inp, dtype: int, device="cuda") -> Params:
+    """Upload seeded synthetic inputs (synth.Inputs); w_r is stored [E, d]."""
+    s = inp.s
+    b = inp.bias()
+    wg = torch.empty((s.E, s.d, s.f), dtype=torch_dtype(dtype), device=device)
+    wu = torch.empty_like(wg)
+    wd = torch.empty((s.E, s.f, s.d), dtype=torch_dtype(dtype), device=device)
+    for e in range(s.E):  # expert by expert: bounded host memory for large layers
+        wg[e].copy_(torch.from_numpy(inp.w_gate_e(e)))
+        wu[e].copy_(torch.from_numpy(inp.w_up_e(e)))
+        wd[e].copy_(torch.from_numpy(inp.w_down_e(e)))
+    return Params(
+        x=to_device(inp.x(), dtype, device),
+        w_router=to_device(np.ascontiguousarray(inp.w_r().T), dtype, device),
+        bias=None if b is None else torch.from_numpy(b).to(device),
+        w_gate=wg, w_up=wu, w_down=wd,
+        dy=to_device(inp.dy(), dtype, device),
+    )
+
+
+class Buffers:
+    """Every activation, gradient and metadata buffer of one layer shape."""
+
+    def __init__(self, T, d, E, k, f, dtype, device="cuda"):
+        self.T, self.d, self.E, self.k, self.f, self.dtype = T, d, E, k, f, dtype
+        R = T * k
+        self.R = R
+        td = torch_dtype(dtype)
+        i32, f32 = torch.int32, torch.float32
+        z = lambda *sh, dt=td: torch.empty(sh, dtype=dt, device=device)  # noqa: E731
+        self.logits = z(T, E, dt=f32)
+        self.topk_idx = z(T, k, dt=i32)
+        self.gates = z(T, k, dt=f32)
+        self.counts = z(E, dt=i32)
+        self.offsets = z(E + 1, dt=i32)
+        self.dest_row = z(T, k, dt=i32)
+        self.src_row = z(R, dt=i32)
+        self.x_perm = z(R, d)
+        self.h_save = z(R, 2 * f)
+        self.a_save = z(R, f)
+        self.y_perm = z(R, d)
+        self.y = z(T, d)
+        self.dy_perm = z(R, d)
+        self.dgates = z(T, k, dt=f32)
+        self.dlogits = z(T, E, dt=f32)
+        self.dw_router = z(E, d, dt=f32)
+        self.dx_perm = z(R, d)
+        self.dx = z(T, d)
+        self.dw_gate = z(E, d, f)
+        self.dw_up = z(E, d, f)
+        self.dw_down = z(E, f, d)
+        self.workspace = torch.empty(max(1, N.moe_workspace_size(T, d, E, k, f, dtype)),
+                                     dtype=torch.uint8, device=device)
+
+
+def forward(p: Params, b: Buffers, logits_in: bool = False, stream=None):
+    T, d, E, k, f, dt = b.T, b.d, b.E, b.k, b.f, b.dtype
+    N.moe_route(p.x, p.w_router, p.bias, dt, T, d, E, k, b.logits,
+                N.MOE_ROUTE_LOGITS_IN if logits_in else 0, b.topk_idx, b.gates, b.counts, b.offsets,
+                b.dest_row, b.src_row, b.workspace, stream)
+    N.moe_permute(p.x, dt, T, d, k, b.dest_row, b.x_perm, stream)
+    N.moe_grouped_mlp_fwd(b.x_perm, p.w_gate, p.w_up, p.w_down, dt, b.offsets, b.R, E, d, f, b.h_save,
+                          b.a_save, b.y_perm, b.workspace, stream)
+    N.moe_combine_fwd(b.y_perm, b.gates, b.dest_row, dt, T, d, k, b.y, stream)
+
+
+def backward(p: Params, b: Buffers, stream=None):
+    T, d, E, k, f, dt = b.T, b.d, b.E, b.k, b.f, b.dtype
+    N.moe_combine_bwd(p.dy, b.y_perm, b.gates, b.dest_row, dt, T, d, k, b.dy_perm, b.dgates, stream)
+    N.moe_route_bwd(b.dgates, b.gates, b.topk_idx, b.offsets, b.src_row, b.x_perm, dt, T, d, E, k,
+                    b.dlogits, b.dw_router, stream)
+    N.moe_grouped_mlp_bwd(b.dy_perm, b.x_perm, b.h_save, b.a_save, p.w_gate, p.w_up, p.w_down, dt,
+                          b.offsets, b.R, E, d, f, b.dx_perm, b.dw_gate, b.dw_up, b.dw_down, b.workspace,
+                          stream)
+    N.moe_permute_bwd(b.dx_perm, dt, T, d, E, k, b.dest_row, b.topk_idx, b.dlogits, p.w_router, b.dx,
+                      stream)
+
+
+def step(p: Params, b: Buffers, stream=None):
+    """One forward+backward pass of the layer."""
+    forward(p, b, stream=stream)
+    backward(p, b, stream=stream)

@@ -1,0 +1,72 @@
+"""The C ABI library: it builds, loads, exports every declared symbol, and
+rejects bad arguments synchronously (no GPU needed: nothing is launched)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from mixture_experts_layer_prefix_gb300 import _native as N
+from mixture_experts_layer_prefix_gb300 import build as B
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    B.build()
+    return N.load()
+
+
+def declared_functions():
+    names = []
+    for h in os.listdir(os.path.join(ROOT, "include")):
+        if h.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", h)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names += re.findall(r"^\s*(?:moe_status|size_t|int|uint64_t)\s+(\w+)\s*\(", src, flags=re.M)
+    return names
+
+
+def test_header_declares_the_abi():
+    names = declared_functions()
+    assert set(N.EXPORTS) <= set(names), set(N.EXPORTS) - set(names)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+        assert ctypes.cast(getattr(lib, name), ctypes.c_void_p).value
+
+
+def test_workspace_size_is_host_only(lib):
+    assert N.moe_workspace_size(16384, 2048, 128, 4, 1024, N.MOE_BF16) > 0
+    assert N.moe_workspace_size(-1, 2048, 128, 4, 1024, N.MOE_BF16) == 0
+
+
+FAKE = 0x100000  # never dereferenced: every call below fails validation first
+
+
+def test_invalid_arguments_rejected_before_launch(lib):
+    L = lib
+    # k > E
+    assert L.moe_route(FAKE, FAKE, None, 1, 8, 64, 4, 5, FAKE, 0, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
+                       FAKE, 1 << 20, None) == 1
+    # k > 8 and d not a multiple of 64: unsupported
+    assert L.moe_route(FAKE, FAKE, None, 1, 8, 64, 16, 9, FAKE, 0, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
+                       FAKE, 1 << 20, None) == 2
+    assert L.moe_permute(FAKE, 1, 8, 96, 2, FAKE, FAKE, None) == 2
+    # misaligned pointer
+    assert L.moe_permute(FAKE + 2, 1, 8, 64, 2, FAKE, FAKE, None) == 3
+    # unknown dtype
+    assert L.moe_combine_fwd(FAKE, FAKE, FAKE, 7, 8, 64, 2, FAKE, None) == 2
+    # workspace too small
+    assert L.moe_route(FAKE, FAKE, None, 1, 4096, 64, 16, 2, FAKE, 0, FAKE, FAKE, FAKE, FAKE, FAKE,
+                       FAKE, FAKE, 16, None) == 4
+    # missing buffer
+    assert L.moe_combine_bwd(FAKE, None, FAKE, FAKE, 1, 8, 64, 2, FAKE, FAKE, None) == 1
+    # router term: all three or none
+    assert L.moe_permute_bwd(FAKE, 1, 8, 64, 4, 2, FAKE, FAKE, None, FAKE, FAKE, None) == 1
+    # f not a multiple of 64
+    assert L.moe_grouped_mlp_fwd(FAKE, FAKE, FAKE, FAKE, 1, FAKE, 16, 4, 64, 100, FAKE, FAKE, FAKE,
+                                 FAKE, 0, None) == 2

@@ -56,9 +56,11 @@ moe_status check_dtype(int dtype) {
     if (!aligned16(p)) return MOE_ERR_ALIGNMENT;      \
   } while (0)
 
-// Workspace of the backward GEMM chain: dA [R][f] and dh [R][2f].
+// Workspace of the backward GEMM chain: dh [R][2f], plus dA [R][f] on the
+// fp32 path (the bf16 path fuses the SwiGLU backward into the dA GEMM).
 size_t mlp_bwd_ws(long R, int f, int dtype) {
-  return align256((size_t)R * f * elem_bytes(dtype)) + align256((size_t)R * 2 * f * elem_bytes(dtype));
+  const size_t dh = align256((size_t)R * 2 * f * elem_bytes(dtype));
+  return dtype == MOE_F32 ? align256((size_t)R * f * elem_bytes(dtype)) + dh : dh;
 }
 
 template <typename T>
@@ -181,9 +183,9 @@ moe_status moe_permute_bwd(const void* dx_perm, int dtype, int T, int d, int E, 
                            const void* w_router, void* dx, void* stream) {
   MOE_TRY(check_dims(T, d, E, k));
   MOE_TRY(check_dtype(dtype));
+  if (T == 0) return MOE_OK;
   const int given = (topk_idx != nullptr) + (dlogits != nullptr) + (w_router != nullptr);
   if (given != 0 && given != 3) return MOE_ERR_INVALID_ARG;
-  if (T == 0) return MOE_OK;
   MOE_NEED(dx_perm); MOE_NEED(dest_row); MOE_NEED(dx);
   if (given == 3) { MOE_NEED(topk_idx); MOE_NEED(dlogits); MOE_NEED(w_router); }
   if (dtype == MOE_F32)
@@ -260,8 +262,9 @@ moe_status moe_grouped_mlp_fwd(const void* x_perm, const void* w_gate, const voi
   if (dtype == MOE_F32)
     return mlp_fwd_simt<float>(x_perm, w_gate, w_up, w_down, offsets, R, E, d, f, h_save, a_save, y_perm,
                                S(stream));
-  return mlp_fwd_simt<__nv_bfloat16>(x_perm, w_gate, w_up, w_down, offsets, R, E, d, f, h_save, a_save,
-                                     y_perm, S(stream));
+  MOE_CUDA_TRY(tc_mlp_fwd(x_perm, w_gate, w_up, w_down, offsets, R, E, d, f, h_save, a_save, y_perm,
+                          S(stream)));
+  return MOE_OK;
 }
 
 moe_status moe_grouped_mlp_bwd(const void* dy_perm, const void* x_perm, const void* h_save,
@@ -284,8 +287,9 @@ moe_status moe_grouped_mlp_bwd(const void* dy_perm, const void* x_perm, const vo
   if (dtype == MOE_F32)
     return mlp_bwd_simt<float>(dy_perm, x_perm, h_save, a_save, w_gate, w_up, w_down, offsets, R, E, d,
                                f, dx_perm, dw_gate, dw_up, dw_down, workspace, S(stream));
-  return mlp_bwd_simt<__nv_bfloat16>(dy_perm, x_perm, h_save, a_save, w_gate, w_up, w_down, offsets, R,
-                                     E, d, f, dx_perm, dw_gate, dw_up, dw_down, workspace, S(stream));
+  MOE_CUDA_TRY(tc_mlp_bwd(dy_perm, x_perm, h_save, a_save, w_gate, w_up, w_down, offsets, R, E, d, f,
+                          dx_perm, dw_gate, dw_up, dw_down, workspace, S(stream)));
+  return MOE_OK;
 }
 
 moe_status mxfp8_quantize(const void* src, int rows, int K, int axis, const int32_t* seg_offsets,

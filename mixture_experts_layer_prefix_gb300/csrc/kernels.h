@@ -61,4 +61,12 @@ cudaError_t launch_swiglu_fwd(const void* h, long rows, int f, void* a, cudaStre
 template <typename T>
 cudaError_t launch_swiglu_bwd(const void* da, const void* h, long rows, int f, void* dh, cudaStream_t st);
 
+// ------------------------------------------- tcgen05 grouped GEMMs (bf16)
+cudaError_t tc_mlp_fwd(const void* x_perm, const void* wg, const void* wu, const void* wd,
+                       const int32_t* offsets, int R, int E, int d, int f, void* h, void* a, void* y,
+                       cudaStream_t st);
+cudaError_t tc_mlp_bwd(const void* dy_perm, const void* x_perm, const void* h, const void* a, const void* wg,
+                       const void* wu, const void* wd, const int32_t* offsets, int R, int E, int d, int f,
+                       void* dx_perm, void* dwg, void* dwu, void* dwd, void* dh, cudaStream_t st);
+
 }  // namespace moe

@@ -160,7 +160,7 @@ moe_status moe_route(const void* x, const void* w_router, const float* bias, int
     g.C0 = logits; g.C1 = logits; g.sCm = E; g.sCn = 1; g.cSplit = E;
     g.col_bias = bias; g.offsets = nullptr; g.E = 1; g.M = T; g.N = E; g.K = d;
     if (dtype == MOE_F32) MOE_CUDA_TRY((launch_simt_gemm<float, float, float>(g, st)));
-    else MOE_CUDA_TRY((launch_simt_gemm<__nv_bfloat16, __nv_bfloat16, float>(g, st)));
+    else MOE_CUDA_TRY(tc_router_logits(x, w_router, bias, T, d, E, logits, st));
   }
   MOE_CUDA_TRY(launch_route_meta(logits, T, E, k, topk_idx, gates, counts, offsets, dest_row, src_row,
                                  static_cast<int32_t*>(workspace), st));

@@ -9,8 +9,9 @@
 //   warp 1      TMEM owner and MMA issuer: tcgen05.mma M=128 N=256 K=16 into
 //               one of two 256-column fp32 accumulators (512 TMEM columns),
 //               so the epilogue of tile i overlaps the MMAs of tile i+1.
-//   warps 2..5  epilogue: tcgen05.ld of the accumulator, fused SwiGLU (fwd or
-//               bwd) math, bf16 stores with row/column masks.
+//   warps 2..9  epilogue: tcgen05.ld of the accumulator, fused SwiGLU (fwd or
+//               bwd) math, bf16 (or fp32 router logits) stores with row/column
+//               masks; two warps per TMEM lane quadrant, each half the columns.
 // Tiles are enumerated on the device from the expert offsets (the host never
 // sees the per-expert counts): forward/dgrad tiles cover 128 routed rows of
 // one expert (rows past the expert's end are computed and not stored);
@@ -34,14 +35,16 @@ constexpr int A_BYTES = BM * BK * 2;
 constexpr int B_BYTES = BN * BK * 2;
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int BOX_BYTES = 64 * 64 * 2;  // one 64 (MN) x 64 (K) MN-major box
-constexpr int NUM_THREADS = 192;
+constexpr int NUM_EPI_WARPS = 8;  // two warps per TMEM lane quadrant, each half the columns
+constexpr int NUM_THREADS = 64 + 32 * NUM_EPI_WARPS;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr long long kWaitLimitCycles = 4000000000LL;  // ~2 s at 2 GHz
 
-enum Kind { FPROP1 = 0, FPROP2 = 1, DGRAD2 = 2, DGRAD1 = 3, WGRAD2 = 4, WGRAD1 = 5 };
+enum Kind { FPROP1 = 0, FPROP2 = 1, DGRAD2 = 2, DGRAD1 = 3, WGRAD2 = 4, WGRAD1 = 5, ROUTER = 6 };
 
 struct Params {
-  const int32_t* offsets;
+  const int32_t* offsets;  // nullptr: one dense group of R rows (router GEMM)
+  const float* bias;       // router: per-column bias (or nullptr)
   int E, R, d, f;
   int N;        // output columns of the GEMM
   int M;        // wgrad: output rows
@@ -65,6 +68,8 @@ template <> struct Traits<DGRAD1> { static constexpr bool kragged = false, a_mn 
 template <> struct Traits<WGRAD2> { static constexpr bool kragged = true, a_mn = true, b_mn = true; };
 // [dWg|dWu][e] = x_perm_e^T dh_e (A MN-major [R][d]; B MN-major [R][2f])
 template <> struct Traits<WGRAD1> { static constexpr bool kragged = true, a_mn = true, b_mn = true; };
+// logits = x . W_r^T + bias, fp32 out (A K-major [T][d]; B K-major W_r[E][d])
+template <> struct Traits<ROUTER> { static constexpr bool kragged = false, a_mn = false, b_mn = false; };
 
 struct Smem {
   uint64_t full[STAGES];
@@ -111,7 +116,7 @@ __device__ __forceinline__ Tile decode(int t, const Params& p, const int* offs, 
     tl.n_idx = local % p.n_tiles;
     tl.m0 = offs[e] + tl.m_idx * BM;
     tl.row_end = offs[e + 1];
-    const int K = (KIND == FPROP1 || KIND == DGRAD2) ? p.d : (KIND == FPROP2 ? p.f : 2 * p.f);
+    const int K = (KIND == FPROP1 || KIND == DGRAD2 || KIND == ROUTER) ? p.d : (KIND == FPROP2 ? p.f : 2 * p.f);
     tl.nkb = K / BK;
     tl.k_row0 = 0;
   } else {
@@ -169,7 +174,12 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   // ---- prologue: offsets and the tile table in shared memory
-  for (int i = threadIdx.x; i <= p.E; i += NUM_THREADS) offs[i] = p.offsets[i];
+  if (p.offsets) {
+    for (int i = threadIdx.x; i <= p.E; i += NUM_THREADS) offs[i] = p.offsets[i];
+  } else if (threadIdx.x == 0) {
+    offs[0] = 0;
+    offs[1] = p.R;
+  }
   __syncthreads();
   int total;
   if (!Tr::kragged) {
@@ -197,7 +207,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     }
     for (int b = 0; b < 2; ++b) {
       ptx::mbar_init(&sm->tfull[b], 1);
-      ptx::mbar_init(&sm->tempty[b], 4);
+      ptx::mbar_init(&sm->tempty[b], NUM_EPI_WARPS);
     }
     ptx::mbar_init(&sm->drain, 1);
     sm->abort_flag = 0;
@@ -248,6 +258,9 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           } else if (KIND == DGRAD2) {
             ptx::tma_load_2d(a, &tmA, fb, k0, tl.m0);
             ptx::tma_load_3d(b, &tmB0, fb, k0, tl.n_idx * BN, tl.e);
+          } else if (KIND == ROUTER) {
+            ptx::tma_load_2d(a, &tmA, fb, k0, tl.m0);
+            ptx::tma_load_2d(b, &tmB0, fb, k0, tl.n_idx * BN);
           } else if (KIND == DGRAD1) {
             ptx::tma_load_2d(a, &tmA, fb, k0, tl.m0);
             if (k0 < p.f) ptx::tma_load_3d(b, &tmB0, fb, k0, tl.n_idx * BN, tl.e);
@@ -333,7 +346,11 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     }
   } else {
     // ============================================================ epilogue
-    const int q = warp & 3;  // TMEM lane quadrant this warp may access
+    // Warp w reads TMEM lanes 32*(w%4)..+31 (rows of the tile); the two warps
+    // of a quadrant split the tile's columns in halves.
+    const int ew = warp - 2;
+    const int q = warp & 3;
+    const int half = ew >> 2;
     const int row_in_tile = q * 32 + lane;
     uint32_t acc_it = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
@@ -342,58 +359,54 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         const int m = tl.m0 + row_in_tile;
         const int n0 = tl.n_idx * BN;
         const bool row_ok = m < p.M;
-        if (tl.nkb == 0) {
-          float z[32];
-#pragma unroll
-          for (int i = 0; i < 32; ++i) z[i] = 0.0f;
-          for (int c = 0; c < BN / 32; ++c) {
-            const int n = n0 + c * 32;
-            if (!row_ok || n >= p.N) continue;
-            __nv_bfloat16* dst;
-            if (KIND == WGRAD2) dst = static_cast<__nv_bfloat16*>(p.out0) + ((size_t)tl.e * p.M + m) * p.N + n;
-            else dst = n < p.f ? static_cast<__nv_bfloat16*>(p.out0) + ((size_t)tl.e * p.d + m) * p.f + n
-                               : static_cast<__nv_bfloat16*>(p.out1) + ((size_t)tl.e * p.d + m) * p.f + (n - p.f);
-            store_bf16x32(dst, z);
-          }
-          continue;
+        const bool empty_k = tl.nkb == 0;
+        int buf = 0;
+        if (!empty_k) {
+          buf = acc_it & 1;
+          const uint32_t aph = (acc_it >> 1) & 1u;
+          if (!wait_bar(&sm->tfull[buf], aph, sm, p.err)) break;
+          ptx::tc_fence_after();
         }
-        const int buf = acc_it & 1;
-        const uint32_t aph = (acc_it >> 1) & 1u;
-        if (!wait_bar(&sm->tfull[buf], aph, sm, p.err)) break;
-        ptx::tc_fence_after();
         const uint32_t tbase = tmem + static_cast<uint32_t>(buf * BN) + (static_cast<uint32_t>(q * 32) << 16);
-        for (int c = 0; c < BN / 32; ++c) {
-          uint32_t r[32];
-          ptx::tmem_ld32(tbase + c * 32, r);
-          ptx::tmem_wait_ld();
+        for (int c = half * 4; c < half * 4 + 4; ++c) {
+          float v[32];
+          if (!empty_k) {
+            uint32_t r[32];
+            ptx::tmem_ld32(tbase + c * 32, r);
+            ptx::tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = 0.0f;
+          }
           const int n = n0 + c * 32;
           if (!row_ok || n >= p.N) continue;
-          float v[32];
-#pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
           __nv_bfloat16* dst;
           if (KIND == WGRAD2) dst = static_cast<__nv_bfloat16*>(p.out0) + ((size_t)tl.e * p.M + m) * p.N + n;
           else dst = n < p.f ? static_cast<__nv_bfloat16*>(p.out0) + ((size_t)tl.e * p.d + m) * p.f + n
                              : static_cast<__nv_bfloat16*>(p.out1) + ((size_t)tl.e * p.d + m) * p.f + (n - p.f);
           store_bf16x32(dst, v);
         }
-        ptx::tc_fence_before();
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(&sm->tempty[buf]);
-        ++acc_it;
+        if (!empty_k) {
+          ptx::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(&sm->tempty[buf]);
+          ++acc_it;
+        }
         continue;
       }
       // row-ragged epilogues
       const int buf = acc_it & 1;
       const uint32_t aph = (acc_it >> 1) & 1u;
+      const int row = tl.m0 + row_in_tile;
+      const bool row_ok = row < tl.row_end;
       if (!wait_bar(&sm->tfull[buf], aph, sm, p.err)) break;
       ptx::tc_fence_after();
       const uint32_t tbase = tmem + static_cast<uint32_t>(buf * BN) + (static_cast<uint32_t>(q * 32) << 16);
-      const int row = tl.m0 + row_in_tile;
-      const bool row_ok = row < tl.row_end;
       if (KIND == FPROP1) {
         const int n0 = tl.n_idx * 128;
-        for (int c = 0; c < 4; ++c) {
+        for (int c = half * 2; c < half * 2 + 2; ++c) {
           uint32_t rg[32], ru[32];
           ptx::tmem_ld32(tbase + c * 32, rg);
           ptx::tmem_ld32(tbase + 128 + c * 32, ru);
@@ -412,9 +425,63 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           store_bf16x32(h + p.f + n, hu);
           store_bf16x32(static_cast<__nv_bfloat16*>(p.out1) + (size_t)row * p.f + n, av);
         }
-      } else {
+      } else if (KIND == DGRAD2) {
+        // dh_g = da * h_u * silu'(h_g), dh_u = da * silu(h_g); h is loaded before the
+        // accumulator so the global latency overlaps the TMEM read
         const int n0 = tl.n_idx * BN;
-        for (int c = 0; c < BN / 32; ++c) {
+        const __nv_bfloat16* h = static_cast<const __nv_bfloat16*>(p.aux) + (size_t)row * 2 * p.f;
+        __nv_bfloat16* dh = static_cast<__nv_bfloat16*>(p.out0) + (size_t)row * 2 * p.f;
+        for (int c = half * 4; c < half * 4 + 4; ++c) {
+          const int n = n0 + c * 32;
+          const bool ok = row_ok && n < p.N;
+          float hg[32], hu[32];
+          if (ok) {
+            load_bf16x32(h + n, hg);
+            load_bf16x32(h + p.f + n, hu);
+          }
+          uint32_t r[32];
+          ptx::tmem_ld32(tbase + c * 32, r);
+          ptx::tmem_wait_ld();
+          if (!ok) continue;
+          float dg[32], du[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const float da = __uint_as_float(r[i]);
+            const float s = sigmoid_f(hg[i]);
+            dg[i] = da * hu[i] * s * (1.0f + hg[i] * (1.0f - s));
+            du[i] = da * hg[i] * s;
+          }
+          store_bf16x32(dh + n, dg);
+          store_bf16x32(dh + p.f + n, du);
+        }
+      } else if (KIND == ROUTER) {
+        const int n0 = tl.n_idx * BN;
+        float* out = static_cast<float*>(p.out0) + (size_t)row * p.N;
+        for (int c = half * 4; c < half * 4 + 4; ++c) {
+          uint32_t r[32];
+          ptx::tmem_ld32(tbase + c * 32, r);
+          ptx::tmem_wait_ld();
+          const int n = n0 + c * 32;
+          if (!row_ok || n >= p.N) continue;
+          if (n + 32 <= p.N && (p.N & 3) == 0) {
+#pragma unroll
+            for (int i = 0; i < 32; i += 4) {
+              float4 o;
+              o.x = __uint_as_float(r[i]) + (p.bias ? p.bias[n + i] : 0.0f);
+              o.y = __uint_as_float(r[i + 1]) + (p.bias ? p.bias[n + i + 1] : 0.0f);
+              o.z = __uint_as_float(r[i + 2]) + (p.bias ? p.bias[n + i + 2] : 0.0f);
+              o.w = __uint_as_float(r[i + 3]) + (p.bias ? p.bias[n + i + 3] : 0.0f);
+              *reinterpret_cast<float4*>(out + n + i) = o;
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (n + i < p.N) out[n + i] = __uint_as_float(r[i]) + (p.bias ? p.bias[n + i] : 0.0f);
+          }
+        }
+      } else {  // FPROP2, DGRAD1: plain bf16 store
+        const int n0 = tl.n_idx * BN;
+        for (int c = half * 4; c < half * 4 + 4; ++c) {
           uint32_t r[32];
           ptx::tmem_ld32(tbase + c * 32, r);
           ptx::tmem_wait_ld();
@@ -423,24 +490,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           float v[32];
 #pragma unroll
           for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-          if (KIND == DGRAD2) {
-            // dh_g = da * h_u * silu'(h_g), dh_u = da * silu(h_g)
-            const __nv_bfloat16* h = static_cast<const __nv_bfloat16*>(p.aux) + (size_t)row * 2 * p.f;
-            float hg[32], hu[32], dg[32], du[32];
-            load_bf16x32(h + n, hg);
-            load_bf16x32(h + p.f + n, hu);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              const float s = sigmoid_f(hg[i]);
-              dg[i] = v[i] * hu[i] * s * (1.0f + hg[i] * (1.0f - s));
-              du[i] = v[i] * hg[i] * s;
-            }
-            __nv_bfloat16* dh = static_cast<__nv_bfloat16*>(p.out0) + (size_t)row * 2 * p.f;
-            store_bf16x32(dh + n, dg);
-            store_bf16x32(dh + p.f + n, du);
-          } else {
-            store_bf16x32(static_cast<__nv_bfloat16*>(p.out0) + (size_t)row * p.N + n, v);
-          }
+          store_bf16x32(static_cast<__nv_bfloat16*>(p.out0) + (size_t)row * p.N + n, v);
         }
       }
       ptx::tc_fence_before();
@@ -577,6 +627,16 @@ cudaError_t tc_mlp_bwd(const void* dy_perm, const void* x_perm, const void* h, c
   p.M = d; p.N = 2 * f; p.m_tiles = (d + BM - 1) / BM; p.n_tiles = (2 * f + BN - 1) / BN;
   p.out0 = dwg; p.out1 = dwu;
   return launch<WGRAD1>(mA, mB0, mB0, p, (long)E * p.m_tiles * p.n_tiles, st);
+}
+
+cudaError_t tc_router_logits(const void* x, const void* w_r, const float* bias, int T, int d, int E,
+                             float* logits, cudaStream_t st) {
+  CUtensorMap mA, mB;
+  Params p{};
+  p.offsets = nullptr; p.bias = bias; p.E = 1; p.R = T; p.d = d; p.f = 0; p.err = device_error_word();
+  if (!map_2d(&mA, x, d, T, 64, BM) || !map_2d(&mB, w_r, d, E, 64, BN)) return cudaErrorInvalidValue;
+  p.N = E; p.n_tiles = (E + BN - 1) / BN; p.out0 = logits;
+  return launch<ROUTER>(mA, mB, mB, p, (long)((T + BM - 1) / BM) * p.n_tiles, st);
 }
 
 }  // namespace moe

@@ -69,4 +69,7 @@ cudaError_t tc_mlp_bwd(const void* dy_perm, const void* x_perm, const void* h, c
                        const void* wu, const void* wd, const int32_t* offsets, int R, int E, int d, int f,
                        void* dx_perm, void* dwg, void* dwu, void* dwd, void* dh, cudaStream_t st);
 
+cudaError_t tc_router_logits(const void* x, const void* w_r, const float* bias, int T, int d, int E,
+                             float* logits, cudaStream_t st);
+
 }  // namespace moe

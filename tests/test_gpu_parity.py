@@ -44,6 +44,7 @@ SMALL = [
     _shape("bf16_single_expert", 300, 128, 1, 1, 128),
     _shape("bf16_k_eq_E", 77, 192, 3, 3, 64),
     _shape("bf16_one_token", 1, 64, 4, 2, 64),
+    _shape("bf16_e320_k2", 600, 128, 320, 2, 64),
 ]
 
 

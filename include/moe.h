@@ -168,6 +168,22 @@ moe_status moe_grouped_mlp_bwd(const void* dy_perm, const void* x_perm, const vo
 moe_status mxfp8_quantize(const void* src, int rows, int K, int axis, const int32_t* seg_offsets,
                           int nseg, uint8_t* dst_e4m3, uint8_t* dst_e8m0, void* stream);
 
+/* moe_route for callers that cannot allocate device memory (the pages have no
+   counterpart to this call). It computes exactly what moe_route computes, with
+   the same arguments minus the workspace: its scratch lives in a 4 MiB array
+   compiled into the library, which every GPU that loads the library keeps
+   until the process exits. Shapes with ceil(T/8) * E > 1,048,576 return
+   MOE_ERR_WORKSPACE without launching anything. The first call on a device
+   looks up the array's device address (once per device, with that device
+   current); make that first call before any stream capture. The call
+   allocates nothing. All calls on a device share the one array, so calls
+   that may overlap on the GPU (different streams, or different host threads)
+   race with each other and must be ordered by the caller. */
+moe_status moe_route_noalloc(const void* x, const void* w_router, const float* bias, int dtype, int T,
+                             int d, int E, int k, float* logits, int flags, int32_t* topk_idx,
+                             float* gates, int32_t* counts, int32_t* offsets, int32_t* dest_row,
+                             int32_t* src_row, void* stream);
+
 /* Synchronises `stream`, then returns and clears this device's error word
    (MOE_OK if no kernel reported an error). */
 moe_status moe_get_device_error(void* stream);

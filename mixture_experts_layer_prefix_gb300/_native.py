@@ -24,7 +24,7 @@ STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "M
 # every symbol include/moe.h declares
 EXPORTS = ("moe_workspace_size", "moe_route", "moe_permute", "moe_permute_bwd", "moe_combine_fwd",
            "moe_combine_bwd", "moe_route_bwd", "moe_grouped_mlp_fwd", "moe_grouped_mlp_bwd",
-           "mxfp8_quantize", "moe_get_device_error", "moe_sm_count", "moe_launch_count")
+           "mxfp8_quantize", "moe_get_device_error", "moe_sm_count", "moe_launch_count", "moe_route_noalloc")
 
 
 class MoEError(RuntimeError):
@@ -59,6 +59,7 @@ def load(path: str = LIB_PATH):
         "moe_get_device_error": ([P], I),
         "moe_sm_count": ([], I),
         "moe_launch_count": ([], ctypes.c_uint64),
+        "moe_route_noalloc": ([P, P, P, I, I, I, I, I, P, I, P, P, P, P, P, P, P], I),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -160,3 +161,11 @@ def moe_sm_count():
 
 def moe_launch_count():
     return int(load().moe_launch_count())
+
+
+def moe_route_noalloc(x, w_router, bias, dtype, T, d, E, k, logits, flags, topk_idx, gates, counts, offsets,
+                      dest_row, src_row, stream=None):
+    """moe_route without a workspace argument: for callers that cannot allocate."""
+    _chk("moe_route_noalloc", load().moe_route_noalloc(
+        _p(x), _p(w_router), _p(bias), dtype, T, d, E, k, _p(logits), flags, _p(topk_idx), _p(gates),
+        _p(counts), _p(offsets), _p(dest_row), _p(src_row), _s(stream)))

@@ -1,0 +1,122 @@
+"""Parity at the workloads' full sizes, in the launch configuration bench.py
+times, on outputs the oracle computes one by one.
+
+For each workload the whole layer runs forward+backward on the GPU; then
+  - routing metadata is compared bit-exactly over all T tokens, with the
+    oracle routing on the GPU's own fp32 logits;
+  - router logits of sampled tokens against the oracle's fp64 router GEMM;
+  - y, dx, dgates, dlogits of sampled tokens against the oracle restricted to
+    the experts those tokens use (exact: other experts do not touch them);
+  - weight gradients of sampled experts, from an oracle call that routes
+    exactly that expert's tokens to it with their gates (dW_e depends on
+    nothing else).
+The router weight gradient is a per-expert sum of dlogits-weighted rows; its
+kernel is compared element by element on the small shapes of
+test_gpu_parity.py, and here through the sampled dlogits it reduces.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from mixture_experts_layer_prefix_gb300 import _native as N
+from mixture_experts_layer_prefix_gb300 import build as B
+from mixture_experts_layer_prefix_gb300 import layer as L
+from mixture_experts_layer_prefix_gb300 import synth
+
+from helpers import BF16_TOL, maxnorm_err, np_of
+
+pytestmark = pytest.mark.gpu
+
+WORKLOADS = {  # name -> (token sample size, experts sampled for dW, max rows of a sampled expert)
+    "e8_top4": (64, 1, 4096),
+    "e128_top4": (64, 3, 4096),
+    "e128_top4_skew": (64, 3, 4096),
+    "e128_top4_bf16_twin": (32, 2, 4096),
+    "stress_e256_top8": (8, 2, 700),
+}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    B.build()
+    N.load()
+
+
+def _token_sample_check(inp, b, gl, ref_route, tokens):
+    s = inp.s
+    idx = ref_route["topk_idx"][tokens]
+    used = np.unique(idx)
+    local = np.searchsorted(used, idx).astype(np.int32)
+    x, dy = inp.x()[tokens], inp.dy()[tokens]
+    w = inp.for_experts(used)
+    wr = inp.w_r()[:, used]
+    g = ref_route["gates"][tokens]
+    fw = oracle.forward(x, w["w_gate"], w["w_up"], w["w_down"], local, g)
+    bw = oracle.backward(x, wr, w["w_gate"], w["w_up"], w["w_down"], dy, local, g, fw)
+    dl_full = np.zeros((len(tokens), s.E))
+    dl_full[:, used] = bw["dlogits"]
+    errs = {
+        "y": maxnorm_err(np_of(b.y)[tokens], fw["y"]),
+        "dx": maxnorm_err(np_of(b.dx)[tokens], bw["dx"]),
+        "dgates": maxnorm_err(np_of(b.dgates)[tokens], bw["dgates"]),
+        "dlogits": maxnorm_err(np_of(b.dlogits)[tokens], dl_full),
+    }
+    return errs
+
+
+def _expert_dw_check(inp, b, ref_route, e):
+    s = inp.s
+    idx, g = ref_route["topk_idx"], ref_route["gates"]
+    tok, slot = np.nonzero(idx == e)
+    n = len(tok)
+    w = inp.for_experts([e])
+    zeros = np.zeros((n, 1), np.int32)
+    ge = g[tok, slot][:, None]
+    x, dy = inp.x()[tok], inp.dy()[tok]
+    fw = oracle.forward(x, w["w_gate"], w["w_up"], w["w_down"], zeros, ge)
+    bw = oracle.backward(x, np.zeros((s.d, 1), np.float32), w["w_gate"], w["w_up"], w["w_down"], dy, zeros,
+                         ge, fw)
+    return {
+        f"dw_gate[{e}]": maxnorm_err(np_of(b.dw_gate[e]), bw["dw_gate"][0]),
+        f"dw_up[{e}]": maxnorm_err(np_of(b.dw_up[e]), bw["dw_up"][0]),
+        f"dw_down[{e}]": maxnorm_err(np_of(b.dw_down[e]), bw["dw_down"][0]),
+    }
+
+
+@pytest.mark.parametrize("name", list(WORKLOADS))
+def test_fullsize_sampled_parity(name):
+    s = synth.CONFIGS[name]
+    n_tok, n_exp, max_rows = WORKLOADS[name]
+    inp = synth.Inputs(s, seed=0)
+    p = L.params_from_inputs(inp, N.MOE_BF16)
+    b = L.Buffers(s.T, s.d, s.E, s.k, s.f, N.MOE_BF16)
+    L.forward(p, b)
+    L.backward(p, b)
+    torch.cuda.synchronize()
+    assert N.moe_get_device_error() == 0
+
+    gl = b.logits.cpu().numpy()
+    ref_route = oracle.route(gl.astype(np.float64), s.k, s.E)
+    for key in ("topk_idx", "counts", "offsets", "dest_row", "src_row"):
+        np.testing.assert_array_equal(getattr(b, key).cpu().numpy(), ref_route[key], err_msg=key)
+    np.testing.assert_allclose(b.gates.cpu().numpy(), ref_route["gates"], rtol=0, atol=2e-6)
+    assert int(b.offsets[-1]) == s.T * s.k
+
+    rng = np.random.default_rng(123)
+    tokens = np.sort(rng.choice(s.T, size=n_tok, replace=False))
+    ref_l = oracle.router_logits(inp.x()[tokens], inp.w_r(), inp.bias())
+    assert maxnorm_err(gl[tokens], ref_l) < 1e-5
+
+    errs = _token_sample_check(inp, b, gl, ref_route, tokens)
+    counts = ref_route["counts"]
+    cand = np.flatnonzero((counts > 0) & (counts <= max_rows))
+    picks = [int(cand[np.argmin(counts[cand])]), int(cand[np.argmax(counts[cand])])]
+    picks += [int(e) for e in rng.choice(cand, size=max(0, n_exp - 2), replace=False)]
+    for e in sorted(set(picks))[:max(n_exp, 1)]:
+        errs.update(_expert_dw_check(inp, b, ref_route, e))
+    empty = np.flatnonzero(counts == 0)
+    for e in empty[:2]:
+        assert float(b.dw_gate[int(e)].float().abs().max()) == 0.0
+    bad = {k: v for k, v in errs.items() if not v <= BF16_TOL}
+    assert not bad, f"{name}: {bad} (all: {errs})"

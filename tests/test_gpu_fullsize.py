@@ -35,7 +35,7 @@ WORKLOADS = {  # name -> (token sample size, experts sampled for dW, max rows of
     "e128_top4": (64, 3, 1 << 30),
     "e128_top4_skew": (64, 3, 1 << 30),
     "e128_top4_bf16_twin": (32, 2, 1 << 30),
-    "stress_e256_top8": (8, 2, 4096),
+    "stress_e256_top8": (8, 2, 1024),
 }
 
 

@@ -294,9 +294,17 @@ moe_status moe_grouped_mlp_bwd(const void* dy_perm, const void* x_perm, const vo
 
 moe_status mxfp8_quantize(const void* src, int rows, int K, int axis, const int32_t* seg_offsets,
                           int nseg, uint8_t* dst_e4m3, uint8_t* dst_e8m0, void* stream) {
-  (void)src; (void)rows; (void)K; (void)axis; (void)seg_offsets; (void)nseg; (void)dst_e4m3;
-  (void)dst_e8m0; (void)stream;
-  return MOE_ERR_UNSUPPORTED;
+  if (rows < 0 || K <= 0 || (axis != 0 && axis != 1)) return MOE_ERR_INVALID_ARG;
+  if (axis == 0 && K % 32 != 0) return MOE_ERR_UNSUPPORTED;
+  if (axis == 1 && (K % 2 != 0 || (seg_offsets && (nseg <= 0 || nseg > 4096)))) return MOE_ERR_UNSUPPORTED;
+  if (rows == 0) return MOE_OK;
+  MOE_NEED(src); MOE_NEED(dst_e4m3); MOE_NEED(dst_e8m0);
+  if (seg_offsets) MOE_NEED(seg_offsets);
+  if (axis == 0)
+    MOE_CUDA_TRY(launch_mxfp8_quant_rows(src, rows, K, dst_e4m3, dst_e8m0, S(stream)));
+  else
+    MOE_CUDA_TRY(launch_mxfp8_quant_cols(src, rows, K, seg_offsets, nseg, dst_e4m3, dst_e8m0, S(stream)));
+  return MOE_OK;
 }
 
 moe_status moe_get_device_error(void* stream) {

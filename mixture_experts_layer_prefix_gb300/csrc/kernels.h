@@ -69,6 +69,12 @@ cudaError_t tc_mlp_bwd(const void* dy_perm, const void* x_perm, const void* h, c
                        const void* wu, const void* wd, const int32_t* offsets, int R, int E, int d, int f,
                        void* dx_perm, void* dwg, void* dwu, void* dwd, void* dh, cudaStream_t st);
 
+// ------------------------------------------------------------------ MXFP8
+cudaError_t launch_mxfp8_quant_rows(const void* src, long rows, long K, uint8_t* q, uint8_t* sc,
+                                    cudaStream_t st);
+cudaError_t launch_mxfp8_quant_cols(const void* src, int rows, int C, const int32_t* seg, int nseg,
+                                    uint8_t* q, uint8_t* sc, cudaStream_t st);
+
 cudaError_t tc_router_logits(const void* x, const void* w_r, const float* bias, int T, int d, int E,
                              float* logits, cudaStream_t st);
 

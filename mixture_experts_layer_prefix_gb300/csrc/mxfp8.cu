@@ -1,0 +1,164 @@
+// mxfp8.cu -- MXFP8 block quantisation ("Introducing Olmo-core 3", section
+// "Scaling and optimizing MoE training": MXFP8, a lower-precision format whose
+// savings must exceed the cost of converting between formats).
+//
+// A block is 32 consecutive elements along the GEMM's K. Its E8M0 byte is
+// s + 127 with s = ceil(log2(amax / 448)) clamped to [-127, 127] (the
+// smallest power of two that needs no saturation; an all-zero block gets
+// s = -127); elements are round-to-nearest-even of v * 2^-s, saturated to
+// +-448, through CUDA's fp8 conversion.
+//
+//   rows kernel: blocks along the contiguous axis of [rows][K]; one thread per
+//                block (64 B in, 32 B + 1 B out), coalesced across threads.
+//   cols kernel: blocks of 32 consecutive rows of one column, starting at each
+//                segment's first row (segments = per-expert row ranges from
+//                the device offsets); a segment's last block is zero-padded.
+//                One CTA per (block row, 256 columns); each thread owns two
+//                columns and keeps its 32x2 values in registers.
+#include <cuda_fp8.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+namespace {
+
+// E8M0 exponent from the fp32 bits of amax (amax >= 0, finite).
+__device__ __forceinline__ int e8m0_exponent(float amax) {
+  const uint32_t b = __float_as_uint(amax);
+  const int ef = static_cast<int>((b >> 23) & 0xFFu);
+  if (ef == 0) return -127;                  // zero or subnormal: 2^e <= 2^-127
+  int s = (ef - 127) - 8;                    // amax in [2^e, 2^(e+1)), 448 = 1.75 * 2^8
+  if ((b & 0x7FFFFFu) > 0x600000u) s += 1;   // mantissa above 1.75: 2^(e-8) * 448 < amax
+  return s < -127 ? -127 : (s > 127 ? 127 : s);
+}
+
+// 2^-s as an exact fp32 (s in [-127, 127]; 2^-127 is subnormal).
+__device__ __forceinline__ float pow2_neg(int s) {
+  const int ef = 127 - s;
+  return ef >= 1 ? __uint_as_float(static_cast<uint32_t>(ef) << 23) : __uint_as_float(1u << 22);
+}
+
+__device__ __forceinline__ uint32_t e4m3(float v) {
+  return static_cast<uint32_t>(__nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3));
+}
+
+__global__ void __launch_bounds__(256)
+quant_rows_kernel(const __nv_bfloat16* __restrict__ src, long nblocks, uint8_t* __restrict__ q,
+                  uint8_t* __restrict__ sc) {
+  const long blk = blockIdx.x * (long)blockDim.x + threadIdx.x;
+  if (blk >= nblocks) return;
+  float v[32];
+  const __nv_bfloat16* p = src + blk * 32;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) Vec16<__nv_bfloat16>::load(p + 8 * i, v + 8 * i);
+  float amax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
+  const int s = e8m0_exponent(amax);
+  const float m = pow2_neg(s);
+  uint32_t w[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    w[i] = e4m3(v[4 * i] * m) | (e4m3(v[4 * i + 1] * m) << 8) | (e4m3(v[4 * i + 2] * m) << 16) |
+           (e4m3(v[4 * i + 3] * m) << 24);
+  uint4* out = reinterpret_cast<uint4*>(q + blk * 32);
+  out[0] = make_uint4(w[0], w[1], w[2], w[3]);
+  out[1] = make_uint4(w[4], w[5], w[6], w[7]);
+  sc[blk] = static_cast<uint8_t>(s + 127);
+}
+
+// Block-row table: segment g owns block rows [bstart[g], bstart[g+1]).
+__global__ void __launch_bounds__(128)
+quant_cols_kernel(const __nv_bfloat16* __restrict__ src, int rows, int C, const int32_t* __restrict__ seg,
+                  int nseg, uint8_t* __restrict__ q, uint8_t* __restrict__ sc) {
+  extern __shared__ int bstart[];  // nseg + 1
+  __shared__ int s_r0, s_r1;
+  const int tid = threadIdx.x, lane = tid & 31;
+  if (tid < 32) {
+    int carry = 0;
+    for (int base = 0; base < nseg; base += 32) {
+      const int g = base + lane;
+      int len = 0;
+      if (g < nseg) len = seg ? seg[g + 1] - seg[g] : rows;
+      const int v = (len + 31) / 32;
+      int incl = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int nb = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += nb;
+      }
+      if (g < nseg) bstart[g] = carry + incl - v;
+      carry += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) bstart[nseg] = carry;
+  }
+  __syncthreads();
+  const int brow = blockIdx.x;
+  if (tid == 0) {
+    int r0 = -1, r1 = -1;
+    if (brow < bstart[nseg]) {
+      int lo = 0, hi = nseg;  // bstart[lo] <= brow < bstart[lo + 1]
+      while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (bstart[mid] <= brow) lo = mid; else hi = mid;
+      }
+      const int g0 = seg ? seg[lo] : 0, g1 = seg ? seg[lo + 1] : rows;
+      r0 = g0 + (brow - bstart[lo]) * 32;
+      r1 = min(r0 + 32, g1);
+    }
+    s_r0 = r0;
+    s_r1 = r1;
+  }
+  __syncthreads();
+  const int r0 = s_r0, r1 = s_r1;
+  if (r0 < 0) return;
+  const int c = (blockIdx.y * 128 + tid) * 2;
+  if (c >= C) return;
+  float v0[32], v1[32];
+  float a0 = 0.0f, a1 = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    v0[i] = 0.0f;
+    v1[i] = 0.0f;
+    if (r0 + i < r1) {
+      const __nv_bfloat162 h = *reinterpret_cast<const __nv_bfloat162*>(src + (size_t)(r0 + i) * C + c);
+      v0[i] = __low2float(h);
+      v1[i] = __high2float(h);
+    }
+    a0 = fmaxf(a0, fabsf(v0[i]));
+    a1 = fmaxf(a1, fabsf(v1[i]));
+  }
+  const int s0 = e8m0_exponent(a0), s1 = e8m0_exponent(a1);
+  const float m0 = pow2_neg(s0), m1 = pow2_neg(s1);
+#pragma unroll
+  for (int i = 0; i < 32; ++i)
+    if (r0 + i < r1)
+      *reinterpret_cast<uint16_t*>(q + (size_t)(r0 + i) * C + c) =
+          static_cast<uint16_t>(e4m3(v0[i] * m0) | (e4m3(v1[i] * m1) << 8));
+  *reinterpret_cast<uint16_t*>(sc + (size_t)brow * C + c) = static_cast<uint16_t>((s0 + 127) | ((s1 + 127) << 8));
+}
+
+}  // namespace
+
+cudaError_t launch_mxfp8_quant_rows(const void* src, long rows, long K, uint8_t* q, uint8_t* sc,
+                                    cudaStream_t st) {
+  const long nblocks = rows * (K / 32);
+  if (nblocks == 0) return cudaSuccess;
+  MOE_COUNTED quant_rows_kernel<<<static_cast<unsigned>((nblocks + 255) / 256), 256, 0, st>>>(
+      static_cast<const __nv_bfloat16*>(src), nblocks, q, sc);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_mxfp8_quant_cols(const void* src, int rows, int C, const int32_t* seg, int nseg,
+                                    uint8_t* q, uint8_t* sc, cudaStream_t st) {
+  const int nseg_eff = seg ? nseg : 1;
+  const long max_brows = (rows + 31) / 32 + nseg_eff;
+  if (rows == 0) return cudaSuccess;
+  dim3 grid(static_cast<unsigned>(max_brows), static_cast<unsigned>((C / 2 + 127) / 128));
+  MOE_COUNTED quant_cols_kernel<<<grid, 128, (nseg_eff + 1) * sizeof(int), st>>>(
+      static_cast<const __nv_bfloat16*>(src), rows, C, seg, nseg_eff, q, sc);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -28,7 +28,7 @@ def _values(rows, K, seed):
     if rows > 3 and K >= 64:
         v[3, 32:64] = 0.0
         v[2, :32] = 448.0
-        v[1, :32] = -449.0
+        v[1, :32] = -450.0  # bf16-exact, just above 448
     return v
 
 

@@ -41,8 +41,12 @@ moe_status check_dims(int T, int d, int E, int k) {
 }
 
 moe_status check_dtype(int dtype) {
-  return (dtype == MOE_F32 || dtype == MOE_BF16) ? MOE_OK : MOE_ERR_UNSUPPORTED;
+  return (dtype == MOE_F32 || dtype == MOE_BF16 || dtype == MOE_MXFP8) ? MOE_OK : MOE_ERR_UNSUPPORTED;
 }
+
+// Activations and weights are bf16 in memory on the MXFP8 path too; only the
+// expert GEMMs quantise their operands.
+inline int storage(int dtype) { return dtype == MOE_MXFP8 ? MOE_BF16 : dtype; }
 
 #define MOE_TRY(expr)                    \
   do {                                   \
@@ -135,7 +139,13 @@ size_t moe_workspace_size(int T, int d, int E, int k, int f, int dtype) {
   const long R = (long)T * k;
   size_t route = align256(route_workspace_bytes(T, E));
   size_t bwd = mlp_bwd_ws(R, f, dtype == MOE_F32 ? MOE_F32 : MOE_BF16);
-  return route > bwd ? route : bwd;
+  size_t ws = route > bwd ? route : bwd;
+  if (dtype == MOE_MXFP8) {
+    const size_t mf = mx_fwd_workspace(R, E, d, f), mb = mx_bwd_workspace(R, E, d, f);
+    ws = ws > mf ? ws : mf;
+    ws = ws > mb ? ws : mb;
+  }
+  return ws;
 }
 
 moe_status moe_route(const void* x, const void* w_router, const float* bias, int dtype, int T, int d,
@@ -144,6 +154,7 @@ moe_status moe_route(const void* x, const void* w_router, const float* bias, int
                      void* workspace, size_t workspace_bytes, void* stream) {
   MOE_TRY(check_dims(T, d, E, k));
   MOE_TRY(check_dtype(dtype));
+  dtype = storage(dtype);
   MOE_NEED(counts); MOE_NEED(offsets);
   if (T > 0) {
     MOE_NEED(logits); MOE_NEED(topk_idx); MOE_NEED(gates); MOE_NEED(dest_row); MOE_NEED(src_row);
@@ -171,6 +182,7 @@ moe_status moe_permute(const void* x, int dtype, int T, int d, int k, const int3
                        void* x_perm, void* stream) {
   MOE_TRY(check_dims(T, d, k, k));
   MOE_TRY(check_dtype(dtype));
+  dtype = storage(dtype);
   if (T == 0) return MOE_OK;
   MOE_NEED(x); MOE_NEED(dest_row); MOE_NEED(x_perm);
   if (dtype == MOE_F32) MOE_CUDA_TRY(launch_permute<float>(x, T, d, k, dest_row, x_perm, S(stream)));
@@ -183,6 +195,7 @@ moe_status moe_permute_bwd(const void* dx_perm, int dtype, int T, int d, int E, 
                            const void* w_router, void* dx, void* stream) {
   MOE_TRY(check_dims(T, d, E, k));
   MOE_TRY(check_dtype(dtype));
+  dtype = storage(dtype);
   if (T == 0) return MOE_OK;
   const int given = (topk_idx != nullptr) + (dlogits != nullptr) + (w_router != nullptr);
   if (given != 0 && given != 3) return MOE_ERR_INVALID_ARG;
@@ -201,6 +214,7 @@ moe_status moe_combine_fwd(const void* y_perm, const float* gates, const int32_t
                            int T, int d, int k, void* y, void* stream) {
   MOE_TRY(check_dims(T, d, k, k));
   MOE_TRY(check_dtype(dtype));
+  dtype = storage(dtype);
   if (T == 0) return MOE_OK;
   MOE_NEED(y_perm); MOE_NEED(gates); MOE_NEED(dest_row); MOE_NEED(y);
   if (dtype == MOE_F32)
@@ -215,6 +229,7 @@ moe_status moe_combine_bwd(const void* dy, const void* y_perm, const float* gate
                            float* dgates, void* stream) {
   MOE_TRY(check_dims(T, d, k, k));
   MOE_TRY(check_dtype(dtype));
+  dtype = storage(dtype);
   if (T == 0) return MOE_OK;
   MOE_NEED(dy); MOE_NEED(y_perm); MOE_NEED(gates); MOE_NEED(dest_row); MOE_NEED(dy_perm);
   MOE_NEED(dgates);
@@ -233,6 +248,7 @@ moe_status moe_route_bwd(const float* dgates, const float* gates, const int32_t*
                          void* stream) {
   MOE_TRY(check_dims(T, d, E, k));
   MOE_TRY(check_dtype(dtype));
+  dtype = storage(dtype);
   MOE_NEED(offsets); MOE_NEED(dw_router);
   if (T > 0) {
     MOE_NEED(dgates); MOE_NEED(gates); MOE_NEED(topk_idx); MOE_NEED(src_row); MOE_NEED(x_perm);
@@ -258,7 +274,14 @@ moe_status moe_grouped_mlp_fwd(const void* x_perm, const void* w_gate, const voi
   MOE_NEED(w_gate); MOE_NEED(w_up); MOE_NEED(w_down); MOE_NEED(offsets);
   if (R == 0) return MOE_OK;
   MOE_NEED(x_perm); MOE_NEED(h_save); MOE_NEED(a_save); MOE_NEED(y_perm);
-  (void)workspace; (void)workspace_bytes;
+  if (dtype == MOE_MXFP8) {
+    if (d % 128 != 0 || f % 128 != 0) return MOE_ERR_UNSUPPORTED;
+    if (workspace_bytes < mx_fwd_workspace(R, E, d, f)) return MOE_ERR_WORKSPACE;
+    MOE_NEED(workspace);
+    MOE_CUDA_TRY(mx_mlp_fwd(x_perm, w_gate, w_up, w_down, offsets, R, E, d, f, h_save, a_save, y_perm,
+                            workspace, S(stream)));
+    return MOE_OK;
+  }
   if (dtype == MOE_F32)
     return mlp_fwd_simt<float>(x_perm, w_gate, w_up, w_down, offsets, R, E, d, f, h_save, a_save, y_perm,
                                S(stream));
@@ -279,6 +302,17 @@ moe_status moe_grouped_mlp_bwd(const void* dy_perm, const void* x_perm, const vo
   if (f % 64 != 0) return MOE_ERR_UNSUPPORTED;
   MOE_NEED(w_gate); MOE_NEED(w_up); MOE_NEED(w_down); MOE_NEED(offsets);
   MOE_NEED(dw_gate); MOE_NEED(dw_up); MOE_NEED(dw_down);
+  if (dtype == MOE_MXFP8) {
+    if (d % 128 != 0 || f % 128 != 0) return MOE_ERR_UNSUPPORTED;
+    if (workspace_bytes < mx_bwd_workspace(R, E, d, f)) return MOE_ERR_WORKSPACE;
+    if (R > 0) {
+      MOE_NEED(dy_perm); MOE_NEED(x_perm); MOE_NEED(h_save); MOE_NEED(a_save); MOE_NEED(dx_perm);
+    }
+    MOE_NEED(workspace);
+    MOE_CUDA_TRY(mx_mlp_bwd(dy_perm, x_perm, h_save, a_save, w_gate, w_up, w_down, offsets, R, E, d, f,
+                            dx_perm, dw_gate, dw_up, dw_down, workspace, S(stream)));
+    return MOE_OK;
+  }
   if (workspace_bytes < mlp_bwd_ws(R, f, dtype)) return MOE_ERR_WORKSPACE;
   if (R > 0) {
     MOE_NEED(dy_perm); MOE_NEED(x_perm); MOE_NEED(h_save); MOE_NEED(a_save); MOE_NEED(dx_perm);

@@ -78,4 +78,13 @@ cudaError_t launch_mxfp8_quant_cols(const void* src, int rows, int C, const int3
 cudaError_t tc_router_logits(const void* x, const void* w_r, const float* bias, int T, int d, int E,
                              float* logits, cudaStream_t st);
 
+// ------------------------------------------- MXFP8 grouped GEMMs (bf16 in/out)
+size_t mx_fwd_workspace(long R, int E, int d, int f);
+size_t mx_bwd_workspace(long R, int E, int d, int f);
+cudaError_t mx_mlp_fwd(const void* x_perm, const void* wg, const void* wu, const void* wd, const int32_t* offsets,
+                       int R, int E, int d, int f, void* h, void* a, void* y, void* ws, cudaStream_t st);
+cudaError_t mx_mlp_bwd(const void* dy_perm, const void* x_perm, const void* h, const void* a, const void* wg,
+                       const void* wu, const void* wd, const int32_t* offsets, int R, int E, int d, int f,
+                       void* dx_perm, void* dwg, void* dwu, void* dwd, void* ws, cudaStream_t st);
+
 }  // namespace moe

@@ -1,0 +1,313 @@
+// tc_common.cuh -- pieces shared by the bf16 and the MXFP8 grouped GEMMs:
+// the GEMM kinds, kernel parameters, the device-side ragged tile decoder, the
+// bounded mbarrier wait and the fused epilogues (TMEM accumulator -> bf16 or
+// fp32 outputs, with the SwiGLU forward/backward math).
+#pragma once
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+#include "tc_ptx.cuh"
+
+namespace moe {
+namespace tc {
+
+constexpr int BM = 128, BN = 256, STAGES = 4;
+constexpr long long kWaitLimitCycles = 4000000000LL;  // ~2 s at 2 GHz
+
+// The six grouped expert GEMMs of the SwiGLU layer and the router GEMM.
+enum Kind { FPROP1 = 0, FPROP2 = 1, DGRAD2 = 2, DGRAD1 = 3, WGRAD2 = 4, WGRAD1 = 5, ROUTER = 6 };
+
+struct Params {
+  const int32_t* offsets;  // [E+1] device offsets; nullptr: one dense group of R rows
+  const float* bias;       // router: per-column bias (or nullptr)
+  int E, R, d, f;
+  int N;                   // output columns of the GEMM
+  int M;                   // wgrad: output rows
+  int n_tiles, m_tiles;
+  void* out0;
+  void* out1;
+  const void* aux;         // DGRAD2: h_save
+  const uint8_t* sfa;      // MXFP8: scale bytes of A (layout per kind)
+  const uint8_t* sfb0;     // MXFP8: scale bytes of B (gate / the only B)
+  const uint8_t* sfb1;     // MXFP8: scale bytes of the second B (up)
+  int* err;
+};
+
+template <int KIND> struct Traits;
+// H = x_perm . [Wg | Wu]   (A K-major [R][d]; B MN-major Wg/Wu[e][d][f])
+template <> struct Traits<FPROP1> { static constexpr bool kragged = false, a_mn = false, b_mn = true; };
+// y_perm = A . Wd          (A K-major [R][f]; B MN-major Wd[e][f][d])
+template <> struct Traits<FPROP2> { static constexpr bool kragged = false, a_mn = false, b_mn = true; };
+// dA = dy_perm . Wd^T      (A K-major [R][d]; B K-major Wd[e][f][d])
+template <> struct Traits<DGRAD2> { static constexpr bool kragged = false, a_mn = false, b_mn = false; };
+// dx_perm = dh . [Wg|Wu]^T (A K-major [R][2f]; B K-major Wg/Wu[e][d][f])
+template <> struct Traits<DGRAD1> { static constexpr bool kragged = false, a_mn = false, b_mn = false; };
+// dWd[e] = A_e^T dy_perm_e (A MN-major [R][f]; B MN-major [R][d])
+template <> struct Traits<WGRAD2> { static constexpr bool kragged = true, a_mn = true, b_mn = true; };
+// [dWg|dWu][e] = x_perm_e^T dh_e (A MN-major [R][d]; B MN-major [R][2f])
+template <> struct Traits<WGRAD1> { static constexpr bool kragged = true, a_mn = true, b_mn = true; };
+// logits = x . W_r^T + bias, fp32 out (A K-major [T][d]; B K-major W_r[E][d])
+template <> struct Traits<ROUTER> { static constexpr bool kragged = false, a_mn = false, b_mn = false; };
+
+// Bounded wait on an mbarrier phase. On expiry: set the device error word and
+// the CTA's abort flag (so the other roles stop too) and return false.
+__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, int* abort_flag, int* err) {
+  if (ptx::mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (true) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    if (*reinterpret_cast<volatile int*>(abort_flag)) return false;
+    if (clock64() - t0 > kWaitLimitCycles) {
+      set_error(err, MOE_ERR_TIMEOUT);
+      *reinterpret_cast<volatile int*>(abort_flag) = 1;
+      return false;
+    }
+  }
+}
+
+struct Tile {
+  int e, m0, row_end, n_idx, m_idx, nkb, k_row0;
+};
+
+template <int KIND>
+__device__ __forceinline__ int gemm_k(const Params& p) {
+  return (KIND == FPROP1 || KIND == DGRAD2 || KIND == ROUTER) ? p.d : (KIND == FPROP2 ? p.f : 2 * p.f);
+}
+
+// Decode linear tile t. Row-ragged: expert e owns tstart[e]..tstart[e+1]
+// (m-tiles x n-tiles, n fastest). K-ragged: every expert owns m_tiles x
+// n_tiles tiles and its K loop runs over its rows, BK rows per stage.
+template <int KIND, int BK>
+__device__ __forceinline__ Tile decode(int t, const Params& p, const int* offs, const int* tstart) {
+  Tile tl;
+  if (!Traits<KIND>::kragged) {
+    int lo = 0, hi = p.E;  // find e with tstart[e] <= t < tstart[e+1]
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (tstart[mid] <= t) lo = mid; else hi = mid;
+    }
+    const int e = lo, local = t - tstart[e];
+    tl.e = e;
+    tl.m_idx = local / p.n_tiles;
+    tl.n_idx = local % p.n_tiles;
+    tl.m0 = offs[e] + tl.m_idx * BM;
+    tl.row_end = offs[e + 1];
+    tl.nkb = gemm_k<KIND>(p) / BK;
+    tl.k_row0 = 0;
+  } else {
+    const int per = p.m_tiles * p.n_tiles;
+    tl.e = t / per;
+    const int local = t % per;
+    tl.m_idx = local / p.n_tiles;
+    tl.n_idx = local % p.n_tiles;
+    tl.m0 = tl.m_idx * BM;
+    tl.row_end = offs[tl.e + 1];
+    tl.k_row0 = offs[tl.e];
+    tl.nkb = (tl.row_end - tl.k_row0 + BK - 1) / BK;
+  }
+  return tl;
+}
+
+// Offsets into shared memory and (row-ragged kinds) the per-expert tile
+// prefix table; called by all threads of the CTA, ends with __syncthreads.
+template <int KIND, int NTHREADS>
+__device__ __forceinline__ void build_tile_table(const Params& p, int* offs, int* tstart) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (p.offsets) {
+    for (int i = threadIdx.x; i <= p.E; i += NTHREADS) offs[i] = p.offsets[i];
+  } else if (threadIdx.x == 0) {
+    offs[0] = 0;
+    offs[1] = p.R;
+  }
+  __syncthreads();
+  if (!Traits<KIND>::kragged && warp == 0) {
+    int carry = 0;
+    for (int base = 0; base < p.E; base += 32) {
+      const int e = base + lane;
+      const int cnt = e < p.E ? offs[e + 1] - offs[e] : 0;
+      const int v = ((cnt + BM - 1) / BM) * p.n_tiles;
+      int incl = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int nb = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += nb;
+      }
+      if (e < p.E) tstart[e] = carry + incl - v;
+      carry += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) tstart[p.E] = carry;
+  }
+  __syncthreads();
+}
+
+__device__ __forceinline__ void store_bf16x32(__nv_bfloat16* dst, const float* v) {
+  uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    uint32_t w[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      __nv_bfloat162 h = __floats2bfloat162_rn(v[8 * i + 2 * j], v[8 * i + 2 * j + 1]);
+      w[j] = *reinterpret_cast<uint32_t*>(&h);
+    }
+    d[i] = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+
+__device__ __forceinline__ void load_bf16x32(const __nv_bfloat16* src, float* v) {
+  const uint4* s = reinterpret_cast<const uint4*>(src);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint4 q = s[i];
+    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      v[8 * i + 2 * j] = __uint_as_float(w[j] << 16);
+      v[8 * i + 2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+    }
+  }
+}
+
+// Epilogue of one tile for the rows of one TMEM lane quadrant: accumulator
+// chunks [c_beg, c_end) of 32 columns (FPROP1: gate chunk c with up chunk
+// c + 4). `zero` writes zeros without reading TMEM (wgrad of an empty expert).
+template <int KIND>
+__device__ __forceinline__ void epilogue_tile(const Params& p, const Tile& tl, uint32_t tbase, int row_in_tile,
+                                              int c_beg, int c_end, bool zero) {
+  if (Traits<KIND>::kragged) {
+    const int m = tl.m0 + row_in_tile;
+    const int n0 = tl.n_idx * BN;
+    const bool row_ok = m < p.M;
+    for (int c = c_beg; c < c_end; ++c) {
+      float v[32];
+      if (!zero) {
+        uint32_t r[32];
+        ptx::tmem_ld32(tbase + c * 32, r);
+        ptx::tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = 0.0f;
+      }
+      const int n = n0 + c * 32;
+      if (!row_ok || n >= p.N) continue;
+      __nv_bfloat16* dst;
+      if (KIND == WGRAD2) dst = static_cast<__nv_bfloat16*>(p.out0) + ((size_t)tl.e * p.M + m) * p.N + n;
+      else dst = n < p.f ? static_cast<__nv_bfloat16*>(p.out0) + ((size_t)tl.e * p.d + m) * p.f + n
+                         : static_cast<__nv_bfloat16*>(p.out1) + ((size_t)tl.e * p.d + m) * p.f + (n - p.f);
+      store_bf16x32(dst, v);
+    }
+    return;
+  }
+  const int row = tl.m0 + row_in_tile;
+  const bool row_ok = row < tl.row_end;
+  if (KIND == FPROP1) {
+    const int n0 = tl.n_idx * 128;
+    for (int c = c_beg; c < c_end; ++c) {
+      uint32_t rg[32], ru[32];
+      ptx::tmem_ld32(tbase + c * 32, rg);
+      ptx::tmem_ld32(tbase + 128 + c * 32, ru);
+      ptx::tmem_wait_ld();
+      const int n = n0 + c * 32;
+      if (!row_ok || n >= p.f) continue;
+      float hg[32], hu[32], av[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        hg[i] = __uint_as_float(rg[i]);
+        hu[i] = __uint_as_float(ru[i]);
+        av[i] = silu_f(hg[i]) * hu[i];
+      }
+      __nv_bfloat16* h = static_cast<__nv_bfloat16*>(p.out0) + (size_t)row * 2 * p.f;
+      store_bf16x32(h + n, hg);
+      store_bf16x32(h + p.f + n, hu);
+      store_bf16x32(static_cast<__nv_bfloat16*>(p.out1) + (size_t)row * p.f + n, av);
+    }
+  } else if (KIND == DGRAD2) {
+    // dh_g = da * h_u * silu'(h_g), dh_u = da * silu(h_g); h is loaded before
+    // the accumulator so the global latency overlaps the TMEM read
+    const int n0 = tl.n_idx * BN;
+    const __nv_bfloat16* h = static_cast<const __nv_bfloat16*>(p.aux) + (size_t)row * 2 * p.f;
+    __nv_bfloat16* dh = static_cast<__nv_bfloat16*>(p.out0) + (size_t)row * 2 * p.f;
+    for (int c = c_beg; c < c_end; ++c) {
+      const int n = n0 + c * 32;
+      const bool ok = row_ok && n < p.N;
+      float hg[32], hu[32];
+      if (ok) {
+        load_bf16x32(h + n, hg);
+        load_bf16x32(h + p.f + n, hu);
+      }
+      uint32_t r[32];
+      ptx::tmem_ld32(tbase + c * 32, r);
+      ptx::tmem_wait_ld();
+      if (!ok) continue;
+      float dg[32], du[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const float da = __uint_as_float(r[i]);
+        const float s = sigmoid_f(hg[i]);
+        dg[i] = da * hu[i] * s * (1.0f + hg[i] * (1.0f - s));
+        du[i] = da * hg[i] * s;
+      }
+      store_bf16x32(dh + n, dg);
+      store_bf16x32(dh + p.f + n, du);
+    }
+  } else if (KIND == ROUTER) {
+    const int n0 = tl.n_idx * BN;
+    float* out = static_cast<float*>(p.out0) + (size_t)row * p.N;
+    for (int c = c_beg; c < c_end; ++c) {
+      uint32_t r[32];
+      ptx::tmem_ld32(tbase + c * 32, r);
+      ptx::tmem_wait_ld();
+      const int n = n0 + c * 32;
+      if (!row_ok || n >= p.N) continue;
+      if (n + 32 <= p.N && (p.N & 3) == 0) {
+#pragma unroll
+        for (int i = 0; i < 32; i += 4) {
+          float4 o;
+          o.x = __uint_as_float(r[i]) + (p.bias ? p.bias[n + i] : 0.0f);
+          o.y = __uint_as_float(r[i + 1]) + (p.bias ? p.bias[n + i + 1] : 0.0f);
+          o.z = __uint_as_float(r[i + 2]) + (p.bias ? p.bias[n + i + 2] : 0.0f);
+          o.w = __uint_as_float(r[i + 3]) + (p.bias ? p.bias[n + i + 3] : 0.0f);
+          *reinterpret_cast<float4*>(out + n + i) = o;
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          if (n + i < p.N) out[n + i] = __uint_as_float(r[i]) + (p.bias ? p.bias[n + i] : 0.0f);
+      }
+    }
+  } else {  // FPROP2, DGRAD1: plain bf16 store
+    const int n0 = tl.n_idx * BN;
+    for (int c = c_beg; c < c_end; ++c) {
+      uint32_t r[32];
+      ptx::tmem_ld32(tbase + c * 32, r);
+      ptx::tmem_wait_ld();
+      const int n = n0 + c * 32;
+      if (!row_ok || n >= p.N) continue;
+      float v[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+      store_bf16x32(static_cast<__nv_bfloat16*>(p.out0) + (size_t)row * p.N + n, v);
+    }
+  }
+}
+
+// Number of 32-column accumulator chunks an epilogue covers (FPROP1 pairs).
+template <int KIND>
+__host__ __device__ constexpr int epi_chunks() { return KIND == FPROP1 ? 4 : BN / 32; }
+
+// ------------------------------------------------------------------ host
+PFN_cuTensorMapEncodeTiled_v12000 encoder();
+// [rows][inner] row-major, box (box_inner, box_rows), 128-byte swizzle
+bool map_2d(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esize, uint64_t inner,
+            uint64_t rows, uint32_t box_inner, uint32_t box_rows);
+// [E][rows][inner], box (box_inner, box_rows, 1)
+bool map_3d(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esize, uint64_t inner,
+            uint64_t rows, uint64_t E, uint32_t box_inner, uint32_t box_rows);
+int sm_count();
+
+}  // namespace tc
+}  // namespace moe

@@ -127,6 +127,52 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, int a_mn_maj
          | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16
 }
 
+// D[tmem] (+)= (A * scale_A)[smem] x (B * scale_B)[smem], kind::mxf8f6f4 with
+// one E8M0 scale per 32 elements along K (scale_vec::1X). Scales are read from
+// TMEM: for A row m at (lane m, column sfa + m/32), for B column n at
+// (lane (n%32) + 32*q, column sfb + n/32) in the lane quadrant q that computes
+// the output row; the byte inside the 32-bit cell is the instruction
+// descriptor's scale-factor id.
+__device__ __forceinline__ void mma_mxf8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                         uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+          d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
+// Instruction descriptor of kind::mxf8f6f4: E4M3 A and B, fp32 D, UE8M0 scales
+// (bit 23), scale-factor ids for B (bits 4-5) and A (bits 29-30).
+__host__ __device__ constexpr uint32_t idesc_mxf8_f32(int M, int N, int a_mn_major, int b_mn_major, int a_sf,
+                                                      int b_sf) {
+  return (static_cast<uint32_t>(b_sf) << 4)            // B scale-factor id
+         | (0u << 7) | (0u << 10)                      // A, B format: E4M3
+         | (static_cast<uint32_t>(a_mn_major) << 15)  // A major-ness
+         | (static_cast<uint32_t>(b_mn_major) << 16)  // B major-ness
+         | (static_cast<uint32_t>(N >> 3) << 17)      // N / 8
+         | (1u << 23)                                  // scale format: UE8M0
+         | (static_cast<uint32_t>(M >> 4) << 24)      // M / 16
+         | (static_cast<uint32_t>(a_sf) << 29);        // A scale-factor id
+}
+
+// Write 4 / 8 consecutive 32-bit TMEM columns of this warp's 32 lanes.
+__device__ __forceinline__ void tmem_st4(uint32_t taddr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr), "r"(a), "r"(b),
+               "r"(c), "r"(d)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
+               "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+               : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
 // 32 lanes x 32 consecutive 32-bit TMEM columns: thread i gets row (lane base + i).
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile(

@@ -65,6 +65,8 @@ def _L():
             lib.oc_e8m0_exponent.restype = ctypes.c_int
             lib.oc_mxfp8_quantize_rows.argtypes = [P, ctypes.c_long, ctypes.c_long, P, P]
             lib.oc_mxfp8_quantize_cols_segmented.argtypes = [P, ctypes.c_long, ctypes.c_long, P, I, P, P]
+            lib.oc_mxfp8_quantize_rows_f64.argtypes = [P, ctypes.c_long, ctypes.c_long, P, P]
+            lib.oc_mxfp8_quantize_cols_segmented_f64.argtypes = [P, ctypes.c_long, ctypes.c_long, P, I, P, P]
             _lib = lib
     return _lib
 
@@ -267,3 +269,26 @@ def mxfp8_dequantize_cols_segmented(q, s, seg):
             vals[b0:b1] *= np.ldexp(1.0, s[brow].astype(np.int32) - 127)[None, :]
             brow += 1
     return vals
+
+
+def mxfp8_fakequant_rows(v):
+    """dequantise(quantise(v)) with 32-element blocks along the last axis (fp64 in, fp64 out)."""
+    v = _f64(v)
+    rows, K = v.shape
+    q = np.empty((rows, K), np.uint8)
+    s = np.empty((rows, K // 32), np.uint8)
+    _L().oc_mxfp8_quantize_rows_f64(_p(v), rows, K, _p(q), _p(s))
+    return mxfp8_dequantize_rows(q, s)
+
+
+def mxfp8_fakequant_cols_segmented(v, seg):
+    """dequantise(quantise(v)) with blocks of 32 rows starting at each segment's
+    first row (fp64 in, fp64 out)."""
+    v = _f64(v)
+    seg = _i32(seg)
+    rows, C = v.shape
+    nblk = int(sum((int(seg[g + 1]) - int(seg[g]) + 31) // 32 for g in range(len(seg) - 1)))
+    q = np.empty((rows, C), np.uint8)
+    s = np.empty((max(nblk, 0), C), np.uint8)
+    _L().oc_mxfp8_quantize_cols_segmented_f64(_p(v), rows, C, _p(seg), len(seg) - 1, _p(q), _p(s))
+    return mxfp8_dequantize_cols_segmented(q, s, seg)

@@ -430,3 +430,35 @@ void oc_mxfp8_quantize_cols_segmented(const float* v, long rows, long C, const i
     }
   }
 }
+
+/* The two quantisers above on double input (intermediates of the MXFP8
+   layer that the oracle keeps in double). Same block rule and rounding. */
+void oc_mxfp8_quantize_rows_f64(const double* v, long rows, long K, uint8_t* q, uint8_t* sc) {
+  for (long r = 0; r < rows; ++r)
+    for (long b = 0; b < K / 32; ++b) {
+      const double* blk = v + r * K + b * 32;
+      double amax = 0.0;
+      for (int i = 0; i < 32; ++i) if (fabs(blk[i]) > amax) amax = fabs(blk[i]);
+      int s = oc_e8m0_exponent(amax);
+      sc[r * (K / 32) + b] = (uint8_t)(s + 127);
+      for (int i = 0; i < 32; ++i) q[r * K + b * 32 + i] = oc_e4m3_encode(ldexp(blk[i], -s));
+    }
+}
+
+void oc_mxfp8_quantize_cols_segmented_f64(const double* v, long rows, long C, const int32_t* seg, int nseg,
+                                          uint8_t* q, uint8_t* sc) {
+  long brow = 0;
+  for (int g = 0; g < nseg; ++g) {
+    long r0 = seg[g], r1 = seg[g + 1];
+    for (long b0 = r0; b0 < r1; b0 += 32, ++brow) {
+      long b1 = b0 + 32 < r1 ? b0 + 32 : r1;
+      for (long c = 0; c < C; ++c) {
+        double amax = 0.0;
+        for (long r = b0; r < b1; ++r) if (fabs(v[r * C + c]) > amax) amax = fabs(v[r * C + c]);
+        int s = oc_e8m0_exponent(amax);
+        sc[brow * C + c] = (uint8_t)(s + 127);
+        for (long r = b0; r < b1; ++r) q[r * C + c] = oc_e4m3_encode(ldexp(v[r * C + c], -s));
+      }
+    }
+  }
+}

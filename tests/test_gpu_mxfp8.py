@@ -64,3 +64,59 @@ def test_quantize_segmented_columns_bit_exact(seg):
     rq, rs = oracle.mxfp8_quantize_cols_segmented(v, segs)
     np.testing.assert_array_equal(s.cpu().numpy()[:rs.shape[0]], rs)
     np.testing.assert_array_equal(q.cpu().numpy(), rq)
+
+
+# ------------------------------------------------- MXFP8 expert GEMMs, whole layer
+from mixture_experts_layer_prefix_gb300 import layer as L  # noqa: E402
+from oracle import mxfp8_layer  # noqa: E402
+
+MX_TOL = 6e-2  # stated bound against the oracle on the same dequantised operands
+
+MX_SHAPES = [
+    synth.MoEShape("mx_e8_k2", 512, 256, 8, 2, 256, "mxfp8", 0.02),
+    synth.MoEShape("mx_e16_k4_skew", 700, 384, 16, 4, 256, "mxfp8", 0.02, zipf_s=1.2, zipf_alpha=0.5, n_dead=2),
+    synth.MoEShape("mx_e4_k1_f384", 300, 128, 4, 1, 384, "mxfp8", 0.02),
+]
+
+
+def _err(got, ref):
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    return float(np.abs(got - ref).max() / max(np.abs(ref).max(), 1e-30))
+
+
+@pytest.mark.parametrize("s", MX_SHAPES, ids=lambda s: s.name)
+def test_mxfp8_layer_parity(s):
+    inp = synth.Inputs(s, seed=2)
+    p = L.params_from_inputs(inp, N.MOE_MXFP8)
+    b = L.Buffers(s.T, s.d, s.E, s.k, s.f, N.MOE_MXFP8)
+    L.forward(p, b)
+    L.backward(p, b)
+    torch.cuda.synchronize()
+    assert N.moe_get_device_error() == 0
+    gl = b.logits.cpu().numpy().astype(np.float64)
+    ref = mxfp8_layer.layer(inp.x(), inp.w_r(), inp.w_gate(), inp.w_up(), inp.w_down(), inp.dy(), s.k, gl)
+    np.testing.assert_array_equal(b.dest_row.cpu().numpy(), ref["dest_row"])
+    f = s.f
+    np_ = lambda t: t.detach().float().cpu().numpy()  # noqa: E731
+    errs = {
+        "h_gate": _err(np_(b.h_save)[:, :f], ref["hg"]),
+        "h_up": _err(np_(b.h_save)[:, f:], ref["hu"]),
+        "a": _err(np_(b.a_save), ref["a"]),
+        "y_perm": _err(np_(b.y_perm), ref["ye"]),
+        "y": _err(np_(b.y), ref["y"]),
+        "dgates": _err(np_(b.dgates), ref["dgates"]),
+        "dlogits": _err(np_(b.dlogits), ref["dlogits"]),
+        "dx": _err(np_(b.dx), ref["dx"]),
+        "dw_gate": _err(np_(b.dw_gate), ref["dw_gate"]),
+        "dw_up": _err(np_(b.dw_up), ref["dw_up"]),
+        "dw_down": _err(np_(b.dw_down), ref["dw_down"]),
+        "dw_router": _err(np_(b.dw_router), ref["dw_r"].T),
+    }
+    bad = {k: v for k, v in errs.items() if not v <= MX_TOL}
+    # reported, not gated: distance of the MXFP8 layer from the unquantised fp64 layer
+    plain = mxfp8_layer.layer(inp.x(), inp.w_r(), inp.w_gate(), inp.w_up(), inp.w_down(), inp.dy(), s.k, gl,
+                              quant=False)
+    print(f"{s.name}: vs MXFP8 oracle {errs}; y vs unquantised {_err(np_(b.y), plain['y']):.4f}, "
+          f"dx vs unquantised {_err(np_(b.dx), plain['dx']):.4f}")
+    assert not bad, f"{s.name}: {bad} (all: {errs})"

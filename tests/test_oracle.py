@@ -352,3 +352,58 @@ def test_mxfp8_segmented_columns_equal_rows_of_padded_transpose():
         np.testing.assert_array_equal(s[brow:brow + nb], st.T)
         brow += nb
     assert brow == s.shape[0]
+
+
+# --------------------------------------------------------- MXFP8 layer oracle
+def test_mxfp8_layer_without_quantisation_is_the_c_oracle():
+    """The MXFP8 layer oracle with its fake-quantisations switched off must equal
+    the token-by-token C oracle on every output (per-pair values compared in
+    dispatch order)."""
+    from oracle import mxfp8_layer
+    rng = np.random.default_rng(12)
+    T, d, E, k, f = 50, 64, 6, 2, 32
+    x = _rand(rng, T, d)
+    wr = _rand(rng, d, E)
+    wg, wu = _rand(rng, E, d, f, std=0.2), _rand(rng, E, d, f, std=0.2)
+    wd = _rand(rng, E, f, d, std=0.2)
+    dy = _rand(rng, T, d)
+    logits = x.astype(np.float64) @ wr.astype(np.float64)
+    logits[:, 0] -= 50.0  # expert 0 empty
+    ref = oracle.layer(x, wr, wg, wu, wd, dy, k, logits=logits)
+    got = mxfp8_layer.layer(x, wr, wg, wu, wd, dy, k, logits, quant=False)
+    dest = ref["dest_row"].ravel()
+    np.testing.assert_allclose(got["hg"][dest], ref["hg"], rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(got["ye"][dest], ref["ye"], rtol=1e-11, atol=1e-12)
+    for key in ("y", "dgates", "dlogits", "dx", "dw_gate", "dw_up", "dw_down", "dw_r"):
+        np.testing.assert_allclose(got[key], ref[key], rtol=1e-10, atol=1e-11, err_msg=key)
+
+
+def test_mxfp8_fakequant_f64_matches_f32_quantiser():
+    rng = np.random.default_rng(13)
+    v = synth.round_bf16((rng.standard_normal((64, 128)) * 3).astype(np.float32))
+    q, s = oracle.mxfp8_quantize_rows(v)
+    np.testing.assert_array_equal(oracle.mxfp8_fakequant_rows(v.astype(np.float64)),
+                                  oracle.mxfp8_dequantize_rows(q, s))
+    seg = np.array([0, 10, 10, 64], np.int32)
+    q, s = oracle.mxfp8_quantize_cols_segmented(v, seg)
+    np.testing.assert_array_equal(oracle.mxfp8_fakequant_cols_segmented(v.astype(np.float64), seg),
+                                  oracle.mxfp8_dequantize_cols_segmented(q, s, seg))
+
+
+def test_mxfp8_layer_close_to_unquantised():
+    """Quantisation error of the whole MXFP8 layer stays at the few-percent level
+    E4M3 implies (3 mantissa bits: relative step 2^-3, error <= 2^-4 per element)."""
+    from oracle import mxfp8_layer
+    rng = np.random.default_rng(14)
+    T, d, E, k, f = 64, 64, 4, 2, 64
+    x = synth.round_bf16(rng.standard_normal((T, d)).astype(np.float32))
+    wr = _rand(rng, d, E, std=0.2)
+    wg, wu = _rand(rng, E, d, f, std=d ** -0.5), _rand(rng, E, d, f, std=d ** -0.5)
+    wd = _rand(rng, E, f, d, std=f ** -0.5)
+    dy = _rand(rng, T, d)
+    logits = x.astype(np.float64) @ wr.astype(np.float64)
+    a = mxfp8_layer.layer(x, wr, wg, wu, wd, dy, k, logits, quant=True)
+    b = mxfp8_layer.layer(x, wr, wg, wu, wd, dy, k, logits, quant=False)
+    for key in ("y", "dx", "dw_gate", "dw_down"):
+        err = np.abs(a[key] - b[key]).max() / np.abs(b[key]).max()
+        assert 1e-4 < err < 0.1, (key, err)

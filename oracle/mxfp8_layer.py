@@ -15,8 +15,12 @@ and the router backward stay in fp64 on unquantised values. Operands:
   wgrad1 x, dh along the expert's rows
 
 Each GEMM is a per-expert matrix product over that expert's rows in dispatch
-order. With quant=False every fake-quantisation is the identity and the
-function must equal the C oracle (its pin).
+order. Activations are stored in bf16 between steps, as on the bf16 path
+(store_bf16=True): h = (hg | hu), a, the expert outputs, dye, dh and dx_perm
+are rounded to bf16 (nearest, ties to even) where they are stored, and later
+steps read the stored values; the arithmetic itself stays fp64. With
+quant=False and store_bf16=False every fake-quantisation and rounding is the
+identity and the function must equal the C oracle (its pin).
 """
 from __future__ import annotations
 
@@ -34,7 +38,14 @@ def _dsilu(z):
     return s * (1.0 + z * (1.0 - s))
 
 
-def layer(x, w_r, w_gate, w_up, w_down, dy, k, logits, quant=True):
+def round_bf16(v):
+    """Round fp64 values to the nearest bfloat16 (8 significant bits, ties to even)."""
+    v = np.asarray(v, np.float64)
+    m, e = np.frexp(v)                 # v = m * 2^e, |m| in [0.5, 1)
+    return np.ldexp(np.rint(np.ldexp(m, 8)), e - 8)
+
+
+def layer(x, w_r, w_gate, w_up, w_down, dy, k, logits, quant=True, store_bf16=True):
     x = np.asarray(x, np.float64)
     dy = np.asarray(dy, np.float64)
     w_r = np.asarray(w_r, np.float64)
@@ -50,6 +61,7 @@ def layer(x, w_r, w_gate, w_up, w_down, dy, k, logits, quant=True):
     gr = g.ravel()[src]     # gate of each dispatched row
 
     fq_rows = mxfp8_fakequant_rows if quant else (lambda v: np.asarray(v, np.float64))
+    st = round_bf16 if store_bf16 else (lambda v: np.asarray(v, np.float64))
 
     def fq_seg(v):
         return mxfp8_fakequant_cols_segmented(v, offsets) if quant else np.asarray(v, np.float64)
@@ -66,17 +78,19 @@ def layer(x, w_r, w_gate, w_up, w_down, dy, k, logits, quant=True):
     for e, r0, r1 in segs:
         hg[r0:r1] = xq[r0:r1] @ fq_wcols(wg[e])
         hu[r0:r1] = xq[r0:r1] @ fq_wcols(wu[e])
-    a = _silu(hg) * hu
+    a = st(_silu(hg) * hu)
+    hg, hu = st(hg), st(hu)
     aq = fq_rows(a)
     for e, r0, r1 in segs:
         ye[r0:r1] = aq[r0:r1] @ fq_wcols(wd[e])
+    ye = st(ye)
     y = np.zeros((T, d))
     for t in range(T):
         for j in range(k):
             y[t] += g[t, j] * ye[dest[t, j]]
 
     # backward
-    dye = gr[:, None] * dy[tok]
+    dye = st(gr[:, None] * dy[tok])
     dgates = np.zeros((T, k))
     for t in range(T):
         for j in range(k):
@@ -87,7 +101,7 @@ def layer(x, w_r, w_gate, w_up, w_down, dy, k, logits, quant=True):
         da[r0:r1] = dyq[r0:r1] @ fq_rows(wd[e]).T
     dhg = da * hu * _dsilu(hg)
     dhu = da * _silu(hg)
-    dh = np.concatenate([dhg, dhu], axis=1)
+    dh = st(np.concatenate([dhg, dhu], axis=1))
     dhq = fq_rows(dh)
     dx_perm = np.zeros((R, d))
     dw_gate = np.zeros_like(wg); dw_up = np.zeros_like(wu); dw_down = np.zeros_like(wd)
@@ -98,6 +112,7 @@ def layer(x, w_r, w_gate, w_up, w_down, dy, k, logits, quant=True):
         dw_gate[e] = x_s[r0:r1].T @ dh_s[r0:r1, :f]
         dw_up[e] = x_s[r0:r1].T @ dh_s[r0:r1, f:]
     # router: softmax over the selected logits
+    dx_perm = st(dx_perm)
     dlogits = np.zeros((T, E))
     for t in range(T):
         for i in range(k):

@@ -163,24 +163,27 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         if (!wait_bar(&sm->full[s], ph, &sm->abort_flag, p.err)) { ok = false; break; }
         ptx::tc_fence_after();
         uint8_t* a = smem + s * STAGE_BYTES;
+        int nks = BK / 16;  // K steps of 16 rows issued for this stage
         if (Tr::kragged) {
           const int valid = tl.row_end - (tl.k_row0 + kb * BK);
           if (valid < BK) {
-            // rows past the expert's end belong to the next expert: zero them in A
-            const int nrow = BK - valid, per_box = nrow * 8;
+            // Rows past the expert's end belong to the next expert. K steps made
+            // only of such rows are skipped; inside the last partial step the
+            // extra rows of A are zeroed.
+            nks = (valid + 15) / 16;
+            const int nrow = nks * 16 - valid, per_box = nrow * 8;
             for (int i = lane; i < 2 * per_box; i += 32) {
               const int box = i / per_box, rem = i % per_box;
               const int row = valid + rem / 8, chunk = rem % 8;
               *reinterpret_cast<uint4*>(a + box * BOX_BYTES + row * 128 + chunk * 16) = make_uint4(0, 0, 0, 0);
             }
-            ptx::fence_proxy_async_smem();
+            if (nrow > 0) ptx::fence_proxy_async_smem();
           }
           __syncwarp();
         }
         if (lane == 0) {
           const uint32_t a_addr = ptx::smem_u32(a), b_addr = a_addr + A_BYTES;
-#pragma unroll
-          for (int ks = 0; ks < BK / 16; ++ks) {
+          for (int ks = 0; ks < nks; ++ks) {
             const uint64_t ad = Tr::a_mn ? ptx::smem_desc_sw128(a_addr + ks * 2048, BOX_BYTES, 1024)
                                          : ptx::smem_desc_sw128(a_addr + ks * 32, 16, 1024);
             const uint64_t bd = Tr::b_mn ? ptx::smem_desc_sw128(b_addr + ks * 2048, BOX_BYTES, 1024)

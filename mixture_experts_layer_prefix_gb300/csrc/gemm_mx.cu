@@ -5,19 +5,25 @@
 // outputs are bf16, with the same fused SwiGLU epilogues as the bf16 GEMMs.
 //
 // One persistent kernel per GEMM, one CTA per SM:
-//   warp 0      TMA producer: 4-stage ring of (A 128x128, B 256x128) E4M3
-//               tiles (128 B rows, 128-byte swizzle).
-//   warp 1      TMEM owner and MMA issuer: tcgen05.mma kind::mxf8f6f4
-//               block_scale (M=128, N=256, K=32; 4 per stage, scale id = K step).
-//   warps 2..5  scale loaders (one per TMEM lane quadrant): read the stage's
-//               E8M0 bytes of A (one 32-bit word per row) and B (eight words
-//               per lane, one per 32 output columns, written in every
-//               quadrant) and store them into a TMEM scale ring with
-//               tcgen05.st, then arrive on the stage's scale barrier.
-//   warps 6..9  epilogue (one per quadrant), as in the bf16 kernel.
-// TMEM: accumulator columns [0,256) (one buffer: the scale ring needs the
-// rest of the columns a second buffer would use), A scales at 256 + 4s, B
-// scales at 272 + 8s for stage s.
+//   warp 0      producer. Lane 0 issues TMA for a 4-stage ring of
+//               (A 128x128, B 256x128) E4M3 tiles (128 B rows, 128-byte
+//               swizzle); all lanes gather the stage's E8M0 scales as 32-bit
+//               words (4 consecutive K blocks each) with cp.async into a small
+//               shared staging area, tracked by the same stage barrier.
+//   warp 1      TMEM owner and MMA issuer: per stage, tcgen05.cp moves the
+//               scales from shared memory into a TMEM ring (32x128b copies
+//               replicated to all four lane quadrants), then four
+//               tcgen05.mma kind::mxf8f6f4 block_scale (M=128, N=256, K=32,
+//               scale-factor id = K step).
+//   warps 2..9  epilogue, two warps per TMEM lane quadrant. The accumulator
+//               is single-buffered (the scale ring takes the columns a second
+//               buffer would need), so each warp first copies its 128 columns
+//               into registers and releases the accumulator, then computes
+//               and stores; the next tile's MMAs overlap the stores.
+// TMEM: accumulator columns [0,256); scales of stage s: A at 256 + 4s, B at
+// 272 + 8s. Shared scale staging of a stage: A 512 B (row r of the copy = tile
+// rows r, 32+r, 64+r, 96+r), then B 2 x 512 B (copy h row r = tile columns
+// 128h + r, +32, +64, +96).
 #include "kernels.h"
 #include "tc_common.cuh"
 
@@ -31,13 +37,14 @@ constexpr int A_BYTES = BM * BK;
 constexpr int B_BYTES = BN * BK;
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int BOX_BYTES = 128 * 128;  // one 128 (MN) x 128 (K) box
-constexpr int NUM_THREADS = 320;
+constexpr int SC_BYTES = 512 + 1024;  // scale staging per stage
+constexpr int NUM_EPI_WARPS = 8;
+constexpr int NUM_THREADS = 64 + 32 * NUM_EPI_WARPS;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t SFA_COL = 256, SFB_COL = 272;
 
 struct Smem {
   uint64_t full[STAGES];
-  uint64_t sfull[STAGES];
   uint64_t empty[STAGES];
   uint64_t tfull;
   uint64_t tempty;
@@ -46,18 +53,46 @@ struct Smem {
   int abort_flag;
 };
 
-__device__ __forceinline__ uint32_t ld_u32(const uint8_t* p) { return *reinterpret_cast<const uint32_t*>(p); }
+__device__ __forceinline__ void cp_async4(void* dst, const void* src, bool valid) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(ptx::smem_u32(dst)), "l"(src),
+               "r"(valid ? 4 : 0)
+               : "memory");
+}
+// The stage barrier completes only once this thread's earlier cp.async copies landed.
+__device__ __forceinline__ void cp_async_arrive(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" ::"r"(ptx::smem_u32(bar)) : "memory");
+}
+// Non-swizzled shared-memory descriptor of a [rows][16 B] source of tcgen05.cp
+// (8-row groups 128 B apart).
+__device__ __forceinline__ uint64_t cp_desc(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
+  d |= static_cast<uint64_t>(16 >> 4) << 16;
+  d |= static_cast<uint64_t>(128 >> 4) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  return d;
+}
+__device__ __forceinline__ void tmem_cp_32x128b_x4(uint32_t taddr, uint64_t desc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(desc) : "memory");
+}
 
-// Four scale bytes of consecutive 32-blocks along K for MN index `col` from a
-// [block rows][ncols] table, or 1.0 (127) where the block is past `nblk`.
-__device__ __forceinline__ uint32_t gather4(const uint8_t* tab, long blk0, int nblk_avail, long ncols, long col) {
-  uint32_t w = 0;
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const uint32_t b = j < nblk_avail ? tab[(blk0 + j) * ncols + col] : 127u;
-    w |= b << (8 * j);
+// bf16 store of one 32-column chunk of a plain or wgrad output.
+template <int KIND>
+__device__ __forceinline__ void store_chunk(const Params& p, const Tile& tl, int r_tile, int c, const float* v) {
+  const int n = tl.n_idx * BN + c * 32;
+  if (Traits<KIND>::kragged) {
+    const int m = tl.m0 + r_tile;
+    if (m >= p.M || n >= p.N) return;
+    __nv_bfloat16* dst;
+    if (KIND == WGRAD2) dst = static_cast<__nv_bfloat16*>(p.out0) + ((size_t)tl.e * p.M + m) * p.N + n;
+    else dst = n < p.f ? static_cast<__nv_bfloat16*>(p.out0) + ((size_t)tl.e * p.d + m) * p.f + n
+                       : static_cast<__nv_bfloat16*>(p.out1) + ((size_t)tl.e * p.d + m) * p.f + (n - p.f);
+    store_bf16x32(dst, v);
+  } else {
+    const int row = tl.m0 + r_tile;
+    if (row >= tl.row_end || n >= p.N) return;
+    store_bf16x32(static_cast<__nv_bfloat16*>(p.out0) + (size_t)row * p.N + n, v);
   }
-  return w;
 }
 
 template <int KIND>
@@ -67,10 +102,11 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   using Tr = Traits<KIND>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  Smem* sm = reinterpret_cast<Smem*>(smem + STAGES * STAGE_BYTES);
+  uint8_t* sc_area = smem + STAGES * STAGE_BYTES;
+  Smem* sm = reinterpret_cast<Smem*>(sc_area + STAGES * SC_BYTES);
   int* offs = reinterpret_cast<int*>(sm + 1);
   int* tstart = offs + (p.E + 1);
-  int* bstart = tstart + (p.E + 1);  // wgrad: first 32-row scale block of each expert segment
+  int* wstart = tstart + (p.E + 1);  // wgrad: first packed scale word row of each expert segment
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   build_tile_table<KIND, NUM_THREADS>(p, offs, tstart);
@@ -78,25 +114,24 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     int carry = 0;
     for (int base = 0; base < p.E; base += 32) {
       const int e = base + lane;
-      const int v = e < p.E ? (offs[e + 1] - offs[e] + 31) / 32 : 0;
+      const int v = e < p.E ? ((offs[e + 1] - offs[e] + 31) / 32 + 3) / 4 : 0;
       int incl = v;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         const int nb = __shfl_up_sync(0xffffffffu, incl, o);
         if (lane >= o) incl += nb;
       }
-      if (e < p.E) bstart[e] = carry + incl - v;
+      if (e < p.E) wstart[e] = carry + incl - v;
       carry += __shfl_sync(0xffffffffu, incl, 31);
     }
   }
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       ptx::mbar_init(&sm->full[s], 1);
-      ptx::mbar_init(&sm->sfull[s], 4);
       ptx::mbar_init(&sm->empty[s], 1);
     }
     ptx::mbar_init(&sm->tfull, 1);
-    ptx::mbar_init(&sm->tempty, 4);
+    ptx::mbar_init(&sm->tempty, NUM_EPI_WARPS);
     ptx::mbar_init(&sm->drain, 1);
     sm->abort_flag = 0;
     ptx::fence_mbar_init();
@@ -111,26 +146,82 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   ptx::tc_fence_after();
   const int total = Tr::kragged ? p.E * p.m_tiles * p.n_tiles : tstart[p.E];
   const uint32_t tmem = sm->tmem_base;
+  const long Kd = gemm_k<KIND>(p);
 
   if (warp == 0) {
-    // ===================================================== TMA producer
+    // ===================================================== producer
     if (lane == 0) {
       ptx::prefetch_tmap(&tmA);
       ptx::prefetch_tmap(&tmB0);
       ptx::prefetch_tmap(&tmB1);
-      uint32_t it = 0;
-      bool ok = true;
-      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-        const Tile tl = decode<KIND, BK>(t, p, offs, tstart);
-        for (int kb = 0; kb < tl.nkb; ++kb, ++it) {
-          const int s = it % STAGES;
-          const uint32_t ph = (it / STAGES) & 1u;
-          if (!wait_bar(&sm->empty[s], ph ^ 1u, &sm->abort_flag, p.err)) { ok = false; break; }
+    }
+    uint32_t it = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+      const Tile tl = decode<KIND, BK>(t, p, offs, tstart);
+      for (int kb = 0; kb < tl.nkb; ++kb, ++it) {
+        const int s = it % STAGES;
+        const uint32_t ph = (it / STAGES) & 1u;
+        if (!wait_bar(&sm->empty[s], ph ^ 1u, &sm->abort_flag, p.err)) { ok = false; break; }
+        uint64_t* fb = &sm->full[s];
+        const int k0 = kb * BK;
+        // ---- scales: A rows of the tile, then B columns
+        uint8_t* sa = sc_area + s * SC_BYTES;
+        uint8_t* sb = sa + 512;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int r = lane + 32 * i;
+          const uint8_t* src = p.sfa;
+          bool valid;
+          if (!Tr::kragged) {  // rows quantised along K: [R][K/32] bytes
+            const int row = tl.m0 + r;
+            valid = row < p.R;
+            if (valid) src = p.sfa + (size_t)row * (Kd / 32) + k0 / 32;
+          } else {  // columns quantised along the expert's rows: [words][M] words
+            const int m = tl.m0 + r;
+            valid = m < p.M;
+            if (valid) src = p.sfa + ((size_t)(wstart[tl.e] + kb) * p.M + m) * 4;
+          }
+          cp_async4(sa + lane * 16 + i * 4, src, valid);
+        }
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const int nt = lane + 32 * c;  // tile column
+          const uint8_t* src = p.sfb0;
+          bool valid = false;
+          if (KIND == FPROP1) {  // gate | up, [E*d/128][f] words
+            const int n = tl.n_idx * 128 + (nt & 127);
+            valid = n < p.f;
+            if (valid) src = (nt < 128 ? p.sfb0 : p.sfb1) + (((size_t)tl.e * p.d + k0) / 128 * p.f + n) * 4;
+          } else if (KIND == FPROP2) {  // [E*f/128][d] words
+            const int n = tl.n_idx * BN + nt;
+            valid = n < p.d;
+            if (valid) src = p.sfb0 + (((size_t)tl.e * p.f + k0) / 128 * p.d + n) * 4;
+          } else if (KIND == DGRAD2) {  // rows of w_down along d: [E*f][d/32] bytes
+            const int n = tl.n_idx * BN + nt;
+            valid = n < p.f;
+            if (valid) src = p.sfb0 + ((size_t)tl.e * p.f + n) * (p.d / 32) + k0 / 32;
+          } else if (KIND == DGRAD1) {  // rows of w_gate / w_up along f: [E*d][f/32] bytes
+            const int n = tl.n_idx * BN + nt;
+            valid = n < p.d;
+            if (valid) {
+              const int kk = k0 < p.f ? k0 : k0 - p.f;
+              src = (k0 < p.f ? p.sfb0 : p.sfb1) + ((size_t)tl.e * p.d + n) * (p.f / 32) + kk / 32;
+            }
+          } else {  // wgrad: columns quantised along the expert's rows, [words][N] words
+            const int n = tl.n_idx * BN + nt;
+            valid = n < p.N;
+            if (valid) src = p.sfb0 + ((size_t)(wstart[tl.e] + kb) * p.N + n) * 4;
+          }
+          cp_async4(sb + (c >> 2) * 512 + lane * 16 + (c & 3) * 4, src, valid);
+        }
+        cp_async_arrive(fb);
+        __syncwarp();
+        if (lane == 0) {
+          // ---- E4M3 tiles
           uint8_t* a = smem + s * STAGE_BYTES;
           uint8_t* b = a + A_BYTES;
-          uint64_t* fb = &sm->full[s];
           ptx::mbar_expect_tx(fb, STAGE_BYTES);
-          const int k0 = kb * BK;
           if (KIND == FPROP1) {
             ptx::tma_load_2d(a, &tmA, fb, k0, tl.m0);
             const int n0 = tl.n_idx * 128;
@@ -156,13 +247,14 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             ptx::tma_load_2d(b + BOX_BYTES, &tmB0, fb, n0 + 128, row);
           }
         }
+        __syncwarp();
       }
-      if (!ok) {
-        for (int s = 0; s < STAGES; ++s) {
-          const long long t0 = clock64();
-          while (clock64() - t0 < kWaitLimitCycles / 8 && !ptx::mbar_try_wait(&sm->full[s], 0) &&
-                 !ptx::mbar_try_wait(&sm->full[s], 1)) {
-          }
+    }
+    if (!ok && lane == 0) {
+      for (int s = 0; s < STAGES; ++s) {
+        const long long t0 = clock64();
+        while (clock64() - t0 < kWaitLimitCycles / 8 && !ptx::mbar_try_wait(&sm->full[s], 0) &&
+               !ptx::mbar_try_wait(&sm->full[s], 1)) {
         }
       }
     }
@@ -178,27 +270,30 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       for (int kb = 0; kb < tl.nkb; ++kb, ++it) {
         const int s = it % STAGES;
         const uint32_t ph = (it / STAGES) & 1u;
-        if (!wait_bar(&sm->full[s], ph, &sm->abort_flag, p.err) ||
-            !wait_bar(&sm->sfull[s], ph, &sm->abort_flag, p.err)) {
-          ok = false;
-          break;
-        }
+        if (!wait_bar(&sm->full[s], ph, &sm->abort_flag, p.err)) { ok = false; break; }
         ptx::tc_fence_after();
         uint8_t* a = smem + s * STAGE_BYTES;
+        int nks = BK / 32;
         if (Tr::kragged) {
           const int valid = tl.row_end - (tl.k_row0 + kb * BK);
           if (valid < BK) {
-            // rows past the expert's end belong to the next expert: zero them in A
-            for (int i = valid * 8 + lane; i < BK * 8; i += 32)
+            // skip K steps made only of rows past the expert's end; zero the
+            // rest of the last partial step in A (one 128-row box)
+            nks = (valid + 31) / 32;
+            for (int i = valid * 8 + lane; i < nks * 32 * 8; i += 32)
               *reinterpret_cast<uint4*>(a + i * 16) = make_uint4(0, 0, 0, 0);
-            ptx::fence_proxy_async_smem();
           }
-          __syncwarp();
         }
+        // cp.async-written scales and the zeroed rows are read by the async proxy
+        ptx::fence_proxy_async_smem();
+        __syncwarp();
         if (lane == 0) {
+          const uint32_t sa = ptx::smem_u32(sc_area + s * SC_BYTES);
+          tmem_cp_32x128b_x4(tmem + SFA_COL + 4 * s, cp_desc(sa));
+          tmem_cp_32x128b_x4(tmem + SFB_COL + 8 * s, cp_desc(sa + 512));
+          tmem_cp_32x128b_x4(tmem + SFB_COL + 8 * s + 4, cp_desc(sa + 1024));
           const uint32_t a_addr = ptx::smem_u32(a), b_addr = a_addr + A_BYTES;
-#pragma unroll
-          for (int ks = 0; ks < BK / 32; ++ks) {
+          for (int ks = 0; ks < nks; ++ks) {
             const uint64_t ad = Tr::a_mn ? ptx::smem_desc_sw128(a_addr + ks * 4096, BOX_BYTES, 1024)
                                          : ptx::smem_desc_sw128(a_addr + ks * 32, 16, 1024);
             const uint64_t bd = Tr::b_mn ? ptx::smem_desc_sw128(b_addr + ks * 4096, BOX_BYTES, 1024)
@@ -222,88 +317,76 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       while (clock64() - t0 < kWaitLimitCycles / 8 && !ptx::mbar_try_wait(&sm->drain, 0)) {
       }
     }
-  } else if (warp < 6) {
-    // ====================================================== scale loaders
-    const int q = warp & 3;
-    const int r_tile = q * 32 + lane;
-    uint32_t it = 0;
-    const long Kd = gemm_k<KIND>(p);
-    for (int t = blockIdx.x; t < total; t += gridDim.x) {
-      const Tile tl = decode<KIND, BK>(t, p, offs, tstart);
-      bool ok = true;
-      for (int kb = 0; kb < tl.nkb; ++kb, ++it) {
-        const int s = it % STAGES;
-        const uint32_t ph = (it / STAGES) & 1u;
-        const int k0 = kb * BK;
-        uint32_t wa, wb[8];
-        if (!Tr::kragged) {
-          // A: rows quantised along K, table [R][K/32]
-          const int row = tl.m0 + r_tile;
-          wa = row < p.R ? ld_u32(p.sfa + (size_t)row * (Kd / 32) + k0 / 32) : 0x7F7F7F7Fu;
-        } else {
-          // A: columns quantised along the expert's rows, table [blocks][M]
-          const int m = tl.m0 + r_tile;
-          const int nblk = (tl.row_end - tl.k_row0 + 31) / 32;
-          wa = m < p.M ? gather4(p.sfa, bstart[tl.e] + 4 * kb, nblk - 4 * kb, p.M, m) : 0x7F7F7F7Fu;
-        }
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          uint32_t w = 0x7F7F7F7Fu;
-          if (KIND == FPROP1) {
-            const int n = tl.n_idx * 128 + lane + 32 * (c & 3);
-            const uint8_t* tab = c < 4 ? p.sfb0 : p.sfb1;  // [E*d/32][f]
-            if (n < p.f) w = gather4(tab, ((long)tl.e * p.d + k0) / 32, 4, p.f, n);
-          } else if (KIND == FPROP2) {
-            const int n = tl.n_idx * BN + lane + 32 * c;  // [E*f/32][d]
-            if (n < p.d) w = gather4(p.sfb0, ((long)tl.e * p.f + k0) / 32, 4, p.d, n);
-          } else if (KIND == DGRAD2) {
-            const int n = tl.n_idx * BN + lane + 32 * c;  // [E*f][d/32]
-            if (n < p.f) w = ld_u32(p.sfb0 + ((size_t)tl.e * p.f + n) * (p.d / 32) + k0 / 32);
-          } else if (KIND == DGRAD1) {
-            const int n = tl.n_idx * BN + lane + 32 * c;  // [E*d][f/32]
-            if (n < p.d) {
-              const uint8_t* tab = k0 < p.f ? p.sfb0 : p.sfb1;
-              const int kk = k0 < p.f ? k0 : k0 - p.f;
-              w = ld_u32(tab + ((size_t)tl.e * p.d + n) * (p.f / 32) + kk / 32);
-            }
-          } else {  // WGRAD: B columns quantised along the expert's rows, table [blocks][N]
-            const int n = tl.n_idx * BN + lane + 32 * c;
-            const int nblk = (tl.row_end - tl.k_row0 + 31) / 32;
-            if (n < p.N) w = gather4(p.sfb0, bstart[tl.e] + 4 * kb, nblk - 4 * kb, p.N, n);
-          }
-          wb[c] = w;
-        }
-        if (!wait_bar(&sm->empty[s], ph ^ 1u, &sm->abort_flag, p.err)) { ok = false; break; }
-        const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
-        ptx::tmem_st4(tmem + lane_base + SFA_COL + 4 * s, wa, wa, wa, wa);
-        ptx::tmem_st8(tmem + lane_base + SFB_COL + 8 * s, wb);
-        ptx::tmem_wait_st();
-        ptx::tc_fence_before();
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(&sm->sfull[s]);
-      }
-      if (!ok) break;
-    }
   } else {
     // ============================================================ epilogue
-    const int q = warp & 3;
-    constexpr int NC = epi_chunks<KIND>();
+    const int ew = warp - 2, q = warp & 3, half = ew >> 2;
+    const int r_tile = q * 32 + lane;
     uint32_t acc_it = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
       const Tile tl = decode<KIND, BK>(t, p, offs, tstart);
-      const bool empty_k = tl.nkb == 0;
-      if (!empty_k) {
-        if (!wait_bar(&sm->tfull, acc_it & 1u, &sm->abort_flag, p.err)) break;
-        ptx::tc_fence_after();
+      if (tl.nkb == 0) {  // wgrad of an expert without rows
+        float z[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) z[i] = 0.0f;
+        for (int c = half * 4; c < half * 4 + 4; ++c) store_chunk<KIND>(p, tl, r_tile, c, z);
+        continue;
       }
+      if (!wait_bar(&sm->tfull, acc_it & 1u, &sm->abort_flag, p.err)) break;
+      ptx::tc_fence_after();
       const uint32_t tbase = tmem + (static_cast<uint32_t>(q * 32) << 16);
-      epilogue_tile<KIND>(p, tl, tbase, q * 32 + lane, 0, NC, empty_k);
-      if (!empty_k) {
+      if (KIND == DGRAD2) {
+        epilogue_tile<KIND>(p, tl, tbase, r_tile, half * 4, half * 4 + 4, false);
         ptx::tc_fence_before();
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(&sm->tempty);
-        ++acc_it;
+      } else {
+        // copy this warp's 128 accumulator columns out, release the accumulator, then store
+        uint32_t acc[4][32];
+        if (KIND == FPROP1) {
+          ptx::tmem_ld32(tbase + (2 * half) * 32, acc[0]);
+          ptx::tmem_ld32(tbase + (2 * half + 1) * 32, acc[1]);
+          ptx::tmem_ld32(tbase + 128 + (2 * half) * 32, acc[2]);
+          ptx::tmem_ld32(tbase + 128 + (2 * half + 1) * 32, acc[3]);
+        } else {
+#pragma unroll
+          for (int c = 0; c < 4; ++c) ptx::tmem_ld32(tbase + (4 * half + c) * 32, acc[c]);
+        }
+        ptx::tmem_wait_ld();
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&sm->tempty);
+        if (KIND == FPROP1) {
+          const int row = tl.m0 + r_tile;
+          if (row < tl.row_end) {
+            __nv_bfloat16* h = static_cast<__nv_bfloat16*>(p.out0) + (size_t)row * 2 * p.f;
+            __nv_bfloat16* ao = static_cast<__nv_bfloat16*>(p.out1) + (size_t)row * p.f;
+#pragma unroll
+            for (int cc = 0; cc < 2; ++cc) {
+              const int n = tl.n_idx * 128 + (2 * half + cc) * 32;
+              if (n >= p.f) continue;
+              float hg[32], hu[32], av[32];
+#pragma unroll
+              for (int i = 0; i < 32; ++i) {
+                hg[i] = __uint_as_float(acc[cc][i]);
+                hu[i] = __uint_as_float(acc[2 + cc][i]);
+                av[i] = silu_f(hg[i]) * hu[i];
+              }
+              store_bf16x32(h + n, hg);
+              store_bf16x32(h + p.f + n, hu);
+              store_bf16x32(ao + n, av);
+            }
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            float v[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(acc[c][i]);
+            store_chunk<KIND>(p, tl, r_tile, 4 * half + c, v);
+          }
+        }
       }
+      ++acc_it;
     }
   }
 
@@ -315,7 +398,9 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   }
 }
 
-size_t smem_bytes(int E) { return 1024 + STAGES * STAGE_BYTES + sizeof(Smem) + 3 * (E + 1) * sizeof(int) + 64; }
+size_t smem_bytes(int E) {
+  return 1024 + STAGES * STAGE_BYTES + STAGES * SC_BYTES + sizeof(Smem) + 3 * (E + 1) * sizeof(int) + 64;
+}
 
 template <int KIND>
 cudaError_t launch(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1, const Params& p,
@@ -357,8 +442,9 @@ struct Carver {
   }
 };
 
-// Scale-block rows of a [rows][C] operand quantised along rows in E segments.
-inline size_t seg_blocks(long rows, int E) { return (size_t)(rows + 31) / 32 + E + 1; }
+// Bytes of the packed scale table of a [rows][C] operand quantised along rows
+// in E segments (32-bit words of 4 blocks; a segment's words start anew).
+inline size_t seg_words_bytes(long rows, int E, long C) { return ((size_t)(rows + 127) / 128 + E + 1) * C * 4; }
 
 }  // namespace
 
@@ -372,13 +458,13 @@ size_t bwd_workspace(long R, int E, int d, int f) {
   const size_t Ed = (size_t)E * d, Ef = (size_t)E * f;
   return al(R * 2 * (size_t)f * 2)                                         // dh (bf16)
          + al(R * (size_t)d) + al(R * (size_t)d / 32)                      // dy rows
-         + al(R * (size_t)d) + al(seg_blocks(R, E) * d)                    // dy segment columns
-         + al(R * (size_t)f) + al(seg_blocks(R, E) * f)                    // a segment columns
+         + al(R * (size_t)d) + al(seg_words_bytes(R, E, d))                    // dy segment columns
+         + al(R * (size_t)f) + al(seg_words_bytes(R, E, f))                    // a segment columns
          + al(Ef * d) + al(Ef * d / 32)                                    // w_down rows
          + al(R * 2 * (size_t)f) + al(R * 2 * (size_t)f / 32)              // dh rows
-         + al(R * 2 * (size_t)f) + al(seg_blocks(R, E) * 2 * f)            // dh segment columns
+         + al(R * 2 * (size_t)f) + al(seg_words_bytes(R, E, 2L * f))            // dh segment columns
          + 2 * (al(Ed * f) + al(Ed * f / 32))                              // w_gate, w_up rows
-         + al(R * (size_t)d) + al(seg_blocks(R, E) * d);                   // x segment columns
+         + al(R * (size_t)d) + al(seg_words_bytes(R, E, d));                   // x segment columns
 }
 
 }  // namespace mx
@@ -399,9 +485,9 @@ cudaError_t mx_mlp_fwd(const void* x_perm, const void* wg, const void* wu, const
   cudaError_t e;
   // operands of GEMM1 along d: x rows, w_gate / w_up columns (32-row blocks never cross experts)
   if ((e = launch_mxfp8_quant_rows(x_perm, R, d, xq.q, xq.s, st)) != cudaSuccess) return e;
-  if ((e = launch_mxfp8_quant_cols(wg, (int)Ed, f, nullptr, 1, wgq.q, wgq.s, st)) != cudaSuccess) return e;
-  if ((e = launch_mxfp8_quant_cols(wu, (int)Ed, f, nullptr, 1, wuq.q, wuq.s, st)) != cudaSuccess) return e;
-  if ((e = launch_mxfp8_quant_cols(wd, (int)Ef, d, nullptr, 1, wdq.q, wdq.s, st)) != cudaSuccess) return e;
+  if ((e = launch_mxfp8_quant_cols(wg, (int)Ed, f, nullptr, 1, wgq.q, wgq.s, st, true)) != cudaSuccess) return e;
+  if ((e = launch_mxfp8_quant_cols(wu, (int)Ed, f, nullptr, 1, wuq.q, wuq.s, st, true)) != cudaSuccess) return e;
+  if ((e = launch_mxfp8_quant_cols(wd, (int)Ef, d, nullptr, 1, wdq.q, wdq.s, st, true)) != cudaSuccess) return e;
 
   CUtensorMap mA, mB0, mB1;
   Params p{};
@@ -429,14 +515,14 @@ cudaError_t mx_mlp_bwd(const void* dy_perm, const void* x_perm, const void* h, c
   const long Ed = (long)E * d, Ef = (long)E * f;
   void* dh = cv.raw((size_t)R * 2 * f * 2);
   QBuf dyr = cv.take((size_t)R * d, (size_t)R * d / 32);
-  QBuf dyc = cv.take((size_t)R * d, seg_blocks(R, E) * d);
-  QBuf ac = cv.take((size_t)R * f, seg_blocks(R, E) * f);
+  QBuf dyc = cv.take((size_t)R * d, seg_words_bytes(R, E, d));
+  QBuf ac = cv.take((size_t)R * f, seg_words_bytes(R, E, f));
   QBuf wdr = cv.take((size_t)Ef * d, (size_t)Ef * d / 32);
   QBuf dhr = cv.take((size_t)R * 2 * f, (size_t)R * 2 * f / 32);
-  QBuf dhc = cv.take((size_t)R * 2 * f, seg_blocks(R, E) * 2 * f);
+  QBuf dhc = cv.take((size_t)R * 2 * f, seg_words_bytes(R, E, 2L * f));
   QBuf wgr = cv.take((size_t)Ed * f, (size_t)Ed * f / 32);
   QBuf wur = cv.take((size_t)Ed * f, (size_t)Ed * f / 32);
-  QBuf xc = cv.take((size_t)R * d, seg_blocks(R, E) * d);
+  QBuf xc = cv.take((size_t)R * d, seg_words_bytes(R, E, d));
   cudaError_t e;
   CUtensorMap mA, mB0, mB1;
   Params p{};
@@ -452,8 +538,8 @@ cudaError_t mx_mlp_bwd(const void* dy_perm, const void* x_perm, const void* h, c
   if ((e = launch<DGRAD2>(mA, mB0, mB0, p, ((long)(R + BM - 1) / BM + E) * p.n_tiles, st)) != cudaSuccess) return e;
 
   // dWd[e] = A_e^T dy_e (K = the expert's rows): A and dy quantised along rows per expert
-  if ((e = launch_mxfp8_quant_cols(a, R, f, offsets, E, ac.q, ac.s, st)) != cudaSuccess) return e;
-  if ((e = launch_mxfp8_quant_cols(dy_perm, R, d, offsets, E, dyc.q, dyc.s, st)) != cudaSuccess) return e;
+  if ((e = launch_mxfp8_quant_cols(a, R, f, offsets, E, ac.q, ac.s, st, true)) != cudaSuccess) return e;
+  if ((e = launch_mxfp8_quant_cols(dy_perm, R, d, offsets, E, dyc.q, dyc.s, st, true)) != cudaSuccess) return e;
   if (!map_2d(&mA, ac.q, U8, 1, f, R, 128, 128) || !map_2d(&mB0, dyc.q, U8, 1, d, R, 128, 128))
     return cudaErrorInvalidValue;
   p.M = f; p.N = d; p.m_tiles = (f + BM - 1) / BM; p.n_tiles = (d + BN - 1) / BN; p.out0 = dwd; p.aux = nullptr;
@@ -472,8 +558,8 @@ cudaError_t mx_mlp_bwd(const void* dy_perm, const void* x_perm, const void* h, c
   if ((e = launch<DGRAD1>(mA, mB0, mB1, p, ((long)(R + BM - 1) / BM + E) * p.n_tiles, st)) != cudaSuccess) return e;
 
   // [dWg | dWu][e] = x_e^T dh_e (K = the expert's rows)
-  if ((e = launch_mxfp8_quant_cols(x_perm, R, d, offsets, E, xc.q, xc.s, st)) != cudaSuccess) return e;
-  if ((e = launch_mxfp8_quant_cols(dh, R, 2 * f, offsets, E, dhc.q, dhc.s, st)) != cudaSuccess) return e;
+  if ((e = launch_mxfp8_quant_cols(x_perm, R, d, offsets, E, xc.q, xc.s, st, true)) != cudaSuccess) return e;
+  if ((e = launch_mxfp8_quant_cols(dh, R, 2 * f, offsets, E, dhc.q, dhc.s, st, true)) != cudaSuccess) return e;
   if (!map_2d(&mA, xc.q, U8, 1, d, R, 128, 128) || !map_2d(&mB0, dhc.q, U8, 1, 2L * f, R, 128, 128))
     return cudaErrorInvalidValue;
   p.M = d; p.N = 2 * f; p.m_tiles = (d + BM - 1) / BM; p.n_tiles = (2 * f + BN - 1) / BN;

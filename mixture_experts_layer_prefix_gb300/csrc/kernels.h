@@ -72,8 +72,10 @@ cudaError_t tc_mlp_bwd(const void* dy_perm, const void* x_perm, const void* h, c
 // ------------------------------------------------------------------ MXFP8
 cudaError_t launch_mxfp8_quant_rows(const void* src, long rows, long K, uint8_t* q, uint8_t* sc,
                                     cudaStream_t st);
+// packed: scales as 32-bit words of 4 consecutive blocks of a column (GEMM operand
+// layout); otherwise one byte per block, [blocks][C] (public layout).
 cudaError_t launch_mxfp8_quant_cols(const void* src, int rows, int C, const int32_t* seg, int nseg,
-                                    uint8_t* q, uint8_t* sc, cudaStream_t st);
+                                    uint8_t* q, uint8_t* sc, cudaStream_t st, bool packed = false);
 
 cudaError_t tc_router_logits(const void* x, const void* w_r, const float* bias, int T, int d, int E,
                              float* logits, cudaStream_t st);

@@ -69,34 +69,50 @@ quant_rows_kernel(const __nv_bfloat16* __restrict__ src, long nblocks, uint8_t* 
 }
 
 // Block-row table: segment g owns block rows [bstart[g], bstart[g+1]).
+// PACKED: scales go to a [words][C] table of 32-bit words, word w of segment
+// g holding its blocks 4w..4w+3 in bytes 0..3 (words of segment g start at
+// sum_{h<g} ceil(blocks_h / 4)); bytes past a segment's last block are 127.
+template <bool PACKED>
 __global__ void __launch_bounds__(128)
 quant_cols_kernel(const __nv_bfloat16* __restrict__ src, int rows, int C, const int32_t* __restrict__ seg,
                   int nseg, uint8_t* __restrict__ q, uint8_t* __restrict__ sc) {
-  extern __shared__ int bstart[];  // nseg + 1
-  __shared__ int s_r0, s_r1;
+  extern __shared__ int bstart[];  // nseg + 1 block-row starts, then nseg + 1 word starts
+  int* wstart = bstart + nseg + 1;
+  __shared__ int s_r0, s_r1, s_word, s_byte, s_last;
   const int tid = threadIdx.x, lane = tid & 31;
   if (tid < 32) {
-    int carry = 0;
+    int carry = 0, wcarry = 0;
     for (int base = 0; base < nseg; base += 32) {
       const int g = base + lane;
       int len = 0;
       if (g < nseg) len = seg ? seg[g + 1] - seg[g] : rows;
-      const int v = (len + 31) / 32;
-      int incl = v;
+      const int v = (len + 31) / 32, vw = (v + 3) / 4;
+      int incl = v, wincl = vw;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         const int nb = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += nb;
+        const int nw = __shfl_up_sync(0xffffffffu, wincl, o);
+        if (lane >= o) {
+          incl += nb;
+          wincl += nw;
+        }
       }
-      if (g < nseg) bstart[g] = carry + incl - v;
+      if (g < nseg) {
+        bstart[g] = carry + incl - v;
+        wstart[g] = wcarry + wincl - vw;
+      }
       carry += __shfl_sync(0xffffffffu, incl, 31);
+      wcarry += __shfl_sync(0xffffffffu, wincl, 31);
     }
-    if (lane == 0) bstart[nseg] = carry;
+    if (lane == 0) {
+      bstart[nseg] = carry;
+      wstart[nseg] = wcarry;
+    }
   }
   __syncthreads();
   const int brow = blockIdx.x;
   if (tid == 0) {
-    int r0 = -1, r1 = -1;
+    int r0 = -1, r1 = -1, word = 0, byte = 0, last = 0;
     if (brow < bstart[nseg]) {
       int lo = 0, hi = nseg;  // bstart[lo] <= brow < bstart[lo + 1]
       while (hi - lo > 1) {
@@ -104,11 +120,20 @@ quant_cols_kernel(const __nv_bfloat16* __restrict__ src, int rows, int C, const 
         if (bstart[mid] <= brow) lo = mid; else hi = mid;
       }
       const int g0 = seg ? seg[lo] : 0, g1 = seg ? seg[lo + 1] : rows;
-      r0 = g0 + (brow - bstart[lo]) * 32;
+      const int local = brow - bstart[lo];
+      r0 = g0 + local * 32;
       r1 = min(r0 + 32, g1);
+      if (PACKED) {
+        word = wstart[lo] + local / 4;
+        byte = local % 4;
+        last = (brow == bstart[lo + 1] - 1);
+      }
     }
     s_r0 = r0;
     s_r1 = r1;
+    s_word = word;
+    s_byte = byte;
+    s_last = last;
   }
   __syncthreads();
   const int r0 = s_r0, r1 = s_r1;
@@ -136,7 +161,18 @@ quant_cols_kernel(const __nv_bfloat16* __restrict__ src, int rows, int C, const 
     if (r0 + i < r1)
       *reinterpret_cast<uint16_t*>(q + (size_t)(r0 + i) * C + c) =
           static_cast<uint16_t>(e4m3(v0[i] * m0) | (e4m3(v1[i] * m1) << 8));
-  *reinterpret_cast<uint16_t*>(sc + (size_t)brow * C + c) = static_cast<uint16_t>((s0 + 127) | ((s1 + 127) << 8));
+  if (!PACKED) {
+    *reinterpret_cast<uint16_t*>(sc + (size_t)brow * C + c) = static_cast<uint16_t>((s0 + 127) | ((s1 + 127) << 8));
+  } else {
+    uint8_t* w0 = sc + ((size_t)s_word * C + c) * 4;
+    w0[s_byte] = static_cast<uint8_t>(s0 + 127);
+    w0[4 + s_byte] = static_cast<uint8_t>(s1 + 127);
+    if (s_last)
+      for (int j = s_byte + 1; j < 4; ++j) {
+        w0[j] = 127;
+        w0[4 + j] = 127;
+      }
+  }
 }
 
 }  // namespace
@@ -151,13 +187,18 @@ cudaError_t launch_mxfp8_quant_rows(const void* src, long rows, long K, uint8_t*
 }
 
 cudaError_t launch_mxfp8_quant_cols(const void* src, int rows, int C, const int32_t* seg, int nseg,
-                                    uint8_t* q, uint8_t* sc, cudaStream_t st) {
+                                    uint8_t* q, uint8_t* sc, cudaStream_t st, bool packed) {
   const int nseg_eff = seg ? nseg : 1;
   const long max_brows = (rows + 31) / 32 + nseg_eff;
   if (rows == 0) return cudaSuccess;
   dim3 grid(static_cast<unsigned>(max_brows), static_cast<unsigned>((C / 2 + 127) / 128));
-  MOE_COUNTED quant_cols_kernel<<<grid, 128, (nseg_eff + 1) * sizeof(int), st>>>(
-      static_cast<const __nv_bfloat16*>(src), rows, C, seg, nseg_eff, q, sc);
+  const size_t smem = 2 * (nseg_eff + 1) * sizeof(int);
+  if (packed)
+    MOE_COUNTED quant_cols_kernel<true><<<grid, 128, smem, st>>>(static_cast<const __nv_bfloat16*>(src), rows, C,
+                                                                 seg, nseg_eff, q, sc);
+  else
+    MOE_COUNTED quant_cols_kernel<false><<<grid, 128, smem, st>>>(static_cast<const __nv_bfloat16*>(src), rows, C,
+                                                                  seg, nseg_eff, q, sc);
   return cudaGetLastError();
 }
 

@@ -330,7 +330,7 @@ moe_status mxfp8_quantize(const void* src, int rows, int K, int axis, const int3
                           int nseg, uint8_t* dst_e4m3, uint8_t* dst_e8m0, void* stream) {
   if (rows < 0 || K <= 0 || (axis != 0 && axis != 1)) return MOE_ERR_INVALID_ARG;
   if (axis == 0 && K % 32 != 0) return MOE_ERR_UNSUPPORTED;
-  if (axis == 1 && (K % 2 != 0 || (seg_offsets && (nseg <= 0 || nseg > 4096)))) return MOE_ERR_UNSUPPORTED;
+  if (axis == 1 && (K % 8 != 0 || (seg_offsets && (nseg <= 0 || nseg > 4096)))) return MOE_ERR_UNSUPPORTED;
   if (rows == 0) return MOE_OK;
   MOE_NEED(src); MOE_NEED(dst_e4m3); MOE_NEED(dst_e8m0);
   if (seg_offsets) MOE_NEED(seg_offsets);

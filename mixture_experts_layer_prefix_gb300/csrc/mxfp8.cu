@@ -13,8 +13,8 @@
 //   cols kernel: blocks of 32 consecutive rows of one column, starting at each
 //                segment's first row (segments = per-expert row ranges from
 //                the device offsets); a segment's last block is zero-padded.
-//                One CTA per (block row, 256 columns); each thread owns two
-//                columns and keeps its 32x2 values in registers.
+//                Each thread owns 8 columns (16-byte loads); two passes over
+//                the block's rows (block maxima, then conversion).
 #include <cuda_fp8.h>
 
 #include "common.cuh"
@@ -72,6 +72,11 @@ quant_rows_kernel(const __nv_bfloat16* __restrict__ src, long nblocks, uint8_t* 
 // PACKED: scales go to a [words][C] table of 32-bit words, word w of segment
 // g holding its blocks 4w..4w+3 in bytes 0..3 (words of segment g start at
 // sum_{h<g} ceil(blocks_h / 4)); bytes past a segment's last block are 127.
+// A CTA handles kColBlockRows block rows of 1024 columns; each thread owns 8
+// consecutive columns: a first pass over the 32 rows finds the 8 block
+// maxima, a second pass (rows now in L1) converts and stores 8 codes per row.
+constexpr int kColBlockRows = 4;
+
 template <bool PACKED>
 __global__ void __launch_bounds__(128)
 quant_cols_kernel(const __nv_bfloat16* __restrict__ src, int rows, int C, const int32_t* __restrict__ seg,
@@ -110,68 +115,85 @@ quant_cols_kernel(const __nv_bfloat16* __restrict__ src, int rows, int C, const 
     }
   }
   __syncthreads();
-  const int brow = blockIdx.x;
-  if (tid == 0) {
-    int r0 = -1, r1 = -1, word = 0, byte = 0, last = 0;
-    if (brow < bstart[nseg]) {
-      int lo = 0, hi = nseg;  // bstart[lo] <= brow < bstart[lo + 1]
-      while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (bstart[mid] <= brow) lo = mid; else hi = mid;
-      }
-      const int g0 = seg ? seg[lo] : 0, g1 = seg ? seg[lo + 1] : rows;
-      const int local = brow - bstart[lo];
-      r0 = g0 + local * 32;
-      r1 = min(r0 + 32, g1);
-      if (PACKED) {
+  const int c = (blockIdx.y * 128 + tid) * 8;
+  for (int brow = blockIdx.x * kColBlockRows; brow < (blockIdx.x + 1) * kColBlockRows; ++brow) {
+    if (tid == 0) {
+      int r0 = -1, r1 = -1, word = 0, byte = 0, last = 0;
+      if (brow < bstart[nseg]) {
+        int lo = 0, hi = nseg;  // bstart[lo] <= brow < bstart[lo + 1]
+        while (hi - lo > 1) {
+          const int mid = (lo + hi) >> 1;
+          if (bstart[mid] <= brow) lo = mid; else hi = mid;
+        }
+        const int g0 = seg ? seg[lo] : 0, g1 = seg ? seg[lo + 1] : rows;
+        const int local = brow - bstart[lo];
+        r0 = g0 + local * 32;
+        r1 = min(r0 + 32, g1);
         word = wstart[lo] + local / 4;
         byte = local % 4;
         last = (brow == bstart[lo + 1] - 1);
       }
+      s_r0 = r0;
+      s_r1 = r1;
+      s_word = word;
+      s_byte = byte;
+      s_last = last;
     }
-    s_r0 = r0;
-    s_r1 = r1;
-    s_word = word;
-    s_byte = byte;
-    s_last = last;
-  }
-  __syncthreads();
-  const int r0 = s_r0, r1 = s_r1;
-  if (r0 < 0) return;
-  const int c = (blockIdx.y * 128 + tid) * 2;
-  if (c >= C) return;
-  float v0[32], v1[32];
-  float a0 = 0.0f, a1 = 0.0f;
+    __syncthreads();
+    const int r0 = s_r0, r1 = s_r1, word = s_word, byte = s_byte, last = s_last;
+    __syncthreads();
+    if (r0 < 0) break;
+    if (c >= C) continue;
+    float amax[8];
 #pragma unroll
-  for (int i = 0; i < 32; ++i) {
-    v0[i] = 0.0f;
-    v1[i] = 0.0f;
-    if (r0 + i < r1) {
-      const __nv_bfloat162 h = *reinterpret_cast<const __nv_bfloat162*>(src + (size_t)(r0 + i) * C + c);
-      v0[i] = __low2float(h);
-      v1[i] = __high2float(h);
-    }
-    a0 = fmaxf(a0, fabsf(v0[i]));
-    a1 = fmaxf(a1, fabsf(v1[i]));
-  }
-  const int s0 = e8m0_exponent(a0), s1 = e8m0_exponent(a1);
-  const float m0 = pow2_neg(s0), m1 = pow2_neg(s1);
+    for (int j = 0; j < 8; ++j) amax[j] = 0.0f;
+#pragma unroll 8
+    for (int i = 0; i < 32; ++i) {
+      if (r0 + i < r1) {
+        float v[8];
+        Vec16<__nv_bfloat16>::load(src + (size_t)(r0 + i) * C + c, v);
 #pragma unroll
-  for (int i = 0; i < 32; ++i)
-    if (r0 + i < r1)
-      *reinterpret_cast<uint16_t*>(q + (size_t)(r0 + i) * C + c) =
-          static_cast<uint16_t>(e4m3(v0[i] * m0) | (e4m3(v1[i] * m1) << 8));
-  if (!PACKED) {
-    *reinterpret_cast<uint16_t*>(sc + (size_t)brow * C + c) = static_cast<uint16_t>((s0 + 127) | ((s1 + 127) << 8));
-  } else {
-    uint8_t* w0 = sc + ((size_t)s_word * C + c) * 4;
-    w0[s_byte] = static_cast<uint8_t>(s0 + 127);
-    w0[4 + s_byte] = static_cast<uint8_t>(s1 + 127);
-    if (s_last)
-      for (int j = s_byte + 1; j < 4; ++j) {
-        w0[j] = 127;
-        w0[4 + j] = 127;
+        for (int j = 0; j < 8; ++j) amax[j] = fmaxf(amax[j], fabsf(v[j]));
       }
+    }
+    int sx[8];
+    float m[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      sx[j] = e8m0_exponent(amax[j]);
+      m[j] = pow2_neg(sx[j]);
+    }
+#pragma unroll 8
+    for (int i = 0; i < 32; ++i) {
+      if (r0 + i < r1) {
+        float v[8];
+        Vec16<__nv_bfloat16>::load(src + (size_t)(r0 + i) * C + c, v);
+        uint32_t lo = 0, hi = 0;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          lo |= e4m3(v[j] * m[j]) << (8 * j);
+          hi |= e4m3(v[4 + j] * m[4 + j]) << (8 * j);
+        }
+        *reinterpret_cast<uint2*>(q + (size_t)(r0 + i) * C + c) = make_uint2(lo, hi);
+      }
+    }
+    if (!PACKED) {
+      uint32_t lo = 0, hi = 0;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        lo |= static_cast<uint32_t>(sx[j] + 127) << (8 * j);
+        hi |= static_cast<uint32_t>(sx[4 + j] + 127) << (8 * j);
+      }
+      *reinterpret_cast<uint2*>(sc + (size_t)brow * C + c) = make_uint2(lo, hi);
+    } else {
+      uint8_t* w = sc + ((size_t)word * C + c) * 4;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        w[4 * j + byte] = static_cast<uint8_t>(sx[j] + 127);
+        if (last)
+          for (int b = byte + 1; b < 4; ++b) w[4 * j + b] = 127;
+      }
+    }
   }
 }
 
@@ -191,7 +213,8 @@ cudaError_t launch_mxfp8_quant_cols(const void* src, int rows, int C, const int3
   const int nseg_eff = seg ? nseg : 1;
   const long max_brows = (rows + 31) / 32 + nseg_eff;
   if (rows == 0) return cudaSuccess;
-  dim3 grid(static_cast<unsigned>(max_brows), static_cast<unsigned>((C / 2 + 127) / 128));
+  dim3 grid(static_cast<unsigned>((max_brows + kColBlockRows - 1) / kColBlockRows),
+            static_cast<unsigned>((C + 1023) / 1024));
   const size_t smem = 2 * (nseg_eff + 1) * sizeof(int);
   if (packed)
     MOE_COUNTED quant_cols_kernel<true><<<grid, 128, smem, st>>>(static_cast<const __nv_bfloat16*>(src), rows, C,

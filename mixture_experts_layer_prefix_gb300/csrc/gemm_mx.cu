@@ -331,11 +331,24 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         for (int c = half * 4; c < half * 4 + 4; ++c) store_chunk<KIND>(p, tl, r_tile, c, z);
         continue;
       }
+      if (KIND == DGRAD2) {
+        // pull this row's h_g / h_u chunks into L2 while the MMAs run
+        const int row = tl.m0 + r_tile;
+        if (row < tl.row_end) {
+          const __nv_bfloat16* h = static_cast<const __nv_bfloat16*>(p.aux) + (size_t)row * 2 * p.f;
+          for (int c = half * 4; c < half * 4 + 4; ++c) {
+            const int n = tl.n_idx * BN + c * 32;
+            if (n >= p.N) continue;
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(h + n));
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(h + p.f + n));
+          }
+        }
+      }
       if (!wait_bar(&sm->tfull, acc_it & 1u, &sm->abort_flag, p.err)) break;
       ptx::tc_fence_after();
       const uint32_t tbase = tmem + (static_cast<uint32_t>(q * 32) << 16);
       if (KIND == DGRAD2) {
-        epilogue_tile<KIND>(p, tl, tbase, r_tile, half * 4, half * 4 + 4, false);
+        epilogue_tile<KIND, true>(p, tl, tbase, r_tile, half * 4, half * 4 + 4, false);
         ptx::tc_fence_before();
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(&sm->tempty);
@@ -374,6 +387,7 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
               store_bf16x32(h + n, hg);
               store_bf16x32(h + p.f + n, hu);
               store_bf16x32(ao + n, av);
+              if (p.qout) quant_chunk_bf16(p, row, p.f, n, av);
             }
           }
         } else {
@@ -497,9 +511,10 @@ cudaError_t mx_mlp_fwd(const void* x_perm, const void* wg, const void* wu, const
     return cudaErrorInvalidValue;
   p.N = f; p.n_tiles = (f + 127) / 128; p.out0 = h; p.out1 = a;
   p.sfa = xq.s; p.sfb0 = wgq.s; p.sfb1 = wuq.s;
+  p.qout = aq.q; p.qsc = aq.s;  // the epilogue also quantises A along f for GEMM2
   if ((e = launch<FPROP1>(mA, mB0, mB1, p, ((long)(R + BM - 1) / BM + E) * p.n_tiles, st)) != cudaSuccess) return e;
-  // GEMM2 along f: A rows, w_down columns
-  if ((e = launch_mxfp8_quant_rows(a, R, f, aq.q, aq.s, st)) != cudaSuccess) return e;
+  p.qout = nullptr; p.qsc = nullptr;
+  // GEMM2 along f: A rows (written by GEMM1's epilogue), w_down columns
   if (!map_2d(&mA, aq.q, U8, 1, f, R, 128, BM) || !map_3d(&mB0, wdq.q, U8, 1, d, f, E, 128, 128))
     return cudaErrorInvalidValue;
   p.N = d; p.n_tiles = (d + BN - 1) / BN; p.out0 = y; p.out1 = nullptr;
@@ -535,7 +550,9 @@ cudaError_t mx_mlp_bwd(const void* dy_perm, const void* x_perm, const void* h, c
     return cudaErrorInvalidValue;
   p.N = f; p.n_tiles = (f + BN - 1) / BN; p.out0 = dh; p.aux = h;
   p.sfa = dyr.s; p.sfb0 = wdr.s;
+  p.qout = dhr.q; p.qsc = dhr.s;  // the epilogue also quantises dh along 2f for the GEMM1 dgrad
   if ((e = launch<DGRAD2>(mA, mB0, mB0, p, ((long)(R + BM - 1) / BM + E) * p.n_tiles, st)) != cudaSuccess) return e;
+  p.qout = nullptr; p.qsc = nullptr;
 
   // dWd[e] = A_e^T dy_e (K = the expert's rows): A and dy quantised along rows per expert
   if ((e = launch_mxfp8_quant_cols(a, R, f, offsets, E, ac.q, ac.s, st, true)) != cudaSuccess) return e;
@@ -547,7 +564,6 @@ cudaError_t mx_mlp_bwd(const void* dy_perm, const void* x_perm, const void* h, c
   if ((e = launch<WGRAD2>(mA, mB0, mB0, p, (long)E * p.m_tiles * p.n_tiles, st)) != cudaSuccess) return e;
 
   // dx_perm = dh . [Wg | Wu]^T (K = 2f): dh rows, w_gate / w_up rows
-  if ((e = launch_mxfp8_quant_rows(dh, R, 2L * f, dhr.q, dhr.s, st)) != cudaSuccess) return e;
   if ((e = launch_mxfp8_quant_rows(wg, Ed, f, wgr.q, wgr.s, st)) != cudaSuccess) return e;
   if ((e = launch_mxfp8_quant_rows(wu, Ed, f, wur.q, wur.s, st)) != cudaSuccess) return e;
   if (!map_2d(&mA, dhr.q, U8, 1, 2L * f, R, 128, BM) || !map_3d(&mB0, wgr.q, U8, 1, f, d, E, 128, BN) ||

@@ -19,29 +19,14 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "mxfp8_common.cuh"
 
 namespace moe {
 namespace {
 
-// E8M0 exponent from the fp32 bits of amax (amax >= 0, finite).
-__device__ __forceinline__ int e8m0_exponent(float amax) {
-  const uint32_t b = __float_as_uint(amax);
-  const int ef = static_cast<int>((b >> 23) & 0xFFu);
-  if (ef == 0) return -127;                  // zero or subnormal: 2^e <= 2^-127
-  int s = (ef - 127) - 8;                    // amax in [2^e, 2^(e+1)), 448 = 1.75 * 2^8
-  if ((b & 0x7FFFFFu) > 0x600000u) s += 1;   // mantissa above 1.75: 2^(e-8) * 448 < amax
-  return s < -127 ? -127 : (s > 127 ? 127 : s);
-}
-
-// 2^-s as an exact fp32 (s in [-127, 127]; 2^-127 is subnormal).
-__device__ __forceinline__ float pow2_neg(int s) {
-  const int ef = 127 - s;
-  return ef >= 1 ? __uint_as_float(static_cast<uint32_t>(ef) << 23) : __uint_as_float(1u << 22);
-}
-
-__device__ __forceinline__ uint32_t e4m3(float v) {
-  return static_cast<uint32_t>(__nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3));
-}
+__device__ __forceinline__ int e8m0_exponent(float amax) { return mx_e8m0_exponent(amax); }
+__device__ __forceinline__ float pow2_neg(int s) { return mx_pow2_neg(s); }
+__device__ __forceinline__ uint32_t e4m3(float v) { return mx_e4m3(v); }
 
 __global__ void __launch_bounds__(256)
 quant_rows_kernel(const __nv_bfloat16* __restrict__ src, long nblocks, uint8_t* __restrict__ q,
@@ -52,20 +37,7 @@ quant_rows_kernel(const __nv_bfloat16* __restrict__ src, long nblocks, uint8_t* 
   const __nv_bfloat16* p = src + blk * 32;
 #pragma unroll
   for (int i = 0; i < 4; ++i) Vec16<__nv_bfloat16>::load(p + 8 * i, v + 8 * i);
-  float amax = 0.0f;
-#pragma unroll
-  for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
-  const int s = e8m0_exponent(amax);
-  const float m = pow2_neg(s);
-  uint32_t w[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i)
-    w[i] = e4m3(v[4 * i] * m) | (e4m3(v[4 * i + 1] * m) << 8) | (e4m3(v[4 * i + 2] * m) << 16) |
-           (e4m3(v[4 * i + 3] * m) << 24);
-  uint4* out = reinterpret_cast<uint4*>(q + blk * 32);
-  out[0] = make_uint4(w[0], w[1], w[2], w[3]);
-  out[1] = make_uint4(w[4], w[5], w[6], w[7]);
-  sc[blk] = static_cast<uint8_t>(s + 127);
+  mx_quant_block32(v, q + blk * 32, sc + blk);
 }
 
 // Block-row table: segment g owns block rows [bstart[g], bstart[g+1]).

@@ -1,0 +1,52 @@
+// mxfp8_common.cuh -- device helpers of the MXFP8 block format shared by the
+// quantisers and the GEMM epilogues that quantise their own outputs: E8M0
+// exponent of a block maximum, exact power-of-two scaling, E4M3 conversion.
+#pragma once
+
+#include <cuda_fp8.h>
+#include <stdint.h>
+
+namespace moe {
+
+// E8M0 exponent s = ceil(log2(amax / 448)) clamped to [-127, 127], from the
+// fp32 bits of amax (amax >= 0, finite); zero or subnormal amax gives -127.
+__device__ __forceinline__ int mx_e8m0_exponent(float amax) {
+  const uint32_t b = __float_as_uint(amax);
+  const int ef = static_cast<int>((b >> 23) & 0xFFu);
+  if (ef == 0) return -127;                  // zero or subnormal: 2^e <= 2^-127
+  int s = (ef - 127) - 8;                    // amax in [2^e, 2^(e+1)), 448 = 1.75 * 2^8
+  if ((b & 0x7FFFFFu) > 0x600000u) s += 1;   // mantissa above 1.75: 2^(e-8) * 448 < amax
+  return s < -127 ? -127 : (s > 127 ? 127 : s);
+}
+
+// 2^-s as an exact fp32 (s in [-127, 127]; 2^-127 is subnormal).
+__device__ __forceinline__ float mx_pow2_neg(int s) {
+  const int ef = 127 - s;
+  return ef >= 1 ? __uint_as_float(static_cast<uint32_t>(ef) << 23) : __uint_as_float(1u << 22);
+}
+
+// Round-to-nearest-even E4M3 code of v, saturated to +-448.
+__device__ __forceinline__ uint32_t mx_e4m3(float v) {
+  return static_cast<uint32_t>(__nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3));
+}
+
+// Quantise one block of 32 values: 32 E4M3 codes (16-byte aligned
+// destination) and one E8M0 byte.
+__device__ __forceinline__ void mx_quant_block32(const float* v, uint8_t* codes, uint8_t* scale) {
+  float amax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
+  const int s = mx_e8m0_exponent(amax);
+  const float m = mx_pow2_neg(s);
+  uint32_t w[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    w[i] = mx_e4m3(v[4 * i] * m) | (mx_e4m3(v[4 * i + 1] * m) << 8) | (mx_e4m3(v[4 * i + 2] * m) << 16) |
+           (mx_e4m3(v[4 * i + 3] * m) << 24);
+  uint4* out = reinterpret_cast<uint4*>(codes);
+  out[0] = make_uint4(w[0], w[1], w[2], w[3]);
+  out[1] = make_uint4(w[4], w[5], w[6], w[7]);
+  *scale = static_cast<uint8_t>(s + 127);
+}
+
+}  // namespace moe

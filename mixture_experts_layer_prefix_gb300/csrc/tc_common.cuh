@@ -8,6 +8,7 @@
 #include <cudaTypedefs.h>
 
 #include "common.cuh"
+#include "mxfp8_common.cuh"
 #include "tc_ptx.cuh"
 
 namespace moe {
@@ -32,6 +33,8 @@ struct Params {
   const uint8_t* sfa;      // MXFP8: scale bytes of A (layout per kind)
   const uint8_t* sfb0;     // MXFP8: scale bytes of B (gate / the only B)
   const uint8_t* sfb1;     // MXFP8: scale bytes of the second B (up)
+  uint8_t* qout;           // optional: the epilogue also writes its bf16 output
+  uint8_t* qsc;            //   quantised along rows (E4M3 codes, E8M0 per 32)
   int* err;
 };
 
@@ -170,10 +173,22 @@ __device__ __forceinline__ void load_bf16x32(const __nv_bfloat16* src, float* v)
   }
 }
 
+// Row quantisation of a 32-column chunk of a bf16 output (values rounded to
+// bf16 first: the GEMMs that read it see the stored values). Codes go to
+// qout[row][col..col+32), the scale to qsc[row][col/32] of a [rows][ld] matrix.
+__device__ __forceinline__ void quant_chunk_bf16(const Params& p, long row, int ld, int col, const float* v) {
+  float r[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) r[i] = __bfloat162float(__float2bfloat16_rn(v[i]));
+  mx_quant_block32(r, p.qout + (size_t)row * ld + col, p.qsc + (size_t)row * (ld / 32) + col / 32);
+}
+
 // Epilogue of one tile for the rows of one TMEM lane quadrant: accumulator
 // chunks [c_beg, c_end) of 32 columns (FPROP1: gate chunk c with up chunk
 // c + 4). `zero` writes zeros without reading TMEM (wgrad of an empty expert).
-template <int KIND>
+// QUANT: also write the MXFP8 row quantisation of A (FPROP1) or dh (DGRAD2)
+// when p.qout is set.
+template <int KIND, bool QUANT = false>
 __device__ __forceinline__ void epilogue_tile(const Params& p, const Tile& tl, uint32_t tbase, int row_in_tile,
                                               int c_beg, int c_end, bool zero) {
   if (Traits<KIND>::kragged) {
@@ -224,6 +239,7 @@ __device__ __forceinline__ void epilogue_tile(const Params& p, const Tile& tl, u
       store_bf16x32(h + n, hg);
       store_bf16x32(h + p.f + n, hu);
       store_bf16x32(static_cast<__nv_bfloat16*>(p.out1) + (size_t)row * p.f + n, av);
+      if (QUANT && p.qout) quant_chunk_bf16(p, row, p.f, n, av);
     }
   } else if (KIND == DGRAD2) {
     // dh_g = da * h_u * silu'(h_g), dh_u = da * silu(h_g); h is loaded before
@@ -253,6 +269,10 @@ __device__ __forceinline__ void epilogue_tile(const Params& p, const Tile& tl, u
       }
       store_bf16x32(dh + n, dg);
       store_bf16x32(dh + p.f + n, du);
+      if (QUANT && p.qout) {
+        quant_chunk_bf16(p, row, 2 * p.f, n, dg);
+        quant_chunk_bf16(p, row, 2 * p.f, p.f + n, du);
+      }
     }
   } else if (KIND == ROUTER) {
     const int n0 = tl.n_idx * BN;

@@ -50,14 +50,24 @@ topk_hist_kernel(const float* __restrict__ logits, int T, int E, int k, int nchu
   __syncwarp();
 
   const int t_end = min(T, (c + 1) * kTokensPerChunk);
+  // the next token's logits are loaded while this token's experts are selected
+  float nxt[NV];
+  auto load_row = [&](int t) {
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+      const int e = lane + 32 * i;
+      nxt[i] = e < E ? __ldg(logits + (size_t)t * E + e) : 0.0f;
+    }
+  };
+  if (c * kTokensPerChunk < t_end) load_row(c * kTokensPerChunk);
   for (int t = c * kTokensPerChunk; t < t_end; ++t) {
-    const float* l = logits + (size_t)t * E;
     uint32_t key[NV];
 #pragma unroll
     for (int i = 0; i < NV; ++i) {
       const int e = lane + 32 * i;
-      key[i] = e < E ? ordered_key(__ldg(l + e)) : 0u;
+      key[i] = e < E ? ordered_key(nxt[i]) : 0u;
     }
+    if (t + 1 < t_end) load_row(t + 1);
     uint32_t taken = 0u;
     int my_idx = 0;
     float my_val = 0.0f, top_val = 0.0f;

@@ -15,15 +15,16 @@
 //               replicated to all four lane quadrants), then four
 //               tcgen05.mma kind::mxf8f6f4 block_scale (M=128, N=256, K=32,
 //               scale-factor id = K step).
-//   warps 2..9  epilogue, two warps per TMEM lane quadrant. The accumulator
-//               is single-buffered (the scale ring takes the columns a second
-//               buffer would need), so each warp first copies its 128 columns
-//               into registers and releases the accumulator, then computes
-//               and stores; the next tile's MMAs overlap the stores.
-// TMEM: accumulator columns [0,256); scales of stage s: A at 256 + 4s, B at
-// 272 + 8s. Shared scale staging of a stage: A 512 B (row r of the copy = tile
-// rows r, 32+r, 64+r, 96+r), then B 2 x 512 B (copy h row r = tile columns
-// 128h + r, +32, +64, +96).
+//   warps 2..9  epilogue, two warps per TMEM lane quadrant.
+// Output tiles are 128 rows by TBN columns. With TBN = 128 two accumulators
+// fit next to the scale ring and alternate, as in the bf16 GEMMs. GEMM1
+// (TBN = 256: 128 gate + 128 up columns) has one accumulator, so each warp
+// first copies its 128 columns into registers and releases it, then computes
+// and stores while the next tile's MMAs run.
+// TMEM: accumulators in columns [0,256); scales of stage s: A at 256 + 4s,
+// B at 272 + (TBN/32)s. Shared scale staging of a stage: A 512 B (row r of the
+// copy = tile rows r, 32+r, 64+r, 96+r), then B TBN/128 x 512 B (copy h row r
+// = tile columns 128h + r, +32, +64, +96).
 #include "kernels.h"
 #include "tc_common.cuh"
 
@@ -34,20 +35,30 @@ namespace {
 
 constexpr int BK = 128;  // E4M3 elements (bytes) per stage along K
 constexpr int A_BYTES = BM * BK;
-constexpr int B_BYTES = BN * BK;
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int BOX_BYTES = 128 * 128;  // one 128 (MN) x 128 (K) box
-constexpr int SC_BYTES = 512 + 1024;  // scale staging per stage
 constexpr int NUM_EPI_WARPS = 8;
 constexpr int NUM_THREADS = 64 + 32 * NUM_EPI_WARPS;
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t SFA_COL = 256, SFB_COL = 272;
+
+// Tile geometry for a tile width TBN (columns of B / of the output tile):
+// TBN = 256 uses one accumulator (the scale ring needs the columns a second
+// one would take); TBN = 128 fits two and double-buffers like the bf16 GEMMs.
+template <int TBN> struct Geo {
+  static constexpr int B_BYTES = TBN * BK;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int SCB = TBN / 128;             // 32x128b copies of B scales per stage
+  static constexpr int SC_BYTES = 512 + 512 * SCB;  // scale staging per stage
+  static constexpr int ACC = TBN == 128 ? 2 : 1;    // accumulator buffers
+  static constexpr uint32_t SFA_COL = 256;          // after the accumulators
+  static constexpr uint32_t SFB_COL = SFA_COL + 4 * STAGES;
+  static constexpr uint32_t SFB_STRIDE = TBN / 32;  // TMEM columns of B scales per stage
+};
 
 struct Smem {
   uint64_t full[STAGES];
   uint64_t empty[STAGES];
-  uint64_t tfull;
-  uint64_t tempty;
+  uint64_t tfull[2];
+  uint64_t tempty[2];
   uint64_t drain;
   uint32_t tmem_base;
   int abort_flag;
@@ -77,9 +88,9 @@ __device__ __forceinline__ void tmem_cp_32x128b_x4(uint32_t taddr, uint64_t desc
 }
 
 // bf16 store of one 32-column chunk of a plain or wgrad output.
-template <int KIND>
+template <int KIND, int TBN>
 __device__ __forceinline__ void store_chunk(const Params& p, const Tile& tl, int r_tile, int c, const float* v) {
-  const int n = tl.n_idx * BN + c * 32;
+  const int n = tl.n_idx * TBN + c * 32;
   if (Traits<KIND>::kragged) {
     const int m = tl.m0 + r_tile;
     if (m >= p.M || n >= p.N) return;
@@ -95,15 +106,17 @@ __device__ __forceinline__ void store_chunk(const Params& p, const Tile& tl, int
   }
 }
 
-template <int KIND>
+template <int KIND, int TBN>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
                const __grid_constant__ CUtensorMap tmB1, const Params p) {
   using Tr = Traits<KIND>;
+  using G = Geo<TBN>;
+  static_assert(KIND != FPROP1 || TBN == 256, "GEMM1 tiles pair 128 gate with 128 up columns");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sc_area = smem + STAGES * STAGE_BYTES;
-  Smem* sm = reinterpret_cast<Smem*>(sc_area + STAGES * SC_BYTES);
+  uint8_t* sc_area = smem + STAGES * G::STAGE_BYTES;
+  Smem* sm = reinterpret_cast<Smem*>(sc_area + STAGES * G::SC_BYTES);
   int* offs = reinterpret_cast<int*>(sm + 1);
   int* tstart = offs + (p.E + 1);
   int* wstart = tstart + (p.E + 1);  // wgrad: first packed scale word row of each expert segment
@@ -130,8 +143,10 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       ptx::mbar_init(&sm->full[s], 1);
       ptx::mbar_init(&sm->empty[s], 1);
     }
-    ptx::mbar_init(&sm->tfull, 1);
-    ptx::mbar_init(&sm->tempty, NUM_EPI_WARPS);
+    for (int b = 0; b < 2; ++b) {
+      ptx::mbar_init(&sm->tfull[b], 1);
+      ptx::mbar_init(&sm->tempty[b], NUM_EPI_WARPS);
+    }
     ptx::mbar_init(&sm->drain, 1);
     sm->abort_flag = 0;
     ptx::fence_mbar_init();
@@ -166,7 +181,7 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         uint64_t* fb = &sm->full[s];
         const int k0 = kb * BK;
         // ---- scales: A rows of the tile, then B columns
-        uint8_t* sa = sc_area + s * SC_BYTES;
+        uint8_t* sa = sc_area + s * G::SC_BYTES;
         uint8_t* sb = sa + 512;
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -185,7 +200,7 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           cp_async4(sa + lane * 16 + i * 4, src, valid);
         }
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
+        for (int c = 0; c < TBN / 32; ++c) {
           const int nt = lane + 32 * c;  // tile column
           const uint8_t* src = p.sfb0;
           bool valid = false;
@@ -194,22 +209,22 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             valid = n < p.f;
             if (valid) src = (nt < 128 ? p.sfb0 : p.sfb1) + (((size_t)tl.e * p.d + k0) / 128 * p.f + n) * 4;
           } else if (KIND == FPROP2) {  // [E*f/128][d] words
-            const int n = tl.n_idx * BN + nt;
+            const int n = tl.n_idx * TBN + nt;
             valid = n < p.d;
             if (valid) src = p.sfb0 + (((size_t)tl.e * p.f + k0) / 128 * p.d + n) * 4;
           } else if (KIND == DGRAD2) {  // rows of w_down along d: [E*f][d/32] bytes
-            const int n = tl.n_idx * BN + nt;
+            const int n = tl.n_idx * TBN + nt;
             valid = n < p.f;
             if (valid) src = p.sfb0 + ((size_t)tl.e * p.f + n) * (p.d / 32) + k0 / 32;
           } else if (KIND == DGRAD1) {  // rows of w_gate / w_up along f: [E*d][f/32] bytes
-            const int n = tl.n_idx * BN + nt;
+            const int n = tl.n_idx * TBN + nt;
             valid = n < p.d;
             if (valid) {
               const int kk = k0 < p.f ? k0 : k0 - p.f;
               src = (k0 < p.f ? p.sfb0 : p.sfb1) + ((size_t)tl.e * p.d + n) * (p.f / 32) + kk / 32;
             }
           } else {  // wgrad: columns quantised along the expert's rows, [words][N] words
-            const int n = tl.n_idx * BN + nt;
+            const int n = tl.n_idx * TBN + nt;
             valid = n < p.N;
             if (valid) src = p.sfb0 + ((size_t)(wstart[tl.e] + kb) * p.N + n) * 4;
           }
@@ -219,9 +234,9 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         __syncwarp();
         if (lane == 0) {
           // ---- E4M3 tiles
-          uint8_t* a = smem + s * STAGE_BYTES;
+          uint8_t* a = smem + s * G::STAGE_BYTES;
           uint8_t* b = a + A_BYTES;
-          ptx::mbar_expect_tx(fb, STAGE_BYTES);
+          ptx::mbar_expect_tx(fb, G::STAGE_BYTES);
           if (KIND == FPROP1) {
             ptx::tma_load_2d(a, &tmA, fb, k0, tl.m0);
             const int n0 = tl.n_idx * 128;
@@ -229,22 +244,22 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             ptx::tma_load_3d(b + BOX_BYTES, &tmB1, fb, n0, k0, tl.e);
           } else if (KIND == FPROP2) {
             ptx::tma_load_2d(a, &tmA, fb, k0, tl.m0);
-            const int n0 = tl.n_idx * BN;
-            ptx::tma_load_3d(b, &tmB0, fb, n0, k0, tl.e);
-            ptx::tma_load_3d(b + BOX_BYTES, &tmB0, fb, n0 + 128, k0, tl.e);
+            const int n0 = tl.n_idx * TBN;
+#pragma unroll
+            for (int j = 0; j < G::SCB; ++j) ptx::tma_load_3d(b + j * BOX_BYTES, &tmB0, fb, n0 + 128 * j, k0, tl.e);
           } else if (KIND == DGRAD2) {
             ptx::tma_load_2d(a, &tmA, fb, k0, tl.m0);
-            ptx::tma_load_3d(b, &tmB0, fb, k0, tl.n_idx * BN, tl.e);
+            ptx::tma_load_3d(b, &tmB0, fb, k0, tl.n_idx * TBN, tl.e);
           } else if (KIND == DGRAD1) {
             ptx::tma_load_2d(a, &tmA, fb, k0, tl.m0);
-            if (k0 < p.f) ptx::tma_load_3d(b, &tmB0, fb, k0, tl.n_idx * BN, tl.e);
-            else ptx::tma_load_3d(b, &tmB1, fb, k0 - p.f, tl.n_idx * BN, tl.e);
+            if (k0 < p.f) ptx::tma_load_3d(b, &tmB0, fb, k0, tl.n_idx * TBN, tl.e);
+            else ptx::tma_load_3d(b, &tmB1, fb, k0 - p.f, tl.n_idx * TBN, tl.e);
           } else {  // WGRAD2 / WGRAD1: K runs over the expert's rows
             const int row = tl.k_row0 + k0;
             ptx::tma_load_2d(a, &tmA, fb, tl.m0, row);
-            const int n0 = tl.n_idx * BN;
-            ptx::tma_load_2d(b, &tmB0, fb, n0, row);
-            ptx::tma_load_2d(b + BOX_BYTES, &tmB0, fb, n0 + 128, row);
+            const int n0 = tl.n_idx * TBN;
+#pragma unroll
+            for (int j = 0; j < G::SCB; ++j) ptx::tma_load_2d(b + j * BOX_BYTES, &tmB0, fb, n0 + 128 * j, row);
           }
         }
         __syncwarp();
@@ -265,14 +280,17 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
       const Tile tl = decode<KIND, BK>(t, p, offs, tstart);
       if (tl.nkb == 0) continue;
-      if (!wait_bar(&sm->tempty, (acc_it & 1u) ^ 1u, &sm->abort_flag, p.err)) { ok = false; break; }
+      const int buf = G::ACC == 2 ? (acc_it & 1) : 0;
+      const uint32_t aph = (G::ACC == 2 ? (acc_it >> 1) : acc_it) & 1u;
+      if (!wait_bar(&sm->tempty[buf], aph ^ 1u, &sm->abort_flag, p.err)) { ok = false; break; }
       ptx::tc_fence_after();
+      const uint32_t d_tmem = tmem + static_cast<uint32_t>(buf * TBN);
       for (int kb = 0; kb < tl.nkb; ++kb, ++it) {
         const int s = it % STAGES;
         const uint32_t ph = (it / STAGES) & 1u;
         if (!wait_bar(&sm->full[s], ph, &sm->abort_flag, p.err)) { ok = false; break; }
         ptx::tc_fence_after();
-        uint8_t* a = smem + s * STAGE_BYTES;
+        uint8_t* a = smem + s * G::STAGE_BYTES;
         int nks = BK / 32;
         if (Tr::kragged) {
           const int valid = tl.row_end - (tl.k_row0 + kb * BK);
@@ -288,26 +306,26 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         ptx::fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-          const uint32_t sa = ptx::smem_u32(sc_area + s * SC_BYTES);
-          tmem_cp_32x128b_x4(tmem + SFA_COL + 4 * s, cp_desc(sa));
-          tmem_cp_32x128b_x4(tmem + SFB_COL + 8 * s, cp_desc(sa + 512));
-          tmem_cp_32x128b_x4(tmem + SFB_COL + 8 * s + 4, cp_desc(sa + 1024));
+          const uint32_t sa = ptx::smem_u32(sc_area + s * G::SC_BYTES);
+          const uint32_t sfa = tmem + G::SFA_COL + 4 * s, sfb = tmem + G::SFB_COL + G::SFB_STRIDE * s;
+          tmem_cp_32x128b_x4(sfa, cp_desc(sa));
+#pragma unroll
+          for (int j = 0; j < G::SCB; ++j) tmem_cp_32x128b_x4(sfb + 4 * j, cp_desc(sa + 512 + 512 * j));
           const uint32_t a_addr = ptx::smem_u32(a), b_addr = a_addr + A_BYTES;
           for (int ks = 0; ks < nks; ++ks) {
             const uint64_t ad = Tr::a_mn ? ptx::smem_desc_sw128(a_addr + ks * 4096, BOX_BYTES, 1024)
                                          : ptx::smem_desc_sw128(a_addr + ks * 32, 16, 1024);
             const uint64_t bd = Tr::b_mn ? ptx::smem_desc_sw128(b_addr + ks * 4096, BOX_BYTES, 1024)
                                          : ptx::smem_desc_sw128(b_addr + ks * 32, 16, 1024);
-            const uint32_t idesc = ptx::idesc_mxf8_f32(BM, BN, Tr::a_mn ? 1 : 0, Tr::b_mn ? 1 : 0, ks, ks);
-            ptx::mma_mxf8(tmem, ad, bd, idesc, tmem + SFA_COL + 4 * s, tmem + SFB_COL + 8 * s,
-                          (kb > 0 || ks > 0) ? 1u : 0u);
+            const uint32_t idesc = ptx::idesc_mxf8_f32(BM, TBN, Tr::a_mn ? 1 : 0, Tr::b_mn ? 1 : 0, ks, ks);
+            ptx::mma_mxf8(d_tmem, ad, bd, idesc, sfa, sfb, (kb > 0 || ks > 0) ? 1u : 0u);
           }
           ptx::mma_commit(&sm->empty[s]);
         }
         __syncwarp();
       }
       if (!ok) break;
-      if (lane == 0) ptx::mma_commit(&sm->tfull);
+      if (lane == 0) ptx::mma_commit(&sm->tfull[buf]);
       __syncwarp();
       ++acc_it;
     }
@@ -321,6 +339,7 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     // ============================================================ epilogue
     const int ew = warp - 2, q = warp & 3, half = ew >> 2;
     const int r_tile = q * 32 + lane;
+    constexpr int NC = KIND == FPROP1 ? 4 : TBN / 32;  // chunks of the tile (FPROP1: gate/up pairs)
     uint32_t acc_it = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
       const Tile tl = decode<KIND, BK>(t, p, offs, tstart);
@@ -328,7 +347,7 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         float z[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) z[i] = 0.0f;
-        for (int c = half * 4; c < half * 4 + 4; ++c) store_chunk<KIND>(p, tl, r_tile, c, z);
+        for (int c = half * NC / 2; c < (half + 1) * NC / 2; ++c) store_chunk<KIND, TBN>(p, tl, r_tile, c, z);
         continue;
       }
       if (KIND == DGRAD2) {
@@ -336,24 +355,27 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         const int row = tl.m0 + r_tile;
         if (row < tl.row_end) {
           const __nv_bfloat16* h = static_cast<const __nv_bfloat16*>(p.aux) + (size_t)row * 2 * p.f;
-          for (int c = half * 4; c < half * 4 + 4; ++c) {
-            const int n = tl.n_idx * BN + c * 32;
+          for (int c = half * NC / 2; c < (half + 1) * NC / 2; ++c) {
+            const int n = tl.n_idx * TBN + c * 32;
             if (n >= p.N) continue;
             asm volatile("prefetch.global.L2 [%0];" ::"l"(h + n));
             asm volatile("prefetch.global.L2 [%0];" ::"l"(h + p.f + n));
           }
         }
       }
-      if (!wait_bar(&sm->tfull, acc_it & 1u, &sm->abort_flag, p.err)) break;
+      const int buf = G::ACC == 2 ? (acc_it & 1) : 0;
+      const uint32_t aph = (G::ACC == 2 ? (acc_it >> 1) : acc_it) & 1u;
+      if (!wait_bar(&sm->tfull[buf], aph, &sm->abort_flag, p.err)) break;
       ptx::tc_fence_after();
-      const uint32_t tbase = tmem + (static_cast<uint32_t>(q * 32) << 16);
-      if (KIND == DGRAD2) {
-        epilogue_tile<KIND, true>(p, tl, tbase, r_tile, half * 4, half * 4 + 4, false);
+      const uint32_t tbase = tmem + static_cast<uint32_t>(buf * TBN) + (static_cast<uint32_t>(q * 32) << 16);
+      if (G::ACC == 2 || KIND == DGRAD2) {
+        // double-buffered (or too many registers to drain first): epilogue straight from TMEM
+        epilogue_tile<KIND, true, TBN>(p, tl, tbase, r_tile, half * NC / 2, (half + 1) * NC / 2, false);
         ptx::tc_fence_before();
         __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(&sm->tempty);
+        if (lane == 0) ptx::mbar_arrive(&sm->tempty[buf]);
       } else {
-        // copy this warp's 128 accumulator columns out, release the accumulator, then store
+        // single accumulator: copy this warp's 128 columns out, release it, then store
         uint32_t acc[4][32];
         if (KIND == FPROP1) {
           ptx::tmem_ld32(tbase + (2 * half) * 32, acc[0]);
@@ -367,7 +389,7 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         ptx::tmem_wait_ld();
         ptx::tc_fence_before();
         __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(&sm->tempty);
+        if (lane == 0) ptx::mbar_arrive(&sm->tempty[buf]);
         if (KIND == FPROP1) {
           const int row = tl.m0 + r_tile;
           if (row < tl.row_end) {
@@ -396,7 +418,7 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             float v[32];
 #pragma unroll
             for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(acc[c][i]);
-            store_chunk<KIND>(p, tl, r_tile, 4 * half + c, v);
+            store_chunk<KIND, TBN>(p, tl, r_tile, 4 * half + c, v);
           }
         }
       }
@@ -412,22 +434,28 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   }
 }
 
+template <int TBN>
 size_t smem_bytes(int E) {
-  return 1024 + STAGES * STAGE_BYTES + STAGES * SC_BYTES + sizeof(Smem) + 3 * (E + 1) * sizeof(int) + 64;
+  return 1024 + STAGES * Geo<TBN>::STAGE_BYTES + STAGES * Geo<TBN>::SC_BYTES + sizeof(Smem) +
+         3 * (E + 1) * sizeof(int) + 64;
 }
 
-template <int KIND>
+template <int KIND, int TBN>
 cudaError_t launch(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1, const Params& p,
                    long max_tiles, cudaStream_t st) {
   if (max_tiles <= 0) return cudaSuccess;
-  const size_t smem = smem_bytes(p.E);
-  cudaError_t e = cudaFuncSetAttribute(mx_gemm_kernel<KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  const size_t smem = smem_bytes<TBN>(p.E);
+  cudaError_t e = cudaFuncSetAttribute(mx_gemm_kernel<KIND, TBN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   const int grid = static_cast<int>(max_tiles < sm_count() ? max_tiles : sm_count());
-  MOE_COUNTED mx_gemm_kernel<KIND><<<grid, NUM_THREADS, smem, st>>>(a, b0, b1, p);
+  MOE_COUNTED mx_gemm_kernel<KIND, TBN><<<grid, NUM_THREADS, smem, st>>>(a, b0, b1, p);
   return cudaGetLastError();
 }
+
+// Output tile widths: GEMM1 pairs 128 gate with 128 up columns (256); the
+// others use 128-column tiles with a double-buffered accumulator.
+constexpr int kN_FPROP1 = 256, kN_FPROP2 = 128, kN_DGRAD2 = 128, kN_DGRAD1 = 256, kN_WGRAD = 128;
 
 constexpr CUtensorMapDataType U8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
 
@@ -512,14 +540,15 @@ cudaError_t mx_mlp_fwd(const void* x_perm, const void* wg, const void* wu, const
   p.N = f; p.n_tiles = (f + 127) / 128; p.out0 = h; p.out1 = a;
   p.sfa = xq.s; p.sfb0 = wgq.s; p.sfb1 = wuq.s;
   p.qout = aq.q; p.qsc = aq.s;  // the epilogue also quantises A along f for GEMM2
-  if ((e = launch<FPROP1>(mA, mB0, mB1, p, ((long)(R + BM - 1) / BM + E) * p.n_tiles, st)) != cudaSuccess) return e;
+  if ((e = launch<FPROP1, kN_FPROP1>(mA, mB0, mB1, p, ((long)(R + BM - 1) / BM + E) * p.n_tiles, st)) != cudaSuccess)
+    return e;
   p.qout = nullptr; p.qsc = nullptr;
   // GEMM2 along f: A rows (written by GEMM1's epilogue), w_down columns
   if (!map_2d(&mA, aq.q, U8, 1, f, R, 128, BM) || !map_3d(&mB0, wdq.q, U8, 1, d, f, E, 128, 128))
     return cudaErrorInvalidValue;
-  p.N = d; p.n_tiles = (d + BN - 1) / BN; p.out0 = y; p.out1 = nullptr;
+  p.N = d; p.n_tiles = (d + kN_FPROP2 - 1) / kN_FPROP2; p.out0 = y; p.out1 = nullptr;
   p.sfa = aq.s; p.sfb0 = wdq.s; p.sfb1 = nullptr;
-  return launch<FPROP2>(mA, mB0, mB0, p, ((long)(R + BM - 1) / BM + E) * p.n_tiles, st);
+  return launch<FPROP2, kN_FPROP2>(mA, mB0, mB0, p, ((long)(R + BM - 1) / BM + E) * p.n_tiles, st);
 }
 
 cudaError_t mx_mlp_bwd(const void* dy_perm, const void* x_perm, const void* h, const void* a, const void* wg,
@@ -546,12 +575,13 @@ cudaError_t mx_mlp_bwd(const void* dy_perm, const void* x_perm, const void* h, c
   // dA = dy . Wd^T (K = d): dy rows, w_down rows; SwiGLU backward fused -> dh
   if ((e = launch_mxfp8_quant_rows(dy_perm, R, d, dyr.q, dyr.s, st)) != cudaSuccess) return e;
   if ((e = launch_mxfp8_quant_rows(wd, Ef, d, wdr.q, wdr.s, st)) != cudaSuccess) return e;
-  if (!map_2d(&mA, dyr.q, U8, 1, d, R, 128, BM) || !map_3d(&mB0, wdr.q, U8, 1, d, f, E, 128, BN))
+  if (!map_2d(&mA, dyr.q, U8, 1, d, R, 128, BM) || !map_3d(&mB0, wdr.q, U8, 1, d, f, E, 128, kN_DGRAD2))
     return cudaErrorInvalidValue;
-  p.N = f; p.n_tiles = (f + BN - 1) / BN; p.out0 = dh; p.aux = h;
+  p.N = f; p.n_tiles = (f + kN_DGRAD2 - 1) / kN_DGRAD2; p.out0 = dh; p.aux = h;
   p.sfa = dyr.s; p.sfb0 = wdr.s;
   p.qout = dhr.q; p.qsc = dhr.s;  // the epilogue also quantises dh along 2f for the GEMM1 dgrad
-  if ((e = launch<DGRAD2>(mA, mB0, mB0, p, ((long)(R + BM - 1) / BM + E) * p.n_tiles, st)) != cudaSuccess) return e;
+  if ((e = launch<DGRAD2, kN_DGRAD2>(mA, mB0, mB0, p, ((long)(R + BM - 1) / BM + E) * p.n_tiles, st)) != cudaSuccess)
+    return e;
   p.qout = nullptr; p.qsc = nullptr;
 
   // dWd[e] = A_e^T dy_e (K = the expert's rows): A and dy quantised along rows per expert
@@ -559,28 +589,30 @@ cudaError_t mx_mlp_bwd(const void* dy_perm, const void* x_perm, const void* h, c
   if ((e = launch_mxfp8_quant_cols(dy_perm, R, d, offsets, E, dyc.q, dyc.s, st, true)) != cudaSuccess) return e;
   if (!map_2d(&mA, ac.q, U8, 1, f, R, 128, 128) || !map_2d(&mB0, dyc.q, U8, 1, d, R, 128, 128))
     return cudaErrorInvalidValue;
-  p.M = f; p.N = d; p.m_tiles = (f + BM - 1) / BM; p.n_tiles = (d + BN - 1) / BN; p.out0 = dwd; p.aux = nullptr;
+  p.M = f; p.N = d; p.m_tiles = (f + BM - 1) / BM; p.n_tiles = (d + kN_WGRAD - 1) / kN_WGRAD; p.out0 = dwd;
+  p.aux = nullptr;
   p.sfa = ac.s; p.sfb0 = dyc.s;
-  if ((e = launch<WGRAD2>(mA, mB0, mB0, p, (long)E * p.m_tiles * p.n_tiles, st)) != cudaSuccess) return e;
+  if ((e = launch<WGRAD2, kN_WGRAD>(mA, mB0, mB0, p, (long)E * p.m_tiles * p.n_tiles, st)) != cudaSuccess) return e;
 
   // dx_perm = dh . [Wg | Wu]^T (K = 2f): dh rows, w_gate / w_up rows
   if ((e = launch_mxfp8_quant_rows(wg, Ed, f, wgr.q, wgr.s, st)) != cudaSuccess) return e;
   if ((e = launch_mxfp8_quant_rows(wu, Ed, f, wur.q, wur.s, st)) != cudaSuccess) return e;
-  if (!map_2d(&mA, dhr.q, U8, 1, 2L * f, R, 128, BM) || !map_3d(&mB0, wgr.q, U8, 1, f, d, E, 128, BN) ||
-      !map_3d(&mB1, wur.q, U8, 1, f, d, E, 128, BN))
+  if (!map_2d(&mA, dhr.q, U8, 1, 2L * f, R, 128, BM) || !map_3d(&mB0, wgr.q, U8, 1, f, d, E, 128, kN_DGRAD1) ||
+      !map_3d(&mB1, wur.q, U8, 1, f, d, E, 128, kN_DGRAD1))
     return cudaErrorInvalidValue;
-  p.N = d; p.n_tiles = (d + BN - 1) / BN; p.out0 = dx_perm;
+  p.N = d; p.n_tiles = (d + kN_DGRAD1 - 1) / kN_DGRAD1; p.out0 = dx_perm;
   p.sfa = dhr.s; p.sfb0 = wgr.s; p.sfb1 = wur.s;
-  if ((e = launch<DGRAD1>(mA, mB0, mB1, p, ((long)(R + BM - 1) / BM + E) * p.n_tiles, st)) != cudaSuccess) return e;
+  if ((e = launch<DGRAD1, kN_DGRAD1>(mA, mB0, mB1, p, ((long)(R + BM - 1) / BM + E) * p.n_tiles, st)) != cudaSuccess)
+    return e;
 
   // [dWg | dWu][e] = x_e^T dh_e (K = the expert's rows)
   if ((e = launch_mxfp8_quant_cols(x_perm, R, d, offsets, E, xc.q, xc.s, st, true)) != cudaSuccess) return e;
   if ((e = launch_mxfp8_quant_cols(dh, R, 2 * f, offsets, E, dhc.q, dhc.s, st, true)) != cudaSuccess) return e;
   if (!map_2d(&mA, xc.q, U8, 1, d, R, 128, 128) || !map_2d(&mB0, dhc.q, U8, 1, 2L * f, R, 128, 128))
     return cudaErrorInvalidValue;
-  p.M = d; p.N = 2 * f; p.m_tiles = (d + BM - 1) / BM; p.n_tiles = (2 * f + BN - 1) / BN;
+  p.M = d; p.N = 2 * f; p.m_tiles = (d + BM - 1) / BM; p.n_tiles = (2 * f + kN_WGRAD - 1) / kN_WGRAD;
   p.out0 = dwg; p.out1 = dwu; p.sfa = xc.s; p.sfb0 = dhc.s; p.sfb1 = nullptr;
-  return launch<WGRAD1>(mA, mB0, mB0, p, (long)E * p.m_tiles * p.n_tiles, st);
+  return launch<WGRAD1, kN_WGRAD>(mA, mB0, mB0, p, (long)E * p.m_tiles * p.n_tiles, st);
 }
 
 size_t mx_fwd_workspace(long R, int E, int d, int f) { return tc::mx::fwd_workspace(R, E, d, f); }

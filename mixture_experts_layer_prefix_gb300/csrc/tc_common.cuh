@@ -186,14 +186,15 @@ __device__ __forceinline__ void quant_chunk_bf16(const Params& p, long row, int 
 // Epilogue of one tile for the rows of one TMEM lane quadrant: accumulator
 // chunks [c_beg, c_end) of 32 columns (FPROP1: gate chunk c with up chunk
 // c + 4). `zero` writes zeros without reading TMEM (wgrad of an empty expert).
+// TBN: columns of the tile (256, or 128 for the narrower MXFP8 tiles).
 // QUANT: also write the MXFP8 row quantisation of A (FPROP1) or dh (DGRAD2)
 // when p.qout is set.
-template <int KIND, bool QUANT = false>
+template <int KIND, bool QUANT = false, int TBN = BN>
 __device__ __forceinline__ void epilogue_tile(const Params& p, const Tile& tl, uint32_t tbase, int row_in_tile,
                                               int c_beg, int c_end, bool zero) {
   if (Traits<KIND>::kragged) {
     const int m = tl.m0 + row_in_tile;
-    const int n0 = tl.n_idx * BN;
+    const int n0 = tl.n_idx * TBN;
     const bool row_ok = m < p.M;
     for (int c = c_beg; c < c_end; ++c) {
       float v[32];
@@ -244,7 +245,7 @@ __device__ __forceinline__ void epilogue_tile(const Params& p, const Tile& tl, u
   } else if (KIND == DGRAD2) {
     // dh_g = da * h_u * silu'(h_g), dh_u = da * silu(h_g); h is loaded before
     // the accumulator so the global latency overlaps the TMEM read
-    const int n0 = tl.n_idx * BN;
+    const int n0 = tl.n_idx * TBN;
     const __nv_bfloat16* h = static_cast<const __nv_bfloat16*>(p.aux) + (size_t)row * 2 * p.f;
     __nv_bfloat16* dh = static_cast<__nv_bfloat16*>(p.out0) + (size_t)row * 2 * p.f;
     for (int c = c_beg; c < c_end; ++c) {
@@ -275,7 +276,7 @@ __device__ __forceinline__ void epilogue_tile(const Params& p, const Tile& tl, u
       }
     }
   } else if (KIND == ROUTER) {
-    const int n0 = tl.n_idx * BN;
+    const int n0 = tl.n_idx * TBN;
     float* out = static_cast<float*>(p.out0) + (size_t)row * p.N;
     for (int c = c_beg; c < c_end; ++c) {
       uint32_t r[32];
@@ -300,7 +301,7 @@ __device__ __forceinline__ void epilogue_tile(const Params& p, const Tile& tl, u
       }
     }
   } else {  // FPROP2, DGRAD1: plain bf16 store
-    const int n0 = tl.n_idx * BN;
+    const int n0 = tl.n_idx * TBN;
     for (int c = c_beg; c < c_end; ++c) {
       uint32_t r[32];
       ptx::tmem_ld32(tbase + c * 32, r);

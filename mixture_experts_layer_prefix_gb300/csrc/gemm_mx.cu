@@ -453,9 +453,11 @@ cudaError_t launch(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMa
   return cudaGetLastError();
 }
 
-// Output tile widths: GEMM1 pairs 128 gate with 128 up columns (256); the
-// others use 128-column tiles with a double-buffered accumulator.
-constexpr int kN_FPROP1 = 256, kN_FPROP2 = 128, kN_DGRAD2 = 128, kN_DGRAD1 = 256, kN_WGRAD = 128;
+// Output tile widths (measured choice): 256 with one accumulator released
+// early, except the GEMM2 dgrad, whose SwiGLU-backward epilogue reads h and
+// gains more from a double-buffered accumulator than it loses to the narrower
+// tile (the wgrads and GEMM2 re-read A twice as often at 128 and got slower).
+constexpr int kN_FPROP1 = 256, kN_FPROP2 = 256, kN_DGRAD2 = 128, kN_DGRAD1 = 256, kN_WGRAD = 256;
 
 constexpr CUtensorMapDataType U8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
 

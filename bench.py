@@ -106,29 +106,52 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------- CPU oracle
-def oracle_sample(s, tokens, seed=0):
-    """The fp64 oracle on the first `tokens` tokens of the workload (full
-    weights), routed on its own fp64 logits. Returns (seconds, threads)."""
-    import oracle
-    inp = synth.Inputs(s, seed=seed)
-    x, dy = inp.x()[:tokens], inp.dy()[:tokens]
-    wr, wg, wu, wd = inp.w_r(), inp.w_gate(), inp.w_up(), inp.w_down()
-    bias = inp.bias()
-    nthreads = len(os.sched_getaffinity(0)) or 1
-    t0 = time.perf_counter()
-    oracle.layer(x, wr, wg, wu, wd, dy, s.k, bias=bias, nthreads=nthreads)
-    return time.perf_counter() - t0, nthreads
+class OracleSampler:
+    """The fp64 oracle on the first n tokens of a workload (full weights,
+    routed on its own fp64 logits). Inputs are drawn once and reused."""
+
+    def __init__(self, s, seed=0):
+        import oracle
+        self.oracle = oracle
+        self.s = s
+        inp = synth.Inputs(s, seed=seed)
+        self.x, self.dy = inp.x(), inp.dy()
+        self.wr, self.wg, self.wu, self.wd = inp.w_r(), inp.w_gate(), inp.w_up(), inp.w_down()
+        self.bias = inp.bias()
+        self.nthreads = len(os.sched_getaffinity(0)) or 1
+
+    def run(self, tokens):
+        """Seconds for one oracle forward+backward of the first `tokens` tokens."""
+        t0 = time.perf_counter()
+        self.oracle.layer(self.x[:tokens], self.wr, self.wg, self.wu, self.wd, self.dy[:tokens], self.s.k,
+                          bias=self.bias, nthreads=self.nthreads)
+        return time.perf_counter() - t0
+
+    def size_for(self, seconds, probe=32):
+        """Token count whose run takes about `seconds` (from a probe run)."""
+        t = self.run(probe)
+        return int(max(probe, min(self.s.T, probe * seconds / max(t, 1e-3))))
 
 
 def cpu_baseline(s, budget_s=15.0):
     """Oracle tokens/s on a bounded sample sized for about `budget_s` seconds."""
-    probe = 8
-    t, _ = oracle_sample(s, probe)
-    n = int(max(probe, min(s.T, probe * budget_s / max(t, 1e-3))))
-    t, th = oracle_sample(s, n)
-    return {"value": n / t, "unit": "tokens/s", "cores": th, "kind": "oracle",
+    o = OracleSampler(s)
+    n = o.size_for(budget_s)
+    t = o.run(n)
+    return {"value": n / t, "unit": "tokens/s", "cores": o.nthreads, "kind": "oracle",
             "sample": f"first {n} of {s.T} tokens of {s.name}, full weights, fp64 C oracle, "
-                      f"{th} threads, {t:.1f} s"}
+                      f"{o.nthreads} threads, {t:.1f} s"}
+
+
+def max_over_ranks(values, device=None):
+    """Element-wise max of a list of floats over all ranks (identity when not
+    distributed). The timed region of every rank counts; the slowest sets it."""
+    import torch
+    if not (torch.distributed.is_available() and torch.distributed.is_initialized()):
+        return [float(v) for v in values]
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
 
 
 # --------------------------------------------------------------- our arm
@@ -227,10 +250,7 @@ def run_ours(args, s, rank, world):
     h2d = x_h.numel() * x_h.element_size() + dy_h.numel() * dy_h.element_size()
     d2h = y_h.numel() * y_h.element_size() + dx_h.numel() * dx_h.element_size()
 
-    if world > 1:
-        tt = torch.tensor([elapsed_ms, e2e_ms], device="cuda")
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        elapsed_ms, e2e_ms = float(tt[0]), float(tt[1])
+    elapsed_ms, e2e_ms = max_over_ranks([elapsed_ms, e2e_ms], device="cuda")
 
     ms_per_step = elapsed_ms / args.steps
     tokens_per_s = world * s.T * args.steps / (elapsed_ms / 1e3)
@@ -297,12 +317,12 @@ def main():
         if rank != 0:
             return
         per_step = max(2.0, min(15.0, 120.0 / (args.steps + args.warmup)))
-        probe = 8
-        t, th = oracle_sample(s, probe)
-        n = int(max(probe, min(s.T, probe * per_step / max(t, 1e-3))))
+        o = OracleSampler(s)
+        n = o.size_for(per_step)
+        th = o.nthreads
         for _ in range(args.warmup):
-            oracle_sample(s, n)
-        times = [oracle_sample(s, n)[0] for _ in range(args.steps)]
+            o.run(n)
+        times = [o.run(n) for _ in range(args.steps)]
         v = n * len(times) / sum(times)
         print(json.dumps({
             "impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": 1,

@@ -35,9 +35,15 @@ constexpr int BOX_BYTES = 64 * 64 * 2;  // one 64 (MN) x 64 (K) MN-major box
 constexpr int NUM_EPI_WARPS = 8;
 constexpr int NUM_THREADS = 64 + 32 * NUM_EPI_WARPS;
 constexpr uint32_t TMEM_COLS = 512;
+// wgrad tiles leave the tensor cores idle and are bound by data movement: they
+// use 3 stages and stage each warp's 32x128 output block in shared memory
+// (two 32x64 boxes, 128-byte swizzle) for TMA stores.
+constexpr int STAGE_OUT_BYTES = 32 * 128 * 2;  // per epilogue warp
+template <int KIND> constexpr int n_stages() { return Traits<KIND>::kragged ? 3 : STAGES; }
+template <int KIND> constexpr int out_bytes() { return Traits<KIND>::kragged ? NUM_EPI_WARPS * STAGE_OUT_BYTES : 0; }
 
 struct Smem {
-  uint64_t full[STAGES];
+  uint64_t full[STAGES];  // the first n_stages<KIND>() are used
   uint64_t empty[STAGES];
   uint64_t tfull[2];
   uint64_t tempty[2];
@@ -49,18 +55,21 @@ struct Smem {
 template <int KIND>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
-               const __grid_constant__ CUtensorMap tmB1, const Params p) {
+               const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmC0,
+               const __grid_constant__ CUtensorMap tmC1, const Params p) {
   using Tr = Traits<KIND>;
+  constexpr int NS = n_stages<KIND>();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  Smem* sm = reinterpret_cast<Smem*>(smem + STAGES * STAGE_BYTES);
+  uint8_t* out_stage = smem + NS * STAGE_BYTES;  // wgrad output staging (1024-aligned)
+  Smem* sm = reinterpret_cast<Smem*>(out_stage + out_bytes<KIND>());
   int* offs = reinterpret_cast<int*>(sm + 1);
   int* tstart = offs + (p.E + 1);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   build_tile_table<KIND, NUM_THREADS>(p, offs, tstart);
   if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
+    for (int s = 0; s < NS; ++s) {
       ptx::mbar_init(&sm->full[s], 1);
       ptx::mbar_init(&sm->empty[s], 1);
     }
@@ -94,8 +103,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
         const Tile tl = decode<KIND, BK>(t, p, offs, tstart);
         for (int kb = 0; kb < tl.nkb; ++kb, ++it) {
-          const int s = it % STAGES;
-          const uint32_t ph = (it / STAGES) & 1u;
+          const int s = it % NS;
+          const uint32_t ph = (it / NS) & 1u;
           if (!wait_bar(&sm->empty[s], ph ^ 1u, &sm->abort_flag, p.err)) { ok = false; break; }
           uint8_t* a = smem + s * STAGE_BYTES;
           uint8_t* b = a + A_BYTES;
@@ -136,7 +145,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       }
       if (!ok) {
         // drain: wait (bounded) for loads already issued into stages the MMA will not consume
-        for (int s = 0; s < STAGES; ++s) {
+        for (int s = 0; s < NS; ++s) {
           const long long t0 = clock64();
           while (clock64() - t0 < kWaitLimitCycles / 8 && !ptx::mbar_try_wait(&sm->full[s], 0) &&
                  !ptx::mbar_try_wait(&sm->full[s], 1)) {
@@ -158,8 +167,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       ptx::tc_fence_after();
       const uint32_t d_tmem = tmem + static_cast<uint32_t>(buf * BN);
       for (int kb = 0; kb < tl.nkb; ++kb, ++it) {
-        const int s = it % STAGES;
-        const uint32_t ph = (it / STAGES) & 1u;
+        const int s = it % NS;
+        const uint32_t ph = (it / NS) & 1u;
         if (!wait_bar(&sm->full[s], ph, &sm->abort_flag, p.err)) { ok = false; break; }
         ptx::tc_fence_after();
         uint8_t* a = smem + s * STAGE_BYTES;
@@ -224,7 +233,51 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         ptx::tc_fence_after();
       }
       const uint32_t tbase = tmem + static_cast<uint32_t>(buf * BN) + (static_cast<uint32_t>(q * 32) << 16);
-      epilogue_tile<KIND>(p, tl, tbase, q * 32 + lane, half * NC / 2, (half + 1) * NC / 2, empty_k);
+      if (Tr::kragged) {
+        // this warp's 32 rows x 128 columns: two 32x64 boxes, 128-byte swizzled
+        uint8_t* st = out_stage + ew * STAGE_OUT_BYTES;
+        if (lane == 0) ptx::bulk_wait_read();  // previous tile's stores have read the staging
+        __syncwarp();
+        for (int c = 0; c < 4; ++c) {
+          uint32_t r[32];
+          if (!empty_k) {
+            ptx::tmem_ld32(tbase + (half * 4 + c) * 32, r);
+            ptx::tmem_wait_ld();
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) r[i] = 0u;
+          }
+          uint8_t* box = st + (c >> 1) * (STAGE_OUT_BYTES / 2) + lane * 128;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            uint32_t w[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              __nv_bfloat162 h2 = __floats2bfloat162_rn(__uint_as_float(r[8 * j + 2 * i]),
+                                                       __uint_as_float(r[8 * j + 2 * i + 1]));
+              w[i] = *reinterpret_cast<uint32_t*>(&h2);
+            }
+            const int chunk = ((c & 1) * 4 + j) ^ (lane & 7);
+            *reinterpret_cast<uint4*>(box + chunk * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+          }
+        }
+        ptx::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          const int m = tl.m0 + q * 32;
+#pragma unroll
+          for (int bx = 0; bx < 2; ++bx) {
+            const int n = tl.n_idx * BN + (half * 4 + 2 * bx) * 32;
+            const void* src = st + bx * (STAGE_OUT_BYTES / 2);
+            if (KIND == WGRAD2) ptx::tma_store_3d(&tmC0, src, n, m, tl.e);
+            else if (n < p.f) ptx::tma_store_3d(&tmC0, src, n, m, tl.e);
+            else ptx::tma_store_3d(&tmC1, src, n - p.f, m, tl.e);
+          }
+          ptx::bulk_commit();
+        }
+      } else {
+        epilogue_tile<KIND>(p, tl, tbase, q * 32 + lane, half * NC / 2, (half + 1) * NC / 2, empty_k);
+      }
       if (!empty_k) {
         ptx::tc_fence_before();
         __syncwarp();
@@ -234,6 +287,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     }
   }
 
+  if (Tr::kragged && warp >= 2 && lane == 0) ptx::bulk_wait_all();  // output stores done before exit
   ptx::tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -242,18 +296,22 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   }
 }
 
-size_t smem_bytes(int E) { return 1024 + STAGES * STAGE_BYTES + sizeof(Smem) + 2 * (E + 1) * sizeof(int) + 64; }
+template <int KIND>
+size_t smem_bytes(int E) {
+  return 1024 + n_stages<KIND>() * STAGE_BYTES + out_bytes<KIND>() + sizeof(Smem) + 2 * (E + 1) * sizeof(int) + 64;
+}
 
 template <int KIND>
 cudaError_t launch(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1, const Params& p,
-                   long max_tiles, cudaStream_t st) {
+                   long max_tiles, cudaStream_t st, const CUtensorMap* c0 = nullptr,
+                   const CUtensorMap* c1 = nullptr) {
   if (max_tiles <= 0) return cudaSuccess;
-  const size_t smem = smem_bytes(p.E);
+  const size_t smem = smem_bytes<KIND>(p.E);
   cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   const int grid = static_cast<int>(max_tiles < sm_count() ? max_tiles : sm_count());
-  MOE_COUNTED tc_gemm_kernel<KIND><<<grid, NUM_THREADS, smem, st>>>(a, b0, b1, p);
+  MOE_COUNTED tc_gemm_kernel<KIND><<<grid, NUM_THREADS, smem, st>>>(a, b0, b1, c0 ? *c0 : a, c1 ? *c1 : a, p);
   return cudaGetLastError();
 }
 
@@ -352,7 +410,9 @@ cudaError_t tc_mlp_bwd(const void* dy_perm, const void* x_perm, const void* h, c
   if (!map_2d(&mA, a, BF, 2, f, R, 64, 64) || !map_2d(&mB0, dy_perm, BF, 2, d, R, 64, 64))
     return cudaErrorInvalidValue;
   p.M = f; p.N = d; p.m_tiles = (f + BM - 1) / BM; p.n_tiles = (d + BN - 1) / BN; p.out0 = dwd;
-  e = launch<WGRAD2>(mA, mB0, mB0, p, (long)E * p.m_tiles * p.n_tiles, st);
+  CUtensorMap mC0, mC1;
+  if (!map_3d(&mC0, dwd, BF, 2, d, f, E, 64, 32)) return cudaErrorInvalidValue;
+  e = launch<WGRAD2>(mA, mB0, mB0, p, (long)E * p.m_tiles * p.n_tiles, st, &mC0, &mC0);
   if (e != cudaSuccess) return e;
   // dx_perm = dh_g . Wg^T + dh_u . Wu^T
   if (!map_2d(&mA, dh, BF, 2, 2L * f, R, 64, BM) || !map_3d(&mB0, wg, BF, 2, f, d, E, 64, BN) ||
@@ -366,7 +426,9 @@ cudaError_t tc_mlp_bwd(const void* dy_perm, const void* x_perm, const void* h, c
     return cudaErrorInvalidValue;
   p.M = d; p.N = 2 * f; p.m_tiles = (d + BM - 1) / BM; p.n_tiles = (2 * f + BN - 1) / BN;
   p.out0 = dwg; p.out1 = dwu;
-  return launch<WGRAD1>(mA, mB0, mB0, p, (long)E * p.m_tiles * p.n_tiles, st);
+  if (!map_3d(&mC0, dwg, BF, 2, f, d, E, 64, 32) || !map_3d(&mC1, dwu, BF, 2, f, d, E, 64, 32))
+    return cudaErrorInvalidValue;
+  return launch<WGRAD1>(mA, mB0, mB0, p, (long)E * p.m_tiles * p.n_tiles, st, &mC0, &mC1);
 }
 
 cudaError_t tc_router_logits(const void* x, const void* w_r, const float* bias, int T, int d, int E,

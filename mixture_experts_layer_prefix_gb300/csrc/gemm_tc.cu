@@ -315,6 +315,218 @@ cudaError_t launch(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMa
   return cudaGetLastError();
 }
 
+// ---------------------------------------------------------------------------
+// Weight gradients: dW_e = X_e^T Y_e over the rows of expert e. These tiles
+// leave the tensor cores idle: they are bound by the operand traffic from L2,
+// so they use 256x256 output tiles (two 128-row halves of M sharing one B
+// tile; both 256-column fp32 accumulators fill TMEM) to cut that traffic per
+// FLOP by 1.5x against 128x256 tiles. Single-buffered accumulator; the
+// producer keeps loading the next tile's stages while the epilogue drains.
+constexpr int WBM = 256;
+constexpr int W_A_BYTES = WBM * BK * 2;  // 4 boxes of 64 (M) x 64 (K rows)
+constexpr int W_B_BYTES = BN * BK * 2;   // 4 boxes of 64 (N) x 64 (K rows)
+constexpr int W_STAGE = W_A_BYTES + W_B_BYTES;
+constexpr int W_NS = 3;
+
+template <int KIND>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+tc_wgrad_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const Params p) {
+  static_assert(Traits<KIND>::kragged, "weight-gradient kinds only");
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  Smem* sm = reinterpret_cast<Smem*>(smem + W_NS * W_STAGE);
+  int* offs = reinterpret_cast<int*>(sm + 1);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  for (int i = threadIdx.x; i <= p.E; i += NUM_THREADS) offs[i] = p.offsets[i];
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < W_NS; ++s) {
+      ptx::mbar_init(&sm->full[s], 1);
+      ptx::mbar_init(&sm->empty[s], 1);
+    }
+    ptx::mbar_init(&sm->tfull[0], 1);
+    ptx::mbar_init(&sm->tempty[0], NUM_EPI_WARPS);
+    ptx::mbar_init(&sm->drain, 1);
+    sm->abort_flag = 0;
+    ptx::fence_mbar_init();
+    ptx::fence_proxy_async_smem();
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(&sm->tmem_base, TMEM_COLS);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const int per = p.m_tiles * p.n_tiles;
+  const int total = p.E * per;
+  const uint32_t tmem = sm->tmem_base;
+  auto decode_w = [&](int t, int& e, int& m0, int& n0, int& r0, int& r1, int& nkb) {
+    e = t / per;
+    const int local = t % per;
+    m0 = (local / p.n_tiles) * WBM;
+    n0 = (local % p.n_tiles) * BN;
+    r0 = offs[e];
+    r1 = offs[e + 1];
+    nkb = (r1 - r0 + BK - 1) / BK;
+  };
+
+  if (warp == 0) {
+    // ===================================================== TMA producer
+    if (lane == 0) {
+      ptx::prefetch_tmap(&tmA);
+      ptx::prefetch_tmap(&tmB);
+      uint32_t it = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+        int e, m0, n0, r0, r1, nkb;
+        decode_w(t, e, m0, n0, r0, r1, nkb);
+        for (int kb = 0; kb < nkb; ++kb, ++it) {
+          const int s = it % W_NS;
+          const uint32_t ph = (it / W_NS) & 1u;
+          if (!wait_bar(&sm->empty[s], ph ^ 1u, &sm->abort_flag, p.err)) { ok = false; break; }
+          uint8_t* a = smem + s * W_STAGE;
+          uint8_t* b = a + W_A_BYTES;
+          uint64_t* fb = &sm->full[s];
+          ptx::mbar_expect_tx(fb, W_STAGE);
+          const int row = r0 + kb * BK;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) ptx::tma_load_2d(a + j * BOX_BYTES, &tmA, fb, m0 + 64 * j, row);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) ptx::tma_load_2d(b + j * BOX_BYTES, &tmB, fb, n0 + 64 * j, row);
+        }
+      }
+      if (!ok) {
+        for (int s = 0; s < W_NS; ++s) {
+          const long long t0 = clock64();
+          while (clock64() - t0 < kWaitLimitCycles / 8 && !ptx::mbar_try_wait(&sm->full[s], 0) &&
+                 !ptx::mbar_try_wait(&sm->full[s], 1)) {
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ========================================================= MMA issuer
+    constexpr uint32_t idesc = ptx::idesc_bf16_f32(BM, BN, 1, 1);
+    uint32_t it = 0, acc_it = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+      int e, m0, n0, r0, r1, nkb;
+      decode_w(t, e, m0, n0, r0, r1, nkb);
+      if (nkb == 0) continue;
+      if (!wait_bar(&sm->tempty[0], (acc_it & 1u) ^ 1u, &sm->abort_flag, p.err)) { ok = false; break; }
+      ptx::tc_fence_after();
+      for (int kb = 0; kb < nkb; ++kb, ++it) {
+        const int s = it % W_NS;
+        const uint32_t ph = (it / W_NS) & 1u;
+        if (!wait_bar(&sm->full[s], ph, &sm->abort_flag, p.err)) { ok = false; break; }
+        ptx::tc_fence_after();
+        uint8_t* a = smem + s * W_STAGE;
+        int nks = BK / 16;
+        const int valid = r1 - (r0 + kb * BK);
+        if (valid < BK) {
+          // rows past the expert's end belong to the next expert: skip K steps made
+          // only of them and zero the rest of the last partial step in the four A boxes
+          nks = (valid + 15) / 16;
+          const int nrow = nks * 16 - valid, per_box = nrow * 8;
+          for (int i = lane; i < 4 * per_box; i += 32) {
+            const int box = i / per_box, rem = i % per_box;
+            const int rr = valid + rem / 8, chunk = rem % 8;
+            *reinterpret_cast<uint4*>(a + box * BOX_BYTES + rr * 128 + chunk * 16) = make_uint4(0, 0, 0, 0);
+          }
+          if (nrow > 0) ptx::fence_proxy_async_smem();
+        }
+        __syncwarp();
+        if (lane == 0) {
+          const uint32_t a_addr = ptx::smem_u32(a), b_addr = a_addr + W_A_BYTES;
+          for (int ks = 0; ks < nks; ++ks) {
+            const uint64_t bd = ptx::smem_desc_sw128(b_addr + ks * 2048, BOX_BYTES, 1024);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const uint64_t ad = ptx::smem_desc_sw128(a_addr + h * 2 * BOX_BYTES + ks * 2048, BOX_BYTES, 1024);
+              ptx::mma_f16(tmem + h * BN, ad, bd, idesc, (kb > 0 || ks > 0) ? 1u : 0u);
+            }
+          }
+          ptx::mma_commit(&sm->empty[s]);
+        }
+        __syncwarp();
+      }
+      if (!ok) break;
+      if (lane == 0) ptx::mma_commit(&sm->tfull[0]);
+      __syncwarp();
+      ++acc_it;
+    }
+    if (!ok && lane == 0) {
+      ptx::mma_commit(&sm->drain);
+      const long long t0 = clock64();
+      while (clock64() - t0 < kWaitLimitCycles / 8 && !ptx::mbar_try_wait(&sm->drain, 0)) {
+      }
+    }
+  } else {
+    // ============================================================ epilogue
+    // warps 2..5 take M half 0, warps 6..9 M half 1; lanes are rows
+    const int ew = warp - 2, q = warp & 3, mh = ew >> 2;
+    uint32_t acc_it = 0;
+    for (int t = blockIdx.x; t < total; t += gridDim.x) {
+      int e, m0, n0, r0, r1, nkb;
+      decode_w(t, e, m0, n0, r0, r1, nkb);
+      const bool empty_k = nkb == 0;
+      if (!empty_k) {
+        if (!wait_bar(&sm->tfull[0], acc_it & 1u, &sm->abort_flag, p.err)) break;
+        ptx::tc_fence_after();
+      }
+      const int m = m0 + mh * 128 + q * 32 + lane;
+      const uint32_t tbase = tmem + static_cast<uint32_t>(mh * BN) + (static_cast<uint32_t>(q * 32) << 16);
+      for (int c = 0; c < BN / 32; ++c) {
+        float v[32];
+        if (!empty_k) {
+          uint32_t r[32];
+          ptx::tmem_ld32(tbase + c * 32, r);
+          ptx::tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = 0.0f;
+        }
+        const int n = n0 + c * 32;
+        if (m >= p.M || n >= p.N) continue;
+        __nv_bfloat16* dst;
+        if (KIND == WGRAD2) dst = static_cast<__nv_bfloat16*>(p.out0) + ((size_t)e * p.M + m) * p.N + n;
+        else dst = n < p.f ? static_cast<__nv_bfloat16*>(p.out0) + ((size_t)e * p.d + m) * p.f + n
+                           : static_cast<__nv_bfloat16*>(p.out1) + ((size_t)e * p.d + m) * p.f + (n - p.f);
+        store_bf16x32(dst, v);
+      }
+      if (!empty_k) {
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&sm->tempty[0]);
+        ++acc_it;
+      }
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+template <int KIND>
+cudaError_t launch_wgrad(const CUtensorMap& a, const CUtensorMap& b, const Params& p, cudaStream_t st) {
+  const long tiles = (long)p.E * p.m_tiles * p.n_tiles;
+  if (tiles <= 0) return cudaSuccess;
+  const size_t smem = 1024 + W_NS * W_STAGE + sizeof(Smem) + (p.E + 1) * sizeof(int) + 64;
+  cudaError_t e = cudaFuncSetAttribute(tc_wgrad_kernel<KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  const int grid = static_cast<int>(tiles < sm_count() ? tiles : sm_count());
+  MOE_COUNTED tc_wgrad_kernel<KIND><<<grid, NUM_THREADS, smem, st>>>(a, b, p);
+  return cudaGetLastError();
+}
+
 constexpr CUtensorMapDataType BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
 
 }  // namespace
@@ -409,10 +621,8 @@ cudaError_t tc_mlp_bwd(const void* dy_perm, const void* x_perm, const void* h, c
   // dWd[e] = A_e^T dy_e
   if (!map_2d(&mA, a, BF, 2, f, R, 64, 64) || !map_2d(&mB0, dy_perm, BF, 2, d, R, 64, 64))
     return cudaErrorInvalidValue;
-  p.M = f; p.N = d; p.m_tiles = (f + BM - 1) / BM; p.n_tiles = (d + BN - 1) / BN; p.out0 = dwd;
-  CUtensorMap mC0, mC1;
-  if (!map_3d(&mC0, dwd, BF, 2, d, f, E, 64, 32)) return cudaErrorInvalidValue;
-  e = launch<WGRAD2>(mA, mB0, mB0, p, (long)E * p.m_tiles * p.n_tiles, st, &mC0, &mC0);
+  p.M = f; p.N = d; p.m_tiles = (f + WBM - 1) / WBM; p.n_tiles = (d + BN - 1) / BN; p.out0 = dwd;
+  e = launch_wgrad<WGRAD2>(mA, mB0, p, st);
   if (e != cudaSuccess) return e;
   // dx_perm = dh_g . Wg^T + dh_u . Wu^T
   if (!map_2d(&mA, dh, BF, 2, 2L * f, R, 64, BM) || !map_3d(&mB0, wg, BF, 2, f, d, E, 64, BN) ||
@@ -424,11 +634,9 @@ cudaError_t tc_mlp_bwd(const void* dy_perm, const void* x_perm, const void* h, c
   // [dWg | dWu][e] = x_perm_e^T dh_e
   if (!map_2d(&mA, x_perm, BF, 2, d, R, 64, 64) || !map_2d(&mB0, dh, BF, 2, 2L * f, R, 64, 64))
     return cudaErrorInvalidValue;
-  p.M = d; p.N = 2 * f; p.m_tiles = (d + BM - 1) / BM; p.n_tiles = (2 * f + BN - 1) / BN;
+  p.M = d; p.N = 2 * f; p.m_tiles = (d + WBM - 1) / WBM; p.n_tiles = (2 * f + BN - 1) / BN;
   p.out0 = dwg; p.out1 = dwu;
-  if (!map_3d(&mC0, dwg, BF, 2, f, d, E, 64, 32) || !map_3d(&mC1, dwu, BF, 2, f, d, E, 64, 32))
-    return cudaErrorInvalidValue;
-  return launch<WGRAD1>(mA, mB0, mB0, p, (long)E * p.m_tiles * p.n_tiles, st, &mC0, &mC1);
+  return launch_wgrad<WGRAD1>(mA, mB0, p, st);
 }
 
 cudaError_t tc_router_logits(const void* x, const void* w_r, const float* bias, int T, int d, int E,

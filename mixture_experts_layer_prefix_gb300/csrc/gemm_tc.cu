@@ -320,13 +320,15 @@ cudaError_t launch(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMa
 // leave the tensor cores idle: they are bound by the operand traffic from L2,
 // so they use 256x256 output tiles (two 128-row halves of M sharing one B
 // tile; both 256-column fp32 accumulators fill TMEM) to cut that traffic per
-// FLOP by 1.5x against 128x256 tiles. Single-buffered accumulator; the
-// producer keeps loading the next tile's stages while the epilogue drains.
+// FLOP by 1.5x against 128x256 tiles. Single-buffered accumulator, drained
+// into registers at once so the stores overlap the next tile's MMAs; the
+// producer keeps loading the next tile's stages meanwhile.
 constexpr int WBM = 256;
 constexpr int W_A_BYTES = WBM * BK * 2;  // 4 boxes of 64 (M) x 64 (K rows)
 constexpr int W_B_BYTES = BN * BK * 2;   // 4 boxes of 64 (N) x 64 (K rows)
 constexpr int W_STAGE = W_A_BYTES + W_B_BYTES;
 constexpr int W_NS = 3;
+constexpr int W_STG = 32 * 128;  // per epilogue warp: 32 rows x 64 bf16, 16-byte granules XOR-swizzled by row
 
 template <int KIND>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
@@ -334,11 +336,10 @@ tc_wgrad_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
   static_assert(Traits<KIND>::kragged, "weight-gradient kinds only");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  Smem* sm = reinterpret_cast<Smem*>(smem + W_NS * W_STAGE);
-  int* offs = reinterpret_cast<int*>(sm + 1);
+  Smem* sm = reinterpret_cast<Smem*>(smem + W_NS * W_STAGE + NUM_EPI_WARPS * W_STG);
+  const int* __restrict__ offs = p.offsets;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  for (int i = threadIdx.x; i <= p.E; i += NUM_THREADS) offs[i] = p.offsets[i];
   if (threadIdx.x == 0) {
     for (int s = 0; s < W_NS; ++s) {
       ptx::mbar_init(&sm->full[s], 1);
@@ -366,8 +367,8 @@ tc_wgrad_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     const int local = t % per;
     m0 = (local / p.n_tiles) * WBM;
     n0 = (local % p.n_tiles) * BN;
-    r0 = offs[e];
-    r1 = offs[e + 1];
+    r0 = __ldg(offs + e);
+    r1 = __ldg(offs + e + 1);
     nkb = (r1 - r0 + BK - 1) / BK;
   };
 
@@ -464,44 +465,74 @@ tc_wgrad_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     }
   } else {
     // ============================================================ epilogue
-    // warps 2..5 take M half 0, warps 6..9 M half 1; lanes are rows
+    // warps 2..5 take M half 0, warps 6..9 M half 1; lanes are rows. Each
+    // thread first moves its whole 256-column row of the accumulator into
+    // registers as packed bf16 pairs (128 words) and hands TMEM back, so the
+    // next tile's MMAs start while this tile's stores go out.
     const int ew = warp - 2, q = warp & 3, mh = ew >> 2;
     uint32_t acc_it = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
       int e, m0, n0, r0, r1, nkb;
       decode_w(t, e, m0, n0, r0, r1, nkb);
-      const bool empty_k = nkb == 0;
-      if (!empty_k) {
+      uint32_t hold[BN / 2];
+      if (nkb > 0) {
         if (!wait_bar(&sm->tfull[0], acc_it & 1u, &sm->abort_flag, p.err)) break;
         ptx::tc_fence_after();
-      }
-      const int m = m0 + mh * 128 + q * 32 + lane;
-      const uint32_t tbase = tmem + static_cast<uint32_t>(mh * BN) + (static_cast<uint32_t>(q * 32) << 16);
-      for (int c = 0; c < BN / 32; ++c) {
-        float v[32];
-        if (!empty_k) {
-          uint32_t r[32];
-          ptx::tmem_ld32(tbase + c * 32, r);
+        const uint32_t tbase = tmem + static_cast<uint32_t>(mh * BN) + (static_cast<uint32_t>(q * 32) << 16);
+#pragma unroll
+        for (int c = 0; c < BN / 16; ++c) {
+          uint32_t r[16];
+          ptx::tmem_ld16(tbase + c * 16, r);
           ptx::tmem_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-        } else {
-#pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] = 0.0f;
+          for (int i = 0; i < 8; ++i) {
+            __nv_bfloat162 h2 = __floats2bfloat162_rn(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
+            hold[c * 8 + i] = *reinterpret_cast<uint32_t*>(&h2);
+          }
         }
-        const int n = n0 + c * 32;
-        if (m >= p.M || n >= p.N) continue;
-        __nv_bfloat16* dst;
-        if (KIND == WGRAD2) dst = static_cast<__nv_bfloat16*>(p.out0) + ((size_t)e * p.M + m) * p.N + n;
-        else dst = n < p.f ? static_cast<__nv_bfloat16*>(p.out0) + ((size_t)e * p.d + m) * p.f + n
-                           : static_cast<__nv_bfloat16*>(p.out1) + ((size_t)e * p.d + m) * p.f + (n - p.f);
-        store_bf16x32(dst, v);
-      }
-      if (!empty_k) {
         ptx::tc_fence_before();
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(&sm->tempty[0]);
         ++acc_it;
+      } else {
+#pragma unroll
+        for (int i = 0; i < BN / 2; ++i) hold[i] = 0u;  // expert with no rows: dW_e = 0
+      }
+      // Stores go out 64 columns at a time through this warp's staging
+      // buffer: each lane writes its row, then each instruction stores four
+      // rows' 128-byte segments (8 lanes per row), so every request covers
+      // whole lines.
+      const int mb = m0 + mh * 128 + q * 32;
+      uint8_t* stg = smem + W_NS * W_STAGE + ew * W_STG;
+#pragma unroll
+      for (int c = 0; c < BN / 64; ++c) {
+        const int n = n0 + c * 64;
+        if (n >= p.N) break;
+#pragma unroll
+        for (int g = 0; g < 8; ++g)
+          *reinterpret_cast<uint4*>(stg + lane * 128 + ((g ^ (lane & 7)) << 4)) =
+              make_uint4(hold[c * 32 + 4 * g], hold[c * 32 + 4 * g + 1], hold[c * 32 + 4 * g + 2],
+                         hold[c * 32 + 4 * g + 3]);
+        __syncwarp();
+        const int g = lane & 7;
+        __nv_bfloat16* base;
+        size_t ld;
+        if (KIND == WGRAD2) {
+          base = static_cast<__nv_bfloat16*>(p.out0) + ((size_t)e * p.M + mb) * p.N + n;
+          ld = p.N;
+        } else {
+          base = n < p.f ? static_cast<__nv_bfloat16*>(p.out0) + ((size_t)e * p.d + mb) * p.f + n
+                         : static_cast<__nv_bfloat16*>(p.out1) + ((size_t)e * p.d + mb) * p.f + (n - p.f);
+          ld = p.f;
+        }
+        base += 8 * g;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int r = 4 * i + (lane >> 3);
+          const uint4 v = *reinterpret_cast<const uint4*>(stg + r * 128 + ((g ^ (r & 7)) << 4));
+          if (mb + r < p.M) *reinterpret_cast<uint4*>(base + r * ld) = v;
+        }
+        __syncwarp();
       }
     }
   }
@@ -518,7 +549,7 @@ template <int KIND>
 cudaError_t launch_wgrad(const CUtensorMap& a, const CUtensorMap& b, const Params& p, cudaStream_t st) {
   const long tiles = (long)p.E * p.m_tiles * p.n_tiles;
   if (tiles <= 0) return cudaSuccess;
-  const size_t smem = 1024 + W_NS * W_STAGE + sizeof(Smem) + (p.E + 1) * sizeof(int) + 64;
+  const size_t smem = 1024 + W_NS * W_STAGE + NUM_EPI_WARPS * W_STG + sizeof(Smem) + 64;
   cudaError_t e = cudaFuncSetAttribute(tc_wgrad_kernel<KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;

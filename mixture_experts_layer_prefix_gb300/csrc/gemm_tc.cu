@@ -35,15 +35,10 @@ constexpr int BOX_BYTES = 64 * 64 * 2;  // one 64 (MN) x 64 (K) MN-major box
 constexpr int NUM_EPI_WARPS = 8;
 constexpr int NUM_THREADS = 64 + 32 * NUM_EPI_WARPS;
 constexpr uint32_t TMEM_COLS = 512;
-// wgrad tiles leave the tensor cores idle and are bound by data movement: they
-// use 3 stages and stage each warp's 32x128 output block in shared memory
-// (two 32x64 boxes, 128-byte swizzle) for TMA stores.
-constexpr int STAGE_OUT_BYTES = 32 * 128 * 2;  // per epilogue warp
-template <int KIND> constexpr int n_stages() { return Traits<KIND>::kragged ? 3 : STAGES; }
-template <int KIND> constexpr int out_bytes() { return Traits<KIND>::kragged ? NUM_EPI_WARPS * STAGE_OUT_BYTES : 0; }
+constexpr int OUT_STG_BYTES = NUM_EPI_WARPS * STG_BYTES;  // epilogue staging, one buffer per warp
 
 struct Smem {
-  uint64_t full[STAGES];  // the first n_stages<KIND>() are used
+  uint64_t full[STAGES];
   uint64_t empty[STAGES];
   uint64_t tfull[2];
   uint64_t tempty[2];
@@ -55,14 +50,14 @@ struct Smem {
 template <int KIND>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
-               const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmC0,
-               const __grid_constant__ CUtensorMap tmC1, const Params p) {
+               const __grid_constant__ CUtensorMap tmB1, const Params p) {
   using Tr = Traits<KIND>;
-  constexpr int NS = n_stages<KIND>();
+  static_assert(!Tr::kragged, "weight gradients run in tc_wgrad_kernel");
+  constexpr int NS = STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* out_stage = smem + NS * STAGE_BYTES;  // wgrad output staging (1024-aligned)
-  Smem* sm = reinterpret_cast<Smem*>(out_stage + out_bytes<KIND>());
+  uint8_t* out_stage = smem + NS * STAGE_BYTES;  // epilogue staging
+  Smem* sm = reinterpret_cast<Smem*>(out_stage + OUT_STG_BYTES);
   int* offs = reinterpret_cast<int*>(sm + 1);
   int* tstart = offs + (p.E + 1);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -89,7 +84,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
-  const int total = Tr::kragged ? p.E * p.m_tiles * p.n_tiles : tstart[p.E];
+  const int total = tstart[p.E];
   const uint32_t tmem = sm->tmem_base;
 
   if (warp == 0) {
@@ -129,17 +124,10 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           } else if (KIND == ROUTER) {
             ptx::tma_load_2d(a, &tmA, fb, k0, tl.m0);
             ptx::tma_load_2d(b, &tmB0, fb, k0, tl.n_idx * BN);
-          } else if (KIND == DGRAD1) {
+          } else {  // DGRAD1
             ptx::tma_load_2d(a, &tmA, fb, k0, tl.m0);
             if (k0 < p.f) ptx::tma_load_3d(b, &tmB0, fb, k0, tl.n_idx * BN, tl.e);
             else ptx::tma_load_3d(b, &tmB1, fb, k0 - p.f, tl.n_idx * BN, tl.e);
-          } else {  // WGRAD2 / WGRAD1: K runs over the expert's rows
-            const int row = tl.k_row0 + k0;
-            ptx::tma_load_2d(a + 0 * BOX_BYTES, &tmA, fb, tl.m0, row);
-            ptx::tma_load_2d(a + 1 * BOX_BYTES, &tmA, fb, tl.m0 + 64, row);
-            const int n0 = tl.n_idx * BN;
-#pragma unroll
-            for (int j = 0; j < 4; ++j) ptx::tma_load_2d(b + j * BOX_BYTES, &tmB0, fb, n0 + 64 * j, row);
           }
         }
       }
@@ -172,27 +160,9 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         if (!wait_bar(&sm->full[s], ph, &sm->abort_flag, p.err)) { ok = false; break; }
         ptx::tc_fence_after();
         uint8_t* a = smem + s * STAGE_BYTES;
-        int nks = BK / 16;  // K steps of 16 rows issued for this stage
-        if (Tr::kragged) {
-          const int valid = tl.row_end - (tl.k_row0 + kb * BK);
-          if (valid < BK) {
-            // Rows past the expert's end belong to the next expert. K steps made
-            // only of such rows are skipped; inside the last partial step the
-            // extra rows of A are zeroed.
-            nks = (valid + 15) / 16;
-            const int nrow = nks * 16 - valid, per_box = nrow * 8;
-            for (int i = lane; i < 2 * per_box; i += 32) {
-              const int box = i / per_box, rem = i % per_box;
-              const int row = valid + rem / 8, chunk = rem % 8;
-              *reinterpret_cast<uint4*>(a + box * BOX_BYTES + row * 128 + chunk * 16) = make_uint4(0, 0, 0, 0);
-            }
-            if (nrow > 0) ptx::fence_proxy_async_smem();
-          }
-          __syncwarp();
-        }
         if (lane == 0) {
           const uint32_t a_addr = ptx::smem_u32(a), b_addr = a_addr + A_BYTES;
-          for (int ks = 0; ks < nks; ++ks) {
+          for (int ks = 0; ks < BK / 16; ++ks) {
             const uint64_t ad = Tr::a_mn ? ptx::smem_desc_sw128(a_addr + ks * 2048, BOX_BYTES, 1024)
                                          : ptx::smem_desc_sw128(a_addr + ks * 32, 16, 1024);
             const uint64_t bd = Tr::b_mn ? ptx::smem_desc_sw128(b_addr + ks * 2048, BOX_BYTES, 1024)
@@ -221,73 +191,27 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     // of a quadrant split the tile's columns in halves.
     const int ew = warp - 2, q = warp & 3, half = ew >> 2;
     constexpr int NC = epi_chunks<KIND>();
+    uint8_t* stg = out_stage + ew * STG_BYTES;
     uint32_t acc_it = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
       const Tile tl = decode<KIND, BK>(t, p, offs, tstart);
-      const bool empty_k = tl.nkb == 0;  // only wgrad tiles of experts without rows
-      int buf = 0;
-      if (!empty_k) {
-        buf = acc_it & 1;
-        const uint32_t aph = (acc_it >> 1) & 1u;
-        if (!wait_bar(&sm->tfull[buf], aph, &sm->abort_flag, p.err)) break;
-        ptx::tc_fence_after();
-      }
+      if (tl.nkb == 0) continue;
+      const int buf = acc_it & 1;
+      const uint32_t aph = (acc_it >> 1) & 1u;
+      if (!wait_bar(&sm->tfull[buf], aph, &sm->abort_flag, p.err)) break;
+      ptx::tc_fence_after();
       const uint32_t tbase = tmem + static_cast<uint32_t>(buf * BN) + (static_cast<uint32_t>(q * 32) << 16);
-      if (Tr::kragged) {
-        // this warp's 32 rows x 128 columns: two 32x64 boxes, 128-byte swizzled
-        uint8_t* st = out_stage + ew * STAGE_OUT_BYTES;
-        if (lane == 0) ptx::bulk_wait_read();  // previous tile's stores have read the staging
-        __syncwarp();
-        for (int c = 0; c < 4; ++c) {
-          uint32_t r[32];
-          if (!empty_k) {
-            ptx::tmem_ld32(tbase + (half * 4 + c) * 32, r);
-            ptx::tmem_wait_ld();
-          } else {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) r[i] = 0u;
-          }
-          uint8_t* box = st + (c >> 1) * (STAGE_OUT_BYTES / 2) + lane * 128;
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            uint32_t w[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              __nv_bfloat162 h2 = __floats2bfloat162_rn(__uint_as_float(r[8 * j + 2 * i]),
-                                                       __uint_as_float(r[8 * j + 2 * i + 1]));
-              w[i] = *reinterpret_cast<uint32_t*>(&h2);
-            }
-            const int chunk = ((c & 1) * 4 + j) ^ (lane & 7);
-            *reinterpret_cast<uint4*>(box + chunk * 16) = make_uint4(w[0], w[1], w[2], w[3]);
-          }
-        }
-        ptx::fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          const int m = tl.m0 + q * 32;
-#pragma unroll
-          for (int bx = 0; bx < 2; ++bx) {
-            const int n = tl.n_idx * BN + (half * 4 + 2 * bx) * 32;
-            const void* src = st + bx * (STAGE_OUT_BYTES / 2);
-            if (KIND == WGRAD2) ptx::tma_store_3d(&tmC0, src, n, m, tl.e);
-            else if (n < p.f) ptx::tma_store_3d(&tmC0, src, n, m, tl.e);
-            else ptx::tma_store_3d(&tmC1, src, n - p.f, m, tl.e);
-          }
-          ptx::bulk_commit();
-        }
-      } else {
-        epilogue_tile<KIND>(p, tl, tbase, q * 32 + lane, half * NC / 2, (half + 1) * NC / 2, empty_k);
-      }
-      if (!empty_k) {
-        ptx::tc_fence_before();
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(&sm->tempty[buf]);
-        ++acc_it;
-      }
+      if constexpr (KIND == ROUTER)
+        epilogue_tile<KIND>(p, tl, tbase, q * 32 + lane, half * NC / 2, (half + 1) * NC / 2, false);
+      else
+        epilogue_tile_staged<KIND>(p, tl, tbase, q, lane, half * NC / 2, (half + 1) * NC / 2, stg);
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&sm->tempty[buf]);
+      ++acc_it;
     }
   }
 
-  if (Tr::kragged && warp >= 2 && lane == 0) ptx::bulk_wait_all();  // output stores done before exit
   ptx::tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -298,20 +222,19 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 
 template <int KIND>
 size_t smem_bytes(int E) {
-  return 1024 + n_stages<KIND>() * STAGE_BYTES + out_bytes<KIND>() + sizeof(Smem) + 2 * (E + 1) * sizeof(int) + 64;
+  return 1024 + STAGES * STAGE_BYTES + OUT_STG_BYTES + sizeof(Smem) + 2 * (E + 1) * sizeof(int) + 64;
 }
 
 template <int KIND>
 cudaError_t launch(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1, const Params& p,
-                   long max_tiles, cudaStream_t st, const CUtensorMap* c0 = nullptr,
-                   const CUtensorMap* c1 = nullptr) {
+                   long max_tiles, cudaStream_t st) {
   if (max_tiles <= 0) return cudaSuccess;
   const size_t smem = smem_bytes<KIND>(p.E);
   cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   const int grid = static_cast<int>(max_tiles < sm_count() ? max_tiles : sm_count());
-  MOE_COUNTED tc_gemm_kernel<KIND><<<grid, NUM_THREADS, smem, st>>>(a, b0, b1, c0 ? *c0 : a, c1 ? *c1 : a, p);
+  MOE_COUNTED tc_gemm_kernel<KIND><<<grid, NUM_THREADS, smem, st>>>(a, b0, b1, p);
   return cudaGetLastError();
 }
 

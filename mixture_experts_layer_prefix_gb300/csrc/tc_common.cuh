@@ -173,6 +173,76 @@ __device__ __forceinline__ void load_bf16x32(const __nv_bfloat16* src, float* v)
   }
 }
 
+// Row-segment traffic through a per-warp staging buffer. An epilogue thread
+// owns one output row (its TMEM lane), so a direct store instruction of a
+// warp touches 32 rows with 16 bytes each. Staged in shared memory (32 rows x
+// 64 bytes, 16-byte granules XOR-swizzled by row pair so that the row-wise and
+// the column-wise accesses are both free of bank conflicts), each global
+// instruction moves 8 rows x 64 contiguous bytes.
+constexpr int STG_BYTES = 32 * 64;
+__device__ __forceinline__ int stg_off(int r, int g) { return r * 64 + ((g ^ ((r >> 1) & 3)) << 4); }
+
+__device__ __forceinline__ void pack_bf16x32(const float* v, uint32_t (&w)[16]) {
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+    w[i] = *reinterpret_cast<uint32_t*>(&h);
+  }
+}
+
+// Lane r holds w = row r's 32 bf16 values; dst is row 0 of the warp's 32 rows
+// (leading dimension ld elements). Rows >= nrows are not written.
+__device__ __forceinline__ void warp_store_rows(uint8_t* stg, const uint32_t (&w)[16], __nv_bfloat16* dst,
+                                                size_t ld, int nrows, int lane) {
+#pragma unroll
+  for (int g = 0; g < 4; ++g)
+    *reinterpret_cast<uint4*>(stg + stg_off(lane, g)) = make_uint4(w[4 * g], w[4 * g + 1], w[4 * g + 2], w[4 * g + 3]);
+  __syncwarp();
+  const int g = lane & 3;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int r = 8 * i + (lane >> 2);
+    const uint4 v = *reinterpret_cast<const uint4*>(stg + stg_off(r, g));
+    if (r < nrows) *reinterpret_cast<uint4*>(dst + (size_t)r * ld + 8 * g) = v;
+  }
+  __syncwarp();
+}
+
+// The reverse, in two halves so that the global latency can overlap other
+// work: issue reads the warp's 32 rows x 32 bf16 from src coalesced (rows >=
+// nrows read as zero); finish hands lane r row r (16 packed bf16 pairs).
+__device__ __forceinline__ void warp_load_rows_issue(uint4 (&t)[4], const __nv_bfloat16* src, size_t ld, int nrows,
+                                                     int lane) {
+  const int g = lane & 3;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int r = 8 * i + (lane >> 2);
+    t[i] = r < nrows ? *reinterpret_cast<const uint4*>(src + (size_t)r * ld + 8 * g) : make_uint4(0, 0, 0, 0);
+  }
+}
+__device__ __forceinline__ void warp_load_rows_finish(uint8_t* stg, const uint4 (&t)[4], uint32_t (&w)[16],
+                                                      int lane) {
+  const int g0 = lane & 3;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) *reinterpret_cast<uint4*>(stg + stg_off(8 * i + (lane >> 2), g0)) = t[i];
+  __syncwarp();
+#pragma unroll
+  for (int g = 0; g < 4; ++g) {
+    const uint4 q = *reinterpret_cast<const uint4*>(stg + stg_off(lane, g));
+    w[4 * g] = q.x;
+    w[4 * g + 1] = q.y;
+    w[4 * g + 2] = q.z;
+    w[4 * g + 3] = q.w;
+  }
+  __syncwarp();
+}
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
 // Row quantisation of a 32-column chunk of a bf16 output (values rounded to
 // bf16 first: the GEMMs that read it see the stored values). Codes go to
 // qout[row][col..col+32), the scale to qsc[row][col/32] of a [rows][ld] matrix.
@@ -189,6 +259,98 @@ __device__ __forceinline__ void quant_chunk_bf16(const Params& p, long row, int 
 // TBN: columns of the tile (256, or 128 for the narrower MXFP8 tiles).
 // QUANT: also write the MXFP8 row quantisation of A (FPROP1) or dh (DGRAD2)
 // when p.qout is set.
+// Staged form of the row-tile epilogue (see warp_store_rows): every lane of
+// the warp takes part; stg is the warp's STG_BYTES buffer. Row-tile kinds
+// FPROP1, FPROP2, DGRAD1, DGRAD2 without quantisation.
+template <int KIND, int TBN = BN>
+__device__ __forceinline__ void epilogue_tile_staged(const Params& p, const Tile& tl, uint32_t tbase, int q, int lane,
+                                                     int c_beg, int c_end, uint8_t* stg) {
+  static_assert(KIND == FPROP1 || KIND == FPROP2 || KIND == DGRAD1 || KIND == DGRAD2, "row-tile kinds");
+  const int wrow = tl.m0 + q * 32;  // the warp's first row
+  const int nrows = max(0, min(32, tl.row_end - wrow));
+  uint32_t w[16];
+  if (KIND == FPROP1) {
+    const int n0 = tl.n_idx * 128;
+    __nv_bfloat16* h = static_cast<__nv_bfloat16*>(p.out0) + (size_t)wrow * 2 * p.f;
+    __nv_bfloat16* a = static_cast<__nv_bfloat16*>(p.out1) + (size_t)wrow * p.f;
+    for (int c = c_beg; c < c_end; ++c) {
+      uint32_t rg[32], ru[32];
+      ptx::tmem_ld32(tbase + c * 32, rg);
+      ptx::tmem_ld32(tbase + 128 + c * 32, ru);
+      ptx::tmem_wait_ld();
+      const int n = n0 + c * 32;
+      if (n >= p.f) continue;
+      uint32_t wa[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const float g0 = __uint_as_float(rg[2 * i]), g1 = __uint_as_float(rg[2 * i + 1]);
+        const float u0 = __uint_as_float(ru[2 * i]), u1 = __uint_as_float(ru[2 * i + 1]);
+        wa[i] = pack_bf16x2(silu_f(g0) * u0, silu_f(g1) * u1);
+        w[i] = pack_bf16x2(g0, g1);
+      }
+      warp_store_rows(stg, w, h + n, 2 * (size_t)p.f, nrows, lane);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(__uint_as_float(ru[2 * i]), __uint_as_float(ru[2 * i + 1]));
+      warp_store_rows(stg, w, h + p.f + n, 2 * (size_t)p.f, nrows, lane);
+      warp_store_rows(stg, wa, a + n, p.f, nrows, lane);
+    }
+  } else if (KIND == DGRAD2) {
+    // dh_g = da * h_u * silu'(h_g), dh_u = da * silu(h_g); the reads of h are
+    // issued before the accumulator load so their latency overlaps it
+    const int n0 = tl.n_idx * TBN;
+    const __nv_bfloat16* h = static_cast<const __nv_bfloat16*>(p.aux) + (size_t)wrow * 2 * p.f;
+    __nv_bfloat16* dh = static_cast<__nv_bfloat16*>(p.out0) + (size_t)wrow * 2 * p.f;
+    for (int c = c_beg; c < c_end; ++c) {
+      const int n = n0 + c * 32;
+      const bool nok = n < p.N;
+      uint4 tg[4], tu[4];
+      if (nok) {
+        warp_load_rows_issue(tg, h + n, 2 * (size_t)p.f, nrows, lane);
+        warp_load_rows_issue(tu, h + p.f + n, 2 * (size_t)p.f, nrows, lane);
+      }
+      uint32_t r[32];
+      ptx::tmem_ld32(tbase + c * 32, r);
+      ptx::tmem_wait_ld();
+      if (!nok) continue;
+      uint32_t hg[16], hu[16], wu[16];
+      warp_load_rows_finish(stg, tg, hg, lane);
+      warp_load_rows_finish(stg, tu, hu, lane);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        float dg2[2], du2[2];
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          const float g = j ? bf16_hi(hg[i]) : bf16_lo(hg[i]);
+          const float u = j ? bf16_hi(hu[i]) : bf16_lo(hu[i]);
+          const float da = __uint_as_float(r[2 * i + j]);
+          const float s = sigmoid_f(g);
+          dg2[j] = da * u * s * (1.0f + g * (1.0f - s));
+          du2[j] = da * g * s;
+        }
+        w[i] = pack_bf16x2(dg2[0], dg2[1]);
+        wu[i] = pack_bf16x2(du2[0], du2[1]);
+      }
+      warp_store_rows(stg, w, dh + n, 2 * (size_t)p.f, nrows, lane);
+      warp_store_rows(stg, wu, dh + p.f + n, 2 * (size_t)p.f, nrows, lane);
+    }
+  } else {  // FPROP2, DGRAD1: plain bf16 store
+    const int n0 = tl.n_idx * TBN;
+    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out0) + (size_t)wrow * p.N;
+    for (int c = c_beg; c < c_end; ++c) {
+      uint32_t r[32];
+      ptx::tmem_ld32(tbase + c * 32, r);
+      ptx::tmem_wait_ld();
+      const int n = n0 + c * 32;
+      if (n >= p.N) continue;
+      float v[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+      pack_bf16x32(v, w);
+      warp_store_rows(stg, w, out + n, p.N, nrows, lane);
+    }
+  }
+}
+
 template <int KIND, bool QUANT = false, int TBN = BN>
 __device__ __forceinline__ void epilogue_tile(const Params& p, const Tile& tl, uint32_t tbase, int row_in_tile,
                                               int c_beg, int c_end, bool zero) {

@@ -116,11 +116,13 @@ moe_status moe_combine_bwd(const void* dy, const void* y_perm, const float* gate
 
 /* Router backward (softmax over the selected logits):
      dlogits[t][i] = g_i * (dg_i - sum_j g_j dg_j) for i in top-k, 0 otherwise
-     dw_router[e][c] = sum over rows r of expert e of dlogits[t(r)][e] * x_perm[r][c]
-   with t(r) = src_row[r] / k. dlogits [T][E] fp32; dw_router [E][d] fp32;
-   x_perm [T*k][d] dtype (rows of x placed by moe_permute). */
+     dw_router[e][c] = sum over rows r of expert e of dlogits[t(r)][e] * x[t(r)][c]
+   with t(r) = src_row[r] / k (fp32 sum in row order, i.e. ascending token).
+   dlogits [T][E] fp32; dw_router [E][d] fp32; x [T][d] dtype, the layer's
+   input (each token's row is read once per selected expert, from L2 after
+   the first). */
 moe_status moe_route_bwd(const float* dgates, const float* gates, const int32_t* topk_idx,
-                         const int32_t* offsets, const int32_t* src_row, const void* x_perm,
+                         const int32_t* offsets, const int32_t* src_row, const void* x,
                          int dtype, int T, int d, int E, int k, float* dlogits, float* dw_router,
                          void* stream);
 

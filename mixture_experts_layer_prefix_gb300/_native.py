@@ -124,10 +124,10 @@ def moe_combine_bwd(dy, y_perm, gates, dest_row, dtype, T, d, k, dy_perm, dgates
                                                    d, k, _p(dy_perm), _p(dgates), _s(stream)))
 
 
-def moe_route_bwd(dgates, gates, topk_idx, offsets, src_row, x_perm, dtype, T, d, E, k, dlogits,
+def moe_route_bwd(dgates, gates, topk_idx, offsets, src_row, x, dtype, T, d, E, k, dlogits,
                   dw_router, stream=None):
     _chk("moe_route_bwd", load().moe_route_bwd(_p(dgates), _p(gates), _p(topk_idx), _p(offsets),
-                                               _p(src_row), _p(x_perm), dtype, T, d, E, k, _p(dlogits),
+                                               _p(src_row), _p(x), dtype, T, d, E, k, _p(dlogits),
                                                _p(dw_router), _s(stream)))
 
 

@@ -243,7 +243,7 @@ moe_status moe_combine_bwd(const void* dy, const void* y_perm, const float* gate
 }
 
 moe_status moe_route_bwd(const float* dgates, const float* gates, const int32_t* topk_idx,
-                         const int32_t* offsets, const int32_t* src_row, const void* x_perm,
+                         const int32_t* offsets, const int32_t* src_row, const void* x,
                          int dtype, int T, int d, int E, int k, float* dlogits, float* dw_router,
                          void* stream) {
   MOE_TRY(check_dims(T, d, E, k));
@@ -251,14 +251,14 @@ moe_status moe_route_bwd(const float* dgates, const float* gates, const int32_t*
   dtype = storage(dtype);
   MOE_NEED(offsets); MOE_NEED(dw_router);
   if (T > 0) {
-    MOE_NEED(dgates); MOE_NEED(gates); MOE_NEED(topk_idx); MOE_NEED(src_row); MOE_NEED(x_perm);
+    MOE_NEED(dgates); MOE_NEED(gates); MOE_NEED(topk_idx); MOE_NEED(src_row); MOE_NEED(x);
     MOE_NEED(dlogits);
   }
   if (dtype == MOE_F32)
-    MOE_CUDA_TRY(launch_route_bwd<float>(dgates, gates, topk_idx, offsets, src_row, x_perm, T, d, E, k,
+    MOE_CUDA_TRY(launch_route_bwd<float>(dgates, gates, topk_idx, offsets, src_row, x, T, d, E, k,
                                          dlogits, dw_router, S(stream)));
   else
-    MOE_CUDA_TRY(launch_route_bwd<__nv_bfloat16>(dgates, gates, topk_idx, offsets, src_row, x_perm, T,
+    MOE_CUDA_TRY(launch_route_bwd<__nv_bfloat16>(dgates, gates, topk_idx, offsets, src_row, x, T,
                                                  d, E, k, dlogits, dw_router, S(stream)));
   return MOE_OK;
 }

@@ -32,7 +32,7 @@ cudaError_t launch_permute_bwd(const void* dx_perm, int Tn, int d, int E, int k,
                                const void* w_r, void* dx, cudaStream_t st);
 template <typename T>
 cudaError_t launch_route_bwd(const float* dgates, const float* gates, const int32_t* topk_idx,
-                             const int32_t* offsets, const int32_t* src_row, const void* x_perm,
+                             const int32_t* offsets, const int32_t* src_row, const void* x,
                              int Tn, int d, int E, int k, float* dlogits, float* dw_r,
                              cudaStream_t st);
 

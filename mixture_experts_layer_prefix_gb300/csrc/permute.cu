@@ -202,13 +202,16 @@ router_dlogits_kernel(const float* __restrict__ dgates, const float* __restrict_
   }
 }
 
-// dw_r[e][c] = sum over rows r of expert e of dlogits[t(r)][e] * x_perm[r][c].
-// Grid (E, ceil(d / 256)); 8 warps split the rows, each lane owns 8 columns;
-// warps are reduced in fixed order through shared memory.
+// dw_r[e][c] = sum over rows r of expert e of dlogits[t(r)][e] * x[t(r)][c],
+// t(r) = src_row[r] / k. The token rows are gathered from x (T rows, which
+// stay in L2 across the k experts that read each) rather than from the
+// k-times larger x_perm. Grid (E, ceil(d / 256)); 8 warps split the rows,
+// each lane owns 8 columns; warps are reduced in fixed order through shared
+// memory.
 template <typename T>
 __global__ void __launch_bounds__(256)
 router_dw_kernel(const float* __restrict__ dlogits, const int32_t* __restrict__ offsets,
-                 const int32_t* __restrict__ src_row, const T* __restrict__ x_perm, int d, int E,
+                 const int32_t* __restrict__ src_row, const T* __restrict__ x, int d, int E,
                  int k, float* __restrict__ dw_r) {
   constexpr int VN = Vec16<T>::N;
   constexpr int COLS = 32 * VN;  // columns per warp pass
@@ -226,9 +229,9 @@ router_dw_kernel(const float* __restrict__ dlogits, const int32_t* __restrict__ 
         float v[4][VN], w[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-          const int rr = r + 8 * u;
-          w[u] = dlogits[(size_t)(src_row[rr] / k) * E + e];
-          Vec16<T>::load(x_perm + (size_t)rr * d + c, v[u]);
+          const int t = src_row[r + 8 * u] / k;
+          w[u] = dlogits[(size_t)t * E + e];
+          Vec16<T>::load(x + (size_t)t * d + c, v[u]);
         }
 #pragma unroll
         for (int u = 0; u < 4; ++u)
@@ -237,8 +240,9 @@ router_dw_kernel(const float* __restrict__ dlogits, const int32_t* __restrict__ 
       }
       for (; r < r1; r += 8) {
         float v[VN];
-        const float w = dlogits[(size_t)(src_row[r] / k) * E + e];
-        Vec16<T>::load(x_perm + (size_t)r * d + c, v);
+        const int t = src_row[r] / k;
+        const float w = dlogits[(size_t)t * E + e];
+        Vec16<T>::load(x + (size_t)t * d + c, v);
 #pragma unroll
         for (int i = 0; i < VN; ++i) acc[i] = fmaf(w, v[i], acc[i]);
       }
@@ -303,14 +307,14 @@ cudaError_t launch_permute_bwd(const void* dx_perm, int Tn, int d, int E, int k,
 
 template <typename T>
 cudaError_t launch_route_bwd(const float* dgates, const float* gates, const int32_t* topk_idx,
-                             const int32_t* offsets, const int32_t* src_row, const void* x_perm,
+                             const int32_t* offsets, const int32_t* src_row, const void* x,
                              int Tn, int d, int E, int k, float* dlogits, float* dw_r,
                              cudaStream_t st) {
   if (Tn > 0)
     MOE_COUNTED router_dlogits_kernel<<<row_grid<T>(Tn), kRowWarps * 32, 0, st>>>(dgates, gates, topk_idx, Tn,
                                                                        E, k, dlogits);
   dim3 grid(E, (d + 255) / 256);
-  MOE_COUNTED router_dw_kernel<T><<<grid, 256, 0, st>>>(dlogits, offsets, src_row, static_cast<const T*>(x_perm),
+  MOE_COUNTED router_dw_kernel<T><<<grid, 256, 0, st>>>(dlogits, offsets, src_row, static_cast<const T*>(x),
                                             d, E, k, dw_r);
   return cudaGetLastError();
 }

@@ -108,7 +108,7 @@ def forward(p: Params, b: Buffers, logits_in: bool = False, stream=None):
 def backward(p: Params, b: Buffers, stream=None):
     T, d, E, k, f, dt = b.T, b.d, b.E, b.k, b.f, b.dtype
     N.moe_combine_bwd(p.dy, b.y_perm, b.gates, b.dest_row, dt, T, d, k, b.dy_perm, b.dgates, stream)
-    N.moe_route_bwd(b.dgates, b.gates, b.topk_idx, b.offsets, b.src_row, b.x_perm, dt, T, d, E, k,
+    N.moe_route_bwd(b.dgates, b.gates, b.topk_idx, b.offsets, b.src_row, p.x, dt, T, d, E, k,
                     b.dlogits, b.dw_router, stream)
     N.moe_grouped_mlp_bwd(b.dy_perm, b.x_perm, b.h_save, b.a_save, p.w_gate, p.w_up, p.w_down, dt,
                           b.offsets, b.R, E, d, f, b.dx_perm, b.dw_gate, b.dw_up, b.dw_down, b.workspace,
@@ -121,3 +121,71 @@ def step(p: Params, b: Buffers, stream=None):
     """One forward+backward pass of the layer."""
     forward(p, b, stream=stream)
     backward(p, b, stream=stream)
+
+
+class HostPipeline:
+    """Forward+backward over a sequence of host batches with the copies hidden.
+
+    Every step's x and dy come from pinned host memory and its y and dx go back
+    to pinned host memory. While step i computes on the caller's stream, step
+    i+1's inputs travel host->device on one copy stream and step i-1's outputs
+    travel device->host on another. The device inputs (x, dy) and outputs
+    (y, dx) are double-buffered; every other buffer of `b` is reused by each
+    step in turn, which the compute stream orders. After `run`, `p.x`, `p.dy`,
+    `b.y` and `b.dx` refer to the buffers of the last step.
+    """
+
+    def __init__(self, p: Params, b: Buffers):
+        self.p, self.b = p, b
+        self.xin = [p.x, torch.empty_like(p.x)]
+        self.dyin = [p.dy, torch.empty_like(p.dy)]
+        self.yout = [b.y, torch.empty_like(b.y)]
+        self.dxout = [b.dx, torch.empty_like(b.dx)]
+        dev = p.x.device
+        self.h2d = torch.cuda.Stream(dev)
+        self.d2h = torch.cuda.Stream(dev)
+        self.loaded = [torch.cuda.Event(), torch.cuda.Event()]    # slot's inputs are on the device
+        self.computed = [torch.cuda.Event(), torch.cuda.Event()]  # slot's step finished
+        self.drained = [torch.cuda.Event(), torch.cuda.Event()]   # slot's outputs are on the host
+
+    def run(self, xs, dys, ys, dxs, stream=None):
+        """xs, dys: pinned host inputs [T, d] per step; ys, dxs: pinned host
+        outputs [T, d] per step (written when the caller's stream reaches the
+        end of this call)."""
+        comp = stream if stream is not None else torch.cuda.current_stream()
+        p, b = self.p, self.b
+        n = len(xs)
+        used = [False, False]
+        self.h2d.wait_stream(comp)
+        self.d2h.wait_stream(comp)
+
+        def load(i):
+            s = i % 2
+            with torch.cuda.stream(self.h2d):
+                if used[s]:
+                    self.h2d.wait_event(self.computed[s])
+                self.xin[s].copy_(xs[i], non_blocking=True)
+                self.dyin[s].copy_(dys[i], non_blocking=True)
+                self.loaded[s].record(self.h2d)
+
+        if n:
+            load(0)
+        for i in range(n):
+            s = i % 2
+            if i + 1 < n:
+                load(i + 1)
+            comp.wait_event(self.loaded[s])
+            if used[s]:
+                comp.wait_event(self.drained[s])
+            p.x, p.dy, b.y, b.dx = self.xin[s], self.dyin[s], self.yout[s], self.dxout[s]
+            forward(p, b, stream=comp)
+            backward(p, b, stream=comp)
+            self.computed[s].record(comp)
+            used[s] = True
+            with torch.cuda.stream(self.d2h):
+                self.d2h.wait_event(self.computed[s])
+                ys[i].copy_(self.yout[s], non_blocking=True)
+                dxs[i].copy_(self.dxout[s], non_blocking=True)
+                self.drained[s].record(self.d2h)
+        comp.wait_stream(self.d2h)
+        comp.wait_stream(self.h2d)

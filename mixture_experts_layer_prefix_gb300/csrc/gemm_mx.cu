@@ -87,22 +87,31 @@ __device__ __forceinline__ void tmem_cp_32x128b_x4(uint32_t taddr, uint64_t desc
   asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(desc) : "memory");
 }
 
-// bf16 store of one 32-column chunk of a plain or wgrad output.
+// bf16 store of one 32-column chunk of a plain or wgrad output: the warp's
+// 32 rows (lane = row), packed bf16 pairs, through the warp's staging buffer.
 template <int KIND, int TBN>
-__device__ __forceinline__ void store_chunk(const Params& p, const Tile& tl, int r_tile, int c, const float* v) {
+__device__ __forceinline__ void store_chunk(const Params& p, const Tile& tl, int q, int lane, int c,
+                                            const uint32_t (&w)[16], uint8_t* stg) {
   const int n = tl.n_idx * TBN + c * 32;
+  if (n >= p.N) return;
   if (Traits<KIND>::kragged) {
-    const int m = tl.m0 + r_tile;
-    if (m >= p.M || n >= p.N) return;
+    const int m = tl.m0 + q * 32;
+    const int nrows = max(0, min(32, p.M - m));
     __nv_bfloat16* dst;
-    if (KIND == WGRAD2) dst = static_cast<__nv_bfloat16*>(p.out0) + ((size_t)tl.e * p.M + m) * p.N + n;
-    else dst = n < p.f ? static_cast<__nv_bfloat16*>(p.out0) + ((size_t)tl.e * p.d + m) * p.f + n
-                       : static_cast<__nv_bfloat16*>(p.out1) + ((size_t)tl.e * p.d + m) * p.f + (n - p.f);
-    store_bf16x32(dst, v);
+    size_t ld;
+    if (KIND == WGRAD2) {
+      dst = static_cast<__nv_bfloat16*>(p.out0) + ((size_t)tl.e * p.M + m) * p.N + n;
+      ld = p.N;
+    } else {
+      dst = n < p.f ? static_cast<__nv_bfloat16*>(p.out0) + ((size_t)tl.e * p.d + m) * p.f + n
+                    : static_cast<__nv_bfloat16*>(p.out1) + ((size_t)tl.e * p.d + m) * p.f + (n - p.f);
+      ld = p.f;
+    }
+    warp_store_rows(stg, w, dst, ld, nrows, lane);
   } else {
-    const int row = tl.m0 + r_tile;
-    if (row >= tl.row_end || n >= p.N) return;
-    store_bf16x32(static_cast<__nv_bfloat16*>(p.out0) + (size_t)row * p.N + n, v);
+    const int wrow = tl.m0 + q * 32;
+    const int nrows = max(0, min(32, tl.row_end - wrow));
+    warp_store_rows(stg, w, static_cast<__nv_bfloat16*>(p.out0) + (size_t)wrow * p.N + n, p.N, nrows, lane);
   }
 }
 
@@ -113,13 +122,17 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   using Tr = Traits<KIND>;
   using G = Geo<TBN>;
   static_assert(KIND != FPROP1 || TBN == 256, "GEMM1 tiles pair 128 gate with 128 up columns");
+  static_assert(!(Tr::kragged && Geo<TBN>::ACC == 2), "weight-gradient tiles use the single 256-column accumulator");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sc_area = smem + STAGES * G::STAGE_BYTES;
-  Smem* sm = reinterpret_cast<Smem*>(sc_area + STAGES * G::SC_BYTES);
+  uint8_t* stg_area = sc_area + STAGES * G::SC_BYTES;  // epilogue staging, STG_BYTES per warp
+  Smem* sm = reinterpret_cast<Smem*>(stg_area + NUM_EPI_WARPS * STG_BYTES);
   int* offs = reinterpret_cast<int*>(sm + 1);
   int* tstart = offs + (p.E + 1);
-  int* wstart = tstart + (p.E + 1);  // wgrad: first packed scale word row of each expert segment
+  // wgrad kinds use no tile table: their second table holds the first packed
+  // scale word row of each expert segment
+  int* wstart = tstart;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   build_tile_table<KIND, NUM_THREADS>(p, offs, tstart);
@@ -339,15 +352,16 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     // ============================================================ epilogue
     const int ew = warp - 2, q = warp & 3, half = ew >> 2;
     const int r_tile = q * 32 + lane;
+    uint8_t* stg = stg_area + ew * STG_BYTES;
     constexpr int NC = KIND == FPROP1 ? 4 : TBN / 32;  // chunks of the tile (FPROP1: gate/up pairs)
     uint32_t acc_it = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
       const Tile tl = decode<KIND, BK>(t, p, offs, tstart);
-      if (tl.nkb == 0) {  // wgrad of an expert without rows
-        float z[32];
+      if (tl.nkb == 0) {  // wgrad of an expert without rows: dW_e = 0
+        uint32_t z[16];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) z[i] = 0.0f;
-        for (int c = half * NC / 2; c < (half + 1) * NC / 2; ++c) store_chunk<KIND, TBN>(p, tl, r_tile, c, z);
+        for (int i = 0; i < 16; ++i) z[i] = 0u;
+        for (int c = half * NC / 2; c < (half + 1) * NC / 2; ++c) store_chunk<KIND, TBN>(p, tl, q, lane, c, z, stg);
         continue;
       }
       if (KIND == DGRAD2) {
@@ -370,56 +384,62 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       const uint32_t tbase = tmem + static_cast<uint32_t>(buf * TBN) + (static_cast<uint32_t>(q * 32) << 16);
       if (G::ACC == 2 || KIND == DGRAD2) {
         // double-buffered (or too many registers to drain first): epilogue straight from TMEM
-        epilogue_tile<KIND, true, TBN>(p, tl, tbase, r_tile, half * NC / 2, (half + 1) * NC / 2, false);
+        if constexpr (!Tr::kragged)
+          epilogue_tile_staged<KIND, TBN, true>(p, tl, tbase, q, lane, half * NC / 2, (half + 1) * NC / 2, stg);
         ptx::tc_fence_before();
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(&sm->tempty[buf]);
       } else {
-        // single accumulator: copy this warp's 128 columns out, release it, then store
-        uint32_t acc[4][32];
-        if (KIND == FPROP1) {
-          ptx::tmem_ld32(tbase + (2 * half) * 32, acc[0]);
-          ptx::tmem_ld32(tbase + (2 * half + 1) * 32, acc[1]);
-          ptx::tmem_ld32(tbase + 128 + (2 * half) * 32, acc[2]);
-          ptx::tmem_ld32(tbase + 128 + (2 * half + 1) * 32, acc[3]);
-        } else {
+        // single accumulator: copy this warp's 128 columns out as packed bf16,
+        // release it, then store
+        if constexpr (KIND == FPROP1) {
+          uint32_t wg[2][16], wu[2][16], wa[2][16];
 #pragma unroll
-          for (int c = 0; c < 4; ++c) ptx::tmem_ld32(tbase + (4 * half + c) * 32, acc[c]);
-        }
-        ptx::tmem_wait_ld();
-        ptx::tc_fence_before();
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(&sm->tempty[buf]);
-        if (KIND == FPROP1) {
-          const int row = tl.m0 + r_tile;
-          if (row < tl.row_end) {
-            __nv_bfloat16* h = static_cast<__nv_bfloat16*>(p.out0) + (size_t)row * 2 * p.f;
-            __nv_bfloat16* ao = static_cast<__nv_bfloat16*>(p.out1) + (size_t)row * p.f;
+          for (int cc = 0; cc < 2; ++cc) {
+            uint32_t rg[32], ru[32];
+            ptx::tmem_ld32(tbase + (2 * half + cc) * 32, rg);
+            ptx::tmem_ld32(tbase + 128 + (2 * half + cc) * 32, ru);
+            ptx::tmem_wait_ld();
 #pragma unroll
-            for (int cc = 0; cc < 2; ++cc) {
-              const int n = tl.n_idx * 128 + (2 * half + cc) * 32;
-              if (n >= p.f) continue;
-              float hg[32], hu[32], av[32];
-#pragma unroll
-              for (int i = 0; i < 32; ++i) {
-                hg[i] = __uint_as_float(acc[cc][i]);
-                hu[i] = __uint_as_float(acc[2 + cc][i]);
-                av[i] = silu_f(hg[i]) * hu[i];
-              }
-              store_bf16x32(h + n, hg);
-              store_bf16x32(h + p.f + n, hu);
-              store_bf16x32(ao + n, av);
-              if (p.qout) quant_chunk_bf16(p, row, p.f, n, av);
+            for (int i = 0; i < 16; ++i) {
+              const float g0 = __uint_as_float(rg[2 * i]), g1 = __uint_as_float(rg[2 * i + 1]);
+              const float u0 = __uint_as_float(ru[2 * i]), u1 = __uint_as_float(ru[2 * i + 1]);
+              wg[cc][i] = pack_bf16x2(g0, g1);
+              wu[cc][i] = pack_bf16x2(u0, u1);
+              wa[cc][i] = pack_bf16x2(silu_f(g0) * u0, silu_f(g1) * u1);
             }
           }
+          ptx::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(&sm->tempty[buf]);
+          const int wrow = tl.m0 + q * 32;
+          const int nrows = max(0, min(32, tl.row_end - wrow));
+          __nv_bfloat16* h = static_cast<__nv_bfloat16*>(p.out0) + (size_t)wrow * 2 * p.f;
+          __nv_bfloat16* ao = static_cast<__nv_bfloat16*>(p.out1) + (size_t)wrow * p.f;
+#pragma unroll
+          for (int cc = 0; cc < 2; ++cc) {
+            const int n = tl.n_idx * 128 + (2 * half + cc) * 32;
+            if (n >= p.f) continue;
+            warp_store_rows(stg, wg[cc], h + n, 2 * (size_t)p.f, nrows, lane);
+            warp_store_rows(stg, wu[cc], h + p.f + n, 2 * (size_t)p.f, nrows, lane);
+            warp_store_rows(stg, wa[cc], ao + n, p.f, nrows, lane);
+            if (p.qout) quant_rows_staged(p, stg, wa[cc], wrow, nrows, p.f, n, lane);
+          }
         } else {
+          uint32_t w[4][16];
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
-            float v[32];
+            uint32_t r[32];
+            ptx::tmem_ld32(tbase + (4 * half + c) * 32, r);
+            ptx::tmem_wait_ld();
 #pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(acc[c][i]);
-            store_chunk<KIND, TBN>(p, tl, r_tile, 4 * half + c, v);
+            for (int i = 0; i < 16; ++i) w[c][i] = pack_bf16x2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
           }
+          ptx::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(&sm->tempty[buf]);
+#pragma unroll
+          for (int c = 0; c < 4; ++c) store_chunk<KIND, TBN>(p, tl, q, lane, 4 * half + c, w[c], stg);
         }
       }
       ++acc_it;
@@ -436,8 +456,8 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 
 template <int TBN>
 size_t smem_bytes(int E) {
-  return 1024 + STAGES * Geo<TBN>::STAGE_BYTES + STAGES * Geo<TBN>::SC_BYTES + sizeof(Smem) +
-         3 * (E + 1) * sizeof(int) + 64;
+  return 1024 + STAGES * Geo<TBN>::STAGE_BYTES + STAGES * Geo<TBN>::SC_BYTES + NUM_EPI_WARPS * STG_BYTES +
+         sizeof(Smem) + 2 * (E + 1) * sizeof(int) + 64;
 }
 
 template <int KIND, int TBN>

@@ -13,8 +13,9 @@
 //   cols kernel: blocks of 32 consecutive rows of one column, starting at each
 //                segment's first row (segments = per-expert row ranges from
 //                the device offsets); a segment's last block is zero-padded.
-//                Each thread owns 8 columns (16-byte loads); two passes over
-//                the block's rows (block maxima, then conversion).
+//                Each thread owns 8 columns (16-byte loads) and keeps the
+//                block's 32 rows in registers between the maxima and the
+//                conversion.
 #include <cuda_fp8.h>
 
 #include "common.cuh"
@@ -44,9 +45,9 @@ quant_rows_kernel(const __nv_bfloat16* __restrict__ src, long nblocks, uint8_t* 
 // PACKED: scales go to a [words][C] table of 32-bit words, word w of segment
 // g holding its blocks 4w..4w+3 in bytes 0..3 (words of segment g start at
 // sum_{h<g} ceil(blocks_h / 4)); bytes past a segment's last block are 127.
-// A CTA handles kColBlockRows block rows of 1024 columns; each thread owns 8
-// consecutive columns: a first pass over the 32 rows finds the 8 block
-// maxima, a second pass (rows now in L1) converts and stores 8 codes per row.
+// A CTA handles kColBlockRows block rows of 512 columns; each thread owns 4
+// consecutive columns and holds its 32 x 4 block in registers, so every
+// input byte is read from memory once (block maxima, then conversion).
 constexpr int kColBlockRows = 4;
 
 template <bool PACKED>
@@ -55,7 +56,6 @@ quant_cols_kernel(const __nv_bfloat16* __restrict__ src, int rows, int C, const 
                   int nseg, uint8_t* __restrict__ q, uint8_t* __restrict__ sc) {
   extern __shared__ int bstart[];  // nseg + 1 block-row starts, then nseg + 1 word starts
   int* wstart = bstart + nseg + 1;
-  __shared__ int s_r0, s_r1, s_word, s_byte, s_last;
   const int tid = threadIdx.x, lane = tid & 31;
   if (tid < 32) {
     int carry = 0, wcarry = 0;
@@ -87,80 +87,60 @@ quant_cols_kernel(const __nv_bfloat16* __restrict__ src, int rows, int C, const 
     }
   }
   __syncthreads();
-  const int c = (blockIdx.y * 128 + tid) * 8;
+  const int c = (blockIdx.y * 128 + tid) * 4;
+  if (c >= C) return;
   for (int brow = blockIdx.x * kColBlockRows; brow < (blockIdx.x + 1) * kColBlockRows; ++brow) {
-    if (tid == 0) {
-      int r0 = -1, r1 = -1, word = 0, byte = 0, last = 0;
-      if (brow < bstart[nseg]) {
-        int lo = 0, hi = nseg;  // bstart[lo] <= brow < bstart[lo + 1]
-        while (hi - lo > 1) {
-          const int mid = (lo + hi) >> 1;
-          if (bstart[mid] <= brow) lo = mid; else hi = mid;
-        }
-        const int g0 = seg ? seg[lo] : 0, g1 = seg ? seg[lo + 1] : rows;
-        const int local = brow - bstart[lo];
-        r0 = g0 + local * 32;
-        r1 = min(r0 + 32, g1);
-        word = wstart[lo] + local / 4;
-        byte = local % 4;
-        last = (brow == bstart[lo + 1] - 1);
-      }
-      s_r0 = r0;
-      s_r1 = r1;
-      s_word = word;
-      s_byte = byte;
-      s_last = last;
+    if (brow >= bstart[nseg]) break;
+    int lo = 0, hi = nseg;  // bstart[lo] <= brow < bstart[lo + 1]
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (bstart[mid] <= brow) lo = mid; else hi = mid;
     }
-    __syncthreads();
-    const int r0 = s_r0, r1 = s_r1, word = s_word, byte = s_byte, last = s_last;
-    __syncthreads();
-    if (r0 < 0) break;
-    if (c >= C) continue;
-    float amax[8];
+    const int g0 = seg ? seg[lo] : 0, g1 = seg ? seg[lo + 1] : rows;
+    const int local = brow - bstart[lo];
+    const int r0 = g0 + local * 32, nr = min(32, g1 - r0);
+    uint2 blk[32];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) amax[j] = 0.0f;
-#pragma unroll 8
+    for (int i = 0; i < 32; ++i)
+      blk[i] = i < nr ? __ldg(reinterpret_cast<const uint2*>(src + (size_t)(r0 + i) * C + c)) : make_uint2(0, 0);
+    float amax[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) amax[j] = 0.0f;
+#pragma unroll
     for (int i = 0; i < 32; ++i) {
-      if (r0 + i < r1) {
-        float v[8];
-        Vec16<__nv_bfloat16>::load(src + (size_t)(r0 + i) * C + c, v);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) amax[j] = fmaxf(amax[j], fabsf(v[j]));
-      }
+      amax[0] = fmaxf(amax[0], fabsf(__uint_as_float(blk[i].x << 16)));
+      amax[1] = fmaxf(amax[1], fabsf(__uint_as_float(blk[i].x & 0xFFFF0000u)));
+      amax[2] = fmaxf(amax[2], fabsf(__uint_as_float(blk[i].y << 16)));
+      amax[3] = fmaxf(amax[3], fabsf(__uint_as_float(blk[i].y & 0xFFFF0000u)));
     }
-    int sx[8];
-    float m[8];
+    int sx[4];
+    float m[4];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
+    for (int j = 0; j < 4; ++j) {
       sx[j] = e8m0_exponent(amax[j]);
       m[j] = pow2_neg(sx[j]);
     }
-#pragma unroll 8
-    for (int i = 0; i < 32; ++i) {
-      if (r0 + i < r1) {
-        float v[8];
-        Vec16<__nv_bfloat16>::load(src + (size_t)(r0 + i) * C + c, v);
-        uint32_t lo = 0, hi = 0;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          lo |= e4m3(v[j] * m[j]) << (8 * j);
-          hi |= e4m3(v[4 + j] * m[4 + j]) << (8 * j);
-        }
-        *reinterpret_cast<uint2*>(q + (size_t)(r0 + i) * C + c) = make_uint2(lo, hi);
+    for (int i = 0; i < 32; ++i) {
+      if (i < nr) {
+        const uint32_t b = e4m3(__uint_as_float(blk[i].x << 16) * m[0]) |
+                           e4m3(__uint_as_float(blk[i].x & 0xFFFF0000u) * m[1]) << 8 |
+                           e4m3(__uint_as_float(blk[i].y << 16) * m[2]) << 16 |
+                           e4m3(__uint_as_float(blk[i].y & 0xFFFF0000u) * m[3]) << 24;
+        *reinterpret_cast<uint32_t*>(q + (size_t)(r0 + i) * C + c) = b;
       }
     }
     if (!PACKED) {
-      uint32_t lo = 0, hi = 0;
+      uint32_t b = 0;
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        lo |= static_cast<uint32_t>(sx[j] + 127) << (8 * j);
-        hi |= static_cast<uint32_t>(sx[4 + j] + 127) << (8 * j);
-      }
-      *reinterpret_cast<uint2*>(sc + (size_t)brow * C + c) = make_uint2(lo, hi);
+      for (int j = 0; j < 4; ++j) b |= static_cast<uint32_t>(sx[j] + 127) << (8 * j);
+      *reinterpret_cast<uint32_t*>(sc + (size_t)brow * C + c) = b;
     } else {
+      const int word = wstart[lo] + local / 4, byte = local % 4;
+      const bool last = brow == bstart[lo + 1] - 1;
       uint8_t* w = sc + ((size_t)word * C + c) * 4;
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
+      for (int j = 0; j < 4; ++j) {
         w[4 * j + byte] = static_cast<uint8_t>(sx[j] + 127);
         if (last)
           for (int b = byte + 1; b < 4; ++b) w[4 * j + b] = 127;
@@ -186,7 +166,7 @@ cudaError_t launch_mxfp8_quant_cols(const void* src, int rows, int C, const int3
   const long max_brows = (rows + 31) / 32 + nseg_eff;
   if (rows == 0) return cudaSuccess;
   dim3 grid(static_cast<unsigned>((max_brows + kColBlockRows - 1) / kColBlockRows),
-            static_cast<unsigned>((C + 1023) / 1024));
+            static_cast<unsigned>((C + 511) / 512));
   const size_t smem = 2 * (nseg_eff + 1) * sizeof(int);
   if (packed)
     MOE_COUNTED quant_cols_kernel<true><<<grid, 128, smem, st>>>(static_cast<const __nv_bfloat16*>(src), rows, C,

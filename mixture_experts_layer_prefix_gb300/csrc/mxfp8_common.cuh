@@ -30,23 +30,29 @@ __device__ __forceinline__ uint32_t mx_e4m3(float v) {
   return static_cast<uint32_t>(__nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3));
 }
 
-// Quantise one block of 32 values: 32 E4M3 codes (16-byte aligned
-// destination) and one E8M0 byte.
-__device__ __forceinline__ void mx_quant_block32(const float* v, uint8_t* codes, uint8_t* scale) {
+// Quantise one block of 32 values into 32 E4M3 codes (w, little-endian
+// bytes in element order); returns the E8M0 byte.
+__device__ __forceinline__ uint8_t mx_quant_block32_regs(const float* v, uint32_t (&w)[8]) {
   float amax = 0.0f;
 #pragma unroll
   for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
   const int s = mx_e8m0_exponent(amax);
   const float m = mx_pow2_neg(s);
-  uint32_t w[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i)
     w[i] = mx_e4m3(v[4 * i] * m) | (mx_e4m3(v[4 * i + 1] * m) << 8) | (mx_e4m3(v[4 * i + 2] * m) << 16) |
            (mx_e4m3(v[4 * i + 3] * m) << 24);
+  return static_cast<uint8_t>(s + 127);
+}
+
+// Quantise one block of 32 values: 32 E4M3 codes (16-byte aligned
+// destination) and one E8M0 byte.
+__device__ __forceinline__ void mx_quant_block32(const float* v, uint8_t* codes, uint8_t* scale) {
+  uint32_t w[8];
+  *scale = mx_quant_block32_regs(v, w);
   uint4* out = reinterpret_cast<uint4*>(codes);
   out[0] = make_uint4(w[0], w[1], w[2], w[3]);
   out[1] = make_uint4(w[4], w[5], w[6], w[7]);
-  *scale = static_cast<uint8_t>(s + 127);
 }
 
 }  // namespace moe

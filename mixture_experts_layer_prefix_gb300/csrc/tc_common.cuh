@@ -190,10 +190,10 @@ __device__ __forceinline__ void pack_bf16x32(const float* v, uint32_t (&w)[16]) 
   }
 }
 
-// Lane r holds w = row r's 32 bf16 values; dst is row 0 of the warp's 32 rows
-// (leading dimension ld elements). Rows >= nrows are not written.
-__device__ __forceinline__ void warp_store_rows(uint8_t* stg, const uint32_t (&w)[16], __nv_bfloat16* dst,
-                                                size_t ld, int nrows, int lane) {
+// Lane r holds w = row r's 64 bytes; dst is row 0 of the warp's 32 rows
+// (leading dimension ld bytes). Rows >= nrows are not written.
+__device__ __forceinline__ void warp_store_rows_b(uint8_t* stg, const uint32_t (&w)[16], uint8_t* dst,
+                                                  size_t ld, int nrows, int lane) {
 #pragma unroll
   for (int g = 0; g < 4; ++g)
     *reinterpret_cast<uint4*>(stg + stg_off(lane, g)) = make_uint4(w[4 * g], w[4 * g + 1], w[4 * g + 2], w[4 * g + 3]);
@@ -203,9 +203,53 @@ __device__ __forceinline__ void warp_store_rows(uint8_t* stg, const uint32_t (&w
   for (int i = 0; i < 4; ++i) {
     const int r = 8 * i + (lane >> 2);
     const uint4 v = *reinterpret_cast<const uint4*>(stg + stg_off(r, g));
-    if (r < nrows) *reinterpret_cast<uint4*>(dst + (size_t)r * ld + 8 * g) = v;
+    if (r < nrows) *reinterpret_cast<uint4*>(dst + (size_t)r * ld + 16 * g) = v;
   }
   __syncwarp();
+}
+// The same for 32 bf16 values per row (ld in elements).
+__device__ __forceinline__ void warp_store_rows(uint8_t* stg, const uint32_t (&w)[16], __nv_bfloat16* dst,
+                                                size_t ld, int nrows, int lane) {
+  warp_store_rows_b(stg, w, reinterpret_cast<uint8_t*>(dst), 2 * ld, nrows, lane);
+}
+// 32-byte rows (32 E4M3 codes per row): 2 granules per row, XOR-swizzled by
+// row quad; each global instruction moves 16 rows x 32 bytes.
+__device__ __forceinline__ int stg32_off(int r, int g) { return r * 32 + ((g ^ ((r >> 2) & 1)) << 4); }
+__device__ __forceinline__ void warp_store_rows32(uint8_t* stg, const uint32_t (&w)[8], uint8_t* dst, size_t ld,
+                                                  int nrows, int lane) {
+#pragma unroll
+  for (int g = 0; g < 2; ++g)
+    *reinterpret_cast<uint4*>(stg + stg32_off(lane, g)) = make_uint4(w[4 * g], w[4 * g + 1], w[4 * g + 2], w[4 * g + 3]);
+  __syncwarp();
+  const int g = lane & 1;
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const int r = 16 * i + (lane >> 1);
+    const uint4 v = *reinterpret_cast<const uint4*>(stg + stg32_off(r, g));
+    if (r < nrows) *reinterpret_cast<uint4*>(dst + (size_t)r * ld + 16 * g) = v;
+  }
+  __syncwarp();
+}
+// MXFP8 row quantisation of a 32-column chunk held as packed bf16 pairs (the
+// stored values): codes to qout[row][col..col+32) through the staging buffer,
+// the scale byte of each valid row to qsc[row][col / 32] ([rows][ld] matrix).
+__device__ __forceinline__ void quant_rows_staged(const Params& p, uint8_t* stg, const uint32_t (&w)[16], int wrow,
+                                                  int nrows, int ld, int col, int lane) {
+  float amax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i)
+    amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(w[i] << 16)), fabsf(__uint_as_float(w[i] & 0xFFFF0000u))));
+  const int sx = mx_e8m0_exponent(amax);
+  const float m = mx_pow2_neg(sx);
+  uint32_t cw[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    cw[i] = mx_e4m3(__uint_as_float(w[2 * i] << 16) * m) | (mx_e4m3(__uint_as_float(w[2 * i] & 0xFFFF0000u) * m) << 8) |
+            (mx_e4m3(__uint_as_float(w[2 * i + 1] << 16) * m) << 16) |
+            (mx_e4m3(__uint_as_float(w[2 * i + 1] & 0xFFFF0000u) * m) << 24);
+  const uint8_t sb = static_cast<uint8_t>(sx + 127);
+  if (lane < nrows) p.qsc[(size_t)(wrow + lane) * (ld / 32) + col / 32] = sb;
+  warp_store_rows32(stg, cw, p.qout + (size_t)wrow * ld + col, ld, nrows, lane);
 }
 
 // The reverse, in two halves so that the global latency can overlap other
@@ -262,7 +306,7 @@ __device__ __forceinline__ void quant_chunk_bf16(const Params& p, long row, int 
 // Staged form of the row-tile epilogue (see warp_store_rows): every lane of
 // the warp takes part; stg is the warp's STG_BYTES buffer. Row-tile kinds
 // FPROP1, FPROP2, DGRAD1, DGRAD2 without quantisation.
-template <int KIND, int TBN = BN>
+template <int KIND, int TBN = BN, bool QUANT = false>
 __device__ __forceinline__ void epilogue_tile_staged(const Params& p, const Tile& tl, uint32_t tbase, int q, int lane,
                                                      int c_beg, int c_end, uint8_t* stg) {
   static_assert(KIND == FPROP1 || KIND == FPROP2 || KIND == DGRAD1 || KIND == DGRAD2, "row-tile kinds");
@@ -293,6 +337,7 @@ __device__ __forceinline__ void epilogue_tile_staged(const Params& p, const Tile
       for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(__uint_as_float(ru[2 * i]), __uint_as_float(ru[2 * i + 1]));
       warp_store_rows(stg, w, h + p.f + n, 2 * (size_t)p.f, nrows, lane);
       warp_store_rows(stg, wa, a + n, p.f, nrows, lane);
+      if (QUANT && p.qout) quant_rows_staged(p, stg, wa, wrow, nrows, p.f, n, lane);
     }
   } else if (KIND == DGRAD2) {
     // dh_g = da * h_u * silu'(h_g), dh_u = da * silu(h_g); the reads of h are
@@ -332,6 +377,10 @@ __device__ __forceinline__ void epilogue_tile_staged(const Params& p, const Tile
       }
       warp_store_rows(stg, w, dh + n, 2 * (size_t)p.f, nrows, lane);
       warp_store_rows(stg, wu, dh + p.f + n, 2 * (size_t)p.f, nrows, lane);
+      if (QUANT && p.qout) {
+        quant_rows_staged(p, stg, w, wrow, nrows, 2 * p.f, n, lane);
+        quant_rows_staged(p, stg, wu, wrow, nrows, 2 * p.f, p.f + n, lane);
+      }
     }
   } else {  // FPROP2, DGRAD1: plain bf16 store
     const int n0 = tl.n_idx * TBN;

@@ -45,13 +45,15 @@ quant_rows_kernel(const __nv_bfloat16* __restrict__ src, long nblocks, uint8_t* 
 // PACKED: scales go to a [words][C] table of 32-bit words, word w of segment
 // g holding its blocks 4w..4w+3 in bytes 0..3 (words of segment g start at
 // sum_{h<g} ceil(blocks_h / 4)); bytes past a segment's last block are 127.
-// A CTA handles kColBlockRows block rows of 512 columns; each thread owns 4
-// consecutive columns and holds its 32 x 4 block in registers, so every
-// input byte is read from memory once (block maxima, then conversion).
+// A CTA handles kColBlockRows block rows of 256 columns; each thread owns 2
+// consecutive columns (a warp reads 128 contiguous bytes of a row) and holds
+// its 32 x 2 block in registers, so every input byte is read from memory
+// once (block maxima, then conversion) at an occupancy that keeps enough
+// loads in flight.
 constexpr int kColBlockRows = 4;
 
 template <bool PACKED>
-__global__ void __launch_bounds__(128)
+__global__ void __launch_bounds__(128, 6)
 quant_cols_kernel(const __nv_bfloat16* __restrict__ src, int rows, int C, const int32_t* __restrict__ seg,
                   int nseg, uint8_t* __restrict__ q, uint8_t* __restrict__ sc) {
   extern __shared__ int bstart[];  // nseg + 1 block-row starts, then nseg + 1 word starts
@@ -87,9 +89,11 @@ quant_cols_kernel(const __nv_bfloat16* __restrict__ src, int rows, int C, const 
     }
   }
   __syncthreads();
-  const int c = (blockIdx.y * 128 + tid) * 4;
+  const int c = (blockIdx.x * 128 + tid) * 2;  // x: column slices, so CTAs in flight share rows
   if (c >= C) return;
-  for (int brow = blockIdx.x * kColBlockRows; brow < (blockIdx.x + 1) * kColBlockRows; ++brow) {
+  const int ngroups = (bstart[nseg] + kColBlockRows - 1) / kColBlockRows;
+  for (int grp = blockIdx.y; grp < ngroups; grp += gridDim.y)
+  for (int brow = grp * kColBlockRows; brow < (grp + 1) * kColBlockRows; ++brow) {
     if (brow >= bstart[nseg]) break;
     int lo = 0, hi = nseg;  // bstart[lo] <= brow < bstart[lo + 1]
     while (hi - lo > 1) {
@@ -99,48 +103,39 @@ quant_cols_kernel(const __nv_bfloat16* __restrict__ src, int rows, int C, const 
     const int g0 = seg ? seg[lo] : 0, g1 = seg ? seg[lo + 1] : rows;
     const int local = brow - bstart[lo];
     const int r0 = g0 + local * 32, nr = min(32, g1 - r0);
-    uint2 blk[32];
+    uint32_t blk[32];
+    const uint32_t* sp = reinterpret_cast<const uint32_t*>(src + (size_t)r0 * C + c);
+    const int cw = C / 2;  // row stride in 32-bit words
 #pragma unroll
-    for (int i = 0; i < 32; ++i)
-      blk[i] = i < nr ? __ldg(reinterpret_cast<const uint2*>(src + (size_t)(r0 + i) * C + c)) : make_uint2(0, 0);
-    float amax[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) amax[j] = 0.0f;
+    for (int i = 0; i < 32; ++i) blk[i] = i < nr ? __ldg(sp + i * cw) : 0u;
+    float amax0 = 0.0f, amax1 = 0.0f;
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
-      amax[0] = fmaxf(amax[0], fabsf(__uint_as_float(blk[i].x << 16)));
-      amax[1] = fmaxf(amax[1], fabsf(__uint_as_float(blk[i].x & 0xFFFF0000u)));
-      amax[2] = fmaxf(amax[2], fabsf(__uint_as_float(blk[i].y << 16)));
-      amax[3] = fmaxf(amax[3], fabsf(__uint_as_float(blk[i].y & 0xFFFF0000u)));
+      amax0 = fmaxf(amax0, fabsf(__uint_as_float(blk[i] << 16)));
+      amax1 = fmaxf(amax1, fabsf(__uint_as_float(blk[i] & 0xFFFF0000u)));
     }
-    int sx[4];
-    float m[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      sx[j] = e8m0_exponent(amax[j]);
-      m[j] = pow2_neg(sx[j]);
-    }
+    int sx[2];
+    sx[0] = e8m0_exponent(amax0);
+    sx[1] = e8m0_exponent(amax1);
+    const float m0 = pow2_neg(sx[0]), m1 = pow2_neg(sx[1]);
+    uint16_t* qp = reinterpret_cast<uint16_t*>(q + (size_t)r0 * C + c);
+    const int ch = C / 2;  // row stride in 16-bit units
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
       if (i < nr) {
-        const uint32_t b = e4m3(__uint_as_float(blk[i].x << 16) * m[0]) |
-                           e4m3(__uint_as_float(blk[i].x & 0xFFFF0000u) * m[1]) << 8 |
-                           e4m3(__uint_as_float(blk[i].y << 16) * m[2]) << 16 |
-                           e4m3(__uint_as_float(blk[i].y & 0xFFFF0000u) * m[3]) << 24;
-        *reinterpret_cast<uint32_t*>(q + (size_t)(r0 + i) * C + c) = b;
+        const uint32_t b = e4m3(__uint_as_float(blk[i] << 16) * m0) | e4m3(__uint_as_float(blk[i] & 0xFFFF0000u) * m1) << 8;
+        qp[i * ch] = static_cast<uint16_t>(b);
       }
     }
     if (!PACKED) {
-      uint32_t b = 0;
-#pragma unroll
-      for (int j = 0; j < 4; ++j) b |= static_cast<uint32_t>(sx[j] + 127) << (8 * j);
-      *reinterpret_cast<uint32_t*>(sc + (size_t)brow * C + c) = b;
+      const uint32_t b = static_cast<uint32_t>(sx[0] + 127) | static_cast<uint32_t>(sx[1] + 127) << 8;
+      *reinterpret_cast<uint16_t*>(sc + (size_t)brow * C + c) = static_cast<uint16_t>(b);
     } else {
       const int word = wstart[lo] + local / 4, byte = local % 4;
       const bool last = brow == bstart[lo + 1] - 1;
       uint8_t* w = sc + ((size_t)word * C + c) * 4;
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
+      for (int j = 0; j < 2; ++j) {
         w[4 * j + byte] = static_cast<uint8_t>(sx[j] + 127);
         if (last)
           for (int b = byte + 1; b < 4; ++b) w[4 * j + b] = 127;
@@ -165,8 +160,8 @@ cudaError_t launch_mxfp8_quant_cols(const void* src, int rows, int C, const int3
   const int nseg_eff = seg ? nseg : 1;
   const long max_brows = (rows + 31) / 32 + nseg_eff;
   if (rows == 0) return cudaSuccess;
-  dim3 grid(static_cast<unsigned>((max_brows + kColBlockRows - 1) / kColBlockRows),
-            static_cast<unsigned>((C + 511) / 512));
+  const long groups = (max_brows + kColBlockRows - 1) / kColBlockRows;
+  dim3 grid(static_cast<unsigned>((C + 255) / 256), static_cast<unsigned>(groups < 65535 ? groups : 65535));
   const size_t smem = 2 * (nseg_eff + 1) * sizeof(int);
   if (packed)
     MOE_COUNTED quant_cols_kernel<true><<<grid, 128, smem, st>>>(static_cast<const __nv_bfloat16*>(src), rows, C,

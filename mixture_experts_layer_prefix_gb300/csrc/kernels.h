@@ -7,6 +7,10 @@
 
 namespace moe {
 
+namespace tc {
+int sm_count();  // SMs of the current device (cached on first use)
+}
+
 // ------------------------------------------------------------- routing
 constexpr int kTokensPerChunk = 8;  // tokens per routing chunk (one warp)
 int route_num_chunks(int T);

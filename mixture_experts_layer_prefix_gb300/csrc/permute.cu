@@ -20,15 +20,15 @@ permute_kernel(const T* __restrict__ x, int Tn, int d, int k, const int32_t* __r
                T* __restrict__ x_perm) {
   using V = Vec16<T>;
   const int lane = threadIdx.x & 31;
-  for (int t = blockIdx.x * kRowWarps + (threadIdx.x >> 5); t < Tn; t += gridDim.x * kRowWarps) {
-    int dest = lane < k ? dest_row[(size_t)t * k + lane] : 0;
-    const T* src = x + (size_t)t * d;
-    for (int c = lane * V::N; c < d; c += 32 * V::N) {
-      const uint4 q = *reinterpret_cast<const uint4*>(src + c);
-      for (int j = 0; j < k; ++j) {
-        const int r = __shfl_sync(0xffffffffu, dest, j);
-        *reinterpret_cast<uint4*>(x_perm + (size_t)r * d + c) = q;
-      }
+  const int t = blockIdx.x * kRowWarps + (threadIdx.x >> 5);
+  if (t >= Tn) return;
+  int dest = lane < k ? dest_row[(size_t)t * k + lane] : 0;
+  const T* src = x + (size_t)t * d;
+  for (int c = lane * V::N; c < d; c += 32 * V::N) {
+    const uint4 q = *reinterpret_cast<const uint4*>(src + c);
+    for (int j = 0; j < k; ++j) {
+      const int r = __shfl_sync(0xffffffffu, dest, j);
+      *reinterpret_cast<uint4*>(x_perm + (size_t)r * d + c) = q;
     }
   }
 }
@@ -40,77 +40,77 @@ combine_fwd_kernel(const T* __restrict__ y_perm, const float* __restrict__ gates
                    const int32_t* __restrict__ dest_row, int Tn, int d, int k, T* __restrict__ y) {
   using V = Vec16<T>;
   const int lane = threadIdx.x & 31;
-  for (int t = blockIdx.x * kRowWarps + (threadIdx.x >> 5); t < Tn; t += gridDim.x * kRowWarps) {
-    const int my_dest = lane < k ? dest_row[(size_t)t * k + lane] : 0;
-    const float my_g = lane < k ? gates[(size_t)t * k + lane] : 0.0f;
-    int dest[8];
-    float g[8];
+  const int t = blockIdx.x * kRowWarps + (threadIdx.x >> 5);
+  if (t >= Tn) return;
+  const int my_dest = lane < k ? dest_row[(size_t)t * k + lane] : 0;
+  const float my_g = lane < k ? gates[(size_t)t * k + lane] : 0.0f;
+  int dest[8];
+  float g[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    dest[j] = __shfl_sync(0xffffffffu, my_dest, j);
+    g[j] = __shfl_sync(0xffffffffu, my_g, j);
+  }
+  for (int c = lane * V::N; c < d; c += 32 * V::N) {
+    float acc[V::N];
+#pragma unroll
+    for (int i = 0; i < V::N; ++i) acc[i] = 0.0f;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-      dest[j] = __shfl_sync(0xffffffffu, my_dest, j);
-      g[j] = __shfl_sync(0xffffffffu, my_g, j);
-    }
-    for (int c = lane * V::N; c < d; c += 32 * V::N) {
-      float acc[V::N];
+      if (j < k) {
+        float v[V::N];
+        V::load(y_perm + (size_t)dest[j] * d + c, v);
 #pragma unroll
-      for (int i = 0; i < V::N; ++i) acc[i] = 0.0f;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        if (j < k) {
-          float v[V::N];
-          V::load(y_perm + (size_t)dest[j] * d + c, v);
-#pragma unroll
-          for (int i = 0; i < V::N; ++i) acc[i] = fmaf(g[j], v[i], acc[i]);
-        }
+        for (int i = 0; i < V::N; ++i) acc[i] = fmaf(g[j], v[i], acc[i]);
       }
-      V::store(y + (size_t)t * d + c, acc);
     }
+    V::store(y + (size_t)t * d + c, acc);
   }
 }
 
 // dy_perm[dest] = g * dy[t];  dgates[t][j] = <dy[t], y_perm[dest]>
 // KMAX: the largest k the instance handles (arrays of per-slot state).
 template <typename T, int KMAX>
-__global__ void __launch_bounds__(kRowWarps * 32, 5)  // five CTAs per SM (measured best)
+__global__ void __launch_bounds__(kRowWarps * 32)
 combine_bwd_kernel(const T* __restrict__ dy, const T* __restrict__ y_perm,
                    const float* __restrict__ gates, const int32_t* __restrict__ dest_row, int Tn,
                    int d, int k, T* __restrict__ dy_perm, float* __restrict__ dgates) {
   using V = Vec16<T>;
   const int lane = threadIdx.x & 31;
-  for (int t = blockIdx.x * kRowWarps + (threadIdx.x >> 5); t < Tn; t += gridDim.x * kRowWarps) {
-    const int my_dest = lane < k ? dest_row[(size_t)t * k + lane] : 0;
-    const float my_g = lane < k ? gates[(size_t)t * k + lane] : 0.0f;
-    int dest[KMAX];
-    float g[KMAX], dot[KMAX];
+  const int t = blockIdx.x * kRowWarps + (threadIdx.x >> 5);
+  if (t >= Tn) return;
+  const int my_dest = lane < k ? dest_row[(size_t)t * k + lane] : 0;
+  const float my_g = lane < k ? gates[(size_t)t * k + lane] : 0.0f;
+  int dest[KMAX];
+  float g[KMAX], dot[KMAX];
 #pragma unroll
-    for (int j = 0; j < KMAX; ++j) {
-      dest[j] = __shfl_sync(0xffffffffu, my_dest, j);
-      g[j] = __shfl_sync(0xffffffffu, my_g, j);
-      dot[j] = 0.0f;
-    }
-    for (int c = lane * V::N; c < d; c += 32 * V::N) {
-      float u[V::N];
-      V::load(dy + (size_t)t * d + c, u);
-#pragma unroll
-      for (int j = 0; j < KMAX; ++j) {
-        if (j < k) {
-          float v[V::N], w[V::N];
-          V::load(y_perm + (size_t)dest[j] * d + c, v);
-#pragma unroll
-          for (int i = 0; i < V::N; ++i) {
-            dot[j] = fmaf(u[i], v[i], dot[j]);
-            w[i] = g[j] * u[i];
-          }
-          V::store(dy_perm + (size_t)dest[j] * d + c, w);
-        }
-      }
-    }
+  for (int j = 0; j < KMAX; ++j) {
+    dest[j] = __shfl_sync(0xffffffffu, my_dest, j);
+    g[j] = __shfl_sync(0xffffffffu, my_g, j);
+    dot[j] = 0.0f;
+  }
+  for (int c = lane * V::N; c < d; c += 32 * V::N) {
+    float u[V::N];
+    V::load(dy + (size_t)t * d + c, u);
 #pragma unroll
     for (int j = 0; j < KMAX; ++j) {
       if (j < k) {
-        const float s = warp_sum(dot[j]);
-        if (lane == 0) dgates[(size_t)t * k + j] = s;
+        float v[V::N], w[V::N];
+        V::load(y_perm + (size_t)dest[j] * d + c, v);
+#pragma unroll
+        for (int i = 0; i < V::N; ++i) {
+          dot[j] = fmaf(u[i], v[i], dot[j]);
+          w[i] = g[j] * u[i];
+        }
+        V::store(dy_perm + (size_t)dest[j] * d + c, w);
       }
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < KMAX; ++j) {
+    if (j < k) {
+      const float s = warp_sum(dot[j]);
+      if (lane == 0) dgates[(size_t)t * k + j] = s;
     }
   }
 }
@@ -124,49 +124,49 @@ permute_bwd_kernel(const T* __restrict__ dx_perm, int Tn, int d, int E, int k,
                    T* __restrict__ dx) {
   using V = Vec16<T>;
   const int lane = threadIdx.x & 31;
-  for (int t = blockIdx.x * kRowWarps + (threadIdx.x >> 5); t < Tn; t += gridDim.x * kRowWarps) {
-    const bool router = dlogits != nullptr;
-    const int my_dest = lane < k ? dest_row[(size_t)t * k + lane] : 0;
-    int my_e = 0;
-    float my_dl = 0.0f;
-    if (router && lane < k) {
-      my_e = topk_idx[(size_t)t * k + lane];
-      my_dl = dlogits[(size_t)t * E + my_e];
-    }
-    int dest[8], ex[8];
-    float dl[8];
+  const int t = blockIdx.x * kRowWarps + (threadIdx.x >> 5);
+  if (t >= Tn) return;
+  const bool router = dlogits != nullptr;
+  const int my_dest = lane < k ? dest_row[(size_t)t * k + lane] : 0;
+  int my_e = 0;
+  float my_dl = 0.0f;
+  if (router && lane < k) {
+    my_e = topk_idx[(size_t)t * k + lane];
+    my_dl = dlogits[(size_t)t * E + my_e];
+  }
+  int dest[8], ex[8];
+  float dl[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    dest[j] = __shfl_sync(0xffffffffu, my_dest, j);
+    ex[j] = __shfl_sync(0xffffffffu, my_e, j);
+    dl[j] = __shfl_sync(0xffffffffu, my_dl, j);
+  }
+  for (int c = lane * V::N; c < d; c += 32 * V::N) {
+    float acc[V::N];
+#pragma unroll
+    for (int i = 0; i < V::N; ++i) acc[i] = 0.0f;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-      dest[j] = __shfl_sync(0xffffffffu, my_dest, j);
-      ex[j] = __shfl_sync(0xffffffffu, my_e, j);
-      dl[j] = __shfl_sync(0xffffffffu, my_dl, j);
-    }
-    for (int c = lane * V::N; c < d; c += 32 * V::N) {
-      float acc[V::N];
+      if (j < k) {
+        float v[V::N];
+        V::load(dx_perm + (size_t)dest[j] * d + c, v);
 #pragma unroll
-      for (int i = 0; i < V::N; ++i) acc[i] = 0.0f;
+        for (int i = 0; i < V::N; ++i) acc[i] += v[i];
+      }
+    }
+    if (router) {
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
         if (j < k) {
-          float v[V::N];
-          V::load(dx_perm + (size_t)dest[j] * d + c, v);
+          float w[V::N];
+          V::load(w_r + (size_t)ex[j] * d + c, w);
 #pragma unroll
-          for (int i = 0; i < V::N; ++i) acc[i] += v[i];
+          for (int i = 0; i < V::N; ++i) acc[i] = fmaf(dl[j], w[i], acc[i]);
         }
       }
-      if (router) {
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          if (j < k) {
-            float w[V::N];
-            V::load(w_r + (size_t)ex[j] * d + c, w);
-#pragma unroll
-            for (int i = 0; i < V::N; ++i) acc[i] = fmaf(dl[j], w[i], acc[i]);
-          }
-        }
-      }
-      V::store(dx + (size_t)t * d + c, acc);
     }
+    V::store(dx + (size_t)t * d + c, acc);
   }
 }
 
@@ -176,30 +176,30 @@ router_dlogits_kernel(const float* __restrict__ dgates, const float* __restrict_
                       const int32_t* __restrict__ topk_idx, int Tn, int E, int k,
                       float* __restrict__ dlogits) {
   const int lane = threadIdx.x & 31;
-  for (int t = blockIdx.x * kRowWarps + (threadIdx.x >> 5); t < Tn; t += gridDim.x * kRowWarps) {
-    float g = 0.0f, dg = 0.0f;
-    int e = -1;
-    if (lane < k) {
-      g = gates[(size_t)t * k + lane];
-      dg = dgates[(size_t)t * k + lane];
-      e = topk_idx[(size_t)t * k + lane];
-    }
-    const float s = warp_sum(g * dg);
-    const float dl = g * (dg - s);
-    int ej[8];
-    float dlj[8];
+  const int t = blockIdx.x * kRowWarps + (threadIdx.x >> 5);
+  if (t >= Tn) return;
+  float g = 0.0f, dg = 0.0f;
+  int e = -1;
+  if (lane < k) {
+    g = gates[(size_t)t * k + lane];
+    dg = dgates[(size_t)t * k + lane];
+    e = topk_idx[(size_t)t * k + lane];
+  }
+  const float s = warp_sum(g * dg);
+  const float dl = g * (dg - s);
+  int ej[8];
+  float dlj[8];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      ej[j] = __shfl_sync(0xffffffffu, e, j);
-      dlj[j] = __shfl_sync(0xffffffffu, dl, j);
-    }
-    for (int c = lane; c < E; c += 32) {
-      float v = 0.0f;
+  for (int j = 0; j < 8; ++j) {
+    ej[j] = __shfl_sync(0xffffffffu, e, j);
+    dlj[j] = __shfl_sync(0xffffffffu, dl, j);
+  }
+  for (int c = lane; c < E; c += 32) {
+    float v = 0.0f;
 #pragma unroll
-      for (int j = 0; j < 8; ++j)
-        if (j < k && ej[j] == c) v = dlj[j];
-      dlogits[(size_t)t * E + c] = v;
-    }
+    for (int j = 0; j < 8; ++j)
+      if (j < k && ej[j] == c) v = dlj[j];
+    dlogits[(size_t)t * E + c] = v;
   }
 }
 
@@ -262,19 +262,7 @@ router_dw_kernel(const float* __restrict__ dlogits, const int32_t* __restrict__ 
   }
 }
 
-// Grid of a one-warp-per-token kernel: enough CTAs for every token, capped at
-// the CTAs that fit on the GPU at once (the kernels loop over tokens with a
-// grid stride), so no partial last wave leaves SMs idle.
-template <auto KERNEL> int row_grid(int Tn) {
-  static int resident = 0;
-  if (!resident) {
-    int per_sm = 0;
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, KERNEL, kRowWarps * 32, 0);
-    resident = (per_sm > 0 ? per_sm : 1) * tc::sm_count();
-  }
-  const int need = (Tn + kRowWarps - 1) / kRowWarps;
-  return need < resident ? need : resident;
-}
+template <typename T> inline int row_grid(int Tn) { return (Tn + kRowWarps - 1) / kRowWarps; }
 
 }  // namespace
 
@@ -282,7 +270,7 @@ template <typename T>
 cudaError_t launch_permute(const void* x, int Tn, int d, int k, const int32_t* dest_row, void* x_perm,
                            cudaStream_t st) {
   if (Tn == 0) return cudaSuccess;
-  MOE_COUNTED permute_kernel<T><<<row_grid<permute_kernel<T>>(Tn), kRowWarps * 32, 0, st>>>(
+  MOE_COUNTED permute_kernel<T><<<row_grid<T>(Tn), kRowWarps * 32, 0, st>>>(
       static_cast<const T*>(x), Tn, d, k, dest_row, static_cast<T*>(x_perm));
   return cudaGetLastError();
 }
@@ -291,7 +279,7 @@ template <typename T>
 cudaError_t launch_combine_fwd(const void* y_perm, const float* gates, const int32_t* dest_row, int Tn,
                                int d, int k, void* y, cudaStream_t st) {
   if (Tn == 0) return cudaSuccess;
-  MOE_COUNTED combine_fwd_kernel<T><<<row_grid<combine_fwd_kernel<T>>(Tn), kRowWarps * 32, 0, st>>>(
+  MOE_COUNTED combine_fwd_kernel<T><<<row_grid<T>(Tn), kRowWarps * 32, 0, st>>>(
       static_cast<const T*>(y_perm), gates, dest_row, Tn, d, k, static_cast<T*>(y));
   return cudaGetLastError();
 }
@@ -302,11 +290,11 @@ cudaError_t launch_combine_bwd(const void* dy, const void* y_perm, const float* 
                                float* dgates, cudaStream_t st) {
   if (Tn == 0) return cudaSuccess;
   if (k <= 4)
-    MOE_COUNTED combine_bwd_kernel<T, 4><<<row_grid<combine_bwd_kernel<T, 4>>(Tn), kRowWarps * 32, 0, st>>>(
+    MOE_COUNTED combine_bwd_kernel<T, 4><<<row_grid<T>(Tn), kRowWarps * 32, 0, st>>>(
         static_cast<const T*>(dy), static_cast<const T*>(y_perm), gates, dest_row, Tn, d, k,
         static_cast<T*>(dy_perm), dgates);
   else
-    MOE_COUNTED combine_bwd_kernel<T, 8><<<row_grid<combine_bwd_kernel<T, 8>>(Tn), kRowWarps * 32, 0, st>>>(
+    MOE_COUNTED combine_bwd_kernel<T, 8><<<row_grid<T>(Tn), kRowWarps * 32, 0, st>>>(
         static_cast<const T*>(dy), static_cast<const T*>(y_perm), gates, dest_row, Tn, d, k,
         static_cast<T*>(dy_perm), dgates);
   return cudaGetLastError();
@@ -317,7 +305,7 @@ cudaError_t launch_permute_bwd(const void* dx_perm, int Tn, int d, int E, int k,
                                const int32_t* dest_row, const int32_t* topk_idx, const float* dlogits,
                                const void* w_r, void* dx, cudaStream_t st) {
   if (Tn == 0) return cudaSuccess;
-  MOE_COUNTED permute_bwd_kernel<T><<<row_grid<permute_bwd_kernel<T>>(Tn), kRowWarps * 32, 0, st>>>(
+  MOE_COUNTED permute_bwd_kernel<T><<<row_grid<T>(Tn), kRowWarps * 32, 0, st>>>(
       static_cast<const T*>(dx_perm), Tn, d, E, k, dest_row, topk_idx, dlogits,
       static_cast<const T*>(w_r), static_cast<T*>(dx));
   return cudaGetLastError();
@@ -329,7 +317,7 @@ cudaError_t launch_route_bwd(const float* dgates, const float* gates, const int3
                              int Tn, int d, int E, int k, float* dlogits, float* dw_r,
                              cudaStream_t st) {
   if (Tn > 0)
-    MOE_COUNTED router_dlogits_kernel<<<row_grid<router_dlogits_kernel>(Tn), kRowWarps * 32, 0, st>>>(dgates, gates, topk_idx, Tn,
+    MOE_COUNTED router_dlogits_kernel<<<row_grid<T>(Tn), kRowWarps * 32, 0, st>>>(dgates, gates, topk_idx, Tn,
                                                                        E, k, dlogits);
   dim3 grid(E, (d + 255) / 256);
   MOE_COUNTED router_dw_kernel<T><<<grid, 256, 0, st>>>(dlogits, offsets, src_row, static_cast<const T*>(x),

@@ -12,6 +12,7 @@ independent replica of the layer (weak scaling; the path has no collective).
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import os
 import statistics
@@ -38,6 +39,24 @@ def peaks():
             p = json.load(fh)
         return p, "measured"
     return FALLBACK_PEAKS, "fallback"
+
+
+def gemm_traffic(config_name):
+    """DRAM bytes per step of the six expert GEMMs, from the committed ncu
+    summary, or None when there is none for this workload or the GEMM sources
+    have changed since the counters were taken."""
+    path = os.path.join(ROOT, "profiles", "gemm_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as fh:
+        rec = json.load(fh).get(config_name)
+    if not rec:
+        return None
+    h = hashlib.sha1()
+    for f in rec["source_files"]:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return rec["dram_bytes_per_step"] if h.hexdigest() == rec["source_sha1"] else None
 
 
 def workload_desc(s):
@@ -174,25 +193,36 @@ def run_ours(args, s, rank, world):
     p = L.params_from_inputs(inp, dt)
     b = L.Buffers(s.T, s.d, s.E, s.k, s.f, dt)
     stream = torch.cuda.current_stream()
+    fused = L.fused_default(dt)
 
     def step_timed(ev):
         # forward and backward through the C ABI; events bracket the GEMM stages
         T, d, E, k, f = s.T, s.d, s.E, s.k, s.f
         N.moe_route(p.x, p.w_router, p.bias, dt, T, d, E, k, b.logits, 0, b.topk_idx, b.gates, b.counts,
                     b.offsets, b.dest_row, b.src_row, b.workspace)
-        N.moe_permute(p.x, dt, T, d, k, b.dest_row, b.x_perm)
-        ev[0].record(stream)
-        N.moe_grouped_mlp_fwd(b.x_perm, p.w_gate, p.w_up, p.w_down, dt, b.offsets, b.R, E, d, f, b.h_save,
-                              b.a_save, b.y_perm, b.workspace)
+        if fused:  # the dispatch runs inside GEMM1 (rows gathered from x)
+            ev[0].record(stream)
+            N.moe_dispatch_mlp_fwd(p.x, b.src_row, T, k, p.w_gate, p.w_up, p.w_down, dt, b.offsets, E, d, f,
+                                   b.h_save, b.a_save, b.y_perm)
+        else:
+            N.moe_permute(p.x, dt, T, d, k, b.dest_row, b.x_perm)
+            ev[0].record(stream)
+            N.moe_grouped_mlp_fwd(b.x_perm, p.w_gate, p.w_up, p.w_down, dt, b.offsets, b.R, E, d, f, b.h_save,
+                                  b.a_save, b.y_perm, b.workspace)
         ev[1].record(stream)
         N.moe_combine_fwd(b.y_perm, b.gates, b.dest_row, dt, T, d, k, b.y)
         N.moe_combine_bwd(p.dy, b.y_perm, b.gates, b.dest_row, dt, T, d, k, b.dy_perm, b.dgates)
         N.moe_route_bwd(b.dgates, b.gates, b.topk_idx, b.offsets, b.src_row, p.x, dt, T, d, E, k,
                         b.dlogits, b.dw_router)
         ev[2].record(stream)
-        N.moe_grouped_mlp_bwd(b.dy_perm, b.x_perm, b.h_save, b.a_save, p.w_gate, p.w_up, p.w_down, dt,
-                              b.offsets, b.R, E, d, f, b.dx_perm, b.dw_gate, b.dw_up, b.dw_down,
-                              b.workspace)
+        if fused:
+            N.moe_dispatch_mlp_bwd(b.dy_perm, p.x, b.src_row, T, k, b.h_save, b.a_save, p.w_gate, p.w_up,
+                                   p.w_down, dt, b.offsets, E, d, f, b.dx_perm, b.dw_gate, b.dw_up, b.dw_down,
+                                   b.workspace)
+        else:
+            N.moe_grouped_mlp_bwd(b.dy_perm, b.x_perm, b.h_save, b.a_save, p.w_gate, p.w_up, p.w_down, dt,
+                                  b.offsets, b.R, E, d, f, b.dx_perm, b.dw_gate, b.dw_up, b.dw_down,
+                                  b.workspace)
         ev[3].record(stream)
         N.moe_permute_bwd(b.dx_perm, dt, T, d, E, k, b.dest_row, b.topk_idx, b.dlogits, p.w_router, b.dx)
 
@@ -258,6 +288,7 @@ def run_ours(args, s, rank, world):
         peak *= 2.0
         peak_kind = f"{pk_kind} bf16 sustained x 2 (nominal FP8/bf16 ratio)"
     achieved = gemm_flops(s) / (gemm_ms / 1e3) / 1e12
+    traffic = None if (args.tokens or args.experts) else gemm_traffic(args.config)
     out = {
         "metric": METRIC,
         "value": tokens_per_s,
@@ -279,7 +310,8 @@ def run_ours(args, s, rank, world):
                                + ("; includes the MXFP8 operand quantisation)" if s.dtype == "mxfp8" else ")"),
                      "bound": "tensor",
                      "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
-                     "peak_kind": peak_kind, "traffic": None,
+                     "peak_kind": peak_kind, "traffic": traffic,
+                     "traffic_unit": "DRAM bytes per step of the six GEMM launches (ncu, see profiles/)",
                      "gemm_ms_per_step": gemm_ms},
         "e2e": {"value": world * s.T / (e2e_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},

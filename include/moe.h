@@ -154,6 +154,32 @@ moe_status moe_grouped_mlp_bwd(const void* dy_perm, const void* x_perm, const vo
                                void* dw_down, void* workspace, size_t workspace_bytes,
                                void* stream);
 
+/* The dispatch fused into the grouped MLP ("Scaling and optimizing MoE
+   training": routed rows go straight into the experts' inputs, and the layer
+   avoids reshuffling data). bf16 only (MOE_ERR_UNSUPPORTED otherwise).
+
+   moe_dispatch_mlp_fwd computes exactly moe_permute followed by
+   moe_grouped_mlp_fwd (same outputs, bit for bit) without writing x_perm:
+   GEMM1 reads row r of its A operand from x[src_row[r] / k] (x [T][d],
+   src_row [T*k] device int32 from moe_route), four rows per TMA gather.
+   R = T*k must fit an int.
+
+   moe_dispatch_mlp_bwd computes exactly moe_grouped_mlp_bwd on that x_perm,
+   with the GEMM1 weight gradient gathering its x rows the same way; it needs
+   the same workspace as moe_grouped_mlp_bwd.
+
+   Cost: every GEMM1 output-column tile gathers its rows again, and one row
+   gather moves 4 x 128 bytes; on GB300 these calls are slower than
+   moe_permute followed by the grouped MLP (which reads whole TMA boxes). */
+moe_status moe_dispatch_mlp_fwd(const void* x, const int32_t* src_row, int T, int k, const void* w_gate,
+                                const void* w_up, const void* w_down, int dtype, const int32_t* offsets, int E,
+                                int d, int f, void* h_save, void* a_save, void* y_perm, void* stream);
+moe_status moe_dispatch_mlp_bwd(const void* dy_perm, const void* x, const int32_t* src_row, int T, int k,
+                                const void* h_save, const void* a_save, const void* w_gate, const void* w_up,
+                                const void* w_down, int dtype, const int32_t* offsets, int E, int d, int f,
+                                void* dx_perm, void* dw_gate, void* dw_up, void* dw_down, void* workspace,
+                                size_t workspace_bytes, void* stream);
+
 /* MXFP8 block quantisation ("Scaling and optimizing MoE training": MXFP8):
    E4M3 codes with one E8M0 scale per 32 consecutive elements.
      axis 0: src [rows][K] bf16, blocks of 32 along K inside a row;

@@ -24,7 +24,8 @@ STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "M
 # every symbol include/moe.h declares
 EXPORTS = ("moe_workspace_size", "moe_route", "moe_permute", "moe_permute_bwd", "moe_combine_fwd",
            "moe_combine_bwd", "moe_route_bwd", "moe_grouped_mlp_fwd", "moe_grouped_mlp_bwd",
-           "mxfp8_quantize", "moe_get_device_error", "moe_sm_count", "moe_launch_count", "moe_route_noalloc")
+           "mxfp8_quantize", "moe_get_device_error", "moe_sm_count", "moe_launch_count", "moe_route_noalloc",
+           "moe_dispatch_mlp_fwd", "moe_dispatch_mlp_bwd")
 
 
 class MoEError(RuntimeError):
@@ -60,6 +61,8 @@ def load(path: str = LIB_PATH):
         "moe_sm_count": ([], I),
         "moe_launch_count": ([], ctypes.c_uint64),
         "moe_route_noalloc": ([P, P, P, I, I, I, I, I, P, I, P, P, P, P, P, P, P], I),
+        "moe_dispatch_mlp_fwd": ([P, P, I, I, P, P, P, I, P, I, I, I, P, P, P, P], I),
+        "moe_dispatch_mlp_bwd": ([P, P, P, I, I, P, P, P, P, P, I, P, I, I, I, P, P, P, P, P, Z, P], I),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -169,3 +172,18 @@ def moe_route_noalloc(x, w_router, bias, dtype, T, d, E, k, logits, flags, topk_
     _chk("moe_route_noalloc", load().moe_route_noalloc(
         _p(x), _p(w_router), _p(bias), dtype, T, d, E, k, _p(logits), flags, _p(topk_idx), _p(gates),
         _p(counts), _p(offsets), _p(dest_row), _p(src_row), _s(stream)))
+
+
+def moe_dispatch_mlp_fwd(x, src_row, T, k, w_gate, w_up, w_down, dtype, offsets, E, d, f, h_save, a_save,
+                         y_perm, stream=None):
+    _chk("moe_dispatch_mlp_fwd", load().moe_dispatch_mlp_fwd(
+        _p(x), _p(src_row), T, k, _p(w_gate), _p(w_up), _p(w_down), dtype, _p(offsets), E, d, f, _p(h_save),
+        _p(a_save), _p(y_perm), _s(stream)))
+
+
+def moe_dispatch_mlp_bwd(dy_perm, x, src_row, T, k, h_save, a_save, w_gate, w_up, w_down, dtype, offsets, E, d,
+                         f, dx_perm, dw_gate, dw_up, dw_down, workspace, stream=None):
+    _chk("moe_dispatch_mlp_bwd", load().moe_dispatch_mlp_bwd(
+        _p(dy_perm), _p(x), _p(src_row), T, k, _p(h_save), _p(a_save), _p(w_gate), _p(w_up), _p(w_down), dtype,
+        _p(offsets), E, d, f, _p(dx_perm), _p(dw_gate), _p(dw_up), _p(dw_down), _p(workspace), _nbytes(workspace),
+        _s(stream)))

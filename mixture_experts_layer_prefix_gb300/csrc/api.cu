@@ -326,6 +326,45 @@ moe_status moe_grouped_mlp_bwd(const void* dy_perm, const void* x_perm, const vo
   return MOE_OK;
 }
 
+moe_status moe_dispatch_mlp_fwd(const void* x, const int32_t* src_row, int T, int k, const void* w_gate,
+                                const void* w_up, const void* w_down, int dtype, const int32_t* offsets, int E,
+                                int d, int f, void* h_save, void* a_save, void* y_perm, void* stream) {
+  MOE_TRY(check_dims(T, d, E, k));
+  MOE_TRY(check_dtype(dtype));
+  if (dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
+  if (f <= 0) return MOE_ERR_INVALID_ARG;
+  if (f % 64 != 0 || (long)T * k > 0x7FFFFFFFL) return MOE_ERR_UNSUPPORTED;
+  MOE_NEED(w_gate); MOE_NEED(w_up); MOE_NEED(w_down); MOE_NEED(offsets);
+  if (T == 0) return MOE_OK;
+  MOE_NEED(x); MOE_NEED(src_row); MOE_NEED(h_save); MOE_NEED(a_save); MOE_NEED(y_perm);
+  MOE_CUDA_TRY(tc_mlp_fwd(x, w_gate, w_up, w_down, offsets, T * k, E, d, f, h_save, a_save, y_perm, S(stream),
+                          src_row, k, T));
+  return MOE_OK;
+}
+
+moe_status moe_dispatch_mlp_bwd(const void* dy_perm, const void* x, const int32_t* src_row, int T, int k,
+                                const void* h_save, const void* a_save, const void* w_gate, const void* w_up,
+                                const void* w_down, int dtype, const int32_t* offsets, int E, int d, int f,
+                                void* dx_perm, void* dw_gate, void* dw_up, void* dw_down, void* workspace,
+                                size_t workspace_bytes, void* stream) {
+  MOE_TRY(check_dims(T, d, E, k));
+  MOE_TRY(check_dtype(dtype));
+  if (dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
+  if (f <= 0) return MOE_ERR_INVALID_ARG;
+  if (f % 64 != 0 || (long)T * k > 0x7FFFFFFFL) return MOE_ERR_UNSUPPORTED;
+  MOE_NEED(w_gate); MOE_NEED(w_up); MOE_NEED(w_down); MOE_NEED(offsets);
+  MOE_NEED(dw_gate); MOE_NEED(dw_up); MOE_NEED(dw_down);
+  const int R = T * k;
+  if (workspace_bytes < mlp_bwd_ws(R, f, dtype)) return MOE_ERR_WORKSPACE;
+  if (R > 0) {
+    MOE_NEED(dy_perm); MOE_NEED(x); MOE_NEED(src_row); MOE_NEED(h_save); MOE_NEED(a_save);
+    MOE_NEED(dx_perm); MOE_NEED(workspace);
+  }
+  MOE_CUDA_TRY(tc_mlp_bwd(dy_perm, x, h_save, a_save, w_gate, w_up, w_down, offsets, R, E, d, f, dx_perm,
+                          dw_gate, dw_up, dw_down, workspace, S(stream), src_row, k, T));
+  return MOE_OK;
+}
+
 moe_status mxfp8_quantize(const void* src, int rows, int K, int axis, const int32_t* seg_offsets,
                           int nseg, uint8_t* dst_e4m3, uint8_t* dst_e8m0, void* stream) {
   if (rows < 0 || K <= 0 || (axis != 0 && axis != 1)) return MOE_ERR_INVALID_ARG;

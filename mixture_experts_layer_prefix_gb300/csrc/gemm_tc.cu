@@ -89,31 +89,55 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 
   if (warp == 0) {
     // ===================================================== TMA producer
+    // Lane 0 waits for free stages and issues the B (and plain A) loads. With
+    // the dispatch fused into GEMM1, lane L gathers A rows 4L..4L+3 of the
+    // tile straight from x (row src_row[r] / gk; rows past R read zeros) with
+    // one TMA row gather per stage.
     if (lane == 0) {
       ptx::prefetch_tmap(&tmA);
       ptx::prefetch_tmap(&tmB0);
       ptx::prefetch_tmap(&tmB1);
-      uint32_t it = 0;
-      bool ok = true;
-      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-        const Tile tl = decode<KIND, BK>(t, p, offs, tstart);
-        for (int kb = 0; kb < tl.nkb; ++kb, ++it) {
-          const int s = it % NS;
-          const uint32_t ph = (it / NS) & 1u;
-          if (!wait_bar(&sm->empty[s], ph ^ 1u, &sm->abort_flag, p.err)) { ok = false; break; }
-          uint8_t* a = smem + s * STAGE_BYTES;
-          uint8_t* b = a + A_BYTES;
-          uint64_t* fb = &sm->full[s];
-          ptx::mbar_expect_tx(fb, STAGE_BYTES);
-          const int k0 = kb * BK;
-          if (KIND == FPROP1) {
-            ptx::tma_load_2d(a, &tmA, fb, k0, tl.m0);
+    }
+    const bool gather = KIND == FPROP1 && p.src_row != nullptr;
+    uint32_t it = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+      const Tile tl = decode<KIND, BK>(t, p, offs, tstart);
+      int tok[4] = {0, 0, 0, 0};
+      if (gather) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int r = tl.m0 + 4 * lane + i;
+          tok[i] = r < p.R ? __ldg(p.src_row + r) / p.gk : p.T;
+        }
+      }
+      for (int kb = 0; kb < tl.nkb; ++kb, ++it) {
+        const int s = it % NS;
+        const uint32_t ph = (it / NS) & 1u;
+        bool free_stage = true;
+        if (lane == 0) free_stage = wait_bar(&sm->empty[s], ph ^ 1u, &sm->abort_flag, p.err);
+        if (!__shfl_sync(0xffffffffu, free_stage, 0)) {
+          ok = false;
+          break;
+        }
+        uint8_t* a = smem + s * STAGE_BYTES;
+        uint8_t* b = a + A_BYTES;
+        uint64_t* fb = &sm->full[s];
+        const int k0 = kb * BK;
+        if (lane == 0) ptx::mbar_expect_tx(fb, STAGE_BYTES);
+        __syncwarp();
+        if (gather) ptx::tma_gather4(a + lane * 512, &tmA, fb, k0, tok[0], tok[1], tok[2], tok[3]);
+        if (KIND == FPROP1) {
+          if (lane == 0) {
+            if (!gather) ptx::tma_load_2d(a, &tmA, fb, k0, tl.m0);
             const int n0 = tl.n_idx * 128;
             ptx::tma_load_3d(b + 0 * BOX_BYTES, &tmB0, fb, n0, k0, tl.e);
             ptx::tma_load_3d(b + 1 * BOX_BYTES, &tmB0, fb, n0 + 64, k0, tl.e);
             ptx::tma_load_3d(b + 2 * BOX_BYTES, &tmB1, fb, n0, k0, tl.e);
             ptx::tma_load_3d(b + 3 * BOX_BYTES, &tmB1, fb, n0 + 64, k0, tl.e);
-          } else if (KIND == FPROP2) {
+          }
+        } else if (lane == 0) {
+          if (KIND == FPROP2) {
             ptx::tma_load_2d(a, &tmA, fb, k0, tl.m0);
             const int n0 = tl.n_idx * BN;
 #pragma unroll
@@ -131,13 +155,13 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           }
         }
       }
-      if (!ok) {
-        // drain: wait (bounded) for loads already issued into stages the MMA will not consume
-        for (int s = 0; s < NS; ++s) {
-          const long long t0 = clock64();
-          while (clock64() - t0 < kWaitLimitCycles / 8 && !ptx::mbar_try_wait(&sm->full[s], 0) &&
-                 !ptx::mbar_try_wait(&sm->full[s], 1)) {
-          }
+    }
+    if (!ok && lane == 0) {
+      // drain: wait (bounded) for loads already issued into stages the MMA will not consume
+      for (int s = 0; s < NS; ++s) {
+        const long long t0 = clock64();
+        while (clock64() - t0 < kWaitLimitCycles / 8 && !ptx::mbar_try_wait(&sm->full[s], 0) &&
+               !ptx::mbar_try_wait(&sm->full[s], 1)) {
         }
       }
     }
@@ -297,35 +321,69 @@ tc_wgrad_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
 
   if (warp == 0) {
     // ===================================================== TMA producer
+    // Lane 0 waits for free stages and issues the B (and plain A) loads. With
+    // the dispatch fused into the GEMM1 wgrad, lane L gathers K rows
+    // 4(L%16)..+3 of the stage for A boxes 2(L/16) and 2(L/16)+1 straight from
+    // x with TMA row gathers; the next stage's token indices load while this
+    // stage waits. Rows past the expert's end (and columns past d) read zeros.
     if (lane == 0) {
       ptx::prefetch_tmap(&tmA);
       ptx::prefetch_tmap(&tmB);
-      uint32_t it = 0;
-      bool ok = true;
-      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-        int e, m0, n0, r0, r1, nkb;
-        decode_w(t, e, m0, n0, r0, r1, nkb);
-        for (int kb = 0; kb < nkb; ++kb, ++it) {
-          const int s = it % W_NS;
-          const uint32_t ph = (it / W_NS) & 1u;
-          if (!wait_bar(&sm->empty[s], ph ^ 1u, &sm->abort_flag, p.err)) { ok = false; break; }
-          uint8_t* a = smem + s * W_STAGE;
-          uint8_t* b = a + W_A_BYTES;
-          uint64_t* fb = &sm->full[s];
-          ptx::mbar_expect_tx(fb, W_STAGE);
-          const int row = r0 + kb * BK;
+    }
+    const bool gather = KIND == WGRAD1 && p.src_row != nullptr;
+    const int grp = lane & 15, jb = (lane >> 4) * 2;
+    uint32_t it = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+      int e, m0, n0, r0, r1, nkb;
+      decode_w(t, e, m0, n0, r0, r1, nkb);
+      auto tokens = [&](int kb, int (&tk)[4]) {
 #pragma unroll
-          for (int j = 0; j < 4; ++j) ptx::tma_load_2d(a + j * BOX_BYTES, &tmA, fb, m0 + 64 * j, row);
+        for (int i = 0; i < 4; ++i) {
+          const int r = r0 + kb * BK + 4 * grp + i;
+          tk[i] = r < r1 ? __ldg(p.src_row + r) / p.gk : p.T;
+        }
+      };
+      int nxt[4] = {0, 0, 0, 0};
+      if (gather && nkb > 0) tokens(0, nxt);
+      for (int kb = 0; kb < nkb; ++kb, ++it) {
+        const int cur[4] = {nxt[0], nxt[1], nxt[2], nxt[3]};
+        if (gather && kb + 1 < nkb) tokens(kb + 1, nxt);
+        const int s = it % W_NS;
+        const uint32_t ph = (it / W_NS) & 1u;
+        bool free_stage = true;
+        if (lane == 0) free_stage = wait_bar(&sm->empty[s], ph ^ 1u, &sm->abort_flag, p.err);
+        if (!__shfl_sync(0xffffffffu, free_stage, 0)) {
+          ok = false;
+          break;
+        }
+        uint8_t* a = smem + s * W_STAGE;
+        uint8_t* b = a + W_A_BYTES;
+        uint64_t* fb = &sm->full[s];
+        if (lane == 0) ptx::mbar_expect_tx(fb, W_STAGE);
+        __syncwarp();
+        const int row = r0 + kb * BK;
+        if (gather) {
+#pragma unroll
+          for (int jj = 0; jj < 2; ++jj)
+            ptx::tma_gather4(a + (jb + jj) * BOX_BYTES + grp * 512, &tmA, fb, m0 + 64 * (jb + jj), cur[0], cur[1],
+                             cur[2], cur[3]);
+        }
+        if (lane == 0) {
+          if (!gather) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) ptx::tma_load_2d(a + j * BOX_BYTES, &tmA, fb, m0 + 64 * j, row);
+          }
 #pragma unroll
           for (int j = 0; j < 4; ++j) ptx::tma_load_2d(b + j * BOX_BYTES, &tmB, fb, n0 + 64 * j, row);
         }
       }
-      if (!ok) {
-        for (int s = 0; s < W_NS; ++s) {
-          const long long t0 = clock64();
-          while (clock64() - t0 < kWaitLimitCycles / 8 && !ptx::mbar_try_wait(&sm->full[s], 0) &&
-                 !ptx::mbar_try_wait(&sm->full[s], 1)) {
-          }
+    }
+    if (!ok && lane == 0) {
+      for (int s = 0; s < W_NS; ++s) {
+        const long long t0 = clock64();
+        while (clock64() - t0 < kWaitLimitCycles / 8 && !ptx::mbar_try_wait(&sm->full[s], 0) &&
+               !ptx::mbar_try_wait(&sm->full[s], 1)) {
         }
       }
     }
@@ -541,17 +599,20 @@ using namespace tc;
 
 cudaError_t tc_mlp_fwd(const void* x_perm, const void* wg, const void* wu, const void* wd,
                        const int32_t* offsets, int R, int E, int d, int f, void* h, void* a, void* y,
-                       cudaStream_t st) {
+                       cudaStream_t st, const int32_t* src_row, int gk, int T) {
   CUtensorMap mA, mB0, mB1;
   Params p{};
   p.offsets = offsets; p.E = E; p.R = R; p.d = d; p.f = f; p.err = device_error_word();
-  // GEMM1 + SwiGLU: tiles of 128 f-columns (gate 128 | up 128 in one N=256 MMA)
-  if (!map_2d(&mA, x_perm, BF, 2, d, R, 64, BM) || !map_3d(&mB0, wg, BF, 2, f, d, E, 64, 64) ||
-      !map_3d(&mB1, wu, BF, 2, f, d, E, 64, 64))
+  // GEMM1 + SwiGLU: tiles of 128 f-columns (gate 128 | up 128 in one N=256 MMA). With src_row,
+  // x_perm is x [T][d] and the A rows are gathered one box row at a time.
+  const bool ok_a = src_row ? map_2d(&mA, x_perm, BF, 2, d, T, 64, 1) : map_2d(&mA, x_perm, BF, 2, d, R, 64, BM);
+  if (!ok_a || !map_3d(&mB0, wg, BF, 2, f, d, E, 64, 64) || !map_3d(&mB1, wu, BF, 2, f, d, E, 64, 64))
     return cudaErrorInvalidValue;
   p.N = f; p.n_tiles = (f + 127) / 128; p.out0 = h; p.out1 = a;
+  p.src_row = src_row; p.gk = gk; p.T = T;
   cudaError_t e = launch<FPROP1>(mA, mB0, mB1, p, ((long)(R + BM - 1) / BM + E) * p.n_tiles, st);
   if (e != cudaSuccess) return e;
+  p.src_row = nullptr;
   // GEMM2
   if (!map_2d(&mA, a, BF, 2, f, R, 64, BM) || !map_3d(&mB0, wd, BF, 2, d, f, E, 64, 64))
     return cudaErrorInvalidValue;
@@ -561,7 +622,8 @@ cudaError_t tc_mlp_fwd(const void* x_perm, const void* wg, const void* wu, const
 
 cudaError_t tc_mlp_bwd(const void* dy_perm, const void* x_perm, const void* h, const void* a, const void* wg,
                        const void* wu, const void* wd, const int32_t* offsets, int R, int E, int d, int f,
-                       void* dx_perm, void* dwg, void* dwu, void* dwd, void* dh, cudaStream_t st) {
+                       void* dx_perm, void* dwg, void* dwu, void* dwd, void* dh, cudaStream_t st,
+                       const int32_t* src_row, int gk, int T) {
   CUtensorMap mA, mB0, mB1;
   Params p{};
   p.offsets = offsets; p.E = E; p.R = R; p.d = d; p.f = f; p.err = device_error_word();
@@ -585,11 +647,12 @@ cudaError_t tc_mlp_bwd(const void* dy_perm, const void* x_perm, const void* h, c
   p.N = d; p.n_tiles = (d + BN - 1) / BN; p.out0 = dx_perm; p.aux = nullptr;
   e = launch<DGRAD1>(mA, mB0, mB1, p, ((long)(R + BM - 1) / BM + E) * p.n_tiles, st);
   if (e != cudaSuccess) return e;
-  // [dWg | dWu][e] = x_perm_e^T dh_e
-  if (!map_2d(&mA, x_perm, BF, 2, d, R, 64, 64) || !map_2d(&mB0, dh, BF, 2, 2L * f, R, 64, 64))
-    return cudaErrorInvalidValue;
+  // [dWg | dWu][e] = x_perm_e^T dh_e (with src_row: K rows gathered from x [T][d])
+  const bool ok_a = src_row ? map_2d(&mA, x_perm, BF, 2, d, T, 64, 1) : map_2d(&mA, x_perm, BF, 2, d, R, 64, 64);
+  if (!ok_a || !map_2d(&mB0, dh, BF, 2, 2L * f, R, 64, 64)) return cudaErrorInvalidValue;
   p.M = d; p.N = 2 * f; p.m_tiles = (d + WBM - 1) / WBM; p.n_tiles = (2 * f + BN - 1) / BN;
   p.out0 = dwg; p.out1 = dwu;
+  p.src_row = src_row; p.gk = gk; p.T = T;
   return launch_wgrad<WGRAD1>(mA, mB0, p, st);
 }
 

@@ -66,12 +66,15 @@ template <typename T>
 cudaError_t launch_swiglu_bwd(const void* da, const void* h, long rows, int f, void* dh, cudaStream_t st);
 
 // ------------------------------------------- tcgen05 grouped GEMMs (bf16)
+// src_row (optional): the dispatch is fused into GEMM1 and its wgrad; x_perm
+// then points at x [T][d] and row r of the dispatched matrix is x[src_row[r] / gk].
 cudaError_t tc_mlp_fwd(const void* x_perm, const void* wg, const void* wu, const void* wd,
                        const int32_t* offsets, int R, int E, int d, int f, void* h, void* a, void* y,
-                       cudaStream_t st);
+                       cudaStream_t st, const int32_t* src_row = nullptr, int gk = 1, int T = 0);
 cudaError_t tc_mlp_bwd(const void* dy_perm, const void* x_perm, const void* h, const void* a, const void* wg,
                        const void* wu, const void* wd, const int32_t* offsets, int R, int E, int d, int f,
-                       void* dx_perm, void* dwg, void* dwu, void* dwd, void* dh, cudaStream_t st);
+                       void* dx_perm, void* dwg, void* dwu, void* dwd, void* dh, cudaStream_t st,
+                       const int32_t* src_row = nullptr, int gk = 1, int T = 0);
 
 // ------------------------------------------------------------------ MXFP8
 cudaError_t launch_mxfp8_quant_rows(const void* src, long rows, long K, uint8_t* q, uint8_t* sc,

@@ -35,6 +35,10 @@ struct Params {
   const uint8_t* sfb1;     // MXFP8: scale bytes of the second B (up)
   uint8_t* qout;           // optional: the epilogue also writes its bf16 output
   uint8_t* qsc;            //   quantised along rows (E4M3 codes, E8M0 per 32)
+  // Dispatch fused into the A operand (GEMM1 forward and wgrad): row r of A is
+  // row src_row[r] / gk of x [T][d] (A's tensor map); nullptr: A is x_perm.
+  const int32_t* src_row;
+  int gk, T;
   int* err;
 };
 

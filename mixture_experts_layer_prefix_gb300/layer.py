@@ -7,6 +7,13 @@ library's kernels. Order of calls:
   forward : moe_route -> moe_permute -> moe_grouped_mlp_fwd -> moe_combine_fwd
   backward: moe_combine_bwd -> moe_route_bwd -> moe_grouped_mlp_bwd
             -> moe_permute_bwd (adds the router's share of dx)
+
+With fused=True (bf16 only) moe_dispatch_mlp_fwd / moe_dispatch_mlp_bwd
+replace moe_permute and the two grouped-MLP calls: GEMM1 and its weight
+gradient gather x's rows with TMA row gathers and x_perm is not written. The
+results are bit-identical, but on GB300 the row gathers (re-issued for every
+output-column tile) run far below the rate of whole-box loads, so the default
+is the permute followed by box loads.
 """
 from __future__ import annotations
 
@@ -94,25 +101,40 @@ class Buffers:
                                      dtype=torch.uint8, device=device)
 
 
-def forward(p: Params, b: Buffers, logits_in: bool = False, stream=None):
+def fused_default(dtype: int) -> bool:
+    """Whether the layer fuses the dispatch into the expert GEMMs by default:
+    no (measured slower than moe_permute + box loads at every tested shape)."""
+    return False
+
+
+def forward(p: Params, b: Buffers, logits_in: bool = False, stream=None, fused=None):
     T, d, E, k, f, dt = b.T, b.d, b.E, b.k, b.f, b.dtype
     N.moe_route(p.x, p.w_router, p.bias, dt, T, d, E, k, b.logits,
                 N.MOE_ROUTE_LOGITS_IN if logits_in else 0, b.topk_idx, b.gates, b.counts, b.offsets,
                 b.dest_row, b.src_row, b.workspace, stream)
-    N.moe_permute(p.x, dt, T, d, k, b.dest_row, b.x_perm, stream)
-    N.moe_grouped_mlp_fwd(b.x_perm, p.w_gate, p.w_up, p.w_down, dt, b.offsets, b.R, E, d, f, b.h_save,
-                          b.a_save, b.y_perm, b.workspace, stream)
+    if fused_default(dt) if fused is None else fused:
+        N.moe_dispatch_mlp_fwd(p.x, b.src_row, T, k, p.w_gate, p.w_up, p.w_down, dt, b.offsets, E, d, f,
+                               b.h_save, b.a_save, b.y_perm, stream)
+    else:
+        N.moe_permute(p.x, dt, T, d, k, b.dest_row, b.x_perm, stream)
+        N.moe_grouped_mlp_fwd(b.x_perm, p.w_gate, p.w_up, p.w_down, dt, b.offsets, b.R, E, d, f, b.h_save,
+                              b.a_save, b.y_perm, b.workspace, stream)
     N.moe_combine_fwd(b.y_perm, b.gates, b.dest_row, dt, T, d, k, b.y, stream)
 
 
-def backward(p: Params, b: Buffers, stream=None):
+def backward(p: Params, b: Buffers, stream=None, fused=None):
     T, d, E, k, f, dt = b.T, b.d, b.E, b.k, b.f, b.dtype
     N.moe_combine_bwd(p.dy, b.y_perm, b.gates, b.dest_row, dt, T, d, k, b.dy_perm, b.dgates, stream)
     N.moe_route_bwd(b.dgates, b.gates, b.topk_idx, b.offsets, b.src_row, p.x, dt, T, d, E, k,
                     b.dlogits, b.dw_router, stream)
-    N.moe_grouped_mlp_bwd(b.dy_perm, b.x_perm, b.h_save, b.a_save, p.w_gate, p.w_up, p.w_down, dt,
-                          b.offsets, b.R, E, d, f, b.dx_perm, b.dw_gate, b.dw_up, b.dw_down, b.workspace,
-                          stream)
+    if fused_default(dt) if fused is None else fused:
+        N.moe_dispatch_mlp_bwd(b.dy_perm, p.x, b.src_row, T, k, b.h_save, b.a_save, p.w_gate, p.w_up, p.w_down,
+                               dt, b.offsets, E, d, f, b.dx_perm, b.dw_gate, b.dw_up, b.dw_down, b.workspace,
+                               stream)
+    else:
+        N.moe_grouped_mlp_bwd(b.dy_perm, b.x_perm, b.h_save, b.a_save, p.w_gate, p.w_up, p.w_down, dt,
+                              b.offsets, b.R, E, d, f, b.dx_perm, b.dw_gate, b.dw_up, b.dw_down, b.workspace,
+                              stream)
     N.moe_permute_bwd(b.dx_perm, dt, T, d, E, k, b.dest_row, b.topk_idx, b.dlogits, p.w_router, b.dx,
                       stream)
 

@@ -70,3 +70,26 @@ def test_invalid_arguments_rejected_before_launch(lib):
     # f not a multiple of 64
     assert L.moe_grouped_mlp_fwd(FAKE, FAKE, FAKE, FAKE, 1, FAKE, 16, 4, 64, 100, FAKE, FAKE, FAKE,
                                  FAKE, 0, None) == 2
+
+
+def test_fused_dispatch_arguments_rejected_before_launch(lib):
+    L = lib
+    # fp32 / MXFP8 are not fused: unsupported
+    assert L.moe_dispatch_mlp_fwd(FAKE, FAKE, 8, 2, FAKE, FAKE, FAKE, 0, FAKE, 4, 64, 64, FAKE, FAKE, FAKE,
+                                  None) == 2
+    assert L.moe_dispatch_mlp_fwd(FAKE, FAKE, 8, 2, FAKE, FAKE, FAKE, 2, FAKE, 4, 64, 64, FAKE, FAKE, FAKE,
+                                  None) == 2
+    # k > E
+    assert L.moe_dispatch_mlp_fwd(FAKE, FAKE, 8, 5, FAKE, FAKE, FAKE, 1, FAKE, 4, 64, 64, FAKE, FAKE, FAKE,
+                                  None) == 1
+    # missing src_row
+    assert L.moe_dispatch_mlp_fwd(FAKE, None, 8, 2, FAKE, FAKE, FAKE, 1, FAKE, 4, 64, 64, FAKE, FAKE, FAKE,
+                                  None) == 1
+    # T*k past the int range
+    assert L.moe_dispatch_mlp_fwd(FAKE, FAKE, 1 << 30, 4, FAKE, FAKE, FAKE, 1, FAKE, 4, 64, 64, FAKE, FAKE,
+                                  FAKE, None) == 2
+    # backward: workspace too small for dh, misaligned x
+    assert L.moe_dispatch_mlp_bwd(FAKE, FAKE, FAKE, 8, 2, FAKE, FAKE, FAKE, FAKE, FAKE, 1, FAKE, 4, 64, 64,
+                                  FAKE, FAKE, FAKE, FAKE, FAKE, 16, None) == 4
+    assert L.moe_dispatch_mlp_bwd(FAKE, FAKE + 8, FAKE, 8, 2, FAKE, FAKE, FAKE, FAKE, FAKE, 1, FAKE, 4, 64, 64,
+                                  FAKE, FAKE, FAKE, FAKE, FAKE, 1 << 20, None) == 3

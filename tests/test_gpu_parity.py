@@ -137,9 +137,50 @@ def test_deterministic_bitwise():
 def test_permute_is_exact_copy():
     s = _shape("perm", 999, 512, 32, 4, 64)
     inp, p, b = run_gpu(s)
+    N.moe_permute(p.x, N.MOE_BF16, s.T, s.d, s.k, b.dest_row, b.x_perm)
+    torch.cuda.synchronize()
     x = p.x.cpu()
     src = b.src_row.cpu().long() // s.k
     assert torch.equal(b.x_perm.cpu(), x[src])
+
+
+FUSED_SHAPES = [
+    _shape("fused_ragged", 1000, 256, 16, 4, 192),
+    _shape("fused_skew_dead", 1500, 320, 32, 4, 256, zipf_s=1.2, zipf_alpha=0.8, n_dead=3),
+    _shape("fused_e320_k2", 600, 128, 320, 2, 64),
+    _shape("fused_one_token", 1, 64, 4, 2, 64),
+    _shape("fused_e8_k2_wide", 2048, 1024, 8, 2, 512),
+]
+
+
+@pytest.mark.parametrize("s", FUSED_SHAPES, ids=lambda s: s.name)
+def test_fused_dispatch_matches_permute_path(s):
+    """The dispatch fused into GEMM1 and its weight gradient (rows gathered from
+    x through src_row) reads the same values as moe_permute + the grouped MLP,
+    so every output is bit-identical."""
+    dt = N.MOE_BF16
+    inp = synth.Inputs(s, seed=2)
+    p = L.params_from_inputs(inp, dt)
+    outs = []
+    for fused in (False, True):
+        b = L.Buffers(s.T, s.d, s.E, s.k, s.f, dt)
+        L.forward(p, b, fused=fused)
+        L.backward(p, b, fused=fused)
+        torch.cuda.synchronize()
+        assert N.moe_get_device_error() == 0
+        outs.append([t.clone() for t in (b.h_save, b.a_save, b.y_perm, b.y, b.dx_perm, b.dx, b.dw_gate, b.dw_up,
+                                         b.dw_down, b.dw_router)])
+    names = ("h_save", "a_save", "y_perm", "y", "dx_perm", "dx", "dw_gate", "dw_up", "dw_down", "dw_router")
+    for n_, a, c in zip(names, *outs):
+        assert torch.equal(a, c), n_
+
+
+def test_fused_dispatch_rejects_other_dtypes():
+    b = L.Buffers(8, 64, 4, 2, 64, N.MOE_F32)
+    w = torch.zeros(4, 64, 64, device="cuda")
+    with pytest.raises(N.MoEError):
+        N.moe_dispatch_mlp_fwd(torch.zeros(8, 64, device="cuda"), b.src_row, 8, 2, w, w, w, N.MOE_F32, b.offsets,
+                               4, 64, 64, b.h_save, b.a_save, b.y_perm)
 
 
 def test_zero_tokens():

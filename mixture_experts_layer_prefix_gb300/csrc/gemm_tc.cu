@@ -47,7 +47,8 @@ struct Smem {
   int abort_flag;
 };
 
-template <int KIND>
+// GATHER: the dispatch is fused into GEMM1 (FPROP1 only; p.src_row set).
+template <int KIND, bool GATHER = false>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
                const __grid_constant__ CUtensorMap tmB1, const Params p) {
@@ -89,79 +90,110 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 
   if (warp == 0) {
     // ===================================================== TMA producer
-    // Lane 0 waits for free stages and issues the B (and plain A) loads. With
-    // the dispatch fused into GEMM1, lane L gathers A rows 4L..4L+3 of the
-    // tile straight from x (row src_row[r] / gk; rows past R read zeros) with
-    // one TMA row gather per stage.
-    if (lane == 0) {
-      ptx::prefetch_tmap(&tmA);
-      ptx::prefetch_tmap(&tmB0);
-      ptx::prefetch_tmap(&tmB1);
-    }
-    const bool gather = KIND == FPROP1 && p.src_row != nullptr;
-    uint32_t it = 0;
-    bool ok = true;
-    for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-      const Tile tl = decode<KIND, BK>(t, p, offs, tstart);
-      int tok[4] = {0, 0, 0, 0};
-      if (gather) {
+    if constexpr (!GATHER) {
+      if (lane == 0) {
+        ptx::prefetch_tmap(&tmA);
+        ptx::prefetch_tmap(&tmB0);
+        ptx::prefetch_tmap(&tmB1);
+        uint32_t it = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+          const Tile tl = decode<KIND, BK>(t, p, offs, tstart);
+          for (int kb = 0; kb < tl.nkb; ++kb, ++it) {
+            const int s = it % NS;
+            const uint32_t ph = (it / NS) & 1u;
+            if (!wait_bar(&sm->empty[s], ph ^ 1u, &sm->abort_flag, p.err)) { ok = false; break; }
+            uint8_t* a = smem + s * STAGE_BYTES;
+            uint8_t* b = a + A_BYTES;
+            uint64_t* fb = &sm->full[s];
+            ptx::mbar_expect_tx(fb, STAGE_BYTES);
+            const int k0 = kb * BK;
+            if (KIND == FPROP1) {
+              ptx::tma_load_2d(a, &tmA, fb, k0, tl.m0);
+              const int n0 = tl.n_idx * 128;
+              ptx::tma_load_3d(b + 0 * BOX_BYTES, &tmB0, fb, n0, k0, tl.e);
+              ptx::tma_load_3d(b + 1 * BOX_BYTES, &tmB0, fb, n0 + 64, k0, tl.e);
+              ptx::tma_load_3d(b + 2 * BOX_BYTES, &tmB1, fb, n0, k0, tl.e);
+              ptx::tma_load_3d(b + 3 * BOX_BYTES, &tmB1, fb, n0 + 64, k0, tl.e);
+            } else if (KIND == FPROP2) {
+              ptx::tma_load_2d(a, &tmA, fb, k0, tl.m0);
+              const int n0 = tl.n_idx * BN;
+#pragma unroll
+              for (int j = 0; j < 4; ++j) ptx::tma_load_3d(b + j * BOX_BYTES, &tmB0, fb, n0 + 64 * j, k0, tl.e);
+            } else if (KIND == DGRAD2) {
+              ptx::tma_load_2d(a, &tmA, fb, k0, tl.m0);
+              ptx::tma_load_3d(b, &tmB0, fb, k0, tl.n_idx * BN, tl.e);
+            } else if (KIND == ROUTER) {
+              ptx::tma_load_2d(a, &tmA, fb, k0, tl.m0);
+              ptx::tma_load_2d(b, &tmB0, fb, k0, tl.n_idx * BN);
+            } else {  // DGRAD1
+              ptx::tma_load_2d(a, &tmA, fb, k0, tl.m0);
+              if (k0 < p.f) ptx::tma_load_3d(b, &tmB0, fb, k0, tl.n_idx * BN, tl.e);
+              else ptx::tma_load_3d(b, &tmB1, fb, k0 - p.f, tl.n_idx * BN, tl.e);
+            }
+          }
+        }
+        if (!ok) {
+          // drain: wait (bounded) for loads already issued into stages the MMA will not consume
+          for (int s = 0; s < NS; ++s) {
+            const long long t0 = clock64();
+            while (clock64() - t0 < kWaitLimitCycles / 8 && !ptx::mbar_try_wait(&sm->full[s], 0) &&
+                   !ptx::mbar_try_wait(&sm->full[s], 1)) {
+            }
+          }
+        }
+      }
+    } else {
+      // GEMM1 with the dispatch fused: lane 0 waits for free stages and
+      // issues the B loads; lane L gathers A rows 4L..4L+3 of the tile
+      // straight from x (row src_row[r] / gk; rows past R read zeros) with
+      // one TMA row gather per stage.
+      if (lane == 0) {
+        ptx::prefetch_tmap(&tmA);
+        ptx::prefetch_tmap(&tmB0);
+        ptx::prefetch_tmap(&tmB1);
+      }
+      uint32_t it = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+        const Tile tl = decode<KIND, BK>(t, p, offs, tstart);
+        int tok[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const int r = tl.m0 + 4 * lane + i;
           tok[i] = r < p.R ? __ldg(p.src_row + r) / p.gk : p.T;
         }
-      }
-      for (int kb = 0; kb < tl.nkb; ++kb, ++it) {
-        const int s = it % NS;
-        const uint32_t ph = (it / NS) & 1u;
-        bool free_stage = true;
-        if (lane == 0) free_stage = wait_bar(&sm->empty[s], ph ^ 1u, &sm->abort_flag, p.err);
-        if (!__shfl_sync(0xffffffffu, free_stage, 0)) {
-          ok = false;
-          break;
-        }
-        uint8_t* a = smem + s * STAGE_BYTES;
-        uint8_t* b = a + A_BYTES;
-        uint64_t* fb = &sm->full[s];
-        const int k0 = kb * BK;
-        if (lane == 0) ptx::mbar_expect_tx(fb, STAGE_BYTES);
-        __syncwarp();
-        if (gather) ptx::tma_gather4(a + lane * 512, &tmA, fb, k0, tok[0], tok[1], tok[2], tok[3]);
-        if (KIND == FPROP1) {
+        for (int kb = 0; kb < tl.nkb; ++kb, ++it) {
+          const int s = it % NS;
+          const uint32_t ph = (it / NS) & 1u;
+          bool free_stage = true;
+          if (lane == 0) free_stage = wait_bar(&sm->empty[s], ph ^ 1u, &sm->abort_flag, p.err);
+          if (!__shfl_sync(0xffffffffu, free_stage, 0)) {
+            ok = false;
+            break;
+          }
+          uint8_t* a = smem + s * STAGE_BYTES;
+          uint8_t* b = a + A_BYTES;
+          uint64_t* fb = &sm->full[s];
+          const int k0 = kb * BK;
+          if (lane == 0) ptx::mbar_expect_tx(fb, STAGE_BYTES);
+          __syncwarp();
+          ptx::tma_gather4(a + lane * 512, &tmA, fb, k0, tok[0], tok[1], tok[2], tok[3]);
           if (lane == 0) {
-            if (!gather) ptx::tma_load_2d(a, &tmA, fb, k0, tl.m0);
             const int n0 = tl.n_idx * 128;
             ptx::tma_load_3d(b + 0 * BOX_BYTES, &tmB0, fb, n0, k0, tl.e);
             ptx::tma_load_3d(b + 1 * BOX_BYTES, &tmB0, fb, n0 + 64, k0, tl.e);
             ptx::tma_load_3d(b + 2 * BOX_BYTES, &tmB1, fb, n0, k0, tl.e);
             ptx::tma_load_3d(b + 3 * BOX_BYTES, &tmB1, fb, n0 + 64, k0, tl.e);
           }
-        } else if (lane == 0) {
-          if (KIND == FPROP2) {
-            ptx::tma_load_2d(a, &tmA, fb, k0, tl.m0);
-            const int n0 = tl.n_idx * BN;
-#pragma unroll
-            for (int j = 0; j < 4; ++j) ptx::tma_load_3d(b + j * BOX_BYTES, &tmB0, fb, n0 + 64 * j, k0, tl.e);
-          } else if (KIND == DGRAD2) {
-            ptx::tma_load_2d(a, &tmA, fb, k0, tl.m0);
-            ptx::tma_load_3d(b, &tmB0, fb, k0, tl.n_idx * BN, tl.e);
-          } else if (KIND == ROUTER) {
-            ptx::tma_load_2d(a, &tmA, fb, k0, tl.m0);
-            ptx::tma_load_2d(b, &tmB0, fb, k0, tl.n_idx * BN);
-          } else {  // DGRAD1
-            ptx::tma_load_2d(a, &tmA, fb, k0, tl.m0);
-            if (k0 < p.f) ptx::tma_load_3d(b, &tmB0, fb, k0, tl.n_idx * BN, tl.e);
-            else ptx::tma_load_3d(b, &tmB1, fb, k0 - p.f, tl.n_idx * BN, tl.e);
-          }
         }
       }
-    }
-    if (!ok && lane == 0) {
-      // drain: wait (bounded) for loads already issued into stages the MMA will not consume
-      for (int s = 0; s < NS; ++s) {
-        const long long t0 = clock64();
-        while (clock64() - t0 < kWaitLimitCycles / 8 && !ptx::mbar_try_wait(&sm->full[s], 0) &&
-               !ptx::mbar_try_wait(&sm->full[s], 1)) {
+      if (!ok && lane == 0) {
+        for (int s = 0; s < NS; ++s) {
+          const long long t0 = clock64();
+          while (clock64() - t0 < kWaitLimitCycles / 8 && !ptx::mbar_try_wait(&sm->full[s], 0) &&
+                 !ptx::mbar_try_wait(&sm->full[s], 1)) {
+          }
         }
       }
     }
@@ -249,16 +281,16 @@ size_t smem_bytes(int E) {
   return 1024 + STAGES * STAGE_BYTES + OUT_STG_BYTES + sizeof(Smem) + 2 * (E + 1) * sizeof(int) + 64;
 }
 
-template <int KIND>
+template <int KIND, bool GATHER = false>
 cudaError_t launch(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1, const Params& p,
                    long max_tiles, cudaStream_t st) {
   if (max_tiles <= 0) return cudaSuccess;
   const size_t smem = smem_bytes<KIND>(p.E);
-  cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<KIND, GATHER>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   const int grid = static_cast<int>(max_tiles < sm_count() ? max_tiles : sm_count());
-  MOE_COUNTED tc_gemm_kernel<KIND><<<grid, NUM_THREADS, smem, st>>>(a, b0, b1, p);
+  MOE_COUNTED tc_gemm_kernel<KIND, GATHER><<<grid, NUM_THREADS, smem, st>>>(a, b0, b1, p);
   return cudaGetLastError();
 }
 
@@ -277,10 +309,12 @@ constexpr int W_STAGE = W_A_BYTES + W_B_BYTES;
 constexpr int W_NS = 3;
 constexpr int W_STG = 32 * 128;  // per epilogue warp: 32 rows x 64 bf16, 16-byte granules XOR-swizzled by row
 
-template <int KIND>
+// GATHER: the dispatch is fused into the GEMM1 wgrad (WGRAD1 only; p.src_row set).
+template <int KIND, bool GATHER = false>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 tc_wgrad_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const Params p) {
   static_assert(Traits<KIND>::kragged, "weight-gradient kinds only");
+  static_assert(!GATHER || KIND == WGRAD1, "the row gather feeds the GEMM1 wgrad only");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   Smem* sm = reinterpret_cast<Smem*>(smem + W_NS * W_STAGE + NUM_EPI_WARPS * W_STG);
@@ -321,69 +355,97 @@ tc_wgrad_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
 
   if (warp == 0) {
     // ===================================================== TMA producer
-    // Lane 0 waits for free stages and issues the B (and plain A) loads. With
-    // the dispatch fused into the GEMM1 wgrad, lane L gathers K rows
-    // 4(L%16)..+3 of the stage for A boxes 2(L/16) and 2(L/16)+1 straight from
-    // x with TMA row gathers; the next stage's token indices load while this
-    // stage waits. Rows past the expert's end (and columns past d) read zeros.
-    if (lane == 0) {
-      ptx::prefetch_tmap(&tmA);
-      ptx::prefetch_tmap(&tmB);
-    }
-    const bool gather = KIND == WGRAD1 && p.src_row != nullptr;
-    const int grp = lane & 15, jb = (lane >> 4) * 2;
-    uint32_t it = 0;
-    bool ok = true;
-    for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-      int e, m0, n0, r0, r1, nkb;
-      decode_w(t, e, m0, n0, r0, r1, nkb);
-      auto tokens = [&](int kb, int (&tk)[4]) {
+    if constexpr (!GATHER) {
+      if (lane == 0) {
+        ptx::prefetch_tmap(&tmA);
+        ptx::prefetch_tmap(&tmB);
+        uint32_t it = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+          int e, m0, n0, r0, r1, nkb;
+          decode_w(t, e, m0, n0, r0, r1, nkb);
+          for (int kb = 0; kb < nkb; ++kb, ++it) {
+            const int s = it % W_NS;
+            const uint32_t ph = (it / W_NS) & 1u;
+            if (!wait_bar(&sm->empty[s], ph ^ 1u, &sm->abort_flag, p.err)) { ok = false; break; }
+            uint8_t* a = smem + s * W_STAGE;
+            uint8_t* b = a + W_A_BYTES;
+            uint64_t* fb = &sm->full[s];
+            ptx::mbar_expect_tx(fb, W_STAGE);
+            const int row = r0 + kb * BK;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int r = r0 + kb * BK + 4 * grp + i;
-          tk[i] = r < r1 ? __ldg(p.src_row + r) / p.gk : p.T;
+            for (int j = 0; j < 4; ++j) ptx::tma_load_2d(a + j * BOX_BYTES, &tmA, fb, m0 + 64 * j, row);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) ptx::tma_load_2d(b + j * BOX_BYTES, &tmB, fb, n0 + 64 * j, row);
+          }
         }
-      };
-      int nxt[4] = {0, 0, 0, 0};
-      if (gather && nkb > 0) tokens(0, nxt);
-      for (int kb = 0; kb < nkb; ++kb, ++it) {
-        const int cur[4] = {nxt[0], nxt[1], nxt[2], nxt[3]};
-        if (gather && kb + 1 < nkb) tokens(kb + 1, nxt);
-        const int s = it % W_NS;
-        const uint32_t ph = (it / W_NS) & 1u;
-        bool free_stage = true;
-        if (lane == 0) free_stage = wait_bar(&sm->empty[s], ph ^ 1u, &sm->abort_flag, p.err);
-        if (!__shfl_sync(0xffffffffu, free_stage, 0)) {
-          ok = false;
-          break;
+        if (!ok) {
+          for (int s = 0; s < W_NS; ++s) {
+            const long long t0 = clock64();
+            while (clock64() - t0 < kWaitLimitCycles / 8 && !ptx::mbar_try_wait(&sm->full[s], 0) &&
+                   !ptx::mbar_try_wait(&sm->full[s], 1)) {
+            }
+          }
         }
-        uint8_t* a = smem + s * W_STAGE;
-        uint8_t* b = a + W_A_BYTES;
-        uint64_t* fb = &sm->full[s];
-        if (lane == 0) ptx::mbar_expect_tx(fb, W_STAGE);
-        __syncwarp();
-        const int row = r0 + kb * BK;
-        if (gather) {
+      }
+    } else {
+      // GEMM1 wgrad with the dispatch fused: lane 0 waits for free stages and
+      // issues the B loads; lane L gathers K rows 4(L%16)..+3 of the stage for
+      // A boxes 2(L/16) and 2(L/16)+1 straight from x with TMA row gathers,
+      // the next stage's token indices loading while this stage waits. Rows
+      // past the expert's end (and columns past d) read zeros.
+      if (lane == 0) {
+        ptx::prefetch_tmap(&tmA);
+        ptx::prefetch_tmap(&tmB);
+      }
+      const int grp = lane & 15, jb = (lane >> 4) * 2;
+      uint32_t it = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+        int e, m0, n0, r0, r1, nkb;
+        decode_w(t, e, m0, n0, r0, r1, nkb);
+        auto tokens = [&](int kb, int (&tk)[4]) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int r = r0 + kb * BK + 4 * grp + i;
+            tk[i] = r < r1 ? __ldg(p.src_row + r) / p.gk : p.T;
+          }
+        };
+        int nxt[4] = {0, 0, 0, 0};
+        if (nkb > 0) tokens(0, nxt);
+        for (int kb = 0; kb < nkb; ++kb, ++it) {
+          const int cur[4] = {nxt[0], nxt[1], nxt[2], nxt[3]};
+          if (kb + 1 < nkb) tokens(kb + 1, nxt);
+          const int s = it % W_NS;
+          const uint32_t ph = (it / W_NS) & 1u;
+          bool free_stage = true;
+          if (lane == 0) free_stage = wait_bar(&sm->empty[s], ph ^ 1u, &sm->abort_flag, p.err);
+          if (!__shfl_sync(0xffffffffu, free_stage, 0)) {
+            ok = false;
+            break;
+          }
+          uint8_t* a = smem + s * W_STAGE;
+          uint8_t* b = a + W_A_BYTES;
+          uint64_t* fb = &sm->full[s];
+          if (lane == 0) ptx::mbar_expect_tx(fb, W_STAGE);
+          __syncwarp();
 #pragma unroll
           for (int jj = 0; jj < 2; ++jj)
             ptx::tma_gather4(a + (jb + jj) * BOX_BYTES + grp * 512, &tmA, fb, m0 + 64 * (jb + jj), cur[0], cur[1],
                              cur[2], cur[3]);
-        }
-        if (lane == 0) {
-          if (!gather) {
+          if (lane == 0) {
+            const int row = r0 + kb * BK;
 #pragma unroll
-            for (int j = 0; j < 4; ++j) ptx::tma_load_2d(a + j * BOX_BYTES, &tmA, fb, m0 + 64 * j, row);
+            for (int j = 0; j < 4; ++j) ptx::tma_load_2d(b + j * BOX_BYTES, &tmB, fb, n0 + 64 * j, row);
           }
-#pragma unroll
-          for (int j = 0; j < 4; ++j) ptx::tma_load_2d(b + j * BOX_BYTES, &tmB, fb, n0 + 64 * j, row);
         }
       }
-    }
-    if (!ok && lane == 0) {
-      for (int s = 0; s < W_NS; ++s) {
-        const long long t0 = clock64();
-        while (clock64() - t0 < kWaitLimitCycles / 8 && !ptx::mbar_try_wait(&sm->full[s], 0) &&
-               !ptx::mbar_try_wait(&sm->full[s], 1)) {
+      if (!ok && lane == 0) {
+        for (int s = 0; s < W_NS; ++s) {
+          const long long t0 = clock64();
+          while (clock64() - t0 < kWaitLimitCycles / 8 && !ptx::mbar_try_wait(&sm->full[s], 0) &&
+                 !ptx::mbar_try_wait(&sm->full[s], 1)) {
+          }
         }
       }
     }
@@ -526,16 +588,16 @@ tc_wgrad_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
   }
 }
 
-template <int KIND>
+template <int KIND, bool GATHER = false>
 cudaError_t launch_wgrad(const CUtensorMap& a, const CUtensorMap& b, const Params& p, cudaStream_t st) {
   const long tiles = (long)p.E * p.m_tiles * p.n_tiles;
   if (tiles <= 0) return cudaSuccess;
   const size_t smem = 1024 + W_NS * W_STAGE + NUM_EPI_WARPS * W_STG + sizeof(Smem) + 64;
-  cudaError_t e = cudaFuncSetAttribute(tc_wgrad_kernel<KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = cudaFuncSetAttribute(tc_wgrad_kernel<KIND, GATHER>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   const int grid = static_cast<int>(tiles < sm_count() ? tiles : sm_count());
-  MOE_COUNTED tc_wgrad_kernel<KIND><<<grid, NUM_THREADS, smem, st>>>(a, b, p);
+  MOE_COUNTED tc_wgrad_kernel<KIND, GATHER><<<grid, NUM_THREADS, smem, st>>>(a, b, p);
   return cudaGetLastError();
 }
 
@@ -610,7 +672,9 @@ cudaError_t tc_mlp_fwd(const void* x_perm, const void* wg, const void* wu, const
     return cudaErrorInvalidValue;
   p.N = f; p.n_tiles = (f + 127) / 128; p.out0 = h; p.out1 = a;
   p.src_row = src_row; p.gk = gk; p.T = T;
-  cudaError_t e = launch<FPROP1>(mA, mB0, mB1, p, ((long)(R + BM - 1) / BM + E) * p.n_tiles, st);
+  const long fp1_tiles = ((long)(R + BM - 1) / BM + E) * p.n_tiles;
+  cudaError_t e = src_row ? launch<FPROP1, true>(mA, mB0, mB1, p, fp1_tiles, st)
+                          : launch<FPROP1>(mA, mB0, mB1, p, fp1_tiles, st);
   if (e != cudaSuccess) return e;
   p.src_row = nullptr;
   // GEMM2
@@ -653,7 +717,7 @@ cudaError_t tc_mlp_bwd(const void* dy_perm, const void* x_perm, const void* h, c
   p.M = d; p.N = 2 * f; p.m_tiles = (d + WBM - 1) / WBM; p.n_tiles = (2 * f + BN - 1) / BN;
   p.out0 = dwg; p.out1 = dwu;
   p.src_row = src_row; p.gk = gk; p.T = T;
-  return launch_wgrad<WGRAD1>(mA, mB0, p, st);
+  return src_row ? launch_wgrad<WGRAD1, true>(mA, mB0, p, st) : launch_wgrad<WGRAD1>(mA, mB0, p, st);
 }
 
 cudaError_t tc_router_logits(const void* x, const void* w_r, const float* bias, int T, int d, int E,

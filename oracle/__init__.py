@@ -54,6 +54,7 @@ def _L():
             lib.oc_router_logits.argtypes = [P, P, P, I, I, I, P, I]
             lib.oc_topk.argtypes = [P, I, I, I, P]
             lib.oc_gates.argtypes = [P, P, I, I, I, P]
+            lib.oc_route_stats.argtypes = [P, P, I, I, I, P, P]
             lib.oc_dispatch.argtypes = [P, I, I, I, P, P, P, P]
             lib.oc_forward.argtypes = [P, P, P, P, P, P, I, I, I, I, I, P, P, P, P, P, I]
             lib.oc_backward.argtypes = [P] * 12 + [I] * 5 + [P] * 10 + [I]
@@ -121,6 +122,20 @@ def gates(logits, topk_idx):
     g = np.empty((T, k), np.float64)
     _L().oc_gates(_p(l), _p(idx), T, E, k, _p(g))
     return g
+
+
+def route_stats(logits, counts, k):
+    """Routing load statistics: (probs_mean [E], stats [4]) with stats =
+    (E * sum_e f_e probs_mean_e, max load / mean load, empty experts,
+    std / mean of the counts), f_e = counts_e / (T k), probs_mean the mean
+    full softmax over E. The pages give no formula for a balance metric: parity
+    unpinned by the pages (pinned here by closed forms and invariants)."""
+    l, c = _f64(logits), _i32(counts)
+    T, E = l.shape
+    pm = np.empty(E, np.float64)
+    st = np.empty(4, np.float64)
+    _L().oc_route_stats(_p(l), _p(c), T, E, k, _p(pm), _p(st))
+    return pm, st
 
 
 def dispatch(topk_idx, E):

@@ -115,6 +115,44 @@ void oc_topk(const double* logits, int T, int E, int k, int32_t* topk_idx) {
 }
 
 /* gates[t][j] = exp(l_{S_j} - m) / sum_{i in S} exp(l_i - m), m = max over S. */
+/* Routing load statistics (the next step after routing: a load-balance
+ * metric kept alongside the routing metadata). The pages name the concern
+ * (experts gaming or starving the token distribution) but give no formula,
+ * so this is the plainest set of statistics; parity is unpinned by the pages.
+ *   probs_mean[e] = (1/T) sum_t softmax(logits[t])_e   (softmax over all E)
+ *   f_e           = counts[e] / (T k)
+ *   stats[0]      = E * sum_e f_e probs_mean[e]   (1 under perfect balance)
+ *   stats[1]      = max_e counts[e] * E / (T k)   (largest load / mean load)
+ *   stats[2]      = number of experts with counts[e] == 0
+ *   stats[3]      = population std of counts / their mean               */
+void oc_route_stats(const double* logits, const int32_t* counts, int T, int E, int k, double* probs_mean,
+                    double* stats) {
+  for (int e = 0; e < E; ++e) probs_mean[e] = 0.0;
+  for (long t = 0; t < T; ++t) {
+    const double* l = logits + t * E;
+    double m = l[0];
+    for (int e = 1; e < E; ++e) if (l[e] > m) m = l[e];
+    double z = 0.0;
+    for (int e = 0; e < E; ++e) z += exp(l[e] - m);
+    for (int e = 0; e < E; ++e) probs_mean[e] += exp(l[e] - m) / z;
+  }
+  for (int e = 0; e < E; ++e) probs_mean[e] = T > 0 ? probs_mean[e] / T : 0.0;
+  const double R = (double)T * k, mean = R / E;
+  double aux = 0.0, mx = 0.0, var = 0.0;
+  int empty = 0;
+  for (int e = 0; e < E; ++e) {
+    const double f = R > 0 ? counts[e] / R : 0.0;
+    aux += f * probs_mean[e];
+    if (counts[e] > mx) mx = counts[e];
+    if (counts[e] == 0) ++empty;
+    var += (counts[e] - mean) * (counts[e] - mean);
+  }
+  stats[0] = E * aux;
+  stats[1] = mean > 0 ? mx / mean : 0.0;
+  stats[2] = empty;
+  stats[3] = mean > 0 ? sqrt(var / E) / mean : 0.0;
+}
+
 void oc_gates(const double* logits, const int32_t* topk_idx, int T, int E, int k, double* gates) {
   for (long t = 0; t < T; ++t) {
     const double* l = logits + t * E;

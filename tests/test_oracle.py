@@ -415,3 +415,41 @@ def test_mxfp8_oracle_bf16_rounding_matches_library():
     v = rng.standard_normal(100000) * np.exp(rng.uniform(-30, 30, 100000))
     ref = torch.tensor(v, dtype=torch.float64).to(torch.bfloat16).double().numpy()
     np.testing.assert_array_equal(mxfp8_layer.round_bf16(v), ref)
+
+
+# ---------------------------------------------------------------- routing load statistics
+def test_route_stats_uniform_and_balanced():
+    T, E, k = 96, 8, 2
+    pm, st = oracle.route_stats(np.zeros((T, E)), np.full(E, T * k // E, np.int32), k)
+    np.testing.assert_allclose(pm, np.full(E, 1.0 / E), rtol=0, atol=1e-15)
+    np.testing.assert_allclose(st, [1.0, 1.0, 0.0, 0.0], rtol=0, atol=1e-15)
+
+
+def test_route_stats_all_tokens_on_one_expert_closed_forms():
+    T, E, k = 50, 6, 1
+    logits = np.zeros((T, E))
+    logits[:, 2] = 3.0
+    counts = np.zeros(E, np.int32)
+    counts[2] = T
+    pm, st = oracle.route_stats(logits, counts, k)
+    p2 = np.exp(3.0) / (np.exp(3.0) + (E - 1))
+    assert abs(pm[2] - p2) < 1e-15
+    assert abs(st[0] - E * p2) < 1e-13           # E * f_2 * P_2 with f_2 = 1
+    assert st[1] == E                             # T / (T / E)
+    assert st[2] == E - 1
+    assert abs(st[3] - np.sqrt(E - 1)) < 1e-12    # std / mean of (T, 0, ..., 0)
+
+
+def test_route_stats_matches_library_softmax_and_is_label_invariant():
+    special = pytest.importorskip("scipy.special")
+    rng = np.random.default_rng(4)
+    T, E, k = 200, 12, 3
+    logits = rng.standard_normal((T, E)) * 2.0
+    counts = rng.integers(0, 90, E).astype(np.int32)
+    pm, st = oracle.route_stats(logits, counts, k)
+    np.testing.assert_allclose(pm, special.softmax(logits, axis=1).mean(axis=0), rtol=1e-13, atol=0)
+    assert abs(pm.sum() - 1.0) < 1e-13
+    perm = rng.permutation(E)
+    pm2, st2 = oracle.route_stats(logits[:, perm], counts[perm], k)
+    np.testing.assert_allclose(pm2, pm[perm], rtol=1e-13, atol=0)
+    np.testing.assert_allclose(st2, st, rtol=1e-12, atol=0)

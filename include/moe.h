@@ -126,6 +126,21 @@ moe_status moe_route_bwd(const float* dgates, const float* gates, const int32_t*
                          int dtype, int T, int d, int E, int k, float* dlogits, float* dw_router,
                          void* stream);
 
+/* Routing load statistics, kept alongside the routing metadata (the pages
+   name an unbalanced token distribution as the risk of expert routing but
+   give no formula; these are the plainest statistics):
+     probs_mean[e] = (1/T) sum_t softmax(logits[t])_e   (softmax over all E)
+     stats[0] = E * sum_e (counts[e] / (T k)) * probs_mean[e]   (1 if balanced)
+     stats[1] = max_e counts[e] * E / (T k)   (largest load over the mean)
+     stats[2] = number of experts with counts[e] == 0
+     stats[3] = population std of counts / mean count
+   logits [T][E] fp32 and counts [E] int32 as moe_route left them; probs_mean
+   [E] and stats [4] fp32, written on the device (no host sync). Every sum runs
+   in a fixed order (bit-reproducible). workspace: at least
+   ceil(T / 256) * E * 4 bytes (moe_workspace_size is always enough). E <= 1024. */
+moe_status moe_route_stats(const float* logits, const int32_t* counts, int T, int E, int k, float* probs_mean,
+                           float* stats, void* workspace, size_t workspace_bytes, void* stream);
+
 /* Grouped SwiGLU expert MLP, forward, all experts in one launch per GEMM
    ("Scaling and optimizing MoE training": grouped GEMM). For every expert e
    and row r in [offsets[e], offsets[e+1]):

@@ -25,7 +25,7 @@ STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "M
 EXPORTS = ("moe_workspace_size", "moe_route", "moe_permute", "moe_permute_bwd", "moe_combine_fwd",
            "moe_combine_bwd", "moe_route_bwd", "moe_grouped_mlp_fwd", "moe_grouped_mlp_bwd",
            "mxfp8_quantize", "moe_get_device_error", "moe_sm_count", "moe_launch_count", "moe_route_noalloc",
-           "moe_dispatch_mlp_fwd", "moe_dispatch_mlp_bwd")
+           "moe_dispatch_mlp_fwd", "moe_dispatch_mlp_bwd", "moe_route_stats")
 
 
 class MoEError(RuntimeError):
@@ -62,6 +62,7 @@ def load(path: str = LIB_PATH):
         "moe_launch_count": ([], ctypes.c_uint64),
         "moe_route_noalloc": ([P, P, P, I, I, I, I, I, P, I, P, P, P, P, P, P, P], I),
         "moe_dispatch_mlp_fwd": ([P, P, I, I, P, P, P, I, P, I, I, I, P, P, P, P], I),
+        "moe_route_stats": ([P, P, I, I, I, P, P, P, Z, P], I),
         "moe_dispatch_mlp_bwd": ([P, P, P, I, I, P, P, P, P, P, I, P, I, I, I, P, P, P, P, P, Z, P], I),
     }
     for name, (args, res) in sig.items():
@@ -187,3 +188,8 @@ def moe_dispatch_mlp_bwd(dy_perm, x, src_row, T, k, h_save, a_save, w_gate, w_up
         _p(dy_perm), _p(x), _p(src_row), T, k, _p(h_save), _p(a_save), _p(w_gate), _p(w_up), _p(w_down), dtype,
         _p(offsets), E, d, f, _p(dx_perm), _p(dw_gate), _p(dw_up), _p(dw_down), _p(workspace), _nbytes(workspace),
         _s(stream)))
+
+
+def moe_route_stats(logits, counts, T, E, k, probs_mean, stats, workspace, stream=None):
+    _chk("moe_route_stats", load().moe_route_stats(_p(logits), _p(counts), T, E, k, _p(probs_mean), _p(stats),
+                                                   _p(workspace), _nbytes(workspace), _s(stream)))

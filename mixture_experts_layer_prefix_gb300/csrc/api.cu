@@ -140,6 +140,8 @@ size_t moe_workspace_size(int T, int d, int E, int k, int f, int dtype) {
   size_t route = align256(route_workspace_bytes(T, E));
   size_t bwd = mlp_bwd_ws(R, f, dtype == MOE_F32 ? MOE_F32 : MOE_BF16);
   size_t ws = route > bwd ? route : bwd;
+  const size_t stats = align256(route_stats_workspace_bytes(T, E));
+  ws = ws > stats ? ws : stats;
   if (dtype == MOE_MXFP8) {
     const size_t mf = mx_fwd_workspace(R, E, d, f), mb = mx_bwd_workspace(R, E, d, f);
     ws = ws > mf ? ws : mf;
@@ -323,6 +325,21 @@ moe_status moe_grouped_mlp_bwd(const void* dy_perm, const void* x_perm, const vo
                                f, dx_perm, dw_gate, dw_up, dw_down, workspace, S(stream));
   MOE_CUDA_TRY(tc_mlp_bwd(dy_perm, x_perm, h_save, a_save, w_gate, w_up, w_down, offsets, R, E, d, f,
                           dx_perm, dw_gate, dw_up, dw_down, workspace, S(stream)));
+  return MOE_OK;
+}
+
+moe_status moe_route_stats(const float* logits, const int32_t* counts, int T, int E, int k, float* probs_mean,
+                           float* stats, void* workspace, size_t workspace_bytes, void* stream) {
+  if (T < 0 || E <= 0 || k <= 0 || k > E) return MOE_ERR_INVALID_ARG;
+  if (E > 1024) return MOE_ERR_UNSUPPORTED;
+  MOE_NEED(counts); MOE_NEED(probs_mean); MOE_NEED(stats);
+  const size_t need = route_stats_workspace_bytes(T, E);
+  if (workspace_bytes < need) return MOE_ERR_WORKSPACE;
+  if (T > 0) {
+    MOE_NEED(logits); MOE_NEED(workspace);
+  }
+  MOE_CUDA_TRY(launch_route_stats(logits, counts, T, E, k, probs_mean, stats, static_cast<float*>(workspace),
+                                  S(stream)));
   return MOE_OK;
 }
 

@@ -19,6 +19,11 @@ cudaError_t launch_route_meta(const float* logits, int T, int E, int k, int32_t*
                               float* gates, int32_t* counts, int32_t* offsets, int32_t* dest_row,
                               int32_t* src_row, int32_t* hist, cudaStream_t st);
 
+// ------------------------------------------------------ routing statistics
+size_t route_stats_workspace_bytes(int T, int E);
+cudaError_t launch_route_stats(const float* logits, const int32_t* counts, int T, int E, int k, float* probs_mean,
+                               float* stats, float* partial, cudaStream_t st);
+
 // ------------------------------------------------ permute / combine / router bwd
 template <typename T>
 cudaError_t launch_permute(const void* x, int Tn, int d, int k, const int32_t* dest_row, void* x_perm,

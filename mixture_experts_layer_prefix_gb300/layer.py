@@ -101,6 +101,15 @@ class Buffers:
                                      dtype=torch.uint8, device=device)
 
 
+def route_stats(b: Buffers, stream=None):
+    """Routing load statistics of the last moe_route into ``b``: (probs_mean [E],
+    stats [4]) device tensors -- see moe_route_stats in include/moe.h."""
+    pm = torch.empty(b.E, dtype=torch.float32, device=b.logits.device)
+    st = torch.empty(4, dtype=torch.float32, device=b.logits.device)
+    N.moe_route_stats(b.logits, b.counts, b.T, b.E, b.k, pm, st, b.workspace, stream)
+    return pm, st
+
+
 def fused_default(dtype: int) -> bool:
     """Whether the layer fuses the dispatch into the expert GEMMs by default:
     no (measured slower than moe_permute + box loads at every tested shape)."""

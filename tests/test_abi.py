@@ -93,3 +93,11 @@ def test_fused_dispatch_arguments_rejected_before_launch(lib):
                                   FAKE, FAKE, FAKE, FAKE, FAKE, 16, None) == 4
     assert L.moe_dispatch_mlp_bwd(FAKE, FAKE + 8, FAKE, 8, 2, FAKE, FAKE, FAKE, FAKE, FAKE, 1, FAKE, 4, 64, 64,
                                   FAKE, FAKE, FAKE, FAKE, FAKE, 1 << 20, None) == 3
+
+
+def test_route_stats_arguments_rejected_before_launch(lib):
+    L = lib
+    assert L.moe_route_stats(FAKE, FAKE, 8, 4, 5, FAKE, FAKE, FAKE, 1 << 20, None) == 1      # k > E
+    assert L.moe_route_stats(FAKE, FAKE, 8, 2048, 2, FAKE, FAKE, FAKE, 1 << 20, None) == 2   # E > 1024
+    assert L.moe_route_stats(FAKE, FAKE, 4096, 128, 4, FAKE, FAKE, FAKE, 16, None) == 4      # workspace
+    assert L.moe_route_stats(FAKE, None, 8, 4, 2, FAKE, FAKE, FAKE, 1 << 20, None) == 1      # counts

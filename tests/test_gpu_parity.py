@@ -226,3 +226,35 @@ def test_host_pipeline_matches_direct_calls():
         assert torch.equal(b.y.cpu(), ys[i]), f"y of step {i}"
         assert torch.equal(b.dx.cpu(), dxs[i]), f"dx of step {i}"
     assert torch.equal(b.dw_router, dwr_pipe)
+
+
+STATS_SHAPES = [(1000, 16, 4, False), (4096, 128, 4, True), (300, 320, 2, False), (1, 8, 2, False),
+                (777, 1024, 8, True)]
+
+
+@pytest.mark.parametrize("T,E,k,dead", STATS_SHAPES, ids=lambda v: str(v))
+def test_route_stats_parity(T, E, k, dead):
+    """Routing load statistics vs the oracle on the GPU's own logits and counts.
+    fp32 sums over at most ~100 partials per expert: 2e-5 relative."""
+    rng = np.random.default_rng(T + E)
+    logits = (rng.standard_normal((T, E)) * 2.0).astype(np.float32)
+    if dead:
+        logits[:, :3] -= 1e4  # three experts never selected
+        logits[:, 5] += 3.0   # one busy expert
+    b = L.Buffers(T, 64, E, k, 64, N.MOE_BF16)
+    b.logits.copy_(torch.from_numpy(logits))
+    N.moe_route(None, None, None, N.MOE_BF16, T, 64, E, k, b.logits, N.MOE_ROUTE_LOGITS_IN, b.topk_idx,
+                b.gates, b.counts, b.offsets, b.dest_row, b.src_row, b.workspace)
+    pm, st = L.route_stats(b)
+    torch.cuda.synchronize()
+    assert N.moe_get_device_error() == 0
+    counts = b.counts.cpu().numpy()
+    ref_pm, ref_st = oracle.route_stats(logits.astype(np.float64), counts, k)
+    np.testing.assert_allclose(pm.cpu().numpy(), ref_pm, rtol=2e-5, atol=1e-9)
+    got = st.cpu().numpy().astype(np.float64)
+    np.testing.assert_allclose(got[[0, 1, 3]], ref_st[[0, 1, 3]], rtol=2e-5, atol=1e-6)
+    assert got[2] == ref_st[2]
+    if dead:
+        assert got[2] >= 3
+    pm2, st2 = L.route_stats(b)
+    assert torch.equal(pm, pm2) and torch.equal(st, st2)

@@ -194,13 +194,19 @@ def run_ours(args, s, rank, world):
     b = L.Buffers(s.T, s.d, s.E, s.k, s.f, dt)
     stream = torch.cuda.current_stream()
     fused = L.fused_default(dt)
+    mx = dt == N.MOE_MXFP8
 
     def step_timed(ev):
         # forward and backward through the C ABI; events bracket the GEMM stages
         T, d, E, k, f = s.T, s.d, s.E, s.k, s.f
         N.moe_route(p.x, p.w_router, p.bias, dt, T, d, E, k, b.logits, 0, b.topk_idx, b.gates, b.counts,
                     b.offsets, b.dest_row, b.src_row, b.workspace)
-        if fused:  # the dispatch runs inside GEMM1 (rows gathered from x)
+        if mx:  # MXFP8: x quantised as it is dispatched
+            N.moe_permute_mxfp8(p.x, T, d, k, b.dest_row, b.x_q, b.x_sc, b.x_perm)
+            ev[0].record(stream)
+            N.moe_mxfp8_mlp_fwd(b.x_q, b.x_sc, p.w_gate, p.w_up, p.w_down, b.offsets, b.R, E, d, f, b.h_save,
+                                b.a_save, b.y_perm, b.workspace)
+        elif fused:  # the dispatch runs inside GEMM1 (rows gathered from x)
             ev[0].record(stream)
             N.moe_dispatch_mlp_fwd(p.x, b.src_row, T, k, p.w_gate, p.w_up, p.w_down, dt, b.offsets, E, d, f,
                                    b.h_save, b.a_save, b.y_perm)
@@ -211,11 +217,19 @@ def run_ours(args, s, rank, world):
                                   b.a_save, b.y_perm, b.workspace)
         ev[1].record(stream)
         N.moe_combine_fwd(b.y_perm, b.gates, b.dest_row, dt, T, d, k, b.y)
-        N.moe_combine_bwd(p.dy, b.y_perm, b.gates, b.dest_row, dt, T, d, k, b.dy_perm, b.dgates)
+        if mx:  # MXFP8: dy_perm quantised as the combine backward produces it
+            N.moe_combine_bwd_mxfp8(p.dy, b.y_perm, b.gates, b.dest_row, T, d, k, b.dy_q, b.dy_sc, b.dy_perm,
+                                    b.dgates)
+        else:
+            N.moe_combine_bwd(p.dy, b.y_perm, b.gates, b.dest_row, dt, T, d, k, b.dy_perm, b.dgates)
         N.moe_route_bwd(b.dgates, b.gates, b.topk_idx, b.offsets, b.src_row, p.x, dt, T, d, E, k,
                         b.dlogits, b.dw_router)
         ev[2].record(stream)
-        if fused:
+        if mx:
+            N.moe_mxfp8_mlp_bwd(b.dy_q, b.dy_sc, b.dy_perm, b.x_perm, b.h_save, b.a_save, p.w_gate, p.w_up,
+                                p.w_down, b.offsets, b.R, E, d, f, b.dx_perm, b.dw_gate, b.dw_up, b.dw_down,
+                                b.workspace)
+        elif fused:
             N.moe_dispatch_mlp_bwd(b.dy_perm, p.x, b.src_row, T, k, b.h_save, b.a_save, p.w_gate, p.w_up,
                                    p.w_down, dt, b.offsets, E, d, f, b.dx_perm, b.dw_gate, b.dw_up, b.dw_down,
                                    b.workspace)

@@ -195,6 +195,44 @@ moe_status moe_dispatch_mlp_bwd(const void* dy_perm, const void* x, const int32_
                                 void* dx_perm, void* dw_gate, void* dw_up, void* dw_down, void* workspace,
                                 size_t workspace_bytes, void* stream);
 
+/* MXFP8 with the row quantisation of the dispatched activations moved into
+   the kernels that produce them ("Scaling and optimizing MoE training": the
+   MXFP8 gains come from the expert feed-forward and from moving expert data;
+   the savings must exceed the cost of the format conversion):
+
+   moe_permute_mxfp8: the dispatch of x as E4M3 codes x_codes [T*k][d] and
+   E8M0 scales x_scales [T*k][d/32]; row dest_row[t][j] holds x[t] quantised
+   along d in blocks of 32 (the bytes mxfp8_quantize gives for moe_permute's
+   bf16 x_perm). x bf16 [T][d]. x_perm (optional, may be NULL) receives the
+   bf16 dispatch as well (the weight gradient quantises it along its rows).
+
+   moe_combine_bwd_mxfp8: moe_combine_bwd that also writes the row
+   quantisation (dy_codes [T*k][d], dy_scales [T*k][d/32]) of the bf16-rounded
+   values gates[t][j] * dy[t]; dy_perm (optional, may be NULL) receives the
+   bf16 values; dgates as moe_combine_bwd.
+
+   moe_mxfp8_mlp_fwd: moe_grouped_mlp_fwd(MOE_MXFP8) with GEMM1 reading
+   x_codes/x_scales (no separate quantisation pass). Same outputs, same
+   workspace.
+
+   moe_mxfp8_mlp_bwd: moe_grouped_mlp_bwd(MOE_MXFP8) with the GEMM2 dgrad
+   reading dy_codes/dy_scales; dy_perm and x_perm (bf16) feed the
+   expert-segment quantisations of the weight gradients. Same outputs, same
+   workspace. d and f multiples of 128. */
+moe_status moe_permute_mxfp8(const void* x, int T, int d, int k, const int32_t* dest_row, uint8_t* x_codes,
+                             uint8_t* x_scales, void* x_perm, void* stream);
+moe_status moe_combine_bwd_mxfp8(const void* dy, const void* y_perm, const float* gates, const int32_t* dest_row,
+                                 int T, int d, int k, uint8_t* dy_codes, uint8_t* dy_scales, void* dy_perm,
+                                 float* dgates, void* stream);
+moe_status moe_mxfp8_mlp_fwd(const uint8_t* x_codes, const uint8_t* x_scales, const void* w_gate, const void* w_up,
+                             const void* w_down, const int32_t* offsets, int R, int E, int d, int f, void* h_save,
+                             void* a_save, void* y_perm, void* workspace, size_t workspace_bytes, void* stream);
+moe_status moe_mxfp8_mlp_bwd(const uint8_t* dy_codes, const uint8_t* dy_scales, const void* dy_perm,
+                             const void* x_perm, const void* h_save, const void* a_save, const void* w_gate,
+                             const void* w_up, const void* w_down, const int32_t* offsets, int R, int E, int d, int f,
+                             void* dx_perm, void* dw_gate, void* dw_up, void* dw_down, void* workspace,
+                             size_t workspace_bytes, void* stream);
+
 /* MXFP8 block quantisation ("Scaling and optimizing MoE training": MXFP8):
    E4M3 codes with one E8M0 scale per 32 consecutive elements.
      axis 0: src [rows][K] bf16, blocks of 32 along K inside a row;

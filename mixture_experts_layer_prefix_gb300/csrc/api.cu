@@ -328,6 +328,66 @@ moe_status moe_grouped_mlp_bwd(const void* dy_perm, const void* x_perm, const vo
   return MOE_OK;
 }
 
+moe_status moe_permute_mxfp8(const void* x, int T, int d, int k, const int32_t* dest_row, uint8_t* x_codes,
+                             uint8_t* x_scales, void* x_perm, void* stream) {
+  MOE_TRY(check_dims(T, d, k, k));
+  if (T == 0) return MOE_OK;
+  MOE_NEED(x); MOE_NEED(dest_row); MOE_NEED(x_codes); MOE_NEED(x_scales);
+  if (x_perm && !aligned16(x_perm)) return MOE_ERR_ALIGNMENT;
+  MOE_CUDA_TRY(launch_permute_quant(x, T, d, k, dest_row, x_codes, x_scales, x_perm, S(stream)));
+  return MOE_OK;
+}
+
+moe_status moe_combine_bwd_mxfp8(const void* dy, const void* y_perm, const float* gates, const int32_t* dest_row,
+                                 int T, int d, int k, uint8_t* dy_codes, uint8_t* dy_scales, void* dy_perm,
+                                 float* dgates, void* stream) {
+  MOE_TRY(check_dims(T, d, k, k));
+  if (T == 0) return MOE_OK;
+  MOE_NEED(dy); MOE_NEED(y_perm); MOE_NEED(gates); MOE_NEED(dest_row); MOE_NEED(dy_codes); MOE_NEED(dy_scales);
+  MOE_NEED(dgates);
+  if (dy_perm && !aligned16(dy_perm)) return MOE_ERR_ALIGNMENT;
+  MOE_CUDA_TRY(launch_combine_bwd_quant(dy, y_perm, gates, dest_row, T, d, k, dy_codes, dy_scales, dy_perm, dgates,
+                                        S(stream)));
+  return MOE_OK;
+}
+
+moe_status moe_mxfp8_mlp_fwd(const uint8_t* x_codes, const uint8_t* x_scales, const void* w_gate, const void* w_up,
+                             const void* w_down, const int32_t* offsets, int R, int E, int d, int f, void* h_save,
+                             void* a_save, void* y_perm, void* workspace, size_t workspace_bytes, void* stream) {
+  MOE_TRY(check_dims(R, d, E, 1));
+  if (f <= 0) return MOE_ERR_INVALID_ARG;
+  if (d % 128 != 0 || f % 128 != 0) return MOE_ERR_UNSUPPORTED;
+  MOE_NEED(w_gate); MOE_NEED(w_up); MOE_NEED(w_down); MOE_NEED(offsets);
+  if (R == 0) return MOE_OK;
+  MOE_NEED(x_codes); MOE_NEED(x_scales); MOE_NEED(h_save); MOE_NEED(a_save); MOE_NEED(y_perm);
+  if (workspace_bytes < mx_fwd_workspace(R, E, d, f)) return MOE_ERR_WORKSPACE;
+  MOE_NEED(workspace);
+  MOE_CUDA_TRY(mx_mlp_fwd(nullptr, w_gate, w_up, w_down, offsets, R, E, d, f, h_save, a_save, y_perm, workspace,
+                          S(stream), x_codes, x_scales));
+  return MOE_OK;
+}
+
+moe_status moe_mxfp8_mlp_bwd(const uint8_t* dy_codes, const uint8_t* dy_scales, const void* dy_perm,
+                             const void* x_perm, const void* h_save, const void* a_save, const void* w_gate,
+                             const void* w_up, const void* w_down, const int32_t* offsets, int R, int E, int d, int f,
+                             void* dx_perm, void* dw_gate, void* dw_up, void* dw_down, void* workspace,
+                             size_t workspace_bytes, void* stream) {
+  MOE_TRY(check_dims(R, d, E, 1));
+  if (f <= 0) return MOE_ERR_INVALID_ARG;
+  if (d % 128 != 0 || f % 128 != 0) return MOE_ERR_UNSUPPORTED;
+  MOE_NEED(w_gate); MOE_NEED(w_up); MOE_NEED(w_down); MOE_NEED(offsets);
+  MOE_NEED(dw_gate); MOE_NEED(dw_up); MOE_NEED(dw_down);
+  if (workspace_bytes < mx_bwd_workspace(R, E, d, f)) return MOE_ERR_WORKSPACE;
+  MOE_NEED(workspace);
+  if (R > 0) {
+    MOE_NEED(dy_codes); MOE_NEED(dy_scales); MOE_NEED(dy_perm); MOE_NEED(x_perm); MOE_NEED(h_save);
+    MOE_NEED(a_save); MOE_NEED(dx_perm);
+  }
+  MOE_CUDA_TRY(mx_mlp_bwd(dy_perm, x_perm, h_save, a_save, w_gate, w_up, w_down, offsets, R, E, d, f, dx_perm,
+                          dw_gate, dw_up, dw_down, workspace, S(stream), dy_codes, dy_scales));
+  return MOE_OK;
+}
+
 moe_status moe_route_stats(const float* logits, const int32_t* counts, int T, int E, int k, float* probs_mean,
                            float* stats, void* workspace, size_t workspace_bytes, void* stream) {
   if (T < 0 || E <= 0 || k <= 0 || k > E) return MOE_ERR_INVALID_ARG;

@@ -537,7 +537,8 @@ size_t bwd_workspace(long R, int E, int d, int f) {
 using namespace tc;
 
 cudaError_t mx_mlp_fwd(const void* x_perm, const void* wg, const void* wu, const void* wd, const int32_t* offsets,
-                       int R, int E, int d, int f, void* h, void* a, void* y, void* ws, cudaStream_t st) {
+                       int R, int E, int d, int f, void* h, void* a, void* y, void* ws, cudaStream_t st,
+                       const uint8_t* xq_codes, const uint8_t* xq_scales) {
   using namespace mx;
   Carver cv{static_cast<char*>(ws)};
   const long Ed = (long)E * d, Ef = (long)E * f;
@@ -547,8 +548,14 @@ cudaError_t mx_mlp_fwd(const void* x_perm, const void* wg, const void* wu, const
   QBuf wuq = cv.take((size_t)Ed * f, (size_t)Ed / 32 * f);
   QBuf wdq = cv.take((size_t)Ef * d, (size_t)Ef / 32 * d);
   cudaError_t e;
-  // operands of GEMM1 along d: x rows, w_gate / w_up columns (32-row blocks never cross experts)
-  if ((e = launch_mxfp8_quant_rows(x_perm, R, d, xq.q, xq.s, st)) != cudaSuccess) return e;
+  // operands of GEMM1 along d: x rows (already quantised when the dispatch did
+  // it), w_gate / w_up columns (32-row blocks never cross experts)
+  if (xq_codes) {
+    xq.q = const_cast<uint8_t*>(xq_codes);
+    xq.s = const_cast<uint8_t*>(xq_scales);
+  } else if ((e = launch_mxfp8_quant_rows(x_perm, R, d, xq.q, xq.s, st)) != cudaSuccess) {
+    return e;
+  }
   if ((e = launch_mxfp8_quant_cols(wg, (int)Ed, f, nullptr, 1, wgq.q, wgq.s, st, true)) != cudaSuccess) return e;
   if ((e = launch_mxfp8_quant_cols(wu, (int)Ed, f, nullptr, 1, wuq.q, wuq.s, st, true)) != cudaSuccess) return e;
   if ((e = launch_mxfp8_quant_cols(wd, (int)Ef, d, nullptr, 1, wdq.q, wdq.s, st, true)) != cudaSuccess) return e;
@@ -575,7 +582,8 @@ cudaError_t mx_mlp_fwd(const void* x_perm, const void* wg, const void* wu, const
 
 cudaError_t mx_mlp_bwd(const void* dy_perm, const void* x_perm, const void* h, const void* a, const void* wg,
                        const void* wu, const void* wd, const int32_t* offsets, int R, int E, int d, int f,
-                       void* dx_perm, void* dwg, void* dwu, void* dwd, void* ws, cudaStream_t st) {
+                       void* dx_perm, void* dwg, void* dwu, void* dwd, void* ws, cudaStream_t st,
+                       const uint8_t* dyq_codes, const uint8_t* dyq_scales) {
   using namespace mx;
   Carver cv{static_cast<char*>(ws)};
   const long Ed = (long)E * d, Ef = (long)E * f;
@@ -594,8 +602,14 @@ cudaError_t mx_mlp_bwd(const void* dy_perm, const void* x_perm, const void* h, c
   Params p{};
   p.offsets = offsets; p.E = E; p.R = R; p.d = d; p.f = f; p.err = device_error_word();
 
-  // dA = dy . Wd^T (K = d): dy rows, w_down rows; SwiGLU backward fused -> dh
-  if ((e = launch_mxfp8_quant_rows(dy_perm, R, d, dyr.q, dyr.s, st)) != cudaSuccess) return e;
+  // dA = dy . Wd^T (K = d): dy rows (already quantised when the combine
+  // backward did it), w_down rows; SwiGLU backward fused -> dh
+  if (dyq_codes) {
+    dyr.q = const_cast<uint8_t*>(dyq_codes);
+    dyr.s = const_cast<uint8_t*>(dyq_scales);
+  } else if ((e = launch_mxfp8_quant_rows(dy_perm, R, d, dyr.q, dyr.s, st)) != cudaSuccess) {
+    return e;
+  }
   if ((e = launch_mxfp8_quant_rows(wd, Ef, d, wdr.q, wdr.s, st)) != cudaSuccess) return e;
   if (!map_2d(&mA, dyr.q, U8, 1, d, R, 128, BM) || !map_3d(&mB0, wdr.q, U8, 1, d, f, E, 128, kN_DGRAD2))
     return cudaErrorInvalidValue;

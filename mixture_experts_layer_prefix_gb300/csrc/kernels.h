@@ -19,6 +19,11 @@ cudaError_t launch_route_meta(const float* logits, int T, int E, int k, int32_t*
                               float* gates, int32_t* counts, int32_t* offsets, int32_t* dest_row,
                               int32_t* src_row, int32_t* hist, cudaStream_t st);
 
+// combine backward writing the MXFP8 row quantisation of dy_perm (bf16 only)
+cudaError_t launch_combine_bwd_quant(const void* dy, const void* y_perm, const float* gates,
+                                     const int32_t* dest_row, int Tn, int d, int k, uint8_t* q, uint8_t* qsc,
+                                     void* dy_perm, float* dgates, cudaStream_t st);
+
 // ------------------------------------------------------ routing statistics
 size_t route_stats_workspace_bytes(int T, int E);
 cudaError_t launch_route_stats(const float* logits, const int32_t* counts, int T, int E, int k, float* probs_mean,
@@ -88,6 +93,10 @@ cudaError_t launch_mxfp8_quant_rows(const void* src, long rows, long K, uint8_t*
 // layout); otherwise one byte per block, [blocks][C] (public layout).
 cudaError_t launch_mxfp8_quant_cols(const void* src, int rows, int C, const int32_t* seg, int nseg,
                                     uint8_t* q, uint8_t* sc, cudaStream_t st, bool packed = false);
+// Dispatch with the row quantisation fused: q [T*k][d], sc [T*k][d/32]; the
+// bf16 x_perm too when given.
+cudaError_t launch_permute_quant(const void* x, int T, int d, int k, const int32_t* dest_row, uint8_t* q,
+                                 uint8_t* sc, void* x_perm, cudaStream_t st);
 
 cudaError_t tc_router_logits(const void* x, const void* w_r, const float* bias, int T, int d, int E,
                              float* logits, cudaStream_t st);
@@ -96,9 +105,13 @@ cudaError_t tc_router_logits(const void* x, const void* w_r, const float* bias, 
 size_t mx_fwd_workspace(long R, int E, int d, int f);
 size_t mx_bwd_workspace(long R, int E, int d, int f);
 cudaError_t mx_mlp_fwd(const void* x_perm, const void* wg, const void* wu, const void* wd, const int32_t* offsets,
-                       int R, int E, int d, int f, void* h, void* a, void* y, void* ws, cudaStream_t st);
+                       int R, int E, int d, int f, void* h, void* a, void* y, void* ws, cudaStream_t st,
+                       const uint8_t* xq_codes = nullptr, const uint8_t* xq_scales = nullptr);
+// dyq_codes/dyq_scales (optional): dy_perm's rows already quantised by the
+// combine backward.
 cudaError_t mx_mlp_bwd(const void* dy_perm, const void* x_perm, const void* h, const void* a, const void* wg,
                        const void* wu, const void* wd, const int32_t* offsets, int R, int E, int d, int f,
-                       void* dx_perm, void* dwg, void* dwu, void* dwd, void* ws, cudaStream_t st);
+                       void* dx_perm, void* dwg, void* dwu, void* dwd, void* ws, cudaStream_t st,
+                       const uint8_t* dyq_codes = nullptr, const uint8_t* dyq_scales = nullptr);
 
 }  // namespace moe

@@ -144,7 +144,65 @@ quant_cols_kernel(const __nv_bfloat16* __restrict__ src, int rows, int C, const 
   }
 }
 
+// Quantise before dispatch: each token's row of x is quantised once along d
+// (blocks of 32; lane L owns elements 8L + 256i, so a block is 4 lanes) and
+// the codes and scale bytes are written to the token's k dispatched rows
+// (with x_perm given, the bf16 row too). The bytes equal
+// mxfp8_quantize(x_perm, rows) of the bf16 dispatch.
+constexpr int kPermWarps = 8;
+__global__ void __launch_bounds__(kPermWarps * 32)
+permute_quant_kernel(const __nv_bfloat16* __restrict__ x, int T, int d, int k, const int32_t* __restrict__ dest_row,
+                     uint8_t* __restrict__ q, uint8_t* __restrict__ sc, __nv_bfloat16* __restrict__ x_perm) {
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x * kPermWarps + (threadIdx.x >> 5);
+  if (t >= T) return;
+  const int dest = lane < k ? dest_row[(size_t)t * k + lane] : 0;
+  for (int cb = 0; cb < d; cb += 256) {  // warp-uniform: every lane reaches the shuffles
+    const int c = cb + lane * 8;
+    const bool act = c < d;  // d % 32 == 0: a 4-lane block is all in or all out
+    float v[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    uint4 raw = make_uint4(0, 0, 0, 0);
+    if (act) {
+      raw = *reinterpret_cast<const uint4*>(x + (size_t)t * d + c);
+      const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        v[2 * i] = __uint_as_float(w[i] << 16);
+        v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+      }
+    }
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    const int sx = e8m0_exponent(amax);
+    const float m = pow2_neg(sx);
+    uint32_t lo = 0, hi = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      lo |= e4m3(v[i] * m) << (8 * i);
+      hi |= e4m3(v[4 + i] * m) << (8 * i);
+    }
+    for (int j = 0; j < k; ++j) {
+      const int r = __shfl_sync(0xffffffffu, dest, j);
+      if (!act) continue;
+      *reinterpret_cast<uint2*>(q + (size_t)r * d + c) = make_uint2(lo, hi);
+      if (x_perm) *reinterpret_cast<uint4*>(x_perm + (size_t)r * d + c) = raw;
+      if ((lane & 3) == 0) sc[(size_t)r * (d / 32) + c / 32] = static_cast<uint8_t>(sx + 127);
+    }
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_permute_quant(const void* x, int T, int d, int k, const int32_t* dest_row, uint8_t* q,
+                                 uint8_t* sc, void* x_perm, cudaStream_t st) {
+  if (T == 0) return cudaSuccess;
+  MOE_COUNTED permute_quant_kernel<<<(T + kPermWarps - 1) / kPermWarps, kPermWarps * 32, 0, st>>>(
+      static_cast<const __nv_bfloat16*>(x), T, d, k, dest_row, q, sc, static_cast<__nv_bfloat16*>(x_perm));
+  return cudaGetLastError();
+}
 
 cudaError_t launch_mxfp8_quant_rows(const void* src, long rows, long K, uint8_t* q, uint8_t* sc,
                                     cudaStream_t st) {

@@ -6,6 +6,7 @@
 // buffers; the combine is the gate-weighted return to token order.)
 #include "common.cuh"
 #include "kernels.h"
+#include "mxfp8_common.cuh"
 
 namespace moe {
 
@@ -70,11 +71,15 @@ combine_fwd_kernel(const T* __restrict__ y_perm, const float* __restrict__ gates
 
 // dy_perm[dest] = g * dy[t];  dgates[t][j] = <dy[t], y_perm[dest]>
 // KMAX: the largest k the instance handles (arrays of per-slot state).
-template <typename T, int KMAX>
+// QUANT (bf16 only): also write dy_perm's MXFP8 row quantisation (q [T*k][d]
+// E4M3, qsc [T*k][d/32] E8M0) of the bf16-rounded g * dy values -- the bytes
+// mxfp8_quantize(dy_perm, rows) gives -- and dy_perm itself only when given.
+template <typename T, int KMAX, bool QUANT = false>
 __global__ void __launch_bounds__(kRowWarps * 32)
 combine_bwd_kernel(const T* __restrict__ dy, const T* __restrict__ y_perm,
                    const float* __restrict__ gates, const int32_t* __restrict__ dest_row, int Tn,
-                   int d, int k, T* __restrict__ dy_perm, float* __restrict__ dgates) {
+                   int d, int k, T* __restrict__ dy_perm, float* __restrict__ dgates, uint8_t* __restrict__ q = nullptr,
+                   uint8_t* __restrict__ qsc = nullptr) {
   using V = Vec16<T>;
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * kRowWarps + (threadIdx.x >> 5);
@@ -89,20 +94,53 @@ combine_bwd_kernel(const T* __restrict__ dy, const T* __restrict__ y_perm,
     g[j] = __shfl_sync(0xffffffffu, my_g, j);
     dot[j] = 0.0f;
   }
-  for (int c = lane * V::N; c < d; c += 32 * V::N) {
+  // warp-uniform loop (the quantising variant shuffles inside it); lanes past d
+  // contribute zeros and store nothing
+  for (int cb = 0; cb < d; cb += 32 * V::N) {
+    const int c = cb + lane * V::N;
+    const bool act = c < d;
     float u[V::N];
-    V::load(dy + (size_t)t * d + c, u);
+#pragma unroll
+    for (int i = 0; i < V::N; ++i) u[i] = 0.0f;
+    if (act) V::load(dy + (size_t)t * d + c, u);
 #pragma unroll
     for (int j = 0; j < KMAX; ++j) {
       if (j < k) {
         float v[V::N], w[V::N];
-        V::load(y_perm + (size_t)dest[j] * d + c, v);
+#pragma unroll
+        for (int i = 0; i < V::N; ++i) v[i] = 0.0f;
+        if (act) V::load(y_perm + (size_t)dest[j] * d + c, v);
 #pragma unroll
         for (int i = 0; i < V::N; ++i) {
           dot[j] = fmaf(u[i], v[i], dot[j]);
           w[i] = g[j] * u[i];
         }
-        V::store(dy_perm + (size_t)dest[j] * d + c, w);
+        if constexpr (QUANT) {
+          static_assert(V::N == 8, "a 32-element block is 4 lanes of 8 bf16");
+          float amax = 0.0f;
+#pragma unroll
+          for (int i = 0; i < V::N; ++i) {
+            w[i] = __bfloat162float(__float2bfloat16_rn(w[i]));
+            amax = fmaxf(amax, fabsf(w[i]));
+          }
+          amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+          amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+          const int sx = mx_e8m0_exponent(amax);
+          const float m = mx_pow2_neg(sx);
+          uint32_t lo = 0, hi = 0;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            lo |= mx_e4m3(w[i] * m) << (8 * i);
+            hi |= mx_e4m3(w[4 + i] * m) << (8 * i);
+          }
+          if (act) {
+            *reinterpret_cast<uint2*>(q + (size_t)dest[j] * d + c) = make_uint2(lo, hi);
+            if ((lane & 3) == 0) qsc[(size_t)dest[j] * (d / 32) + c / 32] = static_cast<uint8_t>(sx + 127);
+            if (dy_perm) V::store(dy_perm + (size_t)dest[j] * d + c, w);
+          }
+        } else if (act) {
+          V::store(dy_perm + (size_t)dest[j] * d + c, w);
+        }
       }
     }
   }
@@ -297,6 +335,22 @@ cudaError_t launch_combine_bwd(const void* dy, const void* y_perm, const float* 
     MOE_COUNTED combine_bwd_kernel<T, 8><<<row_grid<T>(Tn), kRowWarps * 32, 0, st>>>(
         static_cast<const T*>(dy), static_cast<const T*>(y_perm), gates, dest_row, Tn, d, k,
         static_cast<T*>(dy_perm), dgates);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine_bwd_quant(const void* dy, const void* y_perm, const float* gates,
+                                     const int32_t* dest_row, int Tn, int d, int k, uint8_t* q, uint8_t* qsc,
+                                     void* dy_perm, float* dgates, cudaStream_t st) {
+  using B = __nv_bfloat16;
+  if (Tn == 0) return cudaSuccess;
+  if (k <= 4)
+    MOE_COUNTED combine_bwd_kernel<B, 4, true><<<row_grid<B>(Tn), kRowWarps * 32, 0, st>>>(
+        static_cast<const B*>(dy), static_cast<const B*>(y_perm), gates, dest_row, Tn, d, k, static_cast<B*>(dy_perm),
+        dgates, q, qsc);
+  else
+    MOE_COUNTED combine_bwd_kernel<B, 8, true><<<row_grid<B>(Tn), kRowWarps * 32, 0, st>>>(
+        static_cast<const B*>(dy), static_cast<const B*>(y_perm), gates, dest_row, Tn, d, k, static_cast<B*>(dy_perm),
+        dgates, q, qsc);
   return cudaGetLastError();
 }
 

@@ -8,6 +8,11 @@ library's kernels. Order of calls:
   backward: moe_combine_bwd -> moe_route_bwd -> moe_grouped_mlp_bwd
             -> moe_permute_bwd (adds the router's share of dx)
 
+On the MXFP8 path the dispatched activations are row-quantised where they are
+produced (mx_pre, default on): moe_permute_mxfp8 writes x_perm's E4M3 rows
+next to the bf16 dispatch and moe_combine_bwd_mxfp8 dy_perm's, and
+moe_mxfp8_mlp_fwd / moe_mxfp8_mlp_bwd skip their own row-quantisation passes.
+
 With fused=True (bf16 only) moe_dispatch_mlp_fwd / moe_dispatch_mlp_bwd
 replace moe_permute and the two grouped-MLP calls: GEMM1 and its weight
 gradient gather x's rows with TMA row gathers and x_perm is not written. The
@@ -99,6 +104,10 @@ class Buffers:
         self.dw_down = z(E, f, d)
         self.workspace = torch.empty(max(1, N.moe_workspace_size(T, d, E, k, f, dtype)),
                                      dtype=torch.uint8, device=device)
+        if dtype == N.MOE_MXFP8:  # rows quantised before the dispatch / by the combine backward
+            u8 = torch.uint8
+            self.x_q, self.x_sc = z(R, d, dt=u8), z(R, d // 32, dt=u8)
+            self.dy_q, self.dy_sc = z(R, d, dt=u8), z(R, d // 32, dt=u8)
 
 
 def route_stats(b: Buffers, stream=None):
@@ -116,12 +125,16 @@ def fused_default(dtype: int) -> bool:
     return False
 
 
-def forward(p: Params, b: Buffers, logits_in: bool = False, stream=None, fused=None):
+def forward(p: Params, b: Buffers, logits_in: bool = False, stream=None, fused=None, mx_pre=True):
     T, d, E, k, f, dt = b.T, b.d, b.E, b.k, b.f, b.dtype
     N.moe_route(p.x, p.w_router, p.bias, dt, T, d, E, k, b.logits,
                 N.MOE_ROUTE_LOGITS_IN if logits_in else 0, b.topk_idx, b.gates, b.counts, b.offsets,
                 b.dest_row, b.src_row, b.workspace, stream)
-    if fused_default(dt) if fused is None else fused:
+    if dt == N.MOE_MXFP8 and mx_pre:
+        N.moe_permute_mxfp8(p.x, T, d, k, b.dest_row, b.x_q, b.x_sc, b.x_perm, stream)
+        N.moe_mxfp8_mlp_fwd(b.x_q, b.x_sc, p.w_gate, p.w_up, p.w_down, b.offsets, b.R, E, d, f, b.h_save,
+                            b.a_save, b.y_perm, b.workspace, stream)
+    elif fused_default(dt) if fused is None else fused:
         N.moe_dispatch_mlp_fwd(p.x, b.src_row, T, k, p.w_gate, p.w_up, p.w_down, dt, b.offsets, E, d, f,
                                b.h_save, b.a_save, b.y_perm, stream)
     else:
@@ -131,12 +144,20 @@ def forward(p: Params, b: Buffers, logits_in: bool = False, stream=None, fused=N
     N.moe_combine_fwd(b.y_perm, b.gates, b.dest_row, dt, T, d, k, b.y, stream)
 
 
-def backward(p: Params, b: Buffers, stream=None, fused=None):
+def backward(p: Params, b: Buffers, stream=None, fused=None, mx_pre=True):
     T, d, E, k, f, dt = b.T, b.d, b.E, b.k, b.f, b.dtype
-    N.moe_combine_bwd(p.dy, b.y_perm, b.gates, b.dest_row, dt, T, d, k, b.dy_perm, b.dgates, stream)
+    mx = dt == N.MOE_MXFP8 and mx_pre
+    if mx:
+        N.moe_combine_bwd_mxfp8(p.dy, b.y_perm, b.gates, b.dest_row, T, d, k, b.dy_q, b.dy_sc, b.dy_perm, b.dgates,
+                                stream)
+    else:
+        N.moe_combine_bwd(p.dy, b.y_perm, b.gates, b.dest_row, dt, T, d, k, b.dy_perm, b.dgates, stream)
     N.moe_route_bwd(b.dgates, b.gates, b.topk_idx, b.offsets, b.src_row, p.x, dt, T, d, E, k,
                     b.dlogits, b.dw_router, stream)
-    if fused_default(dt) if fused is None else fused:
+    if mx:
+        N.moe_mxfp8_mlp_bwd(b.dy_q, b.dy_sc, b.dy_perm, b.x_perm, b.h_save, b.a_save, p.w_gate, p.w_up, p.w_down,
+                            b.offsets, b.R, E, d, f, b.dx_perm, b.dw_gate, b.dw_up, b.dw_down, b.workspace, stream)
+    elif fused_default(dt) if fused is None else fused:
         N.moe_dispatch_mlp_bwd(b.dy_perm, p.x, b.src_row, T, k, b.h_save, b.a_save, p.w_gate, p.w_up, p.w_down,
                                dt, b.offsets, E, d, f, b.dx_perm, b.dw_gate, b.dw_up, b.dw_down, b.workspace,
                                stream)

@@ -101,3 +101,16 @@ def test_route_stats_arguments_rejected_before_launch(lib):
     assert L.moe_route_stats(FAKE, FAKE, 8, 2048, 2, FAKE, FAKE, FAKE, 1 << 20, None) == 2   # E > 1024
     assert L.moe_route_stats(FAKE, FAKE, 4096, 128, 4, FAKE, FAKE, FAKE, 16, None) == 4      # workspace
     assert L.moe_route_stats(FAKE, None, 8, 4, 2, FAKE, FAKE, FAKE, 1 << 20, None) == 1      # counts
+
+
+def test_mxfp8_dispatch_arguments_rejected_before_launch(lib):
+    L = lib
+    assert L.moe_permute_mxfp8(FAKE, 8, 96, 2, FAKE, FAKE, FAKE, None, None) == 2            # d % 64
+    assert L.moe_permute_mxfp8(FAKE, 8, 64, 2, FAKE, None, FAKE, None, None) == 1            # codes missing
+    assert L.moe_permute_mxfp8(FAKE, 8, 64, 2, FAKE, FAKE, FAKE, FAKE + 4, None) == 3        # x_perm aligned
+    assert L.moe_combine_bwd_mxfp8(FAKE, FAKE, FAKE, FAKE, 8, 64, 9, FAKE, FAKE, None, FAKE, None) == 2  # k > 8
+    # d not a multiple of 128 for the block-scaled GEMMs
+    assert L.moe_mxfp8_mlp_fwd(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 16, 4, 192, 128, FAKE, FAKE, FAKE, FAKE,
+                               1 << 30, None) == 2
+    assert L.moe_mxfp8_mlp_bwd(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 16, 4, 128, 128,
+                               FAKE, FAKE, FAKE, FAKE, FAKE, 16, None) == 4              # workspace

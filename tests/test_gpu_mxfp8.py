@@ -120,3 +120,73 @@ def test_mxfp8_layer_parity(s):
     print(f"{s.name}: vs MXFP8 oracle {errs}; y vs unquantised {_err(np_(b.y), plain['y']):.4f}, "
           f"dx vs unquantised {_err(np_(b.dx), plain['dx']):.4f}")
     assert not bad, f"{s.name}: {bad} (all: {errs})"
+
+
+# ------------------------------------- quantised where produced (before the dispatch)
+def _dest_rows(T, k, seed):
+    rng = np.random.default_rng(seed)
+    return rng.permutation(T * k).astype(np.int32).reshape(T, k)
+
+
+@pytest.mark.parametrize("T,d,k", [(777, 320, 3), (64, 2048, 8), (1, 64, 1)])
+def test_permute_mxfp8_bytes(T, d, k):
+    """The fused dispatch + row quantisation writes, at row dest_row[t][j], the
+    oracle's row quantisation of x[t] (d=320: a partial last 256-column pass)."""
+    v = _values(T, d, T + d)
+    dest = _dest_rows(T, k, 5)
+    q = torch.zeros((T * k, d), dtype=torch.uint8, device="cuda")
+    s = torch.zeros((T * k, d // 32), dtype=torch.uint8, device="cuda")
+    xp = torch.zeros((T * k, d), dtype=torch.bfloat16, device="cuda")
+    N.moe_permute_mxfp8(_dev(v), T, d, k, torch.from_numpy(dest).cuda(), q, s, xp)
+    torch.cuda.synchronize()
+    rq, rs = oracle.mxfp8_quantize_rows(v)
+    inv = np.argsort(dest.ravel()) // k  # token of each dispatched row
+    np.testing.assert_array_equal(q.cpu().numpy(), rq[inv])
+    np.testing.assert_array_equal(s.cpu().numpy(), rs[inv])
+    np.testing.assert_array_equal(xp.float().cpu().numpy(), v[inv])  # the bf16 dispatch, exact
+
+
+@pytest.mark.parametrize("T,d,k", [(500, 320, 4), (33, 1024, 8)])
+def test_combine_bwd_mxfp8_bytes(T, d, k):
+    """The quantising combine backward writes the oracle's row quantisation of
+    the bf16 dy_perm that moe_combine_bwd stores, and the same dgates bits."""
+    rng = np.random.default_rng(T)
+    dy = _dev(synth.round_bf16(rng.standard_normal((T, d)).astype(np.float32)))
+    y_perm = _dev(synth.round_bf16(rng.standard_normal((T * k, d)).astype(np.float32)))
+    g = torch.from_numpy(rng.random((T, k)).astype(np.float32)).cuda()
+    dest = torch.from_numpy(_dest_rows(T, k, 9)).cuda()
+    dy_perm = torch.empty((T * k, d), dtype=torch.bfloat16, device="cuda")
+    dg0 = torch.empty((T, k), dtype=torch.float32, device="cuda")
+    N.moe_combine_bwd(dy, y_perm, g, dest, N.MOE_BF16, T, d, k, dy_perm, dg0)
+    q = torch.zeros((T * k, d), dtype=torch.uint8, device="cuda")
+    s = torch.zeros((T * k, d // 32), dtype=torch.uint8, device="cuda")
+    dg1 = torch.empty_like(dg0)
+    dy_perm1 = torch.zeros_like(dy_perm)
+    N.moe_combine_bwd_mxfp8(dy, y_perm, g, dest, T, d, k, q, s, dy_perm1, dg1)
+    torch.cuda.synchronize()
+    assert torch.equal(dy_perm1, dy_perm)
+    rq, rs = oracle.mxfp8_quantize_rows(dy_perm.float().cpu().numpy())
+    np.testing.assert_array_equal(q.cpu().numpy(), rq)
+    np.testing.assert_array_equal(s.cpu().numpy(), rs)
+    assert torch.equal(dg0, dg1)
+
+
+@pytest.mark.parametrize("s", MX_SHAPES, ids=lambda s: s.name)
+def test_mxfp8_quantise_before_dispatch_matches(s):
+    """Quantising x and dy_perm where they are produced (and gathering the
+    wgrad operands through src_row) gives bit-identical layer outputs."""
+    inp = synth.Inputs(s, seed=3)
+    p = L.params_from_inputs(inp, N.MOE_MXFP8)
+    outs = []
+    for pre in (False, True):
+        b = L.Buffers(s.T, s.d, s.E, s.k, s.f, N.MOE_MXFP8)
+        L.forward(p, b, mx_pre=pre)
+        L.backward(p, b, mx_pre=pre)
+        torch.cuda.synchronize()
+        assert N.moe_get_device_error() == 0
+        outs.append([t.clone() for t in (b.h_save, b.a_save, b.y_perm, b.y, b.dgates, b.dlogits, b.dx_perm, b.dx,
+                                         b.dw_gate, b.dw_up, b.dw_down, b.dw_router)])
+    names = ("h_save", "a_save", "y_perm", "y", "dgates", "dlogits", "dx_perm", "dx", "dw_gate", "dw_up", "dw_down",
+             "dw_router")
+    for n_, a, c in zip(names, *outs):
+        assert torch.equal(a, c), n_

@@ -258,7 +258,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       ptx::tc_fence_after();
       const uint32_t tbase = tmem + static_cast<uint32_t>(buf * BN) + (static_cast<uint32_t>(q * 32) << 16);
       if constexpr (KIND == ROUTER)
-        epilogue_tile<KIND>(p, tl, tbase, q * 32 + lane, half * NC / 2, (half + 1) * NC / 2, false);
+        epilogue_router(p, tl, tbase, q * 32 + lane, half * NC / 2, (half + 1) * NC / 2);
       else
         epilogue_tile_staged<KIND>(p, tl, tbase, q, lane, half * NC / 2, (half + 1) * NC / 2, stg);
       ptx::tc_fence_before();

@@ -149,34 +149,6 @@ __device__ __forceinline__ void build_tile_table(const Params& p, int* offs, int
   __syncthreads();
 }
 
-__device__ __forceinline__ void store_bf16x32(__nv_bfloat16* dst, const float* v) {
-  uint4* d = reinterpret_cast<uint4*>(dst);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    uint32_t w[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      __nv_bfloat162 h = __floats2bfloat162_rn(v[8 * i + 2 * j], v[8 * i + 2 * j + 1]);
-      w[j] = *reinterpret_cast<uint32_t*>(&h);
-    }
-    d[i] = make_uint4(w[0], w[1], w[2], w[3]);
-  }
-}
-
-__device__ __forceinline__ void load_bf16x32(const __nv_bfloat16* src, float* v) {
-  const uint4* s = reinterpret_cast<const uint4*>(src);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const uint4 q = s[i];
-    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      v[8 * i + 2 * j] = __uint_as_float(w[j] << 16);
-      v[8 * i + 2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
-    }
-  }
-}
-
 // Row-segment traffic through a per-warp staging buffer. An epilogue thread
 // owns one output row (its TMEM lane), so a direct store instruction of a
 // warp touches 32 rows with 16 bytes each. Staged in shared memory (32 rows x
@@ -291,22 +263,6 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
-// Row quantisation of a 32-column chunk of a bf16 output (values rounded to
-// bf16 first: the GEMMs that read it see the stored values). Codes go to
-// qout[row][col..col+32), the scale to qsc[row][col/32] of a [rows][ld] matrix.
-__device__ __forceinline__ void quant_chunk_bf16(const Params& p, long row, int ld, int col, const float* v) {
-  float r[32];
-#pragma unroll
-  for (int i = 0; i < 32; ++i) r[i] = __bfloat162float(__float2bfloat16_rn(v[i]));
-  mx_quant_block32(r, p.qout + (size_t)row * ld + col, p.qsc + (size_t)row * (ld / 32) + col / 32);
-}
-
-// Epilogue of one tile for the rows of one TMEM lane quadrant: accumulator
-// chunks [c_beg, c_end) of 32 columns (FPROP1: gate chunk c with up chunk
-// c + 4). `zero` writes zeros without reading TMEM (wgrad of an empty expert).
-// TBN: columns of the tile (256, or 128 for the narrower MXFP8 tiles).
-// QUANT: also write the MXFP8 row quantisation of A (FPROP1) or dh (DGRAD2)
-// when p.qout is set.
 // Staged form of the row-tile epilogue (see warp_store_rows): every lane of
 // the warp takes part; stg is the warp's STG_BYTES buffer. Row-tile kinds
 // FPROP1, FPROP2, DGRAD1, DGRAD2 without quantisation.
@@ -404,129 +360,36 @@ __device__ __forceinline__ void epilogue_tile_staged(const Params& p, const Tile
   }
 }
 
-template <int KIND, bool QUANT = false, int TBN = BN>
-__device__ __forceinline__ void epilogue_tile(const Params& p, const Tile& tl, uint32_t tbase, int row_in_tile,
-                                              int c_beg, int c_end, bool zero) {
-  if (Traits<KIND>::kragged) {
-    const int m = tl.m0 + row_in_tile;
-    const int n0 = tl.n_idx * TBN;
-    const bool row_ok = m < p.M;
-    for (int c = c_beg; c < c_end; ++c) {
-      float v[32];
-      if (!zero) {
-        uint32_t r[32];
-        ptx::tmem_ld32(tbase + c * 32, r);
-        ptx::tmem_wait_ld();
-#pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-      } else {
-#pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] = 0.0f;
-      }
-      const int n = n0 + c * 32;
-      if (!row_ok || n >= p.N) continue;
-      __nv_bfloat16* dst;
-      if (KIND == WGRAD2) dst = static_cast<__nv_bfloat16*>(p.out0) + ((size_t)tl.e * p.M + m) * p.N + n;
-      else dst = n < p.f ? static_cast<__nv_bfloat16*>(p.out0) + ((size_t)tl.e * p.d + m) * p.f + n
-                         : static_cast<__nv_bfloat16*>(p.out1) + ((size_t)tl.e * p.d + m) * p.f + (n - p.f);
-      store_bf16x32(dst, v);
-    }
-    return;
-  }
+// Epilogue of a router-logits tile for the rows of one TMEM lane quadrant
+// (lane = row): fp32 logits plus the optional bias, accumulator chunks
+// [c_beg, c_end) of 32 columns.
+template <int TBN = BN>
+__device__ __forceinline__ void epilogue_router(const Params& p, const Tile& tl, uint32_t tbase, int row_in_tile,
+                                                int c_beg, int c_end) {
   const int row = tl.m0 + row_in_tile;
   const bool row_ok = row < tl.row_end;
-  if (KIND == FPROP1) {
-    const int n0 = tl.n_idx * 128;
-    for (int c = c_beg; c < c_end; ++c) {
-      uint32_t rg[32], ru[32];
-      ptx::tmem_ld32(tbase + c * 32, rg);
-      ptx::tmem_ld32(tbase + 128 + c * 32, ru);
-      ptx::tmem_wait_ld();
-      const int n = n0 + c * 32;
-      if (!row_ok || n >= p.f) continue;
-      float hg[32], hu[32], av[32];
+  const int n0 = tl.n_idx * TBN;
+  float* out = static_cast<float*>(p.out0) + (size_t)row * p.N;
+  for (int c = c_beg; c < c_end; ++c) {
+    uint32_t r[32];
+    ptx::tmem_ld32(tbase + c * 32, r);
+    ptx::tmem_wait_ld();
+    const int n = n0 + c * 32;
+    if (!row_ok || n >= p.N) continue;
+    if (n + 32 <= p.N && (p.N & 3) == 0) {
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        hg[i] = __uint_as_float(rg[i]);
-        hu[i] = __uint_as_float(ru[i]);
-        av[i] = silu_f(hg[i]) * hu[i];
+      for (int i = 0; i < 32; i += 4) {
+        float4 o;
+        o.x = __uint_as_float(r[i]) + (p.bias ? p.bias[n + i] : 0.0f);
+        o.y = __uint_as_float(r[i + 1]) + (p.bias ? p.bias[n + i + 1] : 0.0f);
+        o.z = __uint_as_float(r[i + 2]) + (p.bias ? p.bias[n + i + 2] : 0.0f);
+        o.w = __uint_as_float(r[i + 3]) + (p.bias ? p.bias[n + i + 3] : 0.0f);
+        *reinterpret_cast<float4*>(out + n + i) = o;
       }
-      __nv_bfloat16* h = static_cast<__nv_bfloat16*>(p.out0) + (size_t)row * 2 * p.f;
-      store_bf16x32(h + n, hg);
-      store_bf16x32(h + p.f + n, hu);
-      store_bf16x32(static_cast<__nv_bfloat16*>(p.out1) + (size_t)row * p.f + n, av);
-      if (QUANT && p.qout) quant_chunk_bf16(p, row, p.f, n, av);
-    }
-  } else if (KIND == DGRAD2) {
-    // dh_g = da * h_u * silu'(h_g), dh_u = da * silu(h_g); h is loaded before
-    // the accumulator so the global latency overlaps the TMEM read
-    const int n0 = tl.n_idx * TBN;
-    const __nv_bfloat16* h = static_cast<const __nv_bfloat16*>(p.aux) + (size_t)row * 2 * p.f;
-    __nv_bfloat16* dh = static_cast<__nv_bfloat16*>(p.out0) + (size_t)row * 2 * p.f;
-    for (int c = c_beg; c < c_end; ++c) {
-      const int n = n0 + c * 32;
-      const bool ok = row_ok && n < p.N;
-      float hg[32], hu[32];
-      if (ok) {
-        load_bf16x32(h + n, hg);
-        load_bf16x32(h + p.f + n, hu);
-      }
-      uint32_t r[32];
-      ptx::tmem_ld32(tbase + c * 32, r);
-      ptx::tmem_wait_ld();
-      if (!ok) continue;
-      float dg[32], du[32];
+    } else {
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const float da = __uint_as_float(r[i]);
-        const float s = sigmoid_f(hg[i]);
-        dg[i] = da * hu[i] * s * (1.0f + hg[i] * (1.0f - s));
-        du[i] = da * hg[i] * s;
-      }
-      store_bf16x32(dh + n, dg);
-      store_bf16x32(dh + p.f + n, du);
-      if (QUANT && p.qout) {
-        quant_chunk_bf16(p, row, 2 * p.f, n, dg);
-        quant_chunk_bf16(p, row, 2 * p.f, p.f + n, du);
-      }
-    }
-  } else if (KIND == ROUTER) {
-    const int n0 = tl.n_idx * TBN;
-    float* out = static_cast<float*>(p.out0) + (size_t)row * p.N;
-    for (int c = c_beg; c < c_end; ++c) {
-      uint32_t r[32];
-      ptx::tmem_ld32(tbase + c * 32, r);
-      ptx::tmem_wait_ld();
-      const int n = n0 + c * 32;
-      if (!row_ok || n >= p.N) continue;
-      if (n + 32 <= p.N && (p.N & 3) == 0) {
-#pragma unroll
-        for (int i = 0; i < 32; i += 4) {
-          float4 o;
-          o.x = __uint_as_float(r[i]) + (p.bias ? p.bias[n + i] : 0.0f);
-          o.y = __uint_as_float(r[i + 1]) + (p.bias ? p.bias[n + i + 1] : 0.0f);
-          o.z = __uint_as_float(r[i + 2]) + (p.bias ? p.bias[n + i + 2] : 0.0f);
-          o.w = __uint_as_float(r[i + 3]) + (p.bias ? p.bias[n + i + 3] : 0.0f);
-          *reinterpret_cast<float4*>(out + n + i) = o;
-        }
-      } else {
-#pragma unroll
-        for (int i = 0; i < 32; ++i)
-          if (n + i < p.N) out[n + i] = __uint_as_float(r[i]) + (p.bias ? p.bias[n + i] : 0.0f);
-      }
-    }
-  } else {  // FPROP2, DGRAD1: plain bf16 store
-    const int n0 = tl.n_idx * TBN;
-    for (int c = c_beg; c < c_end; ++c) {
-      uint32_t r[32];
-      ptx::tmem_ld32(tbase + c * 32, r);
-      ptx::tmem_wait_ld();
-      const int n = n0 + c * 32;
-      if (!row_ok || n >= p.N) continue;
-      float v[32];
-#pragma unroll
-      for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-      store_bf16x32(static_cast<__nv_bfloat16*>(p.out0) + (size_t)row * p.N + n, v);
+      for (int i = 0; i < 32; ++i)
+        if (n + i < p.N) out[n + i] = __uint_as_float(r[i]) + (p.bias ? p.bias[n + i] : 0.0f);
     }
   }
 }

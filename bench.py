@@ -202,10 +202,11 @@ def run_ours(args, s, rank, world):
         N.moe_route(p.x, p.w_router, p.bias, dt, T, d, E, k, b.logits, 0, b.topk_idx, b.gates, b.counts,
                     b.offsets, b.dest_row, b.src_row, b.workspace)
         if mx:  # MXFP8: x quantised as it is dispatched
+            N.moe_mxfp8_prepare_weights(p.w_gate, p.w_up, p.w_down, E, d, f, b.wq)
             N.moe_permute_mxfp8(p.x, T, d, k, b.dest_row, b.x_q, b.x_sc, b.x_perm)
             ev[0].record(stream)
-            N.moe_mxfp8_mlp_fwd(b.x_q, b.x_sc, p.w_gate, p.w_up, p.w_down, b.offsets, b.R, E, d, f, b.h_save,
-                                b.a_save, b.y_perm, b.workspace)
+            N.moe_mxfp8_mlp_fwd(b.x_q, b.x_sc, b.wq, b.offsets, b.R, E, d, f, b.h_save, b.a_save, b.y_perm,
+                                b.workspace)
         elif fused:  # the dispatch runs inside GEMM1 (rows gathered from x)
             ev[0].record(stream)
             N.moe_dispatch_mlp_fwd(p.x, b.src_row, T, k, p.w_gate, p.w_up, p.w_down, dt, b.offsets, E, d, f,
@@ -226,9 +227,8 @@ def run_ours(args, s, rank, world):
                         b.dlogits, b.dw_router)
         ev[2].record(stream)
         if mx:
-            N.moe_mxfp8_mlp_bwd(b.dy_q, b.dy_sc, b.dy_perm, b.x_perm, b.h_save, b.a_save, p.w_gate, p.w_up,
-                                p.w_down, b.offsets, b.R, E, d, f, b.dx_perm, b.dw_gate, b.dw_up, b.dw_down,
-                                b.workspace)
+            N.moe_mxfp8_mlp_bwd(b.dy_q, b.dy_sc, b.dy_perm, b.x_perm, b.h_save, b.a_save, b.wq, b.offsets, b.R, E,
+                                d, f, b.dx_perm, b.dw_gate, b.dw_up, b.dw_down, b.workspace)
         elif fused:
             N.moe_dispatch_mlp_bwd(b.dy_perm, p.x, b.src_row, T, k, b.h_save, b.a_save, p.w_gate, p.w_up,
                                    p.w_down, dt, b.offsets, E, d, f, b.dx_perm, b.dw_gate, b.dw_up, b.dw_down,

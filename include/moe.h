@@ -211,27 +211,37 @@ moe_status moe_dispatch_mlp_bwd(const void* dy_perm, const void* x, const int32_
    values gates[t][j] * dy[t]; dy_perm (optional, may be NULL) receives the
    bf16 values; dgates as moe_combine_bwd.
 
+   moe_mxfp8_prepare_weights: quantises w_gate, w_up and w_down once per
+   weight update into both layouts the expert GEMMs read -- along the weight's
+   rows in blocks of 32 (GEMM1 and GEMM2 forward: K = d, f) and along its
+   columns in blocks of 32 (the dgrads: K = f, d) -- into wq
+   (moe_mxfp8_weights_size(E, d, f) bytes, caller-owned, device). Call it
+   after every weight update; moe_mxfp8_mlp_fwd/bwd read the weights only
+   from wq. d and f multiples of 128.
+
    moe_mxfp8_mlp_fwd: moe_grouped_mlp_fwd(MOE_MXFP8) with GEMM1 reading
-   x_codes/x_scales (no separate quantisation pass). Same outputs, same
-   workspace.
+   x_codes/x_scales and the weights read from wq (no quantisation pass of its
+   own). Same outputs, same workspace.
 
    moe_mxfp8_mlp_bwd: moe_grouped_mlp_bwd(MOE_MXFP8) with the GEMM2 dgrad
-   reading dy_codes/dy_scales; dy_perm and x_perm (bf16) feed the
-   expert-segment quantisations of the weight gradients. Same outputs, same
-   workspace. d and f multiples of 128. */
+   reading dy_codes/dy_scales and the weights read from wq; dy_perm and
+   x_perm (bf16) feed the expert-segment quantisations of the weight
+   gradients. Same outputs, same workspace. d and f multiples of 128. */
+size_t moe_mxfp8_weights_size(int E, int d, int f);
+moe_status moe_mxfp8_prepare_weights(const void* w_gate, const void* w_up, const void* w_down, int E, int d, int f,
+                                     void* wq, size_t wq_bytes, void* stream);
 moe_status moe_permute_mxfp8(const void* x, int T, int d, int k, const int32_t* dest_row, uint8_t* x_codes,
                              uint8_t* x_scales, void* x_perm, void* stream);
 moe_status moe_combine_bwd_mxfp8(const void* dy, const void* y_perm, const float* gates, const int32_t* dest_row,
                                  int T, int d, int k, uint8_t* dy_codes, uint8_t* dy_scales, void* dy_perm,
                                  float* dgates, void* stream);
-moe_status moe_mxfp8_mlp_fwd(const uint8_t* x_codes, const uint8_t* x_scales, const void* w_gate, const void* w_up,
-                             const void* w_down, const int32_t* offsets, int R, int E, int d, int f, void* h_save,
-                             void* a_save, void* y_perm, void* workspace, size_t workspace_bytes, void* stream);
-moe_status moe_mxfp8_mlp_bwd(const uint8_t* dy_codes, const uint8_t* dy_scales, const void* dy_perm,
-                             const void* x_perm, const void* h_save, const void* a_save, const void* w_gate,
-                             const void* w_up, const void* w_down, const int32_t* offsets, int R, int E, int d, int f,
-                             void* dx_perm, void* dw_gate, void* dw_up, void* dw_down, void* workspace,
+moe_status moe_mxfp8_mlp_fwd(const uint8_t* x_codes, const uint8_t* x_scales, const void* wq, const int32_t* offsets,
+                             int R, int E, int d, int f, void* h_save, void* a_save, void* y_perm, void* workspace,
                              size_t workspace_bytes, void* stream);
+moe_status moe_mxfp8_mlp_bwd(const uint8_t* dy_codes, const uint8_t* dy_scales, const void* dy_perm,
+                             const void* x_perm, const void* h_save, const void* a_save, const void* wq,
+                             const int32_t* offsets, int R, int E, int d, int f, void* dx_perm, void* dw_gate,
+                             void* dw_up, void* dw_down, void* workspace, size_t workspace_bytes, void* stream);
 
 /* MXFP8 block quantisation ("Scaling and optimizing MoE training": MXFP8):
    E4M3 codes with one E8M0 scale per 32 consecutive elements.

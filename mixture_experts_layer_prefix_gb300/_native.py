@@ -26,7 +26,8 @@ EXPORTS = ("moe_workspace_size", "moe_route", "moe_permute", "moe_permute_bwd", 
            "moe_combine_bwd", "moe_route_bwd", "moe_grouped_mlp_fwd", "moe_grouped_mlp_bwd",
            "mxfp8_quantize", "moe_get_device_error", "moe_sm_count", "moe_launch_count", "moe_route_noalloc",
            "moe_dispatch_mlp_fwd", "moe_dispatch_mlp_bwd", "moe_route_stats", "moe_permute_mxfp8",
-           "moe_combine_bwd_mxfp8", "moe_mxfp8_mlp_fwd", "moe_mxfp8_mlp_bwd")
+           "moe_combine_bwd_mxfp8", "moe_mxfp8_mlp_fwd", "moe_mxfp8_mlp_bwd", "moe_mxfp8_weights_size",
+           "moe_mxfp8_prepare_weights")
 
 
 class MoEError(RuntimeError):
@@ -66,8 +67,10 @@ def load(path: str = LIB_PATH):
         "moe_route_stats": ([P, P, I, I, I, P, P, P, Z, P], I),
         "moe_permute_mxfp8": ([P, I, I, I, P, P, P, P, P], I),
         "moe_combine_bwd_mxfp8": ([P, P, P, P, I, I, I, P, P, P, P, P], I),
-        "moe_mxfp8_mlp_fwd": ([P, P, P, P, P, P, I, I, I, I, P, P, P, P, Z, P], I),
-        "moe_mxfp8_mlp_bwd": ([P, P, P, P, P, P, P, P, P, P, I, I, I, I, P, P, P, P, P, Z, P], I),
+        "moe_mxfp8_mlp_fwd": ([P, P, P, P, I, I, I, I, P, P, P, P, Z, P], I),
+        "moe_mxfp8_mlp_bwd": ([P, P, P, P, P, P, P, P, I, I, I, I, P, P, P, P, P, Z, P], I),
+        "moe_mxfp8_weights_size": ([I, I, I], Z),
+        "moe_mxfp8_prepare_weights": ([P, P, P, I, I, I, P, Z, P], I),
         "moe_dispatch_mlp_bwd": ([P, P, P, I, I, P, P, P, P, P, I, P, I, I, I, P, P, P, P, P, Z, P], I),
     }
     for name, (args, res) in sig.items():
@@ -211,16 +214,23 @@ def moe_combine_bwd_mxfp8(dy, y_perm, gates, dest_row, T, d, k, dy_codes, dy_sca
         _s(stream)))
 
 
-def moe_mxfp8_mlp_fwd(x_codes, x_scales, w_gate, w_up, w_down, offsets, R, E, d, f, h_save, a_save, y_perm,
-                      workspace, stream=None):
+def moe_mxfp8_weights_size(E, d, f):
+    return load().moe_mxfp8_weights_size(E, d, f)
+
+
+def moe_mxfp8_prepare_weights(w_gate, w_up, w_down, E, d, f, wq, stream=None):
+    _chk("moe_mxfp8_prepare_weights", load().moe_mxfp8_prepare_weights(
+        _p(w_gate), _p(w_up), _p(w_down), E, d, f, _p(wq), _nbytes(wq), _s(stream)))
+
+
+def moe_mxfp8_mlp_fwd(x_codes, x_scales, wq, offsets, R, E, d, f, h_save, a_save, y_perm, workspace, stream=None):
     _chk("moe_mxfp8_mlp_fwd", load().moe_mxfp8_mlp_fwd(
-        _p(x_codes), _p(x_scales), _p(w_gate), _p(w_up), _p(w_down), _p(offsets), R, E, d, f, _p(h_save),
-        _p(a_save), _p(y_perm), _p(workspace), _nbytes(workspace), _s(stream)))
+        _p(x_codes), _p(x_scales), _p(wq), _p(offsets), R, E, d, f, _p(h_save), _p(a_save), _p(y_perm),
+        _p(workspace), _nbytes(workspace), _s(stream)))
 
 
-def moe_mxfp8_mlp_bwd(dy_codes, dy_scales, dy_perm, x_perm, h_save, a_save, w_gate, w_up, w_down, offsets, R, E, d,
-                      f, dx_perm, dw_gate, dw_up, dw_down, workspace, stream=None):
+def moe_mxfp8_mlp_bwd(dy_codes, dy_scales, dy_perm, x_perm, h_save, a_save, wq, offsets, R, E, d, f, dx_perm,
+                      dw_gate, dw_up, dw_down, workspace, stream=None):
     _chk("moe_mxfp8_mlp_bwd", load().moe_mxfp8_mlp_bwd(
-        _p(dy_codes), _p(dy_scales), _p(dy_perm), _p(x_perm), _p(h_save), _p(a_save), _p(w_gate), _p(w_up),
-        _p(w_down), _p(offsets), R, E, d, f, _p(dx_perm), _p(dw_gate), _p(dw_up), _p(dw_down), _p(workspace),
-        _nbytes(workspace), _s(stream)))
+        _p(dy_codes), _p(dy_scales), _p(dy_perm), _p(x_perm), _p(h_save), _p(a_save), _p(wq), _p(offsets), R, E, d,
+        f, _p(dx_perm), _p(dw_gate), _p(dw_up), _p(dw_down), _p(workspace), _nbytes(workspace), _s(stream)))

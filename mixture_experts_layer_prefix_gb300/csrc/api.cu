@@ -351,31 +351,45 @@ moe_status moe_combine_bwd_mxfp8(const void* dy, const void* y_perm, const float
   return MOE_OK;
 }
 
-moe_status moe_mxfp8_mlp_fwd(const uint8_t* x_codes, const uint8_t* x_scales, const void* w_gate, const void* w_up,
-                             const void* w_down, const int32_t* offsets, int R, int E, int d, int f, void* h_save,
-                             void* a_save, void* y_perm, void* workspace, size_t workspace_bytes, void* stream) {
-  MOE_TRY(check_dims(R, d, E, 1));
-  if (f <= 0) return MOE_ERR_INVALID_ARG;
-  if (d % 128 != 0 || f % 128 != 0) return MOE_ERR_UNSUPPORTED;
-  MOE_NEED(w_gate); MOE_NEED(w_up); MOE_NEED(w_down); MOE_NEED(offsets);
-  if (R == 0) return MOE_OK;
-  MOE_NEED(x_codes); MOE_NEED(x_scales); MOE_NEED(h_save); MOE_NEED(a_save); MOE_NEED(y_perm);
-  if (workspace_bytes < mx_fwd_workspace(R, E, d, f)) return MOE_ERR_WORKSPACE;
-  MOE_NEED(workspace);
-  MOE_CUDA_TRY(mx_mlp_fwd(nullptr, w_gate, w_up, w_down, offsets, R, E, d, f, h_save, a_save, y_perm, workspace,
-                          S(stream), x_codes, x_scales));
+size_t moe_mxfp8_weights_size(int E, int d, int f) {
+  if (E <= 0 || d <= 0 || f <= 0) return 0;
+  return mx_weights_bytes(E, d, f);
+}
+
+moe_status moe_mxfp8_prepare_weights(const void* w_gate, const void* w_up, const void* w_down, int E, int d, int f,
+                                     void* wq, size_t wq_bytes, void* stream) {
+  if (E <= 0 || d <= 0 || f <= 0) return MOE_ERR_INVALID_ARG;
+  if (E > 1024 || d % 128 != 0 || f % 128 != 0) return MOE_ERR_UNSUPPORTED;
+  MOE_NEED(w_gate); MOE_NEED(w_up); MOE_NEED(w_down); MOE_NEED(wq);
+  if (wq_bytes < mx_weights_bytes(E, d, f)) return MOE_ERR_WORKSPACE;
+  MOE_CUDA_TRY(mx_prepare_weights(w_gate, w_up, w_down, E, d, f, wq, S(stream)));
   return MOE_OK;
 }
 
-moe_status moe_mxfp8_mlp_bwd(const uint8_t* dy_codes, const uint8_t* dy_scales, const void* dy_perm,
-                             const void* x_perm, const void* h_save, const void* a_save, const void* w_gate,
-                             const void* w_up, const void* w_down, const int32_t* offsets, int R, int E, int d, int f,
-                             void* dx_perm, void* dw_gate, void* dw_up, void* dw_down, void* workspace,
+moe_status moe_mxfp8_mlp_fwd(const uint8_t* x_codes, const uint8_t* x_scales, const void* wq, const int32_t* offsets,
+                             int R, int E, int d, int f, void* h_save, void* a_save, void* y_perm, void* workspace,
                              size_t workspace_bytes, void* stream) {
   MOE_TRY(check_dims(R, d, E, 1));
   if (f <= 0) return MOE_ERR_INVALID_ARG;
   if (d % 128 != 0 || f % 128 != 0) return MOE_ERR_UNSUPPORTED;
-  MOE_NEED(w_gate); MOE_NEED(w_up); MOE_NEED(w_down); MOE_NEED(offsets);
+  MOE_NEED(wq); MOE_NEED(offsets);
+  if (R == 0) return MOE_OK;
+  MOE_NEED(x_codes); MOE_NEED(x_scales); MOE_NEED(h_save); MOE_NEED(a_save); MOE_NEED(y_perm);
+  if (workspace_bytes < mx_fwd_workspace(R, E, d, f)) return MOE_ERR_WORKSPACE;
+  MOE_NEED(workspace);
+  MOE_CUDA_TRY(mx_mlp_fwd(nullptr, nullptr, nullptr, nullptr, offsets, R, E, d, f, h_save, a_save, y_perm, workspace,
+                          S(stream), x_codes, x_scales, wq));
+  return MOE_OK;
+}
+
+moe_status moe_mxfp8_mlp_bwd(const uint8_t* dy_codes, const uint8_t* dy_scales, const void* dy_perm,
+                             const void* x_perm, const void* h_save, const void* a_save, const void* wq,
+                             const int32_t* offsets, int R, int E, int d, int f, void* dx_perm, void* dw_gate,
+                             void* dw_up, void* dw_down, void* workspace, size_t workspace_bytes, void* stream) {
+  MOE_TRY(check_dims(R, d, E, 1));
+  if (f <= 0) return MOE_ERR_INVALID_ARG;
+  if (d % 128 != 0 || f % 128 != 0) return MOE_ERR_UNSUPPORTED;
+  MOE_NEED(wq); MOE_NEED(offsets);
   MOE_NEED(dw_gate); MOE_NEED(dw_up); MOE_NEED(dw_down);
   if (workspace_bytes < mx_bwd_workspace(R, E, d, f)) return MOE_ERR_WORKSPACE;
   MOE_NEED(workspace);
@@ -383,8 +397,8 @@ moe_status moe_mxfp8_mlp_bwd(const uint8_t* dy_codes, const uint8_t* dy_scales, 
     MOE_NEED(dy_codes); MOE_NEED(dy_scales); MOE_NEED(dy_perm); MOE_NEED(x_perm); MOE_NEED(h_save);
     MOE_NEED(a_save); MOE_NEED(dx_perm);
   }
-  MOE_CUDA_TRY(mx_mlp_bwd(dy_perm, x_perm, h_save, a_save, w_gate, w_up, w_down, offsets, R, E, d, f, dx_perm,
-                          dw_gate, dw_up, dw_down, workspace, S(stream), dy_codes, dy_scales));
+  MOE_CUDA_TRY(mx_mlp_bwd(dy_perm, x_perm, h_save, a_save, nullptr, nullptr, nullptr, offsets, R, E, d, f, dx_perm,
+                          dw_gate, dw_up, dw_down, workspace, S(stream), dy_codes, dy_scales, wq));
   return MOE_OK;
 }
 

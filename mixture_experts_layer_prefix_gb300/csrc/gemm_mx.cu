@@ -506,6 +506,25 @@ struct Carver {
   }
 };
 
+// The prepared weights: each of w_gate, w_up, w_down quantised along both of
+// the K axes the expert GEMMs use (columns: blocks of 32 rows, packed scale
+// words; rows: blocks of 32 columns), carved from one caller buffer.
+struct MxWeights {
+  QBuf wg_c, wu_c, wd_c, wd_r, wg_r, wu_r;
+};
+inline MxWeights carve_weights(void* base, int E, int d, int f) {
+  Carver cv{static_cast<char*>(base)};
+  const size_t Ed = (size_t)E * d, Ef = (size_t)E * f;
+  MxWeights w;
+  w.wg_c = cv.take(Ed * f, Ed / 32 * f);
+  w.wu_c = cv.take(Ed * f, Ed / 32 * f);
+  w.wd_c = cv.take(Ef * d, Ef / 32 * d);
+  w.wd_r = cv.take(Ef * d, Ef * d / 32);
+  w.wg_r = cv.take(Ed * f, Ed * f / 32);
+  w.wu_r = cv.take(Ed * f, Ed * f / 32);
+  return w;
+}
+
 // Bytes of the packed scale table of a [rows][C] operand quantised along rows
 // in E segments (32-bit words of 4 blocks; a segment's words start anew).
 inline size_t seg_words_bytes(long rows, int E, long C) { return ((size_t)(rows + 127) / 128 + E + 1) * C * 4; }
@@ -538,7 +557,7 @@ using namespace tc;
 
 cudaError_t mx_mlp_fwd(const void* x_perm, const void* wg, const void* wu, const void* wd, const int32_t* offsets,
                        int R, int E, int d, int f, void* h, void* a, void* y, void* ws, cudaStream_t st,
-                       const uint8_t* xq_codes, const uint8_t* xq_scales) {
+                       const uint8_t* xq_codes, const uint8_t* xq_scales, const void* wq) {
   using namespace mx;
   Carver cv{static_cast<char*>(ws)};
   const long Ed = (long)E * d, Ef = (long)E * f;
@@ -556,9 +575,16 @@ cudaError_t mx_mlp_fwd(const void* x_perm, const void* wg, const void* wu, const
   } else if ((e = launch_mxfp8_quant_rows(x_perm, R, d, xq.q, xq.s, st)) != cudaSuccess) {
     return e;
   }
-  if ((e = launch_mxfp8_quant_cols(wg, (int)Ed, f, nullptr, 1, wgq.q, wgq.s, st, true)) != cudaSuccess) return e;
-  if ((e = launch_mxfp8_quant_cols(wu, (int)Ed, f, nullptr, 1, wuq.q, wuq.s, st, true)) != cudaSuccess) return e;
-  if ((e = launch_mxfp8_quant_cols(wd, (int)Ef, d, nullptr, 1, wdq.q, wdq.s, st, true)) != cudaSuccess) return e;
+  if (wq) {  // prepared once per weight update
+    const MxWeights w = carve_weights(const_cast<void*>(wq), E, d, f);
+    wgq = w.wg_c;
+    wuq = w.wu_c;
+    wdq = w.wd_c;
+  } else {
+    if ((e = launch_mxfp8_quant_cols(wg, (int)Ed, f, nullptr, 1, wgq.q, wgq.s, st, true)) != cudaSuccess) return e;
+    if ((e = launch_mxfp8_quant_cols(wu, (int)Ed, f, nullptr, 1, wuq.q, wuq.s, st, true)) != cudaSuccess) return e;
+    if ((e = launch_mxfp8_quant_cols(wd, (int)Ef, d, nullptr, 1, wdq.q, wdq.s, st, true)) != cudaSuccess) return e;
+  }
 
   CUtensorMap mA, mB0, mB1;
   Params p{};
@@ -583,7 +609,7 @@ cudaError_t mx_mlp_fwd(const void* x_perm, const void* wg, const void* wu, const
 cudaError_t mx_mlp_bwd(const void* dy_perm, const void* x_perm, const void* h, const void* a, const void* wg,
                        const void* wu, const void* wd, const int32_t* offsets, int R, int E, int d, int f,
                        void* dx_perm, void* dwg, void* dwu, void* dwd, void* ws, cudaStream_t st,
-                       const uint8_t* dyq_codes, const uint8_t* dyq_scales) {
+                       const uint8_t* dyq_codes, const uint8_t* dyq_scales, const void* wq) {
   using namespace mx;
   Carver cv{static_cast<char*>(ws)};
   const long Ed = (long)E * d, Ef = (long)E * f;
@@ -610,7 +636,13 @@ cudaError_t mx_mlp_bwd(const void* dy_perm, const void* x_perm, const void* h, c
   } else if ((e = launch_mxfp8_quant_rows(dy_perm, R, d, dyr.q, dyr.s, st)) != cudaSuccess) {
     return e;
   }
-  if ((e = launch_mxfp8_quant_rows(wd, Ef, d, wdr.q, wdr.s, st)) != cudaSuccess) return e;
+  MxWeights w{};
+  if (wq) {
+    w = carve_weights(const_cast<void*>(wq), E, d, f);
+    wdr = w.wd_r;
+  } else if ((e = launch_mxfp8_quant_rows(wd, Ef, d, wdr.q, wdr.s, st)) != cudaSuccess) {
+    return e;
+  }
   if (!map_2d(&mA, dyr.q, U8, 1, d, R, 128, BM) || !map_3d(&mB0, wdr.q, U8, 1, d, f, E, 128, kN_DGRAD2))
     return cudaErrorInvalidValue;
   p.N = f; p.n_tiles = (f + kN_DGRAD2 - 1) / kN_DGRAD2; p.out0 = dh; p.aux = h;
@@ -631,8 +663,13 @@ cudaError_t mx_mlp_bwd(const void* dy_perm, const void* x_perm, const void* h, c
   if ((e = launch<WGRAD2, kN_WGRAD>(mA, mB0, mB0, p, (long)E * p.m_tiles * p.n_tiles, st)) != cudaSuccess) return e;
 
   // dx_perm = dh . [Wg | Wu]^T (K = 2f): dh rows, w_gate / w_up rows
-  if ((e = launch_mxfp8_quant_rows(wg, Ed, f, wgr.q, wgr.s, st)) != cudaSuccess) return e;
-  if ((e = launch_mxfp8_quant_rows(wu, Ed, f, wur.q, wur.s, st)) != cudaSuccess) return e;
+  if (wq) {
+    wgr = w.wg_r;
+    wur = w.wu_r;
+  } else {
+    if ((e = launch_mxfp8_quant_rows(wg, Ed, f, wgr.q, wgr.s, st)) != cudaSuccess) return e;
+    if ((e = launch_mxfp8_quant_rows(wu, Ed, f, wur.q, wur.s, st)) != cudaSuccess) return e;
+  }
   if (!map_2d(&mA, dhr.q, U8, 1, 2L * f, R, 128, BM) || !map_3d(&mB0, wgr.q, U8, 1, f, d, E, 128, kN_DGRAD1) ||
       !map_3d(&mB1, wur.q, U8, 1, f, d, E, 128, kN_DGRAD1))
     return cudaErrorInvalidValue;
@@ -652,6 +689,28 @@ cudaError_t mx_mlp_bwd(const void* dy_perm, const void* x_perm, const void* h, c
 }
 
 size_t mx_fwd_workspace(long R, int E, int d, int f) { return tc::mx::fwd_workspace(R, E, d, f); }
+
+size_t mx_weights_bytes(int E, int d, int f) {  // the carve_weights layout
+  using tc::mx::al;
+  const size_t Ed = (size_t)E * d, Ef = (size_t)E * f;
+  return 2 * (al(Ed * f) + al(Ed / 32 * f)) + (al(Ef * d) + al(Ef / 32 * d)) + (al(Ef * d) + al(Ef * d / 32)) +
+         2 * (al(Ed * f) + al(Ed * f / 32));
+}
+
+cudaError_t mx_prepare_weights(const void* wg, const void* wu, const void* wd, int E, int d, int f, void* wq,
+                               cudaStream_t st) {
+  const tc::mx::MxWeights w = tc::mx::carve_weights(wq, E, d, f);
+  const int Ed = E * d, Ef = E * f;
+  cudaError_t e;
+  // columns: blocks of 32 rows (packed words; blocks never cross experts as
+  // d, f are multiples of 128); rows: blocks of 32 columns
+  if ((e = launch_mxfp8_quant_cols(wg, Ed, f, nullptr, 1, w.wg_c.q, w.wg_c.s, st, true)) != cudaSuccess) return e;
+  if ((e = launch_mxfp8_quant_cols(wu, Ed, f, nullptr, 1, w.wu_c.q, w.wu_c.s, st, true)) != cudaSuccess) return e;
+  if ((e = launch_mxfp8_quant_cols(wd, Ef, d, nullptr, 1, w.wd_c.q, w.wd_c.s, st, true)) != cudaSuccess) return e;
+  if ((e = launch_mxfp8_quant_rows(wd, Ef, d, w.wd_r.q, w.wd_r.s, st)) != cudaSuccess) return e;
+  if ((e = launch_mxfp8_quant_rows(wg, Ed, f, w.wg_r.q, w.wg_r.s, st)) != cudaSuccess) return e;
+  return launch_mxfp8_quant_rows(wu, Ed, f, w.wu_r.q, w.wu_r.s, st);
+}
 size_t mx_bwd_workspace(long R, int E, int d, int f) { return tc::mx::bwd_workspace(R, E, d, f); }
 
 }  // namespace moe

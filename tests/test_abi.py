@@ -110,7 +110,9 @@ def test_mxfp8_dispatch_arguments_rejected_before_launch(lib):
     assert L.moe_permute_mxfp8(FAKE, 8, 64, 2, FAKE, FAKE, FAKE, FAKE + 4, None) == 3        # x_perm aligned
     assert L.moe_combine_bwd_mxfp8(FAKE, FAKE, FAKE, FAKE, 8, 64, 9, FAKE, FAKE, None, FAKE, None) == 2  # k > 8
     # d not a multiple of 128 for the block-scaled GEMMs
-    assert L.moe_mxfp8_mlp_fwd(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 16, 4, 192, 128, FAKE, FAKE, FAKE, FAKE,
-                               1 << 30, None) == 2
-    assert L.moe_mxfp8_mlp_bwd(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 16, 4, 128, 128,
-                               FAKE, FAKE, FAKE, FAKE, FAKE, 16, None) == 4              # workspace
+    assert L.moe_mxfp8_mlp_fwd(FAKE, FAKE, FAKE, FAKE, 16, 4, 192, 128, FAKE, FAKE, FAKE, FAKE, 1 << 30, None) == 2
+    assert L.moe_mxfp8_mlp_bwd(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 16, 4, 128, 128, FAKE, FAKE, FAKE,
+                               FAKE, FAKE, 16, None) == 4                                  # workspace
+    assert L.moe_mxfp8_weights_size(4, 128, 128) > 4 * 128 * 128 * 3 * 2
+    assert L.moe_mxfp8_prepare_weights(FAKE, FAKE, FAKE, 4, 128, 128, FAKE, 16, None) == 4  # wq too small
+    assert L.moe_mxfp8_prepare_weights(FAKE, FAKE, FAKE, 4, 192, 128, FAKE, 1 << 30, None) == 2

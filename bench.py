@@ -277,7 +277,7 @@ def run_ours(args, s, rank, world):
     dy_h = p.dy.cpu().pin_memory()
     y_h = torch.empty_like(b.y, device="cpu").pin_memory()
     dx_h = torch.empty_like(b.dx, device="cpu").pin_memory()
-    e2e_steps = max(1, min(args.steps, 10))
+    e2e_steps = max(1, args.steps)  # the pipeline fill (first upload) and drain (last download) are amortised like the device leg
     pipe = L.HostPipeline(p, b)
     pipe.run([x_h], [dy_h], [y_h], [dx_h], stream=stream)  # warm the second buffer set
     torch.cuda.synchronize()

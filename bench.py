@@ -203,7 +203,7 @@ def run_ours(args, s, rank, world):
                     b.offsets, b.dest_row, b.src_row, b.workspace)
         if mx:  # MXFP8: x quantised as it is dispatched
             N.moe_mxfp8_prepare_weights(p.w_gate, p.w_up, p.w_down, E, d, f, b.wq)
-            N.moe_permute_mxfp8(p.x, T, d, k, b.dest_row, b.x_q, b.x_sc, b.x_perm)
+            N.moe_permute_mxfp8(p.x, T, d, k, E, b.dest_row, b.topk_idx, b.offsets, b.x_q, b.x_sc, b.x_perm)
             ev[0].record(stream)
             N.moe_mxfp8_mlp_fwd(b.x_q, b.x_sc, b.wq, b.offsets, b.R, E, d, f, b.h_save, b.a_save, b.y_perm,
                                 b.workspace)
@@ -219,8 +219,8 @@ def run_ours(args, s, rank, world):
         ev[1].record(stream)
         N.moe_combine_fwd(b.y_perm, b.gates, b.dest_row, dt, T, d, k, b.y)
         if mx:  # MXFP8: dy_perm quantised as the combine backward produces it
-            N.moe_combine_bwd_mxfp8(p.dy, b.y_perm, b.gates, b.dest_row, T, d, k, b.dy_q, b.dy_sc, b.dy_perm,
-                                    b.dgates)
+            N.moe_combine_bwd_mxfp8(p.dy, b.y_perm, b.gates, b.dest_row, b.topk_idx, b.offsets, T, d, k, E, b.dy_q,
+                                    b.dy_sc, b.dy_perm, b.dgates)
         else:
             N.moe_combine_bwd(p.dy, b.y_perm, b.gates, b.dest_row, dt, T, d, k, b.dy_perm, b.dgates)
         N.moe_route_bwd(b.dgates, b.gates, b.topk_idx, b.offsets, b.src_row, p.x, dt, T, d, E, k,

@@ -200,16 +200,32 @@ moe_status moe_dispatch_mlp_bwd(const void* dy_perm, const void* x, const int32_
    MXFP8 gains come from the expert feed-forward and from moving expert data;
    the savings must exceed the cost of the format conversion):
 
+   The expert GEMMs read E8M0 scales as "scale chunks": 512 bytes per (group
+   of 128 rows of an operand, K stage of 128 elements), in the order the
+   tensor-memory scale copy takes them. A row operand ([R][K], rows in expert
+   segments given by offsets) is grouped by per-expert 128-row tiles: row r of
+   expert e (offsets[e] <= r < offsets[e+1]) is index t = (r - offsets[e]) % 128
+   of group G = (offsets[e] + 127 e) / 128 + (r - offsets[e]) / 128, and the
+   scale of its block b (elements 32b..32b+31) is byte
+       512 (G K/128 + b/4) + 16 (t % 32) + 4 ((t / 32) % 4) + b % 4.
+   Bytes of indices past an expert's last row are not written (the GEMMs do
+   not store those rows). Such an operand's scales take
+   moe_mxfp8_row_scales_size(R, E, K) bytes (0 unless K % 128 == 0).
+
    moe_permute_mxfp8: the dispatch of x as E4M3 codes x_codes [T*k][d] and
-   E8M0 scales x_scales [T*k][d/32]; row dest_row[t][j] holds x[t] quantised
-   along d in blocks of 32 (the bytes mxfp8_quantize gives for moe_permute's
-   bf16 x_perm). x bf16 [T][d]. x_perm (optional, may be NULL) receives the
-   bf16 dispatch as well (the weight gradient quantises it along its rows).
+   E8M0 scale chunks x_scales (moe_mxfp8_row_scales_size(T*k, E, d) bytes);
+   row dest_row[t][j] holds x[t] quantised along d in blocks of 32 (the codes
+   and scale values mxfp8_quantize gives for moe_permute's bf16 x_perm).
+   x bf16 [T][d]; topk_idx, offsets as moe_route returned them (they place
+   each row in its expert's tiles). x_perm (optional, may be NULL) receives
+   the bf16 dispatch as well (the weight gradient quantises it along its
+   rows). d % 128 == 0, else MOE_ERR_UNSUPPORTED.
 
    moe_combine_bwd_mxfp8: moe_combine_bwd that also writes the row
-   quantisation (dy_codes [T*k][d], dy_scales [T*k][d/32]) of the bf16-rounded
-   values gates[t][j] * dy[t]; dy_perm (optional, may be NULL) receives the
-   bf16 values; dgates as moe_combine_bwd.
+   quantisation (dy_codes [T*k][d], scale chunks dy_scales of
+   moe_mxfp8_row_scales_size(T*k, E, d) bytes) of the bf16-rounded values
+   gates[t][j] * dy[t]; dy_perm (optional, may be NULL) receives the bf16
+   values; dgates as moe_combine_bwd. d % 128 == 0.
 
    moe_mxfp8_prepare_weights: quantises w_gate, w_up and w_down once per
    weight update into both layouts the expert GEMMs read -- along the weight's
@@ -230,11 +246,13 @@ moe_status moe_dispatch_mlp_bwd(const void* dy_perm, const void* x, const int32_
 size_t moe_mxfp8_weights_size(int E, int d, int f);
 moe_status moe_mxfp8_prepare_weights(const void* w_gate, const void* w_up, const void* w_down, int E, int d, int f,
                                      void* wq, size_t wq_bytes, void* stream);
-moe_status moe_permute_mxfp8(const void* x, int T, int d, int k, const int32_t* dest_row, uint8_t* x_codes,
-                             uint8_t* x_scales, void* x_perm, void* stream);
+size_t moe_mxfp8_row_scales_size(int R, int E, int K);
+moe_status moe_permute_mxfp8(const void* x, int T, int d, int k, int E, const int32_t* dest_row,
+                             const int32_t* topk_idx, const int32_t* offsets, uint8_t* x_codes, uint8_t* x_scales,
+                             void* x_perm, void* stream);
 moe_status moe_combine_bwd_mxfp8(const void* dy, const void* y_perm, const float* gates, const int32_t* dest_row,
-                                 int T, int d, int k, uint8_t* dy_codes, uint8_t* dy_scales, void* dy_perm,
-                                 float* dgates, void* stream);
+                                 const int32_t* topk_idx, const int32_t* offsets, int T, int d, int k, int E,
+                                 uint8_t* dy_codes, uint8_t* dy_scales, void* dy_perm, float* dgates, void* stream);
 moe_status moe_mxfp8_mlp_fwd(const uint8_t* x_codes, const uint8_t* x_scales, const void* wq, const int32_t* offsets,
                              int R, int E, int d, int f, void* h_save, void* a_save, void* y_perm, void* workspace,
                              size_t workspace_bytes, void* stream);

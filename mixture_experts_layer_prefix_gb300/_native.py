@@ -27,7 +27,7 @@ EXPORTS = ("moe_workspace_size", "moe_route", "moe_permute", "moe_permute_bwd", 
            "mxfp8_quantize", "moe_get_device_error", "moe_sm_count", "moe_launch_count", "moe_route_noalloc",
            "moe_dispatch_mlp_fwd", "moe_dispatch_mlp_bwd", "moe_route_stats", "moe_permute_mxfp8",
            "moe_combine_bwd_mxfp8", "moe_mxfp8_mlp_fwd", "moe_mxfp8_mlp_bwd", "moe_mxfp8_weights_size",
-           "moe_mxfp8_prepare_weights")
+           "moe_mxfp8_prepare_weights", "moe_mxfp8_row_scales_size")
 
 
 class MoEError(RuntimeError):
@@ -65,8 +65,9 @@ def load(path: str = LIB_PATH):
         "moe_route_noalloc": ([P, P, P, I, I, I, I, I, P, I, P, P, P, P, P, P, P], I),
         "moe_dispatch_mlp_fwd": ([P, P, I, I, P, P, P, I, P, I, I, I, P, P, P, P], I),
         "moe_route_stats": ([P, P, I, I, I, P, P, P, Z, P], I),
-        "moe_permute_mxfp8": ([P, I, I, I, P, P, P, P, P], I),
-        "moe_combine_bwd_mxfp8": ([P, P, P, P, I, I, I, P, P, P, P, P], I),
+        "moe_permute_mxfp8": ([P, I, I, I, I, P, P, P, P, P, P, P], I),
+        "moe_combine_bwd_mxfp8": ([P, P, P, P, P, P, I, I, I, I, P, P, P, P, P], I),
+        "moe_mxfp8_row_scales_size": ([I, I, I], Z),
         "moe_mxfp8_mlp_fwd": ([P, P, P, P, I, I, I, I, P, P, P, P, Z, P], I),
         "moe_mxfp8_mlp_bwd": ([P, P, P, P, P, P, P, P, I, I, I, I, P, P, P, P, P, Z, P], I),
         "moe_mxfp8_weights_size": ([I, I, I], Z),
@@ -203,15 +204,20 @@ def moe_route_stats(logits, counts, T, E, k, probs_mean, stats, workspace, strea
                                                    _p(workspace), _nbytes(workspace), _s(stream)))
 
 
-def moe_permute_mxfp8(x, T, d, k, dest_row, x_codes, x_scales, x_perm=None, stream=None):
-    _chk("moe_permute_mxfp8", load().moe_permute_mxfp8(_p(x), T, d, k, _p(dest_row), _p(x_codes), _p(x_scales),
-                                                       _p(x_perm), _s(stream)))
+def moe_mxfp8_row_scales_size(R, E, K):
+    return load().moe_mxfp8_row_scales_size(R, E, K)
 
 
-def moe_combine_bwd_mxfp8(dy, y_perm, gates, dest_row, T, d, k, dy_codes, dy_scales, dy_perm, dgates, stream=None):
+def moe_permute_mxfp8(x, T, d, k, E, dest_row, topk_idx, offsets, x_codes, x_scales, x_perm=None, stream=None):
+    _chk("moe_permute_mxfp8", load().moe_permute_mxfp8(_p(x), T, d, k, E, _p(dest_row), _p(topk_idx), _p(offsets),
+                                                       _p(x_codes), _p(x_scales), _p(x_perm), _s(stream)))
+
+
+def moe_combine_bwd_mxfp8(dy, y_perm, gates, dest_row, topk_idx, offsets, T, d, k, E, dy_codes, dy_scales, dy_perm,
+                          dgates, stream=None):
     _chk("moe_combine_bwd_mxfp8", load().moe_combine_bwd_mxfp8(
-        _p(dy), _p(y_perm), _p(gates), _p(dest_row), T, d, k, _p(dy_codes), _p(dy_scales), _p(dy_perm), _p(dgates),
-        _s(stream)))
+        _p(dy), _p(y_perm), _p(gates), _p(dest_row), _p(topk_idx), _p(offsets), T, d, k, E, _p(dy_codes),
+        _p(dy_scales), _p(dy_perm), _p(dgates), _s(stream)))
 
 
 def moe_mxfp8_weights_size(E, d, f):

@@ -6,6 +6,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "mxfp8_common.cuh"
 
 namespace moe {
 
@@ -328,27 +329,35 @@ moe_status moe_grouped_mlp_bwd(const void* dy_perm, const void* x_perm, const vo
   return MOE_OK;
 }
 
-moe_status moe_permute_mxfp8(const void* x, int T, int d, int k, const int32_t* dest_row, uint8_t* x_codes,
-                             uint8_t* x_scales, void* x_perm, void* stream) {
-  MOE_TRY(check_dims(T, d, k, k));
+moe_status moe_permute_mxfp8(const void* x, int T, int d, int k, int E, const int32_t* dest_row,
+                             const int32_t* topk_idx, const int32_t* offsets, uint8_t* x_codes, uint8_t* x_scales,
+                             void* x_perm, void* stream) {
+  MOE_TRY(check_dims(T, d, E, k));
+  if (d % 128 != 0) return MOE_ERR_UNSUPPORTED;
   if (T == 0) return MOE_OK;
-  MOE_NEED(x); MOE_NEED(dest_row); MOE_NEED(x_codes); MOE_NEED(x_scales);
+  MOE_NEED(x); MOE_NEED(dest_row); MOE_NEED(topk_idx); MOE_NEED(offsets); MOE_NEED(x_codes); MOE_NEED(x_scales);
   if (x_perm && !aligned16(x_perm)) return MOE_ERR_ALIGNMENT;
-  MOE_CUDA_TRY(launch_permute_quant(x, T, d, k, dest_row, x_codes, x_scales, x_perm, S(stream)));
+  MOE_CUDA_TRY(launch_permute_quant(x, T, d, k, dest_row, topk_idx, offsets, x_codes, x_scales, x_perm, S(stream)));
   return MOE_OK;
 }
 
 moe_status moe_combine_bwd_mxfp8(const void* dy, const void* y_perm, const float* gates, const int32_t* dest_row,
-                                 int T, int d, int k, uint8_t* dy_codes, uint8_t* dy_scales, void* dy_perm,
-                                 float* dgates, void* stream) {
-  MOE_TRY(check_dims(T, d, k, k));
+                                 const int32_t* topk_idx, const int32_t* offsets, int T, int d, int k, int E,
+                                 uint8_t* dy_codes, uint8_t* dy_scales, void* dy_perm, float* dgates, void* stream) {
+  MOE_TRY(check_dims(T, d, E, k));
+  if (d % 128 != 0) return MOE_ERR_UNSUPPORTED;
   if (T == 0) return MOE_OK;
-  MOE_NEED(dy); MOE_NEED(y_perm); MOE_NEED(gates); MOE_NEED(dest_row); MOE_NEED(dy_codes); MOE_NEED(dy_scales);
-  MOE_NEED(dgates);
+  MOE_NEED(dy); MOE_NEED(y_perm); MOE_NEED(gates); MOE_NEED(dest_row); MOE_NEED(topk_idx); MOE_NEED(offsets);
+  MOE_NEED(dy_codes); MOE_NEED(dy_scales); MOE_NEED(dgates);
   if (dy_perm && !aligned16(dy_perm)) return MOE_ERR_ALIGNMENT;
-  MOE_CUDA_TRY(launch_combine_bwd_quant(dy, y_perm, gates, dest_row, T, d, k, dy_codes, dy_scales, dy_perm, dgates,
-                                        S(stream)));
+  MOE_CUDA_TRY(launch_combine_bwd_quant(dy, y_perm, gates, dest_row, topk_idx, offsets, T, d, k, dy_codes, dy_scales,
+                                        dy_perm, dgates, S(stream)));
   return MOE_OK;
+}
+
+size_t moe_mxfp8_row_scales_size(int R, int E, int K) {
+  if (R < 0 || E <= 0 || K <= 0 || K % 128 != 0) return 0;
+  return (size_t)mx_row_tiles(R, E) * 4 * K;
 }
 
 size_t moe_mxfp8_weights_size(int E, int d, int f) {

@@ -7,9 +7,10 @@
 // One persistent kernel per GEMM, one CTA per SM:
 //   warp 0      producer. Lane 0 issues TMA for a 4-stage ring of
 //               (A 128x128, B 256x128) E4M3 tiles (128 B rows, 128-byte
-//               swizzle); all lanes gather the stage's E8M0 scales as 32-bit
-//               words (4 consecutive K blocks each) with cp.async into a small
-//               shared staging area, tracked by the same stage barrier.
+//               swizzle) and bulk copies of the stage's E8M0 scale chunks
+//               (512 B per 128 rows or columns, stored by the quantisers in
+//               the order the tensor-memory copy takes) into a small shared
+//               staging area, all tracked by the same stage barrier.
 //   warp 1      TMEM owner and MMA issuer: per stage, tcgen05.cp moves the
 //               scales from shared memory into a TMEM ring (32x128b copies
 //               replicated to all four lane quadrants), then four
@@ -64,15 +65,6 @@ struct Smem {
   int abort_flag;
 };
 
-__device__ __forceinline__ void cp_async4(void* dst, const void* src, bool valid) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(ptx::smem_u32(dst)), "l"(src),
-               "r"(valid ? 4 : 0)
-               : "memory");
-}
-// The stage barrier completes only once this thread's earlier cp.async copies landed.
-__device__ __forceinline__ void cp_async_arrive(uint64_t* bar) {
-  asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" ::"r"(ptx::smem_u32(bar)) : "memory");
-}
 // Non-swizzled shared-memory descriptor of a [rows][16 B] source of tcgen05.cp
 // (8-row groups 128 B apart).
 __device__ __forceinline__ uint64_t cp_desc(uint32_t saddr) {
@@ -193,63 +185,47 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         if (!wait_bar(&sm->empty[s], ph ^ 1u, &sm->abort_flag, p.err)) { ok = false; break; }
         uint64_t* fb = &sm->full[s];
         const int k0 = kb * BK;
-        // ---- scales: A rows of the tile, then B columns
-        uint8_t* sa = sc_area + s * G::SC_BYTES;
-        uint8_t* sb = sa + 512;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int r = lane + 32 * i;
-          const uint8_t* src = p.sfa;
-          bool valid;
-          if (!Tr::kragged) {  // rows quantised along K: [R][K/32] bytes
-            const int row = tl.m0 + r;
-            valid = row < p.R;
-            if (valid) src = p.sfa + (size_t)row * (Kd / 32) + k0 / 32;
-          } else {  // columns quantised along the expert's rows: [words][M] words
-            const int m = tl.m0 + r;
-            valid = m < p.M;
-            if (valid) src = p.sfa + ((size_t)(wstart[tl.e] + kb) * p.M + m) * 4;
-          }
-          cp_async4(sa + lane * 16 + i * 4, src, valid);
-        }
-#pragma unroll
-        for (int c = 0; c < TBN / 32; ++c) {
-          const int nt = lane + 32 * c;  // tile column
-          const uint8_t* src = p.sfb0;
-          bool valid = false;
-          if (KIND == FPROP1) {  // gate | up, [E*d/128][f] words
-            const int n = tl.n_idx * 128 + (nt & 127);
-            valid = n < p.f;
-            if (valid) src = (nt < 128 ? p.sfb0 : p.sfb1) + (((size_t)tl.e * p.d + k0) / 128 * p.f + n) * 4;
-          } else if (KIND == FPROP2) {  // [E*f/128][d] words
-            const int n = tl.n_idx * TBN + nt;
-            valid = n < p.d;
-            if (valid) src = p.sfb0 + (((size_t)tl.e * p.f + k0) / 128 * p.d + n) * 4;
-          } else if (KIND == DGRAD2) {  // rows of w_down along d: [E*f][d/32] bytes
-            const int n = tl.n_idx * TBN + nt;
-            valid = n < p.f;
-            if (valid) src = p.sfb0 + ((size_t)tl.e * p.f + n) * (p.d / 32) + k0 / 32;
-          } else if (KIND == DGRAD1) {  // rows of w_gate / w_up along f: [E*d][f/32] bytes
-            const int n = tl.n_idx * TBN + nt;
-            valid = n < p.d;
-            if (valid) {
-              const int kk = k0 < p.f ? k0 : k0 - p.f;
-              src = (k0 < p.f ? p.sfb0 : p.sfb1) + ((size_t)tl.e * p.d + n) * (p.f / 32) + kk / 32;
-            }
-          } else {  // wgrad: columns quantised along the expert's rows, [words][N] words
-            const int n = tl.n_idx * TBN + nt;
-            valid = n < p.N;
-            if (valid) src = p.sfb0 + ((size_t)(wstart[tl.e] + kb) * p.N + n) * 4;
-          }
-          cp_async4(sb + (c >> 2) * 512 + lane * 16 + (c & 3) * 4, src, valid);
-        }
-        cp_async_arrive(fb);
-        __syncwarp();
         if (lane == 0) {
-          // ---- E4M3 tiles
           uint8_t* a = smem + s * G::STAGE_BYTES;
           uint8_t* b = a + A_BYTES;
-          ptx::mbar_expect_tx(fb, G::STAGE_BYTES);
+          ptx::mbar_expect_tx(fb, G::STAGE_BYTES + G::SC_BYTES);
+          // ---- E8M0 scale chunks (512 B per 128 rows or columns and K stage):
+          // A's, then one per 128 columns of B
+          uint8_t* sa = sc_area + s * G::SC_BYTES;
+          uint8_t* sb = sa + 512;
+          if (!Tr::kragged) {  // rows in per-expert 128-row tiles, K = Kd
+            const long grp = mx_row_tile_base(offs[tl.e], tl.e) + tl.m_idx;
+            ptx::bulk_load(sa, p.sfa + ((grp * (Kd / 128) + kb) << 9), 512, fb);
+          } else {  // features m0.. at the expert's K stage
+            ptx::bulk_load(sa, p.sfa + (((long)(wstart[tl.e] + kb) * (p.M / 128) + tl.m_idx) << 9), 512, fb);
+          }
+          if (KIND == FPROP1) {  // w_gate | w_up columns: K stage e d/128 + kb, column group n_idx
+            const long c = ((long)tl.e * (p.d / 128) + kb) * (p.f / 128) + tl.n_idx;
+            ptx::bulk_load(sb, p.sfb0 + (c << 9), 512, fb);
+            ptx::bulk_load(sb + 512, p.sfb1 + (c << 9), 512, fb);
+          } else if (KIND == FPROP2) {  // w_down columns: K stage e f/128 + kb
+            const long c = ((long)tl.e * (p.f / 128) + kb) * (p.d / 128) + (long)tl.n_idx * G::SCB;
+            ptx::bulk_load(sb, p.sfb0 + (c << 9), 512 * G::SCB, fb);
+          } else if (KIND == DGRAD2) {  // w_down rows (f) along d
+#pragma unroll
+            for (int j = 0; j < G::SCB; ++j) {
+              const long grp = (long)tl.e * (p.f / 128) + (long)tl.n_idx * G::SCB + j;
+              ptx::bulk_load(sb + 512 * j, p.sfb0 + ((grp * (p.d / 128) + kb) << 9), 512, fb);
+            }
+          } else if (KIND == DGRAD1) {  // w_gate rows (d) along f for K < f, then w_up's
+            const int kfs = p.f / 128;
+            const uint8_t* src = kb < kfs ? p.sfb0 : p.sfb1;
+            const int kk = kb < kfs ? kb : kb - kfs;
+#pragma unroll
+            for (int j = 0; j < G::SCB; ++j) {
+              const long grp = (long)tl.e * (p.d / 128) + (long)tl.n_idx * G::SCB + j;
+              ptx::bulk_load(sb + 512 * j, src + ((grp * kfs + kk) << 9), 512, fb);
+            }
+          } else {  // wgrad: B features at the expert's K stage
+            const long c = (long)(wstart[tl.e] + kb) * (p.N / 128) + (long)tl.n_idx * G::SCB;
+            ptx::bulk_load(sb, p.sfb0 + (c << 9), 512 * G::SCB, fb);
+          }
+          // ---- E4M3 tiles
           if (KIND == FPROP1) {
             ptx::tma_load_2d(a, &tmA, fb, k0, tl.m0);
             const int n0 = tl.n_idx * 128;
@@ -309,14 +285,14 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           const int valid = tl.row_end - (tl.k_row0 + kb * BK);
           if (valid < BK) {
             // skip K steps made only of rows past the expert's end; zero the
-            // rest of the last partial step in A (one 128-row box)
+            // rest of the last partial step in A (one 128-row box), which the
+            // async proxy then reads
             nks = (valid + 31) / 32;
             for (int i = valid * 8 + lane; i < nks * 32 * 8; i += 32)
               *reinterpret_cast<uint4*>(a + i * 16) = make_uint4(0, 0, 0, 0);
+            ptx::fence_proxy_async_smem();
           }
         }
-        // cp.async-written scales and the zeroed rows are read by the async proxy
-        ptx::fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
           const uint32_t sa = ptx::smem_u32(sc_area + s * G::SC_BYTES);
@@ -423,7 +399,7 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             warp_store_rows(stg, wg[cc], h + n, 2 * (size_t)p.f, nrows, lane);
             warp_store_rows(stg, wu[cc], h + p.f + n, 2 * (size_t)p.f, nrows, lane);
             warp_store_rows(stg, wa[cc], ao + n, p.f, nrows, lane);
-            if (p.qout) quant_rows_staged(p, stg, wa[cc], wrow, nrows, p.f, n, lane);
+            if (p.qout) quant_rows_staged(p, stg, wa[cc], wrow, nrows, p.f, n, lane, tile_scale_row(tl, q, lane, p.f));
           }
         } else {
           uint32_t w[4][16];
@@ -507,8 +483,8 @@ struct Carver {
 };
 
 // The prepared weights: each of w_gate, w_up, w_down quantised along both of
-// the K axes the expert GEMMs use (columns: blocks of 32 rows, packed scale
-// words; rows: blocks of 32 columns), carved from one caller buffer.
+// the K axes the expert GEMMs use (columns: blocks of 32 rows; rows: blocks of
+// 32 columns; scales as scale chunks), carved from one caller buffer.
 struct MxWeights {
   QBuf wg_c, wu_c, wd_c, wd_r, wg_r, wu_r;
 };
@@ -525,26 +501,30 @@ inline MxWeights carve_weights(void* base, int E, int d, int f) {
   return w;
 }
 
-// Bytes of the packed scale table of a [rows][C] operand quantised along rows
-// in E segments (32-bit words of 4 blocks; a segment's words start anew).
+// Bytes of the scale chunks of a [rows][C] operand quantised along rows in E
+// segments (K stages of 4 blocks; a segment's stages start anew).
 inline size_t seg_words_bytes(long rows, int E, long C) { return ((size_t)(rows + 127) / 128 + E + 1) * C * 4; }
 
 }  // namespace
 
+// Bytes of the scale chunks of a row operand with K columns, grouped by
+// per-expert 128-row tiles.
+inline size_t tile_scale_bytes(long R, int E, long K) { return (size_t)mx_row_tiles(R, E) * 4 * K; }
+
 size_t fwd_workspace(long R, int E, int d, int f) {
   const size_t Ed = (size_t)E * d;
-  return al(R * (size_t)d) + al(R * (size_t)d / 32) + al(R * (size_t)f) + al(R * (size_t)f / 32) +
+  return al(R * (size_t)d) + al(tile_scale_bytes(R, E, d)) + al(R * (size_t)f) + al(tile_scale_bytes(R, E, f)) +
          2 * (al(Ed * f) + al(Ed / 32 * f)) + al((size_t)E * f * d) + al((size_t)E * f / 32 * d);
 }
 
 size_t bwd_workspace(long R, int E, int d, int f) {
   const size_t Ed = (size_t)E * d, Ef = (size_t)E * f;
   return al(R * 2 * (size_t)f * 2)                                         // dh (bf16)
-         + al(R * (size_t)d) + al(R * (size_t)d / 32)                      // dy rows
+         + al(R * (size_t)d) + al(tile_scale_bytes(R, E, d))               // dy rows
          + al(R * (size_t)d) + al(seg_words_bytes(R, E, d))                    // dy segment columns
          + al(R * (size_t)f) + al(seg_words_bytes(R, E, f))                    // a segment columns
          + al(Ef * d) + al(Ef * d / 32)                                    // w_down rows
-         + al(R * 2 * (size_t)f) + al(R * 2 * (size_t)f / 32)              // dh rows
+         + al(R * 2 * (size_t)f) + al(tile_scale_bytes(R, E, 2L * f))      // dh rows
          + al(R * 2 * (size_t)f) + al(seg_words_bytes(R, E, 2L * f))            // dh segment columns
          + 2 * (al(Ed * f) + al(Ed * f / 32))                              // w_gate, w_up rows
          + al(R * (size_t)d) + al(seg_words_bytes(R, E, d));                   // x segment columns
@@ -561,8 +541,8 @@ cudaError_t mx_mlp_fwd(const void* x_perm, const void* wg, const void* wu, const
   using namespace mx;
   Carver cv{static_cast<char*>(ws)};
   const long Ed = (long)E * d, Ef = (long)E * f;
-  QBuf xq = cv.take((size_t)R * d, (size_t)R * d / 32);
-  QBuf aq = cv.take((size_t)R * f, (size_t)R * f / 32);
+  QBuf xq = cv.take((size_t)R * d, tile_scale_bytes(R, E, d));
+  QBuf aq = cv.take((size_t)R * f, tile_scale_bytes(R, E, f));
   QBuf wgq = cv.take((size_t)Ed * f, (size_t)Ed / 32 * f);
   QBuf wuq = cv.take((size_t)Ed * f, (size_t)Ed / 32 * f);
   QBuf wdq = cv.take((size_t)Ef * d, (size_t)Ef / 32 * d);
@@ -572,7 +552,7 @@ cudaError_t mx_mlp_fwd(const void* x_perm, const void* wg, const void* wu, const
   if (xq_codes) {
     xq.q = const_cast<uint8_t*>(xq_codes);
     xq.s = const_cast<uint8_t*>(xq_scales);
-  } else if ((e = launch_mxfp8_quant_rows(x_perm, R, d, xq.q, xq.s, st)) != cudaSuccess) {
+  } else if ((e = launch_mxfp8_quant_rows(x_perm, R, d, xq.q, xq.s, st, kScalesTiles, offsets, E)) != cudaSuccess) {
     return e;
   }
   if (wq) {  // prepared once per weight update
@@ -614,11 +594,11 @@ cudaError_t mx_mlp_bwd(const void* dy_perm, const void* x_perm, const void* h, c
   Carver cv{static_cast<char*>(ws)};
   const long Ed = (long)E * d, Ef = (long)E * f;
   void* dh = cv.raw((size_t)R * 2 * f * 2);
-  QBuf dyr = cv.take((size_t)R * d, (size_t)R * d / 32);
+  QBuf dyr = cv.take((size_t)R * d, tile_scale_bytes(R, E, d));
   QBuf dyc = cv.take((size_t)R * d, seg_words_bytes(R, E, d));
   QBuf ac = cv.take((size_t)R * f, seg_words_bytes(R, E, f));
   QBuf wdr = cv.take((size_t)Ef * d, (size_t)Ef * d / 32);
-  QBuf dhr = cv.take((size_t)R * 2 * f, (size_t)R * 2 * f / 32);
+  QBuf dhr = cv.take((size_t)R * 2 * f, tile_scale_bytes(R, E, 2L * f));
   QBuf dhc = cv.take((size_t)R * 2 * f, seg_words_bytes(R, E, 2L * f));
   QBuf wgr = cv.take((size_t)Ed * f, (size_t)Ed * f / 32);
   QBuf wur = cv.take((size_t)Ed * f, (size_t)Ed * f / 32);
@@ -633,14 +613,15 @@ cudaError_t mx_mlp_bwd(const void* dy_perm, const void* x_perm, const void* h, c
   if (dyq_codes) {
     dyr.q = const_cast<uint8_t*>(dyq_codes);
     dyr.s = const_cast<uint8_t*>(dyq_scales);
-  } else if ((e = launch_mxfp8_quant_rows(dy_perm, R, d, dyr.q, dyr.s, st)) != cudaSuccess) {
+  } else if ((e = launch_mxfp8_quant_rows(dy_perm, R, d, dyr.q, dyr.s, st, kScalesTiles, offsets, E)) !=
+             cudaSuccess) {
     return e;
   }
   MxWeights w{};
   if (wq) {
     w = carve_weights(const_cast<void*>(wq), E, d, f);
     wdr = w.wd_r;
-  } else if ((e = launch_mxfp8_quant_rows(wd, Ef, d, wdr.q, wdr.s, st)) != cudaSuccess) {
+  } else if ((e = launch_mxfp8_quant_rows(wd, Ef, d, wdr.q, wdr.s, st, kScalesChunk)) != cudaSuccess) {
     return e;
   }
   if (!map_2d(&mA, dyr.q, U8, 1, d, R, 128, BM) || !map_3d(&mB0, wdr.q, U8, 1, d, f, E, 128, kN_DGRAD2))
@@ -667,8 +648,8 @@ cudaError_t mx_mlp_bwd(const void* dy_perm, const void* x_perm, const void* h, c
     wgr = w.wg_r;
     wur = w.wu_r;
   } else {
-    if ((e = launch_mxfp8_quant_rows(wg, Ed, f, wgr.q, wgr.s, st)) != cudaSuccess) return e;
-    if ((e = launch_mxfp8_quant_rows(wu, Ed, f, wur.q, wur.s, st)) != cudaSuccess) return e;
+    if ((e = launch_mxfp8_quant_rows(wg, Ed, f, wgr.q, wgr.s, st, kScalesChunk)) != cudaSuccess) return e;
+    if ((e = launch_mxfp8_quant_rows(wu, Ed, f, wur.q, wur.s, st, kScalesChunk)) != cudaSuccess) return e;
   }
   if (!map_2d(&mA, dhr.q, U8, 1, 2L * f, R, 128, BM) || !map_3d(&mB0, wgr.q, U8, 1, f, d, E, 128, kN_DGRAD1) ||
       !map_3d(&mB1, wur.q, U8, 1, f, d, E, 128, kN_DGRAD1))
@@ -702,14 +683,14 @@ cudaError_t mx_prepare_weights(const void* wg, const void* wu, const void* wd, i
   const tc::mx::MxWeights w = tc::mx::carve_weights(wq, E, d, f);
   const int Ed = E * d, Ef = E * f;
   cudaError_t e;
-  // columns: blocks of 32 rows (packed words; blocks never cross experts as
-  // d, f are multiples of 128); rows: blocks of 32 columns
+  // columns: blocks of 32 rows (K stages never cross experts as d, f are
+  // multiples of 128); rows: blocks of 32 columns; scales as scale chunks
   if ((e = launch_mxfp8_quant_cols(wg, Ed, f, nullptr, 1, w.wg_c.q, w.wg_c.s, st, true)) != cudaSuccess) return e;
   if ((e = launch_mxfp8_quant_cols(wu, Ed, f, nullptr, 1, w.wu_c.q, w.wu_c.s, st, true)) != cudaSuccess) return e;
   if ((e = launch_mxfp8_quant_cols(wd, Ef, d, nullptr, 1, w.wd_c.q, w.wd_c.s, st, true)) != cudaSuccess) return e;
-  if ((e = launch_mxfp8_quant_rows(wd, Ef, d, w.wd_r.q, w.wd_r.s, st)) != cudaSuccess) return e;
-  if ((e = launch_mxfp8_quant_rows(wg, Ed, f, w.wg_r.q, w.wg_r.s, st)) != cudaSuccess) return e;
-  return launch_mxfp8_quant_rows(wu, Ed, f, w.wu_r.q, w.wu_r.s, st);
+  if ((e = launch_mxfp8_quant_rows(wd, Ef, d, w.wd_r.q, w.wd_r.s, st, kScalesChunk)) != cudaSuccess) return e;
+  if ((e = launch_mxfp8_quant_rows(wg, Ed, f, w.wg_r.q, w.wg_r.s, st, kScalesChunk)) != cudaSuccess) return e;
+  return launch_mxfp8_quant_rows(wu, Ed, f, w.wu_r.q, w.wu_r.s, st, kScalesChunk);
 }
 size_t mx_bwd_workspace(long R, int E, int d, int f) { return tc::mx::bwd_workspace(R, E, d, f); }
 

@@ -19,10 +19,12 @@ cudaError_t launch_route_meta(const float* logits, int T, int E, int k, int32_t*
                               float* gates, int32_t* counts, int32_t* offsets, int32_t* dest_row,
                               int32_t* src_row, int32_t* hist, cudaStream_t st);
 
-// combine backward writing the MXFP8 row quantisation of dy_perm (bf16 only)
+// combine backward writing the MXFP8 row quantisation of dy_perm (bf16 only;
+// scales as scale chunks grouped by per-expert 128-row tiles)
 cudaError_t launch_combine_bwd_quant(const void* dy, const void* y_perm, const float* gates,
-                                     const int32_t* dest_row, int Tn, int d, int k, uint8_t* q, uint8_t* qsc,
-                                     void* dy_perm, float* dgates, cudaStream_t st);
+                                     const int32_t* dest_row, const int32_t* topk_idx, const int32_t* offsets,
+                                     int Tn, int d, int k, uint8_t* q, uint8_t* qsc, void* dy_perm, float* dgates,
+                                     cudaStream_t st);
 
 // ------------------------------------------------------ routing statistics
 size_t route_stats_workspace_bytes(int T, int E);
@@ -87,16 +89,23 @@ cudaError_t tc_mlp_bwd(const void* dy_perm, const void* x_perm, const void* h, c
                        const int32_t* src_row = nullptr, int gk = 1, int T = 0);
 
 // ------------------------------------------------------------------ MXFP8
-cudaError_t launch_mxfp8_quant_rows(const void* src, long rows, long K, uint8_t* q, uint8_t* sc,
-                                    cudaStream_t st);
-// packed: scales as 32-bit words of 4 consecutive blocks of a column (GEMM operand
-// layout); otherwise one byte per block, [blocks][C] (public layout).
+// Where a row quantiser puts the scale byte of block b of row r:
+//   kScalesPlain  sc[r][K/32] (public layout)
+//   kScalesChunk  scale chunks (mxfp8_common.cuh), group r / 128 (weights)
+//   kScalesTiles  scale chunks, group = the row's per-expert 128-row tile
+//                 (offsets: [E+1] expert offsets; GEMM row operands)
+enum ScaleLayout { kScalesPlain = 0, kScalesChunk = 1, kScalesTiles = 2 };
+cudaError_t launch_mxfp8_quant_rows(const void* src, long rows, long K, uint8_t* q, uint8_t* sc, cudaStream_t st,
+                                    int layout = kScalesPlain, const int32_t* offsets = nullptr, int E = 0);
+// packed: scales as scale chunks (GEMM operand layout); otherwise one byte per
+// block, [blocks][C] (public layout).
 cudaError_t launch_mxfp8_quant_cols(const void* src, int rows, int C, const int32_t* seg, int nseg,
                                     uint8_t* q, uint8_t* sc, cudaStream_t st, bool packed = false);
-// Dispatch with the row quantisation fused: q [T*k][d], sc [T*k][d/32]; the
-// bf16 x_perm too when given.
-cudaError_t launch_permute_quant(const void* x, int T, int d, int k, const int32_t* dest_row, uint8_t* q,
-                                 uint8_t* sc, void* x_perm, cudaStream_t st);
+// Dispatch with the row quantisation fused: q [T*k][d], sc as scale chunks
+// grouped by per-expert 128-row tiles; the bf16 x_perm too when given.
+cudaError_t launch_permute_quant(const void* x, int T, int d, int k, const int32_t* dest_row,
+                                 const int32_t* topk_idx, const int32_t* offsets, uint8_t* q, uint8_t* sc,
+                                 void* x_perm, cudaStream_t st);
 
 cudaError_t tc_router_logits(const void* x, const void* w_r, const float* bias, int T, int d, int E,
                              float* logits, cudaStream_t st);

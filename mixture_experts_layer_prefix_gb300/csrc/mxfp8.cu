@@ -29,22 +29,52 @@ __device__ __forceinline__ int e8m0_exponent(float amax) { return mx_e8m0_expone
 __device__ __forceinline__ float pow2_neg(int s) { return mx_pow2_neg(s); }
 __device__ __forceinline__ uint32_t e4m3(float v) { return mx_e4m3(v); }
 
+// MODE (ScaleLayout): where the scale byte of block b of row r goes.
+template <int MODE>
 __global__ void __launch_bounds__(256)
-quant_rows_kernel(const __nv_bfloat16* __restrict__ src, long nblocks, uint8_t* __restrict__ q,
-                  uint8_t* __restrict__ sc) {
+quant_rows_kernel(const __nv_bfloat16* __restrict__ src, long nblocks, int kblocks, uint8_t* __restrict__ q,
+                  uint8_t* __restrict__ sc, const int32_t* __restrict__ offs, int E) {
   const long blk = blockIdx.x * (long)blockDim.x + threadIdx.x;
   if (blk >= nblocks) return;
   float v[32];
   const __nv_bfloat16* p = src + blk * 32;
 #pragma unroll
   for (int i = 0; i < 4; ++i) Vec16<__nv_bfloat16>::load(p + 8 * i, v + 8 * i);
-  mx_quant_block32(v, q + blk * 32, sc + blk);
+  uint32_t w[8];
+  const uint8_t s = mx_quant_block32_regs(v, w);
+  uint4* out = reinterpret_cast<uint4*>(q + blk * 32);
+  out[0] = make_uint4(w[0], w[1], w[2], w[3]);
+  out[1] = make_uint4(w[4], w[5], w[6], w[7]);
+  if (MODE == kScalesPlain) {
+    sc[blk] = s;
+    return;
+  }
+  const long row = blk / kblocks;
+  const int b = static_cast<int>(blk % kblocks);
+  long grp;
+  int t;
+  if (MODE == kScalesChunk) {
+    grp = row >> 7;
+    t = static_cast<int>(row & 127);
+  } else {
+    int lo = 0, hi = E;  // the expert holding the row: offs[lo] <= row < offs[lo + 1]
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (__ldg(offs + mid) <= row) lo = mid; else hi = mid;
+    }
+    const long local = row - __ldg(offs + lo);
+    grp = mx_row_tile_base(__ldg(offs + lo), lo) + (local >> 7);
+    t = static_cast<int>(local & 127);
+  }
+  sc[((grp * (kblocks / 4) + b / 4) << 9) + mx_chunk_lane(t) + (b & 3)] = s;
 }
 
 // Block-row table: segment g owns block rows [bstart[g], bstart[g+1]).
-// PACKED: scales go to a [words][C] table of 32-bit words, word w of segment
-// g holding its blocks 4w..4w+3 in bytes 0..3 (words of segment g start at
-// sum_{h<g} ceil(blocks_h / 4)); bytes past a segment's last block are 127.
+// PACKED: scales go to scale chunks (GEMM operand layout): K stage w (four
+// block rows of a segment; the stages of segment g start at
+// sum_{h<g} ceil(blocks_h / 4)) and column group c / 128 form chunk
+// w * (C / 128) + c / 128, and block 4w + j of column c is byte
+// mx_chunk_lane(c % 128) + j of it; bytes past a segment's last block are 127.
 // A CTA handles kColBlockRows block rows of 256 columns; each thread owns 2
 // consecutive columns (a warp reads 128 contiguous bytes of a row) and holds
 // its 32 x 2 block in registers, so every input byte is read from memory
@@ -133,12 +163,12 @@ quant_cols_kernel(const __nv_bfloat16* __restrict__ src, int rows, int C, const 
     } else {
       const int word = wstart[lo] + local / 4, byte = local % 4;
       const bool last = brow == bstart[lo + 1] - 1;
-      uint8_t* w = sc + ((size_t)word * C + c) * 4;
 #pragma unroll
       for (int j = 0; j < 2; ++j) {
-        w[4 * j + byte] = static_cast<uint8_t>(sx[j] + 127);
+        uint8_t* w = sc + (((size_t)word * (C / 128) + (c + j) / 128) << 9) + mx_chunk_lane(c + j);
+        w[byte] = static_cast<uint8_t>(sx[j] + 127);
         if (last)
-          for (int b = byte + 1; b < 4; ++b) w[4 * j + b] = 127;
+          for (int b = byte + 1; b < 4; ++b) w[b] = 127;
       }
     }
   }
@@ -147,16 +177,25 @@ quant_cols_kernel(const __nv_bfloat16* __restrict__ src, int rows, int C, const 
 // Quantise before dispatch: each token's row of x is quantised once along d
 // (blocks of 32; lane L owns elements 8L + 256i, so a block is 4 lanes) and
 // the codes and scale bytes are written to the token's k dispatched rows
-// (with x_perm given, the bf16 row too). The bytes equal
-// mxfp8_quantize(x_perm, rows) of the bf16 dispatch.
+// (with x_perm given, the bf16 row too). The codes and scale values equal
+// mxfp8_quantize(x_perm, rows) of the bf16 dispatch; the scales are stored as
+// the GEMM's scale chunks, grouped by per-expert 128-row tiles.
 constexpr int kPermWarps = 8;
 __global__ void __launch_bounds__(kPermWarps * 32)
 permute_quant_kernel(const __nv_bfloat16* __restrict__ x, int T, int d, int k, const int32_t* __restrict__ dest_row,
-                     uint8_t* __restrict__ q, uint8_t* __restrict__ sc, __nv_bfloat16* __restrict__ x_perm) {
+                     const int32_t* __restrict__ topk_idx, const int32_t* __restrict__ offs, uint8_t* __restrict__ q,
+                     uint8_t* __restrict__ sc, __nv_bfloat16* __restrict__ x_perm) {
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * kPermWarps + (threadIdx.x >> 5);
   if (t >= T) return;
-  const int dest = lane < k ? dest_row[(size_t)t * k + lane] : 0;
+  int dest = 0, grp = 0, tt = 0;  // lane j < k: dispatched row j, its scale group and index in it
+  if (lane < k) {
+    dest = dest_row[(size_t)t * k + lane];
+    const int e = topk_idx[(size_t)t * k + lane], o = offs[e];
+    grp = static_cast<int>(mx_row_tile_base(o, e)) + ((dest - o) >> 7);
+    tt = (dest - o) & 127;
+  }
+  const int stages = d / 128;
   for (int cb = 0; cb < d; cb += 256) {  // warp-uniform: every lane reaches the shuffles
     const int c = cb + lane * 8;
     const bool act = c < d;  // d % 32 == 0: a 4-lane block is all in or all out
@@ -186,30 +225,42 @@ permute_quant_kernel(const __nv_bfloat16* __restrict__ x, int T, int d, int k, c
     }
     for (int j = 0; j < k; ++j) {
       const int r = __shfl_sync(0xffffffffu, dest, j);
+      const int g = __shfl_sync(0xffffffffu, grp, j), ti = __shfl_sync(0xffffffffu, tt, j);
       if (!act) continue;
       *reinterpret_cast<uint2*>(q + (size_t)r * d + c) = make_uint2(lo, hi);
       if (x_perm) *reinterpret_cast<uint4*>(x_perm + (size_t)r * d + c) = raw;
-      if ((lane & 3) == 0) sc[(size_t)r * (d / 32) + c / 32] = static_cast<uint8_t>(sx + 127);
+      const int b = c / 32;
+      if ((lane & 3) == 0)
+        sc[(((size_t)g * stages + b / 4) << 9) + mx_chunk_lane(ti) + (b & 3)] = static_cast<uint8_t>(sx + 127);
     }
   }
 }
 
 }  // namespace
 
-cudaError_t launch_permute_quant(const void* x, int T, int d, int k, const int32_t* dest_row, uint8_t* q,
-                                 uint8_t* sc, void* x_perm, cudaStream_t st) {
+cudaError_t launch_permute_quant(const void* x, int T, int d, int k, const int32_t* dest_row,
+                                 const int32_t* topk_idx, const int32_t* offsets, uint8_t* q, uint8_t* sc,
+                                 void* x_perm, cudaStream_t st) {
   if (T == 0) return cudaSuccess;
   MOE_COUNTED permute_quant_kernel<<<(T + kPermWarps - 1) / kPermWarps, kPermWarps * 32, 0, st>>>(
-      static_cast<const __nv_bfloat16*>(x), T, d, k, dest_row, q, sc, static_cast<__nv_bfloat16*>(x_perm));
+      static_cast<const __nv_bfloat16*>(x), T, d, k, dest_row, topk_idx, offsets, q, sc,
+      static_cast<__nv_bfloat16*>(x_perm));
   return cudaGetLastError();
 }
 
-cudaError_t launch_mxfp8_quant_rows(const void* src, long rows, long K, uint8_t* q, uint8_t* sc,
-                                    cudaStream_t st) {
+cudaError_t launch_mxfp8_quant_rows(const void* src, long rows, long K, uint8_t* q, uint8_t* sc, cudaStream_t st,
+                                    int layout, const int32_t* offsets, int E) {
   const long nblocks = rows * (K / 32);
   if (nblocks == 0) return cudaSuccess;
-  MOE_COUNTED quant_rows_kernel<<<static_cast<unsigned>((nblocks + 255) / 256), 256, 0, st>>>(
-      static_cast<const __nv_bfloat16*>(src), nblocks, q, sc);
+  const unsigned grid = static_cast<unsigned>((nblocks + 255) / 256);
+  const auto* s = static_cast<const __nv_bfloat16*>(src);
+  const int kb = static_cast<int>(K / 32);
+  if (layout == kScalesPlain)
+    MOE_COUNTED quant_rows_kernel<kScalesPlain><<<grid, 256, 0, st>>>(s, nblocks, kb, q, sc, offsets, E);
+  else if (layout == kScalesChunk)
+    MOE_COUNTED quant_rows_kernel<kScalesChunk><<<grid, 256, 0, st>>>(s, nblocks, kb, q, sc, offsets, E);
+  else
+    MOE_COUNTED quant_rows_kernel<kScalesTiles><<<grid, 256, 0, st>>>(s, nblocks, kb, q, sc, offsets, E);
   return cudaGetLastError();
 }
 

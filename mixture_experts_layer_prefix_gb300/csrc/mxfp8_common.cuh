@@ -25,6 +25,23 @@ __device__ __forceinline__ float mx_pow2_neg(int s) {
   return ef >= 1 ? __uint_as_float(static_cast<uint32_t>(ef) << 23) : __uint_as_float(1u << 22);
 }
 
+// Scale chunks: the block-scaled GEMMs fetch their E8M0 scales as 512-byte
+// chunks, one per (group of 128 rows or columns of an operand, K stage of 128
+// elements), each already in the order the tensor-memory scale copy takes:
+// the scale of index t of the group (t < 128) for block b of the stage
+// (b < 4) is byte mx_chunk_lane(t) + b. Chunk c starts at byte 512 c.
+__host__ __device__ __forceinline__ uint32_t mx_chunk_lane(int t) {
+  return static_cast<uint32_t>((t & 31) * 16 + ((t >> 5) & 3) * 4);
+}
+// Row operands of the grouped GEMMs are tiled per expert: the m-th 128-row
+// tile of expert e (rows from offs_e) is group mx_row_tile_base(offs_e, e) + m.
+// With base (offs_e + 127 e) / 128 the groups of consecutive experts never
+// overlap (base[e+1] - base[e] >= ceil(rows_e / 128)) and no prefix over the
+// experts is needed.
+__host__ __device__ __forceinline__ long mx_row_tile_base(long offs_e, int e) { return (offs_e + 127L * e) >> 7; }
+// Groups spanned by a row operand of R rows over E experts.
+__host__ __device__ __forceinline__ long mx_row_tiles(long R, int E) { return (R + 127L * E) / 128 + 1; }
+
 // Round-to-nearest-even E4M3 code of v, saturated to +-448.
 __device__ __forceinline__ uint32_t mx_e4m3(float v) {
   return static_cast<uint32_t>(__nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3));

@@ -72,14 +72,17 @@ combine_fwd_kernel(const T* __restrict__ y_perm, const float* __restrict__ gates
 // dy_perm[dest] = g * dy[t];  dgates[t][j] = <dy[t], y_perm[dest]>
 // KMAX: the largest k the instance handles (arrays of per-slot state).
 // QUANT (bf16 only): also write dy_perm's MXFP8 row quantisation (q [T*k][d]
-// E4M3, qsc [T*k][d/32] E8M0) of the bf16-rounded g * dy values -- the bytes
-// mxfp8_quantize(dy_perm, rows) gives -- and dy_perm itself only when given.
+// E4M3; qsc E8M0 as the GEMM's scale chunks, grouped by per-expert 128-row
+// tiles found from topk_idx and offs) of the bf16-rounded g * dy values -- the
+// codes and scales mxfp8_quantize(dy_perm, rows) gives -- and dy_perm itself
+// only when given.
 template <typename T, int KMAX, bool QUANT = false>
 __global__ void __launch_bounds__(kRowWarps * 32)
 combine_bwd_kernel(const T* __restrict__ dy, const T* __restrict__ y_perm,
                    const float* __restrict__ gates, const int32_t* __restrict__ dest_row, int Tn,
                    int d, int k, T* __restrict__ dy_perm, float* __restrict__ dgates, uint8_t* __restrict__ q = nullptr,
-                   uint8_t* __restrict__ qsc = nullptr) {
+                   uint8_t* __restrict__ qsc = nullptr, const int32_t* __restrict__ topk_idx = nullptr,
+                   const int32_t* __restrict__ offs = nullptr) {
   using V = Vec16<T>;
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * kRowWarps + (threadIdx.x >> 5);
@@ -93,6 +96,21 @@ combine_bwd_kernel(const T* __restrict__ dy, const T* __restrict__ y_perm,
     dest[j] = __shfl_sync(0xffffffffu, my_dest, j);
     g[j] = __shfl_sync(0xffffffffu, my_g, j);
     dot[j] = 0.0f;
+  }
+  // QUANT: the scale chunk row of each dispatched row (its per-expert 128-row
+  // tile and its index in the tile)
+  size_t sbase[QUANT ? KMAX : 1];
+  if constexpr (QUANT) {
+    int my_grp = 0, my_t = 0;
+    if (lane < k) {
+      const int e = topk_idx[(size_t)t * k + lane], o = offs[e];
+      my_grp = static_cast<int>(mx_row_tile_base(o, e)) + ((my_dest - o) >> 7);
+      my_t = (my_dest - o) & 127;
+    }
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j)
+      sbase[j] = ((size_t)__shfl_sync(0xffffffffu, my_grp, j) * (d / 128) << 9) +
+                 mx_chunk_lane(__shfl_sync(0xffffffffu, my_t, j));
   }
   // warp-uniform loop (the quantising variant shuffles inside it); lanes past d
   // contribute zeros and store nothing
@@ -135,7 +153,8 @@ combine_bwd_kernel(const T* __restrict__ dy, const T* __restrict__ y_perm,
           }
           if (act) {
             *reinterpret_cast<uint2*>(q + (size_t)dest[j] * d + c) = make_uint2(lo, hi);
-            if ((lane & 3) == 0) qsc[(size_t)dest[j] * (d / 32) + c / 32] = static_cast<uint8_t>(sx + 127);
+            const int b = c / 32;
+            if ((lane & 3) == 0) qsc[sbase[j] + ((size_t)(b / 4) << 9) + (b & 3)] = static_cast<uint8_t>(sx + 127);
             if (dy_perm) V::store(dy_perm + (size_t)dest[j] * d + c, w);
           }
         } else if (act) {
@@ -339,18 +358,19 @@ cudaError_t launch_combine_bwd(const void* dy, const void* y_perm, const float* 
 }
 
 cudaError_t launch_combine_bwd_quant(const void* dy, const void* y_perm, const float* gates,
-                                     const int32_t* dest_row, int Tn, int d, int k, uint8_t* q, uint8_t* qsc,
-                                     void* dy_perm, float* dgates, cudaStream_t st) {
+                                     const int32_t* dest_row, const int32_t* topk_idx, const int32_t* offsets,
+                                     int Tn, int d, int k, uint8_t* q, uint8_t* qsc, void* dy_perm, float* dgates,
+                                     cudaStream_t st) {
   using B = __nv_bfloat16;
   if (Tn == 0) return cudaSuccess;
   if (k <= 4)
     MOE_COUNTED combine_bwd_kernel<B, 4, true><<<row_grid<B>(Tn), kRowWarps * 32, 0, st>>>(
         static_cast<const B*>(dy), static_cast<const B*>(y_perm), gates, dest_row, Tn, d, k, static_cast<B*>(dy_perm),
-        dgates, q, qsc);
+        dgates, q, qsc, topk_idx, offsets);
   else
     MOE_COUNTED combine_bwd_kernel<B, 8, true><<<row_grid<B>(Tn), kRowWarps * 32, 0, st>>>(
         static_cast<const B*>(dy), static_cast<const B*>(y_perm), gates, dest_row, Tn, d, k, static_cast<B*>(dy_perm),
-        dgates, q, qsc);
+        dgates, q, qsc, topk_idx, offsets);
   return cudaGetLastError();
 }
 

@@ -206,11 +206,18 @@ __device__ __forceinline__ void warp_store_rows32(uint8_t* stg, const uint32_t (
   }
   __syncwarp();
 }
+// Scale chunk row of row q * 32 + lane of a row tile, in the per-expert
+// 128-row tile layout of an operand with K = ld (see mxfp8_common.cuh).
+__device__ __forceinline__ size_t tile_scale_row(const Tile& tl, int q, int lane, int ld) {
+  const long grp = mx_row_tile_base(tl.m0 - tl.m_idx * BM, tl.e) + tl.m_idx;
+  return ((size_t)grp * (ld / 128) << 9) + mx_chunk_lane(q * 32 + lane);
+}
 // MXFP8 row quantisation of a 32-column chunk held as packed bf16 pairs (the
-// stored values): codes to qout[row][col..col+32) through the staging buffer,
-// the scale byte of each valid row to qsc[row][col / 32] ([rows][ld] matrix).
+// stored values): codes to qout[row][col..col+32) through the staging buffer
+// ([rows][ld] matrix), the scale byte of each valid row into its scale chunk
+// (srow: the lane's tile_scale_row).
 __device__ __forceinline__ void quant_rows_staged(const Params& p, uint8_t* stg, const uint32_t (&w)[16], int wrow,
-                                                  int nrows, int ld, int col, int lane) {
+                                                  int nrows, int ld, int col, int lane, size_t srow) {
   float amax = 0.0f;
 #pragma unroll
   for (int i = 0; i < 16; ++i)
@@ -224,7 +231,7 @@ __device__ __forceinline__ void quant_rows_staged(const Params& p, uint8_t* stg,
             (mx_e4m3(__uint_as_float(w[2 * i + 1] << 16) * m) << 16) |
             (mx_e4m3(__uint_as_float(w[2 * i + 1] & 0xFFFF0000u) * m) << 24);
   const uint8_t sb = static_cast<uint8_t>(sx + 127);
-  if (lane < nrows) p.qsc[(size_t)(wrow + lane) * (ld / 32) + col / 32] = sb;
+  if (lane < nrows) p.qsc[srow + ((size_t)(col >> 7) << 9) + ((col >> 5) & 3)] = sb;
   warp_store_rows32(stg, cw, p.qout + (size_t)wrow * ld + col, ld, nrows, lane);
 }
 
@@ -297,7 +304,7 @@ __device__ __forceinline__ void epilogue_tile_staged(const Params& p, const Tile
       for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(__uint_as_float(ru[2 * i]), __uint_as_float(ru[2 * i + 1]));
       warp_store_rows(stg, w, h + p.f + n, 2 * (size_t)p.f, nrows, lane);
       warp_store_rows(stg, wa, a + n, p.f, nrows, lane);
-      if (QUANT && p.qout) quant_rows_staged(p, stg, wa, wrow, nrows, p.f, n, lane);
+      if (QUANT && p.qout) quant_rows_staged(p, stg, wa, wrow, nrows, p.f, n, lane, tile_scale_row(tl, q, lane, p.f));
     }
   } else if (KIND == DGRAD2) {
     // dh_g = da * h_u * silu'(h_g), dh_u = da * silu(h_g); the reads of h are
@@ -338,8 +345,9 @@ __device__ __forceinline__ void epilogue_tile_staged(const Params& p, const Tile
       warp_store_rows(stg, w, dh + n, 2 * (size_t)p.f, nrows, lane);
       warp_store_rows(stg, wu, dh + p.f + n, 2 * (size_t)p.f, nrows, lane);
       if (QUANT && p.qout) {
-        quant_rows_staged(p, stg, w, wrow, nrows, 2 * p.f, n, lane);
-        quant_rows_staged(p, stg, wu, wrow, nrows, 2 * p.f, p.f + n, lane);
+        const size_t srow = tile_scale_row(tl, q, lane, 2 * p.f);
+        quant_rows_staged(p, stg, w, wrow, nrows, 2 * p.f, n, lane, srow);
+        quant_rows_staged(p, stg, wu, wrow, nrows, 2 * p.f, p.f + n, lane, srow);
       }
     }
   } else {  // FPROP2, DGRAD1: plain bf16 store

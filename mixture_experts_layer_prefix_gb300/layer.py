@@ -107,8 +107,9 @@ class Buffers:
                                      dtype=torch.uint8, device=device)
         if dtype == N.MOE_MXFP8:  # rows quantised before the dispatch / by the combine backward
             u8 = torch.uint8
-            self.x_q, self.x_sc = z(R, d, dt=u8), z(R, d // 32, dt=u8)
-            self.dy_q, self.dy_sc = z(R, d, dt=u8), z(R, d // 32, dt=u8)
+            nsc = max(1, N.moe_mxfp8_row_scales_size(R, E, d))  # scale chunks by per-expert row tiles
+            self.x_q, self.x_sc = z(R, d, dt=u8), z(nsc, dt=u8)
+            self.dy_q, self.dy_sc = z(R, d, dt=u8), z(nsc, dt=u8)
             # the weights quantised once per step in both K layouts
             self.wq = torch.empty(max(1, N.moe_mxfp8_weights_size(E, d, f)), dtype=u8, device=device)
 
@@ -135,7 +136,7 @@ def forward(p: Params, b: Buffers, logits_in: bool = False, stream=None, fused=N
                 b.dest_row, b.src_row, b.workspace, stream)
     if dt == N.MOE_MXFP8 and mx_pre:
         N.moe_mxfp8_prepare_weights(p.w_gate, p.w_up, p.w_down, E, d, f, b.wq, stream)
-        N.moe_permute_mxfp8(p.x, T, d, k, b.dest_row, b.x_q, b.x_sc, b.x_perm, stream)
+        N.moe_permute_mxfp8(p.x, T, d, k, E, b.dest_row, b.topk_idx, b.offsets, b.x_q, b.x_sc, b.x_perm, stream)
         N.moe_mxfp8_mlp_fwd(b.x_q, b.x_sc, b.wq, b.offsets, b.R, E, d, f, b.h_save, b.a_save, b.y_perm,
                             b.workspace, stream)
     elif fused_default(dt) if fused is None else fused:
@@ -152,8 +153,8 @@ def backward(p: Params, b: Buffers, stream=None, fused=None, mx_pre=True):
     T, d, E, k, f, dt = b.T, b.d, b.E, b.k, b.f, b.dtype
     mx = dt == N.MOE_MXFP8 and mx_pre
     if mx:
-        N.moe_combine_bwd_mxfp8(p.dy, b.y_perm, b.gates, b.dest_row, T, d, k, b.dy_q, b.dy_sc, b.dy_perm, b.dgates,
-                                stream)
+        N.moe_combine_bwd_mxfp8(p.dy, b.y_perm, b.gates, b.dest_row, b.topk_idx, b.offsets, T, d, k, E, b.dy_q,
+                                b.dy_sc, b.dy_perm, b.dgates, stream)
     else:
         N.moe_combine_bwd(p.dy, b.y_perm, b.gates, b.dest_row, dt, T, d, k, b.dy_perm, b.dgates, stream)
     N.moe_route_bwd(b.dgates, b.gates, b.topk_idx, b.offsets, b.src_row, p.x, dt, T, d, E, k,

@@ -105,10 +105,20 @@ def test_route_stats_arguments_rejected_before_launch(lib):
 
 def test_mxfp8_dispatch_arguments_rejected_before_launch(lib):
     L = lib
-    assert L.moe_permute_mxfp8(FAKE, 8, 96, 2, FAKE, FAKE, FAKE, None, None) == 2            # d % 64
-    assert L.moe_permute_mxfp8(FAKE, 8, 64, 2, FAKE, None, FAKE, None, None) == 1            # codes missing
-    assert L.moe_permute_mxfp8(FAKE, 8, 64, 2, FAKE, FAKE, FAKE, FAKE + 4, None) == 3        # x_perm aligned
-    assert L.moe_combine_bwd_mxfp8(FAKE, FAKE, FAKE, FAKE, 8, 64, 9, FAKE, FAKE, None, FAKE, None) == 2  # k > 8
+    F = FAKE
+    assert L.moe_permute_mxfp8(F, 8, 96, 2, 4, F, F, F, F, F, None, None) == 2            # d % 64
+    assert L.moe_permute_mxfp8(F, 8, 320, 2, 4, F, F, F, F, F, None, None) == 2           # d % 128 (scale chunks)
+    assert L.moe_permute_mxfp8(F, 8, 128, 2, 4, F, F, F, None, F, None, None) == 1        # codes missing
+    assert L.moe_permute_mxfp8(F, 8, 128, 2, 4, F, None, F, F, F, None, None) == 1        # topk_idx missing
+    assert L.moe_permute_mxfp8(F, 8, 128, 2, 4, F, F, None, F, F, None, None) == 1        # offsets missing
+    assert L.moe_permute_mxfp8(F, 8, 128, 2, 4, F, F, F, F, F, F + 4, None) == 3          # x_perm aligned
+    assert L.moe_permute_mxfp8(F, 8, 128, 5, 4, F, F, F, F, F, None, None) == 1           # k > E
+    assert L.moe_combine_bwd_mxfp8(F, F, F, F, F, F, 8, 128, 9, 16, F, F, None, F, None) == 2  # k > 8
+    assert L.moe_combine_bwd_mxfp8(F, F, F, F, F, F, 8, 320, 2, 16, F, F, None, F, None) == 2  # d % 128
+    assert L.moe_combine_bwd_mxfp8(F, F, F, F, None, F, 8, 128, 2, 16, F, F, None, F, None) == 1  # topk_idx
+    # scale chunks of a row operand: (R + 127 E) / 128 + 1 groups of 4 K bytes
+    assert L.moe_mxfp8_row_scales_size(1000, 8, 256) == ((1000 + 127 * 8) // 128 + 1) * 4 * 256
+    assert L.moe_mxfp8_row_scales_size(1000, 8, 96) == 0
     # d not a multiple of 128 for the block-scaled GEMMs
     assert L.moe_mxfp8_mlp_fwd(FAKE, FAKE, FAKE, FAKE, 16, 4, 192, 128, FAKE, FAKE, FAKE, FAKE, 1 << 30, None) == 2
     assert L.moe_mxfp8_mlp_bwd(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 16, 4, 128, 128, FAKE, FAKE, FAKE,

@@ -123,51 +123,84 @@ def test_mxfp8_layer_parity(s):
 
 
 # ------------------------------------- quantised where produced (before the dispatch)
-def _dest_rows(T, k, seed):
+def _routing(T, k, E, seed):
+    """A valid routing (k distinct experts per token, rows of each expert in
+    token order, as moe_route lays them out): topk_idx, dest_row, offsets."""
     rng = np.random.default_rng(seed)
-    return rng.permutation(T * k).astype(np.int32).reshape(T, k)
+    idx = np.argsort(rng.random((T, E)), axis=1)[:, :k].astype(np.int32)
+    counts = np.bincount(idx.ravel(), minlength=E)
+    offs = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    dest = np.empty((T, k), np.int32)
+    fill = offs[:-1].copy()
+    for t in range(T):
+        for j in range(k):
+            dest[t, j] = fill[idx[t, j]]
+            fill[idx[t, j]] += 1
+    return idx, dest, offs
 
 
-@pytest.mark.parametrize("T,d,k", [(777, 320, 3), (64, 2048, 8), (1, 64, 1)])
-def test_permute_mxfp8_bytes(T, d, k):
+def _unchunk(sc, offs, K):
+    """[R][K/32] scale bytes from the scale-chunk layout that include/moe.h
+    documents for row operands (per-expert 128-row tiles)."""
+    R, E = int(offs[-1]), len(offs) - 1
+    r = np.arange(R)
+    e = np.searchsorted(offs, r, side="right") - 1
+    loc = r - offs[e]
+    grp = (offs[e] + 127 * e) // 128 + loc // 128
+    t = loc % 128
+    b = np.arange(K // 32)
+    byte = (512 * (grp[:, None] * (K // 128) + b[None, :] // 4) + 16 * (t[:, None] % 32)
+            + 4 * ((t[:, None] // 32) % 4) + b[None, :] % 4)
+    return sc[byte]
+
+
+@pytest.mark.parametrize("T,d,k,E", [(777, 384, 3, 5), (64, 2048, 8, 8), (1, 128, 1, 4), (300, 256, 2, 64)])
+def test_permute_mxfp8_bytes(T, d, k, E):
     """The fused dispatch + row quantisation writes, at row dest_row[t][j], the
-    oracle's row quantisation of x[t] (d=320: a partial last 256-column pass)."""
+    oracle's row quantisation of x[t]; its scales land in the documented scale
+    chunks (d=384: a partial last 256-column pass; E=64 at T=300: empty experts
+    and experts of one tile)."""
     v = _values(T, d, T + d)
-    dest = _dest_rows(T, k, 5)
-    q = torch.zeros((T * k, d), dtype=torch.uint8, device="cuda")
-    s = torch.zeros((T * k, d // 32), dtype=torch.uint8, device="cuda")
-    xp = torch.zeros((T * k, d), dtype=torch.bfloat16, device="cuda")
-    N.moe_permute_mxfp8(_dev(v), T, d, k, torch.from_numpy(dest).cuda(), q, s, xp)
+    idx, dest, offs = _routing(T, k, E, 5)
+    R = T * k
+    q = torch.zeros((R, d), dtype=torch.uint8, device="cuda")
+    s = torch.zeros(N.moe_mxfp8_row_scales_size(R, E, d), dtype=torch.uint8, device="cuda")
+    xp = torch.zeros((R, d), dtype=torch.bfloat16, device="cuda")
+    N.moe_permute_mxfp8(_dev(v), T, d, k, E, torch.from_numpy(dest).cuda(), torch.from_numpy(idx).cuda(),
+                        torch.from_numpy(offs).cuda(), q, s, xp)
     torch.cuda.synchronize()
     rq, rs = oracle.mxfp8_quantize_rows(v)
     inv = np.argsort(dest.ravel()) // k  # token of each dispatched row
     np.testing.assert_array_equal(q.cpu().numpy(), rq[inv])
-    np.testing.assert_array_equal(s.cpu().numpy(), rs[inv])
+    np.testing.assert_array_equal(_unchunk(s.cpu().numpy(), offs, d), rs[inv])
     np.testing.assert_array_equal(xp.float().cpu().numpy(), v[inv])  # the bf16 dispatch, exact
 
 
-@pytest.mark.parametrize("T,d,k", [(500, 320, 4), (33, 1024, 8)])
-def test_combine_bwd_mxfp8_bytes(T, d, k):
+@pytest.mark.parametrize("T,d,k,E", [(500, 384, 4, 6), (33, 1024, 8, 8)])
+def test_combine_bwd_mxfp8_bytes(T, d, k, E):
     """The quantising combine backward writes the oracle's row quantisation of
-    the bf16 dy_perm that moe_combine_bwd stores, and the same dgates bits."""
+    the bf16 dy_perm that moe_combine_bwd stores (scales in the documented
+    scale chunks), and the same dgates bits."""
     rng = np.random.default_rng(T)
     dy = _dev(synth.round_bf16(rng.standard_normal((T, d)).astype(np.float32)))
     y_perm = _dev(synth.round_bf16(rng.standard_normal((T * k, d)).astype(np.float32)))
     g = torch.from_numpy(rng.random((T, k)).astype(np.float32)).cuda()
-    dest = torch.from_numpy(_dest_rows(T, k, 9)).cuda()
+    idx, dest_np, offs = _routing(T, k, E, 9)
+    dest = torch.from_numpy(dest_np).cuda()
     dy_perm = torch.empty((T * k, d), dtype=torch.bfloat16, device="cuda")
     dg0 = torch.empty((T, k), dtype=torch.float32, device="cuda")
     N.moe_combine_bwd(dy, y_perm, g, dest, N.MOE_BF16, T, d, k, dy_perm, dg0)
     q = torch.zeros((T * k, d), dtype=torch.uint8, device="cuda")
-    s = torch.zeros((T * k, d // 32), dtype=torch.uint8, device="cuda")
+    s = torch.zeros(N.moe_mxfp8_row_scales_size(T * k, E, d), dtype=torch.uint8, device="cuda")
     dg1 = torch.empty_like(dg0)
     dy_perm1 = torch.zeros_like(dy_perm)
-    N.moe_combine_bwd_mxfp8(dy, y_perm, g, dest, T, d, k, q, s, dy_perm1, dg1)
+    N.moe_combine_bwd_mxfp8(dy, y_perm, g, dest, torch.from_numpy(idx).cuda(), torch.from_numpy(offs).cuda(), T, d,
+                            k, E, q, s, dy_perm1, dg1)
     torch.cuda.synchronize()
     assert torch.equal(dy_perm1, dy_perm)
     rq, rs = oracle.mxfp8_quantize_rows(dy_perm.float().cpu().numpy())
     np.testing.assert_array_equal(q.cpu().numpy(), rq)
-    np.testing.assert_array_equal(s.cpu().numpy(), rs)
+    np.testing.assert_array_equal(_unchunk(s.cpu().numpy(), offs, d), rs)
     assert torch.equal(dg0, dg1)
 
 

@@ -14,7 +14,8 @@
 //               masks; two warps per TMEM lane quadrant, each half the columns.
 // Tiles are enumerated on the device from the expert offsets (the host never
 // sees the per-expert counts): forward/dgrad tiles cover 128 routed rows of
-// one expert (rows past the expert's end are computed and not stored);
+// one expert -- 256 for GEMM2 and the GEMM1 dgrad (tc_row256_kernel) -- and
+// rows past the expert's end are computed and not stored;
 // wgrad tiles cover a 128x256 block of one expert's weight gradient and
 // reduce over that expert's rows (a ragged K; the rows past its end are
 // zeroed in shared memory before the MMA; an expert with no rows gets zeros).
@@ -291,6 +292,202 @@ cudaError_t launch(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMa
   if (e != cudaSuccess) return e;
   const int grid = static_cast<int>(max_tiles < sm_count() ? max_tiles : sm_count());
   MOE_COUNTED tc_gemm_kernel<KIND, GATHER><<<grid, NUM_THREADS, smem, st>>>(a, b0, b1, p);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// GEMM2 forward and the GEMM1 dgrad (plain bf16 epilogues) in 256-row tiles.
+// The row-tile GEMMs are bound by the operand stream from L2, not by the
+// tensor pipe: a 128x256 tile moves 48 KB per 4.2 MFLOP. Here two 128-row
+// halves of A share each B stage (64 KB per 8.4 MFLOP, 1.5x less traffic per
+// FLOP); both 256-column fp32 accumulators fill TMEM, so the epilogue drains
+// them into registers as packed bf16 and releases TMEM before it stores,
+// while the producer already streams the next tile. A tile whose second half
+// holds no rows of its expert loads one A box and issues half the MMAs, so
+// the padding per expert stays below 128 rows.
+constexpr int RBM = 256;
+constexpr int R_A_BYTES = RBM * BK * 2;       // two 128-row K-major boxes
+constexpr int R_STAGE = R_A_BYTES + B_BYTES;  // 64 KB
+constexpr int R_NS = 3;
+
+template <int KIND>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+tc_row256_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
+                 const __grid_constant__ CUtensorMap tmB1, const Params p) {
+  static_assert(KIND == FPROP2 || KIND == DGRAD1, "plain-store row kinds");
+  using Tr = Traits<KIND>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* out_stage = smem + R_NS * R_STAGE;
+  Smem* sm = reinterpret_cast<Smem*>(out_stage + OUT_STG_BYTES);
+  int* offs = reinterpret_cast<int*>(sm + 1);
+  int* tstart = offs + (p.E + 1);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  build_tile_table<KIND, NUM_THREADS, RBM>(p, offs, tstart);
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < R_NS; ++s) {
+      ptx::mbar_init(&sm->full[s], 1);
+      ptx::mbar_init(&sm->empty[s], 1);
+    }
+    ptx::mbar_init(&sm->tfull[0], 1);
+    ptx::mbar_init(&sm->tempty[0], NUM_EPI_WARPS);
+    ptx::mbar_init(&sm->drain, 1);
+    sm->abort_flag = 0;
+    ptx::fence_mbar_init();
+    ptx::fence_proxy_async_smem();
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(&sm->tmem_base, TMEM_COLS);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const int total = tstart[p.E];
+  const uint32_t tmem = sm->tmem_base;
+
+  if (warp == 0) {
+    // ===================================================== TMA producer
+    if (lane == 0) {
+      ptx::prefetch_tmap(&tmA);
+      ptx::prefetch_tmap(&tmB0);
+      ptx::prefetch_tmap(&tmB1);
+      uint32_t it = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+        const Tile tl = decode<KIND, BK, RBM>(t, p, offs, tstart);
+        const bool two = tl.m0 + BM < tl.row_end;  // the second 128-row half holds rows
+        for (int kb = 0; kb < tl.nkb; ++kb, ++it) {
+          const int s = it % R_NS;
+          const uint32_t ph = (it / R_NS) & 1u;
+          if (!wait_bar(&sm->empty[s], ph ^ 1u, &sm->abort_flag, p.err)) { ok = false; break; }
+          uint8_t* a = smem + s * R_STAGE;
+          uint8_t* b = a + R_A_BYTES;
+          uint64_t* fb = &sm->full[s];
+          ptx::mbar_expect_tx(fb, (two ? R_A_BYTES : A_BYTES) + B_BYTES);
+          const int k0 = kb * BK;
+          ptx::tma_load_2d(a, &tmA, fb, k0, tl.m0);
+          if (two) ptx::tma_load_2d(a + A_BYTES, &tmA, fb, k0, tl.m0 + BM);
+          if (KIND == FPROP2) {
+            const int n0 = tl.n_idx * BN;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) ptx::tma_load_3d(b + j * BOX_BYTES, &tmB0, fb, n0 + 64 * j, k0, tl.e);
+          } else {  // DGRAD1: w_gate rows for K < f, then w_up's
+            if (k0 < p.f) ptx::tma_load_3d(b, &tmB0, fb, k0, tl.n_idx * BN, tl.e);
+            else ptx::tma_load_3d(b, &tmB1, fb, k0 - p.f, tl.n_idx * BN, tl.e);
+          }
+        }
+      }
+      if (!ok) {
+        for (int s = 0; s < R_NS; ++s) {
+          const long long t0 = clock64();
+          while (clock64() - t0 < kWaitLimitCycles / 8 && !ptx::mbar_try_wait(&sm->full[s], 0) &&
+                 !ptx::mbar_try_wait(&sm->full[s], 1)) {
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ========================================================= MMA issuer
+    constexpr uint32_t idesc = ptx::idesc_bf16_f32(BM, BN, Tr::a_mn ? 1 : 0, Tr::b_mn ? 1 : 0);
+    uint32_t it = 0, acc_it = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+      const Tile tl = decode<KIND, BK, RBM>(t, p, offs, tstart);
+      const int halves = tl.m0 + BM < tl.row_end ? 2 : 1;
+      if (!wait_bar(&sm->tempty[0], (acc_it & 1u) ^ 1u, &sm->abort_flag, p.err)) { ok = false; break; }
+      ptx::tc_fence_after();
+      for (int kb = 0; kb < tl.nkb; ++kb, ++it) {
+        const int s = it % R_NS;
+        const uint32_t ph = (it / R_NS) & 1u;
+        if (!wait_bar(&sm->full[s], ph, &sm->abort_flag, p.err)) { ok = false; break; }
+        ptx::tc_fence_after();
+        if (lane == 0) {
+          const uint32_t a_addr = ptx::smem_u32(smem + s * R_STAGE), b_addr = a_addr + R_A_BYTES;
+          for (int ks = 0; ks < BK / 16; ++ks) {
+            const uint64_t bd = Tr::b_mn ? ptx::smem_desc_sw128(b_addr + ks * 2048, BOX_BYTES, 1024)
+                                         : ptx::smem_desc_sw128(b_addr + ks * 32, 16, 1024);
+            for (int h = 0; h < halves; ++h) {
+              const uint64_t ad = ptx::smem_desc_sw128(a_addr + h * A_BYTES + ks * 32, 16, 1024);
+              ptx::mma_f16(tmem + h * BN, ad, bd, idesc, (kb > 0 || ks > 0) ? 1u : 0u);
+            }
+          }
+          ptx::mma_commit(&sm->empty[s]);
+        }
+        __syncwarp();
+      }
+      if (!ok) break;
+      if (lane == 0) ptx::mma_commit(&sm->tfull[0]);
+      __syncwarp();
+      ++acc_it;
+    }
+    if (!ok && lane == 0) {
+      ptx::mma_commit(&sm->drain);
+      const long long t0 = clock64();
+      while (clock64() - t0 < kWaitLimitCycles / 8 && !ptx::mbar_try_wait(&sm->drain, 0)) {
+      }
+    }
+  } else {
+    // ============================================================ epilogue
+    // warps 2..5 take rows 0..127 of the tile (accumulator 0), warps 6..9 rows
+    // 128..255 (accumulator 1); lane = row. Each thread moves its 256-column
+    // row into registers as packed bf16, TMEM is handed back, then the rows go
+    // out 32 columns at a time through the warp's staging buffer.
+    const int ew = warp - 2, q = warp & 3, mh = ew >> 2;
+    uint8_t* stg = out_stage + ew * STG_BYTES;
+    uint32_t acc_it = 0;
+    for (int t = blockIdx.x; t < total; t += gridDim.x) {
+      const Tile tl = decode<KIND, BK, RBM>(t, p, offs, tstart);
+      const bool mine = mh == 0 || tl.m0 + BM < tl.row_end;
+      if (!wait_bar(&sm->tfull[0], acc_it & 1u, &sm->abort_flag, p.err)) break;
+      ptx::tc_fence_after();
+      uint32_t hold[BN / 32][16];
+      if (mine) {
+        const uint32_t tbase = tmem + static_cast<uint32_t>(mh * BN) + (static_cast<uint32_t>(q * 32) << 16);
+#pragma unroll
+        for (int c = 0; c < BN / 16; ++c) {  // 16 columns at a time keeps the drain within the register budget
+          uint32_t r[16];
+          ptx::tmem_ld16(tbase + c * 16, r);
+          ptx::tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            hold[c >> 1][(c & 1) * 8 + i] = pack_bf16x2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
+        }
+      }
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&sm->tempty[0]);
+      ++acc_it;
+      if (!mine) continue;
+      const int wrow = tl.m0 + mh * BM + q * 32;
+      const int nrows = max(0, min(32, tl.row_end - wrow));
+      __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out0) + (size_t)wrow * p.N + tl.n_idx * BN;
+#pragma unroll
+      for (int c = 0; c < BN / 32; ++c)
+        if (tl.n_idx * BN + c * 32 < p.N) warp_store_rows(stg, hold[c], out + c * 32, p.N, nrows, lane);
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+template <int KIND>
+cudaError_t launch_row256(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1, const Params& p,
+                          int R, cudaStream_t st) {
+  const long max_tiles = ((long)(R + RBM - 1) / RBM + p.E) * p.n_tiles;
+  if (R <= 0 || max_tiles <= 0) return cudaSuccess;
+  const size_t smem = 1024 + R_NS * R_STAGE + OUT_STG_BYTES + sizeof(Smem) + 2 * (p.E + 1) * sizeof(int) + 64;
+  cudaError_t e = cudaFuncSetAttribute(tc_row256_kernel<KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  const int grid = static_cast<int>(max_tiles < sm_count() ? max_tiles : sm_count());
+  MOE_COUNTED tc_row256_kernel<KIND><<<grid, NUM_THREADS, smem, st>>>(a, b0, b1, p);
   return cudaGetLastError();
 }
 
@@ -681,7 +878,7 @@ cudaError_t tc_mlp_fwd(const void* x_perm, const void* wg, const void* wu, const
   if (!map_2d(&mA, a, BF, 2, f, R, 64, BM) || !map_3d(&mB0, wd, BF, 2, d, f, E, 64, 64))
     return cudaErrorInvalidValue;
   p.N = d; p.n_tiles = (d + BN - 1) / BN; p.out0 = y; p.out1 = nullptr;
-  return launch<FPROP2>(mA, mB0, mB0, p, ((long)(R + BM - 1) / BM + E) * p.n_tiles, st);
+  return launch_row256<FPROP2>(mA, mB0, mB0, p, R, st);
 }
 
 cudaError_t tc_mlp_bwd(const void* dy_perm, const void* x_perm, const void* h, const void* a, const void* wg,
@@ -709,7 +906,7 @@ cudaError_t tc_mlp_bwd(const void* dy_perm, const void* x_perm, const void* h, c
       !map_3d(&mB1, wu, BF, 2, f, d, E, 64, BN))
     return cudaErrorInvalidValue;
   p.N = d; p.n_tiles = (d + BN - 1) / BN; p.out0 = dx_perm; p.aux = nullptr;
-  e = launch<DGRAD1>(mA, mB0, mB1, p, ((long)(R + BM - 1) / BM + E) * p.n_tiles, st);
+  e = launch_row256<DGRAD1>(mA, mB0, mB1, p, R, st);
   if (e != cudaSuccess) return e;
   // [dWg | dWu][e] = x_perm_e^T dh_e (with src_row: K rows gathered from x [T][d])
   const bool ok_a = src_row ? map_2d(&mA, x_perm, BF, 2, d, T, 64, 1) : map_2d(&mA, x_perm, BF, 2, d, R, 64, 64);

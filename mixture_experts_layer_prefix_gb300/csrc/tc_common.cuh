@@ -86,7 +86,7 @@ __device__ __forceinline__ int gemm_k(const Params& p) {
 // Decode linear tile t. Row-ragged: expert e owns tstart[e]..tstart[e+1]
 // (m-tiles x n-tiles, n fastest). K-ragged: every expert owns m_tiles x
 // n_tiles tiles and its K loop runs over its rows, BK rows per stage.
-template <int KIND, int BK>
+template <int KIND, int BK, int TBM = BM>
 __device__ __forceinline__ Tile decode(int t, const Params& p, const int* offs, const int* tstart) {
   Tile tl;
   if (!Traits<KIND>::kragged) {
@@ -99,7 +99,7 @@ __device__ __forceinline__ Tile decode(int t, const Params& p, const int* offs, 
     tl.e = e;
     tl.m_idx = local / p.n_tiles;
     tl.n_idx = local % p.n_tiles;
-    tl.m0 = offs[e] + tl.m_idx * BM;
+    tl.m0 = offs[e] + tl.m_idx * TBM;
     tl.row_end = offs[e + 1];
     tl.nkb = gemm_k<KIND>(p) / BK;
     tl.k_row0 = 0;
@@ -119,7 +119,7 @@ __device__ __forceinline__ Tile decode(int t, const Params& p, const int* offs, 
 
 // Offsets into shared memory and (row-ragged kinds) the per-expert tile
 // prefix table; called by all threads of the CTA, ends with __syncthreads.
-template <int KIND, int NTHREADS>
+template <int KIND, int NTHREADS, int TBM = BM>
 __device__ __forceinline__ void build_tile_table(const Params& p, int* offs, int* tstart) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (p.offsets) {
@@ -134,7 +134,7 @@ __device__ __forceinline__ void build_tile_table(const Params& p, int* offs, int
     for (int base = 0; base < p.E; base += 32) {
       const int e = base + lane;
       const int cnt = e < p.E ? offs[e + 1] - offs[e] : 0;
-      const int v = ((cnt + BM - 1) / BM) * p.n_tiles;
+      const int v = ((cnt + TBM - 1) / TBM) * p.n_tiles;
       int incl = v;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {

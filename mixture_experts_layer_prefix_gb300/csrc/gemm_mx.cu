@@ -683,14 +683,11 @@ cudaError_t mx_prepare_weights(const void* wg, const void* wu, const void* wd, i
   const tc::mx::MxWeights w = tc::mx::carve_weights(wq, E, d, f);
   const int Ed = E * d, Ef = E * f;
   cudaError_t e;
-  // columns: blocks of 32 rows (K stages never cross experts as d, f are
-  // multiples of 128); rows: blocks of 32 columns; scales as scale chunks
-  if ((e = launch_mxfp8_quant_cols(wg, Ed, f, nullptr, 1, w.wg_c.q, w.wg_c.s, st, true)) != cudaSuccess) return e;
-  if ((e = launch_mxfp8_quant_cols(wu, Ed, f, nullptr, 1, w.wu_c.q, w.wu_c.s, st, true)) != cudaSuccess) return e;
-  if ((e = launch_mxfp8_quant_cols(wd, Ef, d, nullptr, 1, w.wd_c.q, w.wd_c.s, st, true)) != cudaSuccess) return e;
-  if ((e = launch_mxfp8_quant_rows(wd, Ef, d, w.wd_r.q, w.wd_r.s, st, kScalesChunk)) != cudaSuccess) return e;
-  if ((e = launch_mxfp8_quant_rows(wg, Ed, f, w.wg_r.q, w.wg_r.s, st, kScalesChunk)) != cudaSuccess) return e;
-  return launch_mxfp8_quant_rows(wu, Ed, f, w.wu_r.q, w.wu_r.s, st, kScalesChunk);
+  // one read per weight: columns (blocks of 32 rows; K stages never cross
+  // experts as d, f are multiples of 128) and rows (blocks of 32 columns)
+  if ((e = launch_mxfp8_quant_dual(wg, Ed, f, w.wg_c.q, w.wg_c.s, w.wg_r.q, w.wg_r.s, st)) != cudaSuccess) return e;
+  if ((e = launch_mxfp8_quant_dual(wu, Ed, f, w.wu_c.q, w.wu_c.s, w.wu_r.q, w.wu_r.s, st)) != cudaSuccess) return e;
+  return launch_mxfp8_quant_dual(wd, Ef, d, w.wd_c.q, w.wd_c.s, w.wd_r.q, w.wd_r.s, st);
 }
 size_t mx_bwd_workspace(long R, int E, int d, int f) { return tc::mx::bwd_workspace(R, E, d, f); }
 

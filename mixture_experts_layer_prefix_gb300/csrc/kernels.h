@@ -101,6 +101,11 @@ cudaError_t launch_mxfp8_quant_rows(const void* src, long rows, long K, uint8_t*
 // block, [blocks][C] (public layout).
 cudaError_t launch_mxfp8_quant_cols(const void* src, int rows, int C, const int32_t* seg, int nseg,
                                     uint8_t* q, uint8_t* sc, cudaStream_t st, bool packed = false);
+// A weight [rows][C] (rows and C multiples of 128) quantised along its
+// columns (qc, sc_c: the packed quant_cols layout) and along its rows (qr,
+// sc_r: kScalesChunk) from one read.
+cudaError_t launch_mxfp8_quant_dual(const void* src, long rows, int C, uint8_t* qc, uint8_t* sc_c, uint8_t* qr,
+                                    uint8_t* sc_r, cudaStream_t st);
 // Dispatch with the row quantisation fused: q [T*k][d], sc as scale chunks
 // grouped by per-expert 128-row tiles; the bf16 x_perm too when given.
 cudaError_t launch_permute_quant(const void* x, int T, int d, int k, const int32_t* dest_row,

@@ -18,6 +18,8 @@
 //                conversion.
 #include <cuda_fp8.h>
 
+#include <algorithm>
+
 #include "common.cuh"
 #include "kernels.h"
 #include "mxfp8_common.cuh"
@@ -27,7 +29,6 @@ namespace {
 
 __device__ __forceinline__ int e8m0_exponent(float amax) { return mx_e8m0_exponent(amax); }
 __device__ __forceinline__ float pow2_neg(int s) { return mx_pow2_neg(s); }
-__device__ __forceinline__ uint32_t e4m3(float v) { return mx_e4m3(v); }
 
 // MODE (ScaleLayout): where the scale byte of block b of row r goes.
 template <int MODE>
@@ -153,7 +154,7 @@ quant_cols_kernel(const __nv_bfloat16* __restrict__ src, int rows, int C, const 
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
       if (i < nr) {
-        const uint32_t b = e4m3(__uint_as_float(blk[i] << 16) * m0) | e4m3(__uint_as_float(blk[i] & 0xFFFF0000u) * m1) << 8;
+        const uint32_t b = mx_e4m3x2(__uint_as_float(blk[i] << 16) * m0, __uint_as_float(blk[i] & 0xFFFF0000u) * m1);
         qp[i * ch] = static_cast<uint16_t>(b);
       }
     }
@@ -172,6 +173,92 @@ quant_cols_kernel(const __nv_bfloat16* __restrict__ src, int rows, int C, const 
       }
     }
   }
+}
+
+// Weights in both K layouts from one read: a CTA stages a 32-row x 128-column
+// tile of W [rows][C] in shared memory and writes it quantised along its
+// columns (blocks of 32 rows: codes qc, scale chunks sc_c grouped by 128-row
+// K stage x 128-column group) and along its rows (blocks of 32 columns:
+// codes qr, scale chunks sc_r grouped by 128-row group x 128-column K stage).
+// rows and C are multiples of 128, so no block crosses a weight matrix. CTAs
+// stride over the tiles (those of one 32-row band are consecutive, so W is
+// read in order) with the next tile's cp.async copies in flight while the
+// current one is converted. The bytes equal those of the separate column and
+// row quantisers.
+constexpr int kDualCols = 128, kDualPitch = kDualCols + 8;  // bf16 per staged row (16-byte pad)
+constexpr int kDualTile = 32 * kDualPitch;
+__global__ void __launch_bounds__(128)
+quant_dual_kernel(const __nv_bfloat16* __restrict__ src, int C, long ntiles, uint8_t* __restrict__ qc,
+                  uint8_t* __restrict__ sc_c, uint8_t* __restrict__ qr, uint8_t* __restrict__ sc_r) {
+  __shared__ __align__(16) __nv_bfloat16 tile[2 * kDualTile];
+  const int tid = threadIdx.x;
+  const int cg = C / kDualCols;
+  auto issue = [&](long t, int buf) {  // a half-warp copies one 256-byte row segment per step
+    const long row0 = t / cg * 32;
+    const int c0 = static_cast<int>(t % cg) * kDualCols;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int id = tid + 128 * i, r = id >> 4, g = id & 15;
+      const __nv_bfloat16* gp = src + (row0 + r) * C + c0 + 8 * g;
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(static_cast<uint32_t>(
+                       __cvta_generic_to_shared(tile + buf * kDualTile + r * kDualPitch + 8 * g))),
+                   "l"(gp)
+                   : "memory");
+    }
+  };
+  long t = blockIdx.x;
+  if (t < ntiles) issue(t, 0);
+  asm volatile("cp.async.commit_group;" ::: "memory");
+  for (int it = 0; t < ntiles; t += gridDim.x, ++it) {
+    if (t + gridDim.x < ntiles) issue(t + gridDim.x, (it + 1) & 1);
+    asm volatile("cp.async.commit_group;" ::: "memory");
+    asm volatile("cp.async.wait_group 1;" ::: "memory");  // this tile's copies have landed
+    __syncthreads();
+    const __nv_bfloat16* tl = tile + (it & 1) * kDualTile;
+    const long row0 = t / cg * 32;
+    const int c0 = static_cast<int>(t % cg) * kDualCols;
+    {  // along the columns: this thread's column over the 32 rows
+      float v[32], amax = 0.0f;
+#pragma unroll
+      for (int r = 0; r < 32; ++r) {
+        v[r] = __bfloat162float(tl[r * kDualPitch + tid]);
+        amax = fmaxf(amax, fabsf(v[r]));
+      }
+      const int sx = e8m0_exponent(amax);
+      const float m = pow2_neg(sx);
+#pragma unroll
+      for (int r = 0; r < 32; r += 2) {
+        const uint32_t b = mx_e4m3x2(v[r] * m, v[r + 1] * m);
+        qc[(row0 + r) * C + c0 + tid] = static_cast<uint8_t>(b);
+        qc[(row0 + r + 1) * C + c0 + tid] = static_cast<uint8_t>(b >> 8);
+      }
+      sc_c[(((row0 >> 7) * cg + c0 / 128) << 9) + mx_chunk_lane(tid) + ((row0 >> 5) & 3)] =
+          static_cast<uint8_t>(sx + 127);
+    }
+    {  // along the rows: block (row r, 32 columns cb); lanes are rows
+      const int r = tid & 31, cb = tid >> 5;
+      float v[32];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint4 u = *reinterpret_cast<const uint4*>(tl + r * kDualPitch + 32 * cb + 8 * i);
+        const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          v[8 * i + 2 * k] = __uint_as_float(w4[k] << 16);
+          v[8 * i + 2 * k + 1] = __uint_as_float(w4[k] & 0xFFFF0000u);
+        }
+      }
+      uint32_t cw[8];
+      const uint8_t sb = mx_quant_block32_regs(v, cw);
+      const long row = row0 + r;
+      uint4* out = reinterpret_cast<uint4*>(qr + row * C + c0 + 32 * cb);
+      out[0] = make_uint4(cw[0], cw[1], cw[2], cw[3]);
+      out[1] = make_uint4(cw[4], cw[5], cw[6], cw[7]);
+      sc_r[(((row >> 7) * cg + c0 / 128) << 9) + mx_chunk_lane(static_cast<int>(row & 127)) + cb] = sb;
+    }
+    __syncthreads();  // the buffer is refilled two tiles on
+  }
+  asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
 // Quantise before dispatch: each token's row of x is quantised once along d
@@ -217,12 +304,8 @@ permute_quant_kernel(const __nv_bfloat16* __restrict__ x, int T, int d, int k, c
     amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
     const int sx = e8m0_exponent(amax);
     const float m = pow2_neg(sx);
-    uint32_t lo = 0, hi = 0;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      lo |= e4m3(v[i] * m) << (8 * i);
-      hi |= e4m3(v[4 + i] * m) << (8 * i);
-    }
+    const uint32_t lo = mx_e4m3x2(v[0] * m, v[1] * m) | mx_e4m3x2(v[2] * m, v[3] * m) << 16;
+    const uint32_t hi = mx_e4m3x2(v[4] * m, v[5] * m) | mx_e4m3x2(v[6] * m, v[7] * m) << 16;
     for (int j = 0; j < k; ++j) {
       const int r = __shfl_sync(0xffffffffu, dest, j);
       const int g = __shfl_sync(0xffffffffu, grp, j), ti = __shfl_sync(0xffffffffu, tt, j);
@@ -261,6 +344,16 @@ cudaError_t launch_mxfp8_quant_rows(const void* src, long rows, long K, uint8_t*
     MOE_COUNTED quant_rows_kernel<kScalesChunk><<<grid, 256, 0, st>>>(s, nblocks, kb, q, sc, offsets, E);
   else
     MOE_COUNTED quant_rows_kernel<kScalesTiles><<<grid, 256, 0, st>>>(s, nblocks, kb, q, sc, offsets, E);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_mxfp8_quant_dual(const void* src, long rows, int C, uint8_t* qc, uint8_t* sc_c, uint8_t* qr,
+                                    uint8_t* sc_r, cudaStream_t st) {
+  if (rows == 0) return cudaSuccess;
+  const long ntiles = rows / 32 * (C / kDualCols);
+  const long grid = std::min<long>(ntiles, (long)tc::sm_count() * 10);
+  MOE_COUNTED quant_dual_kernel<<<static_cast<unsigned>(grid), 128, 0, st>>>(static_cast<const __nv_bfloat16*>(src), C,
+                                                                           ntiles, qc, sc_c, qr, sc_r);
   return cudaGetLastError();
 }
 

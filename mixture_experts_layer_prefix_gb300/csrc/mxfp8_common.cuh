@@ -42,9 +42,10 @@ __host__ __device__ __forceinline__ long mx_row_tile_base(long offs_e, int e) { 
 // Groups spanned by a row operand of R rows over E experts.
 __host__ __device__ __forceinline__ long mx_row_tiles(long R, int E) { return (R + 127L * E) / 128 + 1; }
 
-// Round-to-nearest-even E4M3 code of v, saturated to +-448.
-__device__ __forceinline__ uint32_t mx_e4m3(float v) {
-  return static_cast<uint32_t>(__nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3));
+// Round-to-nearest-even E4M3 codes of v0 (low byte) and v1 (high byte),
+// saturated to +-448, from one paired conversion.
+__device__ __forceinline__ uint32_t mx_e4m3x2(float v0, float v1) {
+  return static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(make_float2(v0, v1), __NV_SATFINITE, __NV_E4M3));
 }
 
 // Quantise one block of 32 values into 32 E4M3 codes (w, little-endian
@@ -57,8 +58,7 @@ __device__ __forceinline__ uint8_t mx_quant_block32_regs(const float* v, uint32_
   const float m = mx_pow2_neg(s);
 #pragma unroll
   for (int i = 0; i < 8; ++i)
-    w[i] = mx_e4m3(v[4 * i] * m) | (mx_e4m3(v[4 * i + 1] * m) << 8) | (mx_e4m3(v[4 * i + 2] * m) << 16) |
-           (mx_e4m3(v[4 * i + 3] * m) << 24);
+    w[i] = mx_e4m3x2(v[4 * i] * m, v[4 * i + 1] * m) | (mx_e4m3x2(v[4 * i + 2] * m, v[4 * i + 3] * m) << 16);
   return static_cast<uint8_t>(s + 127);
 }
 

@@ -145,12 +145,8 @@ combine_bwd_kernel(const T* __restrict__ dy, const T* __restrict__ y_perm,
           amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
           const int sx = mx_e8m0_exponent(amax);
           const float m = mx_pow2_neg(sx);
-          uint32_t lo = 0, hi = 0;
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            lo |= mx_e4m3(w[i] * m) << (8 * i);
-            hi |= mx_e4m3(w[4 + i] * m) << (8 * i);
-          }
+          const uint32_t lo = mx_e4m3x2(w[0] * m, w[1] * m) | mx_e4m3x2(w[2] * m, w[3] * m) << 16;
+          const uint32_t hi = mx_e4m3x2(w[4] * m, w[5] * m) | mx_e4m3x2(w[6] * m, w[7] * m) << 16;
           if (act) {
             *reinterpret_cast<uint2*>(q + (size_t)dest[j] * d + c) = make_uint2(lo, hi);
             const int b = c / 32;

@@ -227,9 +227,8 @@ __device__ __forceinline__ void quant_rows_staged(const Params& p, uint8_t* stg,
   uint32_t cw[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i)
-    cw[i] = mx_e4m3(__uint_as_float(w[2 * i] << 16) * m) | (mx_e4m3(__uint_as_float(w[2 * i] & 0xFFFF0000u) * m) << 8) |
-            (mx_e4m3(__uint_as_float(w[2 * i + 1] << 16) * m) << 16) |
-            (mx_e4m3(__uint_as_float(w[2 * i + 1] & 0xFFFF0000u) * m) << 24);
+    cw[i] = mx_e4m3x2(__uint_as_float(w[2 * i] << 16) * m, __uint_as_float(w[2 * i] & 0xFFFF0000u) * m) |
+            (mx_e4m3x2(__uint_as_float(w[2 * i + 1] << 16) * m, __uint_as_float(w[2 * i + 1] & 0xFFFF0000u) * m) << 16);
   const uint8_t sb = static_cast<uint8_t>(sx + 127);
   if (lane < nrows) p.qsc[srow + ((size_t)(col >> 7) << 9) + ((col >> 5) & 3)] = sb;
   warp_store_rows32(stg, cw, p.qout + (size_t)wrow * ld + col, ld, nrows, lane);

@@ -122,27 +122,9 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   Smem* sm = reinterpret_cast<Smem*>(stg_area + NUM_EPI_WARPS * STG_BYTES);
   int* offs = reinterpret_cast<int*>(sm + 1);
   int* tstart = offs + (p.E + 1);
-  // wgrad kinds use no tile table: their second table holds the first packed
-  // scale word row of each expert segment
-  int* wstart = tstart;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   build_tile_table<KIND, NUM_THREADS>(p, offs, tstart);
-  if (Tr::kragged && warp == 0) {
-    int carry = 0;
-    for (int base = 0; base < p.E; base += 32) {
-      const int e = base + lane;
-      const int v = e < p.E ? ((offs[e + 1] - offs[e] + 31) / 32 + 3) / 4 : 0;
-      int incl = v;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int nb = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += nb;
-      }
-      if (e < p.E) wstart[e] = carry + incl - v;
-      carry += __shfl_sync(0xffffffffu, incl, 31);
-    }
-  }
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       ptx::mbar_init(&sm->full[s], 1);
@@ -196,8 +178,9 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           if (!Tr::kragged) {  // rows in per-expert 128-row tiles, K = Kd
             const long grp = mx_row_tile_base(offs[tl.e], tl.e) + tl.m_idx;
             ptx::bulk_load(sa, p.sfa + ((grp * (Kd / 128) + kb) << 9), 512, fb);
-          } else {  // features m0.. at the expert's K stage
-            ptx::bulk_load(sa, p.sfa + (((long)(wstart[tl.e] + kb) * (p.M / 128) + tl.m_idx) << 9), 512, fb);
+          } else {  // features m0.. at K stage kb of the expert's per-expert 128-row tiles
+            const long w = mx_row_tile_base(offs[tl.e], tl.e) + kb;
+            ptx::bulk_load(sa, p.sfa + ((w * (p.M / 128) + tl.m_idx) << 9), 512, fb);
           }
           if (KIND == FPROP1) {  // w_gate | w_up columns: K stage e d/128 + kb, column group n_idx
             const long c = ((long)tl.e * (p.d / 128) + kb) * (p.f / 128) + tl.n_idx;
@@ -222,7 +205,7 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
               ptx::bulk_load(sb + 512 * j, src + ((grp * kfs + kk) << 9), 512, fb);
             }
           } else {  // wgrad: B features at the expert's K stage
-            const long c = (long)(wstart[tl.e] + kb) * (p.N / 128) + (long)tl.n_idx * G::SCB;
+            const long c = (mx_row_tile_base(offs[tl.e], tl.e) + kb) * (p.N / 128) + (long)tl.n_idx * G::SCB;
             ptx::bulk_load(sb, p.sfb0 + (c << 9), 512 * G::SCB, fb);
           }
           // ---- E4M3 tiles
@@ -519,8 +502,7 @@ size_t fwd_workspace(long R, int E, int d, int f) {
 
 size_t bwd_workspace(long R, int E, int d, int f) {
   const size_t Ed = (size_t)E * d, Ef = (size_t)E * f;
-  return al(R * 2 * (size_t)f * 2)                                         // dh (bf16)
-         + al(R * (size_t)d) + al(tile_scale_bytes(R, E, d))               // dy rows
+  return al(R * (size_t)d) + al(tile_scale_bytes(R, E, d))                 // dy rows
          + al(R * (size_t)d) + al(seg_words_bytes(R, E, d))                    // dy segment columns
          + al(R * (size_t)f) + al(seg_words_bytes(R, E, f))                    // a segment columns
          + al(Ef * d) + al(Ef * d / 32)                                    // w_down rows
@@ -593,7 +575,6 @@ cudaError_t mx_mlp_bwd(const void* dy_perm, const void* x_perm, const void* h, c
   using namespace mx;
   Carver cv{static_cast<char*>(ws)};
   const long Ed = (long)E * d, Ef = (long)E * f;
-  void* dh = cv.raw((size_t)R * 2 * f * 2);
   QBuf dyr = cv.take((size_t)R * d, tile_scale_bytes(R, E, d));
   QBuf dyc = cv.take((size_t)R * d, seg_words_bytes(R, E, d));
   QBuf ac = cv.take((size_t)R * f, seg_words_bytes(R, E, f));
@@ -626,12 +607,15 @@ cudaError_t mx_mlp_bwd(const void* dy_perm, const void* x_perm, const void* h, c
   }
   if (!map_2d(&mA, dyr.q, U8, 1, d, R, 128, BM) || !map_3d(&mB0, wdr.q, U8, 1, d, f, E, 128, kN_DGRAD2))
     return cudaErrorInvalidValue;
-  p.N = f; p.n_tiles = (f + kN_DGRAD2 - 1) / kN_DGRAD2; p.out0 = dh; p.aux = h;
+  // dh itself is never stored: the epilogue quantises it along 2f (the GEMM1
+  // dgrad's A) and along the expert's rows (the GEMM1 wgrad's B)
+  p.N = f; p.n_tiles = (f + kN_DGRAD2 - 1) / kN_DGRAD2; p.out0 = nullptr; p.aux = h;
   p.sfa = dyr.s; p.sfb0 = wdr.s;
-  p.qout = dhr.q; p.qsc = dhr.s;  // the epilogue also quantises dh along 2f for the GEMM1 dgrad
+  p.qout = dhr.q; p.qsc = dhr.s;
+  p.qcol = dhc.q; p.qcsc = dhc.s;
   if ((e = launch<DGRAD2, kN_DGRAD2>(mA, mB0, mB0, p, ((long)(R + BM - 1) / BM + E) * p.n_tiles, st)) != cudaSuccess)
     return e;
-  p.qout = nullptr; p.qsc = nullptr;
+  p.qout = nullptr; p.qsc = nullptr; p.qcol = nullptr; p.qcsc = nullptr;
 
   // dWd[e] = A_e^T dy_e (K = the expert's rows): A and dy quantised along rows per expert
   if ((e = launch_mxfp8_quant_cols(a, R, f, offsets, E, ac.q, ac.s, st, true)) != cudaSuccess) return e;
@@ -661,7 +645,6 @@ cudaError_t mx_mlp_bwd(const void* dy_perm, const void* x_perm, const void* h, c
 
   // [dWg | dWu][e] = x_e^T dh_e (K = the expert's rows)
   if ((e = launch_mxfp8_quant_cols(x_perm, R, d, offsets, E, xc.q, xc.s, st, true)) != cudaSuccess) return e;
-  if ((e = launch_mxfp8_quant_cols(dh, R, 2 * f, offsets, E, dhc.q, dhc.s, st, true)) != cudaSuccess) return e;
   if (!map_2d(&mA, xc.q, U8, 1, d, R, 128, 128) || !map_2d(&mB0, dhc.q, U8, 1, 2L * f, R, 128, 128))
     return cudaErrorInvalidValue;
   p.M = d; p.N = 2 * f; p.m_tiles = (d + BM - 1) / BM; p.n_tiles = (2 * f + kN_WGRAD - 1) / kN_WGRAD;

@@ -72,10 +72,11 @@ quant_rows_kernel(const __nv_bfloat16* __restrict__ src, long nblocks, int kbloc
 
 // Block-row table: segment g owns block rows [bstart[g], bstart[g+1]).
 // PACKED: scales go to scale chunks (GEMM operand layout): K stage w (four
-// block rows of a segment; the stages of segment g start at
-// sum_{h<g} ceil(blocks_h / 4)) and column group c / 128 form chunk
-// w * (C / 128) + c / 128, and block 4w + j of column c is byte
-// mx_chunk_lane(c % 128) + j of it; bytes past a segment's last block are 127.
+// block rows of a segment; the stages of segment g are numbered from
+// mx_row_tile_base(seg[g], g), like the segment's 128-row tiles) and column
+// group c / 128 form chunk w * (C / 128) + c / 128, and block j of the stage
+// of column c is byte mx_chunk_lane(c % 128) + j of it; bytes past a
+// segment's last block are 127.
 // A CTA handles kColBlockRows block rows of 256 columns; each thread owns 2
 // consecutive columns (a warp reads 128 contiguous bytes of a row) and holds
 // its 32 x 2 block in registers, so every input byte is read from memory
@@ -87,37 +88,25 @@ template <bool PACKED>
 __global__ void __launch_bounds__(128, 6)
 quant_cols_kernel(const __nv_bfloat16* __restrict__ src, int rows, int C, const int32_t* __restrict__ seg,
                   int nseg, uint8_t* __restrict__ q, uint8_t* __restrict__ sc) {
-  extern __shared__ int bstart[];  // nseg + 1 block-row starts, then nseg + 1 word starts
-  int* wstart = bstart + nseg + 1;
+  extern __shared__ int bstart[];  // nseg + 1 block-row starts
   const int tid = threadIdx.x, lane = tid & 31;
   if (tid < 32) {
-    int carry = 0, wcarry = 0;
+    int carry = 0;
     for (int base = 0; base < nseg; base += 32) {
       const int g = base + lane;
       int len = 0;
       if (g < nseg) len = seg ? seg[g + 1] - seg[g] : rows;
-      const int v = (len + 31) / 32, vw = (v + 3) / 4;
-      int incl = v, wincl = vw;
+      const int v = (len + 31) / 32;
+      int incl = v;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         const int nb = __shfl_up_sync(0xffffffffu, incl, o);
-        const int nw = __shfl_up_sync(0xffffffffu, wincl, o);
-        if (lane >= o) {
-          incl += nb;
-          wincl += nw;
-        }
+        if (lane >= o) incl += nb;
       }
-      if (g < nseg) {
-        bstart[g] = carry + incl - v;
-        wstart[g] = wcarry + wincl - vw;
-      }
+      if (g < nseg) bstart[g] = carry + incl - v;
       carry += __shfl_sync(0xffffffffu, incl, 31);
-      wcarry += __shfl_sync(0xffffffffu, wincl, 31);
     }
-    if (lane == 0) {
-      bstart[nseg] = carry;
-      wstart[nseg] = wcarry;
-    }
+    if (lane == 0) bstart[nseg] = carry;
   }
   __syncthreads();
   const int c = (blockIdx.x * 128 + tid) * 2;  // x: column slices, so CTAs in flight share rows
@@ -162,7 +151,8 @@ quant_cols_kernel(const __nv_bfloat16* __restrict__ src, int rows, int C, const 
       const uint32_t b = static_cast<uint32_t>(sx[0] + 127) | static_cast<uint32_t>(sx[1] + 127) << 8;
       *reinterpret_cast<uint16_t*>(sc + (size_t)brow * C + c) = static_cast<uint16_t>(b);
     } else {
-      const int word = wstart[lo] + local / 4, byte = local % 4;
+      const long word = mx_row_tile_base(g0, lo) + local / 4;
+      const int byte = local % 4;
       const bool last = brow == bstart[lo + 1] - 1;
 #pragma unroll
       for (int j = 0; j < 2; ++j) {
@@ -364,7 +354,7 @@ cudaError_t launch_mxfp8_quant_cols(const void* src, int rows, int C, const int3
   if (rows == 0) return cudaSuccess;
   const long groups = (max_brows + kColBlockRows - 1) / kColBlockRows;
   dim3 grid(static_cast<unsigned>((C + 255) / 256), static_cast<unsigned>(groups < 65535 ? groups : 65535));
-  const size_t smem = 2 * (nseg_eff + 1) * sizeof(int);
+  const size_t smem = (nseg_eff + 1) * sizeof(int);
   if (packed)
     MOE_COUNTED quant_cols_kernel<true><<<grid, 128, smem, st>>>(static_cast<const __nv_bfloat16*>(src), rows, C,
                                                                  seg, nseg_eff, q, sc);

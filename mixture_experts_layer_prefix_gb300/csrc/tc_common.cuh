@@ -35,6 +35,8 @@ struct Params {
   const uint8_t* sfb1;     // MXFP8: scale bytes of the second B (up)
   uint8_t* qout;           // optional: the epilogue also writes its bf16 output
   uint8_t* qsc;            //   quantised along rows (E4M3 codes, E8M0 per 32)
+  uint8_t* qcol;           // optional (GEMM2 dgrad): ... and along the expert's
+  uint8_t* qcsc;           //   rows in blocks of 32 (weight-gradient operand)
   // Dispatch fused into the A operand (GEMM1 forward and wgrad): row r of A is
   // row src_row[r] / gk of x [T][d] (A's tensor map); nullptr: A is x_perm.
   const int32_t* src_row;
@@ -234,6 +236,40 @@ __device__ __forceinline__ void quant_rows_staged(const Params& p, uint8_t* stg,
   warp_store_rows32(stg, cw, p.qout + (size_t)wrow * ld + col, ld, nrows, lane);
 }
 
+// MXFP8 quantisation of the same chunk along its rows, in blocks of 32 rows:
+// the warp's rows are one such block of the expert segment (rows >= nrows are
+// past the segment's end and count as zero). Codes to qcol[row][col..col+32)
+// ([rows][ld] matrix), the scale of column col + lane into its scale chunk
+// (K stage `stage`, the block q within it; a block wholly past the end gets
+// 127). Lane l reads column l back from the staged rows.
+__device__ __forceinline__ void quant_cols_staged(const Params& p, uint8_t* stg, const uint32_t (&w)[16], int wrow,
+                                                  int nrows, int ld, int col, int lane, long stage, int q) {
+#pragma unroll
+  for (int g = 0; g < 4; ++g)
+    *reinterpret_cast<uint4*>(stg + stg_off(lane, g)) = make_uint4(w[4 * g], w[4 * g + 1], w[4 * g + 2], w[4 * g + 3]);
+  __syncwarp();
+  float v[32], amax = 0.0f;
+#pragma unroll
+  for (int r = 0; r < 32; ++r) {
+    const uint32_t b = *reinterpret_cast<const uint16_t*>(stg + stg_off(r, lane >> 3) + 2 * (lane & 7));
+    v[r] = r < nrows ? __uint_as_float(b << 16) : 0.0f;
+    amax = fmaxf(amax, fabsf(v[r]));
+  }
+  __syncwarp();
+  const int sx = mx_e8m0_exponent(amax);
+  const float m = mx_pow2_neg(sx);
+  uint8_t* dst = p.qcol + (size_t)wrow * ld + col + lane;
+#pragma unroll
+  for (int r = 0; r < 32; r += 2) {
+    const uint32_t b = mx_e4m3x2(v[r] * m, v[r + 1] * m);
+    if (r < nrows) dst[(size_t)r * ld] = static_cast<uint8_t>(b);
+    if (r + 1 < nrows) dst[(size_t)(r + 1) * ld] = static_cast<uint8_t>(b >> 8);
+  }
+  const int c = col + lane;
+  p.qcsc[((stage * (ld / 128) + c / 128) << 9) + mx_chunk_lane(c & 127) + q] =
+      static_cast<uint8_t>(nrows > 0 ? sx + 127 : 127);
+}
+
 // The reverse, in two halves so that the global latency can overlap other
 // work: issue reads the warp's 32 rows x 32 bf16 from src coalesced (rows >=
 // nrows read as zero); finish hands lane r row r (16 packed bf16 pairs).
@@ -341,12 +377,19 @@ __device__ __forceinline__ void epilogue_tile_staged(const Params& p, const Tile
         w[i] = pack_bf16x2(dg2[0], dg2[1]);
         wu[i] = pack_bf16x2(du2[0], du2[1]);
       }
-      warp_store_rows(stg, w, dh + n, 2 * (size_t)p.f, nrows, lane);
-      warp_store_rows(stg, wu, dh + p.f + n, 2 * (size_t)p.f, nrows, lane);
+      if (!QUANT || p.out0) {
+        warp_store_rows(stg, w, dh + n, 2 * (size_t)p.f, nrows, lane);
+        warp_store_rows(stg, wu, dh + p.f + n, 2 * (size_t)p.f, nrows, lane);
+      }
       if (QUANT && p.qout) {
         const size_t srow = tile_scale_row(tl, q, lane, 2 * p.f);
         quant_rows_staged(p, stg, w, wrow, nrows, 2 * p.f, n, lane, srow);
         quant_rows_staged(p, stg, wu, wrow, nrows, 2 * p.f, p.f + n, lane, srow);
+      }
+      if (QUANT && p.qcol) {
+        const long stage = mx_row_tile_base(tl.m0 - tl.m_idx * BM, tl.e) + tl.m_idx;
+        quant_cols_staged(p, stg, w, wrow, nrows, 2 * p.f, n, lane, stage, q);
+        quant_cols_staged(p, stg, wu, wrow, nrows, 2 * p.f, p.f + n, lane, stage, q);
       }
     }
   } else {  // FPROP2, DGRAD1: plain bf16 store

@@ -136,3 +136,58 @@ def test_fullsize_sampled_parity(name):
         assert float(b.dw_gate[int(e)].float().abs().max()) == 0.0
     bad = {k: v for k, v in errs.items() if not v <= BF16_TOL}
     assert not bad, f"{name}: {bad} (all: {errs})"
+
+
+def test_fullsize_mxfp8_sampled_parity():
+    """The MXFP8 workload (T=32768, E=128, k=4) at full size, run as bench.py
+    runs it (weights prepared, rows quantised where produced): routing exact;
+    y, dx, dgates, dlogits of sampled tokens and the weight gradients of
+    sampled experts against the MXFP8 oracle on the same dequantised operands.
+    Every quantisation the oracle applies is local to what is sampled: token
+    rows along d, f and 2f; weights per matrix; the weight-gradient operands
+    along one expert's rows (its tokens in token order, as in the layer)."""
+    from oracle import mxfp8_layer
+
+    s = synth.CONFIGS["e128_top4_mxfp8"]
+    inp = synth.Inputs(s, seed=0)
+    p = L.params_from_inputs(inp, N.MOE_MXFP8)
+    b = L.Buffers(s.T, s.d, s.E, s.k, s.f, N.MOE_MXFP8)
+    L.forward(p, b)
+    L.backward(p, b)
+    torch.cuda.synchronize()
+    assert N.moe_get_device_error() == 0
+
+    gl = b.logits.cpu().numpy().astype(np.float64)
+    ref_route = oracle.route(gl, s.k, s.E)
+    for key in ("topk_idx", "counts", "offsets", "dest_row", "src_row"):
+        np.testing.assert_array_equal(getattr(b, key).cpu().numpy(), ref_route[key], err_msg=key)
+
+    tol = 6e-2
+    rng = np.random.default_rng(321)
+    tokens = np.sort(rng.choice(s.T, size=8, replace=False))
+    used = np.unique(ref_route["topk_idx"][tokens])
+    w = inp.for_experts(used)
+    ref = mxfp8_layer.layer(inp.x()[tokens], inp.w_r()[:, used], w["w_gate"], w["w_up"], w["w_down"],
+                            inp.dy()[tokens], s.k, gl[tokens][:, used])
+    dl_full = np.zeros((len(tokens), s.E))
+    dl_full[:, used] = ref["dlogits"]
+    errs = {
+        "y": maxnorm_err(np_of(b.y)[tokens], ref["y"]),
+        "dx": maxnorm_err(np_of(b.dx)[tokens], ref["dx"]),
+        "dgates": maxnorm_err(np_of(b.dgates)[tokens], ref["dgates"]),
+        "dlogits": maxnorm_err(np_of(b.dlogits)[tokens], dl_full),
+    }
+    counts = ref_route["counts"]
+    cand = np.flatnonzero(counts > 0)
+    for e in (int(cand[np.argmin(counts[cand])]), int(cand[np.argmax(counts[cand])])):
+        tok, slot = np.nonzero(ref_route["topk_idx"] == e)
+        ge = ref_route["gates"][tok, slot][:, None]
+        we = inp.for_experts([e])
+        # one expert, k = 1: gate 1, so dy is pre-scaled by the layer's gates
+        r1 = mxfp8_layer.layer(inp.x()[tok], np.zeros((s.d, 1)), we["w_gate"], we["w_up"], we["w_down"],
+                               ge * inp.dy()[tok].astype(np.float64), 1, np.zeros((len(tok), 1)))
+        errs[f"dw_gate[{e}]"] = maxnorm_err(np_of(b.dw_gate[e]), r1["dw_gate"][0])
+        errs[f"dw_up[{e}]"] = maxnorm_err(np_of(b.dw_up[e]), r1["dw_up"][0])
+        errs[f"dw_down[{e}]"] = maxnorm_err(np_of(b.dw_down[e]), r1["dw_down"][0])
+    bad = {k: v for k, v in errs.items() if not v <= tol}
+    assert not bad, f"{bad} (all: {errs})"

@@ -173,7 +173,8 @@ quant_cols_kernel(const __nv_bfloat16* __restrict__ src, int rows, int C, const 
 // rows and C are multiples of 128, so no block crosses a weight matrix. CTAs
 // stride over the tiles (those of one 32-row band are consecutive, so W is
 // read in order) with the next tile's cp.async copies in flight while the
-// current one is converted. The bytes equal those of the separate column and
+// current one is converted; the column codes are staged so that they leave as
+// 16-byte pieces of rows. The bytes equal those of the separate column and
 // row quantisers.
 constexpr int kDualCols = 128, kDualPitch = kDualCols + 8;  // bf16 per staged row (16-byte pad)
 constexpr int kDualTile = 32 * kDualPitch;
@@ -181,6 +182,7 @@ __global__ void __launch_bounds__(128)
 quant_dual_kernel(const __nv_bfloat16* __restrict__ src, int C, long ntiles, uint8_t* __restrict__ qc,
                   uint8_t* __restrict__ sc_c, uint8_t* __restrict__ qr, uint8_t* __restrict__ sc_r) {
   __shared__ __align__(16) __nv_bfloat16 tile[2 * kDualTile];
+  __shared__ __align__(16) uint8_t cbuf[32 * kDualCols];
   const int tid = threadIdx.x;
   const int cg = C / kDualCols;
   auto issue = [&](long t, int buf) {  // a half-warp copies one 256-byte row segment per step
@@ -219,8 +221,8 @@ quant_dual_kernel(const __nv_bfloat16* __restrict__ src, int C, long ntiles, uin
 #pragma unroll
       for (int r = 0; r < 32; r += 2) {
         const uint32_t b = mx_e4m3x2(v[r] * m, v[r + 1] * m);
-        qc[(row0 + r) * C + c0 + tid] = static_cast<uint8_t>(b);
-        qc[(row0 + r + 1) * C + c0 + tid] = static_cast<uint8_t>(b >> 8);
+        cbuf[r * kDualCols + tid] = static_cast<uint8_t>(b);
+        cbuf[(r + 1) * kDualCols + tid] = static_cast<uint8_t>(b >> 8);
       }
       sc_c[(((row0 >> 7) * cg + c0 / 128) << 9) + mx_chunk_lane(tid) + ((row0 >> 5) & 3)] =
           static_cast<uint8_t>(sx + 127);
@@ -246,7 +248,14 @@ quant_dual_kernel(const __nv_bfloat16* __restrict__ src, int C, long ntiles, uin
       out[1] = make_uint4(cw[4], cw[5], cw[6], cw[7]);
       sc_r[(((row >> 7) * cg + c0 / 128) << 9) + mx_chunk_lane(static_cast<int>(row & 127)) + cb] = sb;
     }
-    __syncthreads();  // the buffer is refilled two tiles on
+    __syncthreads();  // every column's codes are staged
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const int id = tid + 128 * i, r = id >> 3, g = id & 7;
+      *reinterpret_cast<uint4*>(qc + (row0 + r) * C + c0 + 16 * g) =
+          *reinterpret_cast<const uint4*>(cbuf + r * kDualCols + 16 * g);
+    }
+    __syncthreads();  // the buffers are refilled two tiles on
   }
   asm volatile("cp.async.wait_all;" ::: "memory");
 }

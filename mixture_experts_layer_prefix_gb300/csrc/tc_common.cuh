@@ -241,7 +241,8 @@ __device__ __forceinline__ void quant_rows_staged(const Params& p, uint8_t* stg,
 // past the segment's end and count as zero). Codes to qcol[row][col..col+32)
 // ([rows][ld] matrix), the scale of column col + lane into its scale chunk
 // (K stage `stage`, the block q within it; a block wholly past the end gets
-// 127). Lane l reads column l back from the staged rows.
+// 127). Lane l reads column l back from the staged rows; the codes return to
+// row order through the same buffer and leave as 16 rows x 32 B per store.
 __device__ __forceinline__ void quant_cols_staged(const Params& p, uint8_t* stg, const uint32_t (&w)[16], int wrow,
                                                   int nrows, int ld, int col, int lane, long stage, int q) {
 #pragma unroll
@@ -258,13 +259,23 @@ __device__ __forceinline__ void quant_cols_staged(const Params& p, uint8_t* stg,
   __syncwarp();
   const int sx = mx_e8m0_exponent(amax);
   const float m = mx_pow2_neg(sx);
-  uint8_t* dst = p.qcol + (size_t)wrow * ld + col + lane;
 #pragma unroll
   for (int r = 0; r < 32; r += 2) {
     const uint32_t b = mx_e4m3x2(v[r] * m, v[r + 1] * m);
-    if (r < nrows) dst[(size_t)r * ld] = static_cast<uint8_t>(b);
-    if (r + 1 < nrows) dst[(size_t)(r + 1) * ld] = static_cast<uint8_t>(b >> 8);
+    stg[stg32_off(r, lane >> 4) + (lane & 15)] = static_cast<uint8_t>(b);
+    stg[stg32_off(r + 1, lane >> 4) + (lane & 15)] = static_cast<uint8_t>(b >> 8);
   }
+  __syncwarp();
+  {
+    const int g = lane & 1;
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const int r = 16 * i + (lane >> 1);
+      const uint4 cv = *reinterpret_cast<const uint4*>(stg + stg32_off(r, g));
+      if (r < nrows) *reinterpret_cast<uint4*>(p.qcol + (size_t)(wrow + r) * ld + col + 16 * g) = cv;
+    }
+  }
+  __syncwarp();
   const int c = col + lane;
   p.qcsc[((stage * (ld / 128) + c / 128) << 9) + mx_chunk_lane(c & 127) + q] =
       static_cast<uint8_t>(nrows > 0 ? sx + 127 : 127);

@@ -109,8 +109,9 @@ quant_cols_kernel(const __nv_bfloat16* __restrict__ src, int rows, int C, const 
     if (lane == 0) bstart[nseg] = carry;
   }
   __syncthreads();
+  __shared__ __align__(16) uint8_t cbuf[32 * 256];  // the block row's codes, [row][256 columns]
   const int c = (blockIdx.x * 128 + tid) * 2;  // x: column slices, so CTAs in flight share rows
-  if (c >= C) return;
+  const bool act = c < C;  // C % 8 == 0: the 8- or 16-byte pieces below are all in or all out
   const int ngroups = (bstart[nseg] + kColBlockRows - 1) / kColBlockRows;
   for (int grp = blockIdx.y; grp < ngroups; grp += gridDim.y)
   for (int brow = grp * kColBlockRows; brow < (grp + 1) * kColBlockRows; ++brow) {
@@ -124,10 +125,10 @@ quant_cols_kernel(const __nv_bfloat16* __restrict__ src, int rows, int C, const 
     const int local = brow - bstart[lo];
     const int r0 = g0 + local * 32, nr = min(32, g1 - r0);
     uint32_t blk[32];
-    const uint32_t* sp = reinterpret_cast<const uint32_t*>(src + (size_t)r0 * C + c);
+    const uint32_t* sp = reinterpret_cast<const uint32_t*>(src + (size_t)r0 * C + (act ? c : 0));
     const int cw = C / 2;  // row stride in 32-bit words
 #pragma unroll
-    for (int i = 0; i < 32; ++i) blk[i] = i < nr ? __ldg(sp + i * cw) : 0u;
+    for (int i = 0; i < 32; ++i) blk[i] = (act && i < nr) ? __ldg(sp + i * cw) : 0u;
     float amax0 = 0.0f, amax1 = 0.0f;
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
@@ -138,15 +139,31 @@ quant_cols_kernel(const __nv_bfloat16* __restrict__ src, int rows, int C, const 
     sx[0] = e8m0_exponent(amax0);
     sx[1] = e8m0_exponent(amax1);
     const float m0 = pow2_neg(sx[0]), m1 = pow2_neg(sx[1]);
-    uint16_t* qp = reinterpret_cast<uint16_t*>(q + (size_t)r0 * C + c);
-    const int ch = C / 2;  // row stride in 16-bit units
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
-      if (i < nr) {
-        const uint32_t b = mx_e4m3x2(__uint_as_float(blk[i] << 16) * m0, __uint_as_float(blk[i] & 0xFFFF0000u) * m1);
-        qp[i * ch] = static_cast<uint16_t>(b);
+      const uint32_t b = mx_e4m3x2(__uint_as_float(blk[i] << 16) * m0, __uint_as_float(blk[i] & 0xFFFF0000u) * m1);
+      *reinterpret_cast<uint16_t*>(cbuf + i * 256 + 2 * tid) = static_cast<uint16_t>(b);
+    }
+    __syncthreads();
+    if ((C & 15) == 0) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {  // 16 threads per row, 16 bytes each
+        const int id = tid + 128 * j, r = id >> 4, g = id & 15;
+        const int cc = blockIdx.x * 256 + 16 * g;
+        if (r < nr && cc < C)
+          *reinterpret_cast<uint4*>(q + (size_t)(r0 + r) * C + cc) = *reinterpret_cast<const uint4*>(cbuf + r * 256 + 16 * g);
+      }
+    } else {  // C % 16 == 8: rows start 8-byte aligned only
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {  // 32 threads per row, 8 bytes each
+        const int id = tid + 128 * j, r = id >> 5, g = id & 31;
+        const int cc = blockIdx.x * 256 + 8 * g;
+        if (r < nr && cc < C)
+          *reinterpret_cast<uint2*>(q + (size_t)(r0 + r) * C + cc) = *reinterpret_cast<const uint2*>(cbuf + r * 256 + 8 * g);
       }
     }
+    __syncthreads();
+    if (!act) continue;
     if (!PACKED) {
       const uint32_t b = static_cast<uint32_t>(sx[0] + 127) | static_cast<uint32_t>(sx[1] + 127) << 8;
       *reinterpret_cast<uint16_t*>(sc + (size_t)brow * C + c) = static_cast<uint16_t>(b);

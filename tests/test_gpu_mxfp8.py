@@ -48,10 +48,12 @@ def test_quantize_rows_bit_exact(rows, K):
     np.testing.assert_array_equal(q.cpu().numpy(), rq)
 
 
-@pytest.mark.parametrize("seg", [[0, 5, 5, 70, 100], [0, 0, 33, 33, 64, 1000, 1001], None])
-def test_quantize_segmented_columns_bit_exact(seg):
+@pytest.mark.parametrize("seg,C", [([0, 5, 5, 70, 100], 512), ([0, 0, 33, 33, 64, 1000, 1001], 512), (None, 512),
+                                   ([0, 40, 41, 200], 520), (None, 264)])
+def test_quantize_segmented_columns_bit_exact(seg, C):
+    """C = 520 and 264: a column count that is a multiple of 8 but not of 16
+    (rows start 8-byte aligned), and a last CTA with 8 or 16 columns."""
     rows = 100 if seg is None else seg[-1]
-    C = 512
     v = _values(rows, C, 7)
     segs = np.array(seg if seg is not None else [0, rows], np.int32)
     nseg = len(segs) - 1

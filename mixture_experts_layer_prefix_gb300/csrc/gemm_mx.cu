@@ -352,22 +352,15 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         // single accumulator: copy this warp's 128 columns out as packed bf16,
         // release it, then store
         if constexpr (KIND == FPROP1) {
-          uint32_t wg[2][16], wu[2][16], wa[2][16];
+          // the raw fp32 gate/up values leave TMEM first (the shortest hold of
+          // the accumulator); the SwiGLU math runs after its release
+          uint32_t rg[2][32], ru[2][32];
 #pragma unroll
           for (int cc = 0; cc < 2; ++cc) {
-            uint32_t rg[32], ru[32];
-            ptx::tmem_ld32(tbase + (2 * half + cc) * 32, rg);
-            ptx::tmem_ld32(tbase + 128 + (2 * half + cc) * 32, ru);
-            ptx::tmem_wait_ld();
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              const float g0 = __uint_as_float(rg[2 * i]), g1 = __uint_as_float(rg[2 * i + 1]);
-              const float u0 = __uint_as_float(ru[2 * i]), u1 = __uint_as_float(ru[2 * i + 1]);
-              wg[cc][i] = pack_bf16x2(g0, g1);
-              wu[cc][i] = pack_bf16x2(u0, u1);
-              wa[cc][i] = pack_bf16x2(silu_f(g0) * u0, silu_f(g1) * u1);
-            }
+            ptx::tmem_ld32(tbase + (2 * half + cc) * 32, rg[cc]);
+            ptx::tmem_ld32(tbase + 128 + (2 * half + cc) * 32, ru[cc]);
           }
+          ptx::tmem_wait_ld();
           ptx::tc_fence_before();
           __syncwarp();
           if (lane == 0) ptx::mbar_arrive(&sm->tempty[buf]);
@@ -379,10 +372,21 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           for (int cc = 0; cc < 2; ++cc) {
             const int n = tl.n_idx * 128 + (2 * half + cc) * 32;
             if (n >= p.f) continue;
-            warp_store_rows(stg, wg[cc], h + n, 2 * (size_t)p.f, nrows, lane);
-            warp_store_rows(stg, wu[cc], h + p.f + n, 2 * (size_t)p.f, nrows, lane);
-            warp_store_rows(stg, wa[cc], ao + n, p.f, nrows, lane);
-            if (p.qout) quant_rows_staged(p, stg, wa[cc], wrow, nrows, p.f, n, lane, tile_scale_row(tl, q, lane, p.f));
+            uint32_t w[16], wa[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const float g0 = __uint_as_float(rg[cc][2 * i]), g1 = __uint_as_float(rg[cc][2 * i + 1]);
+              const float u0 = __uint_as_float(ru[cc][2 * i]), u1 = __uint_as_float(ru[cc][2 * i + 1]);
+              w[i] = pack_bf16x2(g0, g1);
+              wa[i] = pack_bf16x2(silu_f(g0) * u0, silu_f(g1) * u1);
+            }
+            warp_store_rows(stg, w, h + n, 2 * (size_t)p.f, nrows, lane);
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              w[i] = pack_bf16x2(__uint_as_float(ru[cc][2 * i]), __uint_as_float(ru[cc][2 * i + 1]));
+            warp_store_rows(stg, w, h + p.f + n, 2 * (size_t)p.f, nrows, lane);
+            warp_store_rows(stg, wa, ao + n, p.f, nrows, lane);
+            if (p.qout) quant_rows_staged(p, stg, wa, wrow, nrows, p.f, n, lane, tile_scale_row(tl, q, lane, p.f));
           }
         } else {
           uint32_t w[4][16];

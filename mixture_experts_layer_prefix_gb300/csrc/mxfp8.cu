@@ -13,9 +13,12 @@
 //   cols kernel: blocks of 32 consecutive rows of one column, starting at each
 //                segment's first row (segments = per-expert row ranges from
 //                the device offsets); a segment's last block is zero-padded.
-//                Each thread owns 8 columns (16-byte loads) and keeps the
-//                block's 32 rows in registers between the maxima and the
-//                conversion.
+//                Each thread owns 2 columns and keeps the block's 32 rows in
+//                registers between the maxima and the conversion.
+//   dual kernel: a weight tile read once and written quantised both ways.
+//   dispatch:    the permute with each token's row quantised once (below).
+// The GEMM operands' scales are written as scale chunks (mxfp8_common.cuh);
+// mxfp8_quantize's public layouts are the plain ones.
 #include <cuda_fp8.h>
 
 #include <algorithm>

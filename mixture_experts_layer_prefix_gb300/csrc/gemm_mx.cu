@@ -170,7 +170,10 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         if (lane == 0) {
           uint8_t* a = smem + s * G::STAGE_BYTES;
           uint8_t* b = a + A_BYTES;
-          ptx::mbar_expect_tx(fb, G::STAGE_BYTES + G::SC_BYTES);
+          // B column groups of 128 that exist (N need not be a multiple of
+          // the tile width): only their scale chunks are fetched
+          const int nb = KIND == FPROP1 ? 2 : min(G::SCB, (p.N - tl.n_idx * TBN + 127) / 128);
+          ptx::mbar_expect_tx(fb, G::STAGE_BYTES + 512 + 512 * nb);
           // ---- E8M0 scale chunks (512 B per 128 rows or columns and K stage):
           // A's, then one per 128 columns of B
           uint8_t* sa = sc_area + s * G::SC_BYTES;
@@ -188,10 +191,11 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             ptx::bulk_load(sb + 512, p.sfb1 + (c << 9), 512, fb);
           } else if (KIND == FPROP2) {  // w_down columns: K stage e f/128 + kb
             const long c = ((long)tl.e * (p.f / 128) + kb) * (p.d / 128) + (long)tl.n_idx * G::SCB;
-            ptx::bulk_load(sb, p.sfb0 + (c << 9), 512 * G::SCB, fb);
+            ptx::bulk_load(sb, p.sfb0 + (c << 9), 512 * nb, fb);
           } else if (KIND == DGRAD2) {  // w_down rows (f) along d
 #pragma unroll
             for (int j = 0; j < G::SCB; ++j) {
+              if (j >= nb) break;
               const long grp = (long)tl.e * (p.f / 128) + (long)tl.n_idx * G::SCB + j;
               ptx::bulk_load(sb + 512 * j, p.sfb0 + ((grp * (p.d / 128) + kb) << 9), 512, fb);
             }
@@ -201,12 +205,13 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             const int kk = kb < kfs ? kb : kb - kfs;
 #pragma unroll
             for (int j = 0; j < G::SCB; ++j) {
+              if (j >= nb) break;
               const long grp = (long)tl.e * (p.d / 128) + (long)tl.n_idx * G::SCB + j;
               ptx::bulk_load(sb + 512 * j, src + ((grp * kfs + kk) << 9), 512, fb);
             }
           } else {  // wgrad: B features at the expert's K stage
             const long c = (mx_row_tile_base(offs[tl.e], tl.e) + kb) * (p.N / 128) + (long)tl.n_idx * G::SCB;
-            ptx::bulk_load(sb, p.sfb0 + (c << 9), 512 * G::SCB, fb);
+            ptx::bulk_load(sb, p.sfb0 + (c << 9), 512 * nb, fb);
           }
           // ---- E4M3 tiles
           if (KIND == FPROP1) {

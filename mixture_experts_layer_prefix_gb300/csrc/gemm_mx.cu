@@ -107,6 +107,95 @@ __device__ __forceinline__ void store_chunk(const Params& p, const Tile& tl, int
   }
 }
 
+// GEMM2 dgrad: the h rows (gate and up halves) of a warp's two 32-column
+// chunks are copied into the warp's shared buffer with cp.async when the tile
+// starts, so they land while its MMAs run (H_WARP bytes per warp: chunk j at
+// 4096 j, gate then up, each [32 rows][64 B] in the staging swizzle; rows past
+// the expert's end read as zeros).
+constexpr int H_WARP = 2 * 4096;
+__device__ __forceinline__ void h_prefetch(const Params& p, const Tile& tl, int q, int lane, int c_beg, int c_end,
+                                           int tbn, uint8_t* hbuf) {
+  const int wrow = tl.m0 + q * 32;
+  const int nrows = max(0, min(32, tl.row_end - wrow));
+  const __nv_bfloat16* h = static_cast<const __nv_bfloat16*>(p.aux);
+  for (int c = c_beg; c < c_end; ++c) {
+    const int n = tl.n_idx * tbn + c * 32;
+    if (n >= p.N) continue;
+#pragma unroll
+    for (int part = 0; part < 2; ++part) {  // gate columns n.., up columns f + n..
+      uint8_t* dst = hbuf + (c - c_beg) * 4096 + part * 2048;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int id = lane + 32 * i, r = id >> 2, g = id & 3;
+        const bool ok = r < nrows;
+        const __nv_bfloat16* src = h + (ok ? (size_t)(wrow + r) * 2 * p.f + part * p.f + n + 8 * g : 0);
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(ptx::smem_u32(dst + stg_off(r, g))),
+                     "l"(src), "r"(ok ? 16 : 0)
+                     : "memory");
+      }
+    }
+  }
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+// GEMM2 dgrad epilogue with h taken from the warp's prefetched buffer: dh_g =
+// da * h_u * silu'(h_g), dh_u = da * silu(h_g), quantised along 2f and along
+// the expert's rows (dh itself is stored only when p.out0 is set).
+__device__ __forceinline__ void epilogue_dgrad2_mx(const Params& p, const Tile& tl, uint32_t tbase, int q, int lane,
+                                                   int c_beg, int c_end, int tbn, uint8_t* stg, const uint8_t* hbuf) {
+  const int wrow = tl.m0 + q * 32;
+  const int nrows = max(0, min(32, tl.row_end - wrow));
+  asm volatile("cp.async.wait_group 0;" ::: "memory");
+  __syncwarp();
+  __nv_bfloat16* dh = static_cast<__nv_bfloat16*>(p.out0) + (size_t)wrow * 2 * p.f;
+  const size_t srow = tile_scale_row(tl, q, lane, 2 * p.f);
+  const long stage = mx_row_tile_base(tl.m0 - tl.m_idx * BM, tl.e) + tl.m_idx;
+  for (int c = c_beg; c < c_end; ++c) {
+    const int n = tl.n_idx * tbn + c * 32;
+    uint32_t r[32];
+    ptx::tmem_ld32(tbase + c * 32, r);
+    ptx::tmem_wait_ld();
+    if (n >= p.N) continue;
+    const uint8_t* hb = hbuf + (c - c_beg) * 4096;
+    uint32_t hg[16], hu[16], w[16], wu[16];
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+      const uint4 a = *reinterpret_cast<const uint4*>(hb + stg_off(lane, g));
+      const uint4 b = *reinterpret_cast<const uint4*>(hb + 2048 + stg_off(lane, g));
+      hg[4 * g] = a.x; hg[4 * g + 1] = a.y; hg[4 * g + 2] = a.z; hg[4 * g + 3] = a.w;
+      hu[4 * g] = b.x; hu[4 * g + 1] = b.y; hu[4 * g + 2] = b.z; hu[4 * g + 3] = b.w;
+    }
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      float dg2[2], du2[2];
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const float g = j ? bf16_hi(hg[i]) : bf16_lo(hg[i]);
+        const float u = j ? bf16_hi(hu[i]) : bf16_lo(hu[i]);
+        const float da = __uint_as_float(r[2 * i + j]);
+        const float s = sigmoid_f(g);
+        dg2[j] = da * u * s * (1.0f + g * (1.0f - s));
+        du2[j] = da * g * s;
+      }
+      w[i] = pack_bf16x2(dg2[0], dg2[1]);
+      wu[i] = pack_bf16x2(du2[0], du2[1]);
+    }
+    if (p.out0) {
+      warp_store_rows(stg, w, dh + n, 2 * (size_t)p.f, nrows, lane);
+      warp_store_rows(stg, wu, dh + p.f + n, 2 * (size_t)p.f, nrows, lane);
+    }
+    if (p.qout) {
+      quant_rows_staged(p, stg, w, wrow, nrows, 2 * p.f, n, lane, srow);
+      quant_rows_staged(p, stg, wu, wrow, nrows, 2 * p.f, p.f + n, lane, srow);
+    }
+    if (p.qcol) {
+      quant_cols_staged(p, stg, w, wrow, nrows, 2 * p.f, n, lane, stage, q);
+      quant_cols_staged(p, stg, wu, wrow, nrows, 2 * p.f, p.f + n, lane, stage, q);
+    }
+  }
+  __syncwarp();  // the buffer is refilled for the next tile
+}
+
 template <int KIND, int TBN>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
@@ -115,11 +204,14 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   using G = Geo<TBN>;
   static_assert(KIND != FPROP1 || TBN == 256, "GEMM1 tiles pair 128 gate with 128 up columns");
   static_assert(!(Tr::kragged && Geo<TBN>::ACC == 2), "weight-gradient tiles use the single 256-column accumulator");
+  static_assert(KIND != DGRAD2 || TBN == 128, "the h buffer holds a warp's two 32-column chunks");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sc_area = smem + STAGES * G::STAGE_BYTES;
   uint8_t* stg_area = sc_area + STAGES * G::SC_BYTES;  // epilogue staging, STG_BYTES per warp
-  Smem* sm = reinterpret_cast<Smem*>(stg_area + NUM_EPI_WARPS * STG_BYTES);
+  uint8_t* h_area = stg_area + NUM_EPI_WARPS * STG_BYTES;  // GEMM2 dgrad: h rows, H_WARP per warp
+  constexpr int H_BYTES = KIND == DGRAD2 ? NUM_EPI_WARPS * H_WARP : 0;
+  Smem* sm = reinterpret_cast<Smem*>(h_area + H_BYTES);
   int* offs = reinterpret_cast<int*>(sm + 1);
   int* tstart = offs + (p.E + 1);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -315,7 +407,6 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   } else {
     // ============================================================ epilogue
     const int ew = warp - 2, q = warp & 3, half = ew >> 2;
-    const int r_tile = q * 32 + lane;
     uint8_t* stg = stg_area + ew * STG_BYTES;
     constexpr int NC = KIND == FPROP1 ? 4 : TBN / 32;  // chunks of the tile (FPROP1: gate/up pairs)
     uint32_t acc_it = 0;
@@ -328,19 +419,8 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         for (int c = half * NC / 2; c < (half + 1) * NC / 2; ++c) store_chunk<KIND, TBN>(p, tl, q, lane, c, z, stg);
         continue;
       }
-      if (KIND == DGRAD2) {
-        // pull this row's h_g / h_u chunks into L2 while the MMAs run
-        const int row = tl.m0 + r_tile;
-        if (row < tl.row_end) {
-          const __nv_bfloat16* h = static_cast<const __nv_bfloat16*>(p.aux) + (size_t)row * 2 * p.f;
-          for (int c = half * NC / 2; c < (half + 1) * NC / 2; ++c) {
-            const int n = tl.n_idx * TBN + c * 32;
-            if (n >= p.N) continue;
-            asm volatile("prefetch.global.L2 [%0];" ::"l"(h + n));
-            asm volatile("prefetch.global.L2 [%0];" ::"l"(h + p.f + n));
-          }
-        }
-      }
+      if (KIND == DGRAD2)  // this tile's h rows land in shared memory while its MMAs run
+        h_prefetch(p, tl, q, lane, half * NC / 2, (half + 1) * NC / 2, TBN, h_area + ew * H_WARP);
       const int buf = G::ACC == 2 ? (acc_it & 1) : 0;
       const uint32_t aph = (G::ACC == 2 ? (acc_it >> 1) : acc_it) & 1u;
       if (!wait_bar(&sm->tfull[buf], aph, &sm->abort_flag, p.err)) break;
@@ -348,7 +428,9 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       const uint32_t tbase = tmem + static_cast<uint32_t>(buf * TBN) + (static_cast<uint32_t>(q * 32) << 16);
       if (G::ACC == 2 || KIND == DGRAD2) {
         // double-buffered (or too many registers to drain first): epilogue straight from TMEM
-        if constexpr (!Tr::kragged)
+        if constexpr (KIND == DGRAD2)
+          epilogue_dgrad2_mx(p, tl, tbase, q, lane, half * NC / 2, (half + 1) * NC / 2, TBN, stg, h_area + ew * H_WARP);
+        else if constexpr (!Tr::kragged)
           epilogue_tile_staged<KIND, TBN, true>(p, tl, tbase, q, lane, half * NC / 2, (half + 1) * NC / 2, stg);
         ptx::tc_fence_before();
         __syncwarp();
@@ -422,17 +504,17 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   }
 }
 
-template <int TBN>
+template <int KIND, int TBN>
 size_t smem_bytes(int E) {
   return 1024 + STAGES * Geo<TBN>::STAGE_BYTES + STAGES * Geo<TBN>::SC_BYTES + NUM_EPI_WARPS * STG_BYTES +
-         sizeof(Smem) + 2 * (E + 1) * sizeof(int) + 64;
+         (KIND == DGRAD2 ? NUM_EPI_WARPS * H_WARP : 0) + sizeof(Smem) + 2 * (E + 1) * sizeof(int) + 64;
 }
 
 template <int KIND, int TBN>
 cudaError_t launch(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1, const Params& p,
                    long max_tiles, cudaStream_t st) {
   if (max_tiles <= 0) return cudaSuccess;
-  const size_t smem = smem_bytes<TBN>(p.E);
+  const size_t smem = smem_bytes<KIND, TBN>(p.E);
   cudaError_t e = cudaFuncSetAttribute(mx_gemm_kernel<KIND, TBN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
@@ -466,11 +548,6 @@ struct Carver {
     b.s = reinterpret_cast<uint8_t*>(p + used);
     used += al(scales);
     return b;
-  }
-  void* raw(size_t bytes) {
-    void* r = p + used;
-    used += al(bytes);
-    return r;
   }
 };
 

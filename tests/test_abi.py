@@ -126,3 +126,29 @@ def test_mxfp8_dispatch_arguments_rejected_before_launch(lib):
     assert L.moe_mxfp8_weights_size(4, 128, 128) > 4 * 128 * 128 * 3 * 2
     assert L.moe_mxfp8_prepare_weights(FAKE, FAKE, FAKE, 4, 128, 128, FAKE, 16, None) == 4  # wq too small
     assert L.moe_mxfp8_prepare_weights(FAKE, FAKE, FAKE, 4, 192, 128, FAKE, 1 << 30, None) == 2
+
+
+def test_row_scale_chunks_fit_every_routing(lib):
+    """The scale-chunk layout of row operands (include/moe.h): expert e's
+    128-row tiles are groups (offsets[e] + 127 e) / 128 + m. For random and
+    extreme per-expert counts the groups of different experts never overlap
+    and every byte of every group lies inside moe_mxfp8_row_scales_size."""
+    import numpy as np
+    rng = np.random.default_rng(7)
+    cases = [np.full(8, 512), np.zeros(16, np.int64), np.array([0, 1, 127, 128, 129, 255, 256, 0, 1000]),
+             np.array([65536] + [0] * 127)]
+    cases += [rng.integers(0, 700, size=E) for E in (1, 2, 31, 128, 1024)]
+    for counts in cases:
+        counts = np.asarray(counts, np.int64)
+        E, R = len(counts), int(counts.sum())
+        offs = np.concatenate([[0], np.cumsum(counts)])
+        K = 256
+        size = lib.moe_mxfp8_row_scales_size(R, E, K)
+        used = []
+        for e in range(E):
+            base = (offs[e] + 127 * e) // 128
+            tiles = -(-int(counts[e]) // 128)
+            used += [base + m for m in range(tiles)]
+        assert len(used) == len(set(used)), counts
+        if used:
+            assert (max(used) + 1) * 4 * K <= size, (counts, size)

@@ -64,6 +64,12 @@ def workload_desc(s):
             f"SwiGLU f={s.f}, {s.dtype}")
 
 
+def config_of(s, world):
+    return {"workload": workload_desc(s), "T": s.T, "d": s.d, "E": s.E, "k": s.k, "f": s.f,
+            "parallelism": f"replicas x{world} (no collective)",
+            "l2": "no flush: per-step working set (1.6 GB weights + activations) >> 129 MB L2"}
+
+
 def gemm_flops(s):
     """Algorithmic FLOPs of the six grouped expert GEMMs of one fwd+bwd step
     (routed rows only): forward 6*R*d*f, backward 12*R*d*f."""
@@ -174,23 +180,60 @@ def max_over_ranks(values, device=None):
 
 
 # --------------------------------------------------------------- our arm
-def run_ours(args, s, rank, world):
+# Algorithmic work of each kernel of a step (FLOPs for the tensor-core GEMMs,
+# DRAM bytes for the data-movement kernels), keyed by the kernel names the
+# library's launch-timing recorder reports.
+def kernel_work(s):
+    R, T, d, f, E, k = s.R, s.T, s.d, s.f, s.E, s.k
+    flops = {"gemm1_swiglu": 4.0 * R * d * f, "gemm2": 2.0 * R * f * d, "gemm2_dgrad_swiglu_bwd": 2.0 * R * d * f,
+             "gemm2_wgrad": 2.0 * R * f * d, "gemm1_dgrad": 4.0 * R * f * d, "gemm1_wgrad": 4.0 * R * d * f}
+    flops.update({"mx_" + n: v for n, v in list(flops.items())})
+    byt = {"permute": 2.0 * (T + R) * d, "combine_fwd": 2.0 * (R + T) * d + 8.0 * T * k,
+           "combine_bwd": 2.0 * (T + 2 * R) * d + 12.0 * T * k, "permute_bwd": 2.0 * (R + T) * d + 4.0 * T * E,
+           "router_gemm": 2.0 * T * d + 4.0 * T * E + 2.0 * E * d, "router_dw": 2.0 * T * d + 4.0 * T * E + 4.0 * E * d,
+           "router_dlogits": 12.0 * T * k + 4.0 * T * E, "permute_quant": 2.0 * T * d + (2.0 + 33.0 / 32) * R * d,
+           "quant_dual": 3 * E * d * f * (2.0 + 2 * 33.0 / 32)}
+    return flops, byt
+
+
+class Weights:
+    """Device weights of one (E, d, f) layer, drawn once and shared by every
+    workload of that size (they depend only on the seed, the tensor name and
+    the expert)."""
+
+    def __init__(self):
+        self.cache = {}
+
+    def params(self, s, dt):
+        import torch
+
+        from mixture_experts_layer_prefix_gb300 import layer as L
+        inp = synth.Inputs(s, seed=0)
+        key = (s.E, s.d, s.f, s.router_std, L.torch_dtype(dt))
+        if key not in self.cache:
+            p = L.params_from_inputs(inp, dt)
+            self.cache[key] = (p.w_router, p.w_gate, p.w_up, p.w_down)
+            return p
+        wr, wg, wu, wd = self.cache[key]
+        b = inp.bias()
+        return L.Params(x=L.to_device(inp.x(), dt), w_router=wr,
+                        bias=None if b is None else torch.from_numpy(b).cuda(),
+                        w_gate=wg, w_up=wu, w_down=wd, dy=L.to_device(inp.dy(), dt))
+
+
+def measure(s, weights, steps, warmup, local, e2e=False, world=1):
+    """Time `steps` forward+backward steps of workload `s` through the C ABI
+    (device-resident inputs), then one untimed step with every launch timed
+    on its own; optionally the end-to-end leg from pinned host buffers."""
     import torch
 
     from mixture_experts_layer_prefix_gb300 import _native as N
-    from mixture_experts_layer_prefix_gb300 import build as B
     from mixture_experts_layer_prefix_gb300 import layer as L
 
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    torch.cuda.set_device(local)
-    if rank == 0 or not os.path.exists(B.LIB):
-        B.build()
-    if world > 1:
-        torch.distributed.barrier()
-    N.load()
     dt = {"f32": N.MOE_F32, "bf16": N.MOE_BF16, "mxfp8": N.MOE_MXFP8}[s.dtype]
-    inp = synth.Inputs(s, seed=0)
-    p = L.params_from_inputs(inp, dt)
+    p = weights.params(s, dt)
+    torch.cuda.synchronize()
+    torch.cuda.reset_peak_memory_stats()
     b = L.Buffers(s.T, s.d, s.E, s.k, s.f, dt)
     stream = torch.cuda.current_stream()
     fused = L.fused_default(dt)
@@ -241,15 +284,15 @@ def run_ours(args, s, rank, world):
         N.moe_permute_bwd(b.dx_perm, dt, T, d, E, k, b.dest_row, b.topk_idx, b.dlogits, p.w_router, b.dx)
 
     mk = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
-    for _ in range(args.warmup):
+    for _ in range(warmup):
         step_timed([mk() for _ in range(4)])
     torch.cuda.synchronize()
     err = N.moe_get_device_error()
     if err:
-        raise RuntimeError(f"device error word {err} after warm-up")
+        raise RuntimeError(f"device error word {err} after warm-up ({s.name})")
 
     # ---- timed region (device-resident inputs)
-    evs = [[mk() for _ in range(4)] for _ in range(args.steps)]
+    evs = [[mk() for _ in range(4)] for _ in range(steps)]
     t_start, t_end = mk(), mk()
     clocks = ClockSampler(local)
     if world > 1:
@@ -259,7 +302,7 @@ def run_ours(args, s, rank, world):
     time.sleep(0.3)
     n0 = N.moe_launch_count()
     t_start.record(stream)
-    for i in range(args.steps):
+    for i in range(steps):
         step_timed(evs[i])
     t_end.record(stream)
     torch.cuda.synchronize()
@@ -268,41 +311,127 @@ def run_ours(args, s, rank, world):
         torch.distributed.barrier()
     clk = clocks.stop()
     elapsed_ms = t_start.elapsed_time(t_end)
-    gemm_ms = sum(e[0].elapsed_time(e[1]) + e[2].elapsed_time(e[3]) for e in evs) / args.steps
+    gemm_ms = sum(e[0].elapsed_time(e[1]) + e[2].elapsed_time(e[3]) for e in evs) / steps
     if N.moe_get_device_error():
-        raise RuntimeError("device error word set in the timed region")
+        raise RuntimeError(f"device error word set in the timed region ({s.name})")
+    peak_mem = torch.cuda.max_memory_allocated()
 
-    # ---- end to end through the C ABI with host buffers (pinned), copies timed
-    x_h = p.x.cpu().pin_memory()
-    dy_h = p.dy.cpu().pin_memory()
-    y_h = torch.empty_like(b.y, device="cpu").pin_memory()
-    dx_h = torch.empty_like(b.dx, device="cpu").pin_memory()
-    e2e_steps = max(1, args.steps)  # the pipeline fill (first upload) and drain (last download) are amortised like the device leg
-    pipe = L.HostPipeline(p, b)
-    pipe.run([x_h], [dy_h], [y_h], [dx_h], stream=stream)  # warm the second buffer set
+    # ---- one more step, untimed, with every launch bracketed by its own events
+    # (two plain steps first, so the host runs ahead and no launch waits for it)
+    for _ in range(2):
+        step_timed([mk() for _ in range(4)])
+    N.moe_timing_arm(256)
+    step_timed([mk() for _ in range(4)])
+    N.moe_timing_finish(stream)
+    per_launch = N.moe_timing_read()
     torch.cuda.synchronize()
-    e0, e1 = mk(), mk()
-    e0.record(stream)
-    pipe.run([x_h] * e2e_steps, [dy_h] * e2e_steps, [y_h] * e2e_steps, [dx_h] * e2e_steps, stream=stream)
-    e1.record(stream)
+
+    out = dict(elapsed_ms=elapsed_ms, gemm_ms=gemm_ms, clocks=clk, launches=launches, per_launch=per_launch,
+               peak_mem=peak_mem)
+    if e2e:
+        # ---- end to end through the C ABI with host buffers (pinned), copies timed
+        x_h = p.x.cpu().pin_memory()
+        dy_h = p.dy.cpu().pin_memory()
+        y_h = torch.empty_like(b.y, device="cpu").pin_memory()
+        dx_h = torch.empty_like(b.dx, device="cpu").pin_memory()
+        e2e_steps = max(1, steps)  # pipeline fill (first upload) and drain (last download) amortised like the device leg
+        pipe = L.HostPipeline(p, b)
+        pipe.run([x_h], [dy_h], [y_h], [dx_h], stream=stream)  # warm the second buffer set
+        torch.cuda.synchronize()
+        e0, e1 = mk(), mk()
+        e0.record(stream)
+        pipe.run([x_h] * e2e_steps, [dy_h] * e2e_steps, [y_h] * e2e_steps, [dx_h] * e2e_steps, stream=stream)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        out["e2e_ms"] = e0.elapsed_time(e1) / e2e_steps
+        out["h2d"] = x_h.numel() * x_h.element_size() + dy_h.numel() * dy_h.element_size()
+        out["d2h"] = y_h.numel() * y_h.element_size() + dx_h.numel() * dx_h.element_size()
+        del pipe
+    del b
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / e2e_steps
-    h2d = x_h.numel() * x_h.element_size() + dy_h.numel() * dy_h.element_size()
-    d2h = y_h.numel() * y_h.element_size() + dx_h.numel() * dx_h.element_size()
+    torch.cuda.empty_cache()
+    return out
 
-    elapsed_ms, e2e_ms = max_over_ranks([elapsed_ms, e2e_ms], device="cuda")
 
+def gemm_peak(s, pk, pk_kind, timed_s):
+    """(burst peak, sustained peak, label) in TFLOP/s for this workload's GEMM
+    dtype: FP8 = the measured bf16 peak x 2 (the nominal FP8:bf16 ratio)."""
+    burst = float(pk.get("bf16_tflops"))
+    sus = float(pk.get("bf16_tflops_sustained", burst))
+    mult, dtl = (2.0, "bf16 x 2 (nominal FP8/bf16 ratio)") if s.dtype == "mxfp8" else (1.0, "bf16")
+    return burst * mult, sus * mult, f"{pk_kind} {dtl}"
+
+
+def kernel_table(s, per_launch, pk, pk_kind):
+    """Per-kernel device times of one step (from the launch-timing recorder),
+    with the achieved rate against the roofline that bounds each kernel."""
+    flops, byt = kernel_work(s)
+    burst, _, _ = gemm_peak(s, pk, pk_kind, 0.0)
+    hbm = float(pk.get("hbm_gbs"))
+    agg = {}
+    for name, ms in per_launch:
+        a = agg.setdefault(name, {"launches": 0, "ms": 0.0})
+        a["launches"] += 1
+        a["ms"] += ms
+    total = sum(a["ms"] for a in agg.values()) or 1.0
+    for name, a in agg.items():
+        a["share"] = a["ms"] / total
+        if name in flops:
+            a["tflops"] = flops[name] / (a["ms"] / 1e3) / 1e12
+            a["frac_burst"] = a["tflops"] / burst
+            a["bound"] = "tensor"
+        elif name in byt:
+            a["gbs"] = byt[name] / (a["ms"] / 1e3) / 1e9
+            a["frac_hbm"] = a["gbs"] / hbm
+            a["bound"] = "hbm"
+    return agg
+
+
+def summary(s, m, steps, pk, pk_kind, world=1):
+    """Nested per-workload result: throughput, GEMM roofline fraction, clocks."""
+    ms = m["elapsed_ms"] / steps
+    burst, sus, lab = gemm_peak(s, pk, pk_kind, m["elapsed_ms"] / 1e3)
+    ach = gemm_flops(s) / (m["gemm_ms"] / 1e3) / 1e12
+    kt = kernel_table(s, m["per_launch"], pk, pk_kind)
+    gk = {n: v for n, v in kt.items() if v.get("bound") == "tensor"}
+    g6 = sum(v["ms"] for v in gk.values())
+    return {"workload": workload_desc(s), "value": world * s.T * steps / (m["elapsed_ms"] / 1e3), "unit": "tokens/s",
+            "ms_per_step": ms, "steps": steps,
+            "gemm_frac_burst": ach / burst, "gemm_frac_sustained": ach / sus, "gemm_tflops": ach,
+            "gemm_ms_per_step": m["gemm_ms"], "peak_kind": lab,
+            "six_gemm_kernels_ms": g6, "six_gemm_kernels_frac_burst": (gemm_flops(s) / (g6 / 1e3) / 1e12 / burst)
+            if g6 else None,
+            "peak_memory_gib": m["peak_mem"] / 2 ** 30, "clocks": m["clocks"], "kernels": kt}
+
+
+def run_ours(args, s, rank, world):
+    import torch
+
+    from mixture_experts_layer_prefix_gb300 import _native as N
+    from mixture_experts_layer_prefix_gb300 import build as B
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if rank == 0 or not os.path.exists(B.LIB):
+        B.build()
+    if world > 1:
+        torch.distributed.barrier()
+    N.load()
+    weights = Weights()
+    m = measure(s, weights, args.steps, args.warmup, local, e2e=True, world=world)
+    elapsed_ms, e2e_ms = max_over_ranks([m["elapsed_ms"], m["e2e_ms"]], device="cuda")
     ms_per_step = elapsed_ms / args.steps
     tokens_per_s = world * s.T * args.steps / (elapsed_ms / 1e3)
     pk, pk_kind = peaks()
-    peak = float(pk.get("bf16_tflops_sustained", pk.get("bf16_tflops")))
-    peak_kind = f"{pk_kind} bf16 sustained"
-    if s.dtype == "mxfp8":
-        # FP8 dense peak = the measured bf16 peak x the nominal FP8:bf16 ratio (2)
-        peak *= 2.0
-        peak_kind = f"{pk_kind} bf16 sustained x 2 (nominal FP8/bf16 ratio)"
-    achieved = gemm_flops(s) / (gemm_ms / 1e3) / 1e12
+    timed_s = elapsed_ms / 1e3
+    burst, sus, lab = gemm_peak(s, pk, pk_kind, timed_s)
+    # the timed region is a burst (well under a second of tensor work at the
+    # default step count): the burst peak applies; the sustained one is kept
+    # beside it for runs of several seconds
+    peak = burst if timed_s < 1.0 else sus
+    achieved = gemm_flops(s) / (m["gemm_ms"] / 1e3) / 1e12
     traffic = None if (args.tokens or args.experts) else gemm_traffic(args.config)
+    kt = kernel_table(s, m["per_launch"], pk, pk_kind)
     out = {
         "metric": METRIC,
         "value": tokens_per_s,
@@ -316,22 +445,34 @@ def run_ours(args, s, rank, world):
         "vs_baseline": None,
         "dtype": s.dtype,
         "data": "synthetic (seeded N(0,1) tokens, N(0,1/fan_in) weights, router N(0,0.02^2))",
-        "config": {"workload": workload_desc(s), "T": s.T, "d": s.d, "E": s.E, "k": s.k, "f": s.f,
-                   "parallelism": f"replicas x{world} (no collective)",
-                   "l2": "no flush: per-step working set (1.6 GB weights + activations) >> 129 MB L2"},
+        "config": config_of(s, world),
         "tflops_per_s": step_flops(s) * world * args.steps / (elapsed_ms / 1e3) / 1e12,
         "roofline": {"kernel": "grouped expert GEMMs (fwd+bwd, 6 GEMMs per step"
                                + ("; includes the MXFP8 operand quantisation)" if s.dtype == "mxfp8" else ")"),
                      "bound": "tensor",
                      "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
-                     "peak_kind": peak_kind, "traffic": traffic,
+                     "peak_kind": f"{lab} {'burst' if peak == burst else 'sustained'} (timed region "
+                                  f"{timed_s:.2f} s)",
+                     "frac_burst": achieved / burst, "frac_sustained": achieved / sus,
+                     "traffic": traffic,
                      "traffic_unit": "DRAM bytes per step of the six GEMM launches (ncu, see profiles/)",
-                     "gemm_ms_per_step": gemm_ms},
-        "e2e": {"value": world * s.T / (e2e_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
-        "gpu_launches": launches,
-        "clocks": clk,
+                     "gemm_ms_per_step": m["gemm_ms"],
+                     "per_kernel": kt,
+                     "per_kernel_how": "one untimed step after the timed region, every launch bracketed by CUDA "
+                                       "events on its stream (moe_timing_arm/finish/read)"},
+        "e2e": {"value": world * s.T / (e2e_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": m["h2d"],
+                "d2h_bytes_per_step": m["d2h"], "ms_per_step": e2e_ms},
+        "gpu_launches": m["launches"],
+        "peak_memory_gib": m["peak_mem"] / 2 ** 30,
+        "clocks": m["clocks"],
     }
+    if not args.no_more and world == 1 and not (args.tokens or args.experts) and args.config == DEFAULT_CONFIG:
+        more = {}
+        for name in ("e128_top4_mxfp8", "e128_top4_bf16_twin", "e128_top4_skew"):
+            sn = synth.CONFIGS[name]
+            mm = measure(sn, weights, args.more_steps, args.warmup, local)
+            more[name] = summary(sn, mm, args.more_steps, pk, pk_kind)
+        out["workloads"] = more
     return out
 
 
@@ -345,6 +486,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--tokens", type=int, default=0, help="override T (smaller cases for profiling)")
+    ap.add_argument("--no-more", action="store_true",
+                    help="skip the nested MXFP8 / bf16-twin / skewed-routing workloads of the default line")
+    ap.add_argument("--more-steps", type=int, default=50, help="timed steps of each nested workload")
     ap.add_argument("--experts", type=int, default=0,
                     help="override E (with --tokens: small profiling cases with the same rows per expert)")
     args = ap.parse_args()
@@ -377,7 +521,8 @@ def main():
             "impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": 1,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sum(times) / len(times),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": {"workload": workload_desc(s)},
+            "data": "synthetic (seeded N(0,1) tokens, N(0,1/fan_in) weights, router N(0,0.02^2))",
+            "config": config_of(s, 1),
             "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": th, "kind": "oracle",
                              "sample": f"first {n} of {s.T} tokens per step, fp64 C oracle"},
             "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},

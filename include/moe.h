@@ -64,7 +64,7 @@ typedef enum { MOE_F32 = 0, MOE_BF16 = 1, MOE_MXFP8 = 2 } moe_dtype;
 #define MOE_ROUTE_LOGITS_IN 1 /* skip the router GEMM: `logits` is an input */
 
 /* Bytes of workspace that the calls below need for this shape (the maximum
-   over all calls). */
+   over all calls). A sizing helper: the pages have no counterpart. */
 size_t moe_workspace_size(int T, int d, int E, int k, int f, int dtype);
 
 /* Routing: router GEMM, softmax + top-k gates, per-expert counts, offsets and
@@ -88,13 +88,18 @@ moe_status moe_route(const void* x, const void* w_router, const float* bias, int
                      int32_t* counts, int32_t* offsets, int32_t* dest_row, int32_t* src_row,
                      void* workspace, size_t workspace_bytes, void* stream);
 
-/* Dispatch: x_perm[dest_row[t][j]] = x[t]  (an exact copy).
+/* Dispatch ("Scaling and optimizing MoE training": row-wise expert
+   parallelism writes the routed rows straight into the experts' input
+   buffers; on one GPU those buffers are the contiguous expert segments of
+   x_perm):  x_perm[dest_row[t][j]] = x[t]  (an exact copy).
    x: [T][d]; x_perm: [T*k][d]; both dtype. */
 moe_status moe_permute(const void* x, int dtype, int T, int d, int k, const int32_t* dest_row,
                        void* x_perm, void* stream);
 
-/* Backward of the dispatch, plus the router's share of dx when dlogits is
-   given:  dx[t] = sum_j dx_perm[dest_row[t][j]]
+/* Backward of the dispatch above (same section), plus the router's share
+   of dx when dlogits is given (the benchmark layer's backward -- page 1
+   introduction, 8/128-expert top-4 study -- carries the gate gradient into
+   the router and on to x):  dx[t] = sum_j dx_perm[dest_row[t][j]]
                  + sum_j dlogits[t][topk_idx[t][j]] * w_router[topk_idx[t][j]]
    (fp32 sums in j order, one rounding to dtype). topk_idx, dlogits and
    w_router are either all NULL (no router term) or all given. */
@@ -102,19 +107,28 @@ moe_status moe_permute_bwd(const void* dx_perm, int dtype, int T, int d, int E, 
                            const int32_t* dest_row, const int32_t* topk_idx, const float* dlogits,
                            const void* w_router, void* dx, void* stream);
 
-/* Combine: y[t] = sum_j gates[t][j] * y_perm[dest_row[t][j]]
+/* Combine: the inverse of the dispatch ("Scaling and optimizing MoE
+   training": each routed row's expert output returns from its expert's buffer
+   to its token), weighted by the renormalised gates of the benchmark layer
+   (page 1 introduction):
+     y[t] = sum_j gates[t][j] * y_perm[dest_row[t][j]]
    (fp32 sum in j order, rounded once to dtype). y_perm [T*k][d]; y [T][d]. */
 moe_status moe_combine_fwd(const void* y_perm, const float* gates, const int32_t* dest_row,
                            int dtype, int T, int d, int k, void* y, void* stream);
 
-/* Backward of the combine:
+/* Backward of the combine (same section and layer definition as
+   moe_combine_fwd):
      dy_perm[dest_row[t][j]] = gates[t][j] * dy[t]            (dtype)
      dgates[t][j] = sum_c dy[t][c] * y_perm[dest_row[t][j]][c] (fp32) */
 moe_status moe_combine_bwd(const void* dy, const void* y_perm, const float* gates,
                            const int32_t* dest_row, int dtype, int T, int d, int k, void* dy_perm,
                            float* dgates, void* stream);
 
-/* Router backward (softmax over the selected logits):
+/* Router backward: the gradient through moe_route's gates (softmax over
+   the selected logits, the benchmark layer's renormalised top-k gates, page 1
+   introduction) and its router GEMM ("Scaling and optimizing MoE training":
+   routing tokens to experts). The router's share of dx is added by
+   moe_permute_bwd, which writes dx once.
      dlogits[t][i] = g_i * (dg_i - sum_j g_j dg_j) for i in top-k, 0 otherwise
      dw_router[e][c] = sum over rows r of expert e of dlogits[t(r)][e] * x[t(r)][c]
    with t(r) = src_row[r] / k (fp32 sum in row order, i.e. ascending token).
@@ -154,7 +168,9 @@ moe_status moe_grouped_mlp_fwd(const void* x_perm, const void* w_gate, const voi
                                int d, int f, void* h_save, void* a_save, void* y_perm,
                                void* workspace, size_t workspace_bytes, void* stream);
 
-/* Grouped SwiGLU expert MLP, backward. With dh = (dh_g | dh_u):
+/* Grouped SwiGLU expert MLP, backward, again one launch per GEMM for all
+   experts ("Scaling and optimizing MoE training": grouped GEMM). With
+   dh = (dh_g | dh_u):
      da = dy_perm[r] . w_down[e]^T;  dh_g = da * h_u * silu'(h_g);
      dh_u = da * silu(h_g);  dx_perm[r] = dh_g . w_gate[e]^T + dh_u . w_up[e]^T
      dw_down[e] = sum_r a_save[r]^T dy_perm[r];
@@ -282,10 +298,11 @@ moe_status mxfp8_quantize(const void* src, int rows, int K, int axis, const int3
    the same arguments minus the workspace: its scratch lives in a 4 MiB array
    compiled into the library, which every GPU that loads the library keeps
    until the process exits. Shapes with ceil(T/8) * E > 1,048,576 return
-   MOE_ERR_WORKSPACE without launching anything. The first call on a device
-   looks up the array's device address (once per device, with that device
-   current); make that first call before any stream capture. The call
-   allocates nothing. All calls on a device share the one array, so calls
+   MOE_ERR_WORKSPACE without launching anything. Every call looks up the
+   array's device address on the calling thread's current device (so a device
+   reset leaves no stale address behind); the first call on a device also loads
+   the library's device code there, so make it before any stream capture. The
+   call allocates nothing. All calls on a device share the one array, so calls
    that may overlap on the GPU (different streams, or different host threads)
    race with each other and must be ordered by the caller. */
 moe_status moe_route_noalloc(const void* x, const void* w_router, const float* bias, int dtype, int T,
@@ -293,16 +310,49 @@ moe_status moe_route_noalloc(const void* x, const void* w_router, const float* b
                              float* gates, int32_t* counts, int32_t* offsets, int32_t* dest_row,
                              int32_t* src_row, void* stream);
 
+/* Self-test of the bounded waits (failure detection; the pages have no
+   counterpart). Launches one 64-thread block on `stream` in which warp 0 waits
+   on an mbarrier that nothing arrives on, for at most `cycles` SM clock cycles
+   (1 <= cycles <= 4e9, about 2 s at 2 GHz), while warp 1 waits on another one
+   with the GEMMs' own limit (~2 s). Warp 0's wait expires: it sets the device
+   error word to MOE_ERR_TIMEOUT and raises the block's abort flag, which ends
+   warp 1's wait as well; the kernel then returns normally (no trap). out: [2]
+   int32 device buffer, 16-byte aligned; out[w] = 1 if warp w's wait completed,
+   0 if it gave up (so {0, 0} after a correct run). The caller reads the error
+   word with moe_get_device_error(); the context stays usable. */
+moe_status moe_selftest_wait_timeout(long long cycles, int32_t* out, void* stream);
+
 /* Synchronises `stream`, then returns and clears this device's error word
-   (MOE_OK if no kernel reported an error). */
+   (MOE_OK if no kernel reported an error). Error reporting of this library:
+   the pages have no counterpart. */
 moe_status moe_get_device_error(void* stream);
 
-/* Number of SMs the kernels size their persistent grids for (0 on error). */
+/* Number of SMs the kernels size their persistent grids for (0 on error).
+   Instrumentation: the pages have no counterpart. */
 int moe_sm_count(void);
 
 /* Number of kernels this process has launched through libmoe so far (a host
-   counter, bumped once per successful launch; for instrumentation). */
+   counter, bumped once per successful launch; for instrumentation; the
+   pages have no counterpart). */
 uint64_t moe_launch_count(void);
+
+/* Launch timing, for measurement (instrumentation: the pages have no
+   counterpart). moe_timing_arm(n) arms a process-wide recorder: each of the
+   next n kernel launches made through the library (1 <= n <= 256) records a
+   CUDA event on its own stream just before it starts. moe_timing_finish(stream)
+   records a closing event on `stream` and disarms the recorder.
+   moe_timing_read(ms, names, cap) waits for the closing event and, for the
+   first min(recorded, cap) launches, writes ms[i] = time from launch i's event
+   to the next event (launch i+1's, or the closing one) and names[i] = a static
+   string naming the kernel (names may be NULL); it returns that count, or -1
+   if nothing was finished. When the launches ran back to back on one stream,
+   ms[i] is launch i's device duration (plus any idle gap before the next
+   launch, so the host should run ahead of the GPU). Arming creates CUDA events
+   (not device memory) on the current device the first time. Not meant for
+   concurrent use by several threads. */
+moe_status moe_timing_arm(int n);
+moe_status moe_timing_finish(void* stream);
+int moe_timing_read(float* ms, const char** names, int cap);
 
 #ifdef __cplusplus
 }

@@ -27,7 +27,8 @@ EXPORTS = ("moe_workspace_size", "moe_route", "moe_permute", "moe_permute_bwd", 
            "mxfp8_quantize", "moe_get_device_error", "moe_sm_count", "moe_launch_count", "moe_route_noalloc",
            "moe_dispatch_mlp_fwd", "moe_dispatch_mlp_bwd", "moe_route_stats", "moe_permute_mxfp8",
            "moe_combine_bwd_mxfp8", "moe_mxfp8_mlp_fwd", "moe_mxfp8_mlp_bwd", "moe_mxfp8_weights_size",
-           "moe_mxfp8_prepare_weights", "moe_mxfp8_row_scales_size")
+           "moe_mxfp8_prepare_weights", "moe_mxfp8_row_scales_size", "moe_timing_arm", "moe_timing_finish",
+           "moe_timing_read", "moe_selftest_wait_timeout")
 
 
 class MoEError(RuntimeError):
@@ -73,6 +74,10 @@ def load(path: str = LIB_PATH):
         "moe_mxfp8_weights_size": ([I, I, I], Z),
         "moe_mxfp8_prepare_weights": ([P, P, P, I, I, I, P, Z, P], I),
         "moe_dispatch_mlp_bwd": ([P, P, P, I, I, P, P, P, P, P, I, P, I, I, I, P, P, P, P, P, Z, P], I),
+        "moe_timing_arm": ([I], I),
+        "moe_timing_finish": ([P], I),
+        "moe_timing_read": ([P, P, I], I),
+        "moe_selftest_wait_timeout": ([ctypes.c_longlong, P, P], I),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -240,3 +245,25 @@ def moe_mxfp8_mlp_bwd(dy_codes, dy_scales, dy_perm, x_perm, h_save, a_save, wq, 
     _chk("moe_mxfp8_mlp_bwd", load().moe_mxfp8_mlp_bwd(
         _p(dy_codes), _p(dy_scales), _p(dy_perm), _p(x_perm), _p(h_save), _p(a_save), _p(wq), _p(offsets), R, E, d,
         f, _p(dx_perm), _p(dw_gate), _p(dw_up), _p(dw_down), _p(workspace), _nbytes(workspace), _s(stream)))
+
+
+def moe_timing_arm(n):
+    _chk("moe_timing_arm", load().moe_timing_arm(int(n)))
+
+
+def moe_timing_finish(stream=None):
+    _chk("moe_timing_finish", load().moe_timing_finish(_s(stream)))
+
+
+def moe_timing_read(cap=256):
+    """[(kernel name, ms)] of the launches recorded since moe_timing_arm."""
+    ms = (ctypes.c_float * cap)()
+    names = (ctypes.c_char_p * cap)()
+    n = load().moe_timing_read(ms, names, cap)
+    if n < 0:
+        raise MoEError("moe_timing_read", 1)
+    return [(names[i].decode(), float(ms[i])) for i in range(n)]
+
+
+def moe_selftest_wait_timeout(cycles, out, stream=None):
+    _chk("moe_selftest_wait_timeout", load().moe_selftest_wait_timeout(int(cycles), _p(out), _s(stream)))

@@ -3,6 +3,7 @@
 #include <cuda_bf16.h>
 
 #include <atomic>
+#include <mutex>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -26,6 +27,37 @@ int* device_error_word() {
 
 static std::atomic<unsigned long long> g_launches{0};
 void count_launch(int n) { g_launches.fetch_add((unsigned long long)n, std::memory_order_relaxed); }
+
+// Launch-timing recorder (instrumentation): while armed, each launch records
+// one event on its stream just before it; moe_timing_finish records the
+// closing event. Event i to event i+1 then brackets launch i when the
+// launches ran in order on one stream.
+namespace {
+constexpr int kMaxTimed = 256;
+struct LaunchTimer {
+  std::mutex mu;
+  std::atomic<int> armed{0};  // launches still to record
+  int n = 0;                  // launches recorded
+  int dev = -1;               // device the events belong to
+  bool closed = false;
+  cudaEvent_t ev[kMaxTimed + 1] = {};
+  const char* names[kMaxTimed] = {};
+};
+LaunchTimer& launch_timer() {
+  static LaunchTimer t;
+  return t;
+}
+}  // namespace
+
+void mark_launch(cudaStream_t st, const char* name) {
+  LaunchTimer& t = launch_timer();
+  if (t.armed.load(std::memory_order_relaxed) <= 0) return;
+  std::lock_guard<std::mutex> g(t.mu);
+  if (t.armed.load(std::memory_order_relaxed) <= 0 || t.n >= kMaxTimed) return;
+  if (cudaEventRecord(t.ev[t.n], st) != cudaSuccess) return;
+  t.names[t.n++] = name;
+  t.armed.fetch_sub(1, std::memory_order_relaxed);
+}
 
 namespace {
 
@@ -337,7 +369,8 @@ moe_status moe_permute_mxfp8(const void* x, int T, int d, int k, int E, const in
   if (T == 0) return MOE_OK;
   MOE_NEED(x); MOE_NEED(dest_row); MOE_NEED(topk_idx); MOE_NEED(offsets); MOE_NEED(x_codes); MOE_NEED(x_scales);
   if (x_perm && !aligned16(x_perm)) return MOE_ERR_ALIGNMENT;
-  MOE_CUDA_TRY(launch_permute_quant(x, T, d, k, dest_row, topk_idx, offsets, x_codes, x_scales, x_perm, S(stream)));
+  MOE_CUDA_TRY(launch_permute_quant(x, T, d, k, E, dest_row, topk_idx, offsets, x_codes, x_scales, x_perm,
+                                    S(stream)));
   return MOE_OK;
 }
 
@@ -350,8 +383,8 @@ moe_status moe_combine_bwd_mxfp8(const void* dy, const void* y_perm, const float
   MOE_NEED(dy); MOE_NEED(y_perm); MOE_NEED(gates); MOE_NEED(dest_row); MOE_NEED(topk_idx); MOE_NEED(offsets);
   MOE_NEED(dy_codes); MOE_NEED(dy_scales); MOE_NEED(dgates);
   if (dy_perm && !aligned16(dy_perm)) return MOE_ERR_ALIGNMENT;
-  MOE_CUDA_TRY(launch_combine_bwd_quant(dy, y_perm, gates, dest_row, topk_idx, offsets, T, d, k, dy_codes, dy_scales,
-                                        dy_perm, dgates, S(stream)));
+  MOE_CUDA_TRY(launch_combine_bwd_quant(dy, y_perm, gates, dest_row, topk_idx, offsets, T, d, k, E, dy_codes,
+                                        dy_scales, dy_perm, dgates, S(stream)));
   return MOE_OK;
 }
 
@@ -492,6 +525,52 @@ moe_status moe_get_device_error(void* stream) {
 }
 
 uint64_t moe_launch_count(void) { return (uint64_t)g_launches.load(std::memory_order_relaxed); }
+
+moe_status moe_timing_arm(int n) {
+  if (n <= 0 || n > kMaxTimed) return MOE_ERR_INVALID_ARG;
+  LaunchTimer& t = launch_timer();
+  std::lock_guard<std::mutex> g(t.mu);
+  int dev = 0;
+  MOE_CUDA_TRY(cudaGetDevice(&dev));
+  if (t.dev != dev) {  // events are created on (and belong to) the current device
+    if (t.dev >= 0) {
+      int cur = dev;
+      cudaSetDevice(t.dev);
+      for (auto& e : t.ev) cudaEventDestroy(e);
+      cudaSetDevice(cur);
+    }
+    t.dev = -1;
+    for (auto& e : t.ev) MOE_CUDA_TRY(cudaEventCreate(&e));
+    t.dev = dev;
+  }
+  t.n = 0;
+  t.closed = false;
+  t.armed.store(n, std::memory_order_relaxed);
+  return MOE_OK;
+}
+
+moe_status moe_timing_finish(void* stream) {
+  LaunchTimer& t = launch_timer();
+  std::lock_guard<std::mutex> g(t.mu);
+  t.armed.store(0, std::memory_order_relaxed);
+  if (t.dev < 0) return MOE_ERR_INVALID_ARG;
+  MOE_CUDA_TRY(cudaEventRecord(t.ev[t.n], S(stream)));
+  t.closed = true;
+  return MOE_OK;
+}
+
+int moe_timing_read(float* ms, const char** names, int cap) {
+  LaunchTimer& t = launch_timer();
+  std::lock_guard<std::mutex> g(t.mu);
+  if (!t.closed || ms == nullptr || cap < 0) return -1;
+  if (cudaEventSynchronize(t.ev[t.n]) != cudaSuccess) return -1;
+  const int n = t.n < cap ? t.n : cap;
+  for (int i = 0; i < n; ++i) {
+    if (cudaEventElapsedTime(&ms[i], t.ev[i], t.ev[i + 1]) != cudaSuccess) return -1;
+    if (names) names[i] = t.names[i];
+  }
+  return n;
+}
 
 int moe_sm_count(void) {
   int dev = 0, n = 0;

@@ -19,8 +19,32 @@ __device__ __forceinline__ void set_error(int* err, int code) {
 // Host side: address of this device's error word (api.cu).
 int* device_error_word();
 
+// Caller-supplied row indices of one token's k routed pairs (lane j < k holds
+// pair j's): a pair whose row is outside [0, R), or (when E > 0) whose expert
+// is outside [0, E), sets MOE_ERR_DEVICE_INDEX and is skipped by the caller.
+// Returns the warp-uniform mask of usable pairs (bit j).
+__device__ __forceinline__ unsigned usable_pairs(int row, int e, int lane, int k, long R, int E, int* err) {
+  const bool bad = lane < k && (row < 0 || row >= R || (E > 0 && (e < 0 || e >= E)));
+  const unsigned badm = __ballot_sync(0xffffffffu, bad);
+  if (badm && lane == 0) set_error(err, MOE_ERR_DEVICE_INDEX);
+  return ~badm;
+}
+
 // Host side: count one kernel launch (api.cu).
 void count_launch(int n = 1);
+
+// Host side: when the launch-timing recorder is armed (moe_timing_arm),
+// record a CUDA event on `st` just before the launch named `name` (api.cu).
+void mark_launch(cudaStream_t st, const char* name);
+
+// Names of the grouped GEMM kinds, for the launch-timing recorder.
+__host__ __forceinline__ const char* gemm_kind_name(int kind, bool mx) {
+  static const char* bf[] = {"gemm1_swiglu", "gemm2", "gemm2_dgrad_swiglu_bwd", "gemm1_dgrad",
+                             "gemm2_wgrad", "gemm1_wgrad", "router_gemm"};
+  static const char* q[] = {"mx_gemm1_swiglu", "mx_gemm2", "mx_gemm2_dgrad_swiglu_bwd", "mx_gemm1_dgrad",
+                            "mx_gemm2_wgrad", "mx_gemm1_wgrad", "mx_router_gemm"};
+  return (kind >= 0 && kind < 7) ? (mx ? q[kind] : bf[kind]) : "gemm";
+}
 
 // ---------------------------------------------------- 16-byte vector I/O
 // Load/store 16 bytes of T as floats: 8 bf16 or 4 fp32 elements.
@@ -91,5 +115,7 @@ __device__ __forceinline__ float warp_sum(float v) {
 
 #define MOE_LAUNCH_CHECK() MOE_CUDA_TRY(cudaGetLastError())
 
-// Prefix of every kernel launch: counts it, e.g. MOE_COUNTED kern<<<g, b, s, st>>>(args);
-#define MOE_COUNTED ::moe::count_launch(),
+// Prefix of every kernel launch: counts it and, when the launch-timing
+// recorder is armed, marks it on its stream, e.g.
+//   MOE_COUNTED_AS("permute", st) kern<<<g, b, s, st>>>(args);
+#define MOE_COUNTED_AS(name, st) ::moe::count_launch(), ::moe::mark_launch((st), (name)),

@@ -519,7 +519,7 @@ cudaError_t launch(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMa
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   const int grid = static_cast<int>(max_tiles < sm_count() ? max_tiles : sm_count());
-  MOE_COUNTED mx_gemm_kernel<KIND, TBN><<<grid, NUM_THREADS, smem, st>>>(a, b0, b1, p);
+  MOE_COUNTED_AS(::moe::gemm_kind_name(KIND, true), st) mx_gemm_kernel<KIND, TBN><<<grid, NUM_THREADS, smem, st>>>(a, b0, b1, p);
   return cudaGetLastError();
 }
 

@@ -166,21 +166,21 @@ cudaError_t launch_simt_gemm(const SimtGemm& g, cudaStream_t st) {
   } else {
     grid = dim3((g.M + BM - 1) / BM, (g.N + BN - 1) / BN, g.E);
   }
-  MOE_COUNTED simt_gemm_kernel<TA, TB, TC><<<grid, 256, 0, st>>>(g);
+  MOE_COUNTED_AS("simt_gemm", st) simt_gemm_kernel<TA, TB, TC><<<grid, 256, 0, st>>>(g);
   return cudaGetLastError();
 }
 
 template <typename T>
 cudaError_t launch_swiglu_fwd(const void* h, long rows, int f, void* a, cudaStream_t st) {
   if (rows == 0) return cudaSuccess;
-  MOE_COUNTED swiglu_fwd_kernel<T><<<1024, 256, 0, st>>>(static_cast<const T*>(h), rows, f, static_cast<T*>(a));
+  MOE_COUNTED_AS("swiglu_fwd", st) swiglu_fwd_kernel<T><<<1024, 256, 0, st>>>(static_cast<const T*>(h), rows, f, static_cast<T*>(a));
   return cudaGetLastError();
 }
 
 template <typename T>
 cudaError_t launch_swiglu_bwd(const void* da, const void* h, long rows, int f, void* dh, cudaStream_t st) {
   if (rows == 0) return cudaSuccess;
-  MOE_COUNTED swiglu_bwd_kernel<T><<<1024, 256, 0, st>>>(static_cast<const T*>(da), static_cast<const T*>(h), rows,
+  MOE_COUNTED_AS("swiglu_bwd", st) swiglu_bwd_kernel<T><<<1024, 256, 0, st>>>(static_cast<const T*>(da), static_cast<const T*>(h), rows,
                                              f, static_cast<T*>(dh));
   return cudaGetLastError();
 }

@@ -291,7 +291,7 @@ cudaError_t launch(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMa
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   const int grid = static_cast<int>(max_tiles < sm_count() ? max_tiles : sm_count());
-  MOE_COUNTED tc_gemm_kernel<KIND, GATHER><<<grid, NUM_THREADS, smem, st>>>(a, b0, b1, p);
+  MOE_COUNTED_AS(::moe::gemm_kind_name(KIND, false), st) tc_gemm_kernel<KIND, GATHER><<<grid, NUM_THREADS, smem, st>>>(a, b0, b1, p);
   return cudaGetLastError();
 }
 
@@ -487,7 +487,7 @@ cudaError_t launch_row256(const CUtensorMap& a, const CUtensorMap& b0, const CUt
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   const int grid = static_cast<int>(max_tiles < sm_count() ? max_tiles : sm_count());
-  MOE_COUNTED tc_row256_kernel<KIND><<<grid, NUM_THREADS, smem, st>>>(a, b0, b1, p);
+  MOE_COUNTED_AS(::moe::gemm_kind_name(KIND, false), st) tc_row256_kernel<KIND><<<grid, NUM_THREADS, smem, st>>>(a, b0, b1, p);
   return cudaGetLastError();
 }
 
@@ -794,7 +794,7 @@ cudaError_t launch_wgrad(const CUtensorMap& a, const CUtensorMap& b, const Param
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   const int grid = static_cast<int>(tiles < sm_count() ? tiles : sm_count());
-  MOE_COUNTED tc_wgrad_kernel<KIND, GATHER><<<grid, NUM_THREADS, smem, st>>>(a, b, p);
+  MOE_COUNTED_AS(::moe::gemm_kind_name(KIND, false), st) tc_wgrad_kernel<KIND, GATHER><<<grid, NUM_THREADS, smem, st>>>(a, b, p);
   return cudaGetLastError();
 }
 

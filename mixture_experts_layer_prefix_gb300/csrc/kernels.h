@@ -23,8 +23,8 @@ cudaError_t launch_route_meta(const float* logits, int T, int E, int k, int32_t*
 // scales as scale chunks grouped by per-expert 128-row tiles)
 cudaError_t launch_combine_bwd_quant(const void* dy, const void* y_perm, const float* gates,
                                      const int32_t* dest_row, const int32_t* topk_idx, const int32_t* offsets,
-                                     int Tn, int d, int k, uint8_t* q, uint8_t* qsc, void* dy_perm, float* dgates,
-                                     cudaStream_t st);
+                                     int Tn, int d, int k, int E, uint8_t* q, uint8_t* qsc, void* dy_perm,
+                                     float* dgates, cudaStream_t st);
 
 // ------------------------------------------------------ routing statistics
 size_t route_stats_workspace_bytes(int T, int E);
@@ -108,7 +108,7 @@ cudaError_t launch_mxfp8_quant_dual(const void* src, long rows, int C, uint8_t* 
                                     uint8_t* sc_r, cudaStream_t st);
 // Dispatch with the row quantisation fused: q [T*k][d], sc as scale chunks
 // grouped by per-expert 128-row tiles; the bf16 x_perm too when given.
-cudaError_t launch_permute_quant(const void* x, int T, int d, int k, const int32_t* dest_row,
+cudaError_t launch_permute_quant(const void* x, int T, int d, int k, int E, const int32_t* dest_row,
                                  const int32_t* topk_idx, const int32_t* offsets, uint8_t* q, uint8_t* sc,
                                  void* x_perm, cudaStream_t st);
 

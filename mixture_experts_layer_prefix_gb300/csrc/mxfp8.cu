@@ -288,16 +288,23 @@ quant_dual_kernel(const __nv_bfloat16* __restrict__ src, int C, long ntiles, uin
 // the GEMM's scale chunks, grouped by per-expert 128-row tiles.
 constexpr int kPermWarps = 8;
 __global__ void __launch_bounds__(kPermWarps * 32)
-permute_quant_kernel(const __nv_bfloat16* __restrict__ x, int T, int d, int k, const int32_t* __restrict__ dest_row,
-                     const int32_t* __restrict__ topk_idx, const int32_t* __restrict__ offs, uint8_t* __restrict__ q,
-                     uint8_t* __restrict__ sc, __nv_bfloat16* __restrict__ x_perm) {
+permute_quant_kernel(const __nv_bfloat16* __restrict__ x, int T, int d, int k, int E,
+                     const int32_t* __restrict__ dest_row, const int32_t* __restrict__ topk_idx,
+                     const int32_t* __restrict__ offs, uint8_t* __restrict__ q, uint8_t* __restrict__ sc,
+                     __nv_bfloat16* __restrict__ x_perm, int* err) {
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * kPermWarps + (threadIdx.x >> 5);
   if (t >= T) return;
-  int dest = 0, grp = 0, tt = 0;  // lane j < k: dispatched row j, its scale group and index in it
+  int dest = 0, grp = 0, tt = 0, e = 0;  // lane j < k: dispatched row j, its scale group and index in it
   if (lane < k) {
     dest = dest_row[(size_t)t * k + lane];
-    const int e = topk_idx[(size_t)t * k + lane], o = offs[e];
+    e = topk_idx[(size_t)t * k + lane];
+    // the pair's expert must hold its row (the scale chunk is found from it)
+    if (e >= 0 && e < E && (dest < offs[e] || dest >= offs[e + 1])) e = -1;
+  }
+  const unsigned ok = usable_pairs(dest, e, lane, k, (long)T * k, E, err);
+  if (lane < k && ((ok >> lane) & 1u)) {
+    const int o = offs[e];
     grp = static_cast<int>(mx_row_tile_base(o, e)) + ((dest - o) >> 7);
     tt = (dest - o) & 127;
   }
@@ -328,7 +335,7 @@ permute_quant_kernel(const __nv_bfloat16* __restrict__ x, int T, int d, int k, c
     for (int j = 0; j < k; ++j) {
       const int r = __shfl_sync(0xffffffffu, dest, j);
       const int g = __shfl_sync(0xffffffffu, grp, j), ti = __shfl_sync(0xffffffffu, tt, j);
-      if (!act) continue;
+      if (!act || !((ok >> j) & 1u)) continue;
       *reinterpret_cast<uint2*>(q + (size_t)r * d + c) = make_uint2(lo, hi);
       if (x_perm) *reinterpret_cast<uint4*>(x_perm + (size_t)r * d + c) = raw;
       const int b = c / 32;
@@ -340,13 +347,13 @@ permute_quant_kernel(const __nv_bfloat16* __restrict__ x, int T, int d, int k, c
 
 }  // namespace
 
-cudaError_t launch_permute_quant(const void* x, int T, int d, int k, const int32_t* dest_row,
+cudaError_t launch_permute_quant(const void* x, int T, int d, int k, int E, const int32_t* dest_row,
                                  const int32_t* topk_idx, const int32_t* offsets, uint8_t* q, uint8_t* sc,
                                  void* x_perm, cudaStream_t st) {
   if (T == 0) return cudaSuccess;
-  MOE_COUNTED permute_quant_kernel<<<(T + kPermWarps - 1) / kPermWarps, kPermWarps * 32, 0, st>>>(
-      static_cast<const __nv_bfloat16*>(x), T, d, k, dest_row, topk_idx, offsets, q, sc,
-      static_cast<__nv_bfloat16*>(x_perm));
+  MOE_COUNTED_AS("permute_quant", st) permute_quant_kernel<<<(T + kPermWarps - 1) / kPermWarps, kPermWarps * 32, 0, st>>>(
+      static_cast<const __nv_bfloat16*>(x), T, d, k, E, dest_row, topk_idx, offsets, q, sc,
+      static_cast<__nv_bfloat16*>(x_perm), device_error_word());
   return cudaGetLastError();
 }
 
@@ -358,11 +365,11 @@ cudaError_t launch_mxfp8_quant_rows(const void* src, long rows, long K, uint8_t*
   const auto* s = static_cast<const __nv_bfloat16*>(src);
   const int kb = static_cast<int>(K / 32);
   if (layout == kScalesPlain)
-    MOE_COUNTED quant_rows_kernel<kScalesPlain><<<grid, 256, 0, st>>>(s, nblocks, kb, q, sc, offsets, E);
+    MOE_COUNTED_AS("quant_rows", st) quant_rows_kernel<kScalesPlain><<<grid, 256, 0, st>>>(s, nblocks, kb, q, sc, offsets, E);
   else if (layout == kScalesChunk)
-    MOE_COUNTED quant_rows_kernel<kScalesChunk><<<grid, 256, 0, st>>>(s, nblocks, kb, q, sc, offsets, E);
+    MOE_COUNTED_AS("quant_rows", st) quant_rows_kernel<kScalesChunk><<<grid, 256, 0, st>>>(s, nblocks, kb, q, sc, offsets, E);
   else
-    MOE_COUNTED quant_rows_kernel<kScalesTiles><<<grid, 256, 0, st>>>(s, nblocks, kb, q, sc, offsets, E);
+    MOE_COUNTED_AS("quant_rows", st) quant_rows_kernel<kScalesTiles><<<grid, 256, 0, st>>>(s, nblocks, kb, q, sc, offsets, E);
   return cudaGetLastError();
 }
 
@@ -371,7 +378,7 @@ cudaError_t launch_mxfp8_quant_dual(const void* src, long rows, int C, uint8_t* 
   if (rows == 0) return cudaSuccess;
   const long ntiles = rows / 32 * (C / kDualCols);
   const long grid = std::min<long>(ntiles, (long)tc::sm_count() * 10);
-  MOE_COUNTED quant_dual_kernel<<<static_cast<unsigned>(grid), 128, 0, st>>>(static_cast<const __nv_bfloat16*>(src), C,
+  MOE_COUNTED_AS("quant_dual", st) quant_dual_kernel<<<static_cast<unsigned>(grid), 128, 0, st>>>(static_cast<const __nv_bfloat16*>(src), C,
                                                                            ntiles, qc, sc_c, qr, sc_r);
   return cudaGetLastError();
 }
@@ -385,10 +392,10 @@ cudaError_t launch_mxfp8_quant_cols(const void* src, int rows, int C, const int3
   dim3 grid(static_cast<unsigned>((C + 255) / 256), static_cast<unsigned>(groups < 65535 ? groups : 65535));
   const size_t smem = (nseg_eff + 1) * sizeof(int);
   if (packed)
-    MOE_COUNTED quant_cols_kernel<true><<<grid, 128, smem, st>>>(static_cast<const __nv_bfloat16*>(src), rows, C,
+    MOE_COUNTED_AS("quant_cols", st) quant_cols_kernel<true><<<grid, 128, smem, st>>>(static_cast<const __nv_bfloat16*>(src), rows, C,
                                                                  seg, nseg_eff, q, sc);
   else
-    MOE_COUNTED quant_cols_kernel<false><<<grid, 128, smem, st>>>(static_cast<const __nv_bfloat16*>(src), rows, C,
+    MOE_COUNTED_AS("quant_cols", st) quant_cols_kernel<false><<<grid, 128, smem, st>>>(static_cast<const __nv_bfloat16*>(src), rows, C,
                                                                   seg, nseg_eff, q, sc);
   return cudaGetLastError();
 }

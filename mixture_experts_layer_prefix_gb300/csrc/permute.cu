@@ -18,17 +18,19 @@ constexpr int kRowWarps = 8;
 template <typename T>
 __global__ void __launch_bounds__(kRowWarps * 32)
 permute_kernel(const T* __restrict__ x, int Tn, int d, int k, const int32_t* __restrict__ dest_row,
-               T* __restrict__ x_perm) {
+               T* __restrict__ x_perm, int* err) {
   using V = Vec16<T>;
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * kRowWarps + (threadIdx.x >> 5);
   if (t >= Tn) return;
   int dest = lane < k ? dest_row[(size_t)t * k + lane] : 0;
+  const unsigned ok = usable_pairs(dest, 0, lane, k, (long)Tn * k, 0, err);
   const T* src = x + (size_t)t * d;
   for (int c = lane * V::N; c < d; c += 32 * V::N) {
     const uint4 q = *reinterpret_cast<const uint4*>(src + c);
     for (int j = 0; j < k; ++j) {
       const int r = __shfl_sync(0xffffffffu, dest, j);
+      if (!((ok >> j) & 1u)) continue;
       *reinterpret_cast<uint4*>(x_perm + (size_t)r * d + c) = q;
     }
   }
@@ -38,13 +40,14 @@ permute_kernel(const T* __restrict__ x, int Tn, int d, int k, const int32_t* __r
 template <typename T>
 __global__ void __launch_bounds__(kRowWarps * 32)
 combine_fwd_kernel(const T* __restrict__ y_perm, const float* __restrict__ gates,
-                   const int32_t* __restrict__ dest_row, int Tn, int d, int k, T* __restrict__ y) {
+                   const int32_t* __restrict__ dest_row, int Tn, int d, int k, T* __restrict__ y, int* err) {
   using V = Vec16<T>;
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * kRowWarps + (threadIdx.x >> 5);
   if (t >= Tn) return;
   const int my_dest = lane < k ? dest_row[(size_t)t * k + lane] : 0;
   const float my_g = lane < k ? gates[(size_t)t * k + lane] : 0.0f;
+  const unsigned ok = usable_pairs(my_dest, 0, lane, k, (long)Tn * k, 0, err);
   int dest[8];
   float g[8];
 #pragma unroll
@@ -58,7 +61,7 @@ combine_fwd_kernel(const T* __restrict__ y_perm, const float* __restrict__ gates
     for (int i = 0; i < V::N; ++i) acc[i] = 0.0f;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-      if (j < k) {
+      if (j < k && ((ok >> j) & 1u)) {
         float v[V::N];
         V::load(y_perm + (size_t)dest[j] * d + c, v);
 #pragma unroll
@@ -80,15 +83,23 @@ template <typename T, int KMAX, bool QUANT = false>
 __global__ void __launch_bounds__(kRowWarps * 32)
 combine_bwd_kernel(const T* __restrict__ dy, const T* __restrict__ y_perm,
                    const float* __restrict__ gates, const int32_t* __restrict__ dest_row, int Tn,
-                   int d, int k, T* __restrict__ dy_perm, float* __restrict__ dgates, uint8_t* __restrict__ q = nullptr,
-                   uint8_t* __restrict__ qsc = nullptr, const int32_t* __restrict__ topk_idx = nullptr,
-                   const int32_t* __restrict__ offs = nullptr) {
+                   int d, int k, T* __restrict__ dy_perm, float* __restrict__ dgates, int* err,
+                   uint8_t* __restrict__ q = nullptr, uint8_t* __restrict__ qsc = nullptr,
+                   const int32_t* __restrict__ topk_idx = nullptr, const int32_t* __restrict__ offs = nullptr,
+                   int E = 0) {
   using V = Vec16<T>;
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * kRowWarps + (threadIdx.x >> 5);
   if (t >= Tn) return;
   const int my_dest = lane < k ? dest_row[(size_t)t * k + lane] : 0;
   const float my_g = lane < k ? gates[(size_t)t * k + lane] : 0.0f;
+  // QUANT: the pair's expert must hold its row (the scale chunk is found from it)
+  int my_e = 0;
+  if (QUANT && lane < k) {
+    my_e = topk_idx[(size_t)t * k + lane];
+    if (my_e >= 0 && my_e < E && (my_dest < offs[my_e] || my_dest >= offs[my_e + 1])) my_e = -1;
+  }
+  const unsigned ok = usable_pairs(my_dest, my_e, lane, k, (long)Tn * k, QUANT ? E : 0, err);
   int dest[KMAX];
   float g[KMAX], dot[KMAX];
 #pragma unroll
@@ -102,8 +113,8 @@ combine_bwd_kernel(const T* __restrict__ dy, const T* __restrict__ y_perm,
   size_t sbase[QUANT ? KMAX : 1];
   if constexpr (QUANT) {
     int my_grp = 0, my_t = 0;
-    if (lane < k) {
-      const int e = topk_idx[(size_t)t * k + lane], o = offs[e];
+    if (lane < k && ((ok >> lane) & 1u)) {
+      const int e = my_e, o = offs[e];
       my_grp = static_cast<int>(mx_row_tile_base(o, e)) + ((my_dest - o) >> 7);
       my_t = (my_dest - o) & 127;
     }
@@ -123,7 +134,7 @@ combine_bwd_kernel(const T* __restrict__ dy, const T* __restrict__ y_perm,
     if (act) V::load(dy + (size_t)t * d + c, u);
 #pragma unroll
     for (int j = 0; j < KMAX; ++j) {
-      if (j < k) {
+      if (j < k && ((ok >> j) & 1u)) {
         float v[V::N], w[V::N];
 #pragma unroll
         for (int i = 0; i < V::N; ++i) v[i] = 0.0f;
@@ -174,7 +185,7 @@ __global__ void __launch_bounds__(kRowWarps * 32)
 permute_bwd_kernel(const T* __restrict__ dx_perm, int Tn, int d, int E, int k,
                    const int32_t* __restrict__ dest_row, const int32_t* __restrict__ topk_idx,
                    const float* __restrict__ dlogits, const T* __restrict__ w_r,
-                   T* __restrict__ dx) {
+                   T* __restrict__ dx, int* err) {
   using V = Vec16<T>;
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * kRowWarps + (threadIdx.x >> 5);
@@ -182,11 +193,10 @@ permute_bwd_kernel(const T* __restrict__ dx_perm, int Tn, int d, int E, int k,
   const bool router = dlogits != nullptr;
   const int my_dest = lane < k ? dest_row[(size_t)t * k + lane] : 0;
   int my_e = 0;
+  if (router && lane < k) my_e = topk_idx[(size_t)t * k + lane];
+  const unsigned ok = usable_pairs(my_dest, my_e, lane, k, (long)Tn * k, router ? E : 0, err);
   float my_dl = 0.0f;
-  if (router && lane < k) {
-    my_e = topk_idx[(size_t)t * k + lane];
-    my_dl = dlogits[(size_t)t * E + my_e];
-  }
+  if (router && lane < k && ((ok >> lane) & 1u)) my_dl = dlogits[(size_t)t * E + my_e];
   int dest[8], ex[8];
   float dl[8];
 #pragma unroll
@@ -201,7 +211,7 @@ permute_bwd_kernel(const T* __restrict__ dx_perm, int Tn, int d, int E, int k,
     for (int i = 0; i < V::N; ++i) acc[i] = 0.0f;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-      if (j < k) {
+      if (j < k && ((ok >> j) & 1u)) {
         float v[V::N];
         V::load(dx_perm + (size_t)dest[j] * d + c, v);
 #pragma unroll
@@ -211,7 +221,7 @@ permute_bwd_kernel(const T* __restrict__ dx_perm, int Tn, int d, int E, int k,
     if (router) {
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        if (j < k) {
+        if (j < k && ((ok >> j) & 1u)) {
           float w[V::N];
           V::load(w_r + (size_t)ex[j] * d + c, w);
 #pragma unroll
@@ -323,8 +333,8 @@ template <typename T>
 cudaError_t launch_permute(const void* x, int Tn, int d, int k, const int32_t* dest_row, void* x_perm,
                            cudaStream_t st) {
   if (Tn == 0) return cudaSuccess;
-  MOE_COUNTED permute_kernel<T><<<row_grid<T>(Tn), kRowWarps * 32, 0, st>>>(
-      static_cast<const T*>(x), Tn, d, k, dest_row, static_cast<T*>(x_perm));
+  MOE_COUNTED_AS("permute", st) permute_kernel<T><<<row_grid<T>(Tn), kRowWarps * 32, 0, st>>>(
+      static_cast<const T*>(x), Tn, d, k, dest_row, static_cast<T*>(x_perm), device_error_word());
   return cudaGetLastError();
 }
 
@@ -332,8 +342,8 @@ template <typename T>
 cudaError_t launch_combine_fwd(const void* y_perm, const float* gates, const int32_t* dest_row, int Tn,
                                int d, int k, void* y, cudaStream_t st) {
   if (Tn == 0) return cudaSuccess;
-  MOE_COUNTED combine_fwd_kernel<T><<<row_grid<T>(Tn), kRowWarps * 32, 0, st>>>(
-      static_cast<const T*>(y_perm), gates, dest_row, Tn, d, k, static_cast<T*>(y));
+  MOE_COUNTED_AS("combine_fwd", st) combine_fwd_kernel<T><<<row_grid<T>(Tn), kRowWarps * 32, 0, st>>>(
+      static_cast<const T*>(y_perm), gates, dest_row, Tn, d, k, static_cast<T*>(y), device_error_word());
   return cudaGetLastError();
 }
 
@@ -343,30 +353,30 @@ cudaError_t launch_combine_bwd(const void* dy, const void* y_perm, const float* 
                                float* dgates, cudaStream_t st) {
   if (Tn == 0) return cudaSuccess;
   if (k <= 4)
-    MOE_COUNTED combine_bwd_kernel<T, 4><<<row_grid<T>(Tn), kRowWarps * 32, 0, st>>>(
+    MOE_COUNTED_AS("combine_bwd", st) combine_bwd_kernel<T, 4><<<row_grid<T>(Tn), kRowWarps * 32, 0, st>>>(
         static_cast<const T*>(dy), static_cast<const T*>(y_perm), gates, dest_row, Tn, d, k,
-        static_cast<T*>(dy_perm), dgates);
+        static_cast<T*>(dy_perm), dgates, device_error_word());
   else
-    MOE_COUNTED combine_bwd_kernel<T, 8><<<row_grid<T>(Tn), kRowWarps * 32, 0, st>>>(
+    MOE_COUNTED_AS("combine_bwd", st) combine_bwd_kernel<T, 8><<<row_grid<T>(Tn), kRowWarps * 32, 0, st>>>(
         static_cast<const T*>(dy), static_cast<const T*>(y_perm), gates, dest_row, Tn, d, k,
-        static_cast<T*>(dy_perm), dgates);
+        static_cast<T*>(dy_perm), dgates, device_error_word());
   return cudaGetLastError();
 }
 
 cudaError_t launch_combine_bwd_quant(const void* dy, const void* y_perm, const float* gates,
                                      const int32_t* dest_row, const int32_t* topk_idx, const int32_t* offsets,
-                                     int Tn, int d, int k, uint8_t* q, uint8_t* qsc, void* dy_perm, float* dgates,
-                                     cudaStream_t st) {
+                                     int Tn, int d, int k, int E, uint8_t* q, uint8_t* qsc, void* dy_perm,
+                                     float* dgates, cudaStream_t st) {
   using B = __nv_bfloat16;
   if (Tn == 0) return cudaSuccess;
   if (k <= 4)
-    MOE_COUNTED combine_bwd_kernel<B, 4, true><<<row_grid<B>(Tn), kRowWarps * 32, 0, st>>>(
+    MOE_COUNTED_AS("combine_bwd", st) combine_bwd_kernel<B, 4, true><<<row_grid<B>(Tn), kRowWarps * 32, 0, st>>>(
         static_cast<const B*>(dy), static_cast<const B*>(y_perm), gates, dest_row, Tn, d, k, static_cast<B*>(dy_perm),
-        dgates, q, qsc, topk_idx, offsets);
+        dgates, device_error_word(), q, qsc, topk_idx, offsets, E);
   else
-    MOE_COUNTED combine_bwd_kernel<B, 8, true><<<row_grid<B>(Tn), kRowWarps * 32, 0, st>>>(
+    MOE_COUNTED_AS("combine_bwd", st) combine_bwd_kernel<B, 8, true><<<row_grid<B>(Tn), kRowWarps * 32, 0, st>>>(
         static_cast<const B*>(dy), static_cast<const B*>(y_perm), gates, dest_row, Tn, d, k, static_cast<B*>(dy_perm),
-        dgates, q, qsc, topk_idx, offsets);
+        dgates, device_error_word(), q, qsc, topk_idx, offsets, E);
   return cudaGetLastError();
 }
 
@@ -375,9 +385,9 @@ cudaError_t launch_permute_bwd(const void* dx_perm, int Tn, int d, int E, int k,
                                const int32_t* dest_row, const int32_t* topk_idx, const float* dlogits,
                                const void* w_r, void* dx, cudaStream_t st) {
   if (Tn == 0) return cudaSuccess;
-  MOE_COUNTED permute_bwd_kernel<T><<<row_grid<T>(Tn), kRowWarps * 32, 0, st>>>(
+  MOE_COUNTED_AS("permute_bwd", st) permute_bwd_kernel<T><<<row_grid<T>(Tn), kRowWarps * 32, 0, st>>>(
       static_cast<const T*>(dx_perm), Tn, d, E, k, dest_row, topk_idx, dlogits,
-      static_cast<const T*>(w_r), static_cast<T*>(dx));
+      static_cast<const T*>(w_r), static_cast<T*>(dx), device_error_word());
   return cudaGetLastError();
 }
 
@@ -387,10 +397,10 @@ cudaError_t launch_route_bwd(const float* dgates, const float* gates, const int3
                              int Tn, int d, int E, int k, float* dlogits, float* dw_r,
                              cudaStream_t st) {
   if (Tn > 0)
-    MOE_COUNTED router_dlogits_kernel<<<row_grid<T>(Tn), kRowWarps * 32, 0, st>>>(dgates, gates, topk_idx, Tn,
+    MOE_COUNTED_AS("router_dlogits", st) router_dlogits_kernel<<<row_grid<T>(Tn), kRowWarps * 32, 0, st>>>(dgates, gates, topk_idx, Tn,
                                                                        E, k, dlogits);
   dim3 grid(E, (d + 255) / 256);
-  MOE_COUNTED router_dw_kernel<T><<<grid, 256, 0, st>>>(dlogits, offsets, src_row, static_cast<const T*>(x),
+  MOE_COUNTED_AS("router_dw", st) router_dw_kernel<T><<<grid, 256, 0, st>>>(dlogits, offsets, src_row, static_cast<const T*>(x),
                                             d, E, k, dw_r);
   return cudaGetLastError();
 }

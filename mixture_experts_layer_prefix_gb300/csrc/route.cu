@@ -222,7 +222,7 @@ cudaError_t launch_route_meta(const float* logits, int T, int E, int k, int32_t*
     const size_t smem = (size_t)kWarps * E * sizeof(int32_t);
     const int nv = (E + 31) / 32;
 #define MOE_TOPK_CASE(NVV)                                                                     \
-  MOE_COUNTED topk_hist_kernel<NVV><<<grid, kWarps * 32, smem, st>>>(logits, T, E, k, nchunks, topk_idx, \
+  MOE_COUNTED_AS("topk_hist", st) topk_hist_kernel<NVV><<<grid, kWarps * 32, smem, st>>>(logits, T, E, k, nchunks, topk_idx, \
                                                           gates, hist)
     if (nv <= 1) MOE_TOPK_CASE(1);
     else if (nv <= 2) MOE_TOPK_CASE(2);
@@ -234,12 +234,12 @@ cudaError_t launch_route_meta(const float* logits, int T, int E, int k, int32_t*
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
-  MOE_COUNTED chunk_scan_kernel<<<E, 1024, 0, st>>>(hist, nchunks, E, counts);
-  MOE_COUNTED offsets_kernel<<<1, 1024, 0, st>>>(counts, E, offsets);
+  MOE_COUNTED_AS("chunk_scan", st) chunk_scan_kernel<<<E, 1024, 0, st>>>(hist, nchunks, E, counts);
+  MOE_COUNTED_AS("offsets", st) offsets_kernel<<<1, 1024, 0, st>>>(counts, E, offsets);
   if (nchunks > 0) {
     const int grid = (nchunks + kWarps - 1) / kWarps;
     const size_t smem = (size_t)kWarps * E * sizeof(int32_t);
-    MOE_COUNTED rank_kernel<<<grid, kWarps * 32, smem, st>>>(topk_idx, hist, offsets, T, E, k, nchunks,
+    MOE_COUNTED_AS("rank", st) rank_kernel<<<grid, kWarps * 32, smem, st>>>(topk_idx, hist, offsets, T, E, k, nchunks,
                                                  dest_row, src_row, device_error_word());
   }
   return cudaGetLastError();

@@ -27,18 +27,16 @@ constexpr size_t kRouteScratchInts = size_t(1) << 20;
 // cleared between calls.
 __device__ __align__(256) int32_t g_route_scratch[kRouteScratchInts];
 
-// In host code g_route_scratch names a host-side stand-in, not device memory;
-// the device address is looked up once per device with that device current.
+// In host code g_route_scratch names a host-side stand-in, not device memory.
+// The device address is looked up on every call, for the device current on
+// the calling thread: a cached address would go stale if the device were
+// reset (or its primary context recreated) while the library stays loaded,
+// and a per-call lookup needs no shared state between host threads. The
+// first lookup on a device also loads the library's device code there.
 moe_status route_scratch(int32_t** out) {
-  static int32_t* ptrs[128] = {};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return MOE_ERR_CUDA;
-  if (!ptrs[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_route_scratch) != cudaSuccess || p == nullptr) return MOE_ERR_CUDA;
-    ptrs[dev] = static_cast<int32_t*>(p);
-  }
-  *out = ptrs[dev];
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_route_scratch) != cudaSuccess || p == nullptr) return MOE_ERR_CUDA;
+  *out = static_cast<int32_t*>(p);
   return MOE_OK;
 }
 

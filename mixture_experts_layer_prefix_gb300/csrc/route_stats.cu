@@ -116,9 +116,9 @@ cudaError_t launch_route_stats(const float* logits, const int32_t* counts, int T
                                float* stats, float* partial, cudaStream_t st) {
   const int nblk = (T + kStatTokensPerCta - 1) / kStatTokensPerCta;
   if (nblk > 0)
-    MOE_COUNTED route_stats_partial_kernel<<<nblk, kStatWarps * 32, kStatWarps * E * sizeof(float), st>>>(
+    MOE_COUNTED_AS("route_stats_partial", st) route_stats_partial_kernel<<<nblk, kStatWarps * 32, kStatWarps * E * sizeof(float), st>>>(
         logits, T, E, partial);
-  MOE_COUNTED route_stats_final_kernel<<<1, 1024, 0, st>>>(partial, nblk, counts, T, E, k, probs_mean, stats);
+  MOE_COUNTED_AS("route_stats_final", st) route_stats_final_kernel<<<1, 1024, 0, st>>>(partial, nblk, counts, T, E, k, probs_mean, stats);
   return cudaGetLastError();
 }
 

@@ -60,20 +60,25 @@ template <> struct Traits<WGRAD1> { static constexpr bool kragged = true, a_mn =
 // logits = x . W_r^T + bias, fp32 out (A K-major [T][d]; B K-major W_r[E][d])
 template <> struct Traits<ROUTER> { static constexpr bool kragged = false, a_mn = false, b_mn = false; };
 
-// Bounded wait on an mbarrier phase. On expiry: set the device error word and
-// the CTA's abort flag (so the other roles stop too) and return false.
-__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, int* abort_flag, int* err) {
+// Bounded wait on an mbarrier phase, at most `limit` SM cycles. On expiry:
+// set the device error word and the CTA's abort flag (so the other roles stop
+// too) and return false; a wait that sees the abort flag returns false too.
+__device__ __forceinline__ bool wait_bar_for(uint64_t* bar, uint32_t parity, int* abort_flag, int* err,
+                                             long long limit) {
   if (ptx::mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (true) {
     if (ptx::mbar_try_wait(bar, parity)) return true;
     if (*reinterpret_cast<volatile int*>(abort_flag)) return false;
-    if (clock64() - t0 > kWaitLimitCycles) {
+    if (clock64() - t0 > limit) {
       set_error(err, MOE_ERR_TIMEOUT);
       *reinterpret_cast<volatile int*>(abort_flag) = 1;
       return false;
     }
   }
+}
+__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, int* abort_flag, int* err) {
+  return wait_bar_for(bar, parity, abort_flag, err, kWaitLimitCycles);
 }
 
 struct Tile {

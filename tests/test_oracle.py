@@ -453,3 +453,147 @@ def test_route_stats_matches_library_softmax_and_is_label_invariant():
     pm2, st2 = oracle.route_stats(logits[:, perm], counts[perm], k)
     np.testing.assert_allclose(pm2, pm[perm], rtol=1e-13, atol=0)
     np.testing.assert_allclose(st2, st, rtol=1e-12, atol=0)
+
+
+# ------------------------------------- MXFP8 layer oracle: operand blocking of each GEMM
+# tests/mx_exact_inputs.py builds, per expert GEMM, inputs whose operands are
+# exactly representable under the blocking the oracle states for that GEMM and
+# lose a whole binade band under the transposed blocking. Three pins per GEMM:
+#   1. the oracle's quantised layer gives that GEMM's output bit for bit equal
+#      to its unquantised layer (its blocking keeps every value);
+#   2. the same GEMM with one operand blocked along the other axis (computed
+#      here from the oracle's own quantisers) loses a band: some output row or
+#      column changes by more than half its size -- so the oracle cannot be
+#      using that blocking;
+#   3. one input element given a 5-bit mantissa (17 * 2^p, not in E4M3) changes
+#      that GEMM's output -- so the operand is quantised at all.
+import mx_exact_inputs as MXI  # noqa: E402
+
+
+def _mx_run(c, quant):
+    from oracle import mxfp8_layer
+    return mxfp8_layer.layer(c["x"], c["w_r"], c["w_gate"], c["w_up"], c["w_down"], c["dy"], c["k"], c["logits"],
+                             quant=quant, store_bf16=False)
+
+
+def _slice_err(got, ref, how):
+    """Largest per-row ("row") or per-column ("col") error, each slice normalised by
+    its own largest reference magnitude (slices that are zero in both are skipped)."""
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    ax = -1 if how == "row" else -2
+    num = np.abs(got - ref).max(axis=ax)
+    den = np.abs(ref).max(axis=ax)
+    keep = (den > 0) | (num > 0)
+    return float((num[keep] / np.where(den[keep] > 0, den[keep], 1e-300)).max()) if keep.any() else 0.0
+
+
+def _blocked(v, axis, offsets=None):
+    """The oracle's MXFP8 fake-quantisation of v: 'k' = blocks of 32 along the last
+    axis; 'seg' = blocks of 32 rows from each expert segment's start; 'w' = blocks
+    of 32 rows of a single weight matrix."""
+    if axis == "k":
+        return oracle.mxfp8_fakequant_rows(v)
+    if axis == "seg":
+        return oracle.mxfp8_fakequant_cols_segmented(v, offsets)
+    return oracle.mxfp8_fakequant_cols_segmented(v, np.array([0, v.shape[0]], np.int32))
+
+
+def _gemm_out(name, r, c, a_axis, b_axis):
+    """The targeted GEMM recomputed from the unquantised run's operands, operand A
+    blocked along a_axis and B along b_axis (None: not quantised)."""
+    q = lambda v, ax, offs=None: v if ax is None else _blocked(v, ax, offs)  # noqa: E731
+    offs = r["offsets"]
+    E = c["w_gate"].shape[0]
+    f = c["w_gate"].shape[2]
+    segs = [(e, int(offs[e]), int(offs[e + 1])) for e in range(E) if offs[e + 1] > offs[e]]
+    xp = np.asarray(c["x"], np.float64)[r["src_row"] // c["k"]]
+    if name == "gemm1":
+        A, out = q(xp, a_axis, offs), np.zeros_like(r["hg"])
+        for e, r0, r1 in segs:
+            out[r0:r1] = A[r0:r1] @ q(c["w_gate"][e], b_axis)
+        return out
+    if name == "gemm2":
+        A, out = q(r["a"], a_axis, offs), np.zeros_like(r["ye"])
+        for e, r0, r1 in segs:
+            out[r0:r1] = A[r0:r1] @ q(c["w_down"][e], b_axis)
+        return out
+    if name.startswith("dgrad2"):  # da = dye . w_down^T (da is what dh is made of)
+        A, out = q(r["dye"], a_axis, offs), np.zeros((r["dye"].shape[0], f))
+        for e, r0, r1 in segs:
+            out[r0:r1] = A[r0:r1] @ q(c["w_down"][e], b_axis).T
+        return out
+    if name == "wgrad2":
+        A, B = q(r["a"], a_axis, offs), q(r["dye"], b_axis, offs)
+        out = np.zeros_like(r["dw_down"])
+        for e, r0, r1 in segs:
+            out[e] = A[r0:r1].T @ B[r0:r1]
+        return out
+    if name == "dgrad1":
+        A, out = q(r["dh"], a_axis, offs), np.zeros_like(r["dx_perm"])
+        for e, r0, r1 in segs:
+            out[r0:r1] = A[r0:r1, :f] @ q(c["w_gate"][e], b_axis).T + A[r0:r1, f:] @ q(c["w_up"][e], b_axis).T
+        return out
+    if name == "wgrad1":
+        A, B = q(xp, a_axis, offs), q(r["dh"], b_axis, offs)
+        out = np.zeros_like(r["dw_gate"])
+        for e, r0, r1 in segs:
+            out[e] = A[r0:r1].T @ B[r0:r1, :f]
+        return out
+    raise KeyError(name)
+
+
+# per case: the stated blocking of (A, B), and the transposed one of each
+_MX_AXES = {"gemm1": ("k", "w"), "gemm2": ("k", "w"), "dgrad2_w": ("k", "k"), "dgrad2_dy": ("k", "k"),
+            "wgrad2": ("seg", "seg"), "dgrad1": ("k", "k"), "wgrad1": ("seg", "seg")}
+_MX_WRONG = {"k": "seg", "seg": "k", "w": "k"}
+_MX_WRONG_B = {"gemm1": "k", "gemm2": "k", "dgrad2_w": "w", "dgrad2_dy": "w", "wgrad2": "k", "dgrad1": "w",
+               "wgrad1": "k"}
+# which operands each case discriminates (dgrad2 needs one case per operand)
+_MX_OPS = {"dgrad2_w": ("B",), "dgrad2_dy": ("A",)}
+
+
+@pytest.mark.parametrize("name", list(MXI.TARGETS))
+def test_mxfp8_oracle_blocking_is_exact_as_stated_and_not_transposed(name):
+    c = MXI.case(name)
+    rq, rp = _mx_run(c, True), _mx_run(c, False)
+    gemm, ops = MXI.TARGETS[name]
+    np.testing.assert_array_equal(rq["offsets"], [0, 67, 134, 200, 200])  # ragged segments, one empty
+    # 1. the oracle's quantised GEMM output is the unquantised one, bit for bit
+    for _, key, _ in ops:
+        np.testing.assert_array_equal(rq[key], rp[key], err_msg=f"{gemm}: {key}")
+    # the stated blocking recomputed here is exact too; with no quantisation at all it is the same product
+    a_ax, b_ax = _MX_AXES[name]
+    exact = _gemm_out(name, rp, c, None, None)
+    np.testing.assert_array_equal(_gemm_out(name, rp, c, a_ax, b_ax), exact)
+    # 2. each operand blocked along the other axis loses a band
+    which = _MX_OPS.get(name, ("A", "B"))
+    for (desc, key, how), op in zip(ops, which):
+        if op == "A":
+            alt = _gemm_out(name, rp, c, _MX_WRONG[a_ax], b_ax)
+        else:
+            alt = _gemm_out(name, rp, c, a_ax, _MX_WRONG_B[name])
+        assert _slice_err(alt, exact, how) > 0.5, f"{gemm}: {desc} transposed is not detected"
+
+
+# per case: an input element given a 5-bit mantissa, and the output that must change
+_MX_PERTURB = {"gemm1": [("x", (4, 9), "hg"), ("w_gate", (0, 3, 5), "hg")],
+               "gemm2": [("w_down", (1, 6, 2), "ye")],
+               "dgrad2_w": [("w_down", (0, 6, 0), "dh")],  # token 0: expert 0, dy at column 0
+               "dgrad2_dy": [("dy", (10, 5), "dh")],
+               "wgrad2": [("dy", (7, 4), "dw_down")],
+               "dgrad1": [("w_gate", (2, 8, 6), "dx_perm")],
+               "wgrad1": [("x", (3, 2 * ((7 * 3) % 64) + 1), "dw_gate")]}
+
+
+@pytest.mark.parametrize("name", list(MXI.TARGETS))
+def test_mxfp8_oracle_quantises_each_input_operand(name):
+    for key, idx, out in _MX_PERTURB[name]:
+        c = MXI.case(name)
+        v = c[key][idx]
+        assert v != 0.0
+        p = np.floor(np.log2(abs(v)))
+        c[key] = c[key].copy()
+        c[key][idx] = np.sign(v) * 17.0 * 2.0 ** (p - 4)  # 5 significant bits, same binade as before
+        rq, rp = _mx_run(c, True), _mx_run(c, False)
+        assert np.any(rq[out] != rp[out]), (name, key, out)

@@ -316,14 +316,17 @@ def measure(s, weights, steps, warmup, local, e2e=False, world=1):
         raise RuntimeError(f"device error word set in the timed region ({s.name})")
     peak_mem = torch.cuda.max_memory_allocated()
 
-    # ---- one more step, untimed, with every launch bracketed by its own events
-    # (two plain steps first, so the host runs ahead and no launch waits for it)
+    # ---- a few more steps, untimed, with every launch bracketed by its own
+    # events (two plain steps first, so the host runs ahead and no launch waits
+    # for it); per-kernel times are averaged over the steps
+    prof_steps = 5
     for _ in range(2):
         step_timed([mk() for _ in range(4)])
     N.moe_timing_arm(256)
-    step_timed([mk() for _ in range(4)])
+    for _ in range(prof_steps):
+        step_timed([mk() for _ in range(4)])
     N.moe_timing_finish(stream)
-    per_launch = N.moe_timing_read()
+    per_launch = [(n, ms / prof_steps) for n, ms in N.moe_timing_read()]
     torch.cuda.synchronize()
 
     out = dict(elapsed_ms=elapsed_ms, gemm_ms=gemm_ms, clocks=clk, launches=launches, per_launch=per_launch,
@@ -373,6 +376,9 @@ def kernel_table(s, per_launch, pk, pk_kind):
         a = agg.setdefault(name, {"launches": 0, "ms": 0.0})
         a["launches"] += 1
         a["ms"] += ms
+    steps_seen = max(1, min(a["launches"] for a in agg.values())) if agg else 1
+    for a in agg.values():
+        a["launches"] /= steps_seen  # launches per step
     total = sum(a["ms"] for a in agg.values()) or 1.0
     for name, a in agg.items():
         a["share"] = a["ms"] / total
@@ -458,8 +464,8 @@ def run_ours(args, s, rank, world):
                      "traffic_unit": "DRAM bytes per step of the six GEMM launches (ncu, see profiles/)",
                      "gemm_ms_per_step": m["gemm_ms"],
                      "per_kernel": kt,
-                     "per_kernel_how": "one untimed step after the timed region, every launch bracketed by CUDA "
-                                       "events on its stream (moe_timing_arm/finish/read)"},
+                     "per_kernel_how": "5 untimed steps after the timed region, every launch bracketed by CUDA "
+                                       "events on its stream (moe_timing_arm/finish/read); ms per step"},
         "e2e": {"value": world * s.T / (e2e_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": m["h2d"],
                 "d2h_bytes_per_step": m["d2h"], "ms_per_step": e2e_ms},
         "gpu_launches": m["launches"],

@@ -177,7 +177,9 @@ moe_status moe_grouped_mlp_fwd(const void* x_perm, const void* w_gate, const voi
      dw_gate[e] = sum_r x_perm[r]^T dh_g[r];  dw_up[e] = sum_r x_perm[r]^T dh_u[r]
    (sums over the rows of expert e; experts with no rows get zero
    gradients). dw_* are written (not accumulated), dtype. dh lives in the
-   workspace. */
+   workspace, and so does the order in which the weight-gradient GEMMs walk
+   the experts (most rows first, which balances their ragged cost across the
+   SMs); the workspace is needed even when R = 0 (bf16, MXFP8). */
 moe_status moe_grouped_mlp_bwd(const void* dy_perm, const void* x_perm, const void* h_save,
                                const void* a_save, const void* w_gate, const void* w_up,
                                const void* w_down, int dtype, const int32_t* offsets, int R, int E,

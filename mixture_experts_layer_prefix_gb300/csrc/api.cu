@@ -94,10 +94,11 @@ inline int storage(int dtype) { return dtype == MOE_MXFP8 ? MOE_BF16 : dtype; }
   } while (0)
 
 // Workspace of the backward GEMM chain: dh [R][2f], plus dA [R][f] on the
-// fp32 path (the bf16 path fuses the SwiGLU backward into the dA GEMM).
-size_t mlp_bwd_ws(long R, int f, int dtype) {
+// fp32 path (the bf16 path fuses the SwiGLU backward into the dA GEMM), or the
+// weight gradients' expert order [E] after dh on the bf16 path.
+size_t mlp_bwd_ws(long R, int E, int f, int dtype) {
   const size_t dh = align256((size_t)R * 2 * f * elem_bytes(dtype));
-  return dtype == MOE_F32 ? align256((size_t)R * f * elem_bytes(dtype)) + dh : dh;
+  return dtype == MOE_F32 ? align256((size_t)R * f * elem_bytes(dtype)) + dh : dh + align256((size_t)E * 4);
 }
 
 template <typename T>
@@ -171,7 +172,7 @@ size_t moe_workspace_size(int T, int d, int E, int k, int f, int dtype) {
   if (T < 0 || d <= 0 || E <= 0 || k <= 0 || f <= 0) return 0;
   const long R = (long)T * k;
   size_t route = align256(route_workspace_bytes(T, E));
-  size_t bwd = mlp_bwd_ws(R, f, dtype == MOE_F32 ? MOE_F32 : MOE_BF16);
+  size_t bwd = mlp_bwd_ws(R, E, f, dtype == MOE_F32 ? MOE_F32 : MOE_BF16);
   size_t ws = route > bwd ? route : bwd;
   const size_t stats = align256(route_stats_workspace_bytes(T, E));
   ws = ws > stats ? ws : stats;
@@ -348,11 +349,11 @@ moe_status moe_grouped_mlp_bwd(const void* dy_perm, const void* x_perm, const vo
                             dx_perm, dw_gate, dw_up, dw_down, workspace, S(stream)));
     return MOE_OK;
   }
-  if (workspace_bytes < mlp_bwd_ws(R, f, dtype)) return MOE_ERR_WORKSPACE;
+  if (workspace_bytes < mlp_bwd_ws(R, E, f, dtype)) return MOE_ERR_WORKSPACE;
   if (R > 0) {
     MOE_NEED(dy_perm); MOE_NEED(x_perm); MOE_NEED(h_save); MOE_NEED(a_save); MOE_NEED(dx_perm);
-    MOE_NEED(workspace);
   }
+  if (R > 0 || dtype != MOE_F32) MOE_NEED(workspace);  // bf16: the expert order table lives there
   if (dtype == MOE_F32)
     return mlp_bwd_simt<float>(dy_perm, x_perm, h_save, a_save, w_gate, w_up, w_down, offsets, R, E, d,
                                f, dx_perm, dw_gate, dw_up, dw_down, workspace, S(stream));
@@ -488,10 +489,11 @@ moe_status moe_dispatch_mlp_bwd(const void* dy_perm, const void* x, const int32_
   MOE_NEED(w_gate); MOE_NEED(w_up); MOE_NEED(w_down); MOE_NEED(offsets);
   MOE_NEED(dw_gate); MOE_NEED(dw_up); MOE_NEED(dw_down);
   const int R = T * k;
-  if (workspace_bytes < mlp_bwd_ws(R, f, dtype)) return MOE_ERR_WORKSPACE;
+  if (workspace_bytes < mlp_bwd_ws(R, E, f, dtype)) return MOE_ERR_WORKSPACE;
+  MOE_NEED(workspace);  // the expert order table lives there even when R = 0
   if (R > 0) {
     MOE_NEED(dy_perm); MOE_NEED(x); MOE_NEED(src_row); MOE_NEED(h_save); MOE_NEED(a_save);
-    MOE_NEED(dx_perm); MOE_NEED(workspace);
+    MOE_NEED(dx_perm);
   }
   MOE_CUDA_TRY(tc_mlp_bwd(dy_perm, x, h_save, a_save, w_gate, w_up, w_down, offsets, R, E, d, f, dx_perm,
                           dw_gate, dw_up, dw_down, workspace, S(stream), src_row, k, T));

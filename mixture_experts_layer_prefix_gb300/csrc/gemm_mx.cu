@@ -251,7 +251,7 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     }
     uint32_t it = 0;
     bool ok = true;
-    for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+    for (int r = 0, t = sched_tile<Tr::kragged>(0); t < total && ok; t = sched_tile<Tr::kragged>(++r)) {
       const Tile tl = decode<KIND, BK>(t, p, offs, tstart);
       for (int kb = 0; kb < tl.nkb; ++kb, ++it) {
         const int s = it % STAGES;
@@ -346,7 +346,7 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     // ========================================================= MMA issuer
     uint32_t it = 0, acc_it = 0;
     bool ok = true;
-    for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+    for (int r = 0, t = sched_tile<Tr::kragged>(0); t < total && ok; t = sched_tile<Tr::kragged>(++r)) {
       const Tile tl = decode<KIND, BK>(t, p, offs, tstart);
       if (tl.nkb == 0) continue;
       const int buf = G::ACC == 2 ? (acc_it & 1) : 0;
@@ -410,7 +410,7 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     uint8_t* stg = stg_area + ew * STG_BYTES;
     constexpr int NC = KIND == FPROP1 ? 4 : TBN / 32;  // chunks of the tile (FPROP1: gate/up pairs)
     uint32_t acc_it = 0;
-    for (int t = blockIdx.x; t < total; t += gridDim.x) {
+    for (int r = 0, t = sched_tile<Tr::kragged>(0); t < total; t = sched_tile<Tr::kragged>(++r)) {
       const Tile tl = decode<KIND, BK>(t, p, offs, tstart);
       if (tl.nkb == 0) {  // wgrad of an expert without rows: dW_e = 0
         uint32_t z[16];
@@ -595,7 +595,8 @@ size_t bwd_workspace(long R, int E, int d, int f) {
          + al(R * 2 * (size_t)f) + al(tile_scale_bytes(R, E, 2L * f))      // dh rows
          + al(R * 2 * (size_t)f) + al(seg_words_bytes(R, E, 2L * f))            // dh segment columns
          + 2 * (al(Ed * f) + al(Ed * f / 32))                              // w_gate, w_up rows
-         + al(R * (size_t)d) + al(seg_words_bytes(R, E, d));                   // x segment columns
+         + al(R * (size_t)d) + al(seg_words_bytes(R, E, d))                    // x segment columns
+         + al((size_t)E * 4);                                              // expert order
 }
 
 }  // namespace mx
@@ -670,10 +671,13 @@ cudaError_t mx_mlp_bwd(const void* dy_perm, const void* x_perm, const void* h, c
   QBuf wgr = cv.take((size_t)Ed * f, (size_t)Ed * f / 32);
   QBuf wur = cv.take((size_t)Ed * f, (size_t)Ed * f / 32);
   QBuf xc = cv.take((size_t)R * d, seg_words_bytes(R, E, d));
+  int32_t* order = reinterpret_cast<int32_t*>(cv.p + cv.used);
   cudaError_t e;
   CUtensorMap mA, mB0, mB1;
   Params p{};
   p.offsets = offsets; p.E = E; p.R = R; p.d = d; p.f = f; p.err = device_error_word();
+  // the weight gradients walk their experts largest first
+  if ((e = launch_expert_order(offsets, E, order, st)) != cudaSuccess) return e;
 
   // dA = dy . Wd^T (K = d): dy rows (already quantised when the combine
   // backward did it), w_down rows; SwiGLU backward fused -> dh
@@ -711,7 +715,9 @@ cudaError_t mx_mlp_bwd(const void* dy_perm, const void* x_perm, const void* h, c
   p.M = f; p.N = d; p.m_tiles = (f + BM - 1) / BM; p.n_tiles = (d + kN_WGRAD - 1) / kN_WGRAD; p.out0 = dwd;
   p.aux = nullptr;
   p.sfa = ac.s; p.sfb0 = dyc.s;
+  p.order = order;
   if ((e = launch<WGRAD2, kN_WGRAD>(mA, mB0, mB0, p, (long)E * p.m_tiles * p.n_tiles, st)) != cudaSuccess) return e;
+  p.order = nullptr;
 
   // dx_perm = dh . [Wg | Wu]^T (K = 2f): dh rows, w_gate / w_up rows
   if (wq) {
@@ -735,6 +741,7 @@ cudaError_t mx_mlp_bwd(const void* dy_perm, const void* x_perm, const void* h, c
     return cudaErrorInvalidValue;
   p.M = d; p.N = 2 * f; p.m_tiles = (d + BM - 1) / BM; p.n_tiles = (2 * f + kN_WGRAD - 1) / kN_WGRAD;
   p.out0 = dwg; p.out1 = dwu; p.sfa = xc.s; p.sfb0 = dhc.s; p.sfb1 = nullptr;
+  p.order = order;
   return launch<WGRAD1, kN_WGRAD>(mA, mB0, mB0, p, (long)E * p.m_tiles * p.n_tiles, st);
 }
 

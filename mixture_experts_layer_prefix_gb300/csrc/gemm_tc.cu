@@ -541,7 +541,7 @@ tc_wgrad_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
   const int total = p.E * per;
   const uint32_t tmem = sm->tmem_base;
   auto decode_w = [&](int t, int& e, int& m0, int& n0, int& r0, int& r1, int& nkb) {
-    e = t / per;
+    e = p.order ? __ldg(p.order + t / per) : t / per;
     const int local = t % per;
     m0 = (local / p.n_tiles) * WBM;
     n0 = (local % p.n_tiles) * BN;
@@ -558,7 +558,7 @@ tc_wgrad_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         ptx::prefetch_tmap(&tmB);
         uint32_t it = 0;
         bool ok = true;
-        for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+        for (int r = 0, t = sched_tile<true>(0); t < total && ok; t = sched_tile<true>(++r)) {
           int e, m0, n0, r0, r1, nkb;
           decode_w(t, e, m0, n0, r0, r1, nkb);
           for (int kb = 0; kb < nkb; ++kb, ++it) {
@@ -598,7 +598,7 @@ tc_wgrad_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
       const int grp = lane & 15, jb = (lane >> 4) * 2;
       uint32_t it = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+      for (int r = 0, t = sched_tile<true>(0); t < total && ok; t = sched_tile<true>(++r)) {
         int e, m0, n0, r0, r1, nkb;
         decode_w(t, e, m0, n0, r0, r1, nkb);
         auto tokens = [&](int kb, int (&tk)[4]) {
@@ -651,7 +651,7 @@ tc_wgrad_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     constexpr uint32_t idesc = ptx::idesc_bf16_f32(BM, BN, 1, 1);
     uint32_t it = 0, acc_it = 0;
     bool ok = true;
-    for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+    for (int r = 0, t = sched_tile<true>(0); t < total && ok; t = sched_tile<true>(++r)) {
       int e, m0, n0, r0, r1, nkb;
       decode_w(t, e, m0, n0, r0, r1, nkb);
       if (nkb == 0) continue;
@@ -711,7 +711,7 @@ tc_wgrad_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     // next tile's MMAs start while this tile's stores go out.
     const int ew = warp - 2, q = warp & 3, mh = ew >> 2;
     uint32_t acc_it = 0;
-    for (int t = blockIdx.x; t < total; t += gridDim.x) {
+    for (int r = 0, t = sched_tile<true>(0); t < total; t = sched_tile<true>(++r)) {
       int e, m0, n0, r0, r1, nkb;
       decode_w(t, e, m0, n0, r0, r1, nkb);
       uint32_t hold[BN / 2];
@@ -800,6 +800,25 @@ cudaError_t launch_wgrad(const CUtensorMap& a, const CUtensorMap& b, const Param
 
 constexpr CUtensorMapDataType BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
 
+// Experts ordered by row count, largest first, ties by index (order[i] = the
+// expert of rank i): the walk order of the weight-gradient tiles, whose cost
+// is their expert's row count. One block; E <= 1024.
+__global__ void __launch_bounds__(1024) expert_order_kernel(const int32_t* __restrict__ offsets, int E,
+                                                            int32_t* __restrict__ order) {
+  __shared__ int cnt[1024];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = offsets[e + 1] - offsets[e];
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    const int c = cnt[e];
+    int rank = 0;
+    for (int j = 0; j < E; ++j) {
+      const int cj = cnt[j];
+      rank += (cj > c) | ((cj == c) & (j < e));
+    }
+    order[rank] = e;
+  }
+}
+
 }  // namespace
 
 // ------------------------------------------------------------ shared host
@@ -856,6 +875,12 @@ int sm_count() {
 
 using namespace tc;
 
+cudaError_t launch_expert_order(const int32_t* offsets, int E, int32_t* order, cudaStream_t st) {
+  if (E <= 0 || E > 1024) return cudaErrorInvalidValue;
+  MOE_COUNTED_AS("expert_order", st) expert_order_kernel<<<1, 1024, 0, st>>>(offsets, E, order);
+  return cudaGetLastError();
+}
+
 cudaError_t tc_mlp_fwd(const void* x_perm, const void* wg, const void* wu, const void* wd,
                        const int32_t* offsets, int R, int E, int d, int f, void* h, void* a, void* y,
                        cudaStream_t st, const int32_t* src_row, int gk, int T) {
@@ -889,6 +914,9 @@ cudaError_t tc_mlp_bwd(const void* dy_perm, const void* x_perm, const void* h, c
   Params p{};
   p.offsets = offsets; p.E = E; p.R = R; p.d = d; p.f = f; p.err = device_error_word();
   cudaError_t e;
+  // the weight gradients walk their experts largest first (order table after dh)
+  int32_t* order = reinterpret_cast<int32_t*>(static_cast<char*>(dh) + (((size_t)R * 2 * f * 2 + 255) & ~size_t(255)));
+  if ((e = launch_expert_order(offsets, E, order, st)) != cudaSuccess) return e;
   // dA = dy . Wd^T with the SwiGLU backward fused: writes dh
   if (!map_2d(&mA, dy_perm, BF, 2, d, R, 64, BM) || !map_3d(&mB0, wd, BF, 2, d, f, E, 64, BN))
     return cudaErrorInvalidValue;
@@ -899,7 +927,9 @@ cudaError_t tc_mlp_bwd(const void* dy_perm, const void* x_perm, const void* h, c
   if (!map_2d(&mA, a, BF, 2, f, R, 64, 64) || !map_2d(&mB0, dy_perm, BF, 2, d, R, 64, 64))
     return cudaErrorInvalidValue;
   p.M = f; p.N = d; p.m_tiles = (f + WBM - 1) / WBM; p.n_tiles = (d + BN - 1) / BN; p.out0 = dwd;
+  p.order = order;
   e = launch_wgrad<WGRAD2>(mA, mB0, p, st);
+  p.order = nullptr;
   if (e != cudaSuccess) return e;
   // dx_perm = dh_g . Wg^T + dh_u . Wu^T
   if (!map_2d(&mA, dh, BF, 2, 2L * f, R, 64, BM) || !map_3d(&mB0, wg, BF, 2, f, d, E, 64, BN) ||
@@ -914,6 +944,7 @@ cudaError_t tc_mlp_bwd(const void* dy_perm, const void* x_perm, const void* h, c
   p.M = d; p.N = 2 * f; p.m_tiles = (d + WBM - 1) / WBM; p.n_tiles = (2 * f + BN - 1) / BN;
   p.out0 = dwg; p.out1 = dwu;
   p.src_row = src_row; p.gk = gk; p.T = T;
+  p.order = order;
   return src_row ? launch_wgrad<WGRAD1, true>(mA, mB0, p, st) : launch_wgrad<WGRAD1>(mA, mB0, p, st);
 }
 

@@ -112,6 +112,9 @@ cudaError_t launch_permute_quant(const void* x, int T, int d, int k, int E, cons
                                  const int32_t* topk_idx, const int32_t* offsets, uint8_t* q, uint8_t* sc,
                                  void* x_perm, cudaStream_t st);
 
+// Experts by row count, largest first (ties by index), into order [E]; E <= 1024.
+cudaError_t launch_expert_order(const int32_t* offsets, int E, int32_t* order, cudaStream_t st);
+
 cudaError_t tc_router_logits(const void* x, const void* w_r, const float* bias, int T, int d, int E,
                              float* logits, cudaStream_t st);
 

@@ -269,59 +269,65 @@ router_dlogits_kernel(const float* __restrict__ dgates, const float* __restrict_
 // dw_r[e][c] = sum over rows r of expert e of dlogits[t(r)][e] * x[t(r)][c],
 // t(r) = src_row[r] / k. The token rows are gathered from x (T rows, which
 // stay in L2 across the k experts that read each) rather than from the
-// k-times larger x_perm. Grid (E, ceil(d / 256)); 8 warps split the rows,
-// each lane owns 8 columns; warps are reduced in fixed order through shared
-// memory.
+// k-times larger x_perm. Grid (E, d / 64): a CTA owns 64 columns of one
+// expert, so a heavily loaded expert's rows spread over d / 64 CTAs. A warp
+// reads RPW rows at once (LPR lanes of 16 bytes per row); the row groups of a
+// warp are added by a fixed shuffle tree and the 8 warps in fixed order
+// through shared memory, so the result is bit-reproducible.
 template <typename T>
 __global__ void __launch_bounds__(256)
 router_dw_kernel(const float* __restrict__ dlogits, const int32_t* __restrict__ offsets,
                  const int32_t* __restrict__ src_row, const T* __restrict__ x, int d, int E,
                  int k, float* __restrict__ dw_r) {
-  constexpr int VN = Vec16<T>::N;
-  constexpr int COLS = 32 * VN;  // columns per warp pass
-  __shared__ float part[8][256];
+  constexpr int VN = Vec16<T>::N;   // elements per 16 bytes
+  constexpr int COLS = 64;          // columns per CTA
+  constexpr int LPR = COLS / VN;    // lanes per row
+  constexpr int RPW = 32 / LPR;     // rows a warp reads at once
+  constexpr int STEP = 8 * RPW;     // rows the CTA reads at once
+  __shared__ float part[8][COLS];
   const int e = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int grp = lane / LPR, sub = lane % LPR;
+  const int c = blockIdx.y * COLS + sub * VN;  // d % 64 == 0: always inside the row
   const int r0 = offsets[e], r1 = offsets[e + 1];
-  for (int cbase = blockIdx.y * 256; cbase < min(d, (int)(blockIdx.y + 1) * 256); cbase += COLS) {
-    const int c = cbase + lane * VN;
-    float acc[VN];
+  float acc[VN];
 #pragma unroll
-    for (int i = 0; i < VN; ++i) acc[i] = 0.0f;
-    if (c < d) {
-      int r = r0 + warp;
-      for (; r + 24 < r1; r += 32) {
-        float v[4][VN], w[4];
+  for (int i = 0; i < VN; ++i) acc[i] = 0.0f;
+  int r = r0 + warp * RPW + grp;
+  for (; r + 3 * STEP < r1; r += 4 * STEP) {
+    float v[4][VN], w[4];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int t = src_row[r + 8 * u] / k;
-          w[u] = dlogits[(size_t)t * E + e];
-          Vec16<T>::load(x + (size_t)t * d + c, v[u]);
-        }
-#pragma unroll
-        for (int u = 0; u < 4; ++u)
-#pragma unroll
-          for (int i = 0; i < VN; ++i) acc[i] = fmaf(w[u], v[u][i], acc[i]);
-      }
-      for (; r < r1; r += 8) {
-        float v[VN];
-        const int t = src_row[r] / k;
-        const float w = dlogits[(size_t)t * E + e];
-        Vec16<T>::load(x + (size_t)t * d + c, v);
-#pragma unroll
-        for (int i = 0; i < VN; ++i) acc[i] = fmaf(w, v[i], acc[i]);
-      }
+    for (int u = 0; u < 4; ++u) {
+      const int t = src_row[r + u * STEP] / k;
+      w[u] = dlogits[(size_t)t * E + e];
+      Vec16<T>::load(x + (size_t)t * d + c, v[u]);
     }
 #pragma unroll
-    for (int i = 0; i < VN; ++i) part[warp][(lane * VN + i) % 256] = acc[i];
-    __syncthreads();
-    const int cc = cbase + threadIdx.x;
-    if (threadIdx.x < COLS && cc < d) {
-      float s = 0.0f;
+    for (int u = 0; u < 4; ++u)
 #pragma unroll
-      for (int w = 0; w < 8; ++w) s += part[w][threadIdx.x];
-      dw_r[(size_t)e * d + cc] = s;
-    }
-    __syncthreads();
+      for (int i = 0; i < VN; ++i) acc[i] = fmaf(w[u], v[u][i], acc[i]);
+  }
+  for (; r < r1; r += STEP) {
+    float v[VN];
+    const int t = src_row[r] / k;
+    const float w = dlogits[(size_t)t * E + e];
+    Vec16<T>::load(x + (size_t)t * d + c, v);
+#pragma unroll
+    for (int i = 0; i < VN; ++i) acc[i] = fmaf(w, v[i], acc[i]);
+  }
+#pragma unroll
+  for (int o = LPR; o < 32; o <<= 1)
+#pragma unroll
+    for (int i = 0; i < VN; ++i) acc[i] += __shfl_xor_sync(0xffffffffu, acc[i], o);
+  if (grp == 0) {
+#pragma unroll
+    for (int i = 0; i < VN; ++i) part[warp][sub * VN + i] = acc[i];
+  }
+  __syncthreads();
+  if (threadIdx.x < COLS) {
+    float s = 0.0f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) s += part[w][threadIdx.x];
+    dw_r[(size_t)e * d + blockIdx.y * COLS + threadIdx.x] = s;
   }
 }
 
@@ -399,7 +405,7 @@ cudaError_t launch_route_bwd(const float* dgates, const float* gates, const int3
   if (Tn > 0)
     MOE_COUNTED_AS("router_dlogits", st) router_dlogits_kernel<<<row_grid<T>(Tn), kRowWarps * 32, 0, st>>>(dgates, gates, topk_idx, Tn,
                                                                        E, k, dlogits);
-  dim3 grid(E, (d + 255) / 256);
+  dim3 grid(E, d / 64);
   MOE_COUNTED_AS("router_dw", st) router_dw_kernel<T><<<grid, 256, 0, st>>>(dlogits, offsets, src_row, static_cast<const T*>(x),
                                             d, E, k, dw_r);
   return cudaGetLastError();

@@ -41,6 +41,9 @@ struct Params {
   // row src_row[r] / gk of x [T][d] (A's tensor map); nullptr: A is x_perm.
   const int32_t* src_row;
   int gk, T;
+  // Weight-gradient kinds: experts in the order their tiles are walked
+  // (largest row count first, from expert_order_kernel); nullptr: 0..E-1.
+  const int32_t* order;
   int* err;
 };
 
@@ -85,6 +88,17 @@ struct Tile {
   int e, m0, row_end, n_idx, m_idx, nkb, k_row0;
 };
 
+// Tile index of this CTA's r-th tile. Row-tile kinds stride over the tile list
+// (tile cost is the same K for every tile). Weight-gradient tiles cost their
+// expert's row count, and their list runs from the largest expert down (the
+// expert order table): those are walked in a snake over the CTAs (even rounds
+// CTA b takes slot b, odd rounds slot G-1-b), so a falling cost spreads evenly.
+template <bool KRAGGED>
+__device__ __forceinline__ int sched_tile(int r) {
+  const int g = gridDim.x, b = blockIdx.x;
+  return KRAGGED ? r * g + ((r & 1) ? g - 1 - b : b) : b + r * g;
+}
+
 template <int KIND>
 __device__ __forceinline__ int gemm_k(const Params& p) {
   return (KIND == FPROP1 || KIND == DGRAD2 || KIND == ROUTER) ? p.d : (KIND == FPROP2 ? p.f : 2 * p.f);
@@ -112,7 +126,7 @@ __device__ __forceinline__ Tile decode(int t, const Params& p, const int* offs, 
     tl.k_row0 = 0;
   } else {
     const int per = p.m_tiles * p.n_tiles;
-    tl.e = t / per;
+    tl.e = p.order ? __ldg(p.order + t / per) : t / per;
     const int local = t % per;
     tl.m_idx = local / p.n_tiles;
     tl.n_idx = local % p.n_tiles;

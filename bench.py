@@ -249,7 +249,7 @@ def measure(s, weights, steps, warmup, local, e2e=False, world=1):
             N.moe_permute_mxfp8(p.x, T, d, k, E, b.dest_row, b.topk_idx, b.offsets, b.x_q, b.x_sc, b.x_perm)
             ev[0].record(stream)
             N.moe_mxfp8_mlp_fwd(b.x_q, b.x_sc, b.wq, b.offsets, b.R, E, d, f, b.h_save, b.a_save, b.y_perm,
-                                b.workspace)
+                                b.a_cols, b.workspace)
         elif fused:  # the dispatch runs inside GEMM1 (rows gathered from x)
             ev[0].record(stream)
             N.moe_dispatch_mlp_fwd(p.x, b.src_row, T, k, p.w_gate, p.w_up, p.w_down, dt, b.offsets, E, d, f,
@@ -270,8 +270,8 @@ def measure(s, weights, steps, warmup, local, e2e=False, world=1):
                         b.dlogits, b.dw_router)
         ev[2].record(stream)
         if mx:
-            N.moe_mxfp8_mlp_bwd(b.dy_q, b.dy_sc, b.dy_perm, b.x_perm, b.h_save, b.a_save, b.wq, b.offsets, b.R, E,
-                                d, f, b.dx_perm, b.dw_gate, b.dw_up, b.dw_down, b.workspace)
+            N.moe_mxfp8_mlp_bwd(b.dy_q, b.dy_sc, b.dy_perm, b.x_perm, b.h_save, b.a_save, b.a_cols, b.wq, b.offsets,
+                                b.R, E, d, f, b.dx_perm, b.dw_gate, b.dw_up, b.dw_down, b.workspace)
         elif fused:
             N.moe_dispatch_mlp_bwd(b.dy_perm, p.x, b.src_row, T, k, b.h_save, b.a_save, p.w_gate, p.w_up,
                                    p.w_down, dt, b.offsets, E, d, f, b.dx_perm, b.dw_gate, b.dw_up, b.dw_down,

@@ -255,12 +255,23 @@ moe_status moe_dispatch_mlp_bwd(const void* dy_perm, const void* x, const int32_
 
    moe_mxfp8_mlp_fwd: moe_grouped_mlp_fwd(MOE_MXFP8) with GEMM1 reading
    x_codes/x_scales and the weights read from wq (no quantisation pass of its
-   own). Same outputs, same workspace.
+   own). Same outputs, same workspace. a_cols (optional, may be NULL; device,
+   moe_mxfp8_col_operand_size(R, E, f) bytes, 16-byte aligned): GEMM1's
+   epilogue also writes A = silu(h_g) * h_u quantised along the experts' rows
+   (blocks of 32 rows from each expert's first row, the tail block
+   zero-padded) -- the GEMM2 weight gradient's A operand -- so that the
+   backward need not quantise a_save again.
 
    moe_mxfp8_mlp_bwd: moe_grouped_mlp_bwd(MOE_MXFP8) with the GEMM2 dgrad
    reading dy_codes/dy_scales and the weights read from wq; dy_perm and
    x_perm (bf16) feed the expert-segment quantisations of the weight
-   gradients. Same outputs, same workspace. d and f multiples of 128. */
+   gradients, and a_save that of A unless a_cols (what moe_mxfp8_mlp_fwd wrote
+   there for the same step, or NULL) is given. Same outputs (bit for bit with
+   or without a_cols), same workspace. d and f multiples of 128.
+
+   moe_mxfp8_col_operand_size: bytes of an operand of R rows and K columns
+   quantised along the experts' rows: E4M3 codes [R][K] (padded to 256 bytes)
+   followed by its scale chunks (0 unless K % 128 == 0). */
 size_t moe_mxfp8_weights_size(int E, int d, int f);
 moe_status moe_mxfp8_prepare_weights(const void* w_gate, const void* w_up, const void* w_down, int E, int d, int f,
                                      void* wq, size_t wq_bytes, void* stream);
@@ -271,13 +282,15 @@ moe_status moe_permute_mxfp8(const void* x, int T, int d, int k, int E, const in
 moe_status moe_combine_bwd_mxfp8(const void* dy, const void* y_perm, const float* gates, const int32_t* dest_row,
                                  const int32_t* topk_idx, const int32_t* offsets, int T, int d, int k, int E,
                                  uint8_t* dy_codes, uint8_t* dy_scales, void* dy_perm, float* dgates, void* stream);
+size_t moe_mxfp8_col_operand_size(int R, int E, int K);
 moe_status moe_mxfp8_mlp_fwd(const uint8_t* x_codes, const uint8_t* x_scales, const void* wq, const int32_t* offsets,
-                             int R, int E, int d, int f, void* h_save, void* a_save, void* y_perm, void* workspace,
-                             size_t workspace_bytes, void* stream);
+                             int R, int E, int d, int f, void* h_save, void* a_save, void* y_perm, uint8_t* a_cols,
+                             void* workspace, size_t workspace_bytes, void* stream);
 moe_status moe_mxfp8_mlp_bwd(const uint8_t* dy_codes, const uint8_t* dy_scales, const void* dy_perm,
-                             const void* x_perm, const void* h_save, const void* a_save, const void* wq,
-                             const int32_t* offsets, int R, int E, int d, int f, void* dx_perm, void* dw_gate,
-                             void* dw_up, void* dw_down, void* workspace, size_t workspace_bytes, void* stream);
+                             const void* x_perm, const void* h_save, const void* a_save, const uint8_t* a_cols,
+                             const void* wq, const int32_t* offsets, int R, int E, int d, int f, void* dx_perm,
+                             void* dw_gate, void* dw_up, void* dw_down, void* workspace, size_t workspace_bytes,
+                             void* stream);
 
 /* MXFP8 block quantisation ("Scaling and optimizing MoE training": MXFP8):
    E4M3 codes with one E8M0 scale per 32 consecutive elements.

@@ -28,7 +28,7 @@ EXPORTS = ("moe_workspace_size", "moe_route", "moe_permute", "moe_permute_bwd", 
            "moe_dispatch_mlp_fwd", "moe_dispatch_mlp_bwd", "moe_route_stats", "moe_permute_mxfp8",
            "moe_combine_bwd_mxfp8", "moe_mxfp8_mlp_fwd", "moe_mxfp8_mlp_bwd", "moe_mxfp8_weights_size",
            "moe_mxfp8_prepare_weights", "moe_mxfp8_row_scales_size", "moe_timing_arm", "moe_timing_finish",
-           "moe_timing_read", "moe_selftest_wait_timeout")
+           "moe_timing_read", "moe_selftest_wait_timeout", "moe_mxfp8_col_operand_size")
 
 
 class MoEError(RuntimeError):
@@ -69,8 +69,9 @@ def load(path: str = LIB_PATH):
         "moe_permute_mxfp8": ([P, I, I, I, I, P, P, P, P, P, P, P], I),
         "moe_combine_bwd_mxfp8": ([P, P, P, P, P, P, I, I, I, I, P, P, P, P, P], I),
         "moe_mxfp8_row_scales_size": ([I, I, I], Z),
-        "moe_mxfp8_mlp_fwd": ([P, P, P, P, I, I, I, I, P, P, P, P, Z, P], I),
-        "moe_mxfp8_mlp_bwd": ([P, P, P, P, P, P, P, P, I, I, I, I, P, P, P, P, P, Z, P], I),
+        "moe_mxfp8_mlp_fwd": ([P, P, P, P, I, I, I, I, P, P, P, P, P, Z, P], I),
+        "moe_mxfp8_mlp_bwd": ([P, P, P, P, P, P, P, P, P, I, I, I, I, P, P, P, P, P, Z, P], I),
+        "moe_mxfp8_col_operand_size": ([I, I, I], Z),
         "moe_mxfp8_weights_size": ([I, I, I], Z),
         "moe_mxfp8_prepare_weights": ([P, P, P, I, I, I, P, Z, P], I),
         "moe_dispatch_mlp_bwd": ([P, P, P, I, I, P, P, P, P, P, I, P, I, I, I, P, P, P, P, P, Z, P], I),
@@ -234,17 +235,23 @@ def moe_mxfp8_prepare_weights(w_gate, w_up, w_down, E, d, f, wq, stream=None):
         _p(w_gate), _p(w_up), _p(w_down), E, d, f, _p(wq), _nbytes(wq), _s(stream)))
 
 
-def moe_mxfp8_mlp_fwd(x_codes, x_scales, wq, offsets, R, E, d, f, h_save, a_save, y_perm, workspace, stream=None):
+def moe_mxfp8_col_operand_size(R, E, K):
+    return load().moe_mxfp8_col_operand_size(R, E, K)
+
+
+def moe_mxfp8_mlp_fwd(x_codes, x_scales, wq, offsets, R, E, d, f, h_save, a_save, y_perm, a_cols, workspace,
+                      stream=None):
     _chk("moe_mxfp8_mlp_fwd", load().moe_mxfp8_mlp_fwd(
-        _p(x_codes), _p(x_scales), _p(wq), _p(offsets), R, E, d, f, _p(h_save), _p(a_save), _p(y_perm),
+        _p(x_codes), _p(x_scales), _p(wq), _p(offsets), R, E, d, f, _p(h_save), _p(a_save), _p(y_perm), _p(a_cols),
         _p(workspace), _nbytes(workspace), _s(stream)))
 
 
-def moe_mxfp8_mlp_bwd(dy_codes, dy_scales, dy_perm, x_perm, h_save, a_save, wq, offsets, R, E, d, f, dx_perm,
+def moe_mxfp8_mlp_bwd(dy_codes, dy_scales, dy_perm, x_perm, h_save, a_save, a_cols, wq, offsets, R, E, d, f, dx_perm,
                       dw_gate, dw_up, dw_down, workspace, stream=None):
     _chk("moe_mxfp8_mlp_bwd", load().moe_mxfp8_mlp_bwd(
-        _p(dy_codes), _p(dy_scales), _p(dy_perm), _p(x_perm), _p(h_save), _p(a_save), _p(wq), _p(offsets), R, E, d,
-        f, _p(dx_perm), _p(dw_gate), _p(dw_up), _p(dw_down), _p(workspace), _nbytes(workspace), _s(stream)))
+        _p(dy_codes), _p(dy_scales), _p(dy_perm), _p(x_perm), _p(h_save), _p(a_save), _p(a_cols), _p(wq),
+        _p(offsets), R, E, d, f, _p(dx_perm), _p(dw_gate), _p(dw_up), _p(dw_down), _p(workspace), _nbytes(workspace),
+        _s(stream)))
 
 
 def moe_timing_arm(n):

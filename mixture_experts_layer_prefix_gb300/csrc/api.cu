@@ -409,9 +409,14 @@ moe_status moe_mxfp8_prepare_weights(const void* w_gate, const void* w_up, const
   return MOE_OK;
 }
 
+size_t moe_mxfp8_col_operand_size(int R, int E, int K) {
+  if (R < 0 || E <= 0 || K <= 0 || K % 128 != 0) return 0;
+  return mx_col_operand_bytes(R, E, K);
+}
+
 moe_status moe_mxfp8_mlp_fwd(const uint8_t* x_codes, const uint8_t* x_scales, const void* wq, const int32_t* offsets,
-                             int R, int E, int d, int f, void* h_save, void* a_save, void* y_perm, void* workspace,
-                             size_t workspace_bytes, void* stream) {
+                             int R, int E, int d, int f, void* h_save, void* a_save, void* y_perm, uint8_t* a_cols,
+                             void* workspace, size_t workspace_bytes, void* stream) {
   MOE_TRY(check_dims(R, d, E, 1));
   if (f <= 0) return MOE_ERR_INVALID_ARG;
   if (d % 128 != 0 || f % 128 != 0) return MOE_ERR_UNSUPPORTED;
@@ -420,15 +425,17 @@ moe_status moe_mxfp8_mlp_fwd(const uint8_t* x_codes, const uint8_t* x_scales, co
   MOE_NEED(x_codes); MOE_NEED(x_scales); MOE_NEED(h_save); MOE_NEED(a_save); MOE_NEED(y_perm);
   if (workspace_bytes < mx_fwd_workspace(R, E, d, f)) return MOE_ERR_WORKSPACE;
   MOE_NEED(workspace);
+  if (a_cols && !aligned16(a_cols)) return MOE_ERR_ALIGNMENT;
   MOE_CUDA_TRY(mx_mlp_fwd(nullptr, nullptr, nullptr, nullptr, offsets, R, E, d, f, h_save, a_save, y_perm, workspace,
-                          S(stream), x_codes, x_scales, wq));
+                          S(stream), x_codes, x_scales, wq, a_cols));
   return MOE_OK;
 }
 
 moe_status moe_mxfp8_mlp_bwd(const uint8_t* dy_codes, const uint8_t* dy_scales, const void* dy_perm,
-                             const void* x_perm, const void* h_save, const void* a_save, const void* wq,
-                             const int32_t* offsets, int R, int E, int d, int f, void* dx_perm, void* dw_gate,
-                             void* dw_up, void* dw_down, void* workspace, size_t workspace_bytes, void* stream) {
+                             const void* x_perm, const void* h_save, const void* a_save, const uint8_t* a_cols,
+                             const void* wq, const int32_t* offsets, int R, int E, int d, int f, void* dx_perm,
+                             void* dw_gate, void* dw_up, void* dw_down, void* workspace, size_t workspace_bytes,
+                             void* stream) {
   MOE_TRY(check_dims(R, d, E, 1));
   if (f <= 0) return MOE_ERR_INVALID_ARG;
   if (d % 128 != 0 || f % 128 != 0) return MOE_ERR_UNSUPPORTED;
@@ -440,8 +447,9 @@ moe_status moe_mxfp8_mlp_bwd(const uint8_t* dy_codes, const uint8_t* dy_scales, 
     MOE_NEED(dy_codes); MOE_NEED(dy_scales); MOE_NEED(dy_perm); MOE_NEED(x_perm); MOE_NEED(h_save);
     MOE_NEED(a_save); MOE_NEED(dx_perm);
   }
+  if (a_cols && !aligned16(a_cols)) return MOE_ERR_ALIGNMENT;
   MOE_CUDA_TRY(mx_mlp_bwd(dy_perm, x_perm, h_save, a_save, nullptr, nullptr, nullptr, offsets, R, E, d, f, dx_perm,
-                          dw_gate, dw_up, dw_down, workspace, S(stream), dy_codes, dy_scales, wq));
+                          dw_gate, dw_up, dw_down, workspace, S(stream), dy_codes, dy_scales, wq, a_cols));
   return MOE_OK;
 }
 

@@ -474,6 +474,9 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             warp_store_rows(stg, w, h + p.f + n, 2 * (size_t)p.f, nrows, lane);
             warp_store_rows(stg, wa, ao + n, p.f, nrows, lane);
             if (p.qout) quant_rows_staged(p, stg, wa, wrow, nrows, p.f, n, lane, tile_scale_row(tl, q, lane, p.f));
+            if (p.qcol)  // A along the expert's rows too (the GEMM2 weight gradient's A operand)
+              quant_cols_staged(p, stg, wa, wrow, nrows, p.f, n, lane,
+                                mx_row_tile_base(tl.m0 - tl.m_idx * BM, tl.e) + tl.m_idx, q);
           }
         } else {
           uint32_t w[4][16];
@@ -604,9 +607,11 @@ size_t bwd_workspace(long R, int E, int d, int f) {
 
 using namespace tc;
 
+size_t mx_col_operand_bytes(long R, int E, int K) { return mx::al((size_t)R * K) + mx::al(mx::seg_words_bytes(R, E, K)); }
+
 cudaError_t mx_mlp_fwd(const void* x_perm, const void* wg, const void* wu, const void* wd, const int32_t* offsets,
                        int R, int E, int d, int f, void* h, void* a, void* y, void* ws, cudaStream_t st,
-                       const uint8_t* xq_codes, const uint8_t* xq_scales, const void* wq) {
+                       const uint8_t* xq_codes, const uint8_t* xq_scales, const void* wq, uint8_t* a_cols) {
   using namespace mx;
   Carver cv{static_cast<char*>(ws)};
   const long Ed = (long)E * d, Ef = (long)E * f;
@@ -644,9 +649,13 @@ cudaError_t mx_mlp_fwd(const void* x_perm, const void* wg, const void* wu, const
   p.N = f; p.n_tiles = (f + 127) / 128; p.out0 = h; p.out1 = a;
   p.sfa = xq.s; p.sfb0 = wgq.s; p.sfb1 = wuq.s;
   p.qout = aq.q; p.qsc = aq.s;  // the epilogue also quantises A along f for GEMM2
+  if (a_cols) {                  // ... and along the experts' rows for the GEMM2 weight gradient
+    p.qcol = a_cols;
+    p.qcsc = a_cols + al((size_t)R * f);
+  }
   if ((e = launch<FPROP1, kN_FPROP1>(mA, mB0, mB1, p, ((long)(R + BM - 1) / BM + E) * p.n_tiles, st)) != cudaSuccess)
     return e;
-  p.qout = nullptr; p.qsc = nullptr;
+  p.qout = nullptr; p.qsc = nullptr; p.qcol = nullptr; p.qcsc = nullptr;
   // GEMM2 along f: A rows (written by GEMM1's epilogue), w_down columns
   if (!map_2d(&mA, aq.q, U8, 1, f, R, 128, BM) || !map_3d(&mB0, wdq.q, U8, 1, d, f, E, 128, 128))
     return cudaErrorInvalidValue;
@@ -658,7 +667,7 @@ cudaError_t mx_mlp_fwd(const void* x_perm, const void* wg, const void* wu, const
 cudaError_t mx_mlp_bwd(const void* dy_perm, const void* x_perm, const void* h, const void* a, const void* wg,
                        const void* wu, const void* wd, const int32_t* offsets, int R, int E, int d, int f,
                        void* dx_perm, void* dwg, void* dwu, void* dwd, void* ws, cudaStream_t st,
-                       const uint8_t* dyq_codes, const uint8_t* dyq_scales, const void* wq) {
+                       const uint8_t* dyq_codes, const uint8_t* dyq_scales, const void* wq, const uint8_t* a_cols) {
   using namespace mx;
   Carver cv{static_cast<char*>(ws)};
   const long Ed = (long)E * d, Ef = (long)E * f;
@@ -708,7 +717,13 @@ cudaError_t mx_mlp_bwd(const void* dy_perm, const void* x_perm, const void* h, c
   p.qout = nullptr; p.qsc = nullptr; p.qcol = nullptr; p.qcsc = nullptr;
 
   // dWd[e] = A_e^T dy_e (K = the expert's rows): A and dy quantised along rows per expert
-  if ((e = launch_mxfp8_quant_cols(a, R, f, offsets, E, ac.q, ac.s, st, true)) != cudaSuccess) return e;
+  // (A already, when the forward's GEMM1 epilogue wrote it)
+  if (a_cols) {
+    ac.q = const_cast<uint8_t*>(a_cols);
+    ac.s = const_cast<uint8_t*>(a_cols) + al((size_t)R * f);
+  } else if ((e = launch_mxfp8_quant_cols(a, R, f, offsets, E, ac.q, ac.s, st, true)) != cudaSuccess) {
+    return e;
+  }
   if ((e = launch_mxfp8_quant_cols(dy_perm, R, d, offsets, E, dyc.q, dyc.s, st, true)) != cudaSuccess) return e;
   if (!map_2d(&mA, ac.q, U8, 1, f, R, 128, 128) || !map_2d(&mB0, dyc.q, U8, 1, d, R, 128, 128))
     return cudaErrorInvalidValue;

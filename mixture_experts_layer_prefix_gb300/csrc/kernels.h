@@ -121,17 +121,20 @@ cudaError_t tc_router_logits(const void* x, const void* w_r, const float* bias, 
 // ------------------------------------------- MXFP8 grouped GEMMs (bf16 in/out)
 size_t mx_fwd_workspace(long R, int E, int d, int f);
 size_t mx_bwd_workspace(long R, int E, int d, int f);
+// a_cols (optional): GEMM1's epilogue also writes A quantised along the
+// experts' rows (codes [R][f], then the scale chunks; mx_col_operand_bytes).
+size_t mx_col_operand_bytes(long R, int E, int K);
 cudaError_t mx_mlp_fwd(const void* x_perm, const void* wg, const void* wu, const void* wd, const int32_t* offsets,
                        int R, int E, int d, int f, void* h, void* a, void* y, void* ws, cudaStream_t st,
                        const uint8_t* xq_codes = nullptr, const uint8_t* xq_scales = nullptr,
-                       const void* wq = nullptr);
+                       const void* wq = nullptr, uint8_t* a_cols = nullptr);
 // dyq_codes/dyq_scales (optional): dy_perm's rows already quantised by the
 // combine backward.
 cudaError_t mx_mlp_bwd(const void* dy_perm, const void* x_perm, const void* h, const void* a, const void* wg,
                        const void* wu, const void* wd, const int32_t* offsets, int R, int E, int d, int f,
                        void* dx_perm, void* dwg, void* dwu, void* dwd, void* ws, cudaStream_t st,
                        const uint8_t* dyq_codes = nullptr, const uint8_t* dyq_scales = nullptr,
-                       const void* wq = nullptr);
+                       const void* wq = nullptr, const uint8_t* a_cols = nullptr);
 // The weights quantised once per update in both K layouts (wq: mx_weights_bytes).
 size_t mx_weights_bytes(int E, int d, int f);
 cudaError_t mx_prepare_weights(const void* wg, const void* wu, const void* wd, int E, int d, int f, void* wq,

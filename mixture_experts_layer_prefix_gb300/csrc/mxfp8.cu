@@ -249,24 +249,25 @@ quant_dual_kernel(const __nv_bfloat16* __restrict__ src, int C, long ntiles, uin
     }
     {  // along the rows: block (row r, 32 columns cb); lanes are rows
       const int r = tid & 31, cb = tid >> 5;
-      float v[32];
+      uint32_t w[16];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const uint4 u = *reinterpret_cast<const uint4*>(tl + r * kDualPitch + 32 * cb + 8 * i);
-        const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          v[8 * i + 2 * k] = __uint_as_float(w4[k] << 16);
-          v[8 * i + 2 * k + 1] = __uint_as_float(w4[k] & 0xFFFF0000u);
-        }
+        w[4 * i] = u.x; w[4 * i + 1] = u.y; w[4 * i + 2] = u.z; w[4 * i + 3] = u.w;
       }
+      const int sx = e8m0_exponent(absmax_bf16x32(w));
+      const float m = pow2_neg(sx);
       uint32_t cw[8];
-      const uint8_t sb = mx_quant_block32_regs(v, cw);
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        cw[i] = mx_e4m3x2(bf16_lo(w[2 * i]) * m, bf16_hi(w[2 * i]) * m) |
+                (mx_e4m3x2(bf16_lo(w[2 * i + 1]) * m, bf16_hi(w[2 * i + 1]) * m) << 16);
       const long row = row0 + r;
       uint4* out = reinterpret_cast<uint4*>(qr + row * C + c0 + 32 * cb);
       out[0] = make_uint4(cw[0], cw[1], cw[2], cw[3]);
       out[1] = make_uint4(cw[4], cw[5], cw[6], cw[7]);
-      sc_r[(((row >> 7) * cg + c0 / 128) << 9) + mx_chunk_lane(static_cast<int>(row & 127)) + cb] = sb;
+      sc_r[(((row >> 7) * cg + c0 / 128) << 9) + mx_chunk_lane(static_cast<int>(row & 127)) + cb] =
+          static_cast<uint8_t>(sx + 127);
     }
     __syncthreads();  // every column's codes are staged
 #pragma unroll

@@ -42,6 +42,28 @@ __host__ __device__ __forceinline__ long mx_row_tile_base(long offs_e, int e) { 
 // Groups spanned by a row operand of R rows over E experts.
 __host__ __device__ __forceinline__ long mx_row_tiles(long R, int E) { return (R + 127L * E) / 128 + 1; }
 
+// bf16 pairs held in 32-bit words: element 0 in the low half.
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+// Element-wise maximum of two bf16 pairs.
+__device__ __forceinline__ uint32_t bf16x2_max(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+// Largest magnitude among 32 bf16 values held as 16 pairs (exact).
+__device__ __forceinline__ float absmax_bf16x32(const uint32_t (&w)[16]) {
+  uint32_t m[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) m[i] = bf16x2_max(w[2 * i] & 0x7FFF7FFFu, w[2 * i + 1] & 0x7FFF7FFFu);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) m[i] = bf16x2_max(m[2 * i], m[2 * i + 1]);
+  m[0] = bf16x2_max(m[0], m[1]);
+  m[2] = bf16x2_max(m[2], m[3]);
+  m[0] = bf16x2_max(m[0], m[2]);
+  return fmaxf(bf16_lo(m[0]), bf16_hi(m[0]));
+}
+
 // Round-to-nearest-even E4M3 codes of v0 (low byte) and v1 (high byte),
 // saturated to +-448, from one paired conversion.
 __device__ __forceinline__ uint32_t mx_e4m3x2(float v0, float v1) {

@@ -170,6 +170,7 @@ __device__ __forceinline__ void build_tile_table(const Params& p, int* offs, int
   __syncthreads();
 }
 
+
 // Row-segment traffic through a per-warp staging buffer. An epilogue thread
 // owns one output row (its TMEM lane), so a direct store instruction of a
 // warp touches 32 rows with 16 bytes each. Staged in shared memory (32 rows x
@@ -239,10 +240,7 @@ __device__ __forceinline__ size_t tile_scale_row(const Tile& tl, int q, int lane
 // (srow: the lane's tile_scale_row).
 __device__ __forceinline__ void quant_rows_staged(const Params& p, uint8_t* stg, const uint32_t (&w)[16], int wrow,
                                                   int nrows, int ld, int col, int lane, size_t srow) {
-  float amax = 0.0f;
-#pragma unroll
-  for (int i = 0; i < 16; ++i)
-    amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(w[i] << 16)), fabsf(__uint_as_float(w[i] & 0xFFFF0000u))));
+  const float amax = absmax_bf16x32(w);
   const int sx = mx_e8m0_exponent(amax);
   const float m = mx_pow2_neg(sx);
   uint32_t cw[8];
@@ -255,46 +253,60 @@ __device__ __forceinline__ void quant_rows_staged(const Params& p, uint8_t* stg,
   warp_store_rows32(stg, cw, p.qout + (size_t)wrow * ld + col, ld, nrows, lane);
 }
 
+// One step of a butterfly reduce-scatter of per-column maxima over the warp,
+// on bf16 pairs (word i = columns 2i, 2i+1): with 2H words per lane, the lane
+// keeps the H words picked by lane bit 2H and takes the max with its partner's
+// copy of them (lane ^ 2H; the partner keeps the other H). After the steps
+// H = 8, 4, 2, 1, word 0 of lane l holds columns 2(l/2), 2(l/2)+1, maxed over
+// the 16 lanes that agree with l in bit 0.
+template <int H>
+__device__ __forceinline__ void colmax_step(uint32_t (&a)[16], int lane) {
+  const bool up = (lane & (2 * H)) != 0;
+#pragma unroll
+  for (int i = 0; i < H; ++i) {
+    const uint32_t keep = up ? a[H + i] : a[i];
+    const uint32_t give = up ? a[i] : a[H + i];
+    a[i] = bf16x2_max(keep, __shfl_xor_sync(0xffffffffu, give, 2 * H));
+  }
+}
+
 // MXFP8 quantisation of the same chunk along its rows, in blocks of 32 rows:
 // the warp's rows are one such block of the expert segment (rows >= nrows are
 // past the segment's end and count as zero). Codes to qcol[row][col..col+32)
 // ([rows][ld] matrix), the scale of column col + lane into its scale chunk
 // (K stage `stage`, the block q within it; a block wholly past the end gets
-// 127). Lane l reads column l back from the staged rows; the codes return to
-// row order through the same buffer and leave as 16 rows x 32 B per store.
+// 127). The column maxima come from a butterfly over the lanes on bf16 pairs
+// (16 shuffles: lane l ends with column l's), the 32 scale factors return to every lane
+// through 128 bytes of the warp's staging buffer, and each lane encodes its own
+// row, which leaves as 16 rows x 32 B per store.
 __device__ __forceinline__ void quant_cols_staged(const Params& p, uint8_t* stg, const uint32_t (&w)[16], int wrow,
                                                   int nrows, int ld, int col, int lane, long stage, int q) {
+  const uint32_t live = lane < nrows ? 0x7FFF7FFFu : 0u;  // magnitudes; rows past the end count as zero
+  uint32_t a[16];
 #pragma unroll
-  for (int g = 0; g < 4; ++g)
-    *reinterpret_cast<uint4*>(stg + stg_off(lane, g)) = make_uint4(w[4 * g], w[4 * g + 1], w[4 * g + 2], w[4 * g + 3]);
+  for (int i = 0; i < 16; ++i) a[i] = w[i] & live;
+  colmax_step<8>(a, lane);
+  colmax_step<4>(a, lane);
+  colmax_step<2>(a, lane);
+  colmax_step<1>(a, lane);
+  a[0] = bf16x2_max(a[0], __shfl_xor_sync(0xffffffffu, a[0], 1));
+  const int sx = mx_e8m0_exponent((lane & 1) ? bf16_hi(a[0]) : bf16_lo(a[0]));  // column col + lane
+  float* ms = reinterpret_cast<float*>(stg);
+  ms[lane] = mx_pow2_neg(sx);
   __syncwarp();
-  float v[32], amax = 0.0f;
+  float m[32];
 #pragma unroll
-  for (int r = 0; r < 32; ++r) {
-    const uint32_t b = *reinterpret_cast<const uint16_t*>(stg + stg_off(r, lane >> 3) + 2 * (lane & 7));
-    v[r] = r < nrows ? __uint_as_float(b << 16) : 0.0f;
-    amax = fmaxf(amax, fabsf(v[r]));
+  for (int i = 0; i < 8; ++i) {
+    const float4 v = reinterpret_cast<const float4*>(ms)[i];
+    m[4 * i] = v.x; m[4 * i + 1] = v.y; m[4 * i + 2] = v.z; m[4 * i + 3] = v.w;
   }
-  __syncwarp();
-  const int sx = mx_e8m0_exponent(amax);
-  const float m = mx_pow2_neg(sx);
+  __syncwarp();  // the buffer is reused for the codes below
+  uint32_t cw[8];
 #pragma unroll
-  for (int r = 0; r < 32; r += 2) {
-    const uint32_t b = mx_e4m3x2(v[r] * m, v[r + 1] * m);
-    stg[stg32_off(r, lane >> 4) + (lane & 15)] = static_cast<uint8_t>(b);
-    stg[stg32_off(r + 1, lane >> 4) + (lane & 15)] = static_cast<uint8_t>(b >> 8);
-  }
-  __syncwarp();
-  {
-    const int g = lane & 1;
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      const int r = 16 * i + (lane >> 1);
-      const uint4 cv = *reinterpret_cast<const uint4*>(stg + stg32_off(r, g));
-      if (r < nrows) *reinterpret_cast<uint4*>(p.qcol + (size_t)(wrow + r) * ld + col + 16 * g) = cv;
-    }
-  }
-  __syncwarp();
+  for (int i = 0; i < 8; ++i)
+    cw[i] = mx_e4m3x2(bf16_lo(w[2 * i]) * m[4 * i], bf16_hi(w[2 * i]) * m[4 * i + 1]) |
+            (mx_e4m3x2(bf16_lo(w[2 * i + 1]) * m[4 * i + 2], bf16_hi(w[2 * i + 1]) * m[4 * i + 3]) << 16);
+  warp_store_rows32(stg, cw, p.qcol + (size_t)wrow * ld + col, ld, nrows, lane);
   const int c = col + lane;
   p.qcsc[((stage * (ld / 128) + c / 128) << 9) + mx_chunk_lane(c & 127) + q] =
       static_cast<uint8_t>(nrows > 0 ? sx + 127 : 127);
@@ -328,8 +340,6 @@ __device__ __forceinline__ void warp_load_rows_finish(uint8_t* stg, const uint4 
   }
   __syncwarp();
 }
-__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&h);

@@ -11,8 +11,10 @@ library's kernels. Order of calls:
 On the MXFP8 path the dispatched activations are row-quantised where they are
 produced (mx_pre, default on): moe_permute_mxfp8 writes x_perm's E4M3 rows
 next to the bf16 dispatch and moe_combine_bwd_mxfp8 dy_perm's; moe_mxfp8_prepare_weights quantises every
-weight once per step in both K layouts; moe_mxfp8_mlp_fwd / moe_mxfp8_mlp_bwd
-then run no quantisation of their own for those operands.
+weight once per step in both K layouts; moe_mxfp8_mlp_fwd also writes A
+quantised along the experts' rows (a_cols) from its GEMM1 epilogue;
+moe_mxfp8_mlp_fwd / moe_mxfp8_mlp_bwd then run no quantisation of their own
+for those operands.
 
 With fused=True (bf16 only) moe_dispatch_mlp_fwd / moe_dispatch_mlp_bwd
 replace moe_permute and the two grouped-MLP calls: GEMM1 and its weight
@@ -112,6 +114,8 @@ class Buffers:
             self.dy_q, self.dy_sc = z(R, d, dt=u8), z(nsc, dt=u8)
             # the weights quantised once per step in both K layouts
             self.wq = torch.empty(max(1, N.moe_mxfp8_weights_size(E, d, f)), dtype=u8, device=device)
+            # A quantised along the experts' rows by GEMM1's epilogue, read by the GEMM2 wgrad
+            self.a_cols = torch.empty(max(1, N.moe_mxfp8_col_operand_size(R, E, f)), dtype=u8, device=device)
 
 
 def route_stats(b: Buffers, stream=None):
@@ -137,7 +141,7 @@ def forward(p: Params, b: Buffers, logits_in: bool = False, stream=None, fused=N
     if dt == N.MOE_MXFP8 and mx_pre:
         N.moe_mxfp8_prepare_weights(p.w_gate, p.w_up, p.w_down, E, d, f, b.wq, stream)
         N.moe_permute_mxfp8(p.x, T, d, k, E, b.dest_row, b.topk_idx, b.offsets, b.x_q, b.x_sc, b.x_perm, stream)
-        N.moe_mxfp8_mlp_fwd(b.x_q, b.x_sc, b.wq, b.offsets, b.R, E, d, f, b.h_save, b.a_save, b.y_perm,
+        N.moe_mxfp8_mlp_fwd(b.x_q, b.x_sc, b.wq, b.offsets, b.R, E, d, f, b.h_save, b.a_save, b.y_perm, b.a_cols,
                             b.workspace, stream)
     elif fused_default(dt) if fused is None else fused:
         N.moe_dispatch_mlp_fwd(p.x, b.src_row, T, k, p.w_gate, p.w_up, p.w_down, dt, b.offsets, E, d, f,
@@ -160,8 +164,8 @@ def backward(p: Params, b: Buffers, stream=None, fused=None, mx_pre=True):
     N.moe_route_bwd(b.dgates, b.gates, b.topk_idx, b.offsets, b.src_row, p.x, dt, T, d, E, k,
                     b.dlogits, b.dw_router, stream)
     if mx:
-        N.moe_mxfp8_mlp_bwd(b.dy_q, b.dy_sc, b.dy_perm, b.x_perm, b.h_save, b.a_save, b.wq, b.offsets, b.R, E, d, f,
-                            b.dx_perm, b.dw_gate, b.dw_up, b.dw_down, b.workspace, stream)
+        N.moe_mxfp8_mlp_bwd(b.dy_q, b.dy_sc, b.dy_perm, b.x_perm, b.h_save, b.a_save, b.a_cols, b.wq, b.offsets, b.R,
+                            E, d, f, b.dx_perm, b.dw_gate, b.dw_up, b.dw_down, b.workspace, stream)
     elif fused_default(dt) if fused is None else fused:
         N.moe_dispatch_mlp_bwd(b.dy_perm, p.x, b.src_row, T, k, b.h_save, b.a_save, p.w_gate, p.w_up, p.w_down,
                                dt, b.offsets, E, d, f, b.dx_perm, b.dw_gate, b.dw_up, b.dw_down, b.workspace,

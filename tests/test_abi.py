@@ -120,9 +120,16 @@ def test_mxfp8_dispatch_arguments_rejected_before_launch(lib):
     assert L.moe_mxfp8_row_scales_size(1000, 8, 256) == ((1000 + 127 * 8) // 128 + 1) * 4 * 256
     assert L.moe_mxfp8_row_scales_size(1000, 8, 96) == 0
     # d not a multiple of 128 for the block-scaled GEMMs
-    assert L.moe_mxfp8_mlp_fwd(FAKE, FAKE, FAKE, FAKE, 16, 4, 192, 128, FAKE, FAKE, FAKE, FAKE, 1 << 30, None) == 2
-    assert L.moe_mxfp8_mlp_bwd(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 16, 4, 128, 128, FAKE, FAKE, FAKE,
-                               FAKE, FAKE, 16, None) == 4                                  # workspace
+    assert L.moe_mxfp8_mlp_fwd(FAKE, FAKE, FAKE, FAKE, 16, 4, 192, 128, FAKE, FAKE, FAKE, None, FAKE, 1 << 30,
+                               None) == 2
+    assert L.moe_mxfp8_mlp_bwd(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, FAKE, 16, 4, 128, 128, FAKE, FAKE,
+                               FAKE, FAKE, FAKE, 16, None) == 4                            # workspace
+    # a_cols misaligned
+    assert L.moe_mxfp8_mlp_fwd(FAKE, FAKE, FAKE, FAKE, 16, 4, 128, 128, FAKE, FAKE, FAKE, FAKE + 4, FAKE, 1 << 30,
+                               None) == 3
+    # an operand quantised along the experts' rows: codes (256-byte padded) + scale chunks
+    assert L.moe_mxfp8_col_operand_size(1000, 8, 256) == 1000 * 256 + ((1000 + 127) // 128 + 8 + 1) * 256 * 4
+    assert L.moe_mxfp8_col_operand_size(1000, 8, 96) == 0
     assert L.moe_mxfp8_weights_size(4, 128, 128) > 4 * 128 * 128 * 3 * 2
     assert L.moe_mxfp8_prepare_weights(FAKE, FAKE, FAKE, 4, 128, 128, FAKE, 16, None) == 4  # wq too small
     assert L.moe_mxfp8_prepare_weights(FAKE, FAKE, FAKE, 4, 192, 128, FAKE, 1 << 30, None) == 2

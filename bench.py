@@ -188,11 +188,17 @@ def kernel_work(s):
     flops = {"gemm1_swiglu": 4.0 * R * d * f, "gemm2": 2.0 * R * f * d, "gemm2_dgrad_swiglu_bwd": 2.0 * R * d * f,
              "gemm2_wgrad": 2.0 * R * f * d, "gemm1_dgrad": 4.0 * R * f * d, "gemm1_wgrad": 4.0 * R * d * f}
     flops.update({"mx_" + n: v for n, v in list(flops.items())})
-    byt = {"permute": 2.0 * (T + R) * d, "combine_fwd": 2.0 * (R + T) * d + 8.0 * T * k,
-           "combine_bwd": 2.0 * (T + 2 * R) * d + 12.0 * T * k, "permute_bwd": 2.0 * (R + T) * d + 4.0 * T * E,
-           "router_gemm": 2.0 * T * d + 4.0 * T * E + 2.0 * E * d, "router_dw": 2.0 * T * d + 4.0 * T * E + 4.0 * E * d,
-           "router_dlogits": 12.0 * T * k + 4.0 * T * E, "permute_quant": 2.0 * T * d + (2.0 + 33.0 / 32) * R * d,
-           "quant_dual": 3 * E * d * f * (2.0 + 2 * 33.0 / 32)}
+    # bytes each kernel must move at least once (index and gate arrays included;
+    # rows gathered more than once from L2 counted once)
+    byt = {"permute": 2.0 * (T + R) * d + 4.0 * R,
+           "combine_fwd": 2.0 * (R + T) * d + 8.0 * R,
+           "combine_bwd": 2.0 * (T + 2 * R) * d + 12.0 * R,
+           "permute_bwd": 2.0 * (R + T) * d + 12.0 * R + 2.0 * E * d,
+           "router_gemm": 2.0 * T * d + 4.0 * T * E + 2.0 * E * d,
+           "router_dw": 2.0 * T * d + 8.0 * R + 4.0 * E * d,
+           "router_dlogits": 12.0 * R + 4.0 * T * E,
+           "permute_quant": 2.0 * T * d + (2.0 + 1.0 + 1.0 / 32) * R * d + 12.0 * R,
+           "quant_dual": 3.0 * E * d * f * (2.0 + 2 * 33.0 / 32)}
     return flops, byt
 
 

@@ -21,7 +21,7 @@
  *    Floating Point (OFP8) specifications (bias 7, max normal 448,
  *    S.1111.111 is NaN; E8M0 bias 127).
  *
- * Readings taken where the pages are silent (each is listed in the design doc):
+ * Readings taken where the pages are silent:
  *  - top-k compares logits (not probabilities); equal logits keep the
  *    smaller expert index; the k slots are ordered by (logit desc, index asc).
  *  - g_j = exp(l_j - m) / sum_{i in S} exp(l_i - m): softmax over E followed

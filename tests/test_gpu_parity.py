@@ -45,6 +45,8 @@ SMALL = [
     _shape("bf16_k_eq_E", 77, 192, 3, 3, 64),
     _shape("bf16_one_token", 1, 64, 4, 2, 64),
     _shape("bf16_e320_k2", 600, 128, 320, 2, 64),
+    # the largest supported expert count: most experts empty, one block ranks all 1024 for the wgrads
+    _shape("bf16_e1024_k2", 700, 128, 1024, 2, 64),
 ]
 
 

@@ -55,7 +55,9 @@ typedef enum {
   MOE_ERR_WORKSPACE = 4,     /* workspace smaller than moe_workspace_size()    */
   MOE_ERR_CUDA = 5,          /* a CUDA runtime call failed                     */
   MOE_ERR_DEVICE_INDEX = 6,  /* device error word: index out of range          */
-  MOE_ERR_TIMEOUT = 7        /* device error word: a bounded wait ran out      */
+  MOE_ERR_TIMEOUT = 7,       /* device error word: a bounded wait ran out      */
+  MOE_ERR_DEVICE_PAIR = 8    /* device error word: the two CTAs of a pair got
+                                different TMEM columns (their GEMM is skipped) */
 } moe_status;
 
 typedef enum { MOE_F32 = 0, MOE_BF16 = 1, MOE_MXFP8 = 2 } moe_dtype;
@@ -186,6 +188,19 @@ moe_status moe_grouped_mlp_bwd(const void* dy_perm, const void* x_perm, const vo
                                int d, int f, void* dx_perm, void* dw_gate, void* dw_up,
                                void* dw_down, void* workspace, size_t workspace_bytes,
                                void* stream);
+
+/* Selects the kernel of the bf16 weight-gradient GEMMs: both of
+   moe_grouped_mlp_bwd, and the GEMM2 one of moe_dispatch_mlp_bwd (its GEMM1
+   weight gradient gathers rows and keeps one CTA per SM). Process-wide, for
+   launches issued after the call ("Scaling and optimizing MoE
+   training": grouped GEMM; the kernel choice itself has no counterpart in
+   the pages). 0 (the default): one CTA per SM computes 256x256 gradient tiles,
+   its two fp32 accumulators filling TMEM. 1: CTA pairs (2-CTA clusters) compute
+   the same tiles with tcgen05.mma.cta_group::2 (M=256 across both SMs), each SM
+   holding a 128x256 half twice over so that the epilogue overlaps the next
+   tile's MMAs. Both give the same results up to fp32 summation order. Returns
+   MOE_OK. */
+moe_status moe_use_cta_pairs(int enable);
 
 /* The dispatch fused into the grouped MLP ("Scaling and optimizing MoE
    training": routed rows go straight into the experts' inputs, and the layer

@@ -19,7 +19,8 @@ LIB_PATH = os.path.join(_PKG, "libmoe.so")
 MOE_F32, MOE_BF16, MOE_MXFP8 = 0, 1, 2
 MOE_ROUTE_LOGITS_IN = 1
 STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_ALIGNMENT",
-          4: "MOE_ERR_WORKSPACE", 5: "MOE_ERR_CUDA", 6: "MOE_ERR_DEVICE_INDEX", 7: "MOE_ERR_TIMEOUT"}
+          4: "MOE_ERR_WORKSPACE", 5: "MOE_ERR_CUDA", 6: "MOE_ERR_DEVICE_INDEX", 7: "MOE_ERR_TIMEOUT",
+          8: "MOE_ERR_DEVICE_PAIR"}
 
 # every symbol include/moe.h declares
 EXPORTS = ("moe_workspace_size", "moe_route", "moe_permute", "moe_permute_bwd", "moe_combine_fwd",
@@ -28,7 +29,8 @@ EXPORTS = ("moe_workspace_size", "moe_route", "moe_permute", "moe_permute_bwd", 
            "moe_dispatch_mlp_fwd", "moe_dispatch_mlp_bwd", "moe_route_stats", "moe_permute_mxfp8",
            "moe_combine_bwd_mxfp8", "moe_mxfp8_mlp_fwd", "moe_mxfp8_mlp_bwd", "moe_mxfp8_weights_size",
            "moe_mxfp8_prepare_weights", "moe_mxfp8_row_scales_size", "moe_timing_arm", "moe_timing_finish",
-           "moe_timing_read", "moe_selftest_wait_timeout", "moe_mxfp8_col_operand_size")
+           "moe_timing_read", "moe_selftest_wait_timeout", "moe_mxfp8_col_operand_size",
+           "moe_use_cta_pairs")
 
 
 class MoEError(RuntimeError):
@@ -79,6 +81,7 @@ def load(path: str = LIB_PATH):
         "moe_timing_finish": ([P], I),
         "moe_timing_read": ([P, P, I], I),
         "moe_selftest_wait_timeout": ([ctypes.c_longlong, P, P], I),
+        "moe_use_cta_pairs": ([I], I),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -270,6 +273,10 @@ def moe_timing_read(cap=256):
     if n < 0:
         raise MoEError("moe_timing_read", 1)
     return [(names[i].decode(), float(ms[i])) for i in range(n)]
+
+
+def moe_use_cta_pairs(enable):
+    _chk("moe_use_cta_pairs", load().moe_use_cta_pairs(1 if enable else 0))
 
 
 def moe_selftest_wait_timeout(cycles, out, stream=None):

@@ -409,6 +409,11 @@ moe_status moe_mxfp8_prepare_weights(const void* w_gate, const void* w_up, const
   return MOE_OK;
 }
 
+moe_status moe_use_cta_pairs(int enable) {
+  set_cta_pairs(enable);
+  return MOE_OK;
+}
+
 size_t moe_mxfp8_col_operand_size(int R, int E, int K) {
   if (R < 0 || E <= 0 || K <= 0 || K % 128 != 0) return 0;
   return mx_col_operand_bytes(R, E, K);

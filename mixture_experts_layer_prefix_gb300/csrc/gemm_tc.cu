@@ -21,6 +21,8 @@
 // zeroed in shared memory before the MMA; an expert with no rows gets zeros).
 // Every wait is bounded; on a timeout the CTA sets the device error word,
 // drains what it started and returns.
+#include <atomic>
+
 #include "kernels.h"
 #include "tc_common.cuh"
 
@@ -798,6 +800,366 @@ cudaError_t launch_wgrad(const CUtensorMap& a, const CUtensorMap& b, const Param
   return cudaGetLastError();
 }
 
+// ---------------------------------------------------------------------------
+// Weight gradients on CTA pairs (2-CTA clusters, tcgen05.mma.cta_group::2),
+// selected with moe_use_cta_pairs(1). A pair computes a 256x256 block of one
+// expert's gradient: each CTA loads its own 128 rows of M (A boxes) and its own
+// 128 of the N columns (B boxes), 64 KB per 128-row K stage, and the even CTA
+// issues one M=256 N=256 MMA per K step that reads both CTAs' shared memory.
+// Each CTA's TMEM receives its 128 rows x 256 columns, so the 512 columns hold
+// two accumulators: the next tile's MMAs run while the epilogue drains the
+// previous one. Operand bytes per FLOP are those of the single-CTA 256x256
+// tile, whose accumulators fill TMEM instead.
+//   warp 0      both CTAs: TMA producer of its own half of each stage.
+//   warp 1      even CTA: MMA issuer; it commits each stage's release to both
+//               CTAs' `empty` barriers and each finished accumulator to both
+//               CTAs' `tfull` barriers.
+//               odd CTA: relay; waits for its half of a stage to land, zeroes
+//               the rows past the expert's end in its A boxes, then arrives on
+//               the even CTA's `full` barrier (two arrivals per phase there:
+//               its producer's and the relay's).
+//   warps 2..9  both CTAs: epilogue of its own 128 rows; they arrive on the even
+//               CTA's `tempty` barrier when the accumulator has been read.
+// All 32 lanes of a warp poll each barrier: a warp whose other lanes sit at a
+// warp barrier while one lane polls resumes late after the phase completes.
+// Every wait is bounded; a CTA that gives up raises both CTAs' abort flags.
+constexpr int PBK = 128;              // K rows per stage
+constexpr int P_BOX = 64 * PBK * 2;   // one 64 (M or N) x 128 (K rows) box
+constexpr int P_A_BYTES = 2 * P_BOX;  // this CTA's 128 rows of M
+constexpr int P_STAGE = 4 * P_BOX;    // + its 128 columns of N
+constexpr int P_NS = 3;
+
+struct PairSmem {
+  uint64_t full[P_NS];
+  uint64_t empty[P_NS];
+  uint64_t tfull[2];
+  uint64_t tempty[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+// Bounded wait on a local mbarrier whose arrivals may come from the other CTA
+// of the pair. On expiry it sets the error word and both CTAs' abort flags.
+__device__ __forceinline__ bool wait_pair(uint64_t* bar, uint32_t parity, int* abort_flag, uint32_t peer_abort,
+                                          int* err) {
+  if (ptx::mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (true) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    if (*reinterpret_cast<volatile int*>(abort_flag)) return false;
+    if (clock64() - t0 > kWaitLimitCycles) {
+      set_error(err, MOE_ERR_TIMEOUT);
+      *reinterpret_cast<volatile int*>(abort_flag) = 1;
+      ptx::st_cluster_u32(peer_abort, 1u);
+      return false;
+    }
+  }
+}
+
+template <int KIND>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+tc_wgrad_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                     const Params p) {
+  static_assert(Traits<KIND>::kragged, "weight-gradient kinds only");
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  PairSmem* sm = reinterpret_cast<PairSmem*>(smem + P_NS * P_STAGE + NUM_EPI_WARPS * W_STG);
+  const int* __restrict__ offs = p.offsets;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = ptx::cluster_ctarank(), peer = rank ^ 1u;
+  const int cid = static_cast<int>(ptx::cluster_id_x()), ncl = static_cast<int>(ptx::n_clusters_x());
+  auto in_cta = [&](const void* x, uint32_t r) { return ptx::mapa(ptx::smem_u32(x), r); };
+  const uint32_t peer_abort = in_cta(&sm->abort_flag, peer);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < P_NS; ++s) {
+      ptx::mbar_init(&sm->full[s], rank == 0 ? 2 : 1);
+      ptx::mbar_init(&sm->empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      ptx::mbar_init(&sm->tfull[b], 1);
+      ptx::mbar_init(&sm->tempty[b], 2 * NUM_EPI_WARPS);
+    }
+    ptx::mbar_init(&sm->drain, 1);
+    sm->abort_flag = 0;
+    ptx::fence_mbar_init();
+    ptx::fence_proxy_async_smem();
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc_pair(&sm->tmem_base, TMEM_COLS);
+    ptx::tmem_relinquish_pair();
+  }
+  ptx::tc_fence_before();
+  ptx::cluster_sync();  // both CTAs' barriers initialised and TMEM allocated
+  ptx::tc_fence_after();
+  const uint32_t tmem = sm->tmem_base;
+  if (threadIdx.x == 0 && ptx::ld_cluster_u32(in_cta(&sm->tmem_base, peer)) != tmem) {
+    set_error(p.err, MOE_ERR_DEVICE_PAIR);
+    sm->abort_flag = 1;
+  }
+  __syncthreads();
+  const bool run = sm->abort_flag == 0;
+
+  const int per = p.m_tiles * p.n_tiles;
+  const int total = p.E * per;
+  // the pair's r-th tile: experts largest first, a snake over the pairs
+  auto tile_of = [&](int r) { return r * ncl + ((r & 1) ? ncl - 1 - cid : cid); };
+  struct WT {
+    int e, m0, n0, r0, r1, nkb;
+  };
+  auto decode_w = [&](int t) {
+    WT w;
+    w.e = p.order ? __ldg(p.order + t / per) : t / per;
+    const int local = t % per;
+    w.m0 = (local / p.n_tiles) * WBM;
+    w.n0 = (local % p.n_tiles) * BN;
+    w.r0 = __ldg(offs + w.e);
+    w.r1 = __ldg(offs + w.e + 1);
+    w.nkb = (w.r1 - w.r0 + PBK - 1) / PBK;
+    return w;
+  };
+  auto warp_wait = [&](uint64_t* bar, uint32_t parity) {
+    const bool ok = wait_pair(bar, parity, &sm->abort_flag, peer_abort, p.err);
+    return __all_sync(0xffffffffu, ok) != 0;
+  };
+  // rows past the expert's end belong to the next expert: zero them in this
+  // CTA's two A boxes of the stage (whole K steps of them are skipped)
+  auto zero_tail = [&](uint8_t* a, int valid) {
+    const int nks = (valid + 15) / 16;
+    const int nrow = nks * 16 - valid, per_box = nrow * 8;
+    for (int i = lane; i < 2 * per_box; i += 32) {
+      const int box = i / per_box, rem = i % per_box;
+      *reinterpret_cast<uint4*>(a + box * P_BOX + (valid + rem / 8) * 128 + (rem % 8) * 16) =
+          make_uint4(0, 0, 0, 0);
+    }
+    if (nrow > 0) ptx::fence_proxy_async_smem();
+    return nks;
+  };
+
+  if (warp == 0) {
+    // ===================================================== TMA producer
+    if (run) {
+      if (lane == 0) {
+        ptx::prefetch_tmap(&tmA);
+        ptx::prefetch_tmap(&tmB);
+      }
+      uint32_t it = 0;
+      bool ok = true;
+      for (int r = 0, t = tile_of(0); t < total && ok; t = tile_of(++r)) {
+        const WT w = decode_w(t);
+        for (int kb = 0; kb < w.nkb; ++kb, ++it) {
+          const int s = it % P_NS;
+          if (!warp_wait(&sm->empty[s], ((it / P_NS) & 1u) ^ 1u)) { ok = false; break; }
+          if (lane == 0) {
+            uint8_t* a = smem + s * P_STAGE;
+            uint8_t* b = a + P_A_BYTES;
+            uint64_t* fb = &sm->full[s];
+            ptx::mbar_expect_tx(fb, P_STAGE);
+            const int row = w.r0 + kb * PBK;
+#pragma unroll
+            for (int j = 0; j < 2; ++j) ptx::tma_load_2d(a + j * P_BOX, &tmA, fb, w.m0 + 128 * rank + 64 * j, row);
+#pragma unroll
+            for (int j = 0; j < 2; ++j) ptx::tma_load_2d(b + j * P_BOX, &tmB, fb, w.n0 + 128 * rank + 64 * j, row);
+          }
+          __syncwarp();
+        }
+      }
+      // the even CTA's commits release these stages: wait for the last ones
+      // to land before the CTA may finish
+      for (int k = 0; k < P_NS && ok; ++k, ++it) ok = warp_wait(&sm->empty[it % P_NS], ((it / P_NS) & 1u) ^ 1u);
+      if (!ok && lane == 0) {
+        // let loads in flight finish (bounded) before the CTA leaves
+        for (int s = 0; s < P_NS; ++s) {
+          const long long t0 = clock64();
+          while (clock64() - t0 < kWaitLimitCycles / 8 && !ptx::mbar_try_wait(&sm->full[s], 0) &&
+                 !ptx::mbar_try_wait(&sm->full[s], 1)) {
+          }
+        }
+      }
+    }
+  } else if (warp == 1 && rank == 1) {
+    // ============================================ relay (odd CTA of the pair)
+    const uint32_t leader_full0 = in_cta(&sm->full[0], 0);
+    uint32_t it = 0;
+    bool ok = run;
+    for (int r = 0, t = tile_of(0); t < total && ok; t = tile_of(++r)) {
+      const WT w = decode_w(t);
+      for (int kb = 0; kb < w.nkb; ++kb, ++it) {
+        const int s = it % P_NS;
+        if (!warp_wait(&sm->full[s], (it / P_NS) & 1u)) { ok = false; break; }
+        const int valid = w.r1 - (w.r0 + kb * PBK);
+        if (valid < PBK) zero_tail(smem + s * P_STAGE, valid);
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive_cluster(leader_full0 + 8u * s);
+      }
+    }
+  } else if (warp == 1) {
+    // ============================================ MMA issuer (even CTA)
+    constexpr uint32_t idesc = ptx::idesc_bf16_f32(2 * BM, BN, 1, 1);
+    const uint32_t peer_empty0 = in_cta(&sm->empty[0], 1), peer_tfull0 = in_cta(&sm->tfull[0], 1);
+    uint32_t it = 0, acc_it = 0;
+    bool ok = run;
+    for (int r = 0, t = tile_of(0); t < total && ok; t = tile_of(++r)) {
+      const WT w = decode_w(t);
+      if (w.nkb == 0) continue;
+      const uint32_t buf = acc_it & 1u;
+      if (!warp_wait(&sm->tempty[buf], ((acc_it >> 1) & 1u) ^ 1u)) { ok = false; break; }
+      ptx::tc_fence_after();
+      const uint32_t d_tmem = tmem + buf * BN;
+      for (int kb = 0; kb < w.nkb; ++kb, ++it) {
+        const int s = it % P_NS;
+        if (!warp_wait(&sm->full[s], (it / P_NS) & 1u)) { ok = false; break; }
+        ptx::tc_fence_after();
+        uint8_t* a = smem + s * P_STAGE;
+        const int valid = w.r1 - (w.r0 + kb * PBK);
+        const int nks = valid < PBK ? zero_tail(a, valid) : PBK / 16;
+        __syncwarp();
+        if (lane == 0) {
+          const uint32_t a_addr = ptx::smem_u32(a), b_addr = a_addr + P_A_BYTES;
+          for (int ks = 0; ks < nks; ++ks) {
+            const uint64_t ad = ptx::smem_desc_sw128(a_addr + ks * 2048, P_BOX, 1024);
+            const uint64_t bd = ptx::smem_desc_sw128(b_addr + ks * 2048, P_BOX, 1024);
+            ptx::mma_f16_pair(d_tmem, ad, bd, idesc, (kb > 0 || ks > 0) ? 1u : 0u);
+          }
+          ptx::mma_commit_pair(ptx::smem_u32(&sm->empty[s]));
+          ptx::mma_commit_pair(peer_empty0 + 8u * s);
+        }
+        __syncwarp();
+      }
+      if (!ok) break;
+      if (lane == 0) {
+        ptx::mma_commit_pair(ptx::smem_u32(&sm->tfull[buf]));
+        ptx::mma_commit_pair(peer_tfull0 + 8u * buf);
+      }
+      __syncwarp();
+      ++acc_it;
+    }
+    if (!ok && run && lane == 0) {
+      ptx::mma_commit_pair(ptx::smem_u32(&sm->drain));
+      const long long t0 = clock64();
+      while (clock64() - t0 < kWaitLimitCycles / 8 && !ptx::mbar_try_wait(&sm->drain, 0)) {
+      }
+    }
+  } else {
+    // ============================================================ epilogue
+    // warp (q, ch): TMEM lanes 32q..32q+31 (this CTA's rows), columns
+    // 128ch..128ch+127 of the accumulator, read and stored 64 at a time.
+    const int ew = warp - 2, q = warp & 3, ch = ew >> 2;
+    const uint32_t leader_tempty0 = in_cta(&sm->tempty[0], 0);
+    uint8_t* stg = smem + P_NS * P_STAGE + ew * W_STG;
+    uint32_t acc_it = 0;
+    for (int r = 0, t = tile_of(0); t < total && run; t = tile_of(++r)) {
+      const WT w = decode_w(t);
+      const uint32_t buf = acc_it & 1u;
+      if (w.nkb > 0) {
+        if (!warp_wait(&sm->tfull[buf], (acc_it >> 1) & 1u)) break;
+        ptx::tc_fence_after();
+      }
+      const uint32_t tbase = tmem + buf * BN + static_cast<uint32_t>(ch * 128) + (static_cast<uint32_t>(q * 32) << 16);
+      const int mb = w.m0 + 128 * static_cast<int>(rank) + 32 * q;
+#pragma unroll 1
+      for (int c = 0; c < 2; ++c) {
+        uint32_t v[32];
+        if (w.nkb > 0) {
+          uint32_t v0[32], v1[32];
+          ptx::tmem_ld32(tbase + c * 64, v0);
+          ptx::tmem_ld32(tbase + c * 64 + 32, v1);
+          ptx::tmem_wait_ld();
+          if (c == 1) {
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive_cluster(leader_tempty0 + 8u * buf);
+          }
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            __nv_bfloat162 h0 = __floats2bfloat162_rn(__uint_as_float(v0[2 * i]), __uint_as_float(v0[2 * i + 1]));
+            __nv_bfloat162 h1 = __floats2bfloat162_rn(__uint_as_float(v1[2 * i]), __uint_as_float(v1[2 * i + 1]));
+            v[i] = *reinterpret_cast<uint32_t*>(&h0);
+            v[16 + i] = *reinterpret_cast<uint32_t*>(&h1);
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = 0u;  // expert with no rows: dW_e = 0
+        }
+        const int n = w.n0 + ch * 128 + c * 64;
+        if (n >= p.N) continue;
+        // each lane writes its row's 128 bytes; each instruction then stores
+        // four rows' 128-byte segments (8 lanes per row)
+#pragma unroll
+        for (int g = 0; g < 8; ++g)
+          *reinterpret_cast<uint4*>(stg + lane * 128 + ((g ^ (lane & 7)) << 4)) =
+              make_uint4(v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]);
+        __syncwarp();
+        const int g = lane & 7;
+        __nv_bfloat16* base;
+        size_t ld;
+        if (KIND == WGRAD2) {
+          base = static_cast<__nv_bfloat16*>(p.out0) + ((size_t)w.e * p.M + mb) * p.N + n;
+          ld = p.N;
+        } else {
+          base = n < p.f ? static_cast<__nv_bfloat16*>(p.out0) + ((size_t)w.e * p.d + mb) * p.f + n
+                         : static_cast<__nv_bfloat16*>(p.out1) + ((size_t)w.e * p.d + mb) * p.f + (n - p.f);
+          ld = p.f;
+        }
+        base += 8 * g;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int rr = 4 * i + (lane >> 3);
+          const uint4 u = *reinterpret_cast<const uint4*>(stg + rr * 128 + ((g ^ (rr & 7)) << 4));
+          if (mb + rr < p.M) *reinterpret_cast<uint4*>(base + rr * ld) = u;
+        }
+        __syncwarp();
+      }
+      if (w.nkb > 0) ++acc_it;
+    }
+  }
+
+  // No CTA of the pair leaves while the other may still reach its shared
+  // memory or TMEM; then both free the pair's TMEM together.
+  __syncwarp();
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::cluster_sync();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc_pair(tmem, TMEM_COLS);
+  }
+}
+
+template <int KIND>
+cudaError_t launch_wgrad_pair(const CUtensorMap& a, const CUtensorMap& b, const Params& p, cudaStream_t st) {
+  const long tiles = (long)p.E * p.m_tiles * p.n_tiles;
+  if (tiles <= 0) return cudaSuccess;
+  const size_t smem = 1024 + P_NS * P_STAGE + NUM_EPI_WARPS * W_STG + sizeof(PairSmem) + 64;
+  cudaError_t e = cudaFuncSetAttribute(tc_wgrad_pair_kernel<KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(NUM_THREADS);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  // pairs resident at once (a pair needs two SMs of one GPC)
+  static int max_pairs = 0;
+  if (max_pairs <= 0) {
+    cfg.gridDim = dim3(2 * (sm_count() / 2));
+    e = cudaOccupancyMaxActiveClusters(&max_pairs, tc_wgrad_pair_kernel<KIND>, &cfg);
+    if (e != cudaSuccess) return e;
+    if (max_pairs <= 0) return cudaErrorLaunchOutOfResources;
+  }
+  const long pairs = tiles < max_pairs ? tiles : max_pairs;
+  cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs));
+  return MOE_COUNTED_AS(::moe::gemm_kind_name(KIND, false), st)
+      cudaLaunchKernelEx(&cfg, tc_wgrad_pair_kernel<KIND>, a, b, p);
+}
+
 constexpr CUtensorMapDataType BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
 
 // Experts ordered by row count, largest first, ties by index (order[i] = the
@@ -875,6 +1237,18 @@ int sm_count() {
 
 using namespace tc;
 
+// Weight-gradient kernel choice (moe_use_cta_pairs): single-CTA 256x256 tiles
+// by default, CTA pairs on request.
+static std::atomic<int> g_cta_pairs{0};
+
+template <int KIND>
+cudaError_t launch_wgrad_any(const CUtensorMap& a, const CUtensorMap& b, const Params& p, cudaStream_t st) {
+  return g_cta_pairs.load(std::memory_order_relaxed) ? launch_wgrad_pair<KIND>(a, b, p, st)
+                                                     : launch_wgrad<KIND>(a, b, p, st);
+}
+
+void set_cta_pairs(int on) { g_cta_pairs.store(on ? 1 : 0, std::memory_order_relaxed); }
+
 cudaError_t launch_expert_order(const int32_t* offsets, int E, int32_t* order, cudaStream_t st) {
   if (E <= 0 || E > 1024) return cudaErrorInvalidValue;
   MOE_COUNTED_AS("expert_order", st) expert_order_kernel<<<1, 1024, 0, st>>>(offsets, E, order);
@@ -924,11 +1298,13 @@ cudaError_t tc_mlp_bwd(const void* dy_perm, const void* x_perm, const void* h, c
   e = launch<DGRAD2>(mA, mB0, mB0, p, ((long)(R + BM - 1) / BM + E) * p.n_tiles, st);
   if (e != cudaSuccess) return e;
   // dWd[e] = A_e^T dy_e
-  if (!map_2d(&mA, a, BF, 2, f, R, 64, 64) || !map_2d(&mB0, dy_perm, BF, 2, d, R, 64, 64))
+  // K rows per stage (TMA box height) of the weight-gradient kernel in use
+  const int wbk = g_cta_pairs.load(std::memory_order_relaxed) ? PBK : BK;
+  if (!map_2d(&mA, a, BF, 2, f, R, 64, wbk) || !map_2d(&mB0, dy_perm, BF, 2, d, R, 64, wbk))
     return cudaErrorInvalidValue;
   p.M = f; p.N = d; p.m_tiles = (f + WBM - 1) / WBM; p.n_tiles = (d + BN - 1) / BN; p.out0 = dwd;
   p.order = order;
-  e = launch_wgrad<WGRAD2>(mA, mB0, p, st);
+  e = launch_wgrad_any<WGRAD2>(mA, mB0, p, st);
   p.order = nullptr;
   if (e != cudaSuccess) return e;
   // dx_perm = dh_g . Wg^T + dh_u . Wu^T
@@ -939,13 +1315,15 @@ cudaError_t tc_mlp_bwd(const void* dy_perm, const void* x_perm, const void* h, c
   e = launch_row256<DGRAD1>(mA, mB0, mB1, p, R, st);
   if (e != cudaSuccess) return e;
   // [dWg | dWu][e] = x_perm_e^T dh_e (with src_row: K rows gathered from x [T][d])
-  const bool ok_a = src_row ? map_2d(&mA, x_perm, BF, 2, d, T, 64, 1) : map_2d(&mA, x_perm, BF, 2, d, R, 64, 64);
-  if (!ok_a || !map_2d(&mB0, dh, BF, 2, 2L * f, R, 64, 64)) return cudaErrorInvalidValue;
+  const int gbk = src_row ? 64 : wbk;
+  const bool ok_a = src_row ? map_2d(&mA, x_perm, BF, 2, d, T, 64, 1) : map_2d(&mA, x_perm, BF, 2, d, R, 64, gbk);
+  if (!ok_a || !map_2d(&mB0, dh, BF, 2, 2L * f, R, 64, gbk)) return cudaErrorInvalidValue;
   p.M = d; p.N = 2 * f; p.m_tiles = (d + WBM - 1) / WBM; p.n_tiles = (2 * f + BN - 1) / BN;
   p.out0 = dwg; p.out1 = dwu;
   p.src_row = src_row; p.gk = gk; p.T = T;
   p.order = order;
-  return src_row ? launch_wgrad<WGRAD1, true>(mA, mB0, p, st) : launch_wgrad<WGRAD1>(mA, mB0, p, st);
+  if (src_row) return launch_wgrad<WGRAD1, true>(mA, mB0, p, st);
+  return launch_wgrad_any<WGRAD1>(mA, mB0, p, st);
 }
 
 cudaError_t tc_router_logits(const void* x, const void* w_r, const float* bias, int T, int d, int E,

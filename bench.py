@@ -429,6 +429,8 @@ def run_ours(args, s, rank, world):
     if world > 1:
         torch.distributed.barrier()
     N.load()
+    if args.cta_pairs:
+        N.moe_use_cta_pairs(1)
     weights = Weights()
     m = measure(s, weights, args.steps, args.warmup, local, e2e=True, world=world)
     elapsed_ms, e2e_ms = max_over_ranks([m["elapsed_ms"], m["e2e_ms"]], device="cuda")
@@ -442,7 +444,7 @@ def run_ours(args, s, rank, world):
     # beside it for runs of several seconds
     peak = burst if timed_s < 1.0 else sus
     achieved = gemm_flops(s) / (m["gemm_ms"] / 1e3) / 1e12
-    traffic = None if (args.tokens or args.experts) else gemm_traffic(args.config)
+    traffic = None if (args.tokens or args.experts or args.cta_pairs) else gemm_traffic(args.config)
     kt = kernel_table(s, m["per_launch"], pk, pk_kind)
     out = {
         "metric": METRIC,
@@ -458,6 +460,7 @@ def run_ours(args, s, rank, world):
         "dtype": s.dtype,
         "data": "synthetic (seeded N(0,1) tokens, N(0,1/fan_in) weights, router N(0,0.02^2))",
         "config": config_of(s, world),
+        "wgrad_kernel": "cta_pairs" if args.cta_pairs else "single_cta",
         "tflops_per_s": step_flops(s) * world * args.steps / (elapsed_ms / 1e3) / 1e12,
         "roofline": {"kernel": "grouped expert GEMMs (fwd+bwd, 6 GEMMs per step"
                                + ("; includes the MXFP8 operand quantisation)" if s.dtype == "mxfp8" else ")"),
@@ -501,6 +504,8 @@ def main():
     ap.add_argument("--no-more", action="store_true",
                     help="skip the nested MXFP8 / bf16-twin / skewed-routing workloads of the default line")
     ap.add_argument("--more-steps", type=int, default=50, help="timed steps of each nested workload")
+    ap.add_argument("--cta-pairs", action="store_true",
+                    help="weight gradients on CTA pairs (moe_use_cta_pairs(1)) instead of single CTAs")
     ap.add_argument("--experts", type=int, default=0,
                     help="override E (with --tokens: small profiling cases with the same rows per expert)")
     args = ap.parse_args()

@@ -185,25 +185,27 @@ quant_cols_kernel(const __nv_bfloat16* __restrict__ src, int rows, int C, const 
   }
 }
 
-// Weights in both K layouts from one read: a CTA stages a 32-row x 128-column
-// tile of W [rows][C] in shared memory and writes it quantised along its
-// columns (blocks of 32 rows: codes qc, scale chunks sc_c grouped by 128-row
-// K stage x 128-column group) and along its rows (blocks of 32 columns:
-// codes qr, scale chunks sc_r grouped by 128-row group x 128-column K stage).
-// rows and C are multiples of 128, so no block crosses a weight matrix. CTAs
-// stride over the tiles (those of one 32-row band are consecutive, so W is
-// read in order) with the next tile's cp.async copies in flight while the
-// current one is converted; the column codes are staged so that they leave as
-// 16-byte pieces of rows. The bytes equal those of the separate column and
-// row quantisers.
+// Weight preparation: each 32x128 tile of a weight [rows][C] is read once
+// (cp.async, two tiles in flight per block) and written quantised along its
+// columns (blocks of 32 rows: the forward GEMMs' K) and along its rows (blocks
+// of 32 columns: the dgrads' K), both as [rows][C] codes plus scale chunks.
+// Warp w takes the tile's columns 32w..32w+31 with one row per lane: the
+// lane's 32 values are its row block; the 32 column maxima come from a
+// butterfly over the lanes on bf16 pairs (16 shuffles), and their scales
+// return to every lane through 128 bytes of shared memory. The bytes equal
+// those of the separate column and row quantisers. rows and C are multiples
+// of 128, so no block crosses a weight matrix; blocks stride over the tiles
+// (those of one 32-row band are consecutive, so W is read in order).
 constexpr int kDualCols = 128, kDualPitch = kDualCols + 8;  // bf16 per staged row (16-byte pad)
 constexpr int kDualTile = 32 * kDualPitch;
-__global__ void __launch_bounds__(128)
+constexpr int kDualCodePitch = kDualCols + 16;  // bytes per staged code row (conflict-free 16-byte stores)
+__global__ void __launch_bounds__(128, 8)
 quant_dual_kernel(const __nv_bfloat16* __restrict__ src, int C, long ntiles, uint8_t* __restrict__ qc,
                   uint8_t* __restrict__ sc_c, uint8_t* __restrict__ qr, uint8_t* __restrict__ sc_r) {
   __shared__ __align__(16) __nv_bfloat16 tile[2 * kDualTile];
-  __shared__ __align__(16) uint8_t cbuf[32 * kDualCols];
-  const int tid = threadIdx.x;
+  __shared__ __align__(16) float col_mul[4][32];
+  __shared__ __align__(16) uint8_t codes[2][32 * kDualCodePitch];  // the tile's row codes, column codes
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int cg = C / kDualCols;
   auto issue = [&](long t, int buf) {  // a half-warp copies one 256-byte row segment per step
     const long row0 = t / cg * 32;
@@ -226,35 +228,18 @@ quant_dual_kernel(const __nv_bfloat16* __restrict__ src, int C, long ntiles, uin
     asm volatile("cp.async.commit_group;" ::: "memory");
     asm volatile("cp.async.wait_group 1;" ::: "memory");  // this tile's copies have landed
     __syncthreads();
-    const __nv_bfloat16* tl = tile + (it & 1) * kDualTile;
-    const long row0 = t / cg * 32;
-    const int c0 = static_cast<int>(t % cg) * kDualCols;
-    {  // along the columns: this thread's column over the 32 rows
-      float v[32], amax = 0.0f;
-#pragma unroll
-      for (int r = 0; r < 32; ++r) {
-        v[r] = __bfloat162float(tl[r * kDualPitch + tid]);
-        amax = fmaxf(amax, fabsf(v[r]));
-      }
-      const int sx = e8m0_exponent(amax);
-      const float m = pow2_neg(sx);
-#pragma unroll
-      for (int r = 0; r < 32; r += 2) {
-        const uint32_t b = mx_e4m3x2(v[r] * m, v[r + 1] * m);
-        cbuf[r * kDualCols + tid] = static_cast<uint8_t>(b);
-        cbuf[(r + 1) * kDualCols + tid] = static_cast<uint8_t>(b >> 8);
-      }
-      sc_c[(((row0 >> 7) * cg + c0 / 128) << 9) + mx_chunk_lane(tid) + ((row0 >> 5) & 3)] =
-          static_cast<uint8_t>(sx + 127);
-    }
-    {  // along the rows: block (row r, 32 columns cb); lanes are rows
-      const int r = tid & 31, cb = tid >> 5;
-      uint32_t w[16];
+    const long row0 = t / cg * 32, row = row0 + lane;  // this lane's row
+    const int c0 = static_cast<int>(t % cg) * kDualCols, cl = 32 * warp;  // this warp's columns c0 + cl ..
+    uint32_t w[16];  // the lane's row, columns cl..cl+31, as bf16 pairs
+    {
+      const __nv_bfloat16* tl = tile + (it & 1) * kDualTile + lane * kDualPitch + cl;
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        const uint4 u = *reinterpret_cast<const uint4*>(tl + r * kDualPitch + 32 * cb + 8 * i);
+        const uint4 u = *reinterpret_cast<const uint4*>(tl + 8 * i);
         w[4 * i] = u.x; w[4 * i + 1] = u.y; w[4 * i + 2] = u.z; w[4 * i + 3] = u.w;
       }
+    }
+    {  // along the row: the lane's 32 values are one block
       const int sx = e8m0_exponent(absmax_bf16x32(w));
       const float m = pow2_neg(sx);
       uint32_t cw[8];
@@ -262,21 +247,50 @@ quant_dual_kernel(const __nv_bfloat16* __restrict__ src, int C, long ntiles, uin
       for (int i = 0; i < 8; ++i)
         cw[i] = mx_e4m3x2(bf16_lo(w[2 * i]) * m, bf16_hi(w[2 * i]) * m) |
                 (mx_e4m3x2(bf16_lo(w[2 * i + 1]) * m, bf16_hi(w[2 * i + 1]) * m) << 16);
-      const long row = row0 + r;
-      uint4* out = reinterpret_cast<uint4*>(qr + row * C + c0 + 32 * cb);
+      uint4* out = reinterpret_cast<uint4*>(codes[0] + lane * kDualCodePitch + cl);
       out[0] = make_uint4(cw[0], cw[1], cw[2], cw[3]);
       out[1] = make_uint4(cw[4], cw[5], cw[6], cw[7]);
-      sc_r[(((row >> 7) * cg + c0 / 128) << 9) + mx_chunk_lane(static_cast<int>(row & 127)) + cb] =
+      sc_r[(((row >> 7) * cg + c0 / 128) << 9) + mx_chunk_lane(static_cast<int>(row & 127)) + warp] =
           static_cast<uint8_t>(sx + 127);
     }
-    __syncthreads();  // every column's codes are staged
+    {  // along the columns: lane l ends with column cl + l's maximum over the 32 rows
+      uint32_t a[16];
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      const int id = tid + 128 * i, r = id >> 3, g = id & 7;
-      *reinterpret_cast<uint4*>(qc + (row0 + r) * C + c0 + 16 * g) =
-          *reinterpret_cast<const uint4*>(cbuf + r * kDualCols + 16 * g);
+      for (int i = 0; i < 16; ++i) a[i] = w[i] & 0x7FFF7FFFu;
+      colmax_step<8>(a, lane);
+      colmax_step<4>(a, lane);
+      colmax_step<2>(a, lane);
+      colmax_step<1>(a, lane);
+      a[0] = bf16x2_max(a[0], __shfl_xor_sync(0xffffffffu, a[0], 1));
+      const int sx = e8m0_exponent((lane & 1) ? bf16_hi(a[0]) : bf16_lo(a[0]));
+      col_mul[warp][lane] = pow2_neg(sx);
+      sc_c[(((row0 >> 7) * cg + c0 / 128) << 9) + mx_chunk_lane(cl + lane) + ((row0 >> 5) & 3)] =
+          static_cast<uint8_t>(sx + 127);
+      __syncwarp();
+      float m[32];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float4 v = reinterpret_cast<const float4*>(col_mul[warp])[i];
+        m[4 * i] = v.x; m[4 * i + 1] = v.y; m[4 * i + 2] = v.z; m[4 * i + 3] = v.w;
+      }
+      uint32_t cw[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        cw[i] = mx_e4m3x2(bf16_lo(w[2 * i]) * m[4 * i], bf16_hi(w[2 * i]) * m[4 * i + 1]) |
+                (mx_e4m3x2(bf16_lo(w[2 * i + 1]) * m[4 * i + 2], bf16_hi(w[2 * i + 1]) * m[4 * i + 3]) << 16);
+      uint4* out = reinterpret_cast<uint4*>(codes[1] + lane * kDualCodePitch + cl);
+      out[0] = make_uint4(cw[0], cw[1], cw[2], cw[3]);
+      out[1] = make_uint4(cw[4], cw[5], cw[6], cw[7]);
     }
-    __syncthreads();  // the buffers are refilled two tiles on
+    __syncthreads();  // both code tiles are staged
+    // each instruction stores four rows' 128-byte segments of one layout
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int id = tid + 128 * i, lay = id >> 8, r = (id >> 3) & 31, g = id & 7;
+      uint8_t* dst = (lay == 0 ? qr : qc) + (row0 + r) * C + c0 + 16 * g;
+      *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(codes[lay] + r * kDualCodePitch + 16 * g);
+    }
+    __syncthreads();  // the tile buffer is refilled next iteration; col_mul and codes are reused
   }
   asm volatile("cp.async.wait_all;" ::: "memory");
 }
@@ -378,7 +392,11 @@ cudaError_t launch_mxfp8_quant_dual(const void* src, long rows, int C, uint8_t* 
                                     uint8_t* sc_r, cudaStream_t st) {
   if (rows == 0) return cudaSuccess;
   const long ntiles = rows / 32 * (C / kDualCols);
-  const long grid = std::min<long>(ntiles, (long)tc::sm_count() * 10);
+  static int per_sm = 0;  // resident blocks per SM
+  if (per_sm <= 0 &&
+      (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, quant_dual_kernel, 128, 0) != cudaSuccess || per_sm <= 0))
+    per_sm = 8;
+  const long grid = std::min<long>(ntiles, (long)tc::sm_count() * per_sm);
   MOE_COUNTED_AS("quant_dual", st) quant_dual_kernel<<<static_cast<unsigned>(grid), 128, 0, st>>>(static_cast<const __nv_bfloat16*>(src), C,
                                                                            ntiles, qc, sc_c, qr, sc_r);
   return cudaGetLastError();

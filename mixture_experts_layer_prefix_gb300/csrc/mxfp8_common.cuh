@@ -64,6 +64,23 @@ __device__ __forceinline__ float absmax_bf16x32(const uint32_t (&w)[16]) {
   return fmaxf(bf16_lo(m[0]), bf16_hi(m[0]));
 }
 
+// One step of a butterfly reduce-scatter of per-column maxima over the warp,
+// on bf16 pairs (word i = columns 2i, 2i+1): with 2H words per lane, the lane
+// keeps the H words picked by lane bit 2H and takes the max with its partner's
+// copy of them (lane ^ 2H; the partner keeps the other H). After the steps
+// H = 8, 4, 2, 1, word 0 of lane l holds columns 2(l/2), 2(l/2)+1, maxed over
+// the 16 lanes that agree with l in bit 0.
+template <int H>
+__device__ __forceinline__ void colmax_step(uint32_t (&a)[16], int lane) {
+  const bool up = (lane & (2 * H)) != 0;
+#pragma unroll
+  for (int i = 0; i < H; ++i) {
+    const uint32_t keep = up ? a[H + i] : a[i];
+    const uint32_t give = up ? a[i] : a[H + i];
+    a[i] = bf16x2_max(keep, __shfl_xor_sync(0xffffffffu, give, 2 * H));
+  }
+}
+
 // Round-to-nearest-even E4M3 codes of v0 (low byte) and v1 (high byte),
 // saturated to +-448, from one paired conversion.
 __device__ __forceinline__ uint32_t mx_e4m3x2(float v0, float v1) {

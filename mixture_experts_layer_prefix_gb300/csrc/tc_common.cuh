@@ -253,23 +253,6 @@ __device__ __forceinline__ void quant_rows_staged(const Params& p, uint8_t* stg,
   warp_store_rows32(stg, cw, p.qout + (size_t)wrow * ld + col, ld, nrows, lane);
 }
 
-// One step of a butterfly reduce-scatter of per-column maxima over the warp,
-// on bf16 pairs (word i = columns 2i, 2i+1): with 2H words per lane, the lane
-// keeps the H words picked by lane bit 2H and takes the max with its partner's
-// copy of them (lane ^ 2H; the partner keeps the other H). After the steps
-// H = 8, 4, 2, 1, word 0 of lane l holds columns 2(l/2), 2(l/2)+1, maxed over
-// the 16 lanes that agree with l in bit 0.
-template <int H>
-__device__ __forceinline__ void colmax_step(uint32_t (&a)[16], int lane) {
-  const bool up = (lane & (2 * H)) != 0;
-#pragma unroll
-  for (int i = 0; i < H; ++i) {
-    const uint32_t keep = up ? a[H + i] : a[i];
-    const uint32_t give = up ? a[i] : a[H + i];
-    a[i] = bf16x2_max(keep, __shfl_xor_sync(0xffffffffu, give, 2 * H));
-  }
-}
-
 // MXFP8 quantisation of the same chunk along its rows, in blocks of 32 rows:
 // the warp's rows are one such block of the expert segment (rows >= nrows are
 // past the segment's end and count as zero). Codes to qcol[row][col..col+32)

@@ -68,6 +68,60 @@ def test_quantize_segmented_columns_bit_exact(seg, C):
     np.testing.assert_array_equal(q.cpu().numpy(), rq)
 
 
+def _chunk_lane(t):
+    """Byte of index t (< 128) of a group inside a 512-byte scale chunk, as the
+    tensor-memory scale copy takes it (block b of the K stage adds b)."""
+    t = np.asarray(t)
+    return (t % 32) * 16 + ((t // 32) % 4) * 4
+
+
+def _scales_of_cols(sbuf, rows, C):
+    """[rows/32][C] scales of a [rows][C] operand quantised along its columns,
+    from the chunk layout: chunk (32-row block b // 4, column c // 128), byte
+    mx_chunk_lane(c % 128) + b % 4."""
+    b = np.arange(rows // 32)[:, None]
+    c = np.arange(C)[None, :]
+    idx = ((b // 4) * (C // 128) + c // 128) * 512 + _chunk_lane(c % 128) + b % 4
+    return sbuf[idx]
+
+
+def _scales_of_rows(sbuf, rows, C):
+    """[rows][C/32] scales of a [rows][C] operand quantised along its rows:
+    chunk (row r // 128, column block j // 4), byte mx_chunk_lane(r % 128) + j % 4."""
+    r = np.arange(rows)[:, None]
+    j = np.arange(C // 32)[None, :]
+    idx = ((r // 128) * (C // 128) + j // 4) * 512 + _chunk_lane(r % 128) + j % 4
+    return sbuf[idx]
+
+
+@pytest.mark.parametrize("E,d,f", [(2, 256, 384), (3, 128, 256), (1, 512, 128)])
+def test_prepare_weights_bytes(E, d, f):
+    """moe_mxfp8_prepare_weights: both layouts of every weight (codes and scale
+    chunks) bit-exact against the oracle's quantiser, the layouts read in the
+    order the library carves them (each piece 256-byte aligned)."""
+    wg, wu, wd = _values(E * d, f, 11), _values(E * d, f, 12), _values(E * f, d, 13)
+    wq = torch.zeros(N.moe_mxfp8_weights_size(E, d, f), dtype=torch.uint8, device="cuda")
+    N.moe_mxfp8_prepare_weights(_dev(wg), _dev(wu), _dev(wd), E, d, f, wq)
+    torch.cuda.synchronize()
+    buf = wq.cpu().numpy()
+    parts, used = [], 0
+    Ed, Ef = E * d, E * f
+    for n in (Ed * f, Ed // 32 * f, Ed * f, Ed // 32 * f, Ef * d, Ef // 32 * d,
+              Ef * d, Ef * d // 32, Ed * f, Ed * f // 32, Ed * f, Ed * f // 32):
+        parts.append(buf[used:used + n])
+        used += (n + 255) // 256 * 256
+    cols = [(wg, parts[0], parts[1]), (wu, parts[2], parts[3]), (wd, parts[4], parts[5])]
+    rows = [(wd, parts[6], parts[7]), (wg, parts[8], parts[9]), (wu, parts[10], parts[11])]
+    for w, q, sc in cols:  # blocks of 32 rows of each column (the forward GEMMs' K)
+        rq, rs = oracle.mxfp8_quantize_cols_segmented(w, np.array([0, w.shape[0]], np.int32))
+        np.testing.assert_array_equal(q.reshape(w.shape), rq)
+        np.testing.assert_array_equal(_scales_of_cols(sc, *w.shape), rs[:w.shape[0] // 32])
+    for w, q, sc in rows:  # blocks of 32 columns of each row (the dgrads' K)
+        rq, rs = oracle.mxfp8_quantize_rows(w)
+        np.testing.assert_array_equal(q.reshape(w.shape), rq)
+        np.testing.assert_array_equal(_scales_of_rows(sc, *w.shape), rs)
+
+
 # ------------------------------------------------- MXFP8 expert GEMMs, whole layer
 from mixture_experts_layer_prefix_gb300 import layer as L  # noqa: E402
 from oracle import mxfp8_layer  # noqa: E402

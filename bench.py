@@ -198,7 +198,11 @@ def kernel_work(s):
            "router_dw": 2.0 * T * d + 8.0 * R + 4.0 * E * d,
            "router_dlogits": 12.0 * R + 4.0 * T * E,
            "permute_quant": 2.0 * T * d + (2.0 + 1.0 + 1.0 / 32) * R * d + 12.0 * R,
-           "quant_dual": 3.0 * E * d * f * (2.0 + 2 * 33.0 / 32)}
+           "quant_dual": 3.0 * E * d * f * (2.0 + 2 * 33.0 / 32),
+           # x_perm and dy_perm quantised along the experts' rows: read bf16, write codes + scales
+           "quant_cols": 2.0 * R * d * (2.0 + 33.0 / 32)}
+    if s.dtype == "mxfp8":  # the combine backward also writes g*dy's row codes and scales
+        byt["combine_bwd"] += 33.0 / 32 * R * d
     return flops, byt
 
 

@@ -141,6 +141,51 @@ def _err(got, ref):
     return float(np.abs(got - ref).max() / max(np.abs(ref).max(), 1e-30))
 
 
+def _segment_scales(sbuf, offs, C):
+    """[sum_g ceil(len_g/32)][C] scales of a [R][C] operand quantised along the
+    experts' rows, from the chunk layout grouped by per-expert 128-row tiles:
+    block b of expert e is in stage word (offs[e] + 127 e) // 128 + b // 4,
+    byte mx_chunk_lane(c % 128) + b % 4 of chunk word * (C / 128) + c // 128."""
+    out = []
+    c = np.arange(C)
+    for e in range(len(offs) - 1):
+        for b in range((int(offs[e + 1]) - int(offs[e]) + 31) // 32):
+            word = (int(offs[e]) + 127 * e) // 128 + b // 4
+            out.append(sbuf[(word * (C // 128) + c // 128) * 512 + _chunk_lane(c % 128) + b % 4])
+    return np.array(out, np.uint8).reshape(-1, C)
+
+
+@pytest.mark.parametrize("s", MX_SHAPES, ids=lambda s: s.name)
+def test_mxfp8_segment_quantisers_agree(s):
+    """A quantised along the experts' rows two ways: by the GEMM1 epilogue
+    (a_cols, checked byte by byte against the oracle's segmented quantiser) and
+    by the tiled column quantiser on a_save inside the backward (used when
+    a_cols is NULL). The backward must give the same bits either way."""
+    inp = synth.Inputs(s, seed=6)
+    p = L.params_from_inputs(inp, N.MOE_MXFP8)
+    b = L.Buffers(s.T, s.d, s.E, s.k, s.f, N.MOE_MXFP8)
+    L.forward(p, b)
+    torch.cuda.synchronize()
+    R, f = b.R, s.f
+    offs = b.offsets.cpu().numpy()
+    a = b.a_save.float().cpu().numpy()
+    acols = b.a_cols.cpu().numpy()
+    rq, rs = oracle.mxfp8_quantize_cols_segmented(a, offs)
+    np.testing.assert_array_equal(acols[:R * f].reshape(R, f), rq)
+    np.testing.assert_array_equal(_segment_scales(acols[(R * f + 255) // 256 * 256:], offs, f), rs)
+    outs = []
+    for cols in (b.a_cols, None):
+        grads = [torch.zeros_like(t) for t in (b.dx_perm, b.dw_gate, b.dw_up, b.dw_down)]
+        L.backward(p, b)  # dy codes, dy_perm and the router backward for this step
+        N.moe_mxfp8_mlp_bwd(b.dy_q, b.dy_sc, b.dy_perm, b.x_perm, b.h_save, b.a_save, cols, b.wq, b.offsets, R,
+                            s.E, s.d, f, *grads, b.workspace)
+        torch.cuda.synchronize()
+        outs.append(grads)
+    assert N.moe_get_device_error() == 0
+    for x, y in zip(*outs):
+        assert torch.equal(x, y)
+
+
 @pytest.mark.parametrize("s", MX_SHAPES, ids=lambda s: s.name)
 def test_mxfp8_layer_parity(s):
     inp = synth.Inputs(s, seed=2)

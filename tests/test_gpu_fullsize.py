@@ -191,3 +191,38 @@ def test_fullsize_mxfp8_sampled_parity():
         errs[f"dw_down[{e}]"] = maxnorm_err(np_of(b.dw_down[e]), r1["dw_down"][0])
     bad = {k: v for k, v in errs.items() if not v <= tol}
     assert not bad, f"{bad} (all: {errs})"
+
+
+@pytest.mark.parametrize("name", ["e128_top4", "e128_top4_skew"])
+def test_fullsize_cta_pair_weight_gradients(name):
+    """The weight gradients on CTA pairs (moe_use_cta_pairs(1)) at the
+    workload's full size, in the launch configuration bench.py --cta-pairs
+    times: the smallest, the largest and one more sampled expert against the
+    oracle, and exact zeros for experts without rows."""
+    s = synth.CONFIGS[name]
+    inp = synth.Inputs(s, seed=0)
+    p = L.params_from_inputs(inp, N.MOE_BF16)
+    b = L.Buffers(s.T, s.d, s.E, s.k, s.f, N.MOE_BF16)
+    N.moe_use_cta_pairs(1)
+    try:
+        L.forward(p, b)
+        L.backward(p, b)
+        torch.cuda.synchronize()
+    finally:
+        N.moe_use_cta_pairs(0)
+    assert N.moe_get_device_error() == 0
+    gl = b.logits.cpu().numpy()
+    ref_route = oracle.route(gl.astype(np.float64), s.k, s.E)
+    np.testing.assert_array_equal(b.offsets.cpu().numpy(), ref_route["offsets"])
+    counts = ref_route["counts"]
+    cand = np.flatnonzero(counts > 0)
+    rng = np.random.default_rng(7)
+    picks = {int(cand[np.argmin(counts[cand])]), int(cand[np.argmax(counts[cand])]), int(rng.choice(cand))}
+    errs = {}
+    for e in sorted(picks):
+        errs.update(_expert_dw_check(inp, b, ref_route, e))
+    for e in np.flatnonzero(counts == 0)[:2]:
+        assert float(b.dw_gate[int(e)].float().abs().max()) == 0.0
+        assert float(b.dw_down[int(e)].float().abs().max()) == 0.0
+    bad = {k: v for k, v in errs.items() if not v <= BF16_TOL}
+    assert not bad, f"{name}: {bad} (all: {errs})"

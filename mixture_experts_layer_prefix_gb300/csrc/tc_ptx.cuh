@@ -1,7 +1,7 @@
 // tc_ptx.cuh -- inline-PTX wrappers for sm_100-family features used by the
 // grouped GEMMs: mbarriers, TMA tensor loads, TMEM allocation, tcgen05.mma,
-// tcgen05.commit and tcgen05.ld. Written against the PTX ISA's descriptions
-// of these instructions.
+// tcgen05.commit and tcgen05.ld, and their CTA-pair (2-CTA cluster) forms.
+// Written against the PTX ISA's descriptions of these instructions.
 #pragma once
 
 #include <cuda.h>
@@ -177,21 +177,6 @@ __host__ __device__ constexpr uint32_t idesc_mxf8_f32(int M, int N, int a_mn_maj
          | (1u << 23)                                  // scale format: UE8M0
          | (static_cast<uint32_t>(M >> 4) << 24)      // M / 16
          | (static_cast<uint32_t>(a_sf) << 29);        // A scale-factor id
-}
-
-// Write 4 / 8 consecutive 32-bit TMEM columns of this warp's 32 lanes.
-__device__ __forceinline__ void tmem_st4(uint32_t taddr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-  asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr), "r"(a), "r"(b),
-               "r"(c), "r"(d)
-               : "memory");
-}
-__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
-  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
-               "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
-               : "memory");
-}
-__device__ __forceinline__ void tmem_wait_st() {
-  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
 // 32 lanes x 32 consecutive 32-bit TMEM columns: thread i gets row (lane base + i).

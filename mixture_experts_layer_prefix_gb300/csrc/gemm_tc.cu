@@ -40,9 +40,11 @@ constexpr int NUM_THREADS = 64 + 32 * NUM_EPI_WARPS;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int OUT_STG_BYTES = NUM_EPI_WARPS * STG_BYTES;  // epilogue staging, one buffer per warp
 
+constexpr int MAX_STAGES = 6;  // the deepest ring of the kernels below
+
 struct Smem {
-  uint64_t full[STAGES];
-  uint64_t empty[STAGES];
+  uint64_t full[MAX_STAGES];
+  uint64_t empty[MAX_STAGES];
   uint64_t tfull[2];
   uint64_t tempty[2];
   uint64_t drain;
@@ -50,14 +52,22 @@ struct Smem {
   int abort_flag;
 };
 
+// Stages of the row-tile ring for a tile width TBN: 48 KB stages at the full
+// width, 32 KB stages (and more of them) for the 128-column router tiles.
+template <int TBN> constexpr int row_stages() { return TBN == BN ? STAGES : MAX_STAGES; }
+template <int TBN> constexpr int row_stage_bytes() { return A_BYTES + TBN * BK * 2; }
+
 // GATHER: the dispatch is fused into GEMM1 (FPROP1 only; p.src_row set).
-template <int KIND, bool GATHER = false>
+// TBN: output columns per tile (256; 128 for the router logits, N = E).
+template <int KIND, bool GATHER = false, int TBN = BN>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
                const __grid_constant__ CUtensorMap tmB1, const Params p) {
   using Tr = Traits<KIND>;
   static_assert(!Tr::kragged, "weight gradients run in tc_wgrad_kernel");
-  constexpr int NS = STAGES;
+  static_assert(TBN == BN || (KIND == ROUTER && TBN == 128), "narrow tiles for the router only");
+  constexpr int NS = row_stages<TBN>();
+  constexpr int STAGE_BYTES = row_stage_bytes<TBN>();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* out_stage = smem + NS * STAGE_BYTES;  // epilogue staging
@@ -128,7 +138,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
               ptx::tma_load_3d(b, &tmB0, fb, k0, tl.n_idx * BN, tl.e);
             } else if (KIND == ROUTER) {
               ptx::tma_load_2d(a, &tmA, fb, k0, tl.m0);
-              ptx::tma_load_2d(b, &tmB0, fb, k0, tl.n_idx * BN);
+              ptx::tma_load_2d(b, &tmB0, fb, k0, tl.n_idx * TBN);
             } else {  // DGRAD1
               ptx::tma_load_2d(a, &tmA, fb, k0, tl.m0);
               if (k0 < p.f) ptx::tma_load_3d(b, &tmB0, fb, k0, tl.n_idx * BN, tl.e);
@@ -202,7 +212,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     }
   } else if (warp == 1) {
     // ========================================================= MMA issuer
-    constexpr uint32_t idesc = ptx::idesc_bf16_f32(BM, BN, Tr::a_mn ? 1 : 0, Tr::b_mn ? 1 : 0);
+    constexpr uint32_t idesc = ptx::idesc_bf16_f32(BM, TBN, Tr::a_mn ? 1 : 0, Tr::b_mn ? 1 : 0);
     uint32_t it = 0, acc_it = 0;
     bool ok = true;
     for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
@@ -212,7 +222,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       const uint32_t aph = (acc_it >> 1) & 1u;
       if (!wait_bar(&sm->tempty[buf], aph ^ 1u, &sm->abort_flag, p.err)) { ok = false; break; }
       ptx::tc_fence_after();
-      const uint32_t d_tmem = tmem + static_cast<uint32_t>(buf * BN);
+      const uint32_t d_tmem = tmem + static_cast<uint32_t>(buf * TBN);
       for (int kb = 0; kb < tl.nkb; ++kb, ++it) {
         const int s = it % NS;
         const uint32_t ph = (it / NS) & 1u;
@@ -249,7 +259,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     // Warp w reads TMEM lanes 32*(w%4)..+31 (rows of the tile); the two warps
     // of a quadrant split the tile's columns in halves.
     const int ew = warp - 2, q = warp & 3, half = ew >> 2;
-    constexpr int NC = epi_chunks<KIND>();
+    constexpr int NC = KIND == ROUTER ? TBN / 32 : epi_chunks<KIND>();
     uint8_t* stg = out_stage + ew * STG_BYTES;
     uint32_t acc_it = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
@@ -259,9 +269,9 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       const uint32_t aph = (acc_it >> 1) & 1u;
       if (!wait_bar(&sm->tfull[buf], aph, &sm->abort_flag, p.err)) break;
       ptx::tc_fence_after();
-      const uint32_t tbase = tmem + static_cast<uint32_t>(buf * BN) + (static_cast<uint32_t>(q * 32) << 16);
+      const uint32_t tbase = tmem + static_cast<uint32_t>(buf * TBN) + (static_cast<uint32_t>(q * 32) << 16);
       if constexpr (KIND == ROUTER)
-        epilogue_router(p, tl, tbase, q * 32 + lane, half * NC / 2, (half + 1) * NC / 2);
+        epilogue_router<TBN>(p, tl, tbase, q * 32 + lane, half * NC / 2, (half + 1) * NC / 2);
       else
         epilogue_tile_staged<KIND>(p, tl, tbase, q, lane, half * NC / 2, (half + 1) * NC / 2, stg);
       ptx::tc_fence_before();
@@ -279,21 +289,23 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   }
 }
 
-template <int KIND>
+template <int KIND, int TBN = BN>
 size_t smem_bytes(int E) {
-  return 1024 + STAGES * STAGE_BYTES + OUT_STG_BYTES + sizeof(Smem) + 2 * (E + 1) * sizeof(int) + 64;
+  return 1024 + row_stages<TBN>() * row_stage_bytes<TBN>() + OUT_STG_BYTES + sizeof(Smem) +
+         2 * (E + 1) * sizeof(int) + 64;
 }
 
-template <int KIND, bool GATHER = false>
+template <int KIND, bool GATHER = false, int TBN = BN>
 cudaError_t launch(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1, const Params& p,
                    long max_tiles, cudaStream_t st) {
   if (max_tiles <= 0) return cudaSuccess;
-  const size_t smem = smem_bytes<KIND>(p.E);
-  cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<KIND, GATHER>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
+  const size_t smem = smem_bytes<KIND, TBN>(p.E);
+  cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<KIND, GATHER, TBN>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   const int grid = static_cast<int>(max_tiles < sm_count() ? max_tiles : sm_count());
-  MOE_COUNTED_AS(::moe::gemm_kind_name(KIND, false), st) tc_gemm_kernel<KIND, GATHER><<<grid, NUM_THREADS, smem, st>>>(a, b0, b1, p);
+  MOE_COUNTED_AS(::moe::gemm_kind_name(KIND, false), st)
+      tc_gemm_kernel<KIND, GATHER, TBN><<<grid, NUM_THREADS, smem, st>>>(a, b0, b1, p);
   return cudaGetLastError();
 }
 
@@ -1331,9 +1343,10 @@ cudaError_t tc_router_logits(const void* x, const void* w_r, const float* bias, 
   CUtensorMap mA, mB;
   Params p{};
   p.offsets = nullptr; p.bias = bias; p.E = 1; p.R = T; p.d = d; p.f = 0; p.err = device_error_word();
-  if (!map_2d(&mA, x, BF, 2, d, T, 64, BM) || !map_2d(&mB, w_r, BF, 2, d, E, 64, BN)) return cudaErrorInvalidValue;
-  p.N = E; p.n_tiles = (E + BN - 1) / BN; p.out0 = logits;
-  return launch<ROUTER>(mA, mB, mB, p, (long)((T + BM - 1) / BM) * p.n_tiles, st);
+  constexpr int RBN = 128;  // logits tile width: E is a multiple of 32, most often 128 or less
+  if (!map_2d(&mA, x, BF, 2, d, T, 64, BM) || !map_2d(&mB, w_r, BF, 2, d, E, 64, RBN)) return cudaErrorInvalidValue;
+  p.N = E; p.n_tiles = (E + RBN - 1) / RBN; p.out0 = logits;
+  return launch<ROUTER, false, RBN>(mA, mB, mB, p, (long)((T + BM - 1) / BM) * p.n_tiles, st);
 }
 
 }  // namespace moe

@@ -5,10 +5,10 @@
 // contiguous input buffer).
 //
 // Pipeline (all deterministic, no dependence on atomic ordering):
-//   1. topk_hist: one warp per chunk of TPC tokens. Per token: warp-wide
-//      k-round argmax over 64-bit keys (ordered logit, inverted index), gates
-//      as a softmax over the selected logits, and a per-chunk expert
-//      histogram written to hist[chunk][e].
+//   1. topk_hist: one CTA per chunk of kTokensPerChunk tokens, one warp per
+//      token: warp-wide k-round argmax over 64-bit keys (ordered logit,
+//      inverted index), gates as a softmax over the selected logits, and the
+//      chunk's expert histogram written to hist[chunk][e].
 //   2. chunk_scan: one CTA per expert; exclusive scan of hist[.][e] over the
 //      chunks (in place) and the expert's total count.
 //   3. offsets: exclusive scan of the counts.
@@ -36,38 +36,34 @@ __device__ __forceinline__ float key_value(uint32_t key) {
   return __uint_as_float(b);
 }
 
+// One CTA per chunk, one warp per token (kWarps == kTokensPerChunk). NV:
+// logits per lane (E <= 32 NV). The chunk's expert histogram is summed with
+// shared-memory integer atomics (exact in any order), then written out.
 template <int NV>
 __global__ void __launch_bounds__(kWarps * 32)
 topk_hist_kernel(const float* __restrict__ logits, int T, int E, int k, int nchunks,
                  int32_t* __restrict__ topk_idx, float* __restrict__ gates,
                  int32_t* __restrict__ hist) {
-  extern __shared__ int32_t cnt_all[];
+  static_assert(kWarps == kTokensPerChunk, "one warp per token of the chunk");
+  extern __shared__ int32_t cnt[];  // [E]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int c = blockIdx.x * kWarps + warp;
-  if (c >= nchunks) return;
-  int32_t* cnt = cnt_all + warp * E;
-  for (int e = lane; e < E; e += 32) cnt[e] = 0;
-  __syncwarp();
-
-  const int t_end = min(T, (c + 1) * kTokensPerChunk);
-  // the next token's logits are loaded while this token's experts are selected
-  float nxt[NV];
-  auto load_row = [&](int t) {
+  const int c = blockIdx.x;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = 0;
+  const int t = c * kTokensPerChunk + warp;
+  float row[NV];
 #pragma unroll
-    for (int i = 0; i < NV; ++i) {
-      const int e = lane + 32 * i;
-      nxt[i] = e < E ? __ldg(logits + (size_t)t * E + e) : 0.0f;
-    }
-  };
-  if (c * kTokensPerChunk < t_end) load_row(c * kTokensPerChunk);
-  for (int t = c * kTokensPerChunk; t < t_end; ++t) {
+  for (int i = 0; i < NV; ++i) {
+    const int e = lane + 32 * i;
+    row[i] = (t < T && e < E) ? __ldg(logits + (size_t)t * E + e) : 0.0f;
+  }
+  __syncthreads();  // counters cleared
+  if (t < T) {
     uint32_t key[NV];
 #pragma unroll
     for (int i = 0; i < NV; ++i) {
       const int e = lane + 32 * i;
-      key[i] = e < E ? ordered_key(nxt[i]) : 0u;
+      key[i] = e < E ? ordered_key(row[i]) : 0u;
     }
-    if (t + 1 < t_end) load_row(t + 1);
     uint32_t taken = 0u;
     int my_idx = 0;
     float my_val = 0.0f, top_val = 0.0f;
@@ -91,7 +87,7 @@ topk_hist_kernel(const float* __restrict__ logits, int T, int E, int k, int nchu
       if ((idx & 31) == lane) taken |= 1u << (idx >> 5);
       if (lane == j) { my_idx = idx; my_val = val; }
       if (j == 0) top_val = val;
-      if (lane == 0) cnt[idx] += 1;
+      if (lane == 0) atomicAdd(&cnt[idx], 1);
     }
     const float ex = lane < k ? expf(my_val - top_val) : 0.0f;
     const float z = warp_sum(ex);
@@ -100,8 +96,8 @@ topk_hist_kernel(const float* __restrict__ logits, int T, int E, int k, int nchu
       gates[(size_t)t * k + lane] = ex / z;
     }
   }
-  __syncwarp();
-  for (int e = lane; e < E; e += 32) hist[(size_t)c * E + e] = cnt[e];
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) hist[(size_t)c * E + e] = cnt[e];
 }
 
 // In-place exclusive scan of hist[.][e] over chunks for expert e = blockIdx.x.
@@ -218,12 +214,11 @@ cudaError_t launch_route_meta(const float* logits, int T, int E, int k, int32_t*
                               int32_t* src_row, int32_t* hist, cudaStream_t st) {
   const int nchunks = route_num_chunks(T);
   if (nchunks > 0) {
-    const int grid = (nchunks + kWarps - 1) / kWarps;
-    const size_t smem = (size_t)kWarps * E * sizeof(int32_t);
+    const size_t smem = (size_t)E * sizeof(int32_t);
     const int nv = (E + 31) / 32;
-#define MOE_TOPK_CASE(NVV)                                                                     \
-  MOE_COUNTED_AS("topk_hist", st) topk_hist_kernel<NVV><<<grid, kWarps * 32, smem, st>>>(logits, T, E, k, nchunks, topk_idx, \
-                                                          gates, hist)
+#define MOE_TOPK_CASE(NVV)                                                                           \
+  MOE_COUNTED_AS("topk_hist", st) topk_hist_kernel<NVV><<<nchunks, kWarps * 32, smem, st>>>(          \
+      logits, T, E, k, nchunks, topk_idx, gates, hist)
     if (nv <= 1) MOE_TOPK_CASE(1);
     else if (nv <= 2) MOE_TOPK_CASE(2);
     else if (nv <= 4) MOE_TOPK_CASE(4);

@@ -5,10 +5,12 @@
 //
 // One persistent kernel per GEMM, one CTA per SM, warp-specialised:
 //   warp 0      TMA producer: 4-stage ring of (A 128x64, B 256x64) bf16 tiles,
-//               128-byte swizzled, filled by cp.async.bulk.tensor.
+//               128-byte swizzled, filled by cp.async.bulk.tensor (the router
+//               GEMM, N = E: 6 stages of (A 128x64, B 128x64)).
 //   warp 1      TMEM owner and MMA issuer: tcgen05.mma M=128 N=256 K=16 into
 //               one of two 256-column fp32 accumulators (512 TMEM columns),
-//               so the epilogue of tile i overlaps the MMAs of tile i+1.
+//               so the epilogue of tile i overlaps the MMAs of tile i+1
+//               (router: N=128 into two 128-column accumulators).
 //   warps 2..9  epilogue: tcgen05.ld of the accumulator, fused SwiGLU (fwd or
 //               bwd) math, bf16 (or fp32 router logits) stores with row/column
 //               masks; two warps per TMEM lane quadrant, each half the columns.

@@ -14,6 +14,21 @@ namespace {
 
 constexpr int kRowWarps = 8;
 
+// 16 loaded bytes as floats: 8 bf16 or 4 fp32 elements (the load of Vec16
+// split in two, so the bytes can be requested well before they are used).
+__device__ __forceinline__ void unpack16(const uint4& q, float* v, const __nv_bfloat16*) {
+  const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    v[2 * i] = __uint_as_float(w[i] << 16);
+    v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+}
+__device__ __forceinline__ void unpack16(const uint4& q, float* v, const float*) {
+  v[0] = __uint_as_float(q.x); v[1] = __uint_as_float(q.y);
+  v[2] = __uint_as_float(q.z); v[3] = __uint_as_float(q.w);
+}
+
 // x_perm[dest_row[t][j]] = x[t]
 template <typename T>
 __global__ void __launch_bounds__(kRowWarps * 32)
@@ -180,7 +195,11 @@ combine_bwd_kernel(const T* __restrict__ dy, const T* __restrict__ y_perm,
 }
 
 // dx[t] = sum_j dx_perm[dest[t][j]] (+ sum_j dl[t][e_j] * w_r[e_j])
-template <typename T>
+// KMAX: the largest k the instance handles. ROUTER: the router term is added
+// (dlogits and w_r given). Each column step first requests all of its rows --
+// the k rows of dx_perm and, with ROUTER, the k rows of w_r -- and only then
+// adds them, so the two sets of loads wait on memory together.
+template <typename T, int KMAX, bool ROUTER>
 __global__ void __launch_bounds__(kRowWarps * 32)
 permute_bwd_kernel(const T* __restrict__ dx_perm, int Tn, int d, int E, int k,
                    const int32_t* __restrict__ dest_row, const int32_t* __restrict__ topk_idx,
@@ -190,40 +209,48 @@ permute_bwd_kernel(const T* __restrict__ dx_perm, int Tn, int d, int E, int k,
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * kRowWarps + (threadIdx.x >> 5);
   if (t >= Tn) return;
-  const bool router = dlogits != nullptr;
   const int my_dest = lane < k ? dest_row[(size_t)t * k + lane] : 0;
   int my_e = 0;
-  if (router && lane < k) my_e = topk_idx[(size_t)t * k + lane];
-  const unsigned ok = usable_pairs(my_dest, my_e, lane, k, (long)Tn * k, router ? E : 0, err);
+  if (ROUTER && lane < k) my_e = topk_idx[(size_t)t * k + lane];
+  const unsigned ok = usable_pairs(my_dest, my_e, lane, k, (long)Tn * k, ROUTER ? E : 0, err);
   float my_dl = 0.0f;
-  if (router && lane < k && ((ok >> lane) & 1u)) my_dl = dlogits[(size_t)t * E + my_e];
-  int dest[8], ex[8];
-  float dl[8];
+  if (ROUTER && lane < k && ((ok >> lane) & 1u)) my_dl = dlogits[(size_t)t * E + my_e];
+  int dest[KMAX], ex[KMAX];
+  float dl[KMAX];
 #pragma unroll
-  for (int j = 0; j < 8; ++j) {
+  for (int j = 0; j < KMAX; ++j) {
     dest[j] = __shfl_sync(0xffffffffu, my_dest, j);
     ex[j] = __shfl_sync(0xffffffffu, my_e, j);
     dl[j] = __shfl_sync(0xffffffffu, my_dl, j);
   }
   for (int c = lane * V::N; c < d; c += 32 * V::N) {
+    uint4 xv[KMAX], wv[ROUTER ? KMAX : 1];
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j)
+      if (j < k && ((ok >> j) & 1u)) xv[j] = *reinterpret_cast<const uint4*>(dx_perm + (size_t)dest[j] * d + c);
+    if constexpr (ROUTER) {
+#pragma unroll
+      for (int j = 0; j < KMAX; ++j)
+        if (j < k && ((ok >> j) & 1u)) wv[j] = *reinterpret_cast<const uint4*>(w_r + (size_t)ex[j] * d + c);
+    }
     float acc[V::N];
 #pragma unroll
     for (int i = 0; i < V::N; ++i) acc[i] = 0.0f;
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
+    for (int j = 0; j < KMAX; ++j) {
       if (j < k && ((ok >> j) & 1u)) {
         float v[V::N];
-        V::load(dx_perm + (size_t)dest[j] * d + c, v);
+        unpack16(xv[j], v, dx_perm);
 #pragma unroll
         for (int i = 0; i < V::N; ++i) acc[i] += v[i];
       }
     }
-    if (router) {
+    if constexpr (ROUTER) {
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
+      for (int j = 0; j < KMAX; ++j) {
         if (j < k && ((ok >> j) & 1u)) {
           float w[V::N];
-          V::load(w_r + (size_t)ex[j] * d + c, w);
+          unpack16(wv[j], w, w_r);
 #pragma unroll
           for (int i = 0; i < V::N; ++i) acc[i] = fmaf(dl[j], w[i], acc[i]);
         }
@@ -391,9 +418,17 @@ cudaError_t launch_permute_bwd(const void* dx_perm, int Tn, int d, int E, int k,
                                const int32_t* dest_row, const int32_t* topk_idx, const float* dlogits,
                                const void* w_r, void* dx, cudaStream_t st) {
   if (Tn == 0) return cudaSuccess;
-  MOE_COUNTED_AS("permute_bwd", st) permute_bwd_kernel<T><<<row_grid<T>(Tn), kRowWarps * 32, 0, st>>>(
-      static_cast<const T*>(dx_perm), Tn, d, E, k, dest_row, topk_idx, dlogits,
-      static_cast<const T*>(w_r), static_cast<T*>(dx), device_error_word());
+#define MOE_PBWD(KM, RT)                                                                               \
+  MOE_COUNTED_AS("permute_bwd", st) permute_bwd_kernel<T, KM, RT><<<row_grid<T>(Tn), kRowWarps * 32, 0, st>>>( \
+      static_cast<const T*>(dx_perm), Tn, d, E, k, dest_row, topk_idx, dlogits, static_cast<const T*>(w_r),     \
+      static_cast<T*>(dx), device_error_word())
+  const bool router = dlogits != nullptr;
+  if (k <= 4) {
+    if (router) MOE_PBWD(4, true); else MOE_PBWD(4, false);
+  } else {
+    if (router) MOE_PBWD(8, true); else MOE_PBWD(8, false);
+  }
+#undef MOE_PBWD
   return cudaGetLastError();
 }
 

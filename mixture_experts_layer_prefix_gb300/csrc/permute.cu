@@ -52,7 +52,9 @@ permute_kernel(const T* __restrict__ x, int Tn, int d, int k, const int32_t* __r
 }
 
 // y[t] = sum_j g[t][j] * y_perm[dest_row[t][j]]   (fp32, j ascending)
-template <typename T>
+// KMAX: the largest k the instance handles; each column step requests its k
+// rows before adding any.
+template <typename T, int KMAX>
 __global__ void __launch_bounds__(kRowWarps * 32)
 combine_fwd_kernel(const T* __restrict__ y_perm, const float* __restrict__ gates,
                    const int32_t* __restrict__ dest_row, int Tn, int d, int k, T* __restrict__ y, int* err) {
@@ -63,22 +65,26 @@ combine_fwd_kernel(const T* __restrict__ y_perm, const float* __restrict__ gates
   const int my_dest = lane < k ? dest_row[(size_t)t * k + lane] : 0;
   const float my_g = lane < k ? gates[(size_t)t * k + lane] : 0.0f;
   const unsigned ok = usable_pairs(my_dest, 0, lane, k, (long)Tn * k, 0, err);
-  int dest[8];
-  float g[8];
+  int dest[KMAX];
+  float g[KMAX];
 #pragma unroll
-  for (int j = 0; j < 8; ++j) {
+  for (int j = 0; j < KMAX; ++j) {
     dest[j] = __shfl_sync(0xffffffffu, my_dest, j);
     g[j] = __shfl_sync(0xffffffffu, my_g, j);
   }
   for (int c = lane * V::N; c < d; c += 32 * V::N) {
+    uint4 yv[KMAX];
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j)
+      if (j < k && ((ok >> j) & 1u)) yv[j] = *reinterpret_cast<const uint4*>(y_perm + (size_t)dest[j] * d + c);
     float acc[V::N];
 #pragma unroll
     for (int i = 0; i < V::N; ++i) acc[i] = 0.0f;
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
+    for (int j = 0; j < KMAX; ++j) {
       if (j < k && ((ok >> j) & 1u)) {
         float v[V::N];
-        V::load(y_perm + (size_t)dest[j] * d + c, v);
+        unpack16(yv[j], v, y_perm);
 #pragma unroll
         for (int i = 0; i < V::N; ++i) acc[i] = fmaf(g[j], v[i], acc[i]);
       }
@@ -143,17 +149,21 @@ combine_bwd_kernel(const T* __restrict__ dy, const T* __restrict__ y_perm,
   for (int cb = 0; cb < d; cb += 32 * V::N) {
     const int c = cb + lane * V::N;
     const bool act = c < d;
-    float u[V::N];
+    // every row of the step is requested before any is used
+    uint4 uq = make_uint4(0, 0, 0, 0), yq[KMAX];
+    if (act) uq = *reinterpret_cast<const uint4*>(dy + (size_t)t * d + c);
 #pragma unroll
-    for (int i = 0; i < V::N; ++i) u[i] = 0.0f;
-    if (act) V::load(dy + (size_t)t * d + c, u);
+    for (int j = 0; j < KMAX; ++j) {
+      yq[j] = make_uint4(0, 0, 0, 0);
+      if (act && j < k && ((ok >> j) & 1u)) yq[j] = *reinterpret_cast<const uint4*>(y_perm + (size_t)dest[j] * d + c);
+    }
+    float u[V::N];
+    unpack16(uq, u, dy);
 #pragma unroll
     for (int j = 0; j < KMAX; ++j) {
       if (j < k && ((ok >> j) & 1u)) {
         float v[V::N], w[V::N];
-#pragma unroll
-        for (int i = 0; i < V::N; ++i) v[i] = 0.0f;
-        if (act) V::load(y_perm + (size_t)dest[j] * d + c, v);
+        unpack16(yq[j], v, y_perm);
 #pragma unroll
         for (int i = 0; i < V::N; ++i) {
           dot[j] = fmaf(u[i], v[i], dot[j]);
@@ -375,8 +385,12 @@ template <typename T>
 cudaError_t launch_combine_fwd(const void* y_perm, const float* gates, const int32_t* dest_row, int Tn,
                                int d, int k, void* y, cudaStream_t st) {
   if (Tn == 0) return cudaSuccess;
-  MOE_COUNTED_AS("combine_fwd", st) combine_fwd_kernel<T><<<row_grid<T>(Tn), kRowWarps * 32, 0, st>>>(
-      static_cast<const T*>(y_perm), gates, dest_row, Tn, d, k, static_cast<T*>(y), device_error_word());
+  if (k <= 4)
+    MOE_COUNTED_AS("combine_fwd", st) combine_fwd_kernel<T, 4><<<row_grid<T>(Tn), kRowWarps * 32, 0, st>>>(
+        static_cast<const T*>(y_perm), gates, dest_row, Tn, d, k, static_cast<T*>(y), device_error_word());
+  else
+    MOE_COUNTED_AS("combine_fwd", st) combine_fwd_kernel<T, 8><<<row_grid<T>(Tn), kRowWarps * 32, 0, st>>>(
+        static_cast<const T*>(y_perm), gates, dest_row, Tn, d, k, static_cast<T*>(y), device_error_word());
   return cudaGetLastError();
 }
 

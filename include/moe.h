@@ -189,17 +189,19 @@ moe_status moe_grouped_mlp_bwd(const void* dy_perm, const void* x_perm, const vo
                                void* dw_down, void* workspace, size_t workspace_bytes,
                                void* stream);
 
-/* Selects the kernel of the bf16 weight-gradient GEMMs: both of
-   moe_grouped_mlp_bwd, and the GEMM2 one of moe_dispatch_mlp_bwd (its GEMM1
-   weight gradient gathers rows and keeps one CTA per SM). Process-wide, for
-   launches issued after the call ("Scaling and optimizing MoE
-   training": grouped GEMM; the kernel choice itself has no counterpart in
-   the pages). 0 (the default): one CTA per SM computes 256x256 gradient tiles,
-   its two fp32 accumulators filling TMEM. 1: CTA pairs (2-CTA clusters) compute
-   the same tiles with tcgen05.mma.cta_group::2 (M=256 across both SMs), each SM
-   holding a 128x256 half twice over so that the epilogue overlaps the next
-   tile's MMAs. Both give the same results up to fp32 summation order. Returns
-   MOE_OK. */
+/* Selects the kernel of the weight-gradient GEMMs: the bf16 ones of
+   moe_grouped_mlp_bwd and the GEMM2 one of moe_dispatch_mlp_bwd (its GEMM1
+   weight gradient gathers rows and keeps one CTA per SM), and the MXFP8 ones
+   of moe_mxfp8_mlp_bwd. Process-wide, for launches issued after the call
+   ("Scaling and optimizing MoE training": grouped GEMM; the kernel choice
+   itself has no counterpart in the pages). 0 (the default): one CTA per SM,
+   bf16 256x256 gradient tiles (two fp32 accumulators fill TMEM), MXFP8
+   128x256 tiles (the block scales take the rest of TMEM). 1: CTA pairs
+   (2-CTA clusters) with tcgen05.mma.cta_group::2 (M=256 across both SMs):
+   bf16 256x256 tiles, each SM holding a 128x256 half twice over so that the
+   epilogue overlaps the next tile's MMAs; MXFP8 256x256 tiles, each SM
+   holding its 128x256 half and the block scales. Both give the same results
+   up to fp32 summation order. Returns MOE_OK. */
 moe_status moe_use_cta_pairs(int enable);
 
 /* The dispatch fused into the grouped MLP ("Scaling and optimizing MoE

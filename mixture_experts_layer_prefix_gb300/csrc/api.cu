@@ -411,6 +411,7 @@ moe_status moe_mxfp8_prepare_weights(const void* w_gate, const void* w_up, const
 
 moe_status moe_use_cta_pairs(int enable) {
   set_cta_pairs(enable);
+  set_mx_cta_pairs(enable);
   return MOE_OK;
 }
 

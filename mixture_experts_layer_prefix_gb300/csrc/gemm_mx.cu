@@ -26,6 +26,8 @@
 // B at 272 + (TBN/32)s. Shared scale staging of a stage: A 512 B (row r of the
 // copy = tile rows r, 32+r, 64+r, 96+r), then B TBN/128 x 512 B (copy h row r
 // = tile columns 128h + r, +32, +64, +96).
+#include <atomic>
+
 #include "kernels.h"
 #include "tc_common.cuh"
 
@@ -526,11 +528,360 @@ cudaError_t launch(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMa
   return cudaGetLastError();
 }
 
+// ---------------------------------------------------------------------------
+// MXFP8 weight gradients on CTA pairs (2-CTA clusters,
+// tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale). A single CTA's tile
+// stops at 128 x 256 here: the block scales take the TMEM columns a second
+// 256-column accumulator would need, so its operands cost 48 KB per 128-row K
+// stage. A pair computes a 256 x 256 block of one expert's gradient: each CTA
+// loads its own 128 features of A and its own 128 columns of B per stage
+// (32 KB for the same MMA work per SM), its own A scale chunk and both B
+// scale chunks. In a pair MMA each CTA's TMEM must hold the B scales of all
+// 256 columns and the A scales of its own rows; tcgen05.cp.cta_group::2,
+// issued by the even CTA, copies each CTA's staged chunks into its own TMEM.
+// Each CTA's TMEM receives its 128 rows x 256 columns of the accumulator (one
+// buffer, drained into registers and released before the stores).
+//   warp 0      both CTAs: producer of its own half of each stage.
+//   warp 1      even CTA: scale copies and MMA issue; each stage's release
+//               and each finished accumulator are committed to both CTAs.
+//               odd CTA: relay; zeroes its A rows past the expert's end once
+//               its half has landed, then arrives on the even CTA's `full`.
+//   warps 2..9  both CTAs: epilogue of its own 128 rows.
+// All 32 lanes of a warp poll each barrier; every wait is bounded, and a CTA
+// that gives up raises both CTAs' abort flags.
+constexpr int PX_NS = 6;
+constexpr int PX_A = 128 * BK;                                 // own 128 features x 128 K rows
+constexpr int PX_STAGE = 2 * PX_A;                             // + own 128 columns of B
+constexpr int PX_SC = 512 + 1024;                              // A chunk, then both B chunks
+constexpr uint32_t PX_SFA = 256, PX_SFB = 288;  // TMEM scale rings (B scales 32-column aligned)
+static_assert(PX_SFA + 4 * PX_NS <= PX_SFB && PX_SFB + 8 * PX_NS <= TMEM_COLS, "scale rings fit next to the accumulator");
+
+struct PxSmem {
+  uint64_t full[PX_NS];
+  uint64_t empty[PX_NS];
+  uint64_t tfull, tempty, drain;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+__device__ __forceinline__ void tmem_cp_pair_32x128b_x4(uint32_t taddr, uint64_t desc) {
+  asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(desc) : "memory");
+}
+__device__ __forceinline__ void mma_mxf8_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                              uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+          d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+// Bounded wait on a local mbarrier whose arrivals may come from the other CTA
+// of the pair; on expiry it sets the error word and both CTAs' abort flags.
+__device__ __forceinline__ bool px_wait(uint64_t* bar, uint32_t parity, int* abort_flag, uint32_t peer_abort,
+                                        int* err) {
+  if (ptx::mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (true) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    if (*reinterpret_cast<volatile int*>(abort_flag)) return false;
+    if (clock64() - t0 > kWaitLimitCycles) {
+      set_error(err, MOE_ERR_TIMEOUT);
+      *reinterpret_cast<volatile int*>(abort_flag) = 1;
+      ptx::st_cluster_u32(peer_abort, 1u);
+      return false;
+    }
+  }
+}
+
+template <int KIND>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+mx_wgrad_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                     const Params p) {
+  static_assert(KIND == WGRAD1 || KIND == WGRAD2, "weight-gradient kinds");
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sc_area = smem + PX_NS * PX_STAGE;
+  uint8_t* stg_area = sc_area + PX_NS * PX_SC;
+  PxSmem* sm = reinterpret_cast<PxSmem*>(stg_area + NUM_EPI_WARPS * STG_BYTES);
+  const int* __restrict__ offs = p.offsets;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = ptx::cluster_ctarank(), peer = rank ^ 1u;
+  const int cid = static_cast<int>(ptx::cluster_id_x()), ncl = static_cast<int>(ptx::n_clusters_x());
+  auto in_cta = [&](const void* x, uint32_t r) { return ptx::mapa(ptx::smem_u32(x), r); };
+  const uint32_t peer_abort = in_cta(&sm->abort_flag, peer);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < PX_NS; ++s) {
+      ptx::mbar_init(&sm->full[s], rank == 0 ? 2 : 1);
+      ptx::mbar_init(&sm->empty[s], 1);
+    }
+    ptx::mbar_init(&sm->tfull, 1);
+    ptx::mbar_init(&sm->tempty, 2 * NUM_EPI_WARPS);
+    ptx::mbar_init(&sm->drain, 1);
+    sm->abort_flag = 0;
+    ptx::fence_mbar_init();
+    ptx::fence_proxy_async_smem();
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc_pair(&sm->tmem_base, TMEM_COLS);
+    ptx::tmem_relinquish_pair();
+  }
+  ptx::tc_fence_before();
+  ptx::cluster_sync();  // both CTAs' barriers initialised and TMEM allocated
+  ptx::tc_fence_after();
+  const uint32_t tmem = sm->tmem_base;
+  if (threadIdx.x == 0 && ptx::ld_cluster_u32(in_cta(&sm->tmem_base, peer)) != tmem) {
+    set_error(p.err, MOE_ERR_DEVICE_PAIR);
+    sm->abort_flag = 1;
+  }
+  __syncthreads();
+  const bool run = sm->abort_flag == 0;
+
+  const int per = p.m_tiles * p.n_tiles;  // m_tiles: blocks of 256 features
+  const int total = p.E * per;
+  // the pair's r-th tile: experts largest first, a snake over the pairs
+  auto tile_of = [&](int r) { return r * ncl + ((r & 1) ? ncl - 1 - cid : cid); };
+  struct WT {
+    int e, m0, n_idx, r0, r1, nkb;
+    long kst0;  // the expert's first K stage in the scale chunks
+  };
+  auto decode_w = [&](int t) {
+    WT w;
+    w.e = p.order ? __ldg(p.order + t / per) : t / per;
+    const int local = t % per;
+    w.m0 = (local / p.n_tiles) * 256;
+    w.n_idx = local % p.n_tiles;
+    w.r0 = __ldg(offs + w.e);
+    w.r1 = __ldg(offs + w.e + 1);
+    w.nkb = (w.r1 - w.r0 + BK - 1) / BK;
+    w.kst0 = mx_row_tile_base(w.r0, w.e);
+    return w;
+  };
+  auto warp_wait = [&](uint64_t* bar, uint32_t parity) {
+    const bool ok = px_wait(bar, parity, &sm->abort_flag, peer_abort, p.err);
+    return __all_sync(0xffffffffu, ok) != 0;
+  };
+  // rows past the expert's end belong to the next expert: zero them in this
+  // CTA's A box (K steps made only of them are skipped); returns the K steps
+  auto zero_tail = [&](uint8_t* a, int valid) {
+    const int nks = (valid + 31) / 32;
+    for (int i = valid * 8 + lane; i < nks * 32 * 8; i += 32)
+      *reinterpret_cast<uint4*>(a + i * 16) = make_uint4(0, 0, 0, 0);
+    ptx::fence_proxy_async_smem();
+    return nks;
+  };
+
+  if (warp == 0) {
+    // ===================================================== producer
+    if (run) {
+      if (lane == 0) {
+        ptx::prefetch_tmap(&tmA);
+        ptx::prefetch_tmap(&tmB);
+      }
+      uint32_t it = 0;
+      bool ok = true;
+      for (int r = 0, t = tile_of(0); t < total && ok; t = tile_of(++r)) {
+        const WT w = decode_w(t);
+        for (int kb = 0; kb < w.nkb; ++kb, ++it) {
+          const int s = it % PX_NS;
+          if (!warp_wait(&sm->empty[s], ((it / PX_NS) & 1u) ^ 1u)) { ok = false; break; }
+          if (lane == 0) {
+            uint8_t* a = smem + s * PX_STAGE;
+            uint8_t* b = a + PX_A;
+            uint8_t* sa = sc_area + s * PX_SC;
+            uint64_t* fb = &sm->full[s];
+            const int n0 = w.n_idx * 256;
+            const int nb = min(2, (p.N - n0 + 127) / 128);  // B column groups that exist
+            ptx::mbar_expect_tx(fb, PX_STAGE + 512 + 512 * nb);
+            const int row = w.r0 + kb * BK;
+            ptx::tma_load_2d(a, &tmA, fb, w.m0 + 128 * static_cast<int>(rank), row);
+            ptx::tma_load_2d(b, &tmB, fb, n0 + 128 * static_cast<int>(rank), row);
+            // scale chunks of K stage kst: this CTA's 128 features (clamped:
+            // a block past M computes rows that are not stored), all of B's
+            const long kst = w.kst0 + kb;
+            const int ga = min(w.m0 / 128 + static_cast<int>(rank), p.M / 128 - 1);
+            ptx::bulk_load(sa, p.sfa + ((kst * (p.M / 128) + ga) << 9), 512, fb);
+            ptx::bulk_load(sa + 512, p.sfb0 + ((kst * (p.N / 128) + n0 / 128) << 9), 512 * nb, fb);
+          }
+          __syncwarp();
+        }
+      }
+      // the even CTA's commits release these stages: wait for the last ones
+      // before the CTA may finish
+      for (int k = 0; k < PX_NS && ok; ++k, ++it) ok = warp_wait(&sm->empty[it % PX_NS], ((it / PX_NS) & 1u) ^ 1u);
+      if (!ok && lane == 0) {
+        for (int s = 0; s < PX_NS; ++s) {
+          const long long t0 = clock64();
+          while (clock64() - t0 < kWaitLimitCycles / 8 && !ptx::mbar_try_wait(&sm->full[s], 0) &&
+                 !ptx::mbar_try_wait(&sm->full[s], 1)) {
+          }
+        }
+      }
+    }
+  } else if (warp == 1 && rank == 1) {
+    // ============================================ relay (odd CTA of the pair)
+    const uint32_t leader_full0 = in_cta(&sm->full[0], 0);
+    uint32_t it = 0;
+    bool ok = run;
+    for (int r = 0, t = tile_of(0); t < total && ok; t = tile_of(++r)) {
+      const WT w = decode_w(t);
+      for (int kb = 0; kb < w.nkb; ++kb, ++it) {
+        const int s = it % PX_NS;
+        if (!warp_wait(&sm->full[s], (it / PX_NS) & 1u)) { ok = false; break; }
+        const int valid = w.r1 - (w.r0 + kb * BK);
+        if (valid < BK) zero_tail(smem + s * PX_STAGE, valid);
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive_cluster(leader_full0 + 8u * s);
+      }
+    }
+  } else if (warp == 1) {
+    // ============================================ MMA issuer (even CTA)
+    const uint32_t peer_empty0 = in_cta(&sm->empty[0], 1), peer_tfull = in_cta(&sm->tfull, 1);
+    uint32_t it = 0, acc_it = 0;
+    bool ok = run;
+    for (int r = 0, t = tile_of(0); t < total && ok; t = tile_of(++r)) {
+      const WT w = decode_w(t);
+      if (w.nkb == 0) continue;
+      if (!warp_wait(&sm->tempty, (acc_it & 1u) ^ 1u)) { ok = false; break; }
+      ptx::tc_fence_after();
+      for (int kb = 0; kb < w.nkb; ++kb, ++it) {
+        const int s = it % PX_NS;
+        if (!warp_wait(&sm->full[s], (it / PX_NS) & 1u)) { ok = false; break; }
+        ptx::tc_fence_after();
+        uint8_t* a = smem + s * PX_STAGE;
+        const int valid = w.r1 - (w.r0 + kb * BK);
+        const int nks = valid < BK ? zero_tail(a, valid) : BK / 32;
+        __syncwarp();
+        if (lane == 0) {
+          const uint32_t sa = ptx::smem_u32(sc_area + s * PX_SC);
+          const uint32_t sfa = tmem + PX_SFA + 4 * s, sfb = tmem + PX_SFB + 8 * s;
+          tmem_cp_pair_32x128b_x4(sfa, cp_desc(sa));
+          tmem_cp_pair_32x128b_x4(sfb, cp_desc(sa + 512));
+          tmem_cp_pair_32x128b_x4(sfb + 4, cp_desc(sa + 1024));
+          const uint32_t a_addr = ptx::smem_u32(a), b_addr = a_addr + PX_A;
+          for (int ks = 0; ks < nks; ++ks) {
+            const uint64_t ad = ptx::smem_desc_sw128(a_addr + ks * 4096, BOX_BYTES, 1024);
+            const uint64_t bd = ptx::smem_desc_sw128(b_addr + ks * 4096, BOX_BYTES, 1024);
+            mma_mxf8_pair(tmem, ad, bd, ptx::idesc_mxf8_f32(2 * BM, 256, 1, 1, ks, ks), sfa, sfb,
+                          (kb > 0 || ks > 0) ? 1u : 0u);
+          }
+          ptx::mma_commit_pair(ptx::smem_u32(&sm->empty[s]));
+          ptx::mma_commit_pair(peer_empty0 + 8u * s);
+        }
+        __syncwarp();
+      }
+      if (!ok) break;
+      if (lane == 0) {
+        ptx::mma_commit_pair(ptx::smem_u32(&sm->tfull));
+        ptx::mma_commit_pair(peer_tfull);
+      }
+      __syncwarp();
+      ++acc_it;
+    }
+    if (!ok && run && lane == 0) {
+      ptx::mma_commit_pair(ptx::smem_u32(&sm->drain));
+      const long long t0 = clock64();
+      while (clock64() - t0 < kWaitLimitCycles / 8 && !ptx::mbar_try_wait(&sm->drain, 0)) {
+      }
+    }
+  } else {
+    // ============================================================ epilogue
+    // warp (q, half): TMEM lanes 32q..32q+31 (this CTA's rows), columns
+    // 128 half .. +127, moved into registers as packed bf16 and released to
+    // the even CTA's `tempty` before the stores.
+    const int ew = warp - 2, q = warp & 3, half = ew >> 2;
+    uint8_t* stg = stg_area + ew * STG_BYTES;
+    const uint32_t leader_tempty = in_cta(&sm->tempty, 0);
+    uint32_t acc_it = 0;
+    for (int r = 0, t = tile_of(0); t < total && run; t = tile_of(++r)) {
+      const WT w = decode_w(t);
+      Tile tl{};
+      tl.e = w.e;
+      tl.m0 = w.m0 + 128 * static_cast<int>(rank);
+      tl.n_idx = w.n_idx;
+      uint32_t v[4][16];
+      if (w.nkb == 0) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int i = 0; i < 16; ++i) v[c][i] = 0u;  // expert with no rows: dW_e = 0
+      } else {
+        if (!warp_wait(&sm->tfull, acc_it & 1u)) break;
+        ptx::tc_fence_after();
+        const uint32_t tbase = tmem + static_cast<uint32_t>(half * 128) + (static_cast<uint32_t>(q * 32) << 16);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t rr[32];
+          ptx::tmem_ld32(tbase + c * 32, rr);
+          ptx::tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 16; ++i) v[c][i] = pack_bf16x2(__uint_as_float(rr[2 * i]), __uint_as_float(rr[2 * i + 1]));
+        }
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive_cluster(leader_tempty);
+        ++acc_it;
+      }
+#pragma unroll
+      for (int c = 0; c < 4; ++c) store_chunk<KIND, 256>(p, tl, q, lane, 4 * half + c, v[c], stg);
+    }
+  }
+
+  // No CTA of the pair leaves while the other may still reach its shared
+  // memory or TMEM; then both free the pair's TMEM together.
+  __syncwarp();
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::cluster_sync();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc_pair(tmem, TMEM_COLS);
+  }
+}
+
+template <int KIND>
+cudaError_t launch_wgrad_pair(const CUtensorMap& a, const CUtensorMap& b, const Params& p, cudaStream_t st) {
+  const long tiles = (long)p.E * p.m_tiles * p.n_tiles;
+  if (tiles <= 0) return cudaSuccess;
+  const size_t smem = 1024 + PX_NS * (PX_STAGE + PX_SC) + NUM_EPI_WARPS * STG_BYTES + sizeof(PxSmem) + 64;
+  cudaError_t e = cudaFuncSetAttribute(mx_wgrad_pair_kernel<KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(NUM_THREADS);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  static int max_pairs = 0;  // pairs resident at once (a pair needs two SMs of one GPC)
+  if (max_pairs <= 0) {
+    cfg.gridDim = dim3(2 * (sm_count() / 2));
+    e = cudaOccupancyMaxActiveClusters(&max_pairs, mx_wgrad_pair_kernel<KIND>, &cfg);
+    if (e != cudaSuccess) return e;
+    if (max_pairs <= 0) return cudaErrorLaunchOutOfResources;
+  }
+  const long pairs = tiles < max_pairs ? tiles : max_pairs;
+  cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs));
+  return MOE_COUNTED_AS(::moe::gemm_kind_name(KIND, true), st)
+      cudaLaunchKernelEx(&cfg, mx_wgrad_pair_kernel<KIND>, a, b, p);
+}
+
+
 // Output tile widths (measured choice): 256 with one accumulator released
 // early, except the GEMM2 dgrad, whose SwiGLU-backward epilogue reads h and
 // gains more from a double-buffered accumulator than it loses to the narrower
 // tile (the wgrads and GEMM2 re-read A twice as often at 128 and got slower).
 constexpr int kN_FPROP1 = 256, kN_FPROP2 = 256, kN_DGRAD2 = 128, kN_DGRAD1 = 256, kN_WGRAD = 256;
+// The weight gradients run on CTA pairs (256 x 256 tiles, mx_wgrad_pair_kernel)
+// when selected with moe_use_cta_pairs(1); one CTA per SM by default.
+std::atomic<int> g_wgrad_pairs{0};
 
 constexpr CUtensorMapDataType U8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
 
@@ -727,11 +1078,19 @@ cudaError_t mx_mlp_bwd(const void* dy_perm, const void* x_perm, const void* h, c
   if ((e = launch_mxfp8_quant_cols(dy_perm, R, d, offsets, E, dyc.q, dyc.s, st, true)) != cudaSuccess) return e;
   if (!map_2d(&mA, ac.q, U8, 1, f, R, 128, 128) || !map_2d(&mB0, dyc.q, U8, 1, d, R, 128, 128))
     return cudaErrorInvalidValue;
-  p.M = f; p.N = d; p.m_tiles = (f + BM - 1) / BM; p.n_tiles = (d + kN_WGRAD - 1) / kN_WGRAD; p.out0 = dwd;
+  p.M = f; p.N = d; p.n_tiles = (d + kN_WGRAD - 1) / kN_WGRAD; p.out0 = dwd;
   p.aux = nullptr;
   p.sfa = ac.s; p.sfb0 = dyc.s;
   p.order = order;
-  if ((e = launch<WGRAD2, kN_WGRAD>(mA, mB0, mB0, p, (long)E * p.m_tiles * p.n_tiles, st)) != cudaSuccess) return e;
+  const bool pairs = g_wgrad_pairs.load(std::memory_order_relaxed) != 0;
+  if (pairs) {
+    p.m_tiles = (f + 255) / 256;
+    e = launch_wgrad_pair<WGRAD2>(mA, mB0, p, st);
+  } else {
+    p.m_tiles = (f + BM - 1) / BM;
+    e = launch<WGRAD2, kN_WGRAD>(mA, mB0, mB0, p, (long)E * p.m_tiles * p.n_tiles, st);
+  }
+  if (e != cudaSuccess) return e;
   p.order = nullptr;
 
   // dx_perm = dh . [Wg | Wu]^T (K = 2f): dh rows, w_gate / w_up rows
@@ -754,9 +1113,14 @@ cudaError_t mx_mlp_bwd(const void* dy_perm, const void* x_perm, const void* h, c
   if ((e = launch_mxfp8_quant_cols(x_perm, R, d, offsets, E, xc.q, xc.s, st, true)) != cudaSuccess) return e;
   if (!map_2d(&mA, xc.q, U8, 1, d, R, 128, 128) || !map_2d(&mB0, dhc.q, U8, 1, 2L * f, R, 128, 128))
     return cudaErrorInvalidValue;
-  p.M = d; p.N = 2 * f; p.m_tiles = (d + BM - 1) / BM; p.n_tiles = (2 * f + kN_WGRAD - 1) / kN_WGRAD;
+  p.M = d; p.N = 2 * f; p.n_tiles = (2 * f + kN_WGRAD - 1) / kN_WGRAD;
   p.out0 = dwg; p.out1 = dwu; p.sfa = xc.s; p.sfb0 = dhc.s; p.sfb1 = nullptr;
   p.order = order;
+  if (pairs) {
+    p.m_tiles = (d + 255) / 256;
+    return launch_wgrad_pair<WGRAD1>(mA, mB0, p, st);
+  }
+  p.m_tiles = (d + BM - 1) / BM;
   return launch<WGRAD1, kN_WGRAD>(mA, mB0, mB0, p, (long)E * p.m_tiles * p.n_tiles, st);
 }
 
@@ -781,5 +1145,6 @@ cudaError_t mx_prepare_weights(const void* wg, const void* wu, const void* wd, i
   return launch_mxfp8_quant_dual(wd, Ef, d, w.wd_c.q, w.wd_c.s, w.wd_r.q, w.wd_r.s, st);
 }
 size_t mx_bwd_workspace(long R, int E, int d, int f) { return tc::mx::bwd_workspace(R, E, d, f); }
+void set_mx_cta_pairs(int on) { tc::mx::g_wgrad_pairs.store(on ? 1 : 0, std::memory_order_relaxed); }
 
 }  // namespace moe

@@ -115,6 +115,7 @@ cudaError_t launch_permute_quant(const void* x, int T, int d, int k, int E, cons
 // Experts by row count, largest first (ties by index), into order [E]; E <= 1024.
 // Weight-gradient kernel choice: 0 single-CTA tiles, 1 CTA pairs (process-wide).
 void set_cta_pairs(int on);
+void set_mx_cta_pairs(int on);
 cudaError_t launch_expert_order(const int32_t* offsets, int E, int32_t* order, cudaStream_t st);
 
 cudaError_t tc_router_logits(const void* x, const void* w_r, const float* bias, int T, int d, int E,

@@ -138,9 +138,11 @@ def test_fullsize_sampled_parity(name):
     assert not bad, f"{name}: {bad} (all: {errs})"
 
 
-def test_fullsize_mxfp8_sampled_parity():
+@pytest.mark.parametrize("pairs", [0, 1], ids=["single_cta", "cta_pairs"])
+def test_fullsize_mxfp8_sampled_parity(pairs):
     """The MXFP8 workload (T=32768, E=128, k=4) at full size, run as bench.py
-    runs it (weights prepared, rows quantised where produced): routing exact;
+    runs it (weights prepared, rows quantised where produced; the weight
+    gradients on single CTAs or, with pairs, as bench.py --cta-pairs): routing exact;
     y, dx, dgates, dlogits of sampled tokens and the weight gradients of
     sampled experts against the MXFP8 oracle on the same dequantised operands.
     Every quantisation the oracle applies is local to what is sampled: token
@@ -152,9 +154,13 @@ def test_fullsize_mxfp8_sampled_parity():
     inp = synth.Inputs(s, seed=0)
     p = L.params_from_inputs(inp, N.MOE_MXFP8)
     b = L.Buffers(s.T, s.d, s.E, s.k, s.f, N.MOE_MXFP8)
-    L.forward(p, b)
-    L.backward(p, b)
-    torch.cuda.synchronize()
+    N.moe_use_cta_pairs(pairs)
+    try:
+        L.forward(p, b)
+        L.backward(p, b)
+        torch.cuda.synchronize()
+    finally:
+        N.moe_use_cta_pairs(0)
     assert N.moe_get_device_error() == 0
 
     gl = b.logits.cpu().numpy().astype(np.float64)

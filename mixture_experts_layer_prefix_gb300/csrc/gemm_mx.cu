@@ -26,6 +26,9 @@
 // B at 272 + (TBN/32)s. Shared scale staging of a stage: A 512 B (row r of the
 // copy = tile rows r, 32+r, 64+r, 96+r), then B TBN/128 x 512 B (copy h row r
 // = tile columns 128h + r, +32, +64, +96).
+// The two weight gradients can also run on CTA pairs (mx_wgrad_pair_kernel,
+// below, selected with moe_use_cta_pairs): 256 x 256 tiles with
+// tcgen05.mma.cta_group::2.
 #include <atomic>
 
 #include "kernels.h"

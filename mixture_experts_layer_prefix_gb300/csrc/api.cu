@@ -13,16 +13,22 @@ namespace moe {
 
 __device__ int g_moe_error_word;
 
+// The error word's device address, cached per device ordinal (host threads
+// may race to fill a slot; they store the same value, so relaxed atomics
+// suffice). A device reset while the library stays loaded reloads its module:
+// callers that reset a device must not keep launching through this library.
 int* device_error_word() {
-  static int* ptrs[128] = {};
+  static std::atomic<int*> ptrs[128] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return nullptr;
-  if (!ptrs[dev]) {
+  int* q = ptrs[dev].load(std::memory_order_relaxed);
+  if (!q) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_moe_error_word) != cudaSuccess) return nullptr;
-    ptrs[dev] = static_cast<int*>(p);
+    q = static_cast<int*>(p);
+    ptrs[dev].store(q, std::memory_order_relaxed);
   }
-  return ptrs[dev];
+  return q;
 }
 
 static std::atomic<unsigned long long> g_launches{0};

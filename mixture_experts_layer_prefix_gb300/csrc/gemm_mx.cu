@@ -863,12 +863,15 @@ cudaError_t launch_wgrad_pair(const CUtensorMap& a, const CUtensorMap& b, const 
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  static int max_pairs = 0;  // pairs resident at once (a pair needs two SMs of one GPC)
+  // pairs resident at once (a pair needs two SMs of one GPC); computed once
+  static std::atomic<int> cached_pairs{0};
+  int max_pairs = cached_pairs.load(std::memory_order_relaxed);
   if (max_pairs <= 0) {
     cfg.gridDim = dim3(2 * (sm_count() / 2));
     e = cudaOccupancyMaxActiveClusters(&max_pairs, mx_wgrad_pair_kernel<KIND>, &cfg);
     if (e != cudaSuccess) return e;
     if (max_pairs <= 0) return cudaErrorLaunchOutOfResources;
+    cached_pairs.store(max_pairs, std::memory_order_relaxed);
   }
   const long pairs = tiles < max_pairs ? tiles : max_pairs;
   cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs));

@@ -1160,13 +1160,15 @@ cudaError_t launch_wgrad_pair(const CUtensorMap& a, const CUtensorMap& b, const 
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  // pairs resident at once (a pair needs two SMs of one GPC)
-  static int max_pairs = 0;
+  // pairs resident at once (a pair needs two SMs of one GPC); computed once
+  static std::atomic<int> cached_pairs{0};
+  int max_pairs = cached_pairs.load(std::memory_order_relaxed);
   if (max_pairs <= 0) {
     cfg.gridDim = dim3(2 * (sm_count() / 2));
     e = cudaOccupancyMaxActiveClusters(&max_pairs, tc_wgrad_pair_kernel<KIND>, &cfg);
     if (e != cudaSuccess) return e;
     if (max_pairs <= 0) return cudaErrorLaunchOutOfResources;
+    cached_pairs.store(max_pairs, std::memory_order_relaxed);
   }
   const long pairs = tiles < max_pairs ? tiles : max_pairs;
   cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs));
@@ -1238,11 +1240,13 @@ bool map_3d(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esize,
 }
 
 int sm_count() {
-  static int n = 0;
+  static std::atomic<int> cached{0};  // host threads may race to fill it with the same value
+  int n = cached.load(std::memory_order_relaxed);
   if (!n) {
     int dev = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    cached.store(n, std::memory_order_relaxed);
   }
   return n;
 }

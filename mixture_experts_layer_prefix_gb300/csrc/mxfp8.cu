@@ -22,6 +22,7 @@
 #include <cuda_fp8.h>
 
 #include <algorithm>
+#include <atomic>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -392,10 +393,13 @@ cudaError_t launch_mxfp8_quant_dual(const void* src, long rows, int C, uint8_t* 
                                     uint8_t* sc_r, cudaStream_t st) {
   if (rows == 0) return cudaSuccess;
   const long ntiles = rows / 32 * (C / kDualCols);
-  static int per_sm = 0;  // resident blocks per SM
-  if (per_sm <= 0 &&
-      (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, quant_dual_kernel, 128, 0) != cudaSuccess || per_sm <= 0))
-    per_sm = 8;
+  static std::atomic<int> cached{0};  // resident blocks per SM, computed once
+  int per_sm = cached.load(std::memory_order_relaxed);
+  if (per_sm <= 0) {
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, quant_dual_kernel, 128, 0) != cudaSuccess || per_sm <= 0)
+      per_sm = 8;
+    cached.store(per_sm, std::memory_order_relaxed);
+  }
   const long grid = std::min<long>(ntiles, (long)tc::sm_count() * per_sm);
   MOE_COUNTED_AS("quant_dual", st) quant_dual_kernel<<<static_cast<unsigned>(grid), 128, 0, st>>>(static_cast<const __nv_bfloat16*>(src), C,
                                                                            ntiles, qc, sc_c, qr, sc_r);

@@ -132,6 +132,8 @@ MX_SHAPES = [
     synth.MoEShape("mx_e8_k2", 512, 256, 8, 2, 256, "mxfp8", 0.02),
     synth.MoEShape("mx_e16_k4_skew", 700, 384, 16, 4, 256, "mxfp8", 0.02, zipf_s=1.2, zipf_alpha=0.5, n_dead=2),
     synth.MoEShape("mx_e4_k1_f384", 300, 128, 4, 1, 384, "mxfp8", 0.02),
+    # eight experts per token: the eight-slot quantising dispatch and combine backward
+    synth.MoEShape("mx_e64_k8", 320, 256, 64, 8, 256, "mxfp8", 0.02),
 ]
 
 
